@@ -1,0 +1,389 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA hot path on GB300: chunked prefill + decode step.
+
+One step = one kda_chunk_prefill over a 145408-token prompt (H=32, Dk=Dv=128,
+fp32 initial state, checkpoints every 32768 tokens and at the end: 5 per head)
+followed by one kda_decode_step over 512 sequences x 32 heads (1.07 GB of fp32
+state updated in place).  Inputs are seeded synthetic tensors with the
+shapes and value distributions of the workloads (see workloads.py), resident
+in HBM and larger than the 129 MB L2, so no L2 flush is needed between steps.
+
+`value` = prefill tokens/s (whole job: tokens of all ranks / max-over-ranks
+time).  The decode step's state-update bandwidth is reported alongside.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores instead (a
+bounded sample of the same workload), the reference arm for this method.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s (T=142k, H=32, D=128) + decode state-update HBM GB/s"
+T_PROMPT, H, D, CKPT = 145408, 32, 128, 32768
+DEC_N = 512
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+
+# Algorithmic bytes: per token per head q, k, v bf16
+# (3 x 256 B), log_alpha fp32 (512 B), beta bf16 (2 B), o bf16 (256 B).
+BYTES_PER_TOKEN_HEAD = 3 * 2 * D + 4 * D + 2 + 2 * D           # 1538
+STATE_BYTES = 4 * D * D                                          # one fp32 head state
+# Useful FLOPs: the FlashKDA count 12C^3 + 8C^2 D + 6 C D^2 per 64-token chunk per head.
+FLOPS_PER_CHUNK = 12 * 64 ** 3 + 8 * 64 ** 2 * D + 6 * 64 * D ** 2
+
+
+def prefill_algorithmic_bytes(T, n_ckpt_per_head):
+    # inputs + output, plus init-state read, final-state write and checkpoint writes
+    return BYTES_PER_TOKEN_HEAD * T * H + STATE_BYTES * H * (2 + n_ckpt_per_head)
+
+
+def decode_algorithmic_bytes(N):
+    # state read + write, plus q, k, v, log_alpha, beta in and o out
+    return N * H * (2 * STATE_BYTES + BYTES_PER_TOKEN_HEAD)
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        hbm = d.get("hbm_gbs") or d.get("hbm_GBps") or d.get("hbm")
+        bf = d.get("bf16_tflops")
+        bfs = d.get("bf16_tflops_sustained")
+        if hbm:
+            return float(hbm), float(bf or FALLBACK_BF16_TFLOPS), float(bfs or bf or FALLBACK_BF16_TFLOPS), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def read_traffic(kernel):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    kernel source that is built now (source hash recorded beside the figure)."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f).get(kernel)
+        if not d:
+            return None
+        src = os.path.join(ROOT, "kimi_delta_attention_06_gb300", "csrc", d["source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return float(d["bytes_per_launch"]) if h == d["source_sha256_16"] else None
+    except (OSError, ValueError, KeyError, TypeError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling during the timed region (SM clock, throttle reasons)."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1])); smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_count():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle(budget_s=12.0):
+    """Time the fp64 oracle on a bounded sample of the same workload: all 32 heads of
+    the first n tokens of the 145408-token prompt, plus a decode step on a subset of
+    the 512 sequences.  n grows until the prefill sample takes about budget_s/2."""
+    import torch
+    import oracle
+    from kimi_delta_attention_06_gb300 import workloads
+    oracle.build()
+    threads = cpu_count()
+    n = 256
+    res = None
+    while True:
+        c = workloads.single_case(n, seed=2)
+        t0 = time.perf_counter()
+        oracle.prefill(c.q, c.k, c.v, c.log_alpha, c.beta, c.cu_seqlens, c.init_state, threads=threads)
+        dt = time.perf_counter() - t0
+        res = (n, dt)
+        if dt > budget_s / 2 or n >= T_PROMPT:
+            break
+        n = min(T_PROMPT, int(n * max(2.0, min(16.0, (budget_s / 2) / max(dt, 1e-3)))))
+    n_tok, dt = res
+    pre_tps = n_tok / dt
+    nd = 64
+    dc = workloads.decode_case(N=nd, H=H, D=D, steps=1, seed=4)
+    s = dc.steps[0]
+    t0 = time.perf_counter()
+    oracle.decode(s["q"], s["k"], s["v"], s["log_alpha"], s["beta"], dc.state, threads=threads)
+    ddt = time.perf_counter() - t0
+    dec_gbs = decode_algorithmic_bytes(nd) / ddt / 1e9
+    return {"value": pre_tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"prefill: first {n_tok} tokens x {H} heads of the {T_PROMPT}-token prompt "
+                      f"({dt:.2f} s); decode: {nd} of {DEC_N} sequences x {H} heads ({ddt:.2f} s)",
+            "decode_gbs": dec_gbs, "prefill_seconds": dt}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return 0
+    samples = []
+    for i in range(args.warmup + args.steps):
+        r = time_oracle(budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
+        if i >= args.warmup:
+            samples.append(r)
+    v = statistics.median(x["value"] for x in samples)
+    cb = dict(samples[-1])
+    cb["value"] = v
+    line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(x["prefill_seconds"] for x in samples),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": f"kda prefill T={T_PROMPT} H={H} D={D} (bounded CPU sample)",
+                       "global_batch": 1, "seq_len": T_PROMPT, "parallelism": "none (host cores)"},
+            "cpu_baseline": cb,
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, rank)
+
+    import torch
+    import torch.distributed as dist
+    from kimi_delta_attention_06_gb300 import build as kbuild
+    from kimi_delta_attention_06_gb300 import kda, workloads
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    kbuild.build()
+    kda.load()
+    stream = torch.cuda.current_stream()
+
+    # ---- inputs (seeded per rank: each rank serves its own prompt and decode batch) ----
+    c = workloads.single_case(T_PROMPT, seed=2 + 1000 * rank, device=dev, ckpt_stride=CKPT)
+    cu_dev = c.cu_seqlens.to(dev)
+    out = torch.empty(T_PROMPT, H, D, device=dev, dtype=torch.bfloat16)
+    fin = torch.empty(1, H, D, D, device=dev, dtype=torch.float32)
+    n_ck = kda.kda_ckpt_count(c.cu_seqlens, CKPT)
+    ck = torch.empty(n_ck, H, D, D, device=dev, dtype=torch.float32)
+    dc = workloads.decode_case(N=DEC_N, H=H, D=D, steps=1, seed=4 + 1000 * rank, device=dev)
+    dstate = dc.state
+    ds = dc.steps[0]
+    dout = torch.empty(DEC_N, H, D, device=dev, dtype=torch.bfloat16)
+
+    def prefill():
+        kda.kda_chunk_prefill(c.q, c.k, c.v, c.log_alpha, c.beta, c.init_state, cu_dev, c.cu_seqlens, 1, T_PROMPT,
+                              H, D, D, out, kda.KDA_OUT_BF16, fin, ck, CKPT, stream)
+
+    def decode():
+        kda.kda_decode_step(ds["q"], ds["k"], ds["v"], ds["log_alpha"], ds["beta"], dstate, dout,
+                            kda.KDA_OUT_BF16, DEC_N, H, D, D, stream)
+
+    for _ in range(max(3, args.warmup)):
+        prefill(); decode()
+    torch.cuda.synchronize()
+    if kda.kda_device_status() != 0:
+        raise RuntimeError("device status after warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        prefill()
+        ev[i][1].record(stream)
+        decode()
+        ev[i][2].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    if world > 1:
+        dist.barrier()
+    total_ms = start.elapsed_time(stop)
+    pre_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    if kda.kda_device_status() != 0:
+        raise RuntimeError("device status after timed region")
+
+    t = torch.tensor([total_ms, sum(pre_ms), sum(dec_ms)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, pre_sum, dec_sum = (float(x) for x in t.tolist())
+    ms_step = total_ms / args.steps
+    pre_avg = pre_sum / args.steps
+    dec_avg = dec_sum / args.steps
+
+    tokens_all = T_PROMPT * world
+    value = tokens_all / (pre_avg / 1e3)
+    hbm, bf16, bf16s, peak_src = read_peaks()
+    pre_bytes = prefill_algorithmic_bytes(T_PROMPT, n_ck)
+    dec_bytes = decode_algorithmic_bytes(DEC_N)
+    pre_gbs = pre_bytes / (pre_avg / 1e3) / 1e9
+    dec_gbs = dec_bytes / (dec_avg / 1e3) / 1e9
+    useful_tflops = FLOPS_PER_CHUNK * (T_PROMPT / 64) * H / (pre_avg / 1e3) / 1e12
+
+    # ---- end to end through host buffers (pinned), copies inside the timed region ----
+    e2e = None
+    if not args.no_e2e:
+        host = {k: torch.empty_like(getattr(c, k), device="cpu").pin_memory()
+                for k in ("q", "k", "v", "log_alpha", "beta")}
+        for k2, hv in host.items():
+            hv.copy_(getattr(c, k2))
+        h_s0 = c.init_state.cpu().pin_memory()
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h_ck = torch.empty(ck.shape, dtype=ck.dtype).pin_memory()
+        h_fin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+        d_in = {k2: torch.empty_like(getattr(c, k2)) for k2 in host}
+        d_s0 = torch.empty_like(c.init_state)
+        h2d = sum(v.numel() * v.element_size() for v in host.values()) + h_s0.numel() * 4
+        d2h = out.numel() * 2 + ck.numel() * 4 + fin.numel() * 4
+        n_e2e = max(1, min(args.steps, 3))
+
+        def e2e_step():
+            for k2 in host:
+                d_in[k2].copy_(host[k2], non_blocking=True)
+            d_s0.copy_(h_s0, non_blocking=True)
+            kda.kda_chunk_prefill(d_in["q"], d_in["k"], d_in["v"], d_in["log_alpha"], d_in["beta"], d_s0, cu_dev,
+                                  c.cu_seqlens, 1, T_PROMPT, H, D, D, out, kda.KDA_OUT_BF16, fin, ck, CKPT, stream)
+            h_out.copy_(out, non_blocking=True)
+            h_ck.copy_(ck, non_blocking=True)
+            h_fin.copy_(fin, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e_ms = torch.tensor([a.elapsed_time(b) / n_e2e], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(e_ms, op=dist.ReduceOp.MAX)
+        e2e = {"value": tokens_all / (float(e_ms.item()) / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": float(e_ms.item()), "steps": n_e2e,
+               "note": "prefill only; pinned host inputs copied in, output + checkpoints + final state copied out"}
+        del host, d_in, h_out, h_ck
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = time_oracle()
+        cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        cpu["decode_gbs"] = cb["decode_gbs"]
+
+    if rank == 0:
+        traffic = read_traffic("kda_prefill_kernel")
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "tf32/f32 (bf16 in/out)", "data": "synthetic",
+            "config": {"workload": f"kda prefill T={T_PROMPT} H={H} Dk=Dv={D} ckpt every {CKPT} "
+                                   f"+ decode N={DEC_N} H={H} D={D}",
+                       "global_batch": world, "seq_len": T_PROMPT, "heads": H, "head_dim": D,
+                       "ckpt_stride": CKPT, "decode_batch": DEC_N,
+                       "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"replicas x{world}"},
+            "prefill_ms": pre_avg, "decode_ms": dec_avg,
+            "decode": {"value": dec_gbs, "unit": "GB/s", "tokens_per_s": DEC_N * world / (dec_avg / 1e3),
+                       "frac_of_hbm_peak": dec_gbs / hbm},
+            "roofline": {"bound": "hbm", "achieved": pre_gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": pre_gbs / hbm, "traffic": traffic, "kernel": "kda_prefill_kernel",
+                         "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": pre_bytes},
+            "useful_flops": {"tflops": useful_tflops, "frac_of_bf16_peak": useful_tflops / bf16,
+                             "frac_of_bf16_sustained": useful_tflops / bf16s, "peak_source": peak_src},
+            "clocks": clocks, "e2e": e2e, "gpu_launches": 2 * args.steps, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,160 @@
+// kda_api.cu -- the C ABI declared in include/kda.h: host-side validation,
+// the device status word, and dispatch to the CUDA kernels.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <cuda_runtime.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+int launch_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* log_alpha,
+                  const uint16_t* beta, float* state, void* out, int out_f32,
+                  int N, int H, int D, cudaStream_t stream);
+int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* la,
+                   const uint16_t* beta, const float* init_state, const int32_t* cu_seqlens,
+                   int num_seqs, int H, int Dk, int Dv, void* out, int out_f32,
+                   float* final_state, float* ckpt, int ckpt_stride, int* status, cudaStream_t stream);
+}  // namespace kda
+
+namespace {
+
+// One status word per device (module-scope device variable; no allocation).
+__device__ int g_kda_status = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_status_ptr[kMaxDevices] = {};
+int g_device_ok[kMaxDevices] = {};   // 0 unknown, 1 supported, -1 unsupported
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Resolve the current device's status word and check it can run sm_103a code.
+int device_setup(int** status) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return KDA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_device_ok[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        g_device_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+        if (g_device_ok[dev] == 1) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_kda_status) != cudaSuccess) { g_device_ok[dev] = 0; return KDA_ERR_CUDA; }
+            g_status_ptr[dev] = static_cast<int*>(p);
+        }
+    }
+    if (g_device_ok[dev] != 1) return KDA_ERR_UNSUPPORTED;
+    *status = g_status_ptr[dev];
+    return KDA_OK;
+}
+
+bool head_dims_ok(int Dk, int Dv) { return (Dk == 64 || Dk == 128) && (Dv == 64 || Dv == 128); }
+
+}  // namespace
+
+extern "C" {
+
+int64_t kda_ckpt_count(const int32_t* cu_seqlens_host, int num_seqs, int ckpt_stride) {
+    if (num_seqs < 0 || ckpt_stride < 0 || (num_seqs > 0 && !cu_seqlens_host)) return -1;
+    if (ckpt_stride == 0) return 0;
+    int64_t total = 0;
+    for (int n = 0; n < num_seqs; ++n) {
+        const int64_t len = static_cast<int64_t>(cu_seqlens_host[n + 1]) - cu_seqlens_host[n];
+        if (len < 0) return -1;
+        total += (len + ckpt_stride - 1) / ckpt_stride;
+    }
+    return total;
+}
+
+int kda_chunk_size(void) { return 64; }
+
+const char* kda_status_string(int status) {
+    switch (status) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_INVALID_ARG: return "invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "unsupported shape or device";
+        case KDA_ERR_CUDA: return "CUDA runtime error";
+        case KDA_ERR_TIMEOUT: return "device-side wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int kda_chunk_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                      const float* log_alpha, const uint16_t* beta,
+                      const float* init_state,
+                      const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                      int num_seqs, int total_tokens, int H, int Dk, int Dv,
+                      void* out, int out_dtype,
+                      float* final_state, float* ckpt_states, int ckpt_stride,
+                      void* stream) {
+    if (num_seqs < 0 || total_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+    if (out_dtype != KDA_OUT_BF16 && out_dtype != KDA_OUT_F32) return KDA_ERR_INVALID_ARG;
+    if (ckpt_stride < 0 || (ckpt_stride % 64) != 0) return KDA_ERR_INVALID_ARG;
+    if (!head_dims_ok(Dk, Dv)) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs > 0 && (!cu_seqlens || !cu_seqlens_host)) return KDA_ERR_INVALID_ARG;
+    if (num_seqs > 0) {
+        if (cu_seqlens_host[0] != 0 || cu_seqlens_host[num_seqs] != total_tokens) return KDA_ERR_INVALID_ARG;
+        for (int n = 0; n < num_seqs; ++n)
+            if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
+    } else if (total_tokens != 0) {
+        return KDA_ERR_INVALID_ARG;
+    }
+    if (total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta || !out)) return KDA_ERR_INVALID_ARG;
+    if (ckpt_states && ckpt_stride == 0) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, log_alpha, beta, init_state, out, final_state, ckpt_states, cu_seqlens};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p) && p != cu_seqlens) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return KDA_ERR_INVALID_ARG;
+    // 32-bit element offsets inside the kernel stay below 2^31 per row of work
+    if (static_cast<int64_t>(total_tokens) * H * (Dk > Dv ? Dk : Dv) >= (int64_t(1) << 40)) return KDA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return KDA_OK;
+    int* status = nullptr;
+    int rc = device_setup(&status);
+    if (rc != KDA_OK) return rc;
+    rc = kda::launch_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, num_seqs, H, Dk, Dv,
+                             out, out_dtype == KDA_OUT_F32, final_state, ckpt_states, ckpt_stride,
+                             status, static_cast<cudaStream_t>(stream));
+    return rc == 0 ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_decode_step(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                    const float* log_alpha, const uint16_t* beta,
+                    float* state, void* out, int out_dtype,
+                    int N, int H, int Dk, int Dv, void* stream) {
+    if (N < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+    if (out_dtype != KDA_OUT_BF16 && out_dtype != KDA_OUT_F32) return KDA_ERR_INVALID_ARG;
+    if (!head_dims_ok(Dk, Dv)) return KDA_ERR_UNSUPPORTED;
+    if (Dk != Dv) return KDA_ERR_UNSUPPORTED;
+    if (N == 0) return KDA_OK;
+    if (!q || !k || !v || !log_alpha || !beta || !state || !out) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, log_alpha, beta, state, out};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return KDA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(N) * H >= (int64_t(1) << 31)) return KDA_ERR_INVALID_ARG;
+    int* status = nullptr;
+    int rc = device_setup(&status);
+    if (rc != KDA_OK) return rc;
+    rc = kda::launch_decode(q, k, v, log_alpha, beta, state, out, out_dtype == KDA_OUT_F32, N, H, Dk,
+                            static_cast<cudaStream_t>(stream));
+    return rc == 0 ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_device_status(void* stream) {
+    int* status = nullptr;
+    int rc = device_setup(&status);
+    if (rc != KDA_OK) return rc;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KDA_ERR_CUDA;
+    int value = 0;
+    if (cudaMemcpyFromSymbol(&value, g_kda_status, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    if (value != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_kda_status, &zero, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    return value;
+}
+
+}  // extern "C"

@@ -1,0 +1,163 @@
+// tc.cuh -- thin inline-PTX wrappers for the sm_100-family tensor-core path
+// (tcgen05 MMA with TMEM accumulators, mbarriers, shared-memory descriptors).
+//
+// Layout conventions (shared-memory operand tiles written by threads):
+//   * K-major, 128-byte swizzle: rows of 128 bytes (32 fp32/tf32 or 64 bf16
+//     elements along K); 8-row groups of 1024 bytes are contiguous; the
+//     16-byte chunk index inside a row is XOR-ed with (row % 8).  A tile with
+//     more than one 128-byte K slab stores the slabs one after another, each
+//     slab holding all rows.  Tile bases are 1024-byte aligned.
+//   * MN-major, 128-byte swizzle: the same physical arrangement with the roles
+//     swapped: each 128-byte row runs along M (or N) and rows are K indices.
+// These two coincide physically, so one tile can serve as a K-major operand
+// of one MMA and as an MN-major operand of another.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace kda {
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- shared-memory matrix descriptor -----------------------------------------------
+// bits  0-13 start address >> 4, 16-29 leading byte offset >> 4,
+// bits 32-45 stride byte offset >> 4, 46-47 version (1), 61-63 layout/swizzle.
+enum : uint32_t { kSwizzleNone = 0, kSwizzle128B = 2, kSwizzle64B = 4, kSwizzle32B = 6 };
+
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(swz & 0x7u) << 61;
+    return d;
+}
+
+// ---- instruction descriptor (kind::f16 / kind::tf32) -------------------------------
+// bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format
+// (kind::f16: 0 = f16, 1 = bf16; kind::tf32: 2 = tf32), bit 15 A major,
+// bit 16 B major (0 = K-major, 1 = MN-major), 17-22 N >> 3, 24-28 M >> 4.
+enum : uint32_t { kFmtF16 = 0, kFmtBF16 = 1, kFmtTF32 = 2 };
+
+__host__ __device__ constexpr uint32_t idesc(int M, int N, uint32_t fmt, bool a_mn, bool b_mn) {
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((a_mn ? 1u : 0u) << 15) |
+           ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ---- MMA issue (one thread) --------------------------------------------------------------
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n"
+        :: "r"(d_tmem), "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n"
+        :: "r"(d_tmem), "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+
+// Arrive on an mbarrier once all previously issued MMAs of this thread complete.
+__device__ __forceinline__ void mma_commit(void* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(smem_u32(bar)) : "memory");
+}
+
+// ---- TMEM allocation (whole warp) ---------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_u32(dst_smem)), "r"(ncols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Make generic-proxy shared-memory writes visible to the tensor core (async proxy).
+__device__ __forceinline__ void fence_smem_to_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---- TMEM -> registers: 32 lanes x 32 bit, 16 consecutive columns ------------------------
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16]) {
+    uint32_t* u = reinterpret_cast<uint32_t*>(r);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
+          "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]),
+          "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---- mbarrier -----------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(void* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t mbar_try_wait(void* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait for phase `parity` of an mbarrier, giving up after `limit_ns`.
+// Returns 1 when the phase completed, 0 on timeout.
+__device__ __forceinline__ uint32_t mbar_wait_bounded(void* bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return 1;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return 1;
+        if (globaltimer_ns() - t0 > limit_ns) return 0;
+    }
+}
+
+// Round an fp32 value to tf32 (nearest, ties away from zero); result stays in an fp32 register.
+__device__ __forceinline__ float to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// ---- swizzled tile addressing ----------------------------------------------------------------
+// Byte offset of 32-bit element (row, col) in a 128B-swizzled tile of `rows` rows whose
+// 128-byte slabs (32 elements of `col`) are stored one after another.
+__host__ __device__ __forceinline__ uint32_t sw128_off32(uint32_t row, uint32_t col, uint32_t rows) {
+    const uint32_t slab = col >> 5, cb = (col & 31u) * 4u;
+    return slab * rows * 128u + row * 128u + ((((cb >> 4) ^ (row & 7u)) << 4) | (cb & 15u));
+}
+// Same for 16-bit elements (64 per 128-byte row).
+__host__ __device__ __forceinline__ uint32_t sw128_off16(uint32_t row, uint32_t col, uint32_t rows) {
+    const uint32_t slab = col >> 6, cb = (col & 63u) * 2u;
+    return slab * rows * 128u + row * 128u + ((((cb >> 4) ^ (row & 7u)) << 4) | (cb & 15u));
+}
+
+}  // namespace tc
+}  // namespace kda

@@ -1,0 +1,172 @@
+"""Thin ctypes binding of the KDA C ABI (include/kda.h).
+
+The functions named like the C entry points (``kda_chunk_prefill``,
+``kda_decode_step``, ``kda_ckpt_count``, ``kda_device_status``,
+``kda_status_string``, ``kda_chunk_size``) only marshal arguments: torch
+tensors become raw device pointers, the current torch stream becomes the
+``stream`` argument, and a negative status raises ``KdaError``.  ``prefill``
+and ``decode_step`` additionally allocate the output tensors with torch.
+
+There is no fallback: if ``libkda.so`` is missing or cannot be loaded the
+first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_lib", "libkda.so")
+_lock = threading.Lock()
+_lib = None
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = -1
+KDA_ERR_UNSUPPORTED = -2
+KDA_ERR_CUDA = -3
+KDA_ERR_TIMEOUT = -4
+KDA_OUT_BF16 = 0
+KDA_OUT_F32 = 1
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {kda_status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libkda.so (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(f"KDA CUDA library not built: {_LIB_PATH} is missing "
+                                   "(run kimi_delta_attention_06_gb300.build.build())")
+            lib = ctypes.CDLL(_LIB_PATH)
+            lib.kda_chunk_prefill.restype = _i
+            lib.kda_chunk_prefill.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                              _i, _i, _i, _i, _i, _vp, _i, _vp, _vp, _i, _vp]
+            lib.kda_decode_step.restype = _i
+            lib.kda_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]
+            lib.kda_ckpt_count.restype = ctypes.c_int64
+            lib.kda_ckpt_count.argtypes = [_vp, _i, _i]
+            lib.kda_device_status.restype = _i
+            lib.kda_device_status.argtypes = [_vp]
+            lib.kda_status_string.restype = ctypes.c_char_p
+            lib.kda_status_string.argtypes = [_i]
+            lib.kda_chunk_size.restype = _i
+            lib.kda_chunk_size.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("KDA tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(rc: int, what: str):
+    if rc != KDA_OK:
+        raise KdaError(rc, what)
+
+
+def _bits16(t: torch.Tensor) -> torch.Tensor:
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"expected a bfloat16 tensor, got {t.dtype}")
+    return t
+
+
+# --- the C entry points, one to one --------------------------------------------------
+
+def kda_status_string(status: int) -> str:
+    return load().kda_status_string(int(status)).decode()
+
+
+def kda_chunk_size() -> int:
+    return int(load().kda_chunk_size())
+
+
+def kda_ckpt_count(cu_seqlens_host: torch.Tensor, ckpt_stride: int) -> int:
+    cu = cu_seqlens_host.to(device="cpu", dtype=torch.int32).contiguous()
+    n = load().kda_ckpt_count(ctypes.c_void_p(cu.data_ptr()), cu.numel() - 1, int(ckpt_stride))
+    if n < 0:
+        raise KdaError(KDA_ERR_INVALID_ARG, "kda_ckpt_count")
+    return int(n)
+
+
+def kda_chunk_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host,
+                      num_seqs: int, total_tokens: int, H: int, Dk: int, Dv: int,
+                      out, out_dtype: int, final_state, ckpt_states, ckpt_stride: int, stream=None):
+    cu_host = cu_seqlens_host.to(device="cpu", dtype=torch.int32).contiguous()
+    rc = load().kda_chunk_prefill(
+        _ptr(_bits16(q)), _ptr(_bits16(k)), _ptr(_bits16(v)), _ptr(log_alpha), _ptr(_bits16(beta)),
+        _ptr(init_state), _ptr(cu_seqlens), ctypes.c_void_p(cu_host.data_ptr()),
+        int(num_seqs), int(total_tokens), int(H), int(Dk), int(Dv),
+        _ptr(out), int(out_dtype), _ptr(final_state), _ptr(ckpt_states), int(ckpt_stride),
+        _stream(stream))
+    _check(rc, "kda_chunk_prefill")
+
+
+def kda_decode_step(q, k, v, log_alpha, beta, state, out, out_dtype: int,
+                    N: int, H: int, Dk: int, Dv: int, stream=None):
+    rc = load().kda_decode_step(_ptr(_bits16(q)), _ptr(_bits16(k)), _ptr(_bits16(v)), _ptr(log_alpha),
+                                _ptr(_bits16(beta)), _ptr(state), _ptr(out), int(out_dtype),
+                                int(N), int(H), int(Dk), int(Dv), _stream(stream))
+    _check(rc, "kda_decode_step")
+
+
+def kda_device_status(stream=None) -> int:
+    return int(load().kda_device_status(_stream(stream)))
+
+
+# --- conveniences: allocate outputs, then call the entry point ----------------------------
+
+def prefill(q, k, v, log_alpha, beta, cu_seqlens_host, init_state=None, ckpt_stride: int = 0,
+            out_dtype=torch.bfloat16, want_final: bool = True, cu_seqlens=None, stream=None):
+    """Allocate outputs and run kda_chunk_prefill.  Returns (out, final_state, ckpt_states)."""
+    T, H, Dk = q.shape
+    Dv = v.shape[2]
+    cu_host = cu_seqlens_host.to(device="cpu", dtype=torch.int32).contiguous()
+    N = cu_host.numel() - 1
+    dev = q.device
+    if cu_seqlens is None:
+        cu_seqlens = cu_host.to(dev, non_blocking=False)
+    out = torch.empty(T, H, Dv, device=dev, dtype=out_dtype)
+    fin = torch.empty(N, H, Dk, Dv, device=dev, dtype=torch.float32) if want_final else None
+    nck = kda_ckpt_count(cu_host, ckpt_stride) if ckpt_stride > 0 else 0
+    ck = torch.empty(nck, H, Dk, Dv, device=dev, dtype=torch.float32) if ckpt_stride > 0 else None
+    kda_chunk_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_host, N, T, H, Dk, Dv,
+                      out, KDA_OUT_F32 if out_dtype == torch.float32 else KDA_OUT_BF16,
+                      fin, ck if nck > 0 else None, ckpt_stride, stream)
+    return out, fin, ck
+
+
+def decode_step(q, k, v, log_alpha, beta, state, out_dtype=torch.bfloat16, stream=None):
+    """Run kda_decode_step in place on ``state``; returns the output tensor."""
+    N, H, Dk = q.shape
+    Dv = v.shape[2]
+    out = torch.empty(N, H, Dv, device=q.device, dtype=out_dtype)
+    kda_decode_step(q, k, v, log_alpha, beta, state, out,
+                    KDA_OUT_F32 if out_dtype == torch.float32 else KDA_OUT_BF16, N, H, Dk, Dv, stream)
+    return out

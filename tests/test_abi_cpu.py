@@ -1,0 +1,109 @@
+"""Host-only checks of the C ABI: the library builds, loads and exports every
+entry point declared in include/kda.h, and invalid calls are rejected on the
+host before anything touches a GPU (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from kimi_delta_attention_06_gb300 import build as kbuild
+from kimi_delta_attention_06_gb300 import kda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kda.load()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "kda.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_\w+)\s*\(", src)))
+
+
+def test_header_declares_expected_entry_points():
+    names = _declared_functions()
+    for n in ["kda_chunk_prefill", "kda_decode_step", "kda_ckpt_count", "kda_device_status",
+              "kda_status_string", "kda_chunk_size"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_status_strings_and_chunk_size(lib):
+    assert kda.kda_status_string(0) == "ok"
+    assert "invalid" in kda.kda_status_string(-1)
+    assert "timed out" in kda.kda_status_string(-4)
+    assert kda.kda_chunk_size() == 64
+
+
+def test_ckpt_count_matches_policy(lib):
+    cu = torch.tensor([0, 145408], dtype=torch.int32)
+    assert kda.kda_ckpt_count(cu, 32768) == 5          # 4 interior + the sequence end
+    cu = torch.tensor([0, 32768, 32768, 32769], dtype=torch.int32)
+    assert kda.kda_ckpt_count(cu, 32768) == 2          # exact multiple: 1; empty: 0; length 1: 1
+    assert kda.kda_ckpt_count(cu, 0) == 0
+    with pytest.raises(kda.KdaError):
+        kda.kda_ckpt_count(torch.tensor([0, 5, 3], dtype=torch.int32), 64)
+
+
+def _prefill_raw(lib, **over):
+    """Call kda_chunk_prefill with fake (never dereferenced) aligned pointers."""
+    cu = (ctypes.c_int32 * 3)(0, 64, 100)
+    a = dict(q=0x1000, k=0x2000, v=0x3000, la=0x4000, beta=0x5000, s0=None, cu=0x6000,
+             cu_host=ctypes.cast(cu, ctypes.c_void_p), N=2, T=100, H=2, Dk=64, Dv=64,
+             out=0x7000, out_dtype=0, fin=None, ck=None, stride=0, stream=None)
+    a.update(over)
+    return lib.kda_chunk_prefill(a["q"], a["k"], a["v"], a["la"], a["beta"], a["s0"], a["cu"],
+                                 a["cu_host"], a["N"], a["T"], a["H"], a["Dk"], a["Dv"], a["out"],
+                                 a["out_dtype"], a["fin"], a["ck"], a["stride"], a["stream"])
+
+
+def test_prefill_rejects_bad_arguments_on_host(lib):
+    bad = ctypes.c_int32 * 3
+    assert _prefill_raw(lib, q=None) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill_raw(lib, Dk=96) == kda.KDA_ERR_UNSUPPORTED
+    assert _prefill_raw(lib, Dv=32) == kda.KDA_ERR_UNSUPPORTED
+    assert _prefill_raw(lib, T=99) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill_raw(lib, stride=100) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill_raw(lib, stride=-64) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill_raw(lib, ck=0x8000, stride=0) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill_raw(lib, out_dtype=7) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill_raw(lib, q=0x1008) == kda.KDA_ERR_INVALID_ARG        # misaligned
+    dec = bad(0, 70, 60)
+    assert _prefill_raw(lib, cu_host=ctypes.cast(dec, ctypes.c_void_p), T=60) == kda.KDA_ERR_INVALID_ARG
+    start = bad(5, 70, 100)
+    assert _prefill_raw(lib, cu_host=ctypes.cast(start, ctypes.c_void_p)) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill_raw(lib, N=-1) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill_raw(lib, N=0, T=0) == kda.KDA_OK                     # nothing to do
+
+
+def test_decode_rejects_bad_arguments_on_host(lib):
+    f = lib.kda_decode_step
+    args = [0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0, 4, 2, 128, 128, None]
+    a = list(args); a[0] = None
+    assert f(*a) == kda.KDA_ERR_INVALID_ARG
+    a = list(args); a[10] = 96; a[11] = 96
+    assert f(*a) == kda.KDA_ERR_UNSUPPORTED
+    a = list(args); a[10] = 64
+    assert f(*a) == kda.KDA_ERR_UNSUPPORTED                                # Dk != Dv
+    a = list(args); a[5] = 0x6004
+    assert f(*a) == kda.KDA_ERR_INVALID_ARG
+    a = list(args); a[8] = 0
+    assert f(*a) == kda.KDA_OK                                             # N = 0: nothing to do
+
+
+def test_binding_refuses_non_bf16(lib):
+    with pytest.raises(TypeError):
+        kda.kda_decode_step(torch.zeros(1, 1, 64), torch.zeros(1, 1, 64), torch.zeros(1, 1, 64),
+                            torch.zeros(1, 1, 64), torch.zeros(1, 1), torch.zeros(1, 1, 64, 64),
+                            torch.zeros(1, 1, 64), 1, 1, 1, 64, 64)
