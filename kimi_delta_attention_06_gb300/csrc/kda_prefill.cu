@@ -20,18 +20,26 @@
 //
 // which is the token recurrence S_t = (I - b k k^T) Diag(a) S_{t-1} + b k v^T,
 // o_t = S_t^T q_t regrouped by chunk (U solves (I + L) U = diag(beta) X).
-// Every product is a tcgen05 MMA with fp32 accumulation in TMEM, except the
-// 64 x 64 triangular inverse (CUDA cores, fp32, 16 x 16 blocks).  The two
+// Products run as tcgen05 MMAs with fp32 accumulation in TMEM.  The two
 // intra-chunk products (Km Kb^T, Qm Kb^T) take tf32 operands: their factors
-// exp(+-(g_t - g_r)) span up to half a chunk of decay in either direction, which
-// only an 8-bit exponent holds.  Everything else -- start-referenced decayed
-// operands (all factors <= 1), A, T, X, U and the state -- is range-safe and
-// runs as fp16 MMAs (same 10-bit mantissa as tf32, twice the rate).
+// exp(+-(g_t - g_r)) span up to half a chunk of decay either way, which needs
+// an 8-bit exponent.  Everything else (start-referenced decayed operands with
+// factors <= 1, A, T, X, U, the state) is range-safe and runs as fp16 MMAs
+// (10-bit mantissa like tf32, twice the rate, half the bytes).  The 64 x 64
+// triangular inverse runs on CUDA cores in fp32 (16 x 16 diagonal blocks, then
+// block rows).
 //
-// Work decomposition: one CTA per (sequence, head, 64-column block of Dv).
-// Value columns are exactly independent (column j of S only ever mixes with
-// column j of V), so the Dv split needs no communication.  The fp32 state block
-// (Dk x 64) lives in registers, one row per thread, for the whole sequence.
+// CTA organisation: one CTA per (sequence, head, 64-column block of Dv); value
+// columns are exactly independent, so the split needs no communication.  The
+// CTA is warp-specialised so that the state-independent preparation of chunk
+// c+1 overlaps the sequential state chain of chunk c:
+//   * prep group, warps 0-7: decays and decayed operand tiles, Km Kb^T / Qm Kb^T,
+//     the inverse, Mqk = A T.  Hands the chain [K~; Q~], K^ (double-buffered),
+//     [T; Mqk] and exp(g_C).
+//   * chain group, warps 8-11: owns the fp32 state block (one row per thread, in
+//     registers for the whole sequence) and runs X, U/O and the state update.
+// The groups hand off through mbarriers; every wait is bounded and a timeout
+// makes the kernel record KDA_ERR_TIMEOUT and return.
 #include "common.cuh"
 #include "tc.cuh"
 #include <cuda_fp16.h>
@@ -39,34 +47,44 @@
 namespace kda {
 namespace prefill {
 
-constexpr int C = 64;        // chunk length (tokens)
-constexpr int DK = 128;      // internal key dim (Dk = 64 is zero-padded)
-constexpr int DVB = 64;      // value columns per CTA
-constexpr int NT = 128;      // threads per CTA (one TMEM lane each)
-constexpr int LS = 68;       // row stride (floats) of the fp32 scratch matrices
+constexpr int C = 64;          // chunk length (tokens)
+constexpr int DK = 128;        // internal key dim (Dk = 64 is zero-padded)
+constexpr int DVB = 64;        // value columns per CTA
+constexpr int NPREP = 256;     // prep group threads (warps 0-7)
+constexpr int NCHAIN = 128;    // chain group threads (warps 8-11, one TMEM lane each)
+constexpr int NT = NPREP + NCHAIN;
+constexpr int LS = 68;         // row stride (floats) of the fp32 scratch matrices
+constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2;   // named barrier ids
 
-// Shared-memory map (bytes from a 1024-aligned base).  "SW128" tiles use the
-// 128-byte swizzle (see tc.cuh); K-major tiles store one row per M/N index,
-// MN-major tiles one row per K index.
-constexpr uint32_t OFF_A1 = 0;                 // [Km; Qm] tf32, 128 rows x 128 K, K-major   (64 KB)
-constexpr uint32_t OFF_B1 = OFF_A1 + 65536;    // Kb tf32, 64 rows (token) x 128 K, K-major    (32 KB)
-constexpr uint32_t OFF_AH = OFF_B1 + 32768;    // [K~; Q~] f16, 128 rows x 128 K, K-major      (32 KB)
-constexpr uint32_t OFF_KH = OFF_AH + 32768;    // K^ f16, 64 rows (token) x 128 (channel)       (16 KB)
-constexpr uint32_t OFF_P = OFF_KH + 16384;     // [A; 0] f16, 128 rows x 64 K, K-major          (16 KB)
-constexpr uint32_t OFF_Q = OFF_P + 16384;      // [T; Mqk] f16, 128 rows x 64 K, K-major        (16 KB)
+// Shared-memory map (bytes from a 1024-aligned base).  SW128 = 128-byte swizzle
+// (tc.cuh); K-major tiles keep one row per M/N index, MN-major one row per K index.
+constexpr uint32_t OFF_A1 = 0;                 // [Km; Qm] tf32, 128 rows x 128 K, K-major    (64 KB)
+constexpr uint32_t OFF_B1 = OFF_A1 + 65536;    // Kb tf32, 64 rows (token) x 128 K, K-major     (32 KB)
+constexpr uint32_t OFF_AH = OFF_B1 + 32768;    // [K~; Q~] f16, 128 rows x 128 K, K-major       (32 KB)
+constexpr uint32_t OFF_KH = OFF_AH + 32768;    // 2 x K^ f16, 64 rows (token) x 128 (channel)  (2 x 16 KB)
+constexpr uint32_t OFF_P = OFF_KH + 32768;     // A f16, 64 rows x 64 K, K-major                (8 KB)
+constexpr uint32_t OFF_Q = OFF_P + 8192;       // [T; Mqk] f16, 128 rows x 64 K, K-major        (16 KB)
 constexpr uint32_t OFF_S = OFF_Q + 16384;      // S f16, 128 rows (channel) x 64 N, MN-major    (16 KB)
 constexpr uint32_t OFF_XU = OFF_S + 16384;     // X then U f16, 64 rows (token) x 64 N, MN-major (8 KB)
-constexpr uint32_t OFF_VEC = OFF_XU + 8192;    // per-chunk vectors
-constexpr uint32_t VEC_BYTES = (64 + 4 * 128) * 4;
-constexpr uint32_t SMEM_BYTES = OFF_VEC + VEC_BYTES + 1024;  // + alignment slack
-// Preparation scratch (fp32), aliased onto [T; Mqk], S and XU, which are dead
-// between the previous chunk's last MMA and the write of T:
-constexpr uint32_t OFF_L = OFF_Q;                       // L, 64 x LS fp32
-constexpr uint32_t OFF_T = OFF_L + 64 * LS * 4;         // T, 64 x LS fp32
-constexpr uint32_t OFF_Y = OFF_T + 64 * LS * 4;         // Y, 16 x 48 fp32
-static_assert(OFF_Y + 16 * 48 * 4 <= OFF_VEC, "scratch overflows its alias");
+constexpr uint32_t OFF_VEC = OFF_XU + 8192;
+constexpr uint32_t V_EGC = 0;                  // exp(g_C) per chunk parity      [2][128] f32
+constexpr uint32_t V_BETA = V_EGC + 1024;      // beta                           [64] f32
+constexpr uint32_t V_TOT = V_BETA + 256;       // token-group log-decay totals   [8][128] f32
+constexpr uint32_t V_BAR = V_TOT + 4096;       // mbarriers                      8 x 8 B
+constexpr uint32_t V_TMEM = V_BAR + 64;        // TMEM base address
+constexpr uint32_t VEC_BYTES = V_TMEM + 16;
+constexpr uint32_t SMEM_BYTES = OFF_VEC + VEC_BYTES + 1024;   // + alignment slack
+// fp32 scratch of the inverse, aliased onto [Km; Qm] (dead once Km Kb^T is done)
+constexpr uint32_t OFF_L = OFF_A1;                      // L, 64 x LS
+constexpr uint32_t OFF_T = OFF_L + 64 * LS * 4;         // T, 64 x LS
+constexpr uint32_t OFF_Y = OFF_T + 64 * LS * 4;         // Y, 16 x 48
+static_assert(OFF_Y + 16 * 48 * 4 <= OFF_B1, "inverse scratch overflows its alias");
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-// TMEM columns.
+// mbarrier slots
+enum { MB_PREP = 0, MB_CHAIN = 1, MB_READY = 2, MB_AHFREE = 3, MB_QTFREE = 4, MB_KHFREE0 = 5, MB_KHFREE1 = 6 };
+
+// TMEM columns (512 allocated; one CTA per SM).
 constexpr uint32_t TM_G1 = 0, TM_M = 64, TM_D1 = 128, TM_D2 = 192, TM_D3 = 256, TM_COLS = 512;
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -94,29 +112,25 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-__device__ __forceinline__ uint16_t f16_bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
-
 __device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// All threads: order tcgen05 work around a CTA barrier.
-__device__ __forceinline__ void cta_sync_tc() {
+__device__ __forceinline__ void group_sync_tc(uint32_t id, uint32_t n) {
     tc::fence_before_sync();
-    __syncthreads();
+    tc::named_sync(id, n);
     tc::fence_after_sync();
 }
 
-// Issue one M x N x K MMA chain (one thread) and commit it to `bar`.
-// F16: kind::f16 with fp16 operands (16-element K steps), else kind::tf32 (8-element steps).
-// A K-major tile is described by its rows per 128-byte slab (slab stride = rows*128);
-// an MN-major tile keeps K as rows (each K step starts k0 rows in) and its
-// M/N slabs `*_p` bytes apart.
+// Issue one M x N x K MMA chain (one thread).  F16: kind::f16 with fp16 operands
+// (16-element K steps), else kind::tf32 (8-element steps).  A K-major tile is
+// described by its rows per 128-byte slab; an MN-major tile keeps K as rows
+// (each K step starts k0 rows in) and its M/N slabs `*_p` bytes apart.
 template <bool F16>
 __device__ __forceinline__ void issue_mma(uint32_t d_tmem, int M, int N, int K,
                                           uint32_t a_base, bool a_mn, uint32_t a_p,
-                                          uint32_t b_base, bool b_mn, uint32_t b_p, uint64_t* bar) {
+                                          uint32_t b_base, bool b_mn, uint32_t b_p) {
     constexpr uint32_t esz = F16 ? 2u : 4u, kstep = 32u / esz, eps = 128u / esz;
     const uint32_t id = tc::idesc(M, N, F16 ? tc::kFmtF16 : tc::kFmtTF32, a_mn, b_mn);
     for (uint32_t s = 0; s < static_cast<uint32_t>(K) / kstep; ++s) {
@@ -128,19 +142,16 @@ __device__ __forceinline__ void issue_mma(uint32_t d_tmem, int M, int N, int K,
         if (F16) tc::mma_f16(d_tmem, da, db, id, s > 0 ? 1u : 0u);
         else     tc::mma_tf32(d_tmem, da, db, id, s > 0 ? 1u : 0u);
     }
-    tc::mma_commit(bar);
 }
 
-// Load 64 consecutive TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_row64(uint32_t taddr, float (&r)[64]) {
-    float t[16];
+// 32 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
+    float a[16], b[16];
+    tc::tmem_ld16(taddr, a);
+    tc::tmem_ld16(taddr + 16u, b);
+    tc::tmem_wait_ld();
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        tc::tmem_ld16(taddr + 16u * c, t);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) r[16 * c + j] = t[j];
-    }
+    for (int j = 0; j < 16; ++j) { r[j] = a[j]; r[16 + j] = b[j]; }
 }
 
 // Store 8 consecutive fp16 values (one 16-byte chunk) of row `row` into a SW128 tile.
@@ -150,18 +161,37 @@ __device__ __forceinline__ void st_h8(uint8_t* tile, uint32_t row, uint32_t col,
     w.z = f16x2_bits(x[4], x[5]); w.w = f16x2_bits(x[6], x[7]);
     *reinterpret_cast<uint4*>(tile + tc::sw128_off16(row, col, rows)) = w;
 }
+// Store 4 consecutive fp16 values (8 bytes).
+__device__ __forceinline__ void st_h4(uint8_t* tile, uint32_t row, uint32_t col, uint32_t rows, float4 x) {
+    uint2 w;
+    w.x = f16x2_bits(x.x, x.y); w.y = f16x2_bits(x.z, x.w);
+    *reinterpret_cast<uint2*>(tile + tc::sw128_off16(row, col, rows)) = w;
+}
+
+__device__ __forceinline__ float4 f4mul(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
+__device__ __forceinline__ float4 f4add(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
+__device__ __forceinline__ float4 f4ex2(float4 a) { return make_float4(ex2(a.x), ex2(a.y), ex2(a.z), ex2(a.w)); }
+__device__ __forceinline__ float4 bf16x4_to_f4(uint2 w) {
+    const float2 a = bf16x2_bits_to_f32(w.x), b = bf16x2_bits_to_f32(w.y);
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// Bounded wait on an mbarrier phase, agreed across a thread group: returns true
+// only if every thread of the group saw the phase complete.
+__device__ __forceinline__ bool group_wait(void* bar, uint32_t parity, uint32_t id, uint32_t n) {
+    const uint32_t ok = tc::mbar_wait_bounded(bar, parity, kWaitLimitNs);
+    const uint32_t all = tc::named_sync_and(id, n, ok);
+    tc::fence_after_sync();
+    return all != 0;
+}
 
 __global__ void __launch_bounds__(NT, 1) kda_prefill_kernel(const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-    __shared__ uint32_t s_tmem;
-    __shared__ __align__(8) uint64_t s_bar;
-
     uint8_t* A1 = sm + OFF_A1;
     uint8_t* B1 = sm + OFF_B1;
     uint8_t* AH = sm + OFF_AH;
-    uint8_t* KH = sm + OFF_KH;
     uint8_t* P = sm + OFF_P;
     uint8_t* Qt = sm + OFF_Q;
     uint8_t* Sb = sm + OFF_S;
@@ -169,302 +199,395 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_kernel(const Params p)
     float* Lbuf = reinterpret_cast<float*>(sm + OFF_L);
     float* Tbuf = reinterpret_cast<float*>(sm + OFF_T);
     float* Ybuf = reinterpret_cast<float*>(sm + OFF_Y);
-    float* s_beta = reinterpret_cast<float*>(sm + OFF_VEC);   // [64]
-    float* s_egr = s_beta + 64;                                // exp(g_r)       [128]
-    float* s_egc = s_egr + 128;                                // exp(g_C)       [128]
-    float* s_ecr = s_egc + 128;                                // exp(g_C - g_r) [128]
+    uint8_t* vec = sm + OFF_VEC;
+    float* s_egc = reinterpret_cast<float*>(vec + V_EGC);     // [2][128]
+    float* s_beta = reinterpret_cast<float*>(vec + V_BETA);   // [64]
+    float* s_tot = reinterpret_cast<float*>(vec + V_TOT);     // [8][128]
+    uint64_t* mb = reinterpret_cast<uint64_t*>(vec + V_BAR);
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(vec + V_TMEM);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int jb = blockIdx.x % p.nvb;
     const int h = (blockIdx.x / p.nvb) % p.H;
     const int n = blockIdx.x / (p.nvb * p.H);
     const int t0 = p.cu_seqlens[n];
     const int len = p.cu_seqlens[n + 1] - t0;
     const int H = p.H, dk = p.dk, dv = p.dv;
-
-    // checkpoint slot of this sequence's first checkpoint
-    long long slot = 0;
-    if (p.ckpt && p.ckpt_stride > 0) {
-        for (int m = 0; m < n; ++m) {
-            const int lm = p.cu_seqlens[m + 1] - p.cu_seqlens[m];
-            slot += (lm + p.ckpt_stride - 1) / p.ckpt_stride;
-        }
-    }
-
-    if (tid == 0) { tc::mbar_init(&s_bar, 1); tc::mbar_fence_init(); }
-    if (warp == 0) tc::tmem_alloc(&s_tmem, TM_COLS);
-    // Zero the padding rows 64..127 of P once (A occupies rows 0..63 only).
-    for (int i = tid; i < 64 * 8; i += NT) {
-        const int row = 64 + i / 8, ch = i % 8;
-        *reinterpret_cast<uint4*>(P + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    tc::fence_smem_to_async();
-    cta_sync_tc();
-    const uint32_t tm = s_tmem;
-    const uint32_t lane_base = tm + (static_cast<uint32_t>(warp * 32) << 16);
-    uint32_t phase = 0;
-    bool aborted = false;
-
-    // fp32 state rows: thread d holds S[d][jb*64 .. jb*64+63]
-    const int d = tid;
-    float S[DVB];
-    {
-        const float* s0 = p.init_state ? p.init_state + ((static_cast<size_t>(n) * H + h) * dk + d) * dv + jb * DVB : nullptr;
-#pragma unroll
-        for (int j = 0; j < DVB; j += 4) {
-            float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (s0 && d < dk) v4 = *reinterpret_cast<const float4*>(s0 + j);
-            S[j] = v4.x; S[j + 1] = v4.y; S[j + 2] = v4.z; S[j + 3] = v4.w;
-        }
-    }
-
-    auto wait_mma = [&]() -> bool {
-        const uint32_t ok = tc::mbar_wait_bounded(&s_bar, phase, kWaitLimitNs);
-        phase ^= 1u;
-        const int all_ok = __syncthreads_and(static_cast<int>(ok));
-        tc::fence_after_sync();
-        if (!all_ok) { if (tid == 0) set_status(p.status, kStatusTimeout); return false; }
-        return true;
-    };
-
-    const size_t tok_stride = static_cast<size_t>(H) * dk;     // q/k/la row stride
+    const size_t tok_stride = static_cast<size_t>(H) * dk;     // q/k/la row stride (elements)
     const size_t vtok_stride = static_cast<size_t>(H) * dv;    // v/out row stride
     const int nchunks = (len + C - 1) / C;
 
-    for (int c = 0; c < nchunks && !aborted; ++c) {
-        const int cs = t0 + c * C;
-        const int nv = min(C, len - c * C);
+    if (tid == 0) {
+        for (int i = 0; i < 7; ++i) tc::mbar_init(&mb[i], 1);
+        tc::mbar_fence_init();
+    }
+    if (warp == 0) tc::tmem_alloc(s_tmem, TM_COLS);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = *s_tmem;
+    const uint32_t lane_base = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);
 
-        // ---- 1. cumulative log-decay and decayed operands (thread = channel d) ----
-        {
-            float g[C];
-            float acc = 0.f;
-            const float* lap = p.la + static_cast<size_t>(cs) * tok_stride + static_cast<size_t>(h) * dk + d;
-#pragma unroll
-            for (int t = 0; t < C; ++t) {
-                const float l = (t < nv && d < dk) ? __ldg(lap + t * tok_stride) : 0.f;
-                acc += l;
-                g[t] = acc * kLog2e;                     // log2 units
-            }
-            const float gr = g[31], gC = g[C - 1];
-            const float egr = ex2(gr), ecr = ex2(gC - gr);
-            s_egr[d] = egr;
-            s_egc[d] = ex2(gC);
-            s_ecr[d] = ecr;
-            const uint16_t* qp = p.q + static_cast<size_t>(cs) * tok_stride + static_cast<size_t>(h) * dk + d;
-            const uint16_t* kp = p.k + static_cast<size_t>(cs) * tok_stride + static_cast<size_t>(h) * dk + d;
-#pragma unroll
-            for (int t = 0; t < C; ++t) {
-                float qv = 0.f, kv = 0.f;
-                if (t < nv && d < dk) { qv = bf16_bits_to_f32(qp[t * tok_stride]); kv = bf16_bits_to_f32(kp[t * tok_stride]); }
-                const float e1 = ex2(g[t] - gr), e2 = ex2(gr - g[t]);
-                const float km = kv * e1, qm = qv * e1, kb = kv * e2;
-                *reinterpret_cast<float*>(A1 + tc::sw128_off32(t, d, 128)) = tc::to_tf32(km);
-                *reinterpret_cast<float*>(A1 + tc::sw128_off32(64 + t, d, 128)) = tc::to_tf32(qm);
-                *reinterpret_cast<float*>(B1 + tc::sw128_off32(t, d, 64)) = tc::to_tf32(kb);
-                // start-referenced copies (all factors <= 1): K~ = k e^{g_t}, Q~ = q e^{g_t}, K^ = k e^{g_C - g_t}
-                *reinterpret_cast<uint16_t*>(AH + tc::sw128_off16(t, d, 128)) = f16_bits(km * egr);
-                *reinterpret_cast<uint16_t*>(AH + tc::sw128_off16(64 + t, d, 128)) = f16_bits(qm * egr);
-                *reinterpret_cast<uint16_t*>(KH + tc::sw128_off16(t, d, 64)) = f16_bits(kb * ecr);
-            }
-            if (tid < C) s_beta[tid] = (tid < nv) ? bf16_bits_to_f32(p.beta[static_cast<size_t>(cs + tid) * H + h]) : 0.f;
-        }
-        tc::fence_smem_to_async();
-        cta_sync_tc();
+    if (tid < NPREP) {
+        // =============================== prep group ===============================
+        const int pt = tid;
+        const int cg = pt & 31, tg = pt >> 5;             // channels 4cg..4cg+3, tokens 8tg..8tg+7
+        const bool ch_ok = 4 * cg < dk;
+        uint32_t ph_prep = 0;
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int cs = t0 + c * C;
+            const int nv = min(C, len - c * C);
+            const int slot = c & 1;
 
-        // ---- 2. G1 = [Km; Qm] Kb^T  (tf32, 128 x 64, K = 128 channels) ----
-        if (tid == 0) issue_mma<false>(tm + TM_G1, 128, 64, DK, tc::smem_u32(A1), false, 128, tc::smem_u32(B1), false, 64, &s_bar);
-        if (!wait_mma()) { aborted = true; break; }
-
-        // ---- 3. L (rows 0..63 -> fp32 scratch) and A (rows 64..127 -> P rows 0..63) ----
-        {
-            float r[64];
-            tmem_row64(lane_base + TM_G1, r);
-            if (tid < 64) {
-                const float b = s_beta[tid];
-                float* Lr = Lbuf + tid * LS;
+            // -- 0. inputs of this chunk (issued before any wait) --
+            float4 g4[8];
+            uint2 q2[8], k2[8];
+            {
+                const size_t base = static_cast<size_t>(cs) * tok_stride + static_cast<size_t>(h) * dk + 4 * cg;
 #pragma unroll
-                for (int i = 0; i < 64; i += 4) {
-                    float4 w;
-                    w.x = (i + 0 < tid) ? b * r[i + 0] : 0.f;
-                    w.y = (i + 1 < tid) ? b * r[i + 1] : 0.f;
-                    w.z = (i + 2 < tid) ? b * r[i + 2] : 0.f;
-                    w.w = (i + 3 < tid) ? b * r[i + 3] : 0.f;
-                    *reinterpret_cast<float4*>(Lr + i) = w;
-                }
-            } else {
-                const int t = tid - 64;
-#pragma unroll
-                for (int i = 0; i < 64; ++i) r[i] = (i <= t) ? r[i] : 0.f;
-#pragma unroll
-                for (int i = 0; i < 64; i += 8) st_h8(P, t, i, 128, r + i);
-            }
-            for (int i = tid; i < 64 * LS; i += NT) Tbuf[i] = 0.f;
-        }
-        cta_sync_tc();
-
-        // ---- 4. T = (I + L)^{-1}: 16 x 16 diagonal blocks, then block rows ----
-        if (tid < 64) {
-            const int bb = tid >> 4, cc = tid & 15;
-            const float* Lb = Lbuf + (16 * bb) * LS + 16 * bb;
-            float x[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float a = (r == cc) ? 1.f : 0.f;
-#pragma unroll
-                for (int i = 0; i < r; ++i) a -= Lb[r * LS + i] * x[i];
-                x[r] = a;
-            }
-#pragma unroll
-            for (int r = 0; r < 16; ++r) Tbuf[(16 * bb + r) * LS + 16 * bb + cc] = x[r];
-        }
-        __syncthreads();
-        for (int bb = 1; bb < 4; ++bb) {
-            const int ncol = 16 * bb;
-            for (int o = tid; o < 16 * ncol; o += NT) {          // Y = L[rows of bb, :16bb] T[:16bb, :16bb]
-                const int rr = o / ncol, cc = o % ncol;
-                const float* Lr = Lbuf + (16 * bb + rr) * LS;
-                float a = 0.f;
-                for (int i = cc; i < ncol; ++i) a += Lr[i] * Tbuf[i * LS + cc];
-                Ybuf[rr * 48 + cc] = a;
-            }
-            __syncthreads();
-            for (int o = tid; o < 16 * ncol; o += NT) {          // T[rows of bb, :16bb] = -T_bb Y
-                const int rr = o / ncol, cc = o % ncol;
-                const float* Tr = Tbuf + (16 * bb + rr) * LS + 16 * bb;
-                float a = 0.f;
-                for (int i = 0; i <= rr; ++i) a += Tr[i] * Ybuf[i * 48 + cc];
-                Tbuf[(16 * bb + rr) * LS + cc] = -a;
-            }
-            __syncthreads();
-        }
-        // T diag(beta) -> rows 0..63 of the [T; Mqk] tile (staged through registers:
-        // the fp32 scratch shares that tile's bytes)
-        {
-            const int t = tid & 63, half = tid >> 6;
-            float tb[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) tb[i] = Tbuf[t * LS + 32 * half + i] * s_beta[32 * half + i];
-            __syncthreads();
-#pragma unroll
-            for (int i = 0; i < 32; i += 8) st_h8(Qt, t, 32 * half + i, 128, tb + i);
-        }
-        tc::fence_smem_to_async();
-        cta_sync_tc();
-
-        // ---- 5. Mqk = A T  (f16; T rows read as an MN-major B) -> rows 64..127 of [T; Mqk] ----
-        if (tid == 0) issue_mma<true>(tm + TM_M, 128, 64, C, tc::smem_u32(P), false, 128, tc::smem_u32(Qt), true, 128u * 128u, &s_bar);
-        if (!wait_mma()) { aborted = true; break; }
-        if (tid < 64) {
-            float r[64];
-            tmem_row64(lane_base + TM_M, r);
-#pragma unroll
-            for (int i = 0; i < 64; i += 8) st_h8(Qt, 64 + tid, i, 128, r + i);
-        }
-        // ---- 6. the state as an MN-major f16 B tile (row = channel d) ----
-#pragma unroll
-        for (int j = 0; j < DVB; j += 8) st_h8(Sb, d, j, 128, S + j);
-        tc::fence_smem_to_async();
-        cta_sync_tc();
-
-        // ---- 7. D1 = [K~; Q~] S  (rows 0..63: K~ S, rows 64..127: Q~ S) ----
-        if (tid == 0) issue_mma<true>(tm + TM_D1, 128, DVB, DK, tc::smem_u32(AH), false, 128, tc::smem_u32(Sb), true, 128u * 128u, &s_bar);
-        if (!wait_mma()) { aborted = true; break; }
-        if (tid < 64) {                                          // X = V - K~ S
-            float r[64];
-            tmem_row64(lane_base + TM_D1, r);
-            const int t = tid;
-            const uint16_t* vp = p.v + static_cast<size_t>(cs + t) * vtok_stride + static_cast<size_t>(h) * dv + jb * DVB;
-#pragma unroll
-            for (int j = 0; j < DVB; j += 8) {
-                uint4 w = make_uint4(0, 0, 0, 0);
-                if (t < nv) w = *reinterpret_cast<const uint4*>(vp + j);
-                const float2 a0 = bf16x2_bits_to_f32(w.x), a1 = bf16x2_bits_to_f32(w.y);
-                const float2 a2 = bf16x2_bits_to_f32(w.z), a3 = bf16x2_bits_to_f32(w.w);
-                float x8[8] = {a0.x - r[j], a0.y - r[j + 1], a1.x - r[j + 2], a1.y - r[j + 3],
-                               a2.x - r[j + 4], a2.y - r[j + 5], a3.x - r[j + 6], a3.y - r[j + 7]};
-                st_h8(XU, t, j, 64, x8);
-            }
-        }
-        tc::fence_smem_to_async();
-        cta_sync_tc();
-
-        // ---- 8. D2 = [T; Mqk] X  (rows 0..63: U, rows 64..127: Mqk X = A U) ----
-        if (tid == 0) issue_mma<true>(tm + TM_D2, 128, DVB, C, tc::smem_u32(Qt), false, 128, tc::smem_u32(XU), true, 64u * 128u, &s_bar);
-        if (!wait_mma()) { aborted = true; break; }
-        if (tid < 64) {                                          // U -> MN-major B tile (overwrites X)
-            float r[64];
-            tmem_row64(lane_base + TM_D2, r);
-#pragma unroll
-            for (int j = 0; j < DVB; j += 8) st_h8(XU, tid, j, 64, r + j);
-        } else {                                                 // O = Q~ S + A U
-            const int t = tid - 64;
-            const size_t ob = static_cast<size_t>(cs + t) * vtok_stride + static_cast<size_t>(h) * dv + jb * DVB;
-#pragma unroll
-            for (int c16 = 0; c16 < DVB; c16 += 16) {
-                float a[16], b[16];
-                tc::tmem_ld16(lane_base + TM_D2 + c16, a);
-                tc::tmem_ld16(lane_base + TM_D1 + c16, b);
-                tc::tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) a[j] += b[j];
-                if (t < nv) {
-                    if (p.out_f32) {
-                        float* op = reinterpret_cast<float*>(p.out) + ob + c16;
-#pragma unroll
-                        for (int j = 0; j < 16; j += 4)
-                            *reinterpret_cast<float4*>(op + j) = make_float4(a[j], a[j + 1], a[j + 2], a[j + 3]);
+                for (int i = 0; i < 8; ++i) {
+                    const int t = 8 * tg + i;
+                    if (t < nv && ch_ok) {
+                        g4[i] = __ldg(reinterpret_cast<const float4*>(p.la + base + t * tok_stride));
+                        q2[i] = __ldg(reinterpret_cast<const uint2*>(p.q + base + t * tok_stride));
+                        k2[i] = __ldg(reinterpret_cast<const uint2*>(p.k + base + t * tok_stride));
                     } else {
-                        uint16_t* op = reinterpret_cast<uint16_t*>(p.out) + ob + c16;
+                        g4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        q2[i] = make_uint2(0u, 0u);
+                        k2[i] = make_uint2(0u, 0u);
+                    }
+                }
+            }
+            float bt = 0.f;
+            if (pt < C && pt < nv) bt = bf16_bits_to_f32(p.beta[static_cast<size_t>(cs + pt) * H + h]);
+            // -- 1a. cumulative log-decay inside each 8-token group --
+            {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                        for (int j = 0; j < 16; j += 8) {
-                            uint4 w;
-                            w.x = f32x2_to_bf16x2_bits(a[j], a[j + 1]);
-                            w.y = f32x2_to_bf16x2_bits(a[j + 2], a[j + 3]);
-                            w.z = f32x2_to_bf16x2_bits(a[j + 4], a[j + 5]);
-                            w.w = f32x2_to_bf16x2_bits(a[j + 6], a[j + 7]);
-                            *reinterpret_cast<uint4*>(op + j) = w;
+                for (int i = 0; i < 8; ++i) { acc = f4add(acc, g4[i]); g4[i] = acc; }
+                *reinterpret_cast<float4*>(s_tot + tg * 128 + 4 * cg) = acc;
+            }
+            // the chain must be done with [K~; Q~] of chunk c-1 and K^ of chunk c-2
+            if (c >= 1 && !group_wait(&mb[MB_AHFREE], (c - 1) & 1, BAR_PREP, NPREP)) { ok = false; break; }
+            if (c >= 2 && !group_wait(&mb[slot ? MB_KHFREE1 : MB_KHFREE0], ((c - 2) >> 1) & 1, BAR_PREP, NPREP)) { ok = false; break; }
+            tc::named_sync(BAR_PREP, NPREP);     // token-group totals visible
+            if (pt < C) s_beta[pt] = bt;
+            // -- 1b. decay factors and operand tiles --
+            {
+                float4 off = make_float4(0.f, 0.f, 0.f, 0.f), gr = off, gc = off;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 tj = *reinterpret_cast<const float4*>(s_tot + j * 128 + 4 * cg);
+                    if (j < tg) off = f4add(off, tj);
+                    if (j < 4) gr = f4add(gr, tj);
+                    gc = f4add(gc, tj);
+                }
+                const float4 L2 = make_float4(kLog2e, kLog2e, kLog2e, kLog2e);
+                const float4 egr = f4ex2(f4mul(gr, L2));
+                const float4 egc = f4ex2(f4mul(gc, L2));
+                const float4 ecr = f4ex2(f4mul(make_float4(gc.x - gr.x, gc.y - gr.y, gc.z - gr.z, gc.w - gr.w), L2));
+                if (tg == 0) *reinterpret_cast<float4*>(s_egc + slot * 128 + 4 * cg) = egc;
+                uint8_t* KH = sm + OFF_KH + slot * 16384;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int t = 8 * tg + i;
+                    const float4 g = f4add(g4[i], off);
+                    const float4 x = make_float4((g.x - gr.x) * kLog2e, (g.y - gr.y) * kLog2e,
+                                                 (g.z - gr.z) * kLog2e, (g.w - gr.w) * kLog2e);
+                    const float4 e1 = f4ex2(x);
+                    const float4 e2 = f4ex2(make_float4(-x.x, -x.y, -x.z, -x.w));
+                    const float4 kv = bf16x4_to_f4(k2[i]), qv = bf16x4_to_f4(q2[i]);
+                    const float4 km = f4mul(kv, e1), qm = f4mul(qv, e1), kb = f4mul(kv, e2);
+                    *reinterpret_cast<float4*>(A1 + tc::sw128_off32(t, 4 * cg, 128)) = km;
+                    *reinterpret_cast<float4*>(A1 + tc::sw128_off32(64 + t, 4 * cg, 128)) = qm;
+                    *reinterpret_cast<float4*>(B1 + tc::sw128_off32(t, 4 * cg, 64)) = kb;
+                    st_h4(AH, t, 4 * cg, 128, f4mul(km, egr));        // K~ = k e^{g_t}
+                    st_h4(AH, 64 + t, 4 * cg, 128, f4mul(qm, egr));   // Q~ = q e^{g_t}
+                    st_h4(KH, t, 4 * cg, 64, f4mul(kb, ecr));         // K^ = k e^{g_C - g_t}
+                }
+            }
+            tc::fence_smem_to_async();
+            group_sync_tc(BAR_PREP, NPREP);
+
+            // -- 2. G1 = [Km; Qm] Kb^T  (tf32, 128 x 64, K = 128 channels) --
+            if (pt == 0) {
+                issue_mma<false>(tm + TM_G1, 128, 64, DK, tc::smem_u32(A1), false, 128, tc::smem_u32(B1), false, 64);
+                tc::mma_commit(&mb[MB_PREP]);
+            }
+            if (!group_wait(&mb[MB_PREP], ph_prep & 1, BAR_PREP, NPREP)) { ok = false; break; }
+            ++ph_prep;
+
+            // -- 3. L (rows 0..63 -> fp32 scratch), A (rows 64..127 -> f16 tile) --
+            {
+                const int r = (warp & 3) * 32 + lane;
+                const int c0 = (warp >> 2) * 32;                 // warps 0-3: cols 0..31, 4-7: 32..63
+                float v[32];
+                tmem_ld32(lane_base + TM_G1 + c0, v);
+                if (r < 64) {
+                    const float b = s_beta[r];
+                    float* Lr = Lbuf + r * LS + c0;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        float4 w;
+                        w.x = (c0 + i + 0 < r) ? b * v[i + 0] : 0.f;
+                        w.y = (c0 + i + 1 < r) ? b * v[i + 1] : 0.f;
+                        w.z = (c0 + i + 2 < r) ? b * v[i + 2] : 0.f;
+                        w.w = (c0 + i + 3 < r) ? b * v[i + 3] : 0.f;
+                        *reinterpret_cast<float4*>(Lr + i) = w;
+                    }
+                } else {
+                    const int t = r - 64;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = (c0 + i <= t) ? v[i] : 0.f;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) st_h8(P, t, c0 + i, 64, v + i);
+                }
+            }
+            group_sync_tc(BAR_PREP, NPREP);
+
+            // -- 4. T = (I + L)^{-1}: 16 x 16 diagonal blocks, then block rows --
+            for (int i = pt; i < 64 * LS / 4; i += NPREP)
+                reinterpret_cast<float4*>(Tbuf)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            tc::named_sync(BAR_PREP, NPREP);
+            if (pt < 64) {
+                const int bb = pt >> 4, cc = pt & 15;
+                const float* Lb = Lbuf + (16 * bb) * LS + 16 * bb;
+                float x[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    float a = (r == cc) ? 1.f : 0.f;
+#pragma unroll
+                    for (int i = 0; i < r; ++i) a -= Lb[r * LS + i] * x[i];
+                    x[r] = a;
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) Tbuf[(16 * bb + r) * LS + 16 * bb + cc] = x[r];
+            }
+            tc::named_sync(BAR_PREP, NPREP);
+            for (int bb = 1; bb < 4; ++bb) {
+                const int ncol = 16 * bb;
+                for (int o = pt; o < 16 * ncol; o += NPREP) {     // Y = L[rows of bb, :16bb] T[:16bb, :16bb]
+                    const int rr = o / ncol, cc = o % ncol;
+                    const float* Lr = Lbuf + (16 * bb + rr) * LS;
+                    float a0 = 0.f, a1 = 0.f;
+                    int i = cc;
+                    for (; i + 1 < ncol; i += 2) { a0 += Lr[i] * Tbuf[i * LS + cc]; a1 += Lr[i + 1] * Tbuf[(i + 1) * LS + cc]; }
+                    if (i < ncol) a0 += Lr[i] * Tbuf[i * LS + cc];
+                    Ybuf[rr * 48 + cc] = a0 + a1;
+                }
+                tc::named_sync(BAR_PREP, NPREP);
+                for (int o = pt; o < 16 * ncol; o += NPREP) {     // T[rows of bb, :16bb] = -T_bb Y
+                    const int rr = o / ncol, cc = o % ncol;
+                    const float* Tr = Tbuf + (16 * bb + rr) * LS + 16 * bb;
+                    float a = 0.f;
+                    for (int i = 0; i <= rr; ++i) a += Tr[i] * Ybuf[i * 48 + cc];
+                    Tbuf[(16 * bb + rr) * LS + cc] = -a;
+                }
+                tc::named_sync(BAR_PREP, NPREP);
+            }
+            // the chain must be done with [T; Mqk] of chunk c-1 before it is rewritten
+            if (c >= 1 && !group_wait(&mb[MB_QTFREE], (c - 1) & 1, BAR_PREP, NPREP)) { ok = false; break; }
+            {   // T diag(beta) -> rows 0..63 of [T; Mqk]: thread -> (row, 16 columns)
+                const int t = pt >> 2, c0 = (pt & 3) * 16;
+                float tb[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) tb[i] = Tbuf[t * LS + c0 + i] * s_beta[c0 + i];
+                st_h8(Qt, t, c0, 128, tb);
+                st_h8(Qt, t, c0 + 8, 128, tb + 8);
+            }
+            tc::fence_smem_to_async();
+            group_sync_tc(BAR_PREP, NPREP);
+
+            // -- 5. Mqk = A T  (f16, M = 64; T rows read as an MN-major B) --
+            if (pt == 0) {
+                issue_mma<true>(tm + TM_M, 64, 64, C, tc::smem_u32(P), false, 64, tc::smem_u32(Qt), true, 128u * 128u);
+                tc::mma_commit(&mb[MB_PREP]);
+            }
+            if (!group_wait(&mb[MB_PREP], ph_prep & 1, BAR_PREP, NPREP)) { ok = false; break; }
+            ++ph_prep;
+            {   // M = 64 layout: row r sits in TMEM lane 32 (r / 16) + r % 16
+                const int c0 = (warp >> 2) * 32;
+                float v[32];
+                tmem_ld32(lane_base + TM_M + c0, v);
+                if (lane < 16) {
+                    const int r = (warp & 3) * 16 + lane;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) st_h8(Qt, 64 + r, c0 + i, 128, v + i);
+                }
+            }
+            tc::fence_smem_to_async();
+            group_sync_tc(BAR_PREP, NPREP);
+            if (pt == 0) tc::mbar_arrive(&mb[MB_READY]);       // chunk c handed to the chain
+        }
+        if (!ok && pt == 0) set_status(p.status, kStatusTimeout);
+    } else {
+        // =============================== chain group ===============================
+        const int d = tid - NPREP;                           // state row = TMEM lane
+        uint32_t ph_chain = 0;
+        bool ok = true;
+        long long slot_ck = 0;
+        if (p.ckpt && p.ckpt_stride > 0) {
+            for (int m = 0; m < n; ++m) {
+                const int lm = p.cu_seqlens[m + 1] - p.cu_seqlens[m];
+                slot_ck += (lm + p.ckpt_stride - 1) / p.ckpt_stride;
+            }
+        }
+        float S[DVB];
+        {
+            const float* s0 = p.init_state ? p.init_state + ((static_cast<size_t>(n) * H + h) * dk + d) * dv + jb * DVB : nullptr;
+#pragma unroll
+            for (int j = 0; j < DVB; j += 4) {
+                float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (s0 && d < dk) v4 = *reinterpret_cast<const float4*>(s0 + j);
+                S[j] = v4.x; S[j + 1] = v4.y; S[j + 2] = v4.z; S[j + 3] = v4.w;
+            }
+        }
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int cs = t0 + c * C;
+            const int nv = min(C, len - c * C);
+            const int slot = c & 1;
+            // value row of this thread's token, fetched before waiting
+            uint4 vr[DVB / 8];
+#pragma unroll
+            for (int j = 0; j < DVB / 8; ++j) vr[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (d < 64 && d < nv) {
+                const uint16_t* vp = p.v + static_cast<size_t>(cs + d) * vtok_stride + static_cast<size_t>(h) * dv + jb * DVB;
+#pragma unroll
+                for (int j = 0; j < DVB / 8; ++j) vr[j] = __ldg(reinterpret_cast<const uint4*>(vp) + j);
+            }
+            if (!group_wait(&mb[MB_READY], c & 1, BAR_CHAIN, NCHAIN)) { ok = false; break; }
+            // exp(g_C) of this chunk: read now, before the prep can reuse the slot (chunk c+2)
+            const float gc = s_egc[slot * 128 + d];
+
+            // -- 6. state as an MN-major f16 tile; D1 = [K~; Q~] S --
+#pragma unroll
+            for (int j = 0; j < DVB; j += 8) st_h8(Sb, d, j, 128, S + j);
+            tc::fence_smem_to_async();
+            group_sync_tc(BAR_CHAIN, NCHAIN);
+            if (d == 0) {
+                issue_mma<true>(tm + TM_D1, 128, DVB, DK, tc::smem_u32(AH), false, 128, tc::smem_u32(Sb), true, 128u * 128u);
+                tc::mma_commit(&mb[MB_CHAIN]);
+                tc::mma_commit(&mb[MB_AHFREE]);
+            }
+            if (!group_wait(&mb[MB_CHAIN], ph_chain & 1, BAR_CHAIN, NCHAIN)) { ok = false; break; }
+            ++ph_chain;
+
+            // -- 7. X = V - K~ S  (rows 0..63) --
+            if (d < 64) {
+                float r[32];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    tmem_ld32(lane_base + TM_D1 + 32 * half, r);
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8) {
+                        const uint4 w = vr[(32 * half + j) / 8];
+                        const float2 a0 = bf16x2_bits_to_f32(w.x), a1 = bf16x2_bits_to_f32(w.y);
+                        const float2 a2 = bf16x2_bits_to_f32(w.z), a3 = bf16x2_bits_to_f32(w.w);
+                        float x8[8] = {a0.x - r[j], a0.y - r[j + 1], a1.x - r[j + 2], a1.y - r[j + 3],
+                                       a2.x - r[j + 4], a2.y - r[j + 5], a3.x - r[j + 6], a3.y - r[j + 7]};
+                        st_h8(XU, d, 32 * half + j, 64, x8);
+                    }
+                }
+            }
+            tc::fence_smem_to_async();
+            group_sync_tc(BAR_CHAIN, NCHAIN);
+
+            // -- 8. D2 = [T; Mqk] X  (rows 0..63: U, rows 64..127: A U) --
+            if (d == 0) {
+                issue_mma<true>(tm + TM_D2, 128, DVB, C, tc::smem_u32(Qt), false, 128, tc::smem_u32(XU), true, 64u * 128u);
+                tc::mma_commit(&mb[MB_CHAIN]);
+                tc::mma_commit(&mb[MB_QTFREE]);
+            }
+            if (!group_wait(&mb[MB_CHAIN], ph_chain & 1, BAR_CHAIN, NCHAIN)) { ok = false; break; }
+            ++ph_chain;
+            if (d < 64) {                                    // U -> MN-major f16 tile (overwrites X)
+                float r[32];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    tmem_ld32(lane_base + TM_D2 + 32 * half, r);
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8) st_h8(XU, d, 32 * half + j, 64, r + j);
+                }
+            } else {                                         // O = Q~ S + A U
+                const int t = d - 64;
+                const size_t ob = static_cast<size_t>(cs + t) * vtok_stride + static_cast<size_t>(h) * dv + jb * DVB;
+#pragma unroll
+                for (int c16 = 0; c16 < DVB; c16 += 16) {
+                    float a[16], b[16];
+                    tc::tmem_ld16(lane_base + TM_D2 + c16, a);
+                    tc::tmem_ld16(lane_base + TM_D1 + c16, b);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) a[j] += b[j];
+                    if (t < nv) {
+                        if (p.out_f32) {
+                            float* op = reinterpret_cast<float*>(p.out) + ob + c16;
+#pragma unroll
+                            for (int j = 0; j < 16; j += 4)
+                                *reinterpret_cast<float4*>(op + j) = make_float4(a[j], a[j + 1], a[j + 2], a[j + 3]);
+                        } else {
+                            uint16_t* op = reinterpret_cast<uint16_t*>(p.out) + ob + c16;
+#pragma unroll
+                            for (int j = 0; j < 16; j += 8) {
+                                uint4 w;
+                                w.x = f32x2_to_bf16x2_bits(a[j], a[j + 1]);
+                                w.y = f32x2_to_bf16x2_bits(a[j + 2], a[j + 3]);
+                                w.z = f32x2_to_bf16x2_bits(a[j + 4], a[j + 5]);
+                                w.w = f32x2_to_bf16x2_bits(a[j + 6], a[j + 7]);
+                                *reinterpret_cast<uint4*>(op + j) = w;
+                            }
                         }
                     }
                 }
             }
-        }
-        tc::fence_smem_to_async();
-        cta_sync_tc();
+            tc::fence_smem_to_async();
+            group_sync_tc(BAR_CHAIN, NCHAIN);
 
-        // ---- 9. D3 = K^^T U  (K^ tile read as an MN-major A: M = channel, K = token) ----
-        if (tid == 0) issue_mma<true>(tm + TM_D3, 128, DVB, C, tc::smem_u32(KH), true, 64u * 128u, tc::smem_u32(XU), true, 64u * 128u, &s_bar);
-        if (!wait_mma()) { aborted = true; break; }
-        {
-            float r[64];
-            tmem_row64(lane_base + TM_D3, r);
-            const float gc = s_egc[d];
+            // -- 9. D3 = K^^T U  (K^ tile as an MN-major A: M = channel, K = token) --
+            if (d == 0) {
+                issue_mma<true>(tm + TM_D3, 128, DVB, C, tc::smem_u32(sm + OFF_KH + slot * 16384), true, 64u * 128u,
+                                tc::smem_u32(XU), true, 64u * 128u);
+                tc::mma_commit(&mb[MB_CHAIN]);
+                tc::mma_commit(&mb[slot ? MB_KHFREE1 : MB_KHFREE0]);
+            }
+            if (!group_wait(&mb[MB_CHAIN], ph_chain & 1, BAR_CHAIN, NCHAIN)) { ok = false; break; }
+            ++ph_chain;
+            {
+                float r[32];
 #pragma unroll
-            for (int j = 0; j < DVB; ++j) S[j] = gc * S[j] + r[j];
-        }
-        // ---- 10. prefix-cache checkpoint at stride multiples and at the sequence end ----
-        if (p.ckpt && p.ckpt_stride > 0) {
-            const int done = c * C + nv;
-            if (done % p.ckpt_stride == 0 || done == len) {
-                if (d < dk) {
-                    float* cp = p.ckpt + ((static_cast<size_t>(slot) * H + h) * dk + d) * dv + jb * DVB;
+                for (int half = 0; half < 2; ++half) {
+                    tmem_ld32(lane_base + TM_D3 + 32 * half, r);
 #pragma unroll
-                    for (int j = 0; j < DVB; j += 4)
-                        *reinterpret_cast<float4*>(cp + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+                    for (int j = 0; j < 32; ++j) S[32 * half + j] = gc * S[32 * half + j] + r[j];
                 }
-                ++slot;
+            }
+            // -- 10. prefix-cache checkpoint at stride multiples and at the sequence end --
+            if (p.ckpt && p.ckpt_stride > 0) {
+                const int done = c * C + nv;
+                if (done % p.ckpt_stride == 0 || done == len) {
+                    if (d < dk) {
+                        float* cp = p.ckpt + ((static_cast<size_t>(slot_ck) * H + h) * dk + d) * dv + jb * DVB;
+#pragma unroll
+                        for (int j = 0; j < DVB; j += 4)
+                            *reinterpret_cast<float4*>(cp + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+                    }
+                    ++slot_ck;
+                }
             }
         }
-        cta_sync_tc();
+        if (ok && p.final_state && d < dk) {
+            float* fp = p.final_state + ((static_cast<size_t>(n) * H + h) * dk + d) * dv + jb * DVB;
+#pragma unroll
+            for (int j = 0; j < DVB; j += 4)
+                *reinterpret_cast<float4*>(fp + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        }
+        if (!ok && d == 0) set_status(p.status, kStatusTimeout);
     }
 
-    if (!aborted && p.final_state && d < dk) {
-        float* fp = p.final_state + ((static_cast<size_t>(n) * H + h) * dk + d) * dv + jb * DVB;
-#pragma unroll
-        for (int j = 0; j < DVB; j += 4)
-            *reinterpret_cast<float4*>(fp + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-    }
-    cta_sync_tc();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
     if (warp == 0) tc::tmem_dealloc(tm, TM_COLS);
 }
 

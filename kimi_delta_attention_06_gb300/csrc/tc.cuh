@@ -161,3 +161,31 @@ __host__ __device__ __forceinline__ uint32_t sw128_off16(uint32_t row, uint32_t 
 
 }  // namespace tc
 }  // namespace kda
+
+namespace kda {
+namespace tc {
+
+// Named CTA barrier over `nthreads` threads (a multiple of 32) with id 1..15.
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also ANDs a predicate across the participating threads.
+__device__ __forceinline__ uint32_t named_sync_and(uint32_t id, uint32_t nthreads, uint32_t pred) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %3, 0;\n\t"
+        "bar.red.and.pred q, %1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(out) : "r"(id), "r"(nthreads), "r"(pred) : "memory");
+    return out;
+}
+
+__device__ __forceinline__ void mbar_arrive(void* bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}\n"
+                 :: "r"(smem_u32(bar)) : "memory");
+}
+
+}  // namespace tc
+}  // namespace kda

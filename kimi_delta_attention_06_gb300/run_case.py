@@ -1,0 +1,66 @@
+"""Run one KDA workload a few times through the C ABI (for profilers and quick timing).
+
+  python -m kimi_delta_attention_06_gb300.run_case --what prefill --T 8192 [--H 32] [--D 128] [--reps 2]
+  python -m kimi_delta_attention_06_gb300.run_case --what decode --N 512 [--H 32] [--D 128] [--reps 2]
+
+Inputs are the seeded synthetic tensors of workloads.py, generated on the GPU.
+Prints the CUDA-event time of each repetition.
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+from . import build, kda, workloads
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--what", choices=["prefill", "decode"], default="prefill")
+    ap.add_argument("--T", type=int, default=8192)
+    ap.add_argument("--N", type=int, default=512)
+    ap.add_argument("--H", type=int, default=32)
+    ap.add_argument("--D", type=int, default=128)
+    ap.add_argument("--ckpt", type=int, default=32768)
+    ap.add_argument("--reps", type=int, default=2)
+    a = ap.parse_args(argv)
+    build.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    if a.what == "prefill":
+        c = workloads.single_case(a.T, seed=2, device=dev, H=a.H, D=a.D, ckpt_stride=a.ckpt)
+        cu = c.cu_seqlens.to(dev)
+        out = torch.empty(a.T, a.H, a.D, device=dev, dtype=torch.bfloat16)
+        fin = torch.empty(1, a.H, a.D, a.D, device=dev)
+        nck = kda.kda_ckpt_count(c.cu_seqlens, a.ckpt)
+        ck = torch.empty(max(nck, 1), a.H, a.D, a.D, device=dev)
+
+        def run():
+            kda.kda_chunk_prefill(c.q, c.k, c.v, c.log_alpha, c.beta, c.init_state, cu, c.cu_seqlens, 1, a.T,
+                                  a.H, a.D, a.D, out, kda.KDA_OUT_BF16, fin, ck if nck else None, a.ckpt, stream)
+        units = f"{a.T} tokens"
+    else:
+        d = workloads.decode_case(N=a.N, H=a.H, D=a.D, steps=1, seed=4, device=dev)
+        s = d.steps[0]
+        out = torch.empty(a.N, a.H, a.D, device=dev, dtype=torch.bfloat16)
+
+        def run():
+            kda.kda_decode_step(s["q"], s["k"], s["v"], s["log_alpha"], s["beta"], d.state, out,
+                                kda.KDA_OUT_BF16, a.N, a.H, a.D, a.D, stream)
+        units = f"{a.N} sequences"
+    for i in range(a.reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        print(f"{a.what} rep {i}: {e0.elapsed_time(e1):.3f} ms ({units})")
+    st = kda.kda_device_status()
+    if st != 0:
+        raise SystemExit(f"device status {st}")
+
+
+if __name__ == "__main__":
+    main()
