@@ -26,20 +26,22 @@
 // an 8-bit exponent.  Everything else (start-referenced decayed operands with
 // factors <= 1, A, T, X, U, the state) is range-safe and runs as fp16 MMAs
 // (10-bit mantissa like tf32, twice the rate, half the bytes).  The 64 x 64
-// triangular inverse runs on CUDA cores in fp32 (16 x 16 diagonal blocks, then
-// block rows).
+// triangular inverse runs on CUDA cores in fp32: 16 x 16 diagonal blocks by
+// forward substitution, then two levels of block doubling.
 //
-// CTA organisation: one CTA per (sequence, head, 64-column block of Dv); value
-// columns are exactly independent, so the split needs no communication.  The
-// CTA is warp-specialised so that the state-independent preparation of chunk
-// c+1 overlaps the sequential state chain of chunk c:
-//   * prep group, warps 0-7: decays and decayed operand tiles, Km Kb^T / Qm Kb^T,
-//     the inverse, Mqk = A T.  Hands the chain [K~; Q~], K^ (double-buffered),
-//     [T; Mqk] and exp(g_C).
-//   * chain group, warps 8-11: owns the fp32 state block (one row per thread, in
-//     registers for the whole sequence) and runs X, U/O and the state update.
-// The groups hand off through mbarriers; every wait is bounded and a timeout
-// makes the kernel record KDA_ERR_TIMEOUT and return.
+// Work decomposition: one thread-block cluster of 4 CTAs per (sequence, head).
+//   * CTA 0 (chain): owns the fp32 state (Dk x Dv, one row per thread, in
+//     registers for the whole sequence; two warpgroups split the value
+//     columns) and runs the sequential part -- X, U and O, the state update --
+//     as three dependent MMAs per chunk.
+//   * CTAs 1-3 (prep): chunk c is prepared by CTA 1 + c % 3.  Each builds
+//     [K~; Q~], K^, [T; Mqk] and exp(g_C) for its chunk in its own shared
+//     memory and ships them, as one contiguous bulk copy, into slot c % 2 of
+//     the chain CTA's shared memory (distributed shared memory).
+// Three chunks are being prepared while the chain consumes a fourth, so the
+// chain's dependent-MMA latency, not the preparation, sets the pace.
+// Hand-offs use mbarriers (remote arrivals, transaction-count completion); every
+// wait is bounded, and a timeout records KDA_ERR_TIMEOUT and ends the kernel.
 #include "common.cuh"
 #include "tc.cuh"
 #include <cuda_fp16.h>
@@ -47,45 +49,52 @@
 namespace kda {
 namespace prefill {
 
-constexpr int C = 64;          // chunk length (tokens)
-constexpr int DK = 128;        // internal key dim (Dk = 64 is zero-padded)
-constexpr int DVB = 64;        // value columns per CTA
-constexpr int NPREP = 256;     // prep group threads (warps 0-7)
-constexpr int NCHAIN = 128;    // chain group threads (warps 8-11, one TMEM lane each)
-constexpr int NT = NPREP + NCHAIN;
-constexpr int LS = 68;         // row stride (floats) of the fp32 scratch matrices
-constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2;   // named barrier ids
+constexpr int C = 64;           // chunk length (tokens)
+constexpr int DK = 128;         // internal key dim (Dk = 64 is zero-padded)
+constexpr int NT = 256;         // threads per CTA
+constexpr int NPREP_CTAS = 3;   // prep CTAs per cluster
+constexpr int CLUSTER = 1 + NPREP_CTAS;
+constexpr int LS = 68;          // row stride (floats) of the fp32 scratch matrices
+constexpr uint32_t BAR_ALL = 1;  // named barrier over the CTA's 256 threads
 
-// Shared-memory map (bytes from a 1024-aligned base).  SW128 = 128-byte swizzle
-// (tc.cuh); K-major tiles keep one row per M/N index, MN-major one row per K index.
-constexpr uint32_t OFF_A1 = 0;                 // [Km; Qm] tf32, 128 rows x 128 K, K-major    (64 KB)
-constexpr uint32_t OFF_B1 = OFF_A1 + 65536;    // Kb tf32, 64 rows (token) x 128 K, K-major     (32 KB)
-constexpr uint32_t OFF_AH = OFF_B1 + 32768;    // [K~; Q~] f16, 128 rows x 128 K, K-major       (32 KB)
-constexpr uint32_t OFF_KH = OFF_AH + 32768;    // 2 x K^ f16, 64 rows (token) x 128 (channel)  (2 x 16 KB)
-constexpr uint32_t OFF_P = OFF_KH + 32768;     // A f16, 64 rows x 64 K, K-major                (8 KB)
-constexpr uint32_t OFF_Q = OFF_P + 8192;       // [T; Mqk] f16, 128 rows x 64 K, K-major        (16 KB)
-constexpr uint32_t OFF_S = OFF_Q + 16384;      // S f16, 128 rows (channel) x 64 N, MN-major    (16 KB)
-constexpr uint32_t OFF_XU = OFF_S + 16384;     // X then U f16, 64 rows (token) x 64 N, MN-major (8 KB)
-constexpr uint32_t OFF_VEC = OFF_XU + 8192;
-constexpr uint32_t V_EGC = 0;                  // exp(g_C) per chunk parity      [2][128] f32
-constexpr uint32_t V_BETA = V_EGC + 1024;      // beta                           [64] f32
-constexpr uint32_t V_TOT = V_BETA + 256;       // token-group log-decay totals   [8][128] f32
-constexpr uint32_t V_BAR = V_TOT + 4096;       // mbarriers                      8 x 8 B
-constexpr uint32_t V_TMEM = V_BAR + 64;        // TMEM base address
-constexpr uint32_t VEC_BYTES = V_TMEM + 16;
-constexpr uint32_t SMEM_BYTES = OFF_VEC + VEC_BYTES + 1024;   // + alignment slack
+// Hand-off block: produced in a prep CTA, copied verbatim into a chain slot.
+constexpr uint32_t H_AH = 0;                 // [K~; Q~] f16, 128 rows x 128 K, K-major  (32 KB)
+constexpr uint32_t H_KH = 32768;             // K^ f16, 64 rows (token) x 128 (channel)  (16 KB)
+constexpr uint32_t H_QT = 49152;             // [T; Mqk] f16, 128 rows x 64 K, K-major   (16 KB)
+constexpr uint32_t H_EGC = 65536;            // exp(g_C), 128 f32                         (512 B)
+constexpr uint32_t H_BYTES = 65536 + 512;
+constexpr uint32_t H_STRIDE = 66560;         // slot pitch (1024-aligned)
+
+// Prep CTA shared memory.
+constexpr uint32_t P_A1 = 0;                 // [Km; Qm] tf32, 128 rows x 128 K, K-major  (64 KB)
+constexpr uint32_t P_B1 = 65536;             // Kb tf32, 64 rows x 128 K, K-major          (32 KB)
+constexpr uint32_t P_OUT = 98304;            // hand-off block                             (65 KB)
+constexpr uint32_t P_P = P_OUT + H_STRIDE;   // A f16, 64 rows x 64 K, K-major             (8 KB)
+constexpr uint32_t P_BETA = P_P + 8192;      // beta [64] f32
+constexpr uint32_t P_TOT = P_BETA + 256;     // token-group log-decay totals [8][128] f32
+constexpr uint32_t P_BAR = P_TOT + 4096;     // mbarriers: 0 mma, 1 recv, 2 free
+constexpr uint32_t P_TMEM = P_BAR + 32;
+constexpr uint32_t P_END = P_TMEM + 16;
 // fp32 scratch of the inverse, aliased onto [Km; Qm] (dead once Km Kb^T is done)
-constexpr uint32_t OFF_L = OFF_A1;                      // L, 64 x LS
-constexpr uint32_t OFF_T = OFF_L + 64 * LS * 4;         // T, 64 x LS
-constexpr uint32_t OFF_Y = OFF_T + 64 * LS * 4;         // Y, 16 x 48
-static_assert(OFF_Y + 16 * 48 * 4 <= OFF_B1, "inverse scratch overflows its alias");
+constexpr uint32_t P_L = P_A1;
+constexpr uint32_t P_T = P_L + 64 * LS * 4;
+constexpr uint32_t P_Y = P_T + 64 * LS * 4;  // 32 x 36 (also 2 x 16 x 20)
+static_assert(P_Y + 32 * 36 * 4 <= P_B1, "inverse scratch overflows its alias");
+
+// Chain CTA shared memory.
+constexpr uint32_t K_SLOT = 0;                       // 2 hand-off slots
+constexpr uint32_t K_S = 2 * H_STRIDE;               // S f16, 128 rows (channel) x 128 N, MN-major (32 KB)
+constexpr uint32_t K_XU = K_S + 32768;               // X then U f16, 64 rows (token) x 128 N, MN-major (16 KB)
+constexpr uint32_t K_BAR = K_XU + 16384;             // mbarriers: 0 mma, 1-2 full[slot]
+constexpr uint32_t K_TMEM = K_BAR + 32;
+constexpr uint32_t K_END = K_TMEM + 16;
+
+constexpr uint32_t SMEM_BYTES = (P_END > K_END ? P_END : K_END) + 1024;   // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-// mbarrier slots
-enum { MB_PREP = 0, MB_CHAIN = 1, MB_READY = 2, MB_AHFREE = 3, MB_QTFREE = 4, MB_KHFREE0 = 5, MB_KHFREE1 = 6 };
-
-// TMEM columns (512 allocated; one CTA per SM).
-constexpr uint32_t TM_G1 = 0, TM_M = 64, TM_D1 = 128, TM_D2 = 192, TM_D3 = 256, TM_COLS = 512;
+// TMEM columns.
+constexpr uint32_t TM_G1 = 0, TM_M = 64, TM_PREP_COLS = 128;                 // prep CTA
+constexpr uint32_t TM_D1 = 0, TM_D2 = 128, TM_D3 = 256, TM_CHAIN_COLS = 512; // chain CTA
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -103,7 +112,7 @@ struct Params {
     int* status;
     int out_f32;
     int ckpt_stride;
-    int H, dk, dv, nvb;
+    int H, dk, dv;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -117,9 +126,9 @@ __device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ void group_sync_tc(uint32_t id, uint32_t n) {
+__device__ __forceinline__ void cta_sync_tc() {
     tc::fence_before_sync();
-    tc::named_sync(id, n);
+    tc::named_sync(BAR_ALL, NT);
     tc::fence_after_sync();
 }
 
@@ -176,419 +185,497 @@ __device__ __forceinline__ float4 bf16x4_to_f4(uint2 w) {
     return make_float4(a.x, a.y, b.x, b.y);
 }
 
-// Bounded wait on an mbarrier phase, agreed across a thread group: returns true
-// only if every thread of the group saw the phase complete.
-__device__ __forceinline__ bool group_wait(void* bar, uint32_t parity, uint32_t id, uint32_t n) {
-    const uint32_t ok = tc::mbar_wait_bounded(bar, parity, kWaitLimitNs);
-    const uint32_t all = tc::named_sync_and(id, n, ok);
+// Bounded wait on an mbarrier phase, agreed by all threads of the CTA.
+__device__ __forceinline__ bool cta_wait(void* bar, uint32_t parity, bool cluster_scope) {
+    const uint32_t ok = cluster_scope ? tc::mbar_wait_cluster_bounded(bar, parity, kWaitLimitNs)
+                                      : tc::mbar_wait_bounded(bar, parity, kWaitLimitNs);
+    const uint32_t all = tc::named_sync_and(BAR_ALL, NT, ok);
     tc::fence_after_sync();
     return all != 0;
+}
+
+// ============================================================================
+// Prep CTA: prepares chunks c = pr, pr + 3, pr + 6, ... of one (sequence, head).
+// ============================================================================
+__device__ void prep_role(const Params& p, uint8_t* sm, int pr, int h, int t0, int len) {
+    uint8_t* A1 = sm + P_A1;
+    uint8_t* B1 = sm + P_B1;
+    uint8_t* OUT = sm + P_OUT;
+    uint8_t* AH = OUT + H_AH;
+    uint8_t* KH = OUT + H_KH;
+    uint8_t* Qt = OUT + H_QT;
+    float* s_egc_out = reinterpret_cast<float*>(OUT + H_EGC);
+    uint8_t* P = sm + P_P;
+    float* Lbuf = reinterpret_cast<float*>(sm + P_L);
+    float* Tbuf = reinterpret_cast<float*>(sm + P_T);
+    float* Ybuf = reinterpret_cast<float*>(sm + P_Y);
+    float* s_beta = reinterpret_cast<float*>(sm + P_BETA);
+    float* s_tot = reinterpret_cast<float*>(sm + P_TOT);
+    uint64_t* mb = reinterpret_cast<uint64_t*>(sm + P_BAR);    // 0: mma, 1: recv, 2: free
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + P_TMEM);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = p.H, dk = p.dk;
+    const size_t tok_stride = static_cast<size_t>(H) * dk;
+    const int nchunks = (len + C - 1) / C;
+
+    if (warp == 0) tc::tmem_alloc(s_tmem, TM_PREP_COLS);
+    cta_sync_tc();
+    const uint32_t tm = *s_tmem;
+    const uint32_t lane_base = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    // the chain CTA's (rank 0) two slots and their full barriers
+    const uint32_t chain_slot0 = tc::mapa(tc::smem_u32(sm + K_SLOT), 0);
+    const uint32_t chain_full0 = tc::mapa(tc::smem_u32(sm + K_BAR + 8), 0);
+
+    const int cg = tid & 31, tg = tid >> 5;             // channels 4cg..4cg+3, tokens 8tg..8tg+7
+    const bool ch_ok = 4 * cg < dk;
+    uint32_t ph_mma = 0, n_recv = 0, n_free = 0;
+    bool ok = true;
+    int kk = 0;                                         // index of this CTA's chunk
+    for (int c = pr; c < nchunks; c += NPREP_CTAS, ++kk) {
+        const int cs = t0 + c * C;
+        const int nv = min(C, len - c * C);
+
+        // -- 0. inputs of this chunk --
+        float4 g4[8];
+        uint2 q2[8], k2[8];
+        {
+            const size_t base = static_cast<size_t>(cs) * tok_stride + static_cast<size_t>(h) * dk + 4 * cg;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int t = 8 * tg + i;
+                if (t < nv && ch_ok) {
+                    g4[i] = __ldg(reinterpret_cast<const float4*>(p.la + base + t * tok_stride));
+                    q2[i] = __ldg(reinterpret_cast<const uint2*>(p.q + base + t * tok_stride));
+                    k2[i] = __ldg(reinterpret_cast<const uint2*>(p.k + base + t * tok_stride));
+                } else {
+                    g4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    q2[i] = make_uint2(0u, 0u);
+                    k2[i] = make_uint2(0u, 0u);
+                }
+            }
+        }
+        float bt = 0.f;
+        if (tid < C && tid < nv) bt = bf16_bits_to_f32(p.beta[static_cast<size_t>(cs + tid) * H + h]);
+        // -- 1a. cumulative log-decay inside each 8-token group --
+        {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) { acc = f4add(acc, g4[i]); g4[i] = acc; }
+            *reinterpret_cast<float4*>(s_tot + tg * 128 + 4 * cg) = acc;
+        }
+        // the previous hand-off of this CTA must have landed before the block is rewritten
+        if (kk >= 1) {
+            if (!cta_wait(&mb[1], n_recv & 1, true)) { ok = false; break; }
+            ++n_recv;
+        }
+        tc::named_sync(BAR_ALL, NT);     // token-group totals visible
+        if (tid < C) s_beta[tid] = bt;
+        // -- 1b. decay factors and operand tiles --
+        {
+            float4 off = make_float4(0.f, 0.f, 0.f, 0.f), gr = off, gc = off;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 tj = *reinterpret_cast<const float4*>(s_tot + j * 128 + 4 * cg);
+                if (j < tg) off = f4add(off, tj);
+                if (j < 4) gr = f4add(gr, tj);
+                gc = f4add(gc, tj);
+            }
+            const float4 L2 = make_float4(kLog2e, kLog2e, kLog2e, kLog2e);
+            const float4 egr = f4ex2(f4mul(gr, L2));
+            const float4 egc = f4ex2(f4mul(gc, L2));
+            const float4 ecr = f4ex2(f4mul(make_float4(gc.x - gr.x, gc.y - gr.y, gc.z - gr.z, gc.w - gr.w), L2));
+            if (tg == 0) *reinterpret_cast<float4*>(s_egc_out + 4 * cg) = egc;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int t = 8 * tg + i;
+                const float4 g = f4add(g4[i], off);
+                const float4 x = make_float4((g.x - gr.x) * kLog2e, (g.y - gr.y) * kLog2e,
+                                             (g.z - gr.z) * kLog2e, (g.w - gr.w) * kLog2e);
+                const float4 e1 = f4ex2(x);
+                const float4 e2 = f4ex2(make_float4(-x.x, -x.y, -x.z, -x.w));
+                const float4 kv = bf16x4_to_f4(k2[i]), qv = bf16x4_to_f4(q2[i]);
+                const float4 km = f4mul(kv, e1), qm = f4mul(qv, e1), kb = f4mul(kv, e2);
+                *reinterpret_cast<float4*>(A1 + tc::sw128_off32(t, 4 * cg, 128)) = km;
+                *reinterpret_cast<float4*>(A1 + tc::sw128_off32(64 + t, 4 * cg, 128)) = qm;
+                *reinterpret_cast<float4*>(B1 + tc::sw128_off32(t, 4 * cg, 64)) = kb;
+                st_h4(AH, t, 4 * cg, 128, f4mul(km, egr));        // K~ = k e^{g_t}
+                st_h4(AH, 64 + t, 4 * cg, 128, f4mul(qm, egr));   // Q~ = q e^{g_t}
+                st_h4(KH, t, 4 * cg, 64, f4mul(kb, ecr));         // K^ = k e^{g_C - g_t}
+            }
+        }
+        tc::fence_smem_to_async();
+        cta_sync_tc();
+
+        // -- 2. G1 = [Km; Qm] Kb^T  (tf32, 128 x 64, K = 128 channels) --
+        if (tid == 0) {
+            issue_mma<false>(tm + TM_G1, 128, 64, DK, tc::smem_u32(A1), false, 128, tc::smem_u32(B1), false, 64);
+            tc::mma_commit(&mb[0]);
+        }
+        if (!cta_wait(&mb[0], ph_mma & 1, false)) { ok = false; break; }
+        ++ph_mma;
+
+        // -- 3. L (rows 0..63 -> fp32 scratch), A (rows 64..127 -> f16 tile) --
+        {
+            const int r = (warp & 3) * 32 + lane;
+            const int c0 = (warp >> 2) * 32;                 // warps 0-3: cols 0..31, 4-7: 32..63
+            float v[32];
+            tmem_ld32(lane_base + TM_G1 + c0, v);
+            if (r < 64) {
+                const float b = s_beta[r];
+                float* Lr = Lbuf + r * LS + c0;
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    float4 w;
+                    w.x = (c0 + i + 0 < r) ? b * v[i + 0] : 0.f;
+                    w.y = (c0 + i + 1 < r) ? b * v[i + 1] : 0.f;
+                    w.z = (c0 + i + 2 < r) ? b * v[i + 2] : 0.f;
+                    w.w = (c0 + i + 3 < r) ? b * v[i + 3] : 0.f;
+                    *reinterpret_cast<float4*>(Lr + i) = w;
+                }
+            } else {
+                const int t = r - 64;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = (c0 + i <= t) ? v[i] : 0.f;
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) st_h8(P, t, c0 + i, 64, v + i);
+            }
+        }
+        cta_sync_tc();
+
+        // -- 4. T = (I + L)^{-1} by recursive doubling over 16 x 16 blocks --
+        //    blocks [[A, 0], [B, D]]^{-1} = [[A^-1, 0], [-D^-1 B A^-1, D^-1]]
+        for (int i = tid; i < 64 * LS / 4; i += NT)
+            reinterpret_cast<float4*>(Tbuf)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        tc::named_sync(BAR_ALL, NT);
+        if (tid < 64) {            // diagonal blocks, column-oriented forward substitution
+            const int bb = tid >> 4, cc = tid & 15;
+            const float* Lb = Lbuf + (16 * bb) * LS + 16 * bb;
+            float s[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) s[r] = (r == cc) ? 1.f : 0.f;
+#pragma unroll
+            for (int j = 0; j < 15; ++j) {
+#pragma unroll
+                for (int r = j + 1; r < 16; ++r) s[r] -= Lb[r * LS + j] * s[j];
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) Tbuf[(16 * bb + r) * LS + 16 * bb + cc] = s[r];
+        }
+        tc::named_sync(BAR_ALL, NT);
+        {                         // 16 -> 32: blocks (1,0) and (3,2), 128 threads each
+            const int pp = tid >> 7, q7 = tid & 127;
+            const int r = q7 >> 3, c2 = (q7 & 7) * 2;
+            const int R = 16 * (2 * pp + 1), Cc = 16 * (2 * pp);
+            const float* Lr = Lbuf + (R + r) * LS + Cc;
+            float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float l = Lr[k];
+                const float2 tk = *reinterpret_cast<const float2*>(Tbuf + (Cc + k) * LS + Cc + c2);
+                y0 += l * tk.x; y1 += l * tk.y;
+            }
+            *reinterpret_cast<float2*>(Ybuf + pp * 16 * 20 + r * 20 + c2) = make_float2(y0, y1);
+            tc::named_sync(BAR_ALL, NT);
+            const float* Tr = Tbuf + (R + r) * LS + R;
+            const float* Yp = Ybuf + pp * 16 * 20;
+            float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float t = Tr[k];
+                const float2 yk = *reinterpret_cast<const float2*>(Yp + k * 20 + c2);
+                z0 += t * yk.x; z1 += t * yk.y;
+            }
+            *reinterpret_cast<float2*>(Tbuf + (R + r) * LS + Cc + c2) = make_float2(-z0, -z1);
+        }
+        tc::named_sync(BAR_ALL, NT);
+        {                         // 32 -> 64: block (1,0) of 32 x 32 blocks
+            const int r = tid >> 3, c4 = (tid & 7) * 4;
+            const float* Lr = Lbuf + (32 + r) * LS;
+            float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+            for (int k = 0; k < 32; ++k) {
+                const float l = Lr[k];
+                const float4 tk = *reinterpret_cast<const float4*>(Tbuf + k * LS + c4);
+                y.x += l * tk.x; y.y += l * tk.y; y.z += l * tk.z; y.w += l * tk.w;
+            }
+            *reinterpret_cast<float4*>(Ybuf + r * 36 + c4) = y;
+            tc::named_sync(BAR_ALL, NT);
+            const float* Tr = Tbuf + (32 + r) * LS + 32;
+            float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+            for (int k = 0; k < 32; ++k) {
+                const float t = Tr[k];
+                const float4 yk = *reinterpret_cast<const float4*>(Ybuf + k * 36 + c4);
+                z.x += t * yk.x; z.y += t * yk.y; z.z += t * yk.z; z.w += t * yk.w;
+            }
+            *reinterpret_cast<float4*>(Tbuf + (32 + r) * LS + c4) = make_float4(-z.x, -z.y, -z.z, -z.w);
+        }
+        tc::named_sync(BAR_ALL, NT);
+        {   // T diag(beta) -> rows 0..63 of [T; Mqk]: thread -> (row, 16 columns)
+            const int t = tid >> 2, c0 = (tid & 3) * 16;
+            float tb[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) tb[i] = Tbuf[t * LS + c0 + i] * s_beta[c0 + i];
+            st_h8(Qt, t, c0, 128, tb);
+            st_h8(Qt, t, c0 + 8, 128, tb + 8);
+        }
+        tc::fence_smem_to_async();
+        cta_sync_tc();
+
+        // -- 5. Mqk = A T  (f16, M = 64; T rows read as an MN-major B) --
+        if (tid == 0) {
+            issue_mma<true>(tm + TM_M, 64, 64, C, tc::smem_u32(P), false, 64, tc::smem_u32(Qt), true, 128u * 128u);
+            tc::mma_commit(&mb[0]);
+        }
+        if (!cta_wait(&mb[0], ph_mma & 1, false)) { ok = false; break; }
+        ++ph_mma;
+        {   // M = 64 layout: row r sits in TMEM lane 32 (r / 16) + r % 16
+            const int c0 = (warp >> 2) * 32;
+            float v[32];
+            tmem_ld32(lane_base + TM_M + c0, v);
+            if (lane < 16) {
+                const int r = (warp & 3) * 16 + lane;
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) st_h8(Qt, 64 + r, c0 + i, 128, v + i);
+            }
+        }
+        tc::fence_smem_to_async();
+        cta_sync_tc();
+
+        // -- 6. hand the block to the chain CTA: slot c % 2, once that slot is free --
+        if (c >= 2) {
+            if (!cta_wait(&mb[2], n_free & 1, true)) { ok = false; break; }
+            ++n_free;
+        }
+        if (tid == 0) {
+            const uint32_t s = static_cast<uint32_t>(c & 1);
+            tc::mbar_arrive_expect_tx_remote(chain_full0 + 8u * s, H_BYTES);
+            tc::bulk_copy_s2cluster(chain_slot0 + s * H_STRIDE, tc::smem_u32(OUT), H_BYTES, chain_full0 + 8u * s);
+        }
+    }
+    if (!ok && tid == 0) set_status(p.status, kStatusTimeout);
+    cta_sync_tc();
+    if (warp == 0) tc::tmem_dealloc(tm, TM_PREP_COLS);
+}
+
+// ============================================================================
+// Chain CTA: the sequential state recurrence of one (sequence, head).
+// ============================================================================
+__device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, int len) {
+    uint8_t* Sb = sm + K_S;
+    uint8_t* XU = sm + K_XU;
+    uint64_t* mb = reinterpret_cast<uint64_t*>(sm + K_BAR);     // 0: mma, 1-2: full[slot]
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + K_TMEM);
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int d = tid & 127;                 // state row = TMEM lane
+    const int wg = tid >> 7;                 // value columns 64 wg .. 64 wg + 63
+    const int H = p.H, dk = p.dk, dv = p.dv;
+    const bool col_ok = 64 * wg < dv;
+    const size_t vtok_stride = static_cast<size_t>(H) * dv;
+    const int nchunks = (len + C - 1) / C;
+
+    if (warp == 0) tc::tmem_alloc(s_tmem, TM_CHAIN_COLS);
+    cta_sync_tc();
+    const uint32_t tm = *s_tmem;
+    const uint32_t lane_base = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t cb = static_cast<uint32_t>(64 * wg);      // this warpgroup's TMEM column offset
+    const uint32_t prep_recv = tc::smem_u32(sm + P_BAR + 8);  // local offsets of the prep barriers
+    const uint32_t prep_free = tc::smem_u32(sm + P_BAR + 16);
+
+    long long slot_ck = 0;
+    if (p.ckpt && p.ckpt_stride > 0) {
+        for (int m = 0; m < n; ++m) {
+            const int lm = p.cu_seqlens[m + 1] - p.cu_seqlens[m];
+            slot_ck += (lm + p.ckpt_stride - 1) / p.ckpt_stride;
+        }
+    }
+    float S[64];
+    {
+        const float* s0 = (p.init_state && col_ok && d < dk)
+            ? p.init_state + ((static_cast<size_t>(n) * H + h) * dk + d) * dv + 64 * wg : nullptr;
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) {
+            float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (s0) v4 = *reinterpret_cast<const float4*>(s0 + j);
+            S[j] = v4.x; S[j + 1] = v4.y; S[j + 2] = v4.z; S[j + 3] = v4.w;
+        }
+    }
+    const int Nmma = dv;                      // 64 or 128 value columns
+    uint32_t ph_mma = 0;
+    bool ok = true;
+    for (int c = 0; c < nchunks; ++c) {
+        const int cs = t0 + c * C;
+        const int nv = min(C, len - c * C);
+        const int s = c & 1;
+        uint8_t* slot = sm + K_SLOT + s * H_STRIDE;
+        // value row of this thread's token (rows 0..63), fetched before waiting
+        uint4 vr[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) vr[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (d < 64 && d < nv && col_ok) {
+            const uint16_t* vp = p.v + static_cast<size_t>(cs + d) * vtok_stride + static_cast<size_t>(h) * dv + 64 * wg;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) vr[j] = __ldg(reinterpret_cast<const uint4*>(vp) + j);
+        }
+        if (!cta_wait(&mb[1 + s], (c >> 1) & 1, false)) { ok = false; break; }
+        // the producer's staging block is free again
+        if (tid == 0) tc::mbar_arrive_remote(tc::mapa(prep_recv, 1 + c % NPREP_CTAS));
+        const float gc = reinterpret_cast<const float*>(slot + H_EGC)[d];
+
+        // -- state as an MN-major f16 tile; D1 = [K~; Q~] S --
+#pragma unroll
+        for (int j = 0; j < 64; j += 8) st_h8(Sb, d, 64 * wg + j, 128, S + j);
+        tc::fence_smem_to_async();
+        cta_sync_tc();
+        if (tid == 0) {
+            issue_mma<true>(tm + TM_D1, 128, Nmma, DK, tc::smem_u32(slot + H_AH), false, 128,
+                            tc::smem_u32(Sb), true, 128u * 128u);
+            tc::mma_commit(&mb[0]);
+        }
+        if (!cta_wait(&mb[0], ph_mma & 1, false)) { ok = false; break; }
+        ++ph_mma;
+
+        // -- X = V - K~ S  (rows 0..63) --
+        if (d < 64) {
+            float r[32];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                tmem_ld32(lane_base + TM_D1 + cb + 32 * half, r);
+#pragma unroll
+                for (int j = 0; j < 32; j += 8) {
+                    const uint4 w = vr[(32 * half + j) / 8];
+                    const float2 a0 = bf16x2_bits_to_f32(w.x), a1 = bf16x2_bits_to_f32(w.y);
+                    const float2 a2 = bf16x2_bits_to_f32(w.z), a3 = bf16x2_bits_to_f32(w.w);
+                    float x8[8] = {a0.x - r[j], a0.y - r[j + 1], a1.x - r[j + 2], a1.y - r[j + 3],
+                                   a2.x - r[j + 4], a2.y - r[j + 5], a3.x - r[j + 6], a3.y - r[j + 7]};
+                    st_h8(XU, d, 64 * wg + 32 * half + j, 64, x8);
+                }
+            }
+        }
+        tc::fence_smem_to_async();
+        cta_sync_tc();
+
+        // -- D2 = [T; Mqk] X  (rows 0..63: U, rows 64..127: A U) --
+        if (tid == 0) {
+            issue_mma<true>(tm + TM_D2, 128, Nmma, C, tc::smem_u32(slot + H_QT), false, 128,
+                            tc::smem_u32(XU), true, 64u * 128u);
+            tc::mma_commit(&mb[0]);
+        }
+        if (!cta_wait(&mb[0], ph_mma & 1, false)) { ok = false; break; }
+        ++ph_mma;
+        if (d < 64) {                                    // U -> MN-major f16 tile (overwrites X)
+            float r[32];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                tmem_ld32(lane_base + TM_D2 + cb + 32 * half, r);
+#pragma unroll
+                for (int j = 0; j < 32; j += 8) st_h8(XU, d, 64 * wg + 32 * half + j, 64, r + j);
+            }
+        } else {                                         // O = Q~ S + A U
+            const int t = d - 64;
+            const size_t ob = static_cast<size_t>(cs + t) * vtok_stride + static_cast<size_t>(h) * dv + 64 * wg;
+#pragma unroll
+            for (int c16 = 0; c16 < 64; c16 += 16) {
+                float a[16], b[16];
+                tc::tmem_ld16(lane_base + TM_D2 + cb + c16, a);
+                tc::tmem_ld16(lane_base + TM_D1 + cb + c16, b);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) a[j] += b[j];
+                if (t < nv && col_ok) {
+                    if (p.out_f32) {
+                        float* op = reinterpret_cast<float*>(p.out) + ob + c16;
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4)
+                            *reinterpret_cast<float4*>(op + j) = make_float4(a[j], a[j + 1], a[j + 2], a[j + 3]);
+                    } else {
+                        uint16_t* op = reinterpret_cast<uint16_t*>(p.out) + ob + c16;
+#pragma unroll
+                        for (int j = 0; j < 16; j += 8) {
+                            uint4 w;
+                            w.x = f32x2_to_bf16x2_bits(a[j], a[j + 1]);
+                            w.y = f32x2_to_bf16x2_bits(a[j + 2], a[j + 3]);
+                            w.z = f32x2_to_bf16x2_bits(a[j + 4], a[j + 5]);
+                            w.w = f32x2_to_bf16x2_bits(a[j + 6], a[j + 7]);
+                            *reinterpret_cast<uint4*>(op + j) = w;
+                        }
+                    }
+                }
+            }
+        }
+        tc::fence_smem_to_async();
+        cta_sync_tc();
+
+        // -- D3 = K^^T U  (K^ tile as an MN-major A: M = channel, K = token) --
+        if (tid == 0) {
+            issue_mma<true>(tm + TM_D3, 128, Nmma, C, tc::smem_u32(slot + H_KH), true, 64u * 128u,
+                            tc::smem_u32(XU), true, 64u * 128u);
+            tc::mma_commit(&mb[0]);
+        }
+        if (!cta_wait(&mb[0], ph_mma & 1, false)) { ok = false; break; }
+        ++ph_mma;
+        // slot s is free: the producer of chunk c + 2 may overwrite it
+        if (tid == 0 && c + 2 < nchunks) tc::mbar_arrive_remote(tc::mapa(prep_free, 1 + (c + 2) % NPREP_CTAS));
+        {
+            float r[32];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                tmem_ld32(lane_base + TM_D3 + cb + 32 * half, r);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) S[32 * half + j] = gc * S[32 * half + j] + r[j];
+            }
+        }
+        // -- prefix-cache checkpoint at stride multiples and at the sequence end --
+        if (p.ckpt && p.ckpt_stride > 0) {
+            const int done = c * C + nv;
+            if (done % p.ckpt_stride == 0 || done == len) {
+                if (d < dk && col_ok) {
+                    float* cp = p.ckpt + ((static_cast<size_t>(slot_ck) * H + h) * dk + d) * dv + 64 * wg;
+#pragma unroll
+                    for (int j = 0; j < 64; j += 4)
+                        *reinterpret_cast<float4*>(cp + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+                }
+                ++slot_ck;
+            }
+        }
+    }
+    if (ok && p.final_state && d < dk && col_ok) {
+        float* fp = p.final_state + ((static_cast<size_t>(n) * H + h) * dk + d) * dv + 64 * wg;
+#pragma unroll
+        for (int j = 0; j < 64; j += 4)
+            *reinterpret_cast<float4*>(fp + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    }
+    if (!ok && tid == 0) set_status(p.status, kStatusTimeout);
+    cta_sync_tc();
+    if (warp == 0) tc::tmem_dealloc(tm, TM_CHAIN_COLS);
 }
 
 __global__ void __launch_bounds__(NT, 1) kda_prefill_kernel(const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint8_t* A1 = sm + OFF_A1;
-    uint8_t* B1 = sm + OFF_B1;
-    uint8_t* AH = sm + OFF_AH;
-    uint8_t* P = sm + OFF_P;
-    uint8_t* Qt = sm + OFF_Q;
-    uint8_t* Sb = sm + OFF_S;
-    uint8_t* XU = sm + OFF_XU;
-    float* Lbuf = reinterpret_cast<float*>(sm + OFF_L);
-    float* Tbuf = reinterpret_cast<float*>(sm + OFF_T);
-    float* Ybuf = reinterpret_cast<float*>(sm + OFF_Y);
-    uint8_t* vec = sm + OFF_VEC;
-    float* s_egc = reinterpret_cast<float*>(vec + V_EGC);     // [2][128]
-    float* s_beta = reinterpret_cast<float*>(vec + V_BETA);   // [64]
-    float* s_tot = reinterpret_cast<float*>(vec + V_TOT);     // [8][128]
-    uint64_t* mb = reinterpret_cast<uint64_t*>(vec + V_BAR);
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(vec + V_TMEM);
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int jb = blockIdx.x % p.nvb;
-    const int h = (blockIdx.x / p.nvb) % p.H;
-    const int n = blockIdx.x / (p.nvb * p.H);
+    const int rank = static_cast<int>(tc::cluster_ctarank());
+    const int cl = blockIdx.x / CLUSTER;                  // (sequence, head)
+    const int h = cl % p.H;
+    const int n = cl / p.H;
     const int t0 = p.cu_seqlens[n];
     const int len = p.cu_seqlens[n + 1] - t0;
-    const int H = p.H, dk = p.dk, dv = p.dv;
-    const size_t tok_stride = static_cast<size_t>(H) * dk;     // q/k/la row stride (elements)
-    const size_t vtok_stride = static_cast<size_t>(H) * dv;    // v/out row stride
-    const int nchunks = (len + C - 1) / C;
 
-    if (tid == 0) {
-        for (int i = 0; i < 7; ++i) tc::mbar_init(&mb[i], 1);
+    // every CTA initialises its barriers before any peer can touch them
+    if (threadIdx.x == 0) {
+        uint64_t* mb = reinterpret_cast<uint64_t*>(sm + (rank == 0 ? K_BAR : P_BAR));
+        tc::mbar_init(&mb[0], 1);
+        tc::mbar_init(&mb[1], 1);
+        tc::mbar_init(&mb[2], 1);
         tc::mbar_fence_init();
     }
-    if (warp == 0) tc::tmem_alloc(s_tmem, TM_COLS);
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tm = *s_tmem;
-    const uint32_t lane_base = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-
-    if (tid < NPREP) {
-        // =============================== prep group ===============================
-        const int pt = tid;
-        const int cg = pt & 31, tg = pt >> 5;             // channels 4cg..4cg+3, tokens 8tg..8tg+7
-        const bool ch_ok = 4 * cg < dk;
-        uint32_t ph_prep = 0;
-        bool ok = true;
-        for (int c = 0; c < nchunks && ok; ++c) {
-            const int cs = t0 + c * C;
-            const int nv = min(C, len - c * C);
-            const int slot = c & 1;
-
-            // -- 0. inputs of this chunk (issued before any wait) --
-            float4 g4[8];
-            uint2 q2[8], k2[8];
-            {
-                const size_t base = static_cast<size_t>(cs) * tok_stride + static_cast<size_t>(h) * dk + 4 * cg;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int t = 8 * tg + i;
-                    if (t < nv && ch_ok) {
-                        g4[i] = __ldg(reinterpret_cast<const float4*>(p.la + base + t * tok_stride));
-                        q2[i] = __ldg(reinterpret_cast<const uint2*>(p.q + base + t * tok_stride));
-                        k2[i] = __ldg(reinterpret_cast<const uint2*>(p.k + base + t * tok_stride));
-                    } else {
-                        g4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        q2[i] = make_uint2(0u, 0u);
-                        k2[i] = make_uint2(0u, 0u);
-                    }
-                }
-            }
-            float bt = 0.f;
-            if (pt < C && pt < nv) bt = bf16_bits_to_f32(p.beta[static_cast<size_t>(cs + pt) * H + h]);
-            // -- 1a. cumulative log-decay inside each 8-token group --
-            {
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) { acc = f4add(acc, g4[i]); g4[i] = acc; }
-                *reinterpret_cast<float4*>(s_tot + tg * 128 + 4 * cg) = acc;
-            }
-            // the chain must be done with [K~; Q~] of chunk c-1 and K^ of chunk c-2
-            if (c >= 1 && !group_wait(&mb[MB_AHFREE], (c - 1) & 1, BAR_PREP, NPREP)) { ok = false; break; }
-            if (c >= 2 && !group_wait(&mb[slot ? MB_KHFREE1 : MB_KHFREE0], ((c - 2) >> 1) & 1, BAR_PREP, NPREP)) { ok = false; break; }
-            tc::named_sync(BAR_PREP, NPREP);     // token-group totals visible
-            if (pt < C) s_beta[pt] = bt;
-            // -- 1b. decay factors and operand tiles --
-            {
-                float4 off = make_float4(0.f, 0.f, 0.f, 0.f), gr = off, gc = off;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float4 tj = *reinterpret_cast<const float4*>(s_tot + j * 128 + 4 * cg);
-                    if (j < tg) off = f4add(off, tj);
-                    if (j < 4) gr = f4add(gr, tj);
-                    gc = f4add(gc, tj);
-                }
-                const float4 L2 = make_float4(kLog2e, kLog2e, kLog2e, kLog2e);
-                const float4 egr = f4ex2(f4mul(gr, L2));
-                const float4 egc = f4ex2(f4mul(gc, L2));
-                const float4 ecr = f4ex2(f4mul(make_float4(gc.x - gr.x, gc.y - gr.y, gc.z - gr.z, gc.w - gr.w), L2));
-                if (tg == 0) *reinterpret_cast<float4*>(s_egc + slot * 128 + 4 * cg) = egc;
-                uint8_t* KH = sm + OFF_KH + slot * 16384;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int t = 8 * tg + i;
-                    const float4 g = f4add(g4[i], off);
-                    const float4 x = make_float4((g.x - gr.x) * kLog2e, (g.y - gr.y) * kLog2e,
-                                                 (g.z - gr.z) * kLog2e, (g.w - gr.w) * kLog2e);
-                    const float4 e1 = f4ex2(x);
-                    const float4 e2 = f4ex2(make_float4(-x.x, -x.y, -x.z, -x.w));
-                    const float4 kv = bf16x4_to_f4(k2[i]), qv = bf16x4_to_f4(q2[i]);
-                    const float4 km = f4mul(kv, e1), qm = f4mul(qv, e1), kb = f4mul(kv, e2);
-                    *reinterpret_cast<float4*>(A1 + tc::sw128_off32(t, 4 * cg, 128)) = km;
-                    *reinterpret_cast<float4*>(A1 + tc::sw128_off32(64 + t, 4 * cg, 128)) = qm;
-                    *reinterpret_cast<float4*>(B1 + tc::sw128_off32(t, 4 * cg, 64)) = kb;
-                    st_h4(AH, t, 4 * cg, 128, f4mul(km, egr));        // K~ = k e^{g_t}
-                    st_h4(AH, 64 + t, 4 * cg, 128, f4mul(qm, egr));   // Q~ = q e^{g_t}
-                    st_h4(KH, t, 4 * cg, 64, f4mul(kb, ecr));         // K^ = k e^{g_C - g_t}
-                }
-            }
-            tc::fence_smem_to_async();
-            group_sync_tc(BAR_PREP, NPREP);
-
-            // -- 2. G1 = [Km; Qm] Kb^T  (tf32, 128 x 64, K = 128 channels) --
-            if (pt == 0) {
-                issue_mma<false>(tm + TM_G1, 128, 64, DK, tc::smem_u32(A1), false, 128, tc::smem_u32(B1), false, 64);
-                tc::mma_commit(&mb[MB_PREP]);
-            }
-            if (!group_wait(&mb[MB_PREP], ph_prep & 1, BAR_PREP, NPREP)) { ok = false; break; }
-            ++ph_prep;
-
-            // -- 3. L (rows 0..63 -> fp32 scratch), A (rows 64..127 -> f16 tile) --
-            {
-                const int r = (warp & 3) * 32 + lane;
-                const int c0 = (warp >> 2) * 32;                 // warps 0-3: cols 0..31, 4-7: 32..63
-                float v[32];
-                tmem_ld32(lane_base + TM_G1 + c0, v);
-                if (r < 64) {
-                    const float b = s_beta[r];
-                    float* Lr = Lbuf + r * LS + c0;
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        float4 w;
-                        w.x = (c0 + i + 0 < r) ? b * v[i + 0] : 0.f;
-                        w.y = (c0 + i + 1 < r) ? b * v[i + 1] : 0.f;
-                        w.z = (c0 + i + 2 < r) ? b * v[i + 2] : 0.f;
-                        w.w = (c0 + i + 3 < r) ? b * v[i + 3] : 0.f;
-                        *reinterpret_cast<float4*>(Lr + i) = w;
-                    }
-                } else {
-                    const int t = r - 64;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = (c0 + i <= t) ? v[i] : 0.f;
-#pragma unroll
-                    for (int i = 0; i < 32; i += 8) st_h8(P, t, c0 + i, 64, v + i);
-                }
-            }
-            group_sync_tc(BAR_PREP, NPREP);
-
-            // -- 4. T = (I + L)^{-1}: 16 x 16 diagonal blocks, then block rows --
-            for (int i = pt; i < 64 * LS / 4; i += NPREP)
-                reinterpret_cast<float4*>(Tbuf)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            tc::named_sync(BAR_PREP, NPREP);
-            if (pt < 64) {
-                const int bb = pt >> 4, cc = pt & 15;
-                const float* Lb = Lbuf + (16 * bb) * LS + 16 * bb;
-                float x[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    float a = (r == cc) ? 1.f : 0.f;
-#pragma unroll
-                    for (int i = 0; i < r; ++i) a -= Lb[r * LS + i] * x[i];
-                    x[r] = a;
-                }
-#pragma unroll
-                for (int r = 0; r < 16; ++r) Tbuf[(16 * bb + r) * LS + 16 * bb + cc] = x[r];
-            }
-            tc::named_sync(BAR_PREP, NPREP);
-            for (int bb = 1; bb < 4; ++bb) {
-                const int ncol = 16 * bb;
-                for (int o = pt; o < 16 * ncol; o += NPREP) {     // Y = L[rows of bb, :16bb] T[:16bb, :16bb]
-                    const int rr = o / ncol, cc = o % ncol;
-                    const float* Lr = Lbuf + (16 * bb + rr) * LS;
-                    float a0 = 0.f, a1 = 0.f;
-                    int i = cc;
-                    for (; i + 1 < ncol; i += 2) { a0 += Lr[i] * Tbuf[i * LS + cc]; a1 += Lr[i + 1] * Tbuf[(i + 1) * LS + cc]; }
-                    if (i < ncol) a0 += Lr[i] * Tbuf[i * LS + cc];
-                    Ybuf[rr * 48 + cc] = a0 + a1;
-                }
-                tc::named_sync(BAR_PREP, NPREP);
-                for (int o = pt; o < 16 * ncol; o += NPREP) {     // T[rows of bb, :16bb] = -T_bb Y
-                    const int rr = o / ncol, cc = o % ncol;
-                    const float* Tr = Tbuf + (16 * bb + rr) * LS + 16 * bb;
-                    float a = 0.f;
-                    for (int i = 0; i <= rr; ++i) a += Tr[i] * Ybuf[i * 48 + cc];
-                    Tbuf[(16 * bb + rr) * LS + cc] = -a;
-                }
-                tc::named_sync(BAR_PREP, NPREP);
-            }
-            // the chain must be done with [T; Mqk] of chunk c-1 before it is rewritten
-            if (c >= 1 && !group_wait(&mb[MB_QTFREE], (c - 1) & 1, BAR_PREP, NPREP)) { ok = false; break; }
-            {   // T diag(beta) -> rows 0..63 of [T; Mqk]: thread -> (row, 16 columns)
-                const int t = pt >> 2, c0 = (pt & 3) * 16;
-                float tb[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) tb[i] = Tbuf[t * LS + c0 + i] * s_beta[c0 + i];
-                st_h8(Qt, t, c0, 128, tb);
-                st_h8(Qt, t, c0 + 8, 128, tb + 8);
-            }
-            tc::fence_smem_to_async();
-            group_sync_tc(BAR_PREP, NPREP);
-
-            // -- 5. Mqk = A T  (f16, M = 64; T rows read as an MN-major B) --
-            if (pt == 0) {
-                issue_mma<true>(tm + TM_M, 64, 64, C, tc::smem_u32(P), false, 64, tc::smem_u32(Qt), true, 128u * 128u);
-                tc::mma_commit(&mb[MB_PREP]);
-            }
-            if (!group_wait(&mb[MB_PREP], ph_prep & 1, BAR_PREP, NPREP)) { ok = false; break; }
-            ++ph_prep;
-            {   // M = 64 layout: row r sits in TMEM lane 32 (r / 16) + r % 16
-                const int c0 = (warp >> 2) * 32;
-                float v[32];
-                tmem_ld32(lane_base + TM_M + c0, v);
-                if (lane < 16) {
-                    const int r = (warp & 3) * 16 + lane;
-#pragma unroll
-                    for (int i = 0; i < 32; i += 8) st_h8(Qt, 64 + r, c0 + i, 128, v + i);
-                }
-            }
-            tc::fence_smem_to_async();
-            group_sync_tc(BAR_PREP, NPREP);
-            if (pt == 0) tc::mbar_arrive(&mb[MB_READY]);       // chunk c handed to the chain
-        }
-        if (!ok && pt == 0) set_status(p.status, kStatusTimeout);
-    } else {
-        // =============================== chain group ===============================
-        const int d = tid - NPREP;                           // state row = TMEM lane
-        uint32_t ph_chain = 0;
-        bool ok = true;
-        long long slot_ck = 0;
-        if (p.ckpt && p.ckpt_stride > 0) {
-            for (int m = 0; m < n; ++m) {
-                const int lm = p.cu_seqlens[m + 1] - p.cu_seqlens[m];
-                slot_ck += (lm + p.ckpt_stride - 1) / p.ckpt_stride;
-            }
-        }
-        float S[DVB];
-        {
-            const float* s0 = p.init_state ? p.init_state + ((static_cast<size_t>(n) * H + h) * dk + d) * dv + jb * DVB : nullptr;
-#pragma unroll
-            for (int j = 0; j < DVB; j += 4) {
-                float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (s0 && d < dk) v4 = *reinterpret_cast<const float4*>(s0 + j);
-                S[j] = v4.x; S[j + 1] = v4.y; S[j + 2] = v4.z; S[j + 3] = v4.w;
-            }
-        }
-        for (int c = 0; c < nchunks && ok; ++c) {
-            const int cs = t0 + c * C;
-            const int nv = min(C, len - c * C);
-            const int slot = c & 1;
-            // value row of this thread's token, fetched before waiting
-            uint4 vr[DVB / 8];
-#pragma unroll
-            for (int j = 0; j < DVB / 8; ++j) vr[j] = make_uint4(0u, 0u, 0u, 0u);
-            if (d < 64 && d < nv) {
-                const uint16_t* vp = p.v + static_cast<size_t>(cs + d) * vtok_stride + static_cast<size_t>(h) * dv + jb * DVB;
-#pragma unroll
-                for (int j = 0; j < DVB / 8; ++j) vr[j] = __ldg(reinterpret_cast<const uint4*>(vp) + j);
-            }
-            if (!group_wait(&mb[MB_READY], c & 1, BAR_CHAIN, NCHAIN)) { ok = false; break; }
-            // exp(g_C) of this chunk: read now, before the prep can reuse the slot (chunk c+2)
-            const float gc = s_egc[slot * 128 + d];
-
-            // -- 6. state as an MN-major f16 tile; D1 = [K~; Q~] S --
-#pragma unroll
-            for (int j = 0; j < DVB; j += 8) st_h8(Sb, d, j, 128, S + j);
-            tc::fence_smem_to_async();
-            group_sync_tc(BAR_CHAIN, NCHAIN);
-            if (d == 0) {
-                issue_mma<true>(tm + TM_D1, 128, DVB, DK, tc::smem_u32(AH), false, 128, tc::smem_u32(Sb), true, 128u * 128u);
-                tc::mma_commit(&mb[MB_CHAIN]);
-                tc::mma_commit(&mb[MB_AHFREE]);
-            }
-            if (!group_wait(&mb[MB_CHAIN], ph_chain & 1, BAR_CHAIN, NCHAIN)) { ok = false; break; }
-            ++ph_chain;
-
-            // -- 7. X = V - K~ S  (rows 0..63) --
-            if (d < 64) {
-                float r[32];
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    tmem_ld32(lane_base + TM_D1 + 32 * half, r);
-#pragma unroll
-                    for (int j = 0; j < 32; j += 8) {
-                        const uint4 w = vr[(32 * half + j) / 8];
-                        const float2 a0 = bf16x2_bits_to_f32(w.x), a1 = bf16x2_bits_to_f32(w.y);
-                        const float2 a2 = bf16x2_bits_to_f32(w.z), a3 = bf16x2_bits_to_f32(w.w);
-                        float x8[8] = {a0.x - r[j], a0.y - r[j + 1], a1.x - r[j + 2], a1.y - r[j + 3],
-                                       a2.x - r[j + 4], a2.y - r[j + 5], a3.x - r[j + 6], a3.y - r[j + 7]};
-                        st_h8(XU, d, 32 * half + j, 64, x8);
-                    }
-                }
-            }
-            tc::fence_smem_to_async();
-            group_sync_tc(BAR_CHAIN, NCHAIN);
-
-            // -- 8. D2 = [T; Mqk] X  (rows 0..63: U, rows 64..127: A U) --
-            if (d == 0) {
-                issue_mma<true>(tm + TM_D2, 128, DVB, C, tc::smem_u32(Qt), false, 128, tc::smem_u32(XU), true, 64u * 128u);
-                tc::mma_commit(&mb[MB_CHAIN]);
-                tc::mma_commit(&mb[MB_QTFREE]);
-            }
-            if (!group_wait(&mb[MB_CHAIN], ph_chain & 1, BAR_CHAIN, NCHAIN)) { ok = false; break; }
-            ++ph_chain;
-            if (d < 64) {                                    // U -> MN-major f16 tile (overwrites X)
-                float r[32];
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    tmem_ld32(lane_base + TM_D2 + 32 * half, r);
-#pragma unroll
-                    for (int j = 0; j < 32; j += 8) st_h8(XU, d, 32 * half + j, 64, r + j);
-                }
-            } else {                                         // O = Q~ S + A U
-                const int t = d - 64;
-                const size_t ob = static_cast<size_t>(cs + t) * vtok_stride + static_cast<size_t>(h) * dv + jb * DVB;
-#pragma unroll
-                for (int c16 = 0; c16 < DVB; c16 += 16) {
-                    float a[16], b[16];
-                    tc::tmem_ld16(lane_base + TM_D2 + c16, a);
-                    tc::tmem_ld16(lane_base + TM_D1 + c16, b);
-                    tc::tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) a[j] += b[j];
-                    if (t < nv) {
-                        if (p.out_f32) {
-                            float* op = reinterpret_cast<float*>(p.out) + ob + c16;
-#pragma unroll
-                            for (int j = 0; j < 16; j += 4)
-                                *reinterpret_cast<float4*>(op + j) = make_float4(a[j], a[j + 1], a[j + 2], a[j + 3]);
-                        } else {
-                            uint16_t* op = reinterpret_cast<uint16_t*>(p.out) + ob + c16;
-#pragma unroll
-                            for (int j = 0; j < 16; j += 8) {
-                                uint4 w;
-                                w.x = f32x2_to_bf16x2_bits(a[j], a[j + 1]);
-                                w.y = f32x2_to_bf16x2_bits(a[j + 2], a[j + 3]);
-                                w.z = f32x2_to_bf16x2_bits(a[j + 4], a[j + 5]);
-                                w.w = f32x2_to_bf16x2_bits(a[j + 6], a[j + 7]);
-                                *reinterpret_cast<uint4*>(op + j) = w;
-                            }
-                        }
-                    }
-                }
-            }
-            tc::fence_smem_to_async();
-            group_sync_tc(BAR_CHAIN, NCHAIN);
-
-            // -- 9. D3 = K^^T U  (K^ tile as an MN-major A: M = channel, K = token) --
-            if (d == 0) {
-                issue_mma<true>(tm + TM_D3, 128, DVB, C, tc::smem_u32(sm + OFF_KH + slot * 16384), true, 64u * 128u,
-                                tc::smem_u32(XU), true, 64u * 128u);
-                tc::mma_commit(&mb[MB_CHAIN]);
-                tc::mma_commit(&mb[slot ? MB_KHFREE1 : MB_KHFREE0]);
-            }
-            if (!group_wait(&mb[MB_CHAIN], ph_chain & 1, BAR_CHAIN, NCHAIN)) { ok = false; break; }
-            ++ph_chain;
-            {
-                float r[32];
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    tmem_ld32(lane_base + TM_D3 + 32 * half, r);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) S[32 * half + j] = gc * S[32 * half + j] + r[j];
-                }
-            }
-            // -- 10. prefix-cache checkpoint at stride multiples and at the sequence end --
-            if (p.ckpt && p.ckpt_stride > 0) {
-                const int done = c * C + nv;
-                if (done % p.ckpt_stride == 0 || done == len) {
-                    if (d < dk) {
-                        float* cp = p.ckpt + ((static_cast<size_t>(slot_ck) * H + h) * dk + d) * dv + jb * DVB;
-#pragma unroll
-                        for (int j = 0; j < DVB; j += 4)
-                            *reinterpret_cast<float4*>(cp + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-                    }
-                    ++slot_ck;
-                }
-            }
-        }
-        if (ok && p.final_state && d < dk) {
-            float* fp = p.final_state + ((static_cast<size_t>(n) * H + h) * dk + d) * dv + jb * DVB;
-#pragma unroll
-            for (int j = 0; j < DVB; j += 4)
-                *reinterpret_cast<float4*>(fp + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-        }
-        if (!ok && d == 0) set_status(p.status, kStatusTimeout);
-    }
-
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    if (warp == 0) tc::tmem_dealloc(tm, TM_COLS);
+    tc::cluster_sync();
+    if (rank == 0) chain_role(p, sm, n, h, t0, len);
+    else prep_role(p, sm, rank - 1, h, t0, len);
+    // no CTA leaves while a peer may still address its shared memory
+    tc::cluster_sync();
 }
 
 }  // namespace prefill
@@ -609,10 +696,22 @@ int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
     p.q = q; p.k = k; p.v = v; p.la = la; p.beta = beta; p.init_state = init_state;
     p.cu_seqlens = cu_seqlens; p.out = out; p.final_state = final_state; p.ckpt = ckpt;
     p.status = status; p.out_f32 = out_f32; p.ckpt_stride = ckpt_stride;
-    p.H = H; p.dk = Dk; p.dv = Dv; p.nvb = Dv / DVB;
-    const long long blocks = static_cast<long long>(num_seqs) * H * p.nvb;
-    if (blocks == 0) return 0;
-    kda_prefill_kernel<<<static_cast<unsigned>(blocks), NT, SMEM_BYTES, stream>>>(p);
+    p.H = H; p.dk = Dk; p.dv = Dv;
+    const long long clusters = static_cast<long long>(num_seqs) * H;
+    if (clusters == 0) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * CLUSTER), 1, 1);
+    cfg.blockDim = dim3(NT, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kda_prefill_kernel, p) != cudaSuccess) return -3;
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
