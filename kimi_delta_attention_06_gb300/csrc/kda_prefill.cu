@@ -35,9 +35,10 @@
 //     columns) and runs the sequential part -- X, U and O, the state update --
 //     as three dependent MMAs per chunk.
 //   * CTAs 1-3 (prep): chunk c is prepared by CTA 1 + c % 3.  Each builds
-//     [K~; Q~], K^, [T; Mqk] and exp(g_C) for its chunk in its own shared
-//     memory and ships them, as one contiguous bulk copy, into slot c % 2 of
-//     the chain CTA's shared memory (distributed shared memory).
+//     [K~; Q~], K^, [T; Mqk], the chunk's values V and exp(g_C) in its own
+//     shared memory and ships them, as one contiguous bulk copy, into slot
+//     c % 2 of the chain CTA's shared memory (distributed shared memory).  The
+//     chain therefore issues no global loads on its critical path.
 // Three chunks are being prepared while the chain consumes a fourth, so the
 // chain's dependent-MMA latency, not the preparation, sets the pace.
 // Hand-offs use mbarriers (remote arrivals, transaction-count completion); every
@@ -61,9 +62,10 @@ constexpr uint32_t BAR_ALL = 1;  // named barrier over the CTA's 256 threads
 constexpr uint32_t H_AH = 0;                 // [K~; Q~] f16, 128 rows x 128 K, K-major  (32 KB)
 constexpr uint32_t H_KH = 32768;             // K^ f16, 64 rows (token) x 128 (channel)  (16 KB)
 constexpr uint32_t H_QT = 49152;             // [T; Mqk] f16, 128 rows x 64 K, K-major   (16 KB)
-constexpr uint32_t H_EGC = 65536;            // exp(g_C), 128 f32                         (512 B)
-constexpr uint32_t H_BYTES = 65536 + 512;
-constexpr uint32_t H_STRIDE = 66560;         // slot pitch (1024-aligned)
+constexpr uint32_t H_V = 65536;              // V bf16, 64 rows (token) x 128, SW128 rows (16 KB)
+constexpr uint32_t H_EGC = 81920;            // exp(g_C), 128 f32                         (512 B)
+constexpr uint32_t H_BYTES = 81920 + 512;
+constexpr uint32_t H_STRIDE = 82944;         // slot pitch (1024-aligned)
 
 // Prep CTA shared memory.
 constexpr uint32_t P_A1 = 0;                 // [Km; Qm] tf32, 128 rows x 128 K, K-major  (64 KB)
@@ -194,6 +196,36 @@ __device__ __forceinline__ bool cta_wait(void* bar, uint32_t parity, bool cluste
     return all != 0;
 }
 
+// Global loads of one chunk's inputs for a prep thread: q, k, log_alpha for
+// tokens 8tg..8tg+7 x channels 4cg..4cg+3, and 32 value columns of token tid / 4.
+__device__ __forceinline__ void load_inputs(const Params& p, int c, int t0, int len, int h, int cg, int tg, bool ch_ok,
+                                            int tid, float4 (&g4)[8], uint2 (&q2)[8], uint2 (&k2)[8], uint4 (&v4)[4],
+                                            float& bt) {
+    const int cs = t0 + c * C;
+    const int nv = min(C, len - c * C);
+    const size_t tok_stride = static_cast<size_t>(p.H) * p.dk;
+    const size_t base = static_cast<size_t>(cs) * tok_stride + static_cast<size_t>(h) * p.dk + 4 * cg;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int t = 8 * tg + i;
+        if (t < nv && ch_ok) {
+            g4[i] = __ldg(reinterpret_cast<const float4*>(p.la + base + t * tok_stride));
+            q2[i] = __ldg(reinterpret_cast<const uint2*>(p.q + base + t * tok_stride));
+            k2[i] = __ldg(reinterpret_cast<const uint2*>(p.k + base + t * tok_stride));
+        } else {
+            g4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            q2[i] = make_uint2(0u, 0u);
+            k2[i] = make_uint2(0u, 0u);
+        }
+    }
+    const int tv = tid >> 2, cv = 32 * (tid & 3);
+    const bool vok = tv < nv && cv < p.dv;
+    const uint16_t* vp = p.v + (static_cast<size_t>(cs + tv) * p.H + h) * p.dv + cv;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v4[j] = vok ? __ldg(reinterpret_cast<const uint4*>(vp) + j) : make_uint4(0u, 0u, 0u, 0u);
+    bt = (tid < C && tid < nv) ? bf16_bits_to_f32(p.beta[static_cast<size_t>(cs + tid) * p.H + h]) : 0.f;
+}
+
 // ============================================================================
 // Prep CTA: prepares chunks c = pr, pr + 3, pr + 6, ... of one (sequence, head).
 // ============================================================================
@@ -215,8 +247,7 @@ __device__ void prep_role(const Params& p, uint8_t* sm, int pr, int h, int t0, i
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + P_TMEM);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int H = p.H, dk = p.dk;
-    const size_t tok_stride = static_cast<size_t>(H) * dk;
+    const int dk = p.dk;
     const int nchunks = (len + C - 1) / C;
 
     if (warp == 0) tc::tmem_alloc(s_tmem, TM_PREP_COLS);
@@ -232,31 +263,15 @@ __device__ void prep_role(const Params& p, uint8_t* sm, int pr, int h, int t0, i
     uint32_t ph_mma = 0, n_recv = 0, n_free = 0;
     bool ok = true;
     int kk = 0;                                         // index of this CTA's chunk
+    float4 g4[8];                                       // log_alpha, then cumulative log-decay
+    uint2 q2[8], k2[8];                                 // q, k (bf16 x 4)
+    uint4 v4[4];                                        // this thread's share of the V tile
+    float bt = 0.f;                                     // beta of token tid (tid < 64)
     for (int c = pr; c < nchunks; c += NPREP_CTAS, ++kk) {
-        const int cs = t0 + c * C;
         const int nv = min(C, len - c * C);
 
-        // -- 0. inputs of this chunk --
-        float4 g4[8];
-        uint2 q2[8], k2[8];
-        {
-            const size_t base = static_cast<size_t>(cs) * tok_stride + static_cast<size_t>(h) * dk + 4 * cg;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int t = 8 * tg + i;
-                if (t < nv && ch_ok) {
-                    g4[i] = __ldg(reinterpret_cast<const float4*>(p.la + base + t * tok_stride));
-                    q2[i] = __ldg(reinterpret_cast<const uint2*>(p.q + base + t * tok_stride));
-                    k2[i] = __ldg(reinterpret_cast<const uint2*>(p.k + base + t * tok_stride));
-                } else {
-                    g4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    q2[i] = make_uint2(0u, 0u);
-                    k2[i] = make_uint2(0u, 0u);
-                }
-            }
-        }
-        float bt = 0.f;
-        if (tid < C && tid < nv) bt = bf16_bits_to_f32(p.beta[static_cast<size_t>(cs + tid) * H + h]);
+        // -- 0. inputs of this chunk (the first chunk loads here; later ones were prefetched) --
+        if (kk == 0) load_inputs(p, c, t0, len, h, cg, tg, ch_ok, tid, g4, q2, k2, v4, bt);
         // -- 1a. cumulative log-decay inside each 8-token group --
         {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -286,6 +301,10 @@ __device__ void prep_role(const Params& p, uint8_t* sm, int pr, int h, int t0, i
             const float4 egc = f4ex2(f4mul(gc, L2));
             const float4 ecr = f4ex2(f4mul(make_float4(gc.x - gr.x, gc.y - gr.y, gc.z - gr.z, gc.w - gr.w), L2));
             if (tg == 0) *reinterpret_cast<float4*>(s_egc_out + 4 * cg) = egc;
+            // V: thread -> (token tid / 4, columns 32 (tid % 4) .. +31), bf16 kept exact
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4*>(OUT + H_V + tc::sw128_off16(tid >> 2, 32 * (tid & 3) + 8 * j, 64)) = v4[j];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int t = 8 * tg + i;
@@ -442,6 +461,8 @@ __device__ void prep_role(const Params& p, uint8_t* sm, int pr, int h, int t0, i
         }
         tc::fence_smem_to_async();
         cta_sync_tc();
+        // prefetch the next chunk of this CTA now: no proxy fence follows before it is used
+        if (c + NPREP_CTAS < nchunks) load_inputs(p, c + NPREP_CTAS, t0, len, h, cg, tg, ch_ok, tid, g4, q2, k2, v4, bt);
 
         // -- 6. hand the block to the chain CTA: slot c % 2, once that slot is free --
         if (c >= 2) {
@@ -510,15 +531,6 @@ __device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, i
         const int nv = min(C, len - c * C);
         const int s = c & 1;
         uint8_t* slot = sm + K_SLOT + s * H_STRIDE;
-        // value row of this thread's token (rows 0..63), fetched before waiting
-        uint4 vr[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) vr[j] = make_uint4(0u, 0u, 0u, 0u);
-        if (d < 64 && d < nv && col_ok) {
-            const uint16_t* vp = p.v + static_cast<size_t>(cs + d) * vtok_stride + static_cast<size_t>(h) * dv + 64 * wg;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) vr[j] = __ldg(reinterpret_cast<const uint4*>(vp) + j);
-        }
         if (!cta_wait(&mb[1 + s], (c >> 1) & 1, false)) { ok = false; break; }
         // the producer's staging block is free again
         if (tid == 0) tc::mbar_arrive_remote(tc::mapa(prep_recv, 1 + c % NPREP_CTAS));
@@ -545,7 +557,7 @@ __device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, i
                 tmem_ld32(lane_base + TM_D1 + cb + 32 * half, r);
 #pragma unroll
                 for (int j = 0; j < 32; j += 8) {
-                    const uint4 w = vr[(32 * half + j) / 8];
+                    const uint4 w = *reinterpret_cast<const uint4*>(slot + H_V + tc::sw128_off16(d, 64 * wg + 32 * half + j, 64));
                     const float2 a0 = bf16x2_bits_to_f32(w.x), a1 = bf16x2_bits_to_f32(w.y);
                     const float2 a2 = bf16x2_bits_to_f32(w.z), a3 = bf16x2_bits_to_f32(w.w);
                     float x8[8] = {a0.x - r[j], a0.y - r[j + 1], a1.x - r[j + 2], a1.y - r[j + 3],
@@ -605,7 +617,7 @@ __device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, i
                 }
             }
         }
-        tc::fence_smem_to_async();
+        if (d < 64) tc::fence_smem_to_async();      // only the U writers touched shared memory
         cta_sync_tc();
 
         // -- D3 = K^^T U  (K^ tile as an MN-major A: M = channel, K = token) --
