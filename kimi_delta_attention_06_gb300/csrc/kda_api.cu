@@ -13,7 +13,7 @@ int launch_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, const
                   int N, int H, int D, cudaStream_t stream);
 int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* la,
                    const uint16_t* beta, const float* init_state, const int32_t* cu_seqlens,
-                   int num_seqs, int H, int Dk, int Dv, void* out, int out_f32,
+                   int num_seqs, int total_tokens, int H, int Dk, int Dv, void* out, int out_f32,
                    float* final_state, float* ckpt, int ckpt_stride, int* status, cudaStream_t stream);
 }  // namespace kda
 
@@ -115,7 +115,7 @@ int kda_chunk_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     int* status = nullptr;
     int rc = device_setup(&status);
     if (rc != KDA_OK) return rc;
-    rc = kda::launch_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, num_seqs, H, Dk, Dv,
+    rc = kda::launch_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, num_seqs, total_tokens, H, Dk, Dv,
                              out, out_dtype == KDA_OUT_F32, final_state, ckpt_states, ckpt_stride,
                              status, static_cast<cudaStream_t>(stream));
     return rc == 0 ? KDA_OK : KDA_ERR_CUDA;

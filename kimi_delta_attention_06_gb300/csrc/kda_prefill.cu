@@ -14,12 +14,14 @@
 //   L    = strict_lower(diag(beta) Km Kb^T)        A = lower_incl(Qm Kb^T)
 //   T    = (I + L)^{-1} diag(beta)                  Mqk = A T
 //   K~   = k * exp(g_t)   Q~ = q * exp(g_t)   K^ = k * exp(g_C - g_t)
-//   X    = V - K~ S
-//   U    = T X,      O = Q~ S + Mqk X               (pseudo-values and outputs)
+//   W    = T K~           Q' = Q~ - Mqk K~                      (WY form)
+//   U    = T V - W S      O  = Mqk V + Q' S                     (pseudo-values, outputs)
 //   S'   = diag(exp(g_C)) S + K^^T U
 //
 // which is the token recurrence S_t = (I - b k k^T) Diag(a) S_{t-1} + b k v^T,
-// o_t = S_t^T q_t regrouped by chunk (U solves (I + L) U = diag(beta) X).
+// o_t = S_t^T q_t regrouped by chunk: U solves (I + L) U = diag(beta) (V - K~ S)
+// and O = Q~ S + A U.  Everything except W S, Q' S and K^^T U is independent of
+// the state and is prepared off the sequential path.
 // Products run as tcgen05 MMAs with fp32 accumulation in TMEM.  The two
 // intra-chunk products (Km Kb^T, Qm Kb^T) take tf32 operands: their factors
 // exp(+-(g_t - g_r)) span up to half a chunk of decay either way, which needs
@@ -32,13 +34,13 @@
 // Work decomposition: one thread-block cluster of 4 CTAs per (sequence, head).
 //   * CTA 0 (chain): owns the fp32 state (Dk x Dv, one row per thread, in
 //     registers for the whole sequence; two warpgroups split the value
-//     columns) and runs the sequential part -- X, U and O, the state update --
-//     as three dependent MMAs per chunk.
-//   * CTAs 1-3 (prep): chunk c is prepared by CTA 1 + c % 3.  Each builds
-//     [K~; Q~], K^, [T; Mqk], the chunk's values V and exp(g_C) in its own
-//     shared memory and ships them, as one contiguous bulk copy, into slot
-//     c % 2 of the chain CTA's shared memory (distributed shared memory).  The
-//     chain therefore issues no global loads on its critical path.
+//     columns) and runs the sequential part as two dependent MMA steps per
+//     chunk: [U; O] = [T; Mqk] V + [-W; Q'] S, then K^^T U for the update.
+//   * CTAs 1-3 (prep): chunk c is prepared by CTA 1 + c % 3.  Its inputs
+//     arrive by TMA; it builds [-W; Q'], K^, [T; Mqk], V (fp16) and exp(g_C)
+//     in its own shared memory and ships them, as one contiguous bulk copy,
+//     into slot c % 2 of the chain CTA's shared memory (distributed shared
+//     memory).  The chain issues no global loads on its critical path.
 // Three chunks are being prepared while the chain consumes a fourth, so the
 // chain's dependent-MMA latency, not the preparation, sets the pace.
 // Hand-offs use mbarriers (remote arrivals, transaction-count completion); every
@@ -46,6 +48,8 @@
 #include "common.cuh"
 #include "tc.cuh"
 #include <cuda_fp16.h>
+#include <cuda.h>
+#include <cstring>
 
 namespace kda {
 namespace prefill {
@@ -59,10 +63,10 @@ constexpr int LS = 68;          // row stride (floats) of the fp32 scratch matri
 constexpr uint32_t BAR_ALL = 1;  // named barrier over the CTA's 256 threads
 
 // Hand-off block: produced in a prep CTA, copied verbatim into a chain slot.
-constexpr uint32_t H_AH = 0;                 // [K~; Q~] f16, 128 rows x 128 K, K-major  (32 KB)
+constexpr uint32_t H_AH = 0;                 // [-W; Q'] f16 (built from [K~; Q~]), 128 rows x 128 K, K-major (32 KB)
 constexpr uint32_t H_KH = 32768;             // K^ f16, 64 rows (token) x 128 (channel)  (16 KB)
 constexpr uint32_t H_QT = 49152;             // [T; Mqk] f16, 128 rows x 64 K, K-major   (16 KB)
-constexpr uint32_t H_V = 65536;              // V bf16, 64 rows (token) x 128, SW128 rows (16 KB)
+constexpr uint32_t H_V = 65536;              // V f16, 64 rows (token) x 128 N, MN-major   (16 KB)
 constexpr uint32_t H_EGC = 81920;            // exp(g_C), 128 f32                         (512 B)
 constexpr uint32_t H_BYTES = 81920 + 512;
 constexpr uint32_t H_STRIDE = 82944;         // slot pitch (1024-aligned)
@@ -70,11 +74,16 @@ constexpr uint32_t H_STRIDE = 82944;         // slot pitch (1024-aligned)
 // Prep CTA shared memory.
 constexpr uint32_t P_A1 = 0;                 // [Km; Qm] tf32, 128 rows x 128 K, K-major  (64 KB)
 constexpr uint32_t P_B1 = 65536;             // Kb tf32, 64 rows x 128 K, K-major          (32 KB)
+// TMA staging of the next chunk's inputs, in the [Km; Qm] / Kb space while it is dead
+constexpr uint32_t ST_LA = P_A1;             // log_alpha f32 [64][dk]
+constexpr uint32_t ST_Q = P_A1 + 32768;      // q bf16 [64][dk]
+constexpr uint32_t ST_K = P_A1 + 49152;      // k bf16 [64][dk]
+constexpr uint32_t ST_V = P_B1;              // v bf16 [64][dv]
 constexpr uint32_t P_OUT = 98304;            // hand-off block                             (65 KB)
 constexpr uint32_t P_P = P_OUT + H_STRIDE;   // A f16, 64 rows x 64 K, K-major             (8 KB)
 constexpr uint32_t P_BETA = P_P + 8192;      // beta [64] f32
 constexpr uint32_t P_TOT = P_BETA + 256;     // token-group log-decay totals [8][128] f32
-constexpr uint32_t P_BAR = P_TOT + 4096;     // mbarriers: 0 mma, 1 recv, 2 free
+constexpr uint32_t P_BAR = P_TOT + 4096;     // mbarriers: 0 mma, 1 recv, 2 free, 3 tma
 constexpr uint32_t P_TMEM = P_BAR + 32;
 constexpr uint32_t P_END = P_TMEM + 16;
 // fp32 scratch of the inverse, aliased onto [Km; Qm] (dead once Km Kb^T is done)
@@ -86,7 +95,7 @@ static_assert(P_Y + 32 * 36 * 4 <= P_B1, "inverse scratch overflows its alias");
 // Chain CTA shared memory.
 constexpr uint32_t K_SLOT = 0;                       // 2 hand-off slots
 constexpr uint32_t K_S = 2 * H_STRIDE;               // S f16, 128 rows (channel) x 128 N, MN-major (32 KB)
-constexpr uint32_t K_XU = K_S + 32768;               // X then U f16, 64 rows (token) x 128 N, MN-major (16 KB)
+constexpr uint32_t K_XU = K_S + 32768;               // U f16, 64 rows (token) x 128 N, MN-major (16 KB)
 constexpr uint32_t K_BAR = K_XU + 16384;             // mbarriers: 0 mma, 1-2 full[slot]
 constexpr uint32_t K_TMEM = K_BAR + 32;
 constexpr uint32_t K_END = K_TMEM + 16;
@@ -95,10 +104,14 @@ constexpr uint32_t SMEM_BYTES = (P_END > K_END ? P_END : K_END) + 1024;   // + a
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // TMEM columns.
-constexpr uint32_t TM_G1 = 0, TM_M = 64, TM_PREP_COLS = 128;                 // prep CTA
-constexpr uint32_t TM_D1 = 0, TM_D2 = 128, TM_D3 = 256, TM_CHAIN_COLS = 512; // chain CTA
+constexpr uint32_t TM_G1 = 0, TM_M = 64, TM_W = 128, TM_PREP_COLS = 256;    // prep CTA
+constexpr uint32_t TM_D1 = 0, TM_D3 = 128, TM_CHAIN_COLS = 256;             // chain CTA
 
 constexpr float kLog2e = 1.4426950408889634f;
+
+struct TensorMaps {
+    CUtensorMap q, k, la, v;     // 2-D views [tokens, H * D]; box = one head x 64 tokens
+};
 
 struct Params {
     const uint16_t* q;
@@ -141,7 +154,7 @@ __device__ __forceinline__ void cta_sync_tc() {
 template <bool F16>
 __device__ __forceinline__ void issue_mma(uint32_t d_tmem, int M, int N, int K,
                                           uint32_t a_base, bool a_mn, uint32_t a_p,
-                                          uint32_t b_base, bool b_mn, uint32_t b_p) {
+                                          uint32_t b_base, bool b_mn, uint32_t b_p, bool acc = false) {
     constexpr uint32_t esz = F16 ? 2u : 4u, kstep = 32u / esz, eps = 128u / esz;
     const uint32_t id = tc::idesc(M, N, F16 ? tc::kFmtF16 : tc::kFmtTF32, a_mn, b_mn);
     for (uint32_t s = 0; s < static_cast<uint32_t>(K) / kstep; ++s) {
@@ -150,8 +163,9 @@ __device__ __forceinline__ void issue_mma(uint32_t d_tmem, int M, int N, int K,
                                  : tc::sdesc(a_base + (k0 / eps) * a_p * 128u + (k0 % eps) * esz, 16, 1024, tc::kSwizzle128B);
         const uint64_t db = b_mn ? tc::sdesc(b_base + k0 * 128u, b_p, 1024, tc::kSwizzle128B)
                                  : tc::sdesc(b_base + (k0 / eps) * b_p * 128u + (k0 % eps) * esz, 16, 1024, tc::kSwizzle128B);
-        if (F16) tc::mma_f16(d_tmem, da, db, id, s > 0 ? 1u : 0u);
-        else     tc::mma_tf32(d_tmem, da, db, id, s > 0 ? 1u : 0u);
+        const uint32_t accum = (acc || s > 0) ? 1u : 0u;
+        if (F16) tc::mma_f16(d_tmem, da, db, id, accum);
+        else     tc::mma_tf32(d_tmem, da, db, id, accum);
     }
 }
 
@@ -196,40 +210,23 @@ __device__ __forceinline__ bool cta_wait(void* bar, uint32_t parity, bool cluste
     return all != 0;
 }
 
-// Global loads of one chunk's inputs for a prep thread: q, k, log_alpha for
-// tokens 8tg..8tg+7 x channels 4cg..4cg+3, and 32 value columns of token tid / 4.
-__device__ __forceinline__ void load_inputs(const Params& p, int c, int t0, int len, int h, int cg, int tg, bool ch_ok,
-                                            int tid, float4 (&g4)[8], uint2 (&q2)[8], uint2 (&k2)[8], uint4 (&v4)[4],
-                                            float& bt) {
-    const int cs = t0 + c * C;
-    const int nv = min(C, len - c * C);
-    const size_t tok_stride = static_cast<size_t>(p.H) * p.dk;
-    const size_t base = static_cast<size_t>(cs) * tok_stride + static_cast<size_t>(h) * p.dk + 4 * cg;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int t = 8 * tg + i;
-        if (t < nv && ch_ok) {
-            g4[i] = __ldg(reinterpret_cast<const float4*>(p.la + base + t * tok_stride));
-            q2[i] = __ldg(reinterpret_cast<const uint2*>(p.q + base + t * tok_stride));
-            k2[i] = __ldg(reinterpret_cast<const uint2*>(p.k + base + t * tok_stride));
-        } else {
-            g4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            q2[i] = make_uint2(0u, 0u);
-            k2[i] = make_uint2(0u, 0u);
-        }
-    }
-    const int tv = tid >> 2, cv = 32 * (tid & 3);
-    const bool vok = tv < nv && cv < p.dv;
-    const uint16_t* vp = p.v + (static_cast<size_t>(cs + tv) * p.H + h) * p.dv + cv;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) v4[j] = vok ? __ldg(reinterpret_cast<const uint4*>(vp) + j) : make_uint4(0u, 0u, 0u, 0u);
-    bt = (tid < C && tid < nv) ? bf16_bits_to_f32(p.beta[static_cast<size_t>(cs + tid) * p.H + h]) : 0.f;
+// Issue the TMA loads of chunk c's inputs (q, k, log_alpha, v of one head) into the
+// staging area; completion is counted on `bar`.  One thread.
+__device__ __forceinline__ void issue_input_tma(const TensorMaps& tmaps, const Params& p, uint8_t* sm, int c,
+                                                int t0, int h, void* bar) {
+    const int y = t0 + c * C;
+    const uint32_t bytes = static_cast<uint32_t>(C * p.dk * (4 + 2 + 2) + C * p.dv * 2);
+    tc::mbar_arrive_expect_tx(bar, bytes);
+    tc::tma_load_2d(tc::smem_u32(sm + ST_LA), &tmaps.la, h * p.dk, y, bar);
+    tc::tma_load_2d(tc::smem_u32(sm + ST_Q), &tmaps.q, h * p.dk, y, bar);
+    tc::tma_load_2d(tc::smem_u32(sm + ST_K), &tmaps.k, h * p.dk, y, bar);
+    tc::tma_load_2d(tc::smem_u32(sm + ST_V), &tmaps.v, h * p.dv, y, bar);
 }
 
 // ============================================================================
 // Prep CTA: prepares chunks c = pr, pr + 3, pr + 6, ... of one (sequence, head).
 // ============================================================================
-__device__ void prep_role(const Params& p, uint8_t* sm, int pr, int h, int t0, int len) {
+__device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm, int pr, int h, int t0, int len) {
     uint8_t* A1 = sm + P_A1;
     uint8_t* B1 = sm + P_B1;
     uint8_t* OUT = sm + P_OUT;
@@ -243,11 +240,11 @@ __device__ void prep_role(const Params& p, uint8_t* sm, int pr, int h, int t0, i
     float* Ybuf = reinterpret_cast<float*>(sm + P_Y);
     float* s_beta = reinterpret_cast<float*>(sm + P_BETA);
     float* s_tot = reinterpret_cast<float*>(sm + P_TOT);
-    uint64_t* mb = reinterpret_cast<uint64_t*>(sm + P_BAR);    // 0: mma, 1: recv, 2: free
+    uint64_t* mb = reinterpret_cast<uint64_t*>(sm + P_BAR);    // 0: mma, 1: recv, 2: free, 3: tma
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + P_TMEM);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int dk = p.dk;
+    const int dk = p.dk, dv = p.dv;
     const int nchunks = (len + C - 1) / C;
 
     if (warp == 0) tc::tmem_alloc(s_tmem, TM_PREP_COLS);
@@ -260,18 +257,49 @@ __device__ void prep_role(const Params& p, uint8_t* sm, int pr, int h, int t0, i
 
     const int cg = tid & 31, tg = tid >> 5;             // channels 4cg..4cg+3, tokens 8tg..8tg+7
     const bool ch_ok = 4 * cg < dk;
+    // beta of token (tid - 128), fetched one chunk ahead by warps 4-5, which never
+    // issue a proxy fence while the load is in flight
+    auto load_beta = [&](int c) -> float {
+        const int t = tid - 128;
+        const int nvb = min(C, len - c * C);
+        return (t >= 0 && t < nvb) ? bf16_bits_to_f32(p.beta[static_cast<size_t>(t0 + c * C + t) * p.H + h]) : 0.f;
+    };
+    float bt = 0.f;
+    if (pr < nchunks) {
+        if (tid == 0) issue_input_tma(tmaps, p, sm, pr, t0, h, &mb[3]);
+        if (tid >= 128 && tid < 192) bt = load_beta(pr);
+    }
     uint32_t ph_mma = 0, n_recv = 0, n_free = 0;
     bool ok = true;
     int kk = 0;                                         // index of this CTA's chunk
-    float4 g4[8];                                       // log_alpha, then cumulative log-decay
-    uint2 q2[8], k2[8];                                 // q, k (bf16 x 4)
-    uint4 v4[4];                                        // this thread's share of the V tile
-    float bt = 0.f;                                     // beta of token tid (tid < 64)
     for (int c = pr; c < nchunks; c += NPREP_CTAS, ++kk) {
         const int nv = min(C, len - c * C);
 
-        // -- 0. inputs of this chunk (the first chunk loads here; later ones were prefetched) --
-        if (kk == 0) load_inputs(p, c, t0, len, h, cg, tg, ch_ok, tid, g4, q2, k2, v4, bt);
+        // -- 0. inputs of this chunk: staging (TMA) -> registers --
+        if (!cta_wait(&mb[3], kk & 1, false)) { ok = false; break; }
+        float4 g4[8];
+        uint2 q2[8], k2[8];
+        uint4 v4[4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int t = 8 * tg + i;
+            if (t < nv && ch_ok) {
+                g4[i] = *reinterpret_cast<const float4*>(sm + ST_LA + (t * dk + 4 * cg) * 4);
+                q2[i] = *reinterpret_cast<const uint2*>(sm + ST_Q + (t * dk + 4 * cg) * 2);
+                k2[i] = *reinterpret_cast<const uint2*>(sm + ST_K + (t * dk + 4 * cg) * 2);
+            } else {
+                g4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                q2[i] = make_uint2(0u, 0u);
+                k2[i] = make_uint2(0u, 0u);
+            }
+        }
+        {
+            const int tv = tid >> 2, cv = 32 * (tid & 3);
+            const bool vok = tv < nv && cv < dv;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                v4[j] = vok ? *reinterpret_cast<const uint4*>(sm + ST_V + (tv * dv + cv + 8 * j) * 2) : make_uint4(0u, 0u, 0u, 0u);
+        }
         // -- 1a. cumulative log-decay inside each 8-token group --
         {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -284,8 +312,8 @@ __device__ void prep_role(const Params& p, uint8_t* sm, int pr, int h, int t0, i
             if (!cta_wait(&mb[1], n_recv & 1, true)) { ok = false; break; }
             ++n_recv;
         }
-        tc::named_sync(BAR_ALL, NT);     // token-group totals visible
-        if (tid < C) s_beta[tid] = bt;
+        tc::named_sync(BAR_ALL, NT);     // totals visible; staging fully read
+        if (tid >= 128 && tid < 192) s_beta[tid - 128] = bt;
         // -- 1b. decay factors and operand tiles --
         {
             float4 off = make_float4(0.f, 0.f, 0.f, 0.f), gr = off, gc = off;
@@ -301,10 +329,16 @@ __device__ void prep_role(const Params& p, uint8_t* sm, int pr, int h, int t0, i
             const float4 egc = f4ex2(f4mul(gc, L2));
             const float4 ecr = f4ex2(f4mul(make_float4(gc.x - gr.x, gc.y - gr.y, gc.z - gr.z, gc.w - gr.w), L2));
             if (tg == 0) *reinterpret_cast<float4*>(s_egc_out + 4 * cg) = egc;
-            // V: thread -> (token tid / 4, columns 32 (tid % 4) .. +31), bf16 kept exact
+            {   // V as an fp16 MN-major tile: thread -> (token tid / 4, columns 32 (tid % 4) .. +31)
+                const int tv = tid >> 2, cv = 32 * (tid & 3);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                *reinterpret_cast<uint4*>(OUT + H_V + tc::sw128_off16(tid >> 2, 32 * (tid & 3) + 8 * j, 64)) = v4[j];
+                for (int j = 0; j < 4; ++j) {
+                    const float2 a0 = bf16x2_bits_to_f32(v4[j].x), a1 = bf16x2_bits_to_f32(v4[j].y);
+                    const float2 a2 = bf16x2_bits_to_f32(v4[j].z), a3 = bf16x2_bits_to_f32(v4[j].w);
+                    const float x8[8] = {a0.x, a0.y, a1.x, a1.y, a2.x, a2.y, a3.x, a3.y};
+                    st_h8(OUT + H_V, tv, cv + 8 * j, 64, x8);
+                }
+            }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int t = 8 * tg + i;
@@ -370,16 +404,16 @@ __device__ void prep_role(const Params& p, uint8_t* sm, int pr, int h, int t0, i
         if (tid < 64) {            // diagonal blocks, column-oriented forward substitution
             const int bb = tid >> 4, cc = tid & 15;
             const float* Lb = Lbuf + (16 * bb) * LS + 16 * bb;
-            float s[16];
+            float sv[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) s[r] = (r == cc) ? 1.f : 0.f;
+            for (int r = 0; r < 16; ++r) sv[r] = (r == cc) ? 1.f : 0.f;
 #pragma unroll
             for (int j = 0; j < 15; ++j) {
 #pragma unroll
-                for (int r = j + 1; r < 16; ++r) s[r] -= Lb[r * LS + j] * s[j];
+                for (int r = j + 1; r < 16; ++r) sv[r] -= Lb[r * LS + j] * sv[j];
             }
 #pragma unroll
-            for (int r = 0; r < 16; ++r) Tbuf[(16 * bb + r) * LS + 16 * bb + cc] = s[r];
+            for (int r = 0; r < 16; ++r) Tbuf[(16 * bb + r) * LS + 16 * bb + cc] = sv[r];
         }
         tc::named_sync(BAR_ALL, NT);
         {                         // 16 -> 32: blocks (1,0) and (3,2), 128 threads each
@@ -441,6 +475,8 @@ __device__ void prep_role(const Params& p, uint8_t* sm, int pr, int h, int t0, i
         }
         tc::fence_smem_to_async();
         cta_sync_tc();
+        // the [Km; Qm] / Kb space is dead until the next chunk: stage that chunk's inputs there
+        if (tid == 0 && c + NPREP_CTAS < nchunks) issue_input_tma(tmaps, p, sm, c + NPREP_CTAS, t0, h, &mb[3]);
 
         // -- 5. Mqk = A T  (f16, M = 64; T rows read as an MN-major B) --
         if (tid == 0) {
@@ -449,22 +485,62 @@ __device__ void prep_role(const Params& p, uint8_t* sm, int pr, int h, int t0, i
         }
         if (!cta_wait(&mb[0], ph_mma & 1, false)) { ok = false; break; }
         ++ph_mma;
-        {   // M = 64 layout: row r sits in TMEM lane 32 (r / 16) + r % 16
-            const int c0 = (warp >> 2) * 32;
+        if (warp < 4) {   // M = 64 layout: row r sits in TMEM lane 32 (r / 16) + r % 16
             float v[32];
-            tmem_ld32(lane_base + TM_M + c0, v);
-            if (lane < 16) {
-                const int r = (warp & 3) * 16 + lane;
 #pragma unroll
-                for (int i = 0; i < 32; i += 8) st_h8(Qt, 64 + r, c0 + i, 128, v + i);
+            for (int half = 0; half < 2; ++half) {
+                tmem_ld32(lane_base + TM_M + 32 * half, v);
+                if (lane < 16) {
+                    const int r = warp * 16 + lane;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) st_h8(Qt, 64 + r, 32 * half + i, 128, v + i);
+                }
+            }
+            tc::fence_smem_to_async();
+        }
+        cta_sync_tc();
+
+        // -- 6. WY form: [W; Mqk K~] = [T; Mqk] K~ (K~ rows of [K~; Q~] read as an MN-major B) --
+        if (tid == 0) {
+            issue_mma<true>(tm + TM_W, 128, DK, C, tc::smem_u32(Qt), false, 128, tc::smem_u32(AH), true, 128u * 128u);
+            tc::mma_commit(&mb[0]);
+        }
+        if (!cta_wait(&mb[0], ph_mma & 1, false)) { ok = false; break; }
+        ++ph_mma;
+        {   // rows 0..63: -W over K~; rows 64..127: Q' = Q~ - Mqk K~ in place (warps 4-7: columns 64..127)
+            const int r = (warp & 3) * 32 + lane;
+            const int c0 = (warp >> 2) * 64;
+            float v[32];
+#pragma unroll
+            for (int q4 = 0; q4 < 2; ++q4) {
+                tmem_ld32(lane_base + TM_W + c0 + 32 * q4, v);
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) {
+                    const int col = c0 + 32 * q4 + i;
+                    float x8[8];
+                    if (r < 64) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) x8[j] = -v[i + j];
+                    } else {
+                        const uint4 w = *reinterpret_cast<const uint4*>(AH + tc::sw128_off16(r, col, 128));
+                        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[j]));
+                            x8[2 * j] = f.x - v[i + 2 * j];
+                            x8[2 * j + 1] = f.y - v[i + 2 * j + 1];
+                        }
+                    }
+                    st_h8(AH, r, col, 128, x8);
+                }
             }
         }
         tc::fence_smem_to_async();
         cta_sync_tc();
-        // prefetch the next chunk of this CTA now: no proxy fence follows before it is used
-        if (c + NPREP_CTAS < nchunks) load_inputs(p, c + NPREP_CTAS, t0, len, h, cg, tg, ch_ok, tid, g4, q2, k2, v4, bt);
+        // next chunk's beta (warps 4-5): no proxy fence runs in these threads before it is used
+        if (c + NPREP_CTAS < nchunks && tid >= 128 && tid < 192) bt = load_beta(c + NPREP_CTAS);
 
-        // -- 6. hand the block to the chain CTA: slot c % 2, once that slot is free --
+        // -- 7. hand the block to the chain CTA: slot c % 2, once that slot is free --
         if (c >= 2) {
             if (!cta_wait(&mb[2], n_free & 1, true)) { ok = false; break; }
             ++n_free;
@@ -526,6 +602,17 @@ __device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, i
     const int Nmma = dv;                      // 64 or 128 value columns
     uint32_t ph_mma = 0;
     bool ok = true;
+    // 'received' signals go out as soon as a hand-off has landed (thread 0 polls the
+    // next slot between its other duties), so a producer can start on its next chunk
+    // without waiting for the chain to reach this one.
+    int received = 0;                         // chunks [0, received) acknowledged
+    auto ack_landed = [&](int upto) {
+        while (received < upto && received < nchunks &&
+               tc::mbar_test_wait(&mb[1 + (received & 1)], (received >> 1) & 1)) {
+            tc::mbar_arrive_remote_relaxed(tc::mapa(prep_recv, 1 + received % NPREP_CTAS));
+            ++received;
+        }
+    };
     for (int c = 0; c < nchunks; ++c) {
         const int cs = t0 + c * C;
         const int nv = min(C, len - c * C);
@@ -533,69 +620,50 @@ __device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, i
         uint8_t* slot = sm + K_SLOT + s * H_STRIDE;
         if (!cta_wait(&mb[1 + s], (c >> 1) & 1, false)) { ok = false; break; }
         // the producer's staging block is free again
-        if (tid == 0) tc::mbar_arrive_remote(tc::mapa(prep_recv, 1 + c % NPREP_CTAS));
+        if (tid == 0) ack_landed(c + 1);
         const float gc = reinterpret_cast<const float*>(slot + H_EGC)[d];
 
-        // -- state as an MN-major f16 tile; D1 = [K~; Q~] S --
+        // -- [U; O] = [T; Mqk] V + [-W; Q'] S  (one accumulator) --
 #pragma unroll
         for (int j = 0; j < 64; j += 8) st_h8(Sb, d, 64 * wg + j, 128, S + j);
         tc::fence_smem_to_async();
         cta_sync_tc();
         if (tid == 0) {
+            issue_mma<true>(tm + TM_D1, 128, Nmma, C, tc::smem_u32(slot + H_QT), false, 128,
+                            tc::smem_u32(slot + H_V), true, 64u * 128u);
             issue_mma<true>(tm + TM_D1, 128, Nmma, DK, tc::smem_u32(slot + H_AH), false, 128,
-                            tc::smem_u32(Sb), true, 128u * 128u);
+                            tc::smem_u32(Sb), true, 128u * 128u, true);
             tc::mma_commit(&mb[0]);
         }
         if (!cta_wait(&mb[0], ph_mma & 1, false)) { ok = false; break; }
         ++ph_mma;
-
-        // -- X = V - K~ S  (rows 0..63) --
-        if (d < 64) {
+        if (d < 64) {                                    // U -> MN-major f16 tile
             float r[32];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 tmem_ld32(lane_base + TM_D1 + cb + 32 * half, r);
 #pragma unroll
-                for (int j = 0; j < 32; j += 8) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(slot + H_V + tc::sw128_off16(d, 64 * wg + 32 * half + j, 64));
-                    const float2 a0 = bf16x2_bits_to_f32(w.x), a1 = bf16x2_bits_to_f32(w.y);
-                    const float2 a2 = bf16x2_bits_to_f32(w.z), a3 = bf16x2_bits_to_f32(w.w);
-                    float x8[8] = {a0.x - r[j], a0.y - r[j + 1], a1.x - r[j + 2], a1.y - r[j + 3],
-                                   a2.x - r[j + 4], a2.y - r[j + 5], a3.x - r[j + 6], a3.y - r[j + 7]};
-                    st_h8(XU, d, 64 * wg + 32 * half + j, 64, x8);
-                }
-            }
-        }
-        tc::fence_smem_to_async();
-        cta_sync_tc();
-
-        // -- D2 = [T; Mqk] X  (rows 0..63: U, rows 64..127: A U) --
-        if (tid == 0) {
-            issue_mma<true>(tm + TM_D2, 128, Nmma, C, tc::smem_u32(slot + H_QT), false, 128,
-                            tc::smem_u32(XU), true, 64u * 128u);
-            tc::mma_commit(&mb[0]);
-        }
-        if (!cta_wait(&mb[0], ph_mma & 1, false)) { ok = false; break; }
-        ++ph_mma;
-        if (d < 64) {                                    // U -> MN-major f16 tile (overwrites X)
-            float r[32];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                tmem_ld32(lane_base + TM_D2 + cb + 32 * half, r);
-#pragma unroll
                 for (int j = 0; j < 32; j += 8) st_h8(XU, d, 64 * wg + 32 * half + j, 64, r + j);
             }
-        } else {                                         // O = Q~ S + A U
+            tc::fence_smem_to_async();                   // only the U writers touched shared memory
+        }
+        cta_sync_tc();
+
+        // -- D3 = K^^T U  (K^ tile as an MN-major A: M = channel, K = token) --
+        if (tid == 0) {
+            issue_mma<true>(tm + TM_D3, 128, Nmma, C, tc::smem_u32(slot + H_KH), true, 64u * 128u,
+                            tc::smem_u32(XU), true, 64u * 128u);
+            tc::mma_commit(&mb[0]);
+            ack_landed(c + 2);
+        }
+        if (d >= 64) {                                   // O rows to global memory while D3 runs
             const int t = d - 64;
             const size_t ob = static_cast<size_t>(cs + t) * vtok_stride + static_cast<size_t>(h) * dv + 64 * wg;
 #pragma unroll
             for (int c16 = 0; c16 < 64; c16 += 16) {
-                float a[16], b[16];
-                tc::tmem_ld16(lane_base + TM_D2 + cb + c16, a);
-                tc::tmem_ld16(lane_base + TM_D1 + cb + c16, b);
+                float a[16];
+                tc::tmem_ld16(lane_base + TM_D1 + cb + c16, a);
                 tc::tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) a[j] += b[j];
                 if (t < nv && col_ok) {
                     if (p.out_f32) {
                         float* op = reinterpret_cast<float*>(p.out) + ob + c16;
@@ -617,19 +685,10 @@ __device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, i
                 }
             }
         }
-        if (d < 64) tc::fence_smem_to_async();      // only the U writers touched shared memory
-        cta_sync_tc();
-
-        // -- D3 = K^^T U  (K^ tile as an MN-major A: M = channel, K = token) --
-        if (tid == 0) {
-            issue_mma<true>(tm + TM_D3, 128, Nmma, C, tc::smem_u32(slot + H_KH), true, 64u * 128u,
-                            tc::smem_u32(XU), true, 64u * 128u);
-            tc::mma_commit(&mb[0]);
-        }
         if (!cta_wait(&mb[0], ph_mma & 1, false)) { ok = false; break; }
         ++ph_mma;
         // slot s is free: the producer of chunk c + 2 may overwrite it
-        if (tid == 0 && c + 2 < nchunks) tc::mbar_arrive_remote(tc::mapa(prep_free, 1 + (c + 2) % NPREP_CTAS));
+        if (tid == 0 && c + 2 < nchunks) tc::mbar_arrive_remote_relaxed(tc::mapa(prep_free, 1 + (c + 2) % NPREP_CTAS));
         {
             float r[32];
 #pragma unroll
@@ -664,7 +723,7 @@ __device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, i
     if (warp == 0) tc::tmem_dealloc(tm, TM_CHAIN_COLS);
 }
 
-__global__ void __launch_bounds__(NT, 1) kda_prefill_kernel(const Params p)
+__global__ void __launch_bounds__(NT, 1) kda_prefill_kernel(const Params p, const __grid_constant__ TensorMaps tmaps)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -678,23 +737,54 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_kernel(const Params p)
     // every CTA initialises its barriers before any peer can touch them
     if (threadIdx.x == 0) {
         uint64_t* mb = reinterpret_cast<uint64_t*>(sm + (rank == 0 ? K_BAR : P_BAR));
-        tc::mbar_init(&mb[0], 1);
-        tc::mbar_init(&mb[1], 1);
-        tc::mbar_init(&mb[2], 1);
+        for (int i = 0; i < 4; ++i) tc::mbar_init(&mb[i], 1);
         tc::mbar_fence_init();
     }
     tc::cluster_sync();
     if (rank == 0) chain_role(p, sm, n, h, t0, len);
-    else prep_role(p, sm, rank - 1, h, t0, len);
+    else prep_role(p, tmaps, sm, rank - 1, h, t0, len);
     // no CTA leaves while a peer may still address its shared memory
     tc::cluster_sync();
 }
 
 }  // namespace prefill
 
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 2-D map over a [rows, cols] row-major tensor; box = box_cols x 64 rows, no swizzle.
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esz, long long rows, long long cols, int box_cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * esz};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), 64u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* la,
                    const uint16_t* beta, const float* init_state, const int32_t* cu_seqlens,
-                   int num_seqs, int H, int Dk, int Dv, void* out, int out_f32,
+                   int num_seqs, int total_tokens, int H, int Dk, int Dv, void* out, int out_f32,
                    float* final_state, float* ckpt, int ckpt_stride, int* status, cudaStream_t stream)
 {
     using namespace prefill;
@@ -710,7 +800,20 @@ int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
     p.status = status; p.out_f32 = out_f32; p.ckpt_stride = ckpt_stride;
     p.H = H; p.dk = Dk; p.dv = Dv;
     const long long clusters = static_cast<long long>(num_seqs) * H;
-    if (clusters == 0) return 0;
+    if (clusters == 0 || total_tokens == 0) {
+        // nothing to stream; empty sequences still hand back their initial states
+        if (clusters == 0) return 0;
+    }
+    TensorMaps tmaps;
+    if (total_tokens > 0) {
+        if (!make_map(&tmaps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, total_tokens, static_cast<long long>(H) * Dk, Dk) ||
+            !make_map(&tmaps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, total_tokens, static_cast<long long>(H) * Dk, Dk) ||
+            !make_map(&tmaps.la, la, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, total_tokens, static_cast<long long>(H) * Dk, Dk) ||
+            !make_map(&tmaps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, total_tokens, static_cast<long long>(H) * Dv, Dv))
+            return -3;
+    } else {
+        memset(&tmaps, 0, sizeof(tmaps));     // never dereferenced: no sequence has a chunk
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * CLUSTER), 1, 1);
     cfg.blockDim = dim3(NT, 1, 1);
@@ -723,7 +826,7 @@ int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kda_prefill_kernel, p) != cudaSuccess) return -3;
+    if (cudaLaunchKernelEx(&cfg, kda_prefill_kernel, p, tmaps) != cudaSuccess) return -3;
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

@@ -244,3 +244,44 @@ __device__ __forceinline__ uint32_t mbar_wait_cluster_bounded(void* bar, uint32_
 
 }  // namespace tc
 }  // namespace kda
+
+namespace kda {
+namespace tc {
+
+// ---- TMA (tensor bulk copies) ------------------------------------------------------------
+__device__ __forceinline__ void mbar_arrive_expect_tx(void* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+// 2-D tiled TMA load of the box at coordinates (x, y) into this CTA's shared memory;
+// completion is reported as transaction bytes on `bar`.  x * element size must be a
+// multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst_smem, const void* tmap, int x, int y, void* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(dst_smem), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
+}
+
+}  // namespace tc
+}  // namespace kda
+
+namespace kda {
+namespace tc {
+
+// Relaxed remote arrival: a pure signal, ordering no memory accesses of this thread.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" :: "r"(cluster_addr) : "memory");
+}
+// Non-blocking probe of an mbarrier phase.
+__device__ __forceinline__ uint32_t mbar_test_wait(void* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok;
+}
+
+}  // namespace tc
+}  // namespace kda
