@@ -59,7 +59,6 @@ constexpr int DK = 128;         // internal key dim (Dk = 64 is zero-padded)
 constexpr int NT = 256;         // threads per CTA
 constexpr int NPREP_CTAS = 3;   // prep CTAs per cluster
 constexpr int CLUSTER = 1 + NPREP_CTAS;
-constexpr int LS = 68;          // row stride (floats) of the fp32 scratch matrices
 constexpr uint32_t BAR_ALL = 1;  // named barrier over the CTA's 256 threads
 
 // Hand-off block: produced in a prep CTA, copied verbatim into a chain slot.
@@ -86,11 +85,13 @@ constexpr uint32_t P_TOT = P_BETA + 256;     // token-group log-decay totals [8]
 constexpr uint32_t P_BAR = P_TOT + 4096;     // mbarriers: 0 mma, 1 recv, 2 free, 3 tma
 constexpr uint32_t P_TMEM = P_BAR + 32;
 constexpr uint32_t P_END = P_TMEM + 16;
-// fp32 scratch of the inverse, aliased onto [Km; Qm] (dead once Km Kb^T is done)
-constexpr uint32_t P_L = P_A1;
-constexpr uint32_t P_T = P_L + 64 * LS * 4;
-constexpr uint32_t P_Y = P_T + 64 * LS * 4;  // 32 x 36 (also 2 x 16 x 20)
-static_assert(P_Y + 32 * 36 * 4 <= P_B1, "inverse scratch overflows its alias");
+// fp16 scratch of the inverse (row pitch LH halves), aliased onto [Km; Qm] (dead once
+// Km Kb^T is done)
+constexpr int LH = 72;
+constexpr uint32_t P_L = P_A1;                       // L  [64][LH]
+constexpr uint32_t P_T = P_L + 64 * LH * 2;          // T  [64][LH]
+constexpr uint32_t P_Y = P_T + 64 * LH * 2;          // Y  [32][LH] (also 2 x [16][LH])
+static_assert(P_Y + 32 * LH * 2 <= P_B1, "inverse scratch overflows its alias");
 
 // Chain CTA shared memory.
 constexpr uint32_t K_SLOT = 0;                       // 2 hand-off slots
@@ -201,6 +202,33 @@ __device__ __forceinline__ float4 bf16x4_to_f4(uint2 w) {
     return make_float4(a.x, a.y, b.x, b.y);
 }
 
+// ---- warp-level MMA for the small products of the triangular inverse ----------------
+// m16n8k16, fp16 inputs, fp32 accumulate.  Fragments come from row-major fp16 tiles
+// through ldmatrix (A: 16 x 16 at (r0, c0); B: 16 (k) x 8 (n) at (k0, n0), transposed).
+__device__ __forceinline__ void ldsm_a(const __half* base, int pitch, int r0, int c0, uint32_t (&a)[4]) {
+    const int l = threadIdx.x & 31, mi = l >> 3, ri = l & 7;
+    const __half* ptr = base + (r0 + ri + 8 * (mi & 1)) * pitch + c0 + 8 * (mi >> 1);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]) : "r"(tc::smem_u32(ptr)));
+}
+__device__ __forceinline__ void ldsm_b(const __half* base, int pitch, int k0, int n0, uint32_t (&b)[2]) {
+    const int l = threadIdx.x & 31, mi = (l >> 3) & 1, ri = l & 7;
+    const __half* ptr = base + (k0 + 8 * mi + ri) * pitch + n0;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(b[0]), "=r"(b[1]) : "r"(tc::smem_u32(ptr)));
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// Store a 16 x 8 fp32 accumulator fragment, scaled by `sc`, as fp16 at (r0, n0) of a row-major tile.
+__device__ __forceinline__ void st_frag(__half* base, int pitch, int r0, int n0, const float (&d)[4], float sc) {
+    const int l = threadIdx.x & 31, g = l >> 2, t = l & 3;
+    *reinterpret_cast<__half2*>(base + (r0 + g) * pitch + n0 + 2 * t) = __floats2half2_rn(sc * d[0], sc * d[1]);
+    *reinterpret_cast<__half2*>(base + (r0 + g + 8) * pitch + n0 + 2 * t) = __floats2half2_rn(sc * d[2], sc * d[3]);
+}
+
 // Bounded wait on an mbarrier phase, agreed by all threads of the CTA.
 __device__ __forceinline__ bool cta_wait(void* bar, uint32_t parity, bool cluster_scope) {
     const uint32_t ok = cluster_scope ? tc::mbar_wait_cluster_bounded(bar, parity, kWaitLimitNs)
@@ -235,9 +263,9 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
     uint8_t* Qt = OUT + H_QT;
     float* s_egc_out = reinterpret_cast<float*>(OUT + H_EGC);
     uint8_t* P = sm + P_P;
-    float* Lbuf = reinterpret_cast<float*>(sm + P_L);
-    float* Tbuf = reinterpret_cast<float*>(sm + P_T);
-    float* Ybuf = reinterpret_cast<float*>(sm + P_Y);
+    __half* Lh = reinterpret_cast<__half*>(sm + P_L);
+    __half* Th = reinterpret_cast<__half*>(sm + P_T);
+    __half* Yh = reinterpret_cast<__half*>(sm + P_Y);
     float* s_beta = reinterpret_cast<float*>(sm + P_BETA);
     float* s_tot = reinterpret_cast<float*>(sm + P_TOT);
     uint64_t* mb = reinterpret_cast<uint64_t*>(sm + P_BAR);    // 0: mma, 1: recv, 2: free, 3: tma
@@ -376,15 +404,15 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             tmem_ld32(lane_base + TM_G1 + c0, v);
             if (r < 64) {
                 const float b = s_beta[r];
-                float* Lr = Lbuf + r * LS + c0;
+                __half* Lr = Lh + r * LH + c0;
 #pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    float4 w;
-                    w.x = (c0 + i + 0 < r) ? b * v[i + 0] : 0.f;
-                    w.y = (c0 + i + 1 < r) ? b * v[i + 1] : 0.f;
-                    w.z = (c0 + i + 2 < r) ? b * v[i + 2] : 0.f;
-                    w.w = (c0 + i + 3 < r) ? b * v[i + 3] : 0.f;
-                    *reinterpret_cast<float4*>(Lr + i) = w;
+                for (int i = 0; i < 32; i += 8) {
+                    uint4 w;
+                    w.x = f16x2_bits((c0 + i + 0 < r) ? b * v[i + 0] : 0.f, (c0 + i + 1 < r) ? b * v[i + 1] : 0.f);
+                    w.y = f16x2_bits((c0 + i + 2 < r) ? b * v[i + 2] : 0.f, (c0 + i + 3 < r) ? b * v[i + 3] : 0.f);
+                    w.z = f16x2_bits((c0 + i + 4 < r) ? b * v[i + 4] : 0.f, (c0 + i + 5 < r) ? b * v[i + 5] : 0.f);
+                    w.w = f16x2_bits((c0 + i + 6 < r) ? b * v[i + 6] : 0.f, (c0 + i + 7 < r) ? b * v[i + 7] : 0.f);
+                    *reinterpret_cast<uint4*>(Lr + i) = w;
                 }
             } else {
                 const int t = r - 64;
@@ -397,79 +425,76 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         cta_sync_tc();
 
         // -- 4. T = (I + L)^{-1} by recursive doubling over 16 x 16 blocks --
-        //    blocks [[A, 0], [B, D]]^{-1} = [[A^-1, 0], [-D^-1 B A^-1, D^-1]]
-        for (int i = tid; i < 64 * LS / 4; i += NT)
-            reinterpret_cast<float4*>(Tbuf)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        //    blocks [[A, 0], [B, D]]^{-1} = [[A^-1, 0], [-D^-1 B A^-1, D^-1]]; the block
+        //    products run on warp-level tensor-core MMAs (fp16 in, fp32 accumulate)
+        for (int i = tid; i < 64 * LH / 8; i += NT)
+            reinterpret_cast<uint4*>(Th)[i] = make_uint4(0u, 0u, 0u, 0u);
         tc::named_sync(BAR_ALL, NT);
-        if (tid < 64) {            // diagonal blocks, column-oriented forward substitution
+        if (tid < 64) {            // diagonal blocks, column-oriented forward substitution (fp32)
             const int bb = tid >> 4, cc = tid & 15;
-            const float* Lb = Lbuf + (16 * bb) * LS + 16 * bb;
+            const __half* Lb = Lh + (16 * bb) * LH + 16 * bb;
             float sv[16];
 #pragma unroll
             for (int r = 0; r < 16; ++r) sv[r] = (r == cc) ? 1.f : 0.f;
 #pragma unroll
             for (int j = 0; j < 15; ++j) {
 #pragma unroll
-                for (int r = j + 1; r < 16; ++r) sv[r] -= Lb[r * LS + j] * sv[j];
+                for (int r = j + 1; r < 16; ++r) sv[r] -= __half2float(Lb[r * LH + j]) * sv[j];
             }
 #pragma unroll
-            for (int r = 0; r < 16; ++r) Tbuf[(16 * bb + r) * LS + 16 * bb + cc] = sv[r];
+            for (int r = 0; r < 16; ++r) Th[(16 * bb + r) * LH + 16 * bb + cc] = __float2half_rn(sv[r]);
         }
         tc::named_sync(BAR_ALL, NT);
-        {                         // 16 -> 32: blocks (1,0) and (3,2), 128 threads each
-            const int pp = tid >> 7, q7 = tid & 127;
-            const int r = q7 >> 3, c2 = (q7 & 7) * 2;
-            const int R = 16 * (2 * pp + 1), Cc = 16 * (2 * pp);
-            const float* Lr = Lbuf + (R + r) * LS + Cc;
-            float y0 = 0.f, y1 = 0.f;
+        if (warp < 2) {           // 16 -> 32: warp 0 merges blocks (1,0), warp 1 blocks (3,2)
+            const int R = 16 * (2 * warp + 1), Cc = 16 * (2 * warp);
+            __half* Yw = Yh + warp * 16 * LH;
+            uint32_t a[4], b[2];
+            ldsm_a(Lh, LH, R, Cc, a);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float l = Lr[k];
-                const float2 tk = *reinterpret_cast<const float2*>(Tbuf + (Cc + k) * LS + Cc + c2);
-                y0 += l * tk.x; y1 += l * tk.y;
+            for (int nt = 0; nt < 2; ++nt) {              // Y = L_DA T_AA
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                ldsm_b(Th, LH, Cc, Cc + 8 * nt, b);
+                mma16816(acc, a, b);
+                st_frag(Yw, LH, 0, 8 * nt, acc, 1.f);
             }
-            *reinterpret_cast<float2*>(Ybuf + pp * 16 * 20 + r * 20 + c2) = make_float2(y0, y1);
-            tc::named_sync(BAR_ALL, NT);
-            const float* Tr = Tbuf + (R + r) * LS + R;
-            const float* Yp = Ybuf + pp * 16 * 20;
-            float z0 = 0.f, z1 = 0.f;
+            __syncwarp();
+            ldsm_a(Th, LH, R, R, a);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float t = Tr[k];
-                const float2 yk = *reinterpret_cast<const float2*>(Yp + k * 20 + c2);
-                z0 += t * yk.x; z1 += t * yk.y;
+            for (int nt = 0; nt < 2; ++nt) {              // T_DA = -T_DD Y
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                ldsm_b(Yw, LH, 0, 8 * nt, b);
+                mma16816(acc, a, b);
+                st_frag(Th, LH, R, Cc + 8 * nt, acc, -1.f);
             }
-            *reinterpret_cast<float2*>(Tbuf + (R + r) * LS + Cc + c2) = make_float2(-z0, -z1);
         }
         tc::named_sync(BAR_ALL, NT);
-        {                         // 32 -> 64: block (1,0) of 32 x 32 blocks
-            const int r = tid >> 3, c4 = (tid & 7) * 4;
-            const float* Lr = Lbuf + (32 + r) * LS;
-            float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-            for (int k = 0; k < 32; ++k) {
-                const float l = Lr[k];
-                const float4 tk = *reinterpret_cast<const float4*>(Tbuf + k * LS + c4);
-                y.x += l * tk.x; y.y += l * tk.y; y.z += l * tk.z; y.w += l * tk.w;
+        {                         // 32 -> 64: warp -> 16 x 8 tile (m = warp / 4, n = warp % 4)
+            const int m = warp >> 2, nn = warp & 3;
+            uint32_t a[4], b[2];
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {              // Y = L[32:64, 0:32] T[0:32, 0:32]
+                ldsm_a(Lh, LH, 32 + 16 * m, 16 * ks, a);
+                ldsm_b(Th, LH, 16 * ks, 8 * nn, b);
+                mma16816(acc, a, b);
             }
-            *reinterpret_cast<float4*>(Ybuf + r * 36 + c4) = y;
+            st_frag(Yh, LH, 16 * m, 8 * nn, acc, 1.f);
             tc::named_sync(BAR_ALL, NT);
-            const float* Tr = Tbuf + (32 + r) * LS + 32;
-            float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-            for (int k = 0; k < 32; ++k) {
-                const float t = Tr[k];
-                const float4 yk = *reinterpret_cast<const float4*>(Ybuf + k * 36 + c4);
-                z.x += t * yk.x; z.y += t * yk.y; z.z += t * yk.z; z.w += t * yk.w;
+            float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {              // T[32:64, 0:32] = -T[32:64, 32:64] Y
+                ldsm_a(Th, LH, 32 + 16 * m, 32 + 16 * ks, a);
+                ldsm_b(Yh, LH, 16 * ks, 8 * nn, b);
+                mma16816(acc2, a, b);
             }
-            *reinterpret_cast<float4*>(Tbuf + (32 + r) * LS + c4) = make_float4(-z.x, -z.y, -z.z, -z.w);
+            st_frag(Th, LH, 32 + 16 * m, 8 * nn, acc2, -1.f);
         }
         tc::named_sync(BAR_ALL, NT);
         {   // T diag(beta) -> rows 0..63 of [T; Mqk]: thread -> (row, 16 columns)
             const int t = tid >> 2, c0 = (tid & 3) * 16;
             float tb[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) tb[i] = Tbuf[t * LS + c0 + i] * s_beta[c0 + i];
+            for (int i = 0; i < 16; ++i) tb[i] = __half2float(Th[t * LH + c0 + i]) * s_beta[c0 + i];
             st_h8(Qt, t, c0, 128, tb);
             st_h8(Qt, t, c0 + 8, 128, tb + 8);
         }
