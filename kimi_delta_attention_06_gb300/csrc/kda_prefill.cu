@@ -68,12 +68,13 @@ constexpr uint32_t H_QT = 49152;             // [T; Mqk] f16, 128 rows x 64 K, K
 constexpr uint32_t H_V = 65536;              // V f16, 64 rows (token) x 128 N, MN-major   (16 KB)
 constexpr uint32_t H_EGC = 81920;            // exp(g_C), 128 f32                         (512 B)
 constexpr uint32_t H_BYTES = 81920 + 512;
+static_assert(H_BYTES % (8 * 16) == 0, "hand-off splits into 8 16-byte-multiple parts");
 constexpr uint32_t H_STRIDE = 82944;         // slot pitch (1024-aligned)
 
 // Prep CTA shared memory.
 constexpr uint32_t P_A1 = 0;                 // [Km; Qm] tf32, 128 rows x 128 K, K-major  (64 KB)
 constexpr uint32_t P_B1 = 65536;             // Kb tf32, 64 rows x 128 K, K-major          (32 KB)
-// TMA staging of the next chunk's inputs, in the [Km; Qm] / Kb space while it is dead
+// TMA staging of the next chunk's inputs, in the [Km; Qm] / Kb space once Km Kb^T is done
 constexpr uint32_t ST_LA = P_A1;             // log_alpha f32 [64][dk]
 constexpr uint32_t ST_Q = P_A1 + 32768;      // q bf16 [64][dk]
 constexpr uint32_t ST_K = P_A1 + 49152;      // k bf16 [64][dk]
@@ -84,14 +85,12 @@ constexpr uint32_t P_BETA = P_P + 8192;      // beta [64] f32
 constexpr uint32_t P_TOT = P_BETA + 256;     // token-group log-decay totals [8][128] f32
 constexpr uint32_t P_BAR = P_TOT + 4096;     // mbarriers: 0 mma, 1 recv, 2 free, 3 tma
 constexpr uint32_t P_TMEM = P_BAR + 32;
-constexpr uint32_t P_END = P_TMEM + 16;
-// fp16 scratch of the inverse (row pitch LH halves), aliased onto [Km; Qm] (dead once
-// Km Kb^T is done)
+// fp16 scratch of the inverse (row pitch LH halves)
 constexpr int LH = 72;
-constexpr uint32_t P_L = P_A1;                       // L  [64][LH]
+constexpr uint32_t P_L = P_TMEM + 32;                // L  [64][LH]
 constexpr uint32_t P_T = P_L + 64 * LH * 2;          // T  [64][LH]
 constexpr uint32_t P_Y = P_T + 64 * LH * 2;          // Y  [32][LH] (also 2 x [16][LH])
-static_assert(P_Y + 32 * LH * 2 <= P_B1, "inverse scratch overflows its alias");
+constexpr uint32_t P_END = P_Y + 32 * LH * 2;
 
 // Chain CTA shared memory.
 constexpr uint32_t K_SLOT = 0;                       // 2 hand-off slots
@@ -395,6 +394,8 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         }
         if (!cta_wait(&mb[0], ph_mma & 1, false)) { ok = false; break; }
         ++ph_mma;
+        // [Km; Qm] and Kb are dead until the next chunk: stage that chunk's inputs there
+        if (tid == 0 && c + NPREP_CTAS < nchunks) issue_input_tma(tmaps, p, sm, c + NPREP_CTAS, t0, h, &mb[3]);
 
         // -- 3. L (rows 0..63 -> fp32 scratch), A (rows 64..127 -> f16 tile) --
         {
@@ -500,8 +501,6 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         }
         tc::fence_smem_to_async();
         cta_sync_tc();
-        // the [Km; Qm] / Kb space is dead until the next chunk: stage that chunk's inputs there
-        if (tid == 0 && c + NPREP_CTAS < nchunks) issue_input_tma(tmaps, p, sm, c + NPREP_CTAS, t0, h, &mb[3]);
 
         // -- 5. Mqk = A T  (f16, M = 64; T rows read as an MN-major B) --
         if (tid == 0) {
@@ -570,10 +569,14 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             if (!cta_wait(&mb[2], n_free & 1, true)) { ok = false; break; }
             ++n_free;
         }
-        if (tid == 0) {
+        {   // 8 concurrent bulk copies of H_BYTES / 8 each, one per warp
             const uint32_t s = static_cast<uint32_t>(c & 1);
-            tc::mbar_arrive_expect_tx_remote(chain_full0 + 8u * s, H_BYTES);
-            tc::bulk_copy_s2cluster(chain_slot0 + s * H_STRIDE, tc::smem_u32(OUT), H_BYTES, chain_full0 + 8u * s);
+            if (tid == 0) tc::mbar_arrive_expect_tx_remote(chain_full0 + 8u * s, H_BYTES);
+            if (lane == 0) {
+                constexpr uint32_t part = H_BYTES / 8;
+                tc::bulk_copy_s2cluster(chain_slot0 + s * H_STRIDE + warp * part, tc::smem_u32(OUT) + warp * part, part,
+                                        chain_full0 + 8u * s);
+            }
         }
     }
     if (!ok && tid == 0) set_status(p.status, kStatusTimeout);
