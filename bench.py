@@ -54,6 +54,27 @@ def decode_algorithmic_bytes(N):
     return N * H * (2 * STATE_BYTES + BYTES_PER_TOKEN_HEAD)
 
 
+def reduce_max(values, device="cpu"):
+    """Element-wise max of a list of floats over all ranks (identity on one process)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_rate(units_per_rank, world, slowest_ms):
+    """Weak-scaling throughput: every rank processes units_per_rank in parallel; the job
+    takes as long as the slowest rank."""
+    return units_per_rank * world / (slowest_ms / 1e3)
+
+
+def rank_seed(base, rank):
+    """Each rank serves its own prompt and decode batch (independent problems)."""
+    return base + 1000 * rank
+
+
 def read_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -110,7 +131,10 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
 
     def stop(self):
         if self.proc is None:
@@ -124,7 +148,9 @@ class ClockSampler:
             self.t.join(timeout=2)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        t_lo, t_hi = getattr(self, "t_start", 0.0), getattr(self, "t_stop", float("inf"))
+        inside = [ln for (ts, ln) in self.lines if t_lo <= ts <= t_hi]
+        for ln in inside or [ln for (_, ln) in self.lines]:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -208,7 +234,7 @@ def run_reference(args, rank):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
@@ -236,13 +262,13 @@ def main(argv=None):
     stream = torch.cuda.current_stream()
 
     # ---- inputs (seeded per rank: each rank serves its own prompt and decode batch) ----
-    c = workloads.single_case(T_PROMPT, seed=2 + 1000 * rank, device=dev, ckpt_stride=CKPT)
+    c = workloads.single_case(T_PROMPT, seed=rank_seed(2, rank), device=dev, ckpt_stride=CKPT)
     cu_dev = c.cu_seqlens.to(dev)
     out = torch.empty(T_PROMPT, H, D, device=dev, dtype=torch.bfloat16)
     fin = torch.empty(1, H, D, D, device=dev, dtype=torch.float32)
     n_ck = kda.kda_ckpt_count(c.cu_seqlens, CKPT)
     ck = torch.empty(n_ck, H, D, D, device=dev, dtype=torch.float32)
-    dc = workloads.decode_case(N=DEC_N, H=H, D=D, steps=1, seed=4 + 1000 * rank, device=dev)
+    dc = workloads.decode_case(N=DEC_N, H=H, D=D, steps=1, seed=rank_seed(4, rank), device=dev)
     dstate = dc.state
     ds = dc.steps[0]
     dout = torch.empty(DEC_N, H, D, device=dev, dtype=torch.bfloat16)
@@ -262,6 +288,7 @@ def main(argv=None):
         raise RuntimeError("device status after warm-up")
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # (events for every step: the split between the prefill and decode kernels)
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if world > 1:
         dist.barrier()
@@ -271,6 +298,8 @@ def main(argv=None):
         time.sleep(0.3)
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.mark("t_start")
     start.record(stream)
     for i in range(args.steps):
         ev[i][0].record(stream)
@@ -280,6 +309,8 @@ def main(argv=None):
         ev[i][2].record(stream)
     stop.record(stream)
     torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("t_stop")
     clocks = sampler.stop() if sampler else None
     if world > 1:
         dist.barrier()
@@ -289,16 +320,13 @@ def main(argv=None):
     if kda.kda_device_status() != 0:
         raise RuntimeError("device status after timed region")
 
-    t = torch.tensor([total_ms, sum(pre_ms), sum(dec_ms)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, pre_sum, dec_sum = (float(x) for x in t.tolist())
+    total_ms, pre_sum, dec_sum = reduce_max([total_ms, sum(pre_ms), sum(dec_ms)], device=dev)
     ms_step = total_ms / args.steps
     pre_avg = pre_sum / args.steps
     dec_avg = dec_sum / args.steps
 
     tokens_all = T_PROMPT * world
-    value = tokens_all / (pre_avg / 1e3)
+    value = whole_job_rate(T_PROMPT, world, pre_avg)
     hbm, bf16, bf16s, peak_src = read_peaks()
     pre_bytes = prefill_algorithmic_bytes(T_PROMPT, n_ck)
     dec_bytes = decode_algorithmic_bytes(DEC_N)
@@ -343,12 +371,10 @@ def main(argv=None):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
-        e_ms = torch.tensor([a.elapsed_time(b) / n_e2e], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(e_ms, op=dist.ReduceOp.MAX)
-        e2e = {"value": tokens_all / (float(e_ms.item()) / 1e3), "unit": "tokens/s",
+        (e_ms,) = reduce_max([a.elapsed_time(b) / n_e2e], device=dev)
+        e2e = {"value": whole_job_rate(T_PROMPT, world, e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": float(e_ms.item()), "steps": n_e2e,
+               "ms_per_step": e_ms, "steps": n_e2e,
                "note": "prefill only; pinned host inputs copied in, output + checkpoints + final state copied out"}
         del host, d_in, h_out, h_ck
 
@@ -370,7 +396,7 @@ def main(argv=None):
                        "ckpt_stride": CKPT, "decode_batch": DEC_N,
                        "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"replicas x{world}"},
             "prefill_ms": pre_avg, "decode_ms": dec_avg,
-            "decode": {"value": dec_gbs, "unit": "GB/s", "tokens_per_s": DEC_N * world / (dec_avg / 1e3),
+            "decode": {"value": dec_gbs * world, "unit": "GB/s", "tokens_per_s": whole_job_rate(DEC_N, world, dec_avg),
                        "frac_of_hbm_peak": dec_gbs / hbm},
             "roofline": {"bound": "hbm", "achieved": pre_gbs, "peak": hbm, "unit": "GB/s",
                          "frac": pre_gbs / hbm, "traffic": traffic, "kernel": "kda_prefill_kernel",

@@ -6,6 +6,9 @@
 #include <cuda_runtime.h>
 
 #include "../../include/kda.h"
+#include "../../include/kda_debug.h"
+#include "common.cuh"
+#include "tc.cuh"
 
 namespace kda {
 int launch_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* log_alpha,
@@ -53,6 +56,16 @@ int device_setup(int** status) {
 }
 
 bool head_dims_ok(int Dk, int Dv) { return (Dk == 64 || Dk == 128) && (Dv == 64 || Dv == 128); }
+
+// One thread waits, with a bound, on an mbarrier phase that nothing completes.
+__global__ void expire_wait_kernel(unsigned long long limit_ns, int* status) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        kda::tc::mbar_init(&bar, 1);
+        kda::tc::mbar_fence_init();
+        if (!kda::tc::mbar_wait_bounded(&bar, 0, limit_ns)) kda::set_status(status, kda::kStatusTimeout);
+    }
+}
 
 }  // namespace
 
@@ -141,6 +154,16 @@ int kda_decode_step(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     rc = kda::launch_decode(q, k, v, log_alpha, beta, state, out, out_dtype == KDA_OUT_F32, N, H, Dk,
                             static_cast<cudaStream_t>(stream));
     return rc == 0 ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_debug_expire_wait(unsigned long long limit_ns, void* stream) {
+    int* status = nullptr;
+    int rc = device_setup(&status);
+    if (rc != KDA_OK) return rc;
+    if (limit_ns < 1000000ull) limit_ns = 1000000ull;
+    if (limit_ns > 1000000000ull) limit_ns = 1000000000ull;
+    expire_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns, status);
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 int kda_device_status(void* stream) {

@@ -68,6 +68,8 @@ def load():
             lib.kda_status_string.argtypes = [_i]
             lib.kda_chunk_size.restype = _i
             lib.kda_chunk_size.argtypes = []
+            lib.kda_debug_expire_wait.restype = _i
+            lib.kda_debug_expire_wait.argtypes = [ctypes.c_ulonglong, _vp]
             _lib = lib
     return _lib
 
@@ -134,6 +136,10 @@ def kda_decode_step(q, k, v, log_alpha, beta, state, out, out_dtype: int,
                                 _ptr(_bits16(beta)), _ptr(state), _ptr(out), int(out_dtype),
                                 int(N), int(H), int(Dk), int(Dv), _stream(stream))
     _check(rc, "kda_decode_step")
+
+
+def kda_debug_expire_wait(limit_ns: int, stream=None):
+    _check(load().kda_debug_expire_wait(int(limit_ns), _stream(stream)), "kda_debug_expire_wait")
 
 
 def kda_device_status(stream=None) -> int:

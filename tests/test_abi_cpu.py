@@ -21,15 +21,19 @@ def lib():
 
 
 def _declared_functions():
-    src = open(os.path.join(ROOT, "include", "kda.h")).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(kda_\w+)\s*\(", src)))
+    names = set()
+    for hdr in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if hdr.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", hdr)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names.update(re.findall(r"\b(kda_\w+)\s*\(", src))
+    return sorted(names)
 
 
 def test_header_declares_expected_entry_points():
     names = _declared_functions()
     for n in ["kda_chunk_prefill", "kda_decode_step", "kda_ckpt_count", "kda_device_status",
-              "kda_status_string", "kda_chunk_size"]:
+              "kda_status_string", "kda_chunk_size", "kda_debug_expire_wait"]:
         assert n in names
 
 
