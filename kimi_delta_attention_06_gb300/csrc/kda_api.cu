@@ -17,7 +17,8 @@ int launch_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, const
 int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* la,
                    const uint16_t* beta, const float* init_state, const int32_t* cu_seqlens,
                    int num_seqs, int total_tokens, int H, int Dk, int Dv, void* out, int out_f32,
-                   float* final_state, float* ckpt, int ckpt_stride, int* status, cudaStream_t stream);
+                   float* final_state, float* ckpt, int ckpt_stride, void* ws, int* status, cudaStream_t stream);
+size_t prefill_workspace_bytes(int num_seqs, int H);
 }  // namespace kda
 
 namespace {
@@ -28,6 +29,7 @@ __device__ int g_kda_status = 0;
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int* g_status_ptr[kMaxDevices] = {};
+cudaMemPool_t g_pool[kMaxDevices] = {};   // stream-ordered pool for the prefill hand-off ring
 int g_device_ok[kMaxDevices] = {};   // 0 unknown, 1 supported, -1 unsupported
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -52,6 +54,31 @@ int device_setup(int** status) {
     }
     if (g_device_ok[dev] != 1) return KDA_ERR_UNSUPPORTED;
     *status = g_status_ptr[dev];
+    return KDA_OK;
+}
+
+// The library's own memory pool on the current device (created once; it keeps what it
+// has reserved, so steady-state calls reuse the same memory without a driver call).
+int workspace_pool(cudaMemPool_t* pool) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_pool[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pl = nullptr;
+        if (cudaMemPoolCreate(&pl, &props) != cudaSuccess) return KDA_ERR_CUDA;
+        uint64_t keep = ~0ull;
+        if (cudaMemPoolSetAttribute(pl, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+            cudaMemPoolDestroy(pl);
+            return KDA_ERR_CUDA;
+        }
+        g_pool[dev] = pl;
+    }
+    *pool = g_pool[dev];
     return KDA_OK;
 }
 
@@ -128,10 +155,18 @@ int kda_chunk_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     int* status = nullptr;
     int rc = device_setup(&status);
     if (rc != KDA_OK) return rc;
+    cudaMemPool_t pool = nullptr;
+    rc = workspace_pool(&pool);
+    if (rc != KDA_OK) return rc;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void* ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, kda::prefill_workspace_bytes(num_seqs, H), pool, st) != cudaSuccess)
+        return KDA_ERR_CUDA;
     rc = kda::launch_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, num_seqs, total_tokens, H, Dk, Dv,
                              out, out_dtype == KDA_OUT_F32, final_state, ckpt_states, ckpt_stride,
-                             status, static_cast<cudaStream_t>(stream));
-    return rc == 0 ? KDA_OK : KDA_ERR_CUDA;
+                             ws, status, st);
+    const bool freed = cudaFreeAsync(ws, st) == cudaSuccess;
+    return (rc == 0 && freed) ? KDA_OK : KDA_ERR_CUDA;
 }
 
 int kda_decode_step(const uint16_t* q, const uint16_t* k, const uint16_t* v,

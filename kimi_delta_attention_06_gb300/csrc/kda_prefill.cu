@@ -33,16 +33,21 @@
 //
 // Work decomposition: one thread-block cluster of 4 CTAs per (sequence, head).
 //   * CTA 0 (chain): owns the fp32 state (Dk x Dv, one row per thread, in
-//     registers for the whole sequence; two warpgroups split the value
-//     columns) and runs the sequential part as two dependent MMA steps per
-//     chunk: [U; O] = [T; Mqk] V + [-W; Q'] S, then K^^T U for the update.
+//     registers for the whole sequence) and runs the sequential part as two
+//     dependent MMA steps per chunk: [U; O] = [T; Mqk] V + [-W; Q'] S, then
+//     K^^T U for the update.  The value columns of the recurrence never mix,
+//     so its two warpgroups each carry 64 of them through their own MMAs and
+//     barriers and never wait for each other.
 //   * CTAs 1-3 (prep): chunk c is prepared by CTA 1 + c % 3.  Its inputs
 //     arrive by TMA; it builds [-W; Q'], K^, [T; Mqk], V (fp16) and exp(g_C)
-//     in its own shared memory and ships them, as one contiguous bulk copy,
-//     into slot c % 2 of the chain CTA's shared memory (distributed shared
-//     memory).  The chain issues no global loads on its critical path.
+//     in its own shared memory and bulk-stores each part, as soon as it is
+//     final, into entry c % 6 of a per-cluster ring in global memory (it stays
+//     in L2).  The chain bulk-loads entry c into slot c % 2 of its shared
+//     memory while it still works on chunk c - 1.
 // Three chunks are being prepared while the chain consumes a fourth, so the
-// chain's dependent-MMA latency, not the preparation, sets the pace.
+// chain's dependent-MMA latency, not the preparation, sets the pace.  (An L2
+// round trip moves a block into one SM several times faster than a
+// distributed-shared-memory copy does.)
 // Hand-offs use mbarriers (remote arrivals, transaction-count completion); every
 // wait is bounded, and a timeout records KDA_ERR_TIMEOUT and ends the kernel.
 #include "common.cuh"
@@ -60,8 +65,9 @@ constexpr int NT = 256;         // threads per CTA
 constexpr int NPREP_CTAS = 3;   // prep CTAs per cluster
 constexpr int CLUSTER = 1 + NPREP_CTAS;
 constexpr uint32_t BAR_ALL = 1;  // named barrier over the CTA's 256 threads
+constexpr int ST_THREAD = 32;    // prep CTA: issues the ring stores and publishes them (not the MMA issuer)
 
-// Hand-off block: produced in a prep CTA, copied verbatim into a chain slot.
+// Hand-off block: produced in a prep CTA, copied verbatim through the global ring into a chain slot.
 constexpr uint32_t H_AH = 0;                 // [-W; Q'] f16 (built from [K~; Q~]), 128 rows x 128 K, K-major (32 KB)
 constexpr uint32_t H_KH = 32768;             // K^ f16, 64 rows (token) x 128 (channel)  (16 KB)
 constexpr uint32_t H_QT = 49152;             // [T; Mqk] f16, 128 rows x 64 K, K-major   (16 KB)
@@ -70,6 +76,8 @@ constexpr uint32_t H_EGC = 81920;            // exp(g_C), 128 f32               
 constexpr uint32_t H_BYTES = 81920 + 512;
 static_assert(H_BYTES % (8 * 16) == 0, "hand-off splits into 8 16-byte-multiple parts");
 constexpr uint32_t H_STRIDE = 82944;         // slot pitch (1024-aligned)
+constexpr int WS_SLOTS = 6;                  // global ring entries per cluster (two per prep CTA)
+constexpr size_t WS_BYTES_PER_CLUSTER = static_cast<size_t>(WS_SLOTS) * H_STRIDE;
 
 // Prep CTA shared memory.
 constexpr uint32_t P_A1 = 0;                 // [Km; Qm] tf32, 128 rows x 128 K, K-major  (64 KB)
@@ -83,7 +91,7 @@ constexpr uint32_t P_OUT = 98304;            // hand-off block                  
 constexpr uint32_t P_P = P_OUT + H_STRIDE;   // A f16, 64 rows x 64 K, K-major             (8 KB)
 constexpr uint32_t P_BETA = P_P + 8192;      // beta [64] f32
 constexpr uint32_t P_TOT = P_BETA + 256;     // token-group log-decay totals [8][128] f32
-constexpr uint32_t P_BAR = P_TOT + 4096;     // mbarriers: 0 mma, 1 recv, 2 free, 3 tma
+constexpr uint32_t P_BAR = P_TOT + 4096;     // mbarriers: 0 mma, 1-2 ring entry free, 3 tma
 constexpr uint32_t P_TMEM = P_BAR + 32;
 // fp16 scratch of the inverse (row pitch LH halves)
 constexpr int LH = 72;
@@ -96,8 +104,13 @@ constexpr uint32_t P_END = P_Y + 32 * LH * 2;
 constexpr uint32_t K_SLOT = 0;                       // 2 hand-off slots
 constexpr uint32_t K_S = 2 * H_STRIDE;               // S f16, 128 rows (channel) x 128 N, MN-major (32 KB)
 constexpr uint32_t K_XU = K_S + 32768;               // U f16, 64 rows (token) x 128 N, MN-major (16 KB)
-constexpr uint32_t K_BAR = K_XU + 16384;             // mbarriers: 0 mma, 1-2 full[slot]
-constexpr uint32_t K_TMEM = K_BAR + 32;
+constexpr uint32_t K_BAR = K_XU + 16384;             // mbarriers (indices below)
+constexpr int KB_MMA = 0;      // [2] MMA completion, one per warpgroup
+constexpr int KB_FULL = 2;     // [2] slot loaded
+constexpr int KB_CONS = 4;     // [2] slot consumed by every active warpgroup
+constexpr int KB_READY = 6;    // [6] ring entry stored by its prep CTA
+constexpr int KB_COUNT = 12;
+constexpr uint32_t K_TMEM = K_BAR + 8 * KB_COUNT;
 constexpr uint32_t K_END = K_TMEM + 16;
 
 constexpr uint32_t SMEM_BYTES = (P_END > K_END ? P_END : K_END) + 1024;   // + alignment slack
@@ -124,6 +137,7 @@ struct Params {
     void* out;
     float* final_state;
     float* ckpt;
+    uint8_t* ws;                 // hand-off ring: WS_BYTES_PER_CLUSTER per cluster
     int* status;
     int out_f32;
     int ckpt_stride;
@@ -228,11 +242,12 @@ __device__ __forceinline__ void st_frag(__half* base, int pitch, int r0, int n0,
     *reinterpret_cast<__half2*>(base + (r0 + g + 8) * pitch + n0 + 2 * t) = __floats2half2_rn(sc * d[2], sc * d[3]);
 }
 
-// Bounded wait on an mbarrier phase, agreed by all threads of the CTA.
-__device__ __forceinline__ bool cta_wait(void* bar, uint32_t parity, bool cluster_scope) {
+// Bounded wait on an mbarrier phase, agreed by all threads of the CTA (together
+// with each thread's own `mine` flag).
+__device__ __forceinline__ bool cta_wait(void* bar, uint32_t parity, bool cluster_scope, bool mine = true) {
     const uint32_t ok = cluster_scope ? tc::mbar_wait_cluster_bounded(bar, parity, kWaitLimitNs)
                                       : tc::mbar_wait_bounded(bar, parity, kWaitLimitNs);
-    const uint32_t all = tc::named_sync_and(BAR_ALL, NT, ok);
+    const uint32_t all = tc::named_sync_and(BAR_ALL, NT, ok && mine);
     tc::fence_after_sync();
     return all != 0;
 }
@@ -251,9 +266,20 @@ __device__ __forceinline__ void issue_input_tma(const TensorMaps& tmaps, const P
 }
 
 // ============================================================================
+// Pull chunk c's inputs into L2 ahead of the TMA load that stages them: a strided
+// tile streamed from DRAM takes several microseconds to land, from L2 a fraction of one.
+__device__ __forceinline__ void prefetch_inputs(const TensorMaps& tmaps, const Params& p, int c, int t0, int h) {
+    const int y = t0 + c * C;
+    tc::tma_prefetch_2d(&tmaps.la, h * p.dk, y);
+    tc::tma_prefetch_2d(&tmaps.q, h * p.dk, y);
+    tc::tma_prefetch_2d(&tmaps.k, h * p.dk, y);
+    tc::tma_prefetch_2d(&tmaps.v, h * p.dv, y);
+}
+
 // Prep CTA: prepares chunks c = pr, pr + 3, pr + 6, ... of one (sequence, head).
 // ============================================================================
-__device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm, int pr, int h, int t0, int len) {
+__device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm, int pr, int h, int t0, int len,
+                          size_t cl) {
     uint8_t* A1 = sm + P_A1;
     uint8_t* B1 = sm + P_B1;
     uint8_t* OUT = sm + P_OUT;
@@ -267,7 +293,7 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
     __half* Yh = reinterpret_cast<__half*>(sm + P_Y);
     float* s_beta = reinterpret_cast<float*>(sm + P_BETA);
     float* s_tot = reinterpret_cast<float*>(sm + P_TOT);
-    uint64_t* mb = reinterpret_cast<uint64_t*>(sm + P_BAR);    // 0: mma, 1: recv, 2: free, 3: tma
+    uint64_t* mb = reinterpret_cast<uint64_t*>(sm + P_BAR);    // 0: mma, 1-2: ring entry free, 3: tma
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + P_TMEM);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -278,31 +304,52 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
     cta_sync_tc();
     const uint32_t tm = *s_tmem;
     const uint32_t lane_base = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    // the chain CTA's (rank 0) two slots and their full barriers
-    const uint32_t chain_slot0 = tc::mapa(tc::smem_u32(sm + K_SLOT), 0);
-    const uint32_t chain_full0 = tc::mapa(tc::smem_u32(sm + K_BAR + 8), 0);
+    // the chain CTA's (rank 0) ring-entry barriers, and this cluster's ring
+    const uint32_t chain_ready0 = tc::mapa(tc::smem_u32(sm + K_BAR + 8 * KB_READY), 0);
+    uint8_t* ring = p.ws + cl * WS_BYTES_PER_CLUSTER;
+    // chunk whose bulk stores may still be in flight (same value in every thread)
+    int pending = -1;
+    auto publish = [&]() {      // ST_THREAD: once the stores of `pending` are complete, tell the chain
+        tc::bulk_wait_all();
+        tc::fence_proxy_async_global();
+        tc::mbar_arrive_remote(chain_ready0 + 8u * static_cast<uint32_t>(pending % WS_SLOTS));
+    };
 
     const int cg = tid & 31, tg = tid >> 5;             // channels 4cg..4cg+3, tokens 8tg..8tg+7
     const bool ch_ok = 4 * cg < dk;
-    // beta of token (tid - 128), fetched one chunk ahead by warps 4-5, which never
-    // issue a proxy fence while the load is in flight
-    auto load_beta = [&](int c) -> float {
-        const int t = tid - 128;
-        const int nvb = min(C, len - c * C);
-        return (t >= 0 && t < nvb) ? bf16_bits_to_f32(p.beta[static_cast<size_t>(t0 + c * C + t) * p.H + h]) : 0.f;
+    // beta of token (tid - 128): warps 4-5 load the raw bits one chunk ahead (converted
+    // only where the value is stored, so the load stays in flight across the chunk
+    // boundary) and pull the lines of the chunk after that into L2
+    const bool beta_thread = tid >= 128 && tid < 192;
+    auto beta_ptr = [&](int c) -> const uint16_t* {
+        return p.beta + static_cast<size_t>(t0 + c * C + (tid - 128)) * p.H + h;
     };
-    float bt = 0.f;
+    auto load_beta = [&](int c) -> uint16_t {
+        return (tid - 128 < min(C, len - c * C)) ? *beta_ptr(c) : static_cast<uint16_t>(0);
+    };
+    auto prefetch_beta = [&](int c) {
+        if (c < nchunks && tid - 128 < min(C, len - c * C))
+            asm volatile("prefetch.global.L2 [%0];" :: "l"(beta_ptr(c)));
+    };
+    uint16_t bt = 0;
     if (pr < nchunks) {
-        if (tid == 0) issue_input_tma(tmaps, p, sm, pr, t0, h, &mb[3]);
-        if (tid >= 128 && tid < 192) bt = load_beta(pr);
+        if (tid == 0) {
+            issue_input_tma(tmaps, p, sm, pr, t0, h, &mb[3]);
+            if (pr + NPREP_CTAS < nchunks) prefetch_inputs(tmaps, p, pr + NPREP_CTAS, t0, h);
+        }
+        if (beta_thread) {
+            bt = load_beta(pr);
+            prefetch_beta(pr + NPREP_CTAS);
+        }
     }
-    uint32_t ph_mma = 0, n_recv = 0, n_free = 0;
+    uint32_t ph_mma = 0;
     bool ok = true;
     int kk = 0;                                         // index of this CTA's chunk
     for (int c = pr; c < nchunks; c += NPREP_CTAS, ++kk) {
         const int nv = min(C, len - c * C);
 
         // -- 0. inputs of this chunk: staging (TMA) -> registers --
+        if (tid == 0 && c + 2 * NPREP_CTAS < nchunks) prefetch_inputs(tmaps, p, c + 2 * NPREP_CTAS, t0, h);
         if (!cta_wait(&mb[3], kk & 1, false)) { ok = false; break; }
         float4 g4[8];
         uint2 q2[8], k2[8];
@@ -334,13 +381,9 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             for (int i = 0; i < 8; ++i) { acc = f4add(acc, g4[i]); g4[i] = acc; }
             *reinterpret_cast<float4*>(s_tot + tg * 128 + 4 * cg) = acc;
         }
-        // the previous hand-off of this CTA must have landed before the block is rewritten
-        if (kk >= 1) {
-            if (!cta_wait(&mb[1], n_recv & 1, true)) { ok = false; break; }
-            ++n_recv;
-        }
-        tc::named_sync(BAR_ALL, NT);     // totals visible; staging fully read
-        if (tid >= 128 && tid < 192) s_beta[tid - 128] = bt;
+        // the stores of the previous block must have read it before it is rewritten
+        if (pending >= 0 && tid == ST_THREAD) tc::bulk_wait_read_all();
+        tc::named_sync(BAR_ALL, NT);     // totals visible; staging fully read; block free
         // -- 1b. decay factors and operand tiles --
         {
             float4 off = make_float4(0.f, 0.f, 0.f, 0.f), gr = off, gc = off;
@@ -384,18 +427,36 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
                 st_h4(KH, t, 4 * cg, 64, f4mul(kb, ecr));         // K^ = k e^{g_C - g_t}
             }
         }
+        if (beta_thread) s_beta[tid - 128] = bf16_bits_to_f32(bt);
         tc::fence_smem_to_async();
         cta_sync_tc();
 
         // -- 2. G1 = [Km; Qm] Kb^T  (tf32, 128 x 64, K = 128 channels) --
+        //    meanwhile K^, V and exp(g_C) (final already) go to ring entry c % 6 once
+        //    the chain has loaded that entry's previous chunk (c - 6)
+        uint8_t* entry = ring + static_cast<size_t>(c % WS_SLOTS) * H_STRIDE;
+        bool ring_ok = true;
         if (tid == 0) {
             issue_mma<false>(tm + TM_G1, 128, 64, DK, tc::smem_u32(A1), false, 128, tc::smem_u32(B1), false, 64);
             tc::mma_commit(&mb[0]);
         }
+        // the previous block's stores have long completed: hand it to the chain (the
+        // release this takes overlaps the MMA)
+        if (tid == ST_THREAD && pending >= 0) publish();
+        pending = -1;
         if (!cta_wait(&mb[0], ph_mma & 1, false)) { ok = false; break; }
         ++ph_mma;
         // [Km; Qm] and Kb are dead until the next chunk: stage that chunk's inputs there
         if (tid == 0 && c + NPREP_CTAS < nchunks) issue_input_tma(tmaps, p, sm, c + NPREP_CTAS, t0, h, &mb[3]);
+        if (tid == ST_THREAD) {
+            if (kk >= 2)
+                ring_ok = tc::mbar_wait_cluster_bounded(&mb[1 + (kk & 1)], ((kk - 2) >> 1) & 1, kWaitLimitNs) != 0;
+            if (ring_ok) {
+                tc::bulk_store_s2g(entry + H_KH, tc::smem_u32(KH), H_QT - H_KH);
+                tc::bulk_store_s2g(entry + H_V, tc::smem_u32(OUT + H_V), H_BYTES - H_V);
+                tc::bulk_commit();
+            }
+        }
 
         // -- 3. L (rows 0..63 -> fp32 scratch), A (rows 64..127 -> f16 tile) --
         {
@@ -423,7 +484,9 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
                 for (int i = 0; i < 32; i += 8) st_h8(P, t, c0 + i, 64, v + i);
             }
         }
-        cta_sync_tc();
+        tc::fence_before_sync();
+        if (!tc::named_sync_and(BAR_ALL, NT, ring_ok)) { ok = false; break; }
+        tc::fence_after_sync();
 
         // -- 4. T = (I + L)^{-1} by recursive doubling over 16 x 16 blocks --
         //    blocks [[A, 0], [B, D]]^{-1} = [[A^-1, 0], [-D^-1 B A^-1, D^-1]]; the block
@@ -523,6 +586,10 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             tc::fence_smem_to_async();
         }
         cta_sync_tc();
+        if (tid == ST_THREAD) {                           // [T; Mqk] is final
+            tc::bulk_store_s2g(entry + H_QT, tc::smem_u32(Qt), H_V - H_QT);
+            tc::bulk_commit();
+        }
 
         // -- 6. WY form: [W; Mqk K~] = [T; Mqk] K~ (K~ rows of [K~; Q~] read as an MN-major B) --
         if (tid == 0) {
@@ -561,23 +628,21 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         }
         tc::fence_smem_to_async();
         cta_sync_tc();
-        // next chunk's beta (warps 4-5): no proxy fence runs in these threads before it is used
-        if (c + NPREP_CTAS < nchunks && tid >= 128 && tid < 192) bt = load_beta(c + NPREP_CTAS);
-
-        // -- 7. hand the block to the chain CTA: slot c % 2, once that slot is free --
-        if (c >= 2) {
-            if (!cta_wait(&mb[2], n_free & 1, true)) { ok = false; break; }
-            ++n_free;
+        if (tid == ST_THREAD) {                           // [-W; Q'] is final: the block is complete
+            tc::bulk_store_s2g(entry + H_AH, tc::smem_u32(AH), H_KH - H_AH);
+            tc::bulk_commit();
         }
-        {   // 8 concurrent bulk copies of H_BYTES / 8 each, one per warp
-            const uint32_t s = static_cast<uint32_t>(c & 1);
-            if (tid == 0) tc::mbar_arrive_expect_tx_remote(chain_full0 + 8u * s, H_BYTES);
-            if (lane == 0) {
-                constexpr uint32_t part = H_BYTES / 8;
-                tc::bulk_copy_s2cluster(chain_slot0 + s * H_STRIDE + warp * part, tc::smem_u32(OUT) + warp * part, part,
-                                        chain_full0 + 8u * s);
-            }
+        pending = c;
+        // next chunk's beta (warps 4-5): it is stored before these threads run their next proxy fence
+        if (beta_thread && c + NPREP_CTAS < nchunks) {
+            bt = load_beta(c + NPREP_CTAS);
+            prefetch_beta(c + 2 * NPREP_CTAS);
         }
+    }
+    if (tid == ST_THREAD) {
+        // the shared-memory block must outlive the stores that read it
+        if (ok && pending >= 0) publish();
+        else tc::bulk_wait_all();
     }
     if (!ok && tid == 0) set_status(p.status, kStatusTimeout);
     cta_sync_tc();
@@ -587,15 +652,29 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
 // ============================================================================
 // Chain CTA: the sequential state recurrence of one (sequence, head).
 // ============================================================================
-__device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, int len) {
+// Named barrier of warpgroup wg (ids 2 and 3), with the tcgen05 ordering fences.
+__device__ __forceinline__ void wg_sync_tc(uint32_t bar_id) {
+    tc::fence_before_sync();
+    tc::named_sync(bar_id, 128);
+    tc::fence_after_sync();
+}
+__device__ __forceinline__ bool wg_wait(void* bar, uint32_t parity, uint32_t bar_id) {
+    const uint32_t ok = tc::mbar_wait_bounded(bar, parity, kWaitLimitNs);
+    const uint32_t all = tc::named_sync_and(bar_id, 128, ok);
+    tc::fence_after_sync();
+    return all != 0;
+}
+
+__device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, int len, size_t cl) {
     uint8_t* Sb = sm + K_S;
     uint8_t* XU = sm + K_XU;
-    uint64_t* mb = reinterpret_cast<uint64_t*>(sm + K_BAR);     // 0: mma, 1-2: full[slot]
+    uint64_t* mb = reinterpret_cast<uint64_t*>(sm + K_BAR);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + K_TMEM);
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int d = tid & 127;                 // state row = TMEM lane
     const int wg = tid >> 7;                 // value columns 64 wg .. 64 wg + 63
+    const uint32_t bar_wg = 2u + static_cast<uint32_t>(wg);
     const int H = p.H, dk = p.dk, dv = p.dv;
     const bool col_ok = 64 * wg < dv;
     const size_t vtok_stride = static_cast<size_t>(H) * dv;
@@ -606,8 +685,8 @@ __device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, i
     const uint32_t tm = *s_tmem;
     const uint32_t lane_base = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t cb = static_cast<uint32_t>(64 * wg);      // this warpgroup's TMEM column offset
-    const uint32_t prep_recv = tc::smem_u32(sm + P_BAR + 8);  // local offsets of the prep barriers
-    const uint32_t prep_free = tc::smem_u32(sm + P_BAR + 16);
+    const uint32_t prep_free = tc::smem_u32(sm + P_BAR + 8);  // local offset of the prep CTAs' ring barriers
+    const uint8_t* ring = p.ws + cl * WS_BYTES_PER_CLUSTER;
 
     long long slot_ck = 0;
     if (p.ckpt && p.ckpt_stride > 0) {
@@ -627,43 +706,69 @@ __device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, i
             S[j] = v4.x; S[j + 1] = v4.y; S[j + 2] = v4.z; S[j + 3] = v4.w;
         }
     }
-    const int Nmma = dv;                      // 64 or 128 value columns
+
+    // Loader (thread 0): chunk j goes from ring entry j % 6 into slot j % 2 once its prep
+    // CTA has stored it and every warpgroup is done with chunk j - 2.  Loads are issued
+    // in order; `issued` counts them.  Non-blocking probes run between thread 0's other
+    // duties so that the next chunk is normally in flight long before it is needed.
+    int issued = 0;
+    bool load_ok = true;
+    auto load = [&](int j, bool block) -> bool {
+        void* cons = &mb[KB_CONS + (j & 1)];
+        void* ready = &mb[KB_READY + j % WS_SLOTS];
+        const uint32_t pc = static_cast<uint32_t>((j - 2) >> 1) & 1u, prd = static_cast<uint32_t>(j / WS_SLOTS) & 1u;
+        if (block) {
+            if (j >= 2 && !tc::mbar_wait_bounded(cons, pc, kWaitLimitNs)) return false;
+            if (!tc::mbar_wait_cluster_bounded(ready, prd, kWaitLimitNs)) return false;
+        } else {
+            if (j >= 2 && !tc::mbar_test_wait(cons, pc)) return false;
+            if (!tc::mbar_test_wait_cluster(ready, prd)) return false;
+        }
+        tc::fence_proxy_async_global();
+        void* full = &mb[KB_FULL + (j & 1)];
+        tc::mbar_arrive_expect_tx(full, H_BYTES);
+        tc::bulk_load_g2s(tc::smem_u32(sm + K_SLOT + (j & 1) * H_STRIDE),
+                          ring + static_cast<size_t>(j % WS_SLOTS) * H_STRIDE, H_BYTES, full);
+        ++issued;
+        return true;
+    };
+    auto probe = [&](int upto) {           // issue what can go now, up to chunk `upto` - 1
+        while (issued < upto && issued < nchunks && load(issued, false)) {}
+    };
+
     uint32_t ph_mma = 0;
     bool ok = true;
-    // 'received' signals go out as soon as a hand-off has landed (thread 0 polls the
-    // next slot between its other duties), so a producer can start on its next chunk
-    // without waiting for the chain to reach this one.
-    int received = 0;                         // chunks [0, received) acknowledged
-    auto ack_landed = [&](int upto) {
-        while (received < upto && received < nchunks &&
-               tc::mbar_test_wait(&mb[1 + (received & 1)], (received >> 1) & 1)) {
-            tc::mbar_arrive_remote_relaxed(tc::mapa(prep_recv, 1 + received % NPREP_CTAS));
-            ++received;
-        }
-    };
-    for (int c = 0; c < nchunks; ++c) {
+    int waited = 0;                           // chunks whose slot this warpgroup has waited for
+    for (int c = 0; col_ok && c < nchunks; ++c) {
         const int cs = t0 + c * C;
         const int nv = min(C, len - c * C);
         const int s = c & 1;
         uint8_t* slot = sm + K_SLOT + s * H_STRIDE;
-        if (!cta_wait(&mb[1 + s], (c >> 1) & 1, false)) { ok = false; break; }
-        // the producer's staging block is free again
-        if (tid == 0) ack_landed(c + 1);
+        if (tid == 0) {
+            if (issued == c && load_ok) load_ok = load(c, true);
+            probe(c + 2);
+        }
+        if (!wg_wait(&mb[KB_FULL + s], (c >> 1) & 1, bar_wg)) { ok = false; break; }
+        waited = c + 1;
+        // the ring entry is free again: its prep CTA may store chunk c + 6 there
+        if (tid == 0 && c + WS_SLOTS < nchunks)
+            tc::mbar_arrive_remote_relaxed(tc::mapa(prep_free + 8u * ((c / NPREP_CTAS) & 1), 1 + c % NPREP_CTAS));
         const float gc = reinterpret_cast<const float*>(slot + H_EGC)[d];
 
-        // -- [U; O] = [T; Mqk] V + [-W; Q'] S  (one accumulator) --
+        // -- [U; O] = [T; Mqk] V + [-W; Q'] S  (one accumulator, this warpgroup's 64 columns) --
 #pragma unroll
         for (int j = 0; j < 64; j += 8) st_h8(Sb, d, 64 * wg + j, 128, S + j);
         tc::fence_smem_to_async();
-        cta_sync_tc();
-        if (tid == 0) {
-            issue_mma<true>(tm + TM_D1, 128, Nmma, C, tc::smem_u32(slot + H_QT), false, 128,
-                            tc::smem_u32(slot + H_V), true, 64u * 128u);
-            issue_mma<true>(tm + TM_D1, 128, Nmma, DK, tc::smem_u32(slot + H_AH), false, 128,
-                            tc::smem_u32(Sb), true, 128u * 128u, true);
-            tc::mma_commit(&mb[0]);
+        wg_sync_tc(bar_wg);
+        if (d == 0) {
+            issue_mma<true>(tm + TM_D1 + cb, 128, 64, C, tc::smem_u32(slot + H_QT), false, 128,
+                            tc::smem_u32(slot + H_V) + 8192u * wg, true, 64u * 128u);
+            issue_mma<true>(tm + TM_D1 + cb, 128, 64, DK, tc::smem_u32(slot + H_AH), false, 128,
+                            tc::smem_u32(Sb) + 16384u * wg, true, 128u * 128u, true);
+            tc::mma_commit(&mb[KB_MMA + wg]);
         }
-        if (!cta_wait(&mb[0], ph_mma & 1, false)) { ok = false; break; }
+        if (tid == 0) probe(c + 2);
+        if (!wg_wait(&mb[KB_MMA + wg], ph_mma & 1, bar_wg)) { ok = false; break; }
         ++ph_mma;
         if (d < 64) {                                    // U -> MN-major f16 tile
             float r[32];
@@ -675,15 +780,15 @@ __device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, i
             }
             tc::fence_smem_to_async();                   // only the U writers touched shared memory
         }
-        cta_sync_tc();
+        wg_sync_tc(bar_wg);
 
         // -- D3 = K^^T U  (K^ tile as an MN-major A: M = channel, K = token) --
-        if (tid == 0) {
-            issue_mma<true>(tm + TM_D3, 128, Nmma, C, tc::smem_u32(slot + H_KH), true, 64u * 128u,
-                            tc::smem_u32(XU), true, 64u * 128u);
-            tc::mma_commit(&mb[0]);
-            ack_landed(c + 2);
+        if (d == 0) {
+            issue_mma<true>(tm + TM_D3 + cb, 128, 64, C, tc::smem_u32(slot + H_KH), true, 64u * 128u,
+                            tc::smem_u32(XU) + 8192u * wg, true, 64u * 128u);
+            tc::mma_commit(&mb[KB_MMA + wg]);
         }
+        if (tid == 0) probe(c + 2);
         if (d >= 64) {                                   // O rows to global memory while D3 runs
             const int t = d - 64;
             const size_t ob = static_cast<size_t>(cs + t) * vtok_stride + static_cast<size_t>(h) * dv + 64 * wg;
@@ -692,7 +797,7 @@ __device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, i
                 float a[16];
                 tc::tmem_ld16(lane_base + TM_D1 + cb + c16, a);
                 tc::tmem_wait_ld();
-                if (t < nv && col_ok) {
+                if (t < nv) {
                     if (p.out_f32) {
                         float* op = reinterpret_cast<float*>(p.out) + ob + c16;
 #pragma unroll
@@ -713,10 +818,11 @@ __device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, i
                 }
             }
         }
-        if (!cta_wait(&mb[0], ph_mma & 1, false)) { ok = false; break; }
+        if (!wg_wait(&mb[KB_MMA + wg], ph_mma & 1, bar_wg)) { ok = false; break; }
         ++ph_mma;
-        // slot s is free: the producer of chunk c + 2 may overwrite it
-        if (tid == 0 && c + 2 < nchunks) tc::mbar_arrive_remote_relaxed(tc::mapa(prep_free, 1 + (c + 2) % NPREP_CTAS));
+        // this warpgroup is done with slot s
+        if (d == 0) tc::mbar_arrive(&mb[KB_CONS + s]);
+        if (tid == 0) probe(c + 3);
         {
             float r[32];
 #pragma unroll
@@ -730,7 +836,7 @@ __device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, i
         if (p.ckpt && p.ckpt_stride > 0) {
             const int done = c * C + nv;
             if (done % p.ckpt_stride == 0 || done == len) {
-                if (d < dk && col_ok) {
+                if (d < dk) {
                     float* cp = p.ckpt + ((static_cast<size_t>(slot_ck) * H + h) * dk + d) * dv + 64 * wg;
 #pragma unroll
                     for (int j = 0; j < 64; j += 4)
@@ -740,13 +846,18 @@ __device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, i
             }
         }
     }
+    if (tid == 0) {
+        // loads still in flight must land before this CTA's shared memory goes away
+        for (int j = waited; j < issued; ++j)
+            tc::mbar_wait_bounded(&mb[KB_FULL + (j & 1)], static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs);
+    }
     if (ok && p.final_state && d < dk && col_ok) {
         float* fp = p.final_state + ((static_cast<size_t>(n) * H + h) * dk + d) * dv + 64 * wg;
 #pragma unroll
         for (int j = 0; j < 64; j += 4)
             *reinterpret_cast<float4*>(fp + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
-    if (!ok && tid == 0) set_status(p.status, kStatusTimeout);
+    if ((!ok || !load_ok) && d == 0) set_status(p.status, kStatusTimeout);
     cta_sync_tc();
     if (warp == 0) tc::tmem_dealloc(tm, TM_CHAIN_COLS);
 }
@@ -764,13 +875,19 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_kernel(const Params p, cons
 
     // every CTA initialises its barriers before any peer can touch them
     if (threadIdx.x == 0) {
-        uint64_t* mb = reinterpret_cast<uint64_t*>(sm + (rank == 0 ? K_BAR : P_BAR));
-        for (int i = 0; i < 4; ++i) tc::mbar_init(&mb[i], 1);
+        if (rank == 0) {
+            uint64_t* mb = reinterpret_cast<uint64_t*>(sm + K_BAR);
+            for (int i = 0; i < KB_COUNT; ++i)      // a slot is consumed once per active warpgroup
+                tc::mbar_init(&mb[i], (i == KB_CONS || i == KB_CONS + 1) ? (p.dv > 64 ? 2u : 1u) : 1u);
+        } else {
+            uint64_t* mb = reinterpret_cast<uint64_t*>(sm + P_BAR);
+            for (int i = 0; i < 4; ++i) tc::mbar_init(&mb[i], 1);
+        }
         tc::mbar_fence_init();
     }
     tc::cluster_sync();
-    if (rank == 0) chain_role(p, sm, n, h, t0, len);
-    else prep_role(p, tmaps, sm, rank - 1, h, t0, len);
+    if (rank == 0) chain_role(p, sm, n, h, t0, len, static_cast<size_t>(cl));
+    else prep_role(p, tmaps, sm, rank - 1, h, t0, len, static_cast<size_t>(cl));
     // no CTA leaves while a peer may still address its shared memory
     tc::cluster_sync();
 }
@@ -810,10 +927,14 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esz,
 
 }  // namespace
 
+size_t prefill_workspace_bytes(int num_seqs, int H) {
+    return static_cast<size_t>(num_seqs) * static_cast<size_t>(H) * prefill::WS_BYTES_PER_CLUSTER;
+}
+
 int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* la,
                    const uint16_t* beta, const float* init_state, const int32_t* cu_seqlens,
                    int num_seqs, int total_tokens, int H, int Dk, int Dv, void* out, int out_f32,
-                   float* final_state, float* ckpt, int ckpt_stride, int* status, cudaStream_t stream)
+                   float* final_state, float* ckpt, int ckpt_stride, void* ws, int* status, cudaStream_t stream)
 {
     using namespace prefill;
     static bool attr_done = false;
@@ -825,6 +946,7 @@ int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
     Params p;
     p.q = q; p.k = k; p.v = v; p.la = la; p.beta = beta; p.init_state = init_state;
     p.cu_seqlens = cu_seqlens; p.out = out; p.final_state = final_state; p.ckpt = ckpt;
+    p.ws = static_cast<uint8_t*>(ws);
     p.status = status; p.out_f32 = out_f32; p.ckpt_stride = ckpt_stride;
     p.H = H; p.dk = Dk; p.dv = Dv;
     const long long clusters = static_cast<long long>(num_seqs) * H;

@@ -253,6 +253,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(void* bar, uint32_t bytes)
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                  :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
+// Prefetch the box at coordinates (x, y) of a tensor map into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 :: "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y) : "memory");
+}
 // 2-D tiled TMA load of the box at coordinates (x, y) into this CTA's shared memory;
 // completion is reported as transaction bytes on `bar`.  x * element size must be a
 // multiple of 16 bytes.
@@ -278,6 +283,45 @@ __device__ __forceinline__ uint32_t mbar_test_wait(void* bar, uint32_t parity) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok;
+}
+
+}  // namespace tc
+}  // namespace kda
+
+namespace kda {
+namespace tc {
+
+// ---- bulk copies between shared and global memory ----------------------------------------
+// Store `bytes` (multiple of 16) of this CTA's shared memory to global memory, tracked in
+// the issuing thread's current bulk group.
+__device__ __forceinline__ void bulk_store_s2g(void* gdst, uint32_t src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(gdst), "r"(src_smem), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every bulk group of this thread has completed (its writes are performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Wait until every bulk group of this thread has finished reading its source.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Load `bytes` (multiple of 16) from global memory into this CTA's shared memory;
+// completion is counted as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load_g2s(uint32_t dst_smem, const void* gsrc, uint32_t bytes, void* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst_smem), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+// Order this thread's global accesses between the generic and the async proxy.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Non-blocking probe with cluster-scope acquire (phases completed by remote arrivals).
+__device__ __forceinline__ uint32_t mbar_test_wait_cluster(void* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.b32 %0, 1, 0, p;\n\t}\n"
         : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
     return ok;
