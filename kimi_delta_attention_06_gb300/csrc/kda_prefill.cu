@@ -33,11 +33,12 @@
 //
 // Work decomposition: one thread-block cluster of 4 CTAs per (sequence, head).
 //   * CTA 0 (chain): owns the fp32 state (Dk x Dv, one row per thread, in
-//     registers for the whole sequence) and runs the sequential part as two
-//     dependent MMA steps per chunk: [U; O] = [T; Mqk] V + [-W; Q'] S, then
-//     K^^T U for the update.  The value columns of the recurrence never mix,
-//     so its two warpgroups each carry 64 of them through their own MMAs and
-//     barriers and never wait for each other.
+//     registers for the whole sequence; two warpgroups split the value
+//     columns) and runs the sequential part as two dependent MMA steps per
+//     chunk: [U; O] = [T; Mqk] V + [-W; Q'] S, then K^^T U for the update.
+//     The state-free [T; Mqk] V part of a chunk is issued as soon as its
+//     block has landed, into a second TMEM accumulator, so only the S part
+//     sits on the sequential path.  O leaves through a TMA store.
 //   * CTAs 1-3 (prep): chunk c is prepared by CTA 1 + c % 3.  Its inputs
 //     arrive by TMA; it builds [-W; Q'], K^, [T; Mqk], V (fp16) and exp(g_C)
 //     in its own shared memory and bulk-stores each part, as soon as it is
@@ -103,11 +104,12 @@ constexpr uint32_t P_END = P_Y + 32 * LH * 2;
 // Chain CTA shared memory.
 constexpr uint32_t K_SLOT = 0;                       // 2 hand-off slots
 constexpr uint32_t K_S = 2 * H_STRIDE;               // S f16, 128 rows (channel) x 128 N, MN-major (32 KB)
-constexpr uint32_t K_XU = K_S + 32768;               // U f16, 64 rows (token) x 128 N, MN-major (16 KB)
-constexpr uint32_t K_BAR = K_XU + 16384;             // mbarriers (indices below)
-constexpr int KB_MMA = 0;      // [2] MMA completion, one per warpgroup
+// (U, 64 tokens x 128 N f16 MN-major, reuses the V tile of its slot once [T; Mqk] V is done)
+constexpr uint32_t K_O = K_S + 32768;                // O bf16 staging, 64 tokens x 64 columns per warpgroup (2 x 8 KB)
+constexpr uint32_t K_BAR = K_O + 16384;              // mbarriers (indices below)
+constexpr int KB_MMA = 0;      // [1] MMA completion (index 1 unused)
 constexpr int KB_FULL = 2;     // [2] slot loaded
-constexpr int KB_CONS = 4;     // [2] slot consumed by every active warpgroup
+constexpr int KB_CONS = 4;     // [2] slot consumed
 constexpr int KB_READY = 6;    // [6] ring entry stored by its prep CTA
 constexpr int KB_COUNT = 12;
 constexpr uint32_t K_TMEM = K_BAR + 8 * KB_COUNT;
@@ -118,12 +120,14 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // TMEM columns.
 constexpr uint32_t TM_G1 = 0, TM_M = 64, TM_W = 128, TM_PREP_COLS = 256;    // prep CTA
-constexpr uint32_t TM_D1 = 0, TM_D3 = 128, TM_CHAIN_COLS = 256;             // chain CTA
+// chain CTA: [U; O] of chunk c in TM_D1[c % 2], so the next chunk's V part can start early
+constexpr uint32_t TM_D1A = 0, TM_D3 = 128, TM_D1B = 256, TM_CHAIN_COLS = 512;
 
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct TensorMaps {
     CUtensorMap q, k, la, v;     // 2-D views [tokens, H * D]; box = one head x 64 tokens
+    CUtensorMap o;               // bf16 output [tokens, H * Dv]; box = 64 columns x 64 tokens, 128B swizzle
 };
 
 struct Params {
@@ -652,29 +656,15 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
 // ============================================================================
 // Chain CTA: the sequential state recurrence of one (sequence, head).
 // ============================================================================
-// Named barrier of warpgroup wg (ids 2 and 3), with the tcgen05 ordering fences.
-__device__ __forceinline__ void wg_sync_tc(uint32_t bar_id) {
-    tc::fence_before_sync();
-    tc::named_sync(bar_id, 128);
-    tc::fence_after_sync();
-}
-__device__ __forceinline__ bool wg_wait(void* bar, uint32_t parity, uint32_t bar_id) {
-    const uint32_t ok = tc::mbar_wait_bounded(bar, parity, kWaitLimitNs);
-    const uint32_t all = tc::named_sync_and(bar_id, 128, ok);
-    tc::fence_after_sync();
-    return all != 0;
-}
-
-__device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, int len, size_t cl) {
+__device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm, int n, int h, int t0, int len,
+                           size_t cl) {
     uint8_t* Sb = sm + K_S;
-    uint8_t* XU = sm + K_XU;
     uint64_t* mb = reinterpret_cast<uint64_t*>(sm + K_BAR);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + K_TMEM);
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int d = tid & 127;                 // state row = TMEM lane
     const int wg = tid >> 7;                 // value columns 64 wg .. 64 wg + 63
-    const uint32_t bar_wg = 2u + static_cast<uint32_t>(wg);
     const int H = p.H, dk = p.dk, dv = p.dv;
     const bool col_ok = 64 * wg < dv;
     const size_t vtok_stride = static_cast<size_t>(H) * dv;
@@ -685,6 +675,9 @@ __device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, i
     const uint32_t tm = *s_tmem;
     const uint32_t lane_base = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t cb = static_cast<uint32_t>(64 * wg);      // this warpgroup's TMEM column offset
+    uint8_t* Ot = sm + K_O + 8192 * wg;                        // this warpgroup's O staging tile
+    const uint32_t bar_o = 2u + static_cast<uint32_t>(wg);   // named barrier of its 64 O writers
+    constexpr int O_ISSUER = 64;                               // O writer (per warpgroup) that issues the TMA store
     const uint32_t prep_free = tc::smem_u32(sm + P_BAR + 8);  // local offset of the prep CTAs' ring barriers
     const uint8_t* ring = p.ws + cl * WS_BYTES_PER_CLUSTER;
 
@@ -708,7 +701,7 @@ __device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, i
     }
 
     // Loader (thread 0): chunk j goes from ring entry j % 6 into slot j % 2 once its prep
-    // CTA has stored it and every warpgroup is done with chunk j - 2.  Loads are issued
+    // CTA has stored it and the chain is done with chunk j - 2.  Loads are issued
     // in order; `issued` counts them.  Non-blocking probes run between thread 0's other
     // duties so that the next chunk is normally in flight long before it is needed.
     int issued = 0;
@@ -738,91 +731,132 @@ __device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, i
 
     uint32_t ph_mma = 0;
     bool ok = true;
-    int waited = 0;                           // chunks whose slot this warpgroup has waited for
-    for (int c = 0; col_ok && c < nchunks; ++c) {
+    int waited = 0;                           // chunks whose slot the CTA has waited for
+    int v_issued = 0;                         // chunks whose V part ([T; Mqk] V) is issued (thread 0)
+    const int Nmma = dv;                      // 64 or 128 value columns per MMA
+    // [U; O] = [T; Mqk] V for chunk j, into TM_D1[j % 2]
+    auto issue_vpart = [&](int j) {
+        const uint8_t* sl = sm + K_SLOT + (j & 1) * H_STRIDE;
+        issue_mma<true>(tm + ((j & 1) ? TM_D1B : TM_D1A), 128, Nmma, C, tc::smem_u32(sl + H_QT), false, 128,
+                        tc::smem_u32(sl + H_V), true, 64u * 128u);
+        v_issued = j + 1;
+    };
+    for (int c = 0; c < nchunks; ++c) {
         const int cs = t0 + c * C;
         const int nv = min(C, len - c * C);
         const int s = c & 1;
         uint8_t* slot = sm + K_SLOT + s * H_STRIDE;
+        const uint32_t d1 = (s ? TM_D1B : TM_D1A);
         if (tid == 0) {
             if (issued == c && load_ok) load_ok = load(c, true);
             probe(c + 2);
         }
-        if (!wg_wait(&mb[KB_FULL + s], (c >> 1) & 1, bar_wg)) { ok = false; break; }
+        if (!cta_wait(&mb[KB_FULL + s], (c >> 1) & 1, false)) { ok = false; break; }
         waited = c + 1;
-        // the ring entry is free again: its prep CTA may store chunk c + 6 there
-        if (tid == 0 && c + WS_SLOTS < nchunks)
-            tc::mbar_arrive_remote_relaxed(tc::mapa(prep_free + 8u * ((c / NPREP_CTAS) & 1), 1 + c % NPREP_CTAS));
+        if (tid == 0) {
+            // the ring entry is free again: its prep CTA may store chunk c + 6 there
+            if (c + WS_SLOTS < nchunks)
+                tc::mbar_arrive_remote_relaxed(tc::mapa(prep_free + 8u * ((c / NPREP_CTAS) & 1), 1 + c % NPREP_CTAS));
+            if (v_issued == c) issue_vpart(c);
+        }
         const float gc = reinterpret_cast<const float*>(slot + H_EGC)[d];
 
-        // -- [U; O] = [T; Mqk] V + [-W; Q'] S  (one accumulator, this warpgroup's 64 columns) --
+        // -- [U; O] = [T; Mqk] V + [-W; Q'] S  (one accumulator) --
 #pragma unroll
         for (int j = 0; j < 64; j += 8) st_h8(Sb, d, 64 * wg + j, 128, S + j);
         tc::fence_smem_to_async();
-        wg_sync_tc(bar_wg);
-        if (d == 0) {
-            issue_mma<true>(tm + TM_D1 + cb, 128, 64, C, tc::smem_u32(slot + H_QT), false, 128,
-                            tc::smem_u32(slot + H_V) + 8192u * wg, true, 64u * 128u);
-            issue_mma<true>(tm + TM_D1 + cb, 128, 64, DK, tc::smem_u32(slot + H_AH), false, 128,
-                            tc::smem_u32(Sb) + 16384u * wg, true, 128u * 128u, true);
-            tc::mma_commit(&mb[KB_MMA + wg]);
+        cta_sync_tc();
+        if (tid == 0) {
+            issue_mma<true>(tm + d1, 128, Nmma, DK, tc::smem_u32(slot + H_AH), false, 128,
+                            tc::smem_u32(Sb), true, 128u * 128u, true);
+            tc::mma_commit(&mb[KB_MMA]);
+            probe(c + 2);
         }
-        if (tid == 0) probe(c + 2);
-        if (!wg_wait(&mb[KB_MMA + wg], ph_mma & 1, bar_wg)) { ok = false; break; }
+        if (!cta_wait(&mb[KB_MMA], ph_mma & 1, false)) { ok = false; break; }
         ++ph_mma;
-        if (d < 64) {                                    // U -> MN-major f16 tile
+        if (d < 64 && col_ok) {   // U -> MN-major f16 tile, over the (now dead) V tile of the slot
             float r[32];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                tmem_ld32(lane_base + TM_D1 + cb + 32 * half, r);
+                tmem_ld32(lane_base + d1 + cb + 32 * half, r);
 #pragma unroll
-                for (int j = 0; j < 32; j += 8) st_h8(XU, d, 64 * wg + 32 * half + j, 64, r + j);
+                for (int j = 0; j < 32; j += 8) st_h8(slot + H_V, d, 64 * wg + 32 * half + j, 64, r + j);
             }
             tc::fence_smem_to_async();                   // only the U writers touched shared memory
         }
-        wg_sync_tc(bar_wg);
+        cta_sync_tc();
 
         // -- D3 = K^^T U  (K^ tile as an MN-major A: M = channel, K = token) --
-        if (d == 0) {
-            issue_mma<true>(tm + TM_D3 + cb, 128, 64, C, tc::smem_u32(slot + H_KH), true, 64u * 128u,
-                            tc::smem_u32(XU) + 8192u * wg, true, 64u * 128u);
-            tc::mma_commit(&mb[KB_MMA + wg]);
+        if (tid == 0) {
+            issue_mma<true>(tm + TM_D3, 128, Nmma, C, tc::smem_u32(slot + H_KH), true, 64u * 128u,
+                            tc::smem_u32(slot + H_V), true, 64u * 128u);
+            tc::mma_commit(&mb[KB_MMA]);
+            // the next chunk's V part can run now if its slot has landed
+            if (c + 1 < nchunks && tc::mbar_test_wait(&mb[KB_FULL + (s ^ 1)], ((c + 1) >> 1) & 1)) issue_vpart(c + 1);
+            probe(c + 2);
         }
-        if (tid == 0) probe(c + 2);
-        if (d >= 64) {                                   // O rows to global memory while D3 runs
+        if (d >= 64 && col_ok) {                         // O rows (TMEM lanes 64..127) while D3 runs
             const int t = d - 64;
-            const size_t ob = static_cast<size_t>(cs + t) * vtok_stride + static_cast<size_t>(h) * dv + 64 * wg;
+            const uint32_t oaddr = lane_base + d1 + cb;
+            if (!p.out_f32 && nv == C) {
+                // staged as a 128B-swizzled bf16 tile per warpgroup, written out by one TMA store
+                if (d == O_ISSUER) tc::bulk_wait_read_all();       // the previous store has read the tile
+                tc::named_sync(bar_o, 64);
 #pragma unroll
-            for (int c16 = 0; c16 < 64; c16 += 16) {
-                float a[16];
-                tc::tmem_ld16(lane_base + TM_D1 + cb + c16, a);
-                tc::tmem_wait_ld();
-                if (t < nv) {
-                    if (p.out_f32) {
-                        float* op = reinterpret_cast<float*>(p.out) + ob + c16;
+                for (int h32 = 0; h32 < 64; h32 += 32) {
+                    float a[32];
+                    tmem_ld32(oaddr + h32, a);
 #pragma unroll
-                        for (int j = 0; j < 16; j += 4)
-                            *reinterpret_cast<float4*>(op + j) = make_float4(a[j], a[j + 1], a[j + 2], a[j + 3]);
-                    } else {
-                        uint16_t* op = reinterpret_cast<uint16_t*>(p.out) + ob + c16;
+                    for (int j = 0; j < 32; j += 8) {
+                        uint4 w;
+                        w.x = f32x2_to_bf16x2_bits(a[j], a[j + 1]);
+                        w.y = f32x2_to_bf16x2_bits(a[j + 2], a[j + 3]);
+                        w.z = f32x2_to_bf16x2_bits(a[j + 4], a[j + 5]);
+                        w.w = f32x2_to_bf16x2_bits(a[j + 6], a[j + 7]);
+                        *reinterpret_cast<uint4*>(Ot + tc::sw128_off16(t, h32 + j, 64)) = w;
+                    }
+                }
+                tc::fence_smem_to_async();
+                tc::named_sync(bar_o, 64);
+                if (d == O_ISSUER) {
+                    tc::tma_store_2d(&tmaps.o, tc::smem_u32(Ot), h * dv + 64 * wg, cs);
+                    tc::bulk_commit();
+                }
+            } else {
+                const size_t ob = static_cast<size_t>(cs + t) * vtok_stride + static_cast<size_t>(h) * dv + 64 * wg;
 #pragma unroll
-                        for (int j = 0; j < 16; j += 8) {
-                            uint4 w;
-                            w.x = f32x2_to_bf16x2_bits(a[j], a[j + 1]);
-                            w.y = f32x2_to_bf16x2_bits(a[j + 2], a[j + 3]);
-                            w.z = f32x2_to_bf16x2_bits(a[j + 4], a[j + 5]);
-                            w.w = f32x2_to_bf16x2_bits(a[j + 6], a[j + 7]);
-                            *reinterpret_cast<uint4*>(op + j) = w;
+                for (int c16 = 0; c16 < 64; c16 += 16) {
+                    float a[16];
+                    tc::tmem_ld16(oaddr + c16, a);
+                    tc::tmem_wait_ld();
+                    if (t < nv) {
+                        if (p.out_f32) {
+                            float* op = reinterpret_cast<float*>(p.out) + ob + c16;
+#pragma unroll
+                            for (int j = 0; j < 16; j += 4)
+                                *reinterpret_cast<float4*>(op + j) = make_float4(a[j], a[j + 1], a[j + 2], a[j + 3]);
+                        } else {
+                            uint16_t* op = reinterpret_cast<uint16_t*>(p.out) + ob + c16;
+#pragma unroll
+                            for (int j = 0; j < 16; j += 8) {
+                                uint4 w;
+                                w.x = f32x2_to_bf16x2_bits(a[j], a[j + 1]);
+                                w.y = f32x2_to_bf16x2_bits(a[j + 2], a[j + 3]);
+                                w.z = f32x2_to_bf16x2_bits(a[j + 4], a[j + 5]);
+                                w.w = f32x2_to_bf16x2_bits(a[j + 6], a[j + 7]);
+                                *reinterpret_cast<uint4*>(op + j) = w;
+                            }
                         }
                     }
                 }
             }
         }
-        if (!wg_wait(&mb[KB_MMA + wg], ph_mma & 1, bar_wg)) { ok = false; break; }
+        if (!cta_wait(&mb[KB_MMA], ph_mma & 1, false)) { ok = false; break; }
         ++ph_mma;
-        // this warpgroup is done with slot s
-        if (d == 0) tc::mbar_arrive(&mb[KB_CONS + s]);
-        if (tid == 0) probe(c + 3);
+        if (tid == 0) {
+            tc::mbar_arrive(&mb[KB_CONS + s]);           // slot s is consumed
+            probe(c + 3);
+        }
         {
             float r[32];
 #pragma unroll
@@ -836,7 +870,7 @@ __device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, i
         if (p.ckpt && p.ckpt_stride > 0) {
             const int done = c * C + nv;
             if (done % p.ckpt_stride == 0 || done == len) {
-                if (d < dk) {
+                if (d < dk && col_ok) {
                     float* cp = p.ckpt + ((static_cast<size_t>(slot_ck) * H + h) * dk + d) * dv + 64 * wg;
 #pragma unroll
                     for (int j = 0; j < 64; j += 4)
@@ -845,6 +879,13 @@ __device__ void chain_role(const Params& p, uint8_t* sm, int n, int h, int t0, i
                 ++slot_ck;
             }
         }
+    }
+    // O tiles must stay until their stores have read them; the MMAs thread 0 issued
+    // (possibly a V part of a chunk the loop never reached) must finish before TMEM is freed
+    if (d == O_ISSUER) tc::bulk_wait_all();
+    if (tid == 0) {
+        tc::mma_commit(&mb[KB_MMA]);
+        tc::mbar_wait_bounded(&mb[KB_MMA], ph_mma & 1, kWaitLimitNs);
     }
     if (tid == 0) {
         // loads still in flight must land before this CTA's shared memory goes away
@@ -877,8 +918,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_kernel(const Params p, cons
     if (threadIdx.x == 0) {
         if (rank == 0) {
             uint64_t* mb = reinterpret_cast<uint64_t*>(sm + K_BAR);
-            for (int i = 0; i < KB_COUNT; ++i)      // a slot is consumed once per active warpgroup
-                tc::mbar_init(&mb[i], (i == KB_CONS || i == KB_CONS + 1) ? (p.dv > 64 ? 2u : 1u) : 1u);
+            for (int i = 0; i < KB_COUNT; ++i) tc::mbar_init(&mb[i], 1);
         } else {
             uint64_t* mb = reinterpret_cast<uint64_t*>(sm + P_BAR);
             for (int i = 0; i < 4; ++i) tc::mbar_init(&mb[i], 1);
@@ -886,7 +926,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_kernel(const Params p, cons
         tc::mbar_fence_init();
     }
     tc::cluster_sync();
-    if (rank == 0) chain_role(p, sm, n, h, t0, len, static_cast<size_t>(cl));
+    if (rank == 0) chain_role(p, tmaps, sm, n, h, t0, len, static_cast<size_t>(cl));
     else prep_role(p, tmaps, sm, rank - 1, h, t0, len, static_cast<size_t>(cl));
     // no CTA leaves while a peer may still address its shared memory
     tc::cluster_sync();
@@ -912,8 +952,9 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D map over a [rows, cols] row-major tensor; box = box_cols x 64 rows, no swizzle.
-bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esz, long long rows, long long cols, int box_cols) {
+// 2-D map over a [rows, cols] row-major tensor; box = box_cols x 64 rows.
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esz, long long rows, long long cols, int box_cols,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -921,7 +962,7 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esz,
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), 64u};
     const cuuint32_t estr[2] = {1u, 1u};
     return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -960,6 +1001,10 @@ int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
             !make_map(&tmaps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, total_tokens, static_cast<long long>(H) * Dk, Dk) ||
             !make_map(&tmaps.la, la, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, total_tokens, static_cast<long long>(H) * Dk, Dk) ||
             !make_map(&tmaps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, total_tokens, static_cast<long long>(H) * Dv, Dv))
+            return -3;
+        memset(&tmaps.o, 0, sizeof(tmaps.o));   // fp32 output is written with plain stores
+        if (!out_f32 && !make_map(&tmaps.o, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, total_tokens,
+                                  static_cast<long long>(H) * Dv, 64, CU_TENSOR_MAP_SWIZZLE_128B))
             return -3;
     } else {
         memset(&tmaps, 0, sizeof(tmaps));     // never dereferenced: no sequence has a chunk
