@@ -83,6 +83,10 @@ typedef enum { KDA_OUT_BF16 = 0, KDA_OUT_F32 = 1 } kda_out_dtype;
  *               j = 1 .. ceil(len / ckpt_stride) - 1, then the state at its end.
  *   ckpt_stride tokens between checkpoints, a positive multiple of 64, or 0 = none.
  *   stream      cudaStream_t (as void*).
+ * Scratch: num_seqs * H * 497664 bytes of device memory for the prep -> chain
+ * hand-off ring, taken stream-ordered on `stream` from a memory pool the library
+ * owns (it keeps what it reserved, so repeated calls reuse it) and given back on
+ * `stream` after the kernel.  Calls on different streams never share scratch.
  * Returns KDA_OK or a negative kda_status.  Deterministic: identical inputs
  * give bit-identical outputs.
  */
@@ -94,6 +98,31 @@ int kda_chunk_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                       void* out, int out_dtype,
                       float* final_state, float* ckpt_states, int ckpt_stride,
                       void* stream);
+
+/*
+ * kda_chunk_prefill_noalloc -- kda_chunk_prefill that allocates nothing.
+ *
+ * The paper has no counterpart for this call: it is an interface variant of this
+ * library for callers that must not allocate (for instance inside stream capture
+ * with allocation disabled).  Arguments, results, determinism and errors are
+ * those of kda_chunk_prefill, except where the scratch comes from: a fixed array
+ * in the library's own device memory (one per device, its address resolved once
+ * per device on first use) that holds the hand-off rings of at most
+ * KDA_NOALLOC_MAX_SEQ_HEADS (sequence, head) pairs.  A call with
+ * num_seqs * H > KDA_NOALLOC_MAX_SEQ_HEADS returns KDA_ERR_UNSUPPORTED before
+ * anything is launched.  All calls on one device share that array, so they must
+ * be ordered with respect to each other (one stream, or explicit
+ * synchronisation between streams).
+ */
+#define KDA_NOALLOC_MAX_SEQ_HEADS 32
+int kda_chunk_prefill_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                              const float* log_alpha, const uint16_t* beta,
+                              const float* init_state,
+                              const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                              int num_seqs, int total_tokens, int H, int Dk, int Dv,
+                              void* out, int out_dtype,
+                              float* final_state, float* ckpt_states, int ckpt_stride,
+                              void* stream);
 
 /*
  * kda_decode_step -- one KDA token for each of N independent sequences.

@@ -9,6 +9,10 @@ namespace kda {
 // Status codes mirrored from include/kda.h (device side).
 constexpr int kStatusTimeout = -4;
 
+// Device scratch of the prefill per (sequence, head): its hand-off ring of six
+// 82944-byte blocks.
+constexpr size_t kPrefillRingBytesPerPair = 6 * 82944;
+
 // Bounded waits give up after this many nanoseconds (about one second).
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 

@@ -26,16 +26,22 @@ namespace {
 // One status word per device (module-scope device variable; no allocation).
 __device__ int g_kda_status = 0;
 
+// Scratch of kda_chunk_prefill_noalloc: the hand-off rings of up to
+// KDA_NOALLOC_MAX_SEQ_HEADS (sequence, head) pairs (module-scope, no allocation).
+__device__ __align__(256) uint8_t g_kda_noalloc_scratch[KDA_NOALLOC_MAX_SEQ_HEADS * kda::kPrefillRingBytesPerPair];
+
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int* g_status_ptr[kMaxDevices] = {};
+uint8_t* g_scratch_ptr[kMaxDevices] = {};
 cudaMemPool_t g_pool[kMaxDevices] = {};   // stream-ordered pool for the prefill hand-off ring
 int g_device_ok[kMaxDevices] = {};   // 0 unknown, 1 supported, -1 unsupported
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Resolve the current device's status word and check it can run sm_103a code.
-int device_setup(int** status) {
+// Resolve the current device's status word (and fixed prefill scratch) and check
+// it can run sm_103a code.
+int device_setup(int** status, uint8_t** scratch = nullptr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return KDA_ERR_UNSUPPORTED;
@@ -48,12 +54,19 @@ int device_setup(int** status) {
         g_device_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
         if (g_device_ok[dev] == 1) {
             void* p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_kda_status) != cudaSuccess) { g_device_ok[dev] = 0; return KDA_ERR_CUDA; }
+            void* sp = nullptr;
+            if (cudaGetSymbolAddress(&p, g_kda_status) != cudaSuccess ||
+                cudaGetSymbolAddress(&sp, g_kda_noalloc_scratch) != cudaSuccess) {
+                g_device_ok[dev] = 0;
+                return KDA_ERR_CUDA;
+            }
             g_status_ptr[dev] = static_cast<int*>(p);
+            g_scratch_ptr[dev] = static_cast<uint8_t*>(sp);
         }
     }
     if (g_device_ok[dev] != 1) return KDA_ERR_UNSUPPORTED;
     *status = g_status_ptr[dev];
+    if (scratch) *scratch = g_scratch_ptr[dev];
     return KDA_OK;
 }
 
@@ -83,6 +96,35 @@ int workspace_pool(cudaMemPool_t* pool) {
 }
 
 bool head_dims_ok(int Dk, int Dv) { return (Dk == 64 || Dk == 128) && (Dv == 64 || Dv == 128); }
+
+// Host-side checks shared by the two prefill entry points.
+int check_prefill_args(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* log_alpha,
+                       const uint16_t* beta, const float* init_state, const int32_t* cu_seqlens,
+                       const int32_t* cu_seqlens_host, int num_seqs, int total_tokens, int H, int Dk, int Dv,
+                       const void* out, int out_dtype, const float* final_state, const float* ckpt_states,
+                       int ckpt_stride) {
+    if (num_seqs < 0 || total_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+    if (out_dtype != KDA_OUT_BF16 && out_dtype != KDA_OUT_F32) return KDA_ERR_INVALID_ARG;
+    if (ckpt_stride < 0 || (ckpt_stride % 64) != 0) return KDA_ERR_INVALID_ARG;
+    if (!head_dims_ok(Dk, Dv)) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs > 0 && (!cu_seqlens || !cu_seqlens_host)) return KDA_ERR_INVALID_ARG;
+    if (num_seqs > 0) {
+        if (cu_seqlens_host[0] != 0 || cu_seqlens_host[num_seqs] != total_tokens) return KDA_ERR_INVALID_ARG;
+        for (int n = 0; n < num_seqs; ++n)
+            if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
+    } else if (total_tokens != 0) {
+        return KDA_ERR_INVALID_ARG;
+    }
+    if (total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta || !out)) return KDA_ERR_INVALID_ARG;
+    if (ckpt_states && ckpt_stride == 0) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, log_alpha, beta, init_state, out, final_state, ckpt_states, cu_seqlens};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p) && p != cu_seqlens) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return KDA_ERR_INVALID_ARG;
+    // 32-bit element offsets inside the kernel stay below 2^31 per row of work
+    if (static_cast<int64_t>(total_tokens) * H * (Dk > Dv ? Dk : Dv) >= (int64_t(1) << 40)) return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
 
 // One thread waits, with a bound, on an mbarrier phase that nothing completes.
 __global__ void expire_wait_kernel(unsigned long long limit_ns, int* status) {
@@ -131,29 +173,11 @@ int kda_chunk_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                       void* out, int out_dtype,
                       float* final_state, float* ckpt_states, int ckpt_stride,
                       void* stream) {
-    if (num_seqs < 0 || total_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
-    if (out_dtype != KDA_OUT_BF16 && out_dtype != KDA_OUT_F32) return KDA_ERR_INVALID_ARG;
-    if (ckpt_stride < 0 || (ckpt_stride % 64) != 0) return KDA_ERR_INVALID_ARG;
-    if (!head_dims_ok(Dk, Dv)) return KDA_ERR_UNSUPPORTED;
-    if (num_seqs > 0 && (!cu_seqlens || !cu_seqlens_host)) return KDA_ERR_INVALID_ARG;
-    if (num_seqs > 0) {
-        if (cu_seqlens_host[0] != 0 || cu_seqlens_host[num_seqs] != total_tokens) return KDA_ERR_INVALID_ARG;
-        for (int n = 0; n < num_seqs; ++n)
-            if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
-    } else if (total_tokens != 0) {
-        return KDA_ERR_INVALID_ARG;
-    }
-    if (total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta || !out)) return KDA_ERR_INVALID_ARG;
-    if (ckpt_states && ckpt_stride == 0) return KDA_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, log_alpha, beta, init_state, out, final_state, ckpt_states, cu_seqlens};
-    for (const void* p : ptrs)
-        if (p && !aligned16(p) && p != cu_seqlens) return KDA_ERR_INVALID_ARG;
-    if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return KDA_ERR_INVALID_ARG;
-    // 32-bit element offsets inside the kernel stay below 2^31 per row of work
-    if (static_cast<int64_t>(total_tokens) * H * (Dk > Dv ? Dk : Dv) >= (int64_t(1) << 40)) return KDA_ERR_INVALID_ARG;
-    if (num_seqs == 0) return KDA_OK;
+    int rc = check_prefill_args(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host, num_seqs,
+                                total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride);
+    if (rc != KDA_OK || num_seqs == 0) return rc;
     int* status = nullptr;
-    int rc = device_setup(&status);
+    rc = device_setup(&status);
     if (rc != KDA_OK) return rc;
     cudaMemPool_t pool = nullptr;
     rc = workspace_pool(&pool);
@@ -167,6 +191,28 @@ int kda_chunk_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                              ws, status, st);
     const bool freed = cudaFreeAsync(ws, st) == cudaSuccess;
     return (rc == 0 && freed) ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_chunk_prefill_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                              const float* log_alpha, const uint16_t* beta,
+                              const float* init_state,
+                              const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                              int num_seqs, int total_tokens, int H, int Dk, int Dv,
+                              void* out, int out_dtype,
+                              float* final_state, float* ckpt_states, int ckpt_stride,
+                              void* stream) {
+    int rc = check_prefill_args(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host, num_seqs,
+                                total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride);
+    if (rc != KDA_OK || num_seqs == 0) return rc;
+    if (static_cast<int64_t>(num_seqs) * H > KDA_NOALLOC_MAX_SEQ_HEADS) return KDA_ERR_UNSUPPORTED;
+    int* status = nullptr;
+    uint8_t* scratch = nullptr;
+    rc = device_setup(&status, &scratch);
+    if (rc != KDA_OK) return rc;
+    rc = kda::launch_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, num_seqs, total_tokens, H, Dk, Dv,
+                             out, out_dtype == KDA_OUT_F32, final_state, ckpt_states, ckpt_stride,
+                             scratch, status, static_cast<cudaStream_t>(stream));
+    return rc == 0 ? KDA_OK : KDA_ERR_CUDA;
 }
 
 int kda_decode_step(const uint16_t* q, const uint16_t* k, const uint16_t* v,

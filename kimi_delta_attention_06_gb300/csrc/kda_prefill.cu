@@ -79,6 +79,7 @@ static_assert(H_BYTES % (8 * 16) == 0, "hand-off splits into 8 16-byte-multiple 
 constexpr uint32_t H_STRIDE = 82944;         // slot pitch (1024-aligned)
 constexpr int WS_SLOTS = 6;                  // global ring entries per cluster (two per prep CTA)
 constexpr size_t WS_BYTES_PER_CLUSTER = static_cast<size_t>(WS_SLOTS) * H_STRIDE;
+static_assert(WS_BYTES_PER_CLUSTER == kPrefillRingBytesPerPair, "ring size is part of the host interface");
 
 // Prep CTA shared memory.
 constexpr uint32_t P_A1 = 0;                 // [Km; Qm] tf32, 128 rows x 128 K, K-major  (64 KB)

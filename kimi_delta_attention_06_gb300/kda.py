@@ -1,8 +1,9 @@
 """Thin ctypes binding of the KDA C ABI (include/kda.h).
 
 The functions named like the C entry points (``kda_chunk_prefill``,
-``kda_decode_step``, ``kda_ckpt_count``, ``kda_device_status``,
-``kda_status_string``, ``kda_chunk_size``) only marshal arguments: torch
+``kda_chunk_prefill_noalloc``, ``kda_decode_step``, ``kda_ckpt_count``,
+``kda_device_status``, ``kda_status_string``, ``kda_chunk_size``) only marshal
+arguments: torch
 tensors become raw device pointers, the current torch stream becomes the
 ``stream`` argument, and a negative status raises ``KdaError``.  ``prefill``
 and ``decode_step`` additionally allocate the output tensors with torch.
@@ -31,6 +32,7 @@ KDA_ERR_CUDA = -3
 KDA_ERR_TIMEOUT = -4
 KDA_OUT_BF16 = 0
 KDA_OUT_F32 = 1
+KDA_NOALLOC_MAX_SEQ_HEADS = 32
 
 _vp = ctypes.c_void_p
 _i = ctypes.c_int
@@ -55,9 +57,10 @@ def load():
                 raise RuntimeError(f"KDA CUDA library not built: {_LIB_PATH} is missing "
                                    "(run kimi_delta_attention_06_gb300.build.build())")
             lib = ctypes.CDLL(_LIB_PATH)
-            lib.kda_chunk_prefill.restype = _i
-            lib.kda_chunk_prefill.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
-                                              _i, _i, _i, _i, _i, _vp, _i, _vp, _vp, _i, _vp]
+            for name in ("kda_chunk_prefill", "kda_chunk_prefill_noalloc"):
+                fn = getattr(lib, name)
+                fn.restype = _i
+                fn.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp, _vp, _i, _vp]
             lib.kda_decode_step.restype = _i
             lib.kda_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]
             lib.kda_ckpt_count.restype = ctypes.c_int64
@@ -117,17 +120,31 @@ def kda_ckpt_count(cu_seqlens_host: torch.Tensor, ckpt_stride: int) -> int:
     return int(n)
 
 
-def kda_chunk_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host,
-                      num_seqs: int, total_tokens: int, H: int, Dk: int, Dv: int,
-                      out, out_dtype: int, final_state, ckpt_states, ckpt_stride: int, stream=None):
+def _call_prefill(name, q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host, num_seqs,
+                  total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, stream):
     cu_host = cu_seqlens_host.to(device="cpu", dtype=torch.int32).contiguous()
-    rc = load().kda_chunk_prefill(
+    rc = getattr(load(), name)(
         _ptr(_bits16(q)), _ptr(_bits16(k)), _ptr(_bits16(v)), _ptr(log_alpha), _ptr(_bits16(beta)),
         _ptr(init_state), _ptr(cu_seqlens), ctypes.c_void_p(cu_host.data_ptr()),
         int(num_seqs), int(total_tokens), int(H), int(Dk), int(Dv),
         _ptr(out), int(out_dtype), _ptr(final_state), _ptr(ckpt_states), int(ckpt_stride),
         _stream(stream))
-    _check(rc, "kda_chunk_prefill")
+    _check(rc, name)
+
+
+def kda_chunk_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host,
+                      num_seqs: int, total_tokens: int, H: int, Dk: int, Dv: int,
+                      out, out_dtype: int, final_state, ckpt_states, ckpt_stride: int, stream=None):
+    _call_prefill("kda_chunk_prefill", q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host,
+                  num_seqs, total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, stream)
+
+
+def kda_chunk_prefill_noalloc(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host,
+                              num_seqs: int, total_tokens: int, H: int, Dk: int, Dv: int,
+                              out, out_dtype: int, final_state, ckpt_states, ckpt_stride: int, stream=None):
+    _call_prefill("kda_chunk_prefill_noalloc", q, k, v, log_alpha, beta, init_state, cu_seqlens,
+                  cu_seqlens_host, num_seqs, total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states,
+                  ckpt_stride, stream)
 
 
 def kda_decode_step(q, k, v, log_alpha, beta, state, out, out_dtype: int,

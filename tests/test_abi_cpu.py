@@ -32,8 +32,8 @@ def _declared_functions():
 
 def test_header_declares_expected_entry_points():
     names = _declared_functions()
-    for n in ["kda_chunk_prefill", "kda_decode_step", "kda_ckpt_count", "kda_device_status",
-              "kda_status_string", "kda_chunk_size", "kda_debug_expire_wait"]:
+    for n in ["kda_chunk_prefill", "kda_chunk_prefill_noalloc", "kda_decode_step", "kda_ckpt_count",
+              "kda_device_status", "kda_status_string", "kda_chunk_size", "kda_debug_expire_wait"]:
         assert n in names
 
 
@@ -60,14 +60,14 @@ def test_ckpt_count_matches_policy(lib):
         kda.kda_ckpt_count(torch.tensor([0, 5, 3], dtype=torch.int32), 64)
 
 
-def _prefill_raw(lib, **over):
-    """Call kda_chunk_prefill with fake (never dereferenced) aligned pointers."""
+def _prefill_raw(lib, fn="kda_chunk_prefill", **over):
+    """Call a prefill entry point with fake (never dereferenced) aligned pointers."""
     cu = (ctypes.c_int32 * 3)(0, 64, 100)
     a = dict(q=0x1000, k=0x2000, v=0x3000, la=0x4000, beta=0x5000, s0=None, cu=0x6000,
              cu_host=ctypes.cast(cu, ctypes.c_void_p), N=2, T=100, H=2, Dk=64, Dv=64,
              out=0x7000, out_dtype=0, fin=None, ck=None, stride=0, stream=None)
     a.update(over)
-    return lib.kda_chunk_prefill(a["q"], a["k"], a["v"], a["la"], a["beta"], a["s0"], a["cu"],
+    return getattr(lib, fn)(a["q"], a["k"], a["v"], a["la"], a["beta"], a["s0"], a["cu"],
                                  a["cu_host"], a["N"], a["T"], a["H"], a["Dk"], a["Dv"], a["out"],
                                  a["out_dtype"], a["fin"], a["ck"], a["stride"], a["stream"])
 
@@ -89,6 +89,15 @@ def test_prefill_rejects_bad_arguments_on_host(lib):
     assert _prefill_raw(lib, cu_host=ctypes.cast(start, ctypes.c_void_p)) == kda.KDA_ERR_INVALID_ARG
     assert _prefill_raw(lib, N=-1) == kda.KDA_ERR_INVALID_ARG
     assert _prefill_raw(lib, N=0, T=0) == kda.KDA_OK                     # nothing to do
+
+
+def test_noalloc_prefill_rejects_on_host(lib):
+    f = "kda_chunk_prefill_noalloc"
+    # more (sequence, head) pairs than its fixed scratch holds: refused before any device call
+    assert _prefill_raw(lib, fn=f, H=kda.KDA_NOALLOC_MAX_SEQ_HEADS) == kda.KDA_ERR_UNSUPPORTED   # 2 x 32 pairs
+    assert _prefill_raw(lib, fn=f, q=None) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill_raw(lib, fn=f, stride=100) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill_raw(lib, fn=f, N=0, T=0) == kda.KDA_OK
 
 
 def test_decode_rejects_bad_arguments_on_host(lib):
