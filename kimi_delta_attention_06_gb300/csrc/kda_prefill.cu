@@ -198,6 +198,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
     for (int j = 0; j < 16; ++j) { r[j] = a[j]; r[16 + j] = b[j]; }
 }
 
+// 64 consecutive TMEM columns of this thread's lane, one completion wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&r)[64]) {
+    float a[16], b[16], c[16], e[16];
+    tc::tmem_ld16(taddr, a);
+    tc::tmem_ld16(taddr + 16u, b);
+    tc::tmem_ld16(taddr + 32u, c);
+    tc::tmem_ld16(taddr + 48u, e);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) { r[j] = a[j]; r[16 + j] = b[j]; r[32 + j] = c[j]; r[48 + j] = e[j]; }
+}
+
 // Store 8 consecutive fp16 values (one 16-byte chunk) of row `row` into a SW128 tile.
 __device__ __forceinline__ void st_h8(uint8_t* tile, uint32_t row, uint32_t col, uint32_t rows, const float* x) {
     uint4 w;
@@ -252,6 +264,7 @@ __device__ __forceinline__ void st_frag(__half* base, int pitch, int r0, int n0,
 __device__ __forceinline__ bool cta_wait(void* bar, uint32_t parity, bool cluster_scope, bool mine = true) {
     const uint32_t ok = cluster_scope ? tc::mbar_wait_cluster_bounded(bar, parity, kWaitLimitNs)
                                       : tc::mbar_wait_bounded(bar, parity, kWaitLimitNs);
+    tc::fence_before_sync();
     const uint32_t all = tc::named_sync_and(BAR_ALL, NT, ok && mine);
     tc::fence_after_sync();
     return all != 0;
@@ -742,6 +755,14 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
                         tc::smem_u32(sl + H_V), true, 64u * 128u);
         v_issued = j + 1;
     };
+    // S as the fp16 B operand of the next chunk's MMA (each thread: its row, its columns);
+    // the barrier of the next slot wait publishes it
+    auto write_sb = [&]() {
+#pragma unroll
+        for (int j = 0; j < 64; j += 8) st_h8(Sb, d, 64 * wg + j, 128, S + j);
+        tc::fence_smem_to_async();
+    };
+    if (nchunks > 0) write_sb();
     for (int c = 0; c < nchunks; ++c) {
         const int cs = t0 + c * C;
         const int nv = min(C, len - c * C);
@@ -759,30 +780,20 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
             if (c + WS_SLOTS < nchunks)
                 tc::mbar_arrive_remote_relaxed(tc::mapa(prep_free + 8u * ((c / NPREP_CTAS) & 1), 1 + c % NPREP_CTAS));
             if (v_issued == c) issue_vpart(c);
-        }
-        const float gc = reinterpret_cast<const float*>(slot + H_EGC)[d];
-
-        // -- [U; O] = [T; Mqk] V + [-W; Q'] S  (one accumulator) --
-#pragma unroll
-        for (int j = 0; j < 64; j += 8) st_h8(Sb, d, 64 * wg + j, 128, S + j);
-        tc::fence_smem_to_async();
-        cta_sync_tc();
-        if (tid == 0) {
+            // -- [U; O] = [T; Mqk] V + [-W; Q'] S  (one accumulator) --
             issue_mma<true>(tm + d1, 128, Nmma, DK, tc::smem_u32(slot + H_AH), false, 128,
                             tc::smem_u32(Sb), true, 128u * 128u, true);
             tc::mma_commit(&mb[KB_MMA]);
             probe(c + 2);
         }
+        const float gc = reinterpret_cast<const float*>(slot + H_EGC)[d];
         if (!cta_wait(&mb[KB_MMA], ph_mma & 1, false)) { ok = false; break; }
         ++ph_mma;
         if (d < 64 && col_ok) {   // U -> MN-major f16 tile, over the (now dead) V tile of the slot
-            float r[32];
+            float r[64];
+            tmem_ld64(lane_base + d1 + cb, r);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                tmem_ld32(lane_base + d1 + cb + 32 * half, r);
-#pragma unroll
-                for (int j = 0; j < 32; j += 8) st_h8(slot + H_V, d, 64 * wg + 32 * half + j, 64, r + j);
-            }
+            for (int j = 0; j < 64; j += 8) st_h8(slot + H_V, d, 64 * wg + j, 64, r + j);
             tc::fence_smem_to_async();                   // only the U writers touched shared memory
         }
         cta_sync_tc();
@@ -801,21 +812,18 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
             const uint32_t oaddr = lane_base + d1 + cb;
             if (!p.out_f32 && nv == C) {
                 // staged as a 128B-swizzled bf16 tile per warpgroup, written out by one TMA store
+                float a[64];
+                tmem_ld64(oaddr, a);
                 if (d == O_ISSUER) tc::bulk_wait_read_all();       // the previous store has read the tile
                 tc::named_sync(bar_o, 64);
 #pragma unroll
-                for (int h32 = 0; h32 < 64; h32 += 32) {
-                    float a[32];
-                    tmem_ld32(oaddr + h32, a);
-#pragma unroll
-                    for (int j = 0; j < 32; j += 8) {
-                        uint4 w;
-                        w.x = f32x2_to_bf16x2_bits(a[j], a[j + 1]);
-                        w.y = f32x2_to_bf16x2_bits(a[j + 2], a[j + 3]);
-                        w.z = f32x2_to_bf16x2_bits(a[j + 4], a[j + 5]);
-                        w.w = f32x2_to_bf16x2_bits(a[j + 6], a[j + 7]);
-                        *reinterpret_cast<uint4*>(Ot + tc::sw128_off16(t, h32 + j, 64)) = w;
-                    }
+                for (int j = 0; j < 64; j += 8) {
+                    uint4 w;
+                    w.x = f32x2_to_bf16x2_bits(a[j], a[j + 1]);
+                    w.y = f32x2_to_bf16x2_bits(a[j + 2], a[j + 3]);
+                    w.z = f32x2_to_bf16x2_bits(a[j + 4], a[j + 5]);
+                    w.w = f32x2_to_bf16x2_bits(a[j + 6], a[j + 7]);
+                    *reinterpret_cast<uint4*>(Ot + tc::sw128_off16(t, j, 64)) = w;
                 }
                 tc::fence_smem_to_async();
                 tc::named_sync(bar_o, 64);
@@ -859,14 +867,12 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
             probe(c + 3);
         }
         {
-            float r[32];
+            float r[64];
+            tmem_ld64(lane_base + TM_D3 + cb, r);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                tmem_ld32(lane_base + TM_D3 + cb + 32 * half, r);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) S[32 * half + j] = gc * S[32 * half + j] + r[j];
-            }
+            for (int j = 0; j < 64; ++j) S[j] = gc * S[j] + r[j];
         }
+        if (c + 1 < nchunks) write_sb();
         // -- prefix-cache checkpoint at stride multiples and at the sequence end --
         if (p.ckpt && p.ckpt_stride > 0) {
             const int done = c * C + nv;
