@@ -1,10 +1,13 @@
 """Run one KDA workload a few times through the C ABI (for profilers and quick timing).
 
   python -m kimi_delta_attention_06_gb300.run_case --what prefill --T 8192 [--H 32] [--D 128] [--reps 2]
+  python -m kimi_delta_attention_06_gb300.run_case --what varlen [--H 32] [--D 128] [--reps 2]
   python -m kimi_delta_attention_06_gb300.run_case --what decode --N 512 [--H 32] [--D 128] [--reps 2]
 
-Inputs are the seeded synthetic tensors of workloads.py, generated on the GPU.
-Prints the CUDA-event time of each repetition.
+Inputs are the seeded synthetic tensors of workloads.py, generated on the GPU
+(varlen: 16 packed sequences of log-uniform length, about 280k tokens).
+Prints the CUDA-event time of each repetition and the median rate of the
+repetitions after the first.
 """
 from __future__ import annotations
 
@@ -17,7 +20,7 @@ from . import build, kda, workloads
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--what", choices=["prefill", "decode"], default="prefill")
+    ap.add_argument("--what", choices=["prefill", "varlen", "decode"], default="prefill")
     ap.add_argument("--T", type=int, default=8192)
     ap.add_argument("--N", type=int, default=512)
     ap.add_argument("--H", type=int, default=32)
@@ -28,18 +31,22 @@ def main(argv=None):
     build.build()
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
-    if a.what == "prefill":
-        c = workloads.single_case(a.T, seed=2, device=dev, H=a.H, D=a.D, ckpt_stride=a.ckpt)
+    if a.what in ("prefill", "varlen"):
+        if a.what == "prefill":
+            c = workloads.single_case(a.T, seed=2, device=dev, H=a.H, D=a.D, ckpt_stride=a.ckpt)
+        else:
+            c = workloads.varlen_case(device=dev, H=a.H, D=a.D, ckpt_stride=a.ckpt)
+        T, N = c.T, c.N
         cu = c.cu_seqlens.to(dev)
-        out = torch.empty(a.T, a.H, a.D, device=dev, dtype=torch.bfloat16)
-        fin = torch.empty(1, a.H, a.D, a.D, device=dev)
+        out = torch.empty(T, a.H, a.D, device=dev, dtype=torch.bfloat16)
+        fin = torch.empty(N, a.H, a.D, a.D, device=dev)
         nck = kda.kda_ckpt_count(c.cu_seqlens, a.ckpt)
         ck = torch.empty(max(nck, 1), a.H, a.D, a.D, device=dev)
 
         def run():
-            kda.kda_chunk_prefill(c.q, c.k, c.v, c.log_alpha, c.beta, c.init_state, cu, c.cu_seqlens, 1, a.T,
+            kda.kda_chunk_prefill(c.q, c.k, c.v, c.log_alpha, c.beta, c.init_state, cu, c.cu_seqlens, N, T,
                                   a.H, a.D, a.D, out, kda.KDA_OUT_BF16, fin, ck if nck else None, a.ckpt, stream)
-        units = f"{a.T} tokens"
+        units, count = f"{T} tokens, {N} sequences", T
     else:
         d = workloads.decode_case(N=a.N, H=a.H, D=a.D, steps=1, seed=4, device=dev)
         s = d.steps[0]
@@ -48,7 +55,8 @@ def main(argv=None):
         def run():
             kda.kda_decode_step(s["q"], s["k"], s["v"], s["log_alpha"], s["beta"], d.state, out,
                                 kda.KDA_OUT_BF16, a.N, a.H, a.D, a.D, stream)
-        units = f"{a.N} sequences"
+        units, count = f"{a.N} sequences", a.N
+    times = []
     for i in range(a.reps):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -56,7 +64,12 @@ def main(argv=None):
         run()
         e1.record(stream)
         torch.cuda.synchronize()
-        print(f"{a.what} rep {i}: {e0.elapsed_time(e1):.3f} ms ({units})")
+        times.append(e0.elapsed_time(e1))
+        print(f"{a.what} rep {i}: {times[-1]:.3f} ms ({units})")
+    if len(times) > 1:
+        med = sorted(times[1:])[(len(times) - 1) // 2]
+        print(f"{a.what} median of reps 1..{len(times) - 1}: {med:.3f} ms = {count / med * 1e3:.4g} "
+              f"{'tokens' if a.what != 'decode' else 'sequences'}/s")
     st = kda.kda_device_status()
     if st != 0:
         raise SystemExit(f"device status {st}")
