@@ -143,6 +143,39 @@ int kda_decode_step(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                     float* state, void* out, int out_dtype,
                     int N, int H, int Dk, int Dv, void* stream);
 
+/*
+ * kda_decode_multi -- serving-shaped decode: states in a slot pool, several tokens
+ * per sequence in one pass (speculative verify / commit).
+ *
+ * Sequence n's state is state_pool[state_slots[n]] (or slot n when state_slots is
+ * NULL).  Its first num_tokens[n] tokens (all K when num_tokens is NULL) are applied
+ * in order, each exactly as one kda_decode_step, with the state held on chip in
+ * between: the state is read once and, when commit != 0, written back once after the
+ * last applied token.  With commit == 0 (verify) the pool is only read, so a caller
+ * can check K draft tokens, then commit the accepted prefix with a second call that
+ * passes num_tokens = the accepted counts.
+ *
+ *   q, k        (device) bf16 [N, K, H, Dk]
+ *   v           (device) bf16 [N, K, H, Dv]
+ *   log_alpha   (device) fp32 [N, K, H, Dk], finite, <= 0
+ *   beta        (device) bf16 [N, K, H]
+ *   state_pool  (device) fp32 [num_slots, H, Dk, Dv]
+ *   state_slots (device) int32 [N] in [0, num_slots), distinct when commit != 0; or NULL
+ *               (then num_slots >= N and sequence n uses slot n)
+ *   num_tokens  (device) int32 [N] in [0, K], or NULL (= K for every sequence)
+ *   out         (device) [N, K, H, Dv], bf16 or fp32 per out_dtype; o for token j of
+ *               sequence n, written for j < num_tokens[n] only.
+ * Dk == Dv in {64, 128}.  Host-side argument errors return as usual; an out-of-range
+ * slot or token count found on the device skips that sequence and makes the next
+ * kda_device_status return KDA_ERR_INVALID_ARG.
+ */
+int kda_decode_multi(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     const float* log_alpha, const uint16_t* beta,
+                     float* state_pool, int num_slots, const int32_t* state_slots,
+                     const int32_t* num_tokens, int commit,
+                     void* out, int out_dtype,
+                     int N, int K, int H, int Dk, int Dv, void* stream);
+
 /* Number of checkpoint slots kda_chunk_prefill writes: sum over sequences of
  * ceil(len / ckpt_stride) (0 when ckpt_stride == 0).  cu_seqlens_host is a host
  * array of num_seqs + 1 offsets.  Returns -1 on invalid arguments. */
@@ -150,8 +183,9 @@ int64_t kda_ckpt_count(const int32_t* cu_seqlens_host, int num_seqs, int ckpt_st
 
 /* Synchronises `stream`, then returns and clears the device status word:
  * KDA_OK, KDA_ERR_TIMEOUT (a bounded wait inside a kernel expired and the
- * kernel returned early; its outputs are undefined), or KDA_ERR_CUDA if the
- * synchronisation itself failed. */
+ * kernel returned early; its outputs are undefined), KDA_ERR_INVALID_ARG (a
+ * device-side index of kda_decode_multi was out of range), or KDA_ERR_CUDA if
+ * the synchronisation itself failed. */
 int kda_device_status(void* stream);
 
 /* Static, NUL-terminated description of a kda_status value. */

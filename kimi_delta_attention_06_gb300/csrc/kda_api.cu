@@ -19,6 +19,10 @@ int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
                    int num_seqs, int total_tokens, int H, int Dk, int Dv, void* out, int out_f32,
                    float* final_state, float* ckpt, int ckpt_stride, void* ws, int* status, cudaStream_t stream);
 size_t prefill_workspace_bytes(int num_seqs, int H);
+int launch_decode_multi(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* log_alpha,
+                        const uint16_t* beta, float* pool, int num_slots, const int32_t* slots,
+                        const int32_t* ntok, int commit, void* out, int out_f32,
+                        int N, int K, int H, int D, int* status, cudaStream_t stream);
 }  // namespace kda
 
 namespace {
@@ -234,6 +238,37 @@ int kda_decode_step(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     if (rc != KDA_OK) return rc;
     rc = kda::launch_decode(q, k, v, log_alpha, beta, state, out, out_dtype == KDA_OUT_F32, N, H, Dk,
                             static_cast<cudaStream_t>(stream));
+    return rc == 0 ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_decode_multi(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     const float* log_alpha, const uint16_t* beta,
+                     float* state_pool, int num_slots, const int32_t* state_slots,
+                     const int32_t* num_tokens, int commit,
+                     void* out, int out_dtype,
+                     int N, int K, int H, int Dk, int Dv, void* stream) {
+    if (N < 0 || K < 0 || H <= 0 || num_slots < 0) return KDA_ERR_INVALID_ARG;
+    if (out_dtype != KDA_OUT_BF16 && out_dtype != KDA_OUT_F32) return KDA_ERR_INVALID_ARG;
+    if (commit != 0 && commit != 1) return KDA_ERR_INVALID_ARG;
+    if (!head_dims_ok(Dk, Dv)) return KDA_ERR_UNSUPPORTED;
+    if (Dk != Dv) return KDA_ERR_UNSUPPORTED;
+    if (N == 0 || K == 0) return KDA_OK;
+    if (!q || !k || !v || !log_alpha || !beta || !state_pool || !out) return KDA_ERR_INVALID_ARG;
+    if (!state_slots && num_slots < N) return KDA_ERR_INVALID_ARG;
+    if (num_slots == 0) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, log_alpha, beta, state_pool, out};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return KDA_ERR_INVALID_ARG;
+    if ((state_slots && (reinterpret_cast<uintptr_t>(state_slots) & 3u)) ||
+        (num_tokens && (reinterpret_cast<uintptr_t>(num_tokens) & 3u)))
+        return KDA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(N) * K * H >= (int64_t(1) << 31) || static_cast<int64_t>(N) * H >= (int64_t(1) << 31))
+        return KDA_ERR_INVALID_ARG;
+    int* status = nullptr;
+    int rc = device_setup(&status);
+    if (rc != KDA_OK) return rc;
+    rc = kda::launch_decode_multi(q, k, v, log_alpha, beta, state_pool, num_slots, state_slots, num_tokens, commit,
+                                  out, out_dtype == KDA_OUT_F32, N, K, H, Dk, status, static_cast<cudaStream_t>(stream));
     return rc == 0 ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -124,6 +124,141 @@ kda_decode_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// Serving-shaped decode (pages: the DSpark speculative decoding of the serving notes, and
+// the prefix-cache state pool of section 5).  Sequence n's state lives in slot
+// slots[n] of a state pool; up to K of its tokens are applied in one pass: the state is
+// read once, stepped K times in registers (each step exactly the single-token update
+// above), and written back once -- or not at all (verify: outputs only, the pool is left
+// untouched so the caller can accept any prefix and commit it with a second call).
+// ---------------------------------------------------------------------------------------
+constexpr int kStatusBadIndex = -1;     // KDA_ERR_INVALID_ARG, recorded on the device
+
+template <int D, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, 2)
+kda_decode_multi_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+                        const uint16_t* __restrict__ v, const float* __restrict__ log_alpha,
+                        const uint16_t* __restrict__ beta, float* __restrict__ pool, int num_slots,
+                        const int32_t* __restrict__ slots, const int32_t* __restrict__ ntok, int commit,
+                        void* __restrict__ out, int out_f32, int K, int H, int* status)
+{
+    using Sh = DecodeShape<D, WARPS>;
+    __shared__ float s_a[D], s_k[D], s_ak[D], s_aq[D], s_u[D];
+    __shared__ float s_red[WARPS][2][D];
+    __shared__ float s_qk[WARPS];
+
+    const int pair = blockIdx.x;                       // n * H + h
+    const int n = pair / H, h = pair - n * H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int slot = slots ? slots[n] : n;
+    const int nt = ntok ? ntok[n] : K;
+    if (slot < 0 || slot >= num_slots || nt < 0 || nt > K) {
+        if (tid == 0) set_status(status, kStatusBadIndex);
+        return;
+    }
+    float4* S = reinterpret_cast<float4*>(pool + (static_cast<size_t>(slot) * H + h) * D * D);
+
+    const int c4 = lane % Sh::kLanesPerRow;
+    const int rsub = lane / Sh::kLanesPerRow;
+    float4 s[Sh::kIters];
+#pragma unroll
+    for (int it = 0; it < Sh::kIters; ++it) {
+        const int r = warp * Sh::kRowsPerWarp + it * Sh::kRowsPerIter + rsub;
+        s[it] = commit ? __ldcs(S + r * Sh::kLanesPerRow + c4) : __ldg(S + r * Sh::kLanesPerRow + c4);
+    }
+
+    for (int j = 0; j < nt; ++j) {
+        const size_t tok = static_cast<size_t>(n) * K + j;          // token row [n][j]
+        const size_t vec = (tok * H + h) * D;                       // its [H, D] vectors
+        float qk_part = 0.f;
+        if (tid < D) {
+            const float qi = bf16_bits_to_f32(q[vec + tid]);
+            const float ki = bf16_bits_to_f32(k[vec + tid]);
+            const float a = expf(log_alpha[vec + tid]);
+            s_a[tid] = a;
+            s_k[tid] = ki;
+            s_ak[tid] = a * ki;
+            s_aq[tid] = a * qi;
+            qk_part = qi * ki;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) qk_part += __shfl_xor_sync(0xffffffffu, qk_part, off);
+        if (lane == 0) s_qk[warp] = qk_part;
+        __syncthreads();
+
+        float4 r1 = make_float4(0.f, 0.f, 0.f, 0.f), r2 = r1;
+#pragma unroll
+        for (int it = 0; it < Sh::kIters; ++it) {
+            const int r = warp * Sh::kRowsPerWarp + it * Sh::kRowsPerIter + rsub;
+            const float ak = s_ak[r], aq = s_aq[r];
+            r1.x += ak * s[it].x; r1.y += ak * s[it].y; r1.z += ak * s[it].z; r1.w += ak * s[it].w;
+            r2.x += aq * s[it].x; r2.y += aq * s[it].y; r2.z += aq * s[it].z; r2.w += aq * s[it].w;
+        }
+#pragma unroll
+        for (int off = Sh::kLanesPerRow; off < 32; off <<= 1) {
+            r1.x += __shfl_xor_sync(0xffffffffu, r1.x, off); r1.y += __shfl_xor_sync(0xffffffffu, r1.y, off);
+            r1.z += __shfl_xor_sync(0xffffffffu, r1.z, off); r1.w += __shfl_xor_sync(0xffffffffu, r1.w, off);
+            r2.x += __shfl_xor_sync(0xffffffffu, r2.x, off); r2.y += __shfl_xor_sync(0xffffffffu, r2.y, off);
+            r2.z += __shfl_xor_sync(0xffffffffu, r2.z, off); r2.w += __shfl_xor_sync(0xffffffffu, r2.w, off);
+        }
+        if (rsub == 0) {
+            *reinterpret_cast<float4*>(&s_red[warp][0][4 * c4]) = r1;
+            *reinterpret_cast<float4*>(&s_red[warp][1][4 * c4]) = r2;
+        }
+        __syncthreads();
+
+        const float b = bf16_bits_to_f32(beta[tok * H + h]);
+        if (tid < D) {
+            float t1 = 0.f, t2 = 0.f, qk = 0.f;
+#pragma unroll
+            for (int w = 0; w < WARPS; ++w) { t1 += s_red[w][0][tid]; t2 += s_red[w][1][tid]; qk += s_qk[w]; }
+            const float u = bf16_bits_to_f32(v[vec + tid]) - t1;
+            s_u[tid] = u;
+            const float ov = t2 + b * qk * u;
+            if (out_f32) reinterpret_cast<float*>(out)[vec + tid] = ov;
+            else reinterpret_cast<uint16_t*>(out)[vec + tid] = f32_to_bf16_bits(ov);
+        }
+        __syncthreads();
+
+        const float4 u4 = *reinterpret_cast<const float4*>(&s_u[4 * c4]);
+#pragma unroll
+        for (int it = 0; it < Sh::kIters; ++it) {
+            const int r = warp * Sh::kRowsPerWarp + it * Sh::kRowsPerIter + rsub;
+            const float a = s_a[r];
+            const float kr = b * s_k[r];
+            s[it].x = a * s[it].x + kr * u4.x;
+            s[it].y = a * s[it].y + kr * u4.y;
+            s[it].z = a * s[it].z + kr * u4.z;
+            s[it].w = a * s[it].w + kr * u4.w;
+        }
+        __syncthreads();       // the shared scalars of this token are dead only now
+    }
+    if (commit && nt > 0) {
+#pragma unroll
+        for (int it = 0; it < Sh::kIters; ++it) {
+            const int r = warp * Sh::kRowsPerWarp + it * Sh::kRowsPerIter + rsub;
+            __stcs(S + r * Sh::kLanesPerRow + c4, s[it]);
+        }
+    }
+}
+
+int launch_decode_multi(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* log_alpha,
+                        const uint16_t* beta, float* pool, int num_slots, const int32_t* slots,
+                        const int32_t* ntok, int commit, void* out, int out_f32,
+                        int N, int K, int H, int D, int* status, cudaStream_t stream)
+{
+    const long long pairs = static_cast<long long>(N) * H;
+    if (pairs == 0) return 0;
+    if (D == 128) {
+        kda_decode_multi_kernel<128, 8><<<static_cast<unsigned>(pairs), 256, 0, stream>>>(
+            q, k, v, log_alpha, beta, pool, num_slots, slots, ntok, commit, out, out_f32, K, H, status);
+    } else {
+        kda_decode_multi_kernel<64, 4><<<static_cast<unsigned>(pairs), 128, 0, stream>>>(
+            q, k, v, log_alpha, beta, pool, num_slots, slots, ntok, commit, out, out_f32, K, H, status);
+    }
+    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
 int launch_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* log_alpha,
                   const uint16_t* beta, float* state, void* out, int out_f32,
                   int N, int H, int D, cudaStream_t stream)

@@ -1,7 +1,7 @@
 """Thin ctypes binding of the KDA C ABI (include/kda.h).
 
 The functions named like the C entry points (``kda_chunk_prefill``,
-``kda_chunk_prefill_noalloc``, ``kda_decode_step``, ``kda_ckpt_count``,
+``kda_chunk_prefill_noalloc``, ``kda_decode_step``, ``kda_decode_multi``, ``kda_ckpt_count``,
 ``kda_device_status``, ``kda_status_string``, ``kda_chunk_size``) only marshal
 arguments: torch
 tensors become raw device pointers, the current torch stream becomes the
@@ -63,6 +63,9 @@ def load():
                 fn.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp, _vp, _i, _vp]
             lib.kda_decode_step.restype = _i
             lib.kda_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]
+            lib.kda_decode_multi.restype = _i
+            lib.kda_decode_multi.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _i,
+                                             _i, _i, _i, _i, _i, _vp]
             lib.kda_ckpt_count.restype = ctypes.c_int64
             lib.kda_ckpt_count.argtypes = [_vp, _i, _i]
             lib.kda_device_status.restype = _i
@@ -153,6 +156,15 @@ def kda_decode_step(q, k, v, log_alpha, beta, state, out, out_dtype: int,
                                 _ptr(_bits16(beta)), _ptr(state), _ptr(out), int(out_dtype),
                                 int(N), int(H), int(Dk), int(Dv), _stream(stream))
     _check(rc, "kda_decode_step")
+
+
+def kda_decode_multi(q, k, v, log_alpha, beta, state_pool, num_slots: int, state_slots, num_tokens,
+                     commit: int, out, out_dtype: int, N: int, K: int, H: int, Dk: int, Dv: int, stream=None):
+    rc = load().kda_decode_multi(_ptr(_bits16(q)), _ptr(_bits16(k)), _ptr(_bits16(v)), _ptr(log_alpha),
+                                 _ptr(_bits16(beta)), _ptr(state_pool), int(num_slots), _ptr(state_slots),
+                                 _ptr(num_tokens), int(commit), _ptr(out), int(out_dtype),
+                                 int(N), int(K), int(H), int(Dk), int(Dv), _stream(stream))
+    _check(rc, "kda_decode_multi")
 
 
 def kda_debug_expire_wait(limit_ns: int, stream=None):

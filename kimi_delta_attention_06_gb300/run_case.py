@@ -3,6 +3,7 @@
   python -m kimi_delta_attention_06_gb300.run_case --what prefill --T 8192 [--H 32] [--D 128] [--reps 2]
   python -m kimi_delta_attention_06_gb300.run_case --what varlen [--H 32] [--D 128] [--reps 2]
   python -m kimi_delta_attention_06_gb300.run_case --what decode --N 512 [--H 32] [--D 128] [--reps 2]
+  python -m kimi_delta_attention_06_gb300.run_case --what decode_multi --N 512 --K 4 [--commit 1] [--reps 2]
 
 Inputs are the seeded synthetic tensors of workloads.py, generated on the GPU
 (varlen: 16 packed sequences of log-uniform length, about 280k tokens).
@@ -20,7 +21,9 @@ from . import build, kda, workloads
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--what", choices=["prefill", "varlen", "decode"], default="prefill")
+    ap.add_argument("--what", choices=["prefill", "varlen", "decode", "decode_multi"], default="prefill")
+    ap.add_argument("--K", type=int, default=4, help="tokens per sequence (decode_multi)")
+    ap.add_argument("--commit", type=int, default=0, help="decode_multi: 1 writes the states back")
     ap.add_argument("--T", type=int, default=8192)
     ap.add_argument("--N", type=int, default=512)
     ap.add_argument("--H", type=int, default=32)
@@ -47,6 +50,16 @@ def main(argv=None):
             kda.kda_chunk_prefill(c.q, c.k, c.v, c.log_alpha, c.beta, c.init_state, cu, c.cu_seqlens, N, T,
                                   a.H, a.D, a.D, out, kda.KDA_OUT_BF16, fin, ck if nck else None, a.ckpt, stream)
         units, count = f"{T} tokens, {N} sequences", T
+    elif a.what == "decode_multi":
+        d = workloads.decode_case(N=a.N, H=a.H, D=a.D, steps=a.K, seed=4, device=dev)
+        tok = {key: torch.stack([s[key] for s in d.steps], dim=1).contiguous()
+               for key in ("q", "k", "v", "log_alpha", "beta")}
+        out = torch.empty(a.N, a.K, a.H, a.D, device=dev, dtype=torch.bfloat16)
+
+        def run():
+            kda.kda_decode_multi(tok["q"], tok["k"], tok["v"], tok["log_alpha"], tok["beta"], d.state, a.N, None,
+                                 None, a.commit, out, kda.KDA_OUT_BF16, a.N, a.K, a.H, a.D, a.D, stream)
+        units, count = f"{a.N} sequences x {a.K} tokens, commit={a.commit}", a.N * a.K
     else:
         d = workloads.decode_case(N=a.N, H=a.H, D=a.D, steps=1, seed=4, device=dev)
         s = d.steps[0]
@@ -69,7 +82,7 @@ def main(argv=None):
     if len(times) > 1:
         med = sorted(times[1:])[(len(times) - 1) // 2]
         print(f"{a.what} median of reps 1..{len(times) - 1}: {med:.3f} ms = {count / med * 1e3:.4g} "
-              f"{'tokens' if a.what != 'decode' else 'sequences'}/s")
+              f"{'sequences' if a.what == 'decode' else 'tokens'}/s")
     st = kda.kda_device_status()
     if st != 0:
         raise SystemExit(f"device status {st}")

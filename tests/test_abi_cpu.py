@@ -32,7 +32,7 @@ def _declared_functions():
 
 def test_header_declares_expected_entry_points():
     names = _declared_functions()
-    for n in ["kda_chunk_prefill", "kda_chunk_prefill_noalloc", "kda_decode_step", "kda_ckpt_count",
+    for n in ["kda_chunk_prefill", "kda_chunk_prefill_noalloc", "kda_decode_step", "kda_decode_multi", "kda_ckpt_count",
               "kda_device_status", "kda_status_string", "kda_chunk_size", "kda_debug_expire_wait"]:
         assert n in names
 
@@ -113,6 +113,25 @@ def test_decode_rejects_bad_arguments_on_host(lib):
     assert f(*a) == kda.KDA_ERR_INVALID_ARG
     a = list(args); a[8] = 0
     assert f(*a) == kda.KDA_OK                                             # N = 0: nothing to do
+
+
+def test_decode_multi_rejects_bad_arguments_on_host(lib):
+    f = lib.kda_decode_multi
+    #       q       k       v       la      beta    pool    slots  sl    ntok  commit out  dt  N  K  H  Dk   Dv  stream
+    args = [0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 8, None, None, 0, 0x7000, 0, 4, 3, 2, 128, 128, None]
+    def call(**kw):
+        a = list(args)
+        for i, val in kw.items():
+            a[int(i[1:])] = val
+        return f(*a)
+    assert call(a0=None) == kda.KDA_ERR_INVALID_ARG
+    assert call(a6=3) == kda.KDA_ERR_INVALID_ARG          # identity slots need num_slots >= N
+    assert call(a9=2) == kda.KDA_ERR_INVALID_ARG          # commit is 0 or 1
+    assert call(a15=64) == kda.KDA_ERR_UNSUPPORTED        # Dk != Dv
+    assert call(a15=96, a16=96) == kda.KDA_ERR_UNSUPPORTED
+    assert call(a5=0x6004) == kda.KDA_ERR_INVALID_ARG     # misaligned pool
+    assert call(a7=0x8002) == kda.KDA_ERR_INVALID_ARG     # misaligned slot array
+    assert call(a12=0) == kda.KDA_OK and call(a13=0) == kda.KDA_OK   # nothing to do
 
 
 def test_binding_refuses_non_bf16(lib):
