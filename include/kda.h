@@ -61,6 +61,13 @@ typedef enum {
 /* Output element type of the attention output `out`. */
 typedef enum { KDA_OUT_BF16 = 0, KDA_OUT_F32 = 1 } kda_out_dtype;
 
+/* Layout of the decay input log_alpha (the KDA lineage: KDA widens Gated DeltaNet's
+ * scalar forget gate to a per-channel diagonal; DeltaNet has none):
+ *   KDA_DECAY_CHANNEL  log_alpha [tokens, H, Dk]  -- KDA, Diag(alpha_t)
+ *   KDA_DECAY_HEAD     log_alpha [tokens, H]      -- Gated DeltaNet, alpha_t I
+ *   KDA_DECAY_NONE     log_alpha unused (NULL)    -- DeltaNet, alpha_t = 1 */
+typedef enum { KDA_DECAY_CHANNEL = 0, KDA_DECAY_HEAD = 1, KDA_DECAY_NONE = 2 } kda_decay;
+
 /*
  * kda_chunk_prefill -- chunked KDA prefill over packed variable-length sequences.
  *
@@ -98,6 +105,24 @@ int kda_chunk_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                       void* out, int out_dtype,
                       float* final_state, float* ckpt_states, int ckpt_stride,
                       void* stream);
+
+/*
+ * kda_chunk_prefill_ex -- kda_chunk_prefill with a choice of decay layout.
+ *
+ * Identical to kda_chunk_prefill when decay == KDA_DECAY_CHANNEL.  With
+ * KDA_DECAY_HEAD, log_alpha is fp32 [total_tokens, H] (one log-decay per head and
+ * token, applied to every channel) and H must be a multiple of 4 (its 16-byte rows are
+ * staged by TMA), else KDA_ERR_UNSUPPORTED.  With KDA_DECAY_NONE, log_alpha must be
+ * NULL and alpha = 1.
+ */
+int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         const float* log_alpha, const uint16_t* beta,
+                         const float* init_state,
+                         const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                         int num_seqs, int total_tokens, int H, int Dk, int Dv,
+                         void* out, int out_dtype,
+                         float* final_state, float* ckpt_states, int ckpt_stride,
+                         int decay, void* stream);
 
 /*
  * kda_chunk_prefill_noalloc -- kda_chunk_prefill that allocates nothing.
@@ -157,7 +182,8 @@ int kda_decode_step(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  *
  *   q, k        (device) bf16 [N, K, H, Dk]
  *   v           (device) bf16 [N, K, H, Dv]
- *   log_alpha   (device) fp32 [N, K, H, Dk], finite, <= 0
+ *   log_alpha   (device) fp32 [N, K, H, Dk] (decay KDA_DECAY_CHANNEL), [N, K, H]
+ *               (KDA_DECAY_HEAD) or NULL (KDA_DECAY_NONE); finite, <= 0
  *   beta        (device) bf16 [N, K, H]
  *   state_pool  (device) fp32 [num_slots, H, Dk, Dv]
  *   state_slots (device) int32 [N] in [0, num_slots), distinct when commit != 0; or NULL
@@ -174,7 +200,7 @@ int kda_decode_multi(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                      float* state_pool, int num_slots, const int32_t* state_slots,
                      const int32_t* num_tokens, int commit,
                      void* out, int out_dtype,
-                     int N, int K, int H, int Dk, int Dv, void* stream);
+                     int N, int K, int H, int Dk, int Dv, int decay, void* stream);
 
 /* Number of checkpoint slots kda_chunk_prefill writes: sum over sequences of
  * ceil(len / ckpt_stride) (0 when ckpt_stride == 0).  cu_seqlens_host is a host

@@ -17,12 +17,13 @@ int launch_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, const
 int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* la,
                    const uint16_t* beta, const float* init_state, const int32_t* cu_seqlens,
                    int num_seqs, int total_tokens, int H, int Dk, int Dv, void* out, int out_f32,
-                   float* final_state, float* ckpt, int ckpt_stride, void* ws, int* status, cudaStream_t stream);
+                   float* final_state, float* ckpt, int ckpt_stride, int decay, void* ws, int* status,
+                   cudaStream_t stream);
 size_t prefill_workspace_bytes(int num_seqs, int H);
 int launch_decode_multi(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* log_alpha,
                         const uint16_t* beta, float* pool, int num_slots, const int32_t* slots,
                         const int32_t* ntok, int commit, void* out, int out_f32,
-                        int N, int K, int H, int D, int* status, cudaStream_t stream);
+                        int N, int K, int H, int D, int decay, int* status, cudaStream_t stream);
 }  // namespace kda
 
 namespace {
@@ -106,8 +107,11 @@ int check_prefill_args(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
                        const uint16_t* beta, const float* init_state, const int32_t* cu_seqlens,
                        const int32_t* cu_seqlens_host, int num_seqs, int total_tokens, int H, int Dk, int Dv,
                        const void* out, int out_dtype, const float* final_state, const float* ckpt_states,
-                       int ckpt_stride) {
+                       int ckpt_stride, int decay) {
     if (num_seqs < 0 || total_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+    if (decay != KDA_DECAY_CHANNEL && decay != KDA_DECAY_HEAD && decay != KDA_DECAY_NONE) return KDA_ERR_INVALID_ARG;
+    if (decay == KDA_DECAY_HEAD && H % 4 != 0) return KDA_ERR_UNSUPPORTED;
+    if (decay == KDA_DECAY_NONE && log_alpha) return KDA_ERR_INVALID_ARG;
     if (out_dtype != KDA_OUT_BF16 && out_dtype != KDA_OUT_F32) return KDA_ERR_INVALID_ARG;
     if (ckpt_stride < 0 || (ckpt_stride % 64) != 0) return KDA_ERR_INVALID_ARG;
     if (!head_dims_ok(Dk, Dv)) return KDA_ERR_UNSUPPORTED;
@@ -119,7 +123,8 @@ int check_prefill_args(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
     } else if (total_tokens != 0) {
         return KDA_ERR_INVALID_ARG;
     }
-    if (total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta || !out)) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q || !k || !v || !beta || !out)) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && decay != KDA_DECAY_NONE && !log_alpha) return KDA_ERR_INVALID_ARG;
     if (ckpt_states && ckpt_stride == 0) return KDA_ERR_INVALID_ARG;
     const void* ptrs[] = {q, k, v, log_alpha, beta, init_state, out, final_state, ckpt_states, cu_seqlens};
     for (const void* p : ptrs)
@@ -169,16 +174,13 @@ const char* kda_status_string(int status) {
     }
 }
 
-int kda_chunk_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                      const float* log_alpha, const uint16_t* beta,
-                      const float* init_state,
-                      const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
-                      int num_seqs, int total_tokens, int H, int Dk, int Dv,
-                      void* out, int out_dtype,
-                      float* final_state, float* ckpt_states, int ckpt_stride,
-                      void* stream) {
+static int prefill_pooled(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* log_alpha,
+                          const uint16_t* beta, const float* init_state, const int32_t* cu_seqlens,
+                          const int32_t* cu_seqlens_host, int num_seqs, int total_tokens, int H, int Dk, int Dv,
+                          void* out, int out_dtype, float* final_state, float* ckpt_states, int ckpt_stride,
+                          int decay, void* stream) {
     int rc = check_prefill_args(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host, num_seqs,
-                                total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride);
+                                total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, decay);
     if (rc != KDA_OK || num_seqs == 0) return rc;
     int* status = nullptr;
     rc = device_setup(&status);
@@ -191,10 +193,34 @@ int kda_chunk_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     if (cudaMallocFromPoolAsync(&ws, kda::prefill_workspace_bytes(num_seqs, H), pool, st) != cudaSuccess)
         return KDA_ERR_CUDA;
     rc = kda::launch_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, num_seqs, total_tokens, H, Dk, Dv,
-                             out, out_dtype == KDA_OUT_F32, final_state, ckpt_states, ckpt_stride,
+                             out, out_dtype == KDA_OUT_F32, final_state, ckpt_states, ckpt_stride, decay,
                              ws, status, st);
     const bool freed = cudaFreeAsync(ws, st) == cudaSuccess;
     return (rc == 0 && freed) ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_chunk_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                      const float* log_alpha, const uint16_t* beta,
+                      const float* init_state,
+                      const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                      int num_seqs, int total_tokens, int H, int Dk, int Dv,
+                      void* out, int out_dtype,
+                      float* final_state, float* ckpt_states, int ckpt_stride,
+                      void* stream) {
+    return prefill_pooled(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host, num_seqs, total_tokens,
+                          H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, KDA_DECAY_CHANNEL, stream);
+}
+
+int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         const float* log_alpha, const uint16_t* beta,
+                         const float* init_state,
+                         const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                         int num_seqs, int total_tokens, int H, int Dk, int Dv,
+                         void* out, int out_dtype,
+                         float* final_state, float* ckpt_states, int ckpt_stride,
+                         int decay, void* stream) {
+    return prefill_pooled(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host, num_seqs, total_tokens,
+                          H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, decay, stream);
 }
 
 int kda_chunk_prefill_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -206,7 +232,8 @@ int kda_chunk_prefill_noalloc(const uint16_t* q, const uint16_t* k, const uint16
                               float* final_state, float* ckpt_states, int ckpt_stride,
                               void* stream) {
     int rc = check_prefill_args(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host, num_seqs,
-                                total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride);
+                                total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride,
+                                KDA_DECAY_CHANNEL);
     if (rc != KDA_OK || num_seqs == 0) return rc;
     if (static_cast<int64_t>(num_seqs) * H > KDA_NOALLOC_MAX_SEQ_HEADS) return KDA_ERR_UNSUPPORTED;
     int* status = nullptr;
@@ -215,7 +242,7 @@ int kda_chunk_prefill_noalloc(const uint16_t* q, const uint16_t* k, const uint16
     if (rc != KDA_OK) return rc;
     rc = kda::launch_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, num_seqs, total_tokens, H, Dk, Dv,
                              out, out_dtype == KDA_OUT_F32, final_state, ckpt_states, ckpt_stride,
-                             scratch, status, static_cast<cudaStream_t>(stream));
+                             KDA_DECAY_CHANNEL, scratch, status, static_cast<cudaStream_t>(stream));
     return rc == 0 ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -246,19 +273,21 @@ int kda_decode_multi(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                      float* state_pool, int num_slots, const int32_t* state_slots,
                      const int32_t* num_tokens, int commit,
                      void* out, int out_dtype,
-                     int N, int K, int H, int Dk, int Dv, void* stream) {
+                     int N, int K, int H, int Dk, int Dv, int decay, void* stream) {
     if (N < 0 || K < 0 || H <= 0 || num_slots < 0) return KDA_ERR_INVALID_ARG;
+    if (decay != KDA_DECAY_CHANNEL && decay != KDA_DECAY_HEAD && decay != KDA_DECAY_NONE) return KDA_ERR_INVALID_ARG;
     if (out_dtype != KDA_OUT_BF16 && out_dtype != KDA_OUT_F32) return KDA_ERR_INVALID_ARG;
     if (commit != 0 && commit != 1) return KDA_ERR_INVALID_ARG;
     if (!head_dims_ok(Dk, Dv)) return KDA_ERR_UNSUPPORTED;
     if (Dk != Dv) return KDA_ERR_UNSUPPORTED;
     if (N == 0 || K == 0) return KDA_OK;
-    if (!q || !k || !v || !log_alpha || !beta || !state_pool || !out) return KDA_ERR_INVALID_ARG;
+    if (!q || !k || !v || !beta || !state_pool || !out) return KDA_ERR_INVALID_ARG;
+    if ((decay == KDA_DECAY_NONE) != (log_alpha == nullptr)) return KDA_ERR_INVALID_ARG;
     if (!state_slots && num_slots < N) return KDA_ERR_INVALID_ARG;
     if (num_slots == 0) return KDA_ERR_INVALID_ARG;
     const void* ptrs[] = {q, k, v, log_alpha, beta, state_pool, out};
     for (const void* p : ptrs)
-        if (!aligned16(p)) return KDA_ERR_INVALID_ARG;
+        if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
     if ((state_slots && (reinterpret_cast<uintptr_t>(state_slots) & 3u)) ||
         (num_tokens && (reinterpret_cast<uintptr_t>(num_tokens) & 3u)))
         return KDA_ERR_INVALID_ARG;
@@ -268,7 +297,8 @@ int kda_decode_multi(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     int rc = device_setup(&status);
     if (rc != KDA_OK) return rc;
     rc = kda::launch_decode_multi(q, k, v, log_alpha, beta, state_pool, num_slots, state_slots, num_tokens, commit,
-                                  out, out_dtype == KDA_OUT_F32, N, K, H, Dk, status, static_cast<cudaStream_t>(stream));
+                                  out, out_dtype == KDA_OUT_F32, N, K, H, Dk, decay, status,
+                                  static_cast<cudaStream_t>(stream));
     return rc == 0 ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -140,7 +140,7 @@ kda_decode_multi_kernel(const uint16_t* __restrict__ q, const uint16_t* __restri
                         const uint16_t* __restrict__ v, const float* __restrict__ log_alpha,
                         const uint16_t* __restrict__ beta, float* __restrict__ pool, int num_slots,
                         const int32_t* __restrict__ slots, const int32_t* __restrict__ ntok, int commit,
-                        void* __restrict__ out, int out_f32, int K, int H, int* status)
+                        void* __restrict__ out, int out_f32, int K, int H, int decay, int* status)
 {
     using Sh = DecodeShape<D, WARPS>;
     __shared__ float s_a[D], s_k[D], s_ak[D], s_aq[D], s_u[D];
@@ -174,7 +174,9 @@ kda_decode_multi_kernel(const uint16_t* __restrict__ q, const uint16_t* __restri
         if (tid < D) {
             const float qi = bf16_bits_to_f32(q[vec + tid]);
             const float ki = bf16_bits_to_f32(k[vec + tid]);
-            const float a = expf(log_alpha[vec + tid]);
+            // decay layouts: per channel (KDA), per head (Gated DeltaNet), none (DeltaNet)
+            const float a = decay == 0 ? expf(log_alpha[vec + tid])
+                          : decay == 1 ? expf(log_alpha[tok * H + h]) : 1.f;
             s_a[tid] = a;
             s_k[tid] = ki;
             s_ak[tid] = a * ki;
@@ -245,16 +247,16 @@ kda_decode_multi_kernel(const uint16_t* __restrict__ q, const uint16_t* __restri
 int launch_decode_multi(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* log_alpha,
                         const uint16_t* beta, float* pool, int num_slots, const int32_t* slots,
                         const int32_t* ntok, int commit, void* out, int out_f32,
-                        int N, int K, int H, int D, int* status, cudaStream_t stream)
+                        int N, int K, int H, int D, int decay, int* status, cudaStream_t stream)
 {
     const long long pairs = static_cast<long long>(N) * H;
     if (pairs == 0) return 0;
     if (D == 128) {
         kda_decode_multi_kernel<128, 8><<<static_cast<unsigned>(pairs), 256, 0, stream>>>(
-            q, k, v, log_alpha, beta, pool, num_slots, slots, ntok, commit, out, out_f32, K, H, status);
+            q, k, v, log_alpha, beta, pool, num_slots, slots, ntok, commit, out, out_f32, K, H, decay, status);
     } else {
         kda_decode_multi_kernel<64, 4><<<static_cast<unsigned>(pairs), 128, 0, stream>>>(
-            q, k, v, log_alpha, beta, pool, num_slots, slots, ntok, commit, out, out_f32, K, H, status);
+            q, k, v, log_alpha, beta, pool, num_slots, slots, ntok, commit, out, out_f32, K, H, decay, status);
     }
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }

@@ -85,7 +85,7 @@ static_assert(WS_BYTES_PER_CLUSTER == kPrefillRingBytesPerPair, "ring size is pa
 constexpr uint32_t P_A1 = 0;                 // [Km; Qm] tf32, 128 rows x 128 K, K-major  (64 KB)
 constexpr uint32_t P_B1 = 65536;             // Kb tf32, 64 rows x 128 K, K-major          (32 KB)
 // TMA staging of the next chunk's inputs, in the [Km; Qm] / Kb space once Km Kb^T is done
-constexpr uint32_t ST_LA = P_A1;             // log_alpha f32 [64][dk]
+constexpr uint32_t ST_LA = P_A1;             // log_alpha f32 [64][dk] (per-head decay: [64][4] around head h)
 constexpr uint32_t ST_Q = P_A1 + 32768;      // q bf16 [64][dk]
 constexpr uint32_t ST_K = P_A1 + 49152;      // k bf16 [64][dk]
 constexpr uint32_t ST_V = P_B1;              // v bf16 [64][dv]
@@ -126,8 +126,13 @@ constexpr uint32_t TM_D1A = 0, TM_D3 = 128, TM_D1B = 256, TM_CHAIN_COLS = 512;
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Decay layouts (include/kda.h kda_decay): per channel (KDA), one scalar per head and
+// token (Gated DeltaNet), or none (alpha = 1, DeltaNet).
+constexpr int DECAY_CHANNEL = 0, DECAY_HEAD = 1, DECAY_NONE = 2;
+
 struct TensorMaps {
     CUtensorMap q, k, la, v;     // 2-D views [tokens, H * D]; box = one head x 64 tokens
+                                 // (per-head decay: la is [tokens, H], box = 4 heads x 64 tokens)
     CUtensorMap o;               // bf16 output [tokens, H * Dv]; box = 64 columns x 64 tokens, 128B swizzle
 };
 
@@ -145,6 +150,7 @@ struct Params {
     uint8_t* ws;                 // hand-off ring: WS_BYTES_PER_CLUSTER per cluster
     int* status;
     int out_f32;
+    int decay;                   // DECAY_CHANNEL / DECAY_HEAD / DECAY_NONE
     int ckpt_stride;
     int H, dk, dv;
 };
@@ -275,9 +281,11 @@ __device__ __forceinline__ bool cta_wait(void* bar, uint32_t parity, bool cluste
 __device__ __forceinline__ void issue_input_tma(const TensorMaps& tmaps, const Params& p, uint8_t* sm, int c,
                                                 int t0, int h, void* bar) {
     const int y = t0 + c * C;
-    const uint32_t bytes = static_cast<uint32_t>(C * p.dk * (4 + 2 + 2) + C * p.dv * 2);
+    const uint32_t la_bytes = p.decay == DECAY_CHANNEL ? C * p.dk * 4 : p.decay == DECAY_HEAD ? C * 4 * 4 : 0;
+    const uint32_t bytes = static_cast<uint32_t>(C * p.dk * (2 + 2) + C * p.dv * 2) + la_bytes;
     tc::mbar_arrive_expect_tx(bar, bytes);
-    tc::tma_load_2d(tc::smem_u32(sm + ST_LA), &tmaps.la, h * p.dk, y, bar);
+    if (p.decay == DECAY_CHANNEL) tc::tma_load_2d(tc::smem_u32(sm + ST_LA), &tmaps.la, h * p.dk, y, bar);
+    else if (p.decay == DECAY_HEAD) tc::tma_load_2d(tc::smem_u32(sm + ST_LA), &tmaps.la, h & ~3, y, bar);
     tc::tma_load_2d(tc::smem_u32(sm + ST_Q), &tmaps.q, h * p.dk, y, bar);
     tc::tma_load_2d(tc::smem_u32(sm + ST_K), &tmaps.k, h * p.dk, y, bar);
     tc::tma_load_2d(tc::smem_u32(sm + ST_V), &tmaps.v, h * p.dv, y, bar);
@@ -288,7 +296,8 @@ __device__ __forceinline__ void issue_input_tma(const TensorMaps& tmaps, const P
 // tile streamed from DRAM takes several microseconds to land, from L2 a fraction of one.
 __device__ __forceinline__ void prefetch_inputs(const TensorMaps& tmaps, const Params& p, int c, int t0, int h) {
     const int y = t0 + c * C;
-    tc::tma_prefetch_2d(&tmaps.la, h * p.dk, y);
+    if (p.decay == DECAY_CHANNEL) tc::tma_prefetch_2d(&tmaps.la, h * p.dk, y);
+    else if (p.decay == DECAY_HEAD) tc::tma_prefetch_2d(&tmaps.la, h & ~3, y);
     tc::tma_prefetch_2d(&tmaps.q, h * p.dk, y);
     tc::tma_prefetch_2d(&tmaps.k, h * p.dk, y);
     tc::tma_prefetch_2d(&tmaps.v, h * p.dv, y);
@@ -376,7 +385,14 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         for (int i = 0; i < 8; ++i) {
             const int t = 8 * tg + i;
             if (t < nv && ch_ok) {
-                g4[i] = *reinterpret_cast<const float4*>(sm + ST_LA + (t * dk + 4 * cg) * 4);
+                if (p.decay == DECAY_CHANNEL) {
+                    g4[i] = *reinterpret_cast<const float4*>(sm + ST_LA + (t * dk + 4 * cg) * 4);
+                } else if (p.decay == DECAY_HEAD) {      // the head's scalar, on every channel
+                    const float x = *reinterpret_cast<const float*>(sm + ST_LA + (t * 4 + (h & 3)) * 4);
+                    g4[i] = make_float4(x, x, x, x);
+                } else {
+                    g4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
                 q2[i] = *reinterpret_cast<const uint2*>(sm + ST_Q + (t * dk + 4 * cg) * 2);
                 k2[i] = *reinterpret_cast<const uint2*>(sm + ST_K + (t * dk + 4 * cg) * 2);
             } else {
@@ -982,7 +998,8 @@ size_t prefill_workspace_bytes(int num_seqs, int H) {
 int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* la,
                    const uint16_t* beta, const float* init_state, const int32_t* cu_seqlens,
                    int num_seqs, int total_tokens, int H, int Dk, int Dv, void* out, int out_f32,
-                   float* final_state, float* ckpt, int ckpt_stride, void* ws, int* status, cudaStream_t stream)
+                   float* final_state, float* ckpt, int ckpt_stride, int decay, void* ws, int* status,
+                   cudaStream_t stream)
 {
     using namespace prefill;
     static bool attr_done = false;
@@ -995,7 +1012,7 @@ int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
     p.q = q; p.k = k; p.v = v; p.la = la; p.beta = beta; p.init_state = init_state;
     p.cu_seqlens = cu_seqlens; p.out = out; p.final_state = final_state; p.ckpt = ckpt;
     p.ws = static_cast<uint8_t*>(ws);
-    p.status = status; p.out_f32 = out_f32; p.ckpt_stride = ckpt_stride;
+    p.status = status; p.out_f32 = out_f32; p.ckpt_stride = ckpt_stride; p.decay = decay;
     p.H = H; p.dk = Dk; p.dv = Dv;
     const long long clusters = static_cast<long long>(num_seqs) * H;
     if (clusters == 0 || total_tokens == 0) {
@@ -1006,8 +1023,13 @@ int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
     if (total_tokens > 0) {
         if (!make_map(&tmaps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, total_tokens, static_cast<long long>(H) * Dk, Dk) ||
             !make_map(&tmaps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, total_tokens, static_cast<long long>(H) * Dk, Dk) ||
-            !make_map(&tmaps.la, la, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, total_tokens, static_cast<long long>(H) * Dk, Dk) ||
             !make_map(&tmaps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, total_tokens, static_cast<long long>(H) * Dv, Dv))
+            return -3;
+        memset(&tmaps.la, 0, sizeof(tmaps.la));
+        if (decay == DECAY_CHANNEL &&
+            !make_map(&tmaps.la, la, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, total_tokens, static_cast<long long>(H) * Dk, Dk))
+            return -3;
+        if (decay == DECAY_HEAD && !make_map(&tmaps.la, la, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, total_tokens, H, 4))
             return -3;
         memset(&tmaps.o, 0, sizeof(tmaps.o));   // fp32 output is written with plain stores
         if (!out_f32 && !make_map(&tmaps.o, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, total_tokens,

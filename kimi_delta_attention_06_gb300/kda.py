@@ -1,7 +1,7 @@
 """Thin ctypes binding of the KDA C ABI (include/kda.h).
 
 The functions named like the C entry points (``kda_chunk_prefill``,
-``kda_chunk_prefill_noalloc``, ``kda_decode_step``, ``kda_decode_multi``, ``kda_ckpt_count``,
+``kda_chunk_prefill_ex``, ``kda_chunk_prefill_noalloc``, ``kda_decode_step``, ``kda_decode_multi``, ``kda_ckpt_count``,
 ``kda_device_status``, ``kda_status_string``, ``kda_chunk_size``) only marshal
 arguments: torch
 tensors become raw device pointers, the current torch stream becomes the
@@ -33,6 +33,9 @@ KDA_ERR_TIMEOUT = -4
 KDA_OUT_BF16 = 0
 KDA_OUT_F32 = 1
 KDA_NOALLOC_MAX_SEQ_HEADS = 32
+KDA_DECAY_CHANNEL = 0
+KDA_DECAY_HEAD = 1
+KDA_DECAY_NONE = 2
 
 _vp = ctypes.c_void_p
 _i = ctypes.c_int
@@ -61,11 +64,14 @@ def load():
                 fn = getattr(lib, name)
                 fn.restype = _i
                 fn.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp, _vp, _i, _vp]
+            lib.kda_chunk_prefill_ex.restype = _i
+            lib.kda_chunk_prefill_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i,
+                                                 _vp, _vp, _i, _i, _vp]
             lib.kda_decode_step.restype = _i
             lib.kda_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]
             lib.kda_decode_multi.restype = _i
             lib.kda_decode_multi.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _i,
-                                             _i, _i, _i, _i, _i, _vp]
+                                             _i, _i, _i, _i, _i, _i, _vp]
             lib.kda_ckpt_count.restype = ctypes.c_int64
             lib.kda_ckpt_count.argtypes = [_vp, _i, _i]
             lib.kda_device_status.restype = _i
@@ -124,14 +130,15 @@ def kda_ckpt_count(cu_seqlens_host: torch.Tensor, ckpt_stride: int) -> int:
 
 
 def _call_prefill(name, q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host, num_seqs,
-                  total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, stream):
+                  total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, stream,
+                  *extra):
     cu_host = cu_seqlens_host.to(device="cpu", dtype=torch.int32).contiguous()
     rc = getattr(load(), name)(
         _ptr(_bits16(q)), _ptr(_bits16(k)), _ptr(_bits16(v)), _ptr(log_alpha), _ptr(_bits16(beta)),
         _ptr(init_state), _ptr(cu_seqlens), ctypes.c_void_p(cu_host.data_ptr()),
         int(num_seqs), int(total_tokens), int(H), int(Dk), int(Dv),
         _ptr(out), int(out_dtype), _ptr(final_state), _ptr(ckpt_states), int(ckpt_stride),
-        _stream(stream))
+        *[int(x) for x in extra], _stream(stream))
     _check(rc, name)
 
 
@@ -140,6 +147,14 @@ def kda_chunk_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqle
                       out, out_dtype: int, final_state, ckpt_states, ckpt_stride: int, stream=None):
     _call_prefill("kda_chunk_prefill", q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host,
                   num_seqs, total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, stream)
+
+
+def kda_chunk_prefill_ex(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host,
+                         num_seqs: int, total_tokens: int, H: int, Dk: int, Dv: int,
+                         out, out_dtype: int, final_state, ckpt_states, ckpt_stride: int, decay: int, stream=None):
+    _call_prefill("kda_chunk_prefill_ex", q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host,
+                  num_seqs, total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, stream,
+                  decay)
 
 
 def kda_chunk_prefill_noalloc(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host,
@@ -159,11 +174,12 @@ def kda_decode_step(q, k, v, log_alpha, beta, state, out, out_dtype: int,
 
 
 def kda_decode_multi(q, k, v, log_alpha, beta, state_pool, num_slots: int, state_slots, num_tokens,
-                     commit: int, out, out_dtype: int, N: int, K: int, H: int, Dk: int, Dv: int, stream=None):
+                     commit: int, out, out_dtype: int, N: int, K: int, H: int, Dk: int, Dv: int,
+                     decay: int = KDA_DECAY_CHANNEL, stream=None):
     rc = load().kda_decode_multi(_ptr(_bits16(q)), _ptr(_bits16(k)), _ptr(_bits16(v)), _ptr(log_alpha),
                                  _ptr(_bits16(beta)), _ptr(state_pool), int(num_slots), _ptr(state_slots),
                                  _ptr(num_tokens), int(commit), _ptr(out), int(out_dtype),
-                                 int(N), int(K), int(H), int(Dk), int(Dv), _stream(stream))
+                                 int(N), int(K), int(H), int(Dk), int(Dv), int(decay), _stream(stream))
     _check(rc, "kda_decode_multi")
 
 
@@ -178,8 +194,10 @@ def kda_device_status(stream=None) -> int:
 # --- conveniences: allocate outputs, then call the entry point ----------------------------
 
 def prefill(q, k, v, log_alpha, beta, cu_seqlens_host, init_state=None, ckpt_stride: int = 0,
-            out_dtype=torch.bfloat16, want_final: bool = True, cu_seqlens=None, stream=None):
-    """Allocate outputs and run kda_chunk_prefill.  Returns (out, final_state, ckpt_states)."""
+            out_dtype=torch.bfloat16, want_final: bool = True, cu_seqlens=None, stream=None,
+            decay: int = KDA_DECAY_CHANNEL):
+    """Allocate outputs and run kda_chunk_prefill (kda_chunk_prefill_ex for another decay
+    layout).  Returns (out, final_state, ckpt_states)."""
     T, H, Dk = q.shape
     Dv = v.shape[2]
     cu_host = cu_seqlens_host.to(device="cpu", dtype=torch.int32).contiguous()
@@ -191,9 +209,13 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens_host, init_state=None, ckpt_str
     fin = torch.empty(N, H, Dk, Dv, device=dev, dtype=torch.float32) if want_final else None
     nck = kda_ckpt_count(cu_host, ckpt_stride) if ckpt_stride > 0 else 0
     ck = torch.empty(nck, H, Dk, Dv, device=dev, dtype=torch.float32) if ckpt_stride > 0 else None
-    kda_chunk_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_host, N, T, H, Dk, Dv,
-                      out, KDA_OUT_F32 if out_dtype == torch.float32 else KDA_OUT_BF16,
-                      fin, ck if nck > 0 else None, ckpt_stride, stream)
+    odt = KDA_OUT_F32 if out_dtype == torch.float32 else KDA_OUT_BF16
+    if decay == KDA_DECAY_CHANNEL:
+        kda_chunk_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_host, N, T, H, Dk, Dv,
+                          out, odt, fin, ck if nck > 0 else None, ckpt_stride, stream)
+    else:
+        kda_chunk_prefill_ex(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_host, N, T, H, Dk, Dv,
+                             out, odt, fin, ck if nck > 0 else None, ckpt_stride, decay, stream)
     return out, fin, ck
 
 

@@ -2,6 +2,7 @@
 
   python -m kimi_delta_attention_06_gb300.run_case --what prefill --T 8192 [--H 32] [--D 128] [--reps 2]
   python -m kimi_delta_attention_06_gb300.run_case --what varlen [--H 32] [--D 128] [--reps 2]
+      (prefill / varlen also take --decay channel|head|none: KDA, Gated DeltaNet, DeltaNet)
   python -m kimi_delta_attention_06_gb300.run_case --what decode --N 512 [--H 32] [--D 128] [--reps 2]
   python -m kimi_delta_attention_06_gb300.run_case --what decode_multi --N 512 --K 4 [--commit 1] [--reps 2]
 
@@ -24,6 +25,8 @@ def main(argv=None):
     ap.add_argument("--what", choices=["prefill", "varlen", "decode", "decode_multi"], default="prefill")
     ap.add_argument("--K", type=int, default=4, help="tokens per sequence (decode_multi)")
     ap.add_argument("--commit", type=int, default=0, help="decode_multi: 1 writes the states back")
+    ap.add_argument("--decay", choices=["channel", "head", "none"], default="channel",
+                    help="prefill decay layout (per channel = KDA, per head = Gated DeltaNet, none = DeltaNet)")
     ap.add_argument("--T", type=int, default=8192)
     ap.add_argument("--N", type=int, default=512)
     ap.add_argument("--H", type=int, default=32)
@@ -41,15 +44,18 @@ def main(argv=None):
             c = workloads.varlen_case(device=dev, H=a.H, D=a.D, ckpt_stride=a.ckpt)
         T, N = c.T, c.N
         cu = c.cu_seqlens.to(dev)
+        decay = {"channel": kda.KDA_DECAY_CHANNEL, "head": kda.KDA_DECAY_HEAD, "none": kda.KDA_DECAY_NONE}[a.decay]
+        la = {kda.KDA_DECAY_CHANNEL: c.log_alpha, kda.KDA_DECAY_HEAD: c.log_alpha[:, :, 0].contiguous(),
+              kda.KDA_DECAY_NONE: None}[decay]
         out = torch.empty(T, a.H, a.D, device=dev, dtype=torch.bfloat16)
         fin = torch.empty(N, a.H, a.D, a.D, device=dev)
         nck = kda.kda_ckpt_count(c.cu_seqlens, a.ckpt)
         ck = torch.empty(max(nck, 1), a.H, a.D, a.D, device=dev)
 
         def run():
-            kda.kda_chunk_prefill(c.q, c.k, c.v, c.log_alpha, c.beta, c.init_state, cu, c.cu_seqlens, N, T,
-                                  a.H, a.D, a.D, out, kda.KDA_OUT_BF16, fin, ck if nck else None, a.ckpt, stream)
-        units, count = f"{T} tokens, {N} sequences", T
+            kda.kda_chunk_prefill_ex(c.q, c.k, c.v, la, c.beta, c.init_state, cu, c.cu_seqlens, N, T, a.H, a.D,
+                                     a.D, out, kda.KDA_OUT_BF16, fin, ck if nck else None, a.ckpt, decay, stream)
+        units, count = f"{T} tokens, {N} sequences, decay {a.decay}", T
     elif a.what == "decode_multi":
         d = workloads.decode_case(N=a.N, H=a.H, D=a.D, steps=a.K, seed=4, device=dev)
         tok = {key: torch.stack([s[key] for s in d.steps], dim=1).contiguous()

@@ -117,8 +117,8 @@ def test_decode_rejects_bad_arguments_on_host(lib):
 
 def test_decode_multi_rejects_bad_arguments_on_host(lib):
     f = lib.kda_decode_multi
-    #       q       k       v       la      beta    pool    slots  sl    ntok  commit out  dt  N  K  H  Dk   Dv  stream
-    args = [0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 8, None, None, 0, 0x7000, 0, 4, 3, 2, 128, 128, None]
+    #       q       k       v       la      beta    pool    slots  sl    ntok  commit out  dt  N  K  H  Dk   Dv decay stream
+    args = [0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 8, None, None, 0, 0x7000, 0, 4, 3, 2, 128, 128, 0, None]
     def call(**kw):
         a = list(args)
         for i, val in kw.items():
@@ -132,6 +132,27 @@ def test_decode_multi_rejects_bad_arguments_on_host(lib):
     assert call(a5=0x6004) == kda.KDA_ERR_INVALID_ARG     # misaligned pool
     assert call(a7=0x8002) == kda.KDA_ERR_INVALID_ARG     # misaligned slot array
     assert call(a12=0) == kda.KDA_OK and call(a13=0) == kda.KDA_OK   # nothing to do
+    assert call(a17=3) == kda.KDA_ERR_INVALID_ARG         # unknown decay layout
+    assert call(a17=2) == kda.KDA_ERR_INVALID_ARG         # no decay: log_alpha must be NULL
+    assert call(a3=None) == kda.KDA_ERR_INVALID_ARG       # a decay layout needs log_alpha
+
+
+def test_prefill_ex_decay_rules_on_host(lib):
+    f = "kda_chunk_prefill_ex"
+    def raw(decay, **over):
+        cu = (ctypes.c_int32 * 3)(0, 64, 100)
+        a = dict(q=0x1000, k=0x2000, v=0x3000, la=0x4000, beta=0x5000, s0=None, cu=0x6000,
+                 cu_host=ctypes.cast(cu, ctypes.c_void_p), N=2, T=100, H=4, Dk=64, Dv=64,
+                 out=0x7000, out_dtype=0, fin=None, ck=None, stride=0, stream=None)
+        a.update(over)
+        return getattr(lib, f)(a["q"], a["k"], a["v"], a["la"], a["beta"], a["s0"], a["cu"], a["cu_host"], a["N"],
+                               a["T"], a["H"], a["Dk"], a["Dv"], a["out"], a["out_dtype"], a["fin"], a["ck"],
+                               a["stride"], decay, a["stream"])
+    assert raw(kda.KDA_DECAY_HEAD, H=6) == kda.KDA_ERR_UNSUPPORTED     # per-head rows need H % 4 == 0
+    assert raw(kda.KDA_DECAY_NONE) == kda.KDA_ERR_INVALID_ARG          # log_alpha given but unused
+    assert raw(kda.KDA_DECAY_CHANNEL, la=None) == kda.KDA_ERR_INVALID_ARG
+    assert raw(7) == kda.KDA_ERR_INVALID_ARG
+    assert raw(kda.KDA_DECAY_NONE, la=None, N=0, T=0) == kda.KDA_OK
 
 
 def test_binding_refuses_non_bf16(lib):
