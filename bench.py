@@ -49,6 +49,12 @@ def prefill_algorithmic_bytes(T, n_ckpt_per_head):
     return BYTES_PER_TOKEN_HEAD * T * H + STATE_BYTES * H * (2 + n_ckpt_per_head)
 
 
+def kv_state_bytes(n_ckpt_per_head):
+    """Bytes of recurrent state one prefill hands to a prefix cache: the final state and
+    every checkpoint, all heads (the 'KV size' of KV throughput = KV size / prefill time)."""
+    return STATE_BYTES * H * (1 + n_ckpt_per_head)
+
+
 def decode_algorithmic_bytes(N):
     # state read + write, plus q, k, v, log_alpha, beta in and o out
     return N * H * (2 * STATE_BYTES + BYTES_PER_TOKEN_HEAD)
@@ -403,6 +409,9 @@ def main(argv=None):
                          "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": pre_bytes},
             "useful_flops": {"tflops": useful_tflops, "frac_of_bf16_peak": useful_tflops / bf16,
                              "frac_of_bf16_sustained": useful_tflops / bf16s, "peak_source": peak_src},
+            "kv_throughput": {"value": kv_state_bytes(n_ck) * world / (pre_avg * 1e-3) / 1e9, "unit": "GB/s",
+                              "state_bytes_per_prefill": kv_state_bytes(n_ck),
+                              "note": "final state + checkpoints written per prefill / prefill time"},
             "clocks": clocks, "e2e": e2e, "gpu_launches": 2 * args.steps, "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

@@ -51,3 +51,5 @@ def test_single_process_helpers():
     # weak scaling: 2 ranks x 1000 tokens in 4 ms (slowest rank) = 500k tokens/s
     assert bench.whole_job_rate(1000, 2, 4.0) == pytest.approx(500_000.0)
     assert bench.prefill_algorithmic_bytes(64, 1) == 1538 * 64 * 32 + 65536 * 32 * 3
+    # final state + 5 checkpoints of 32 heads x 128 x 128 fp32 (the T=145408 prompt)
+    assert bench.kv_state_bytes(5) == 6 * 32 * 128 * 128 * 4
