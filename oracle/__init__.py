@@ -41,6 +41,7 @@ _lib = None
 
 _dp = ctypes.POINTER(ctypes.c_double)
 _ip = ctypes.POINTER(ctypes.c_int32)
+_lp = ctypes.POINTER(ctypes.c_int64)
 
 
 def build(force: bool = False) -> str:
@@ -64,7 +65,7 @@ def _load():
             lib = ctypes.CDLL(build())
             lib.kda_oracle_prefill.restype = ctypes.c_int
             lib.kda_oracle_prefill.argtypes = [
-                _dp, _dp, _dp, _dp, _dp, _dp, _ip,
+                _dp, _dp, _dp, _dp, _dp, _dp, _ip, _lp,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 _dp, _dp, _dp, ctypes.c_int]
             lib.kda_oracle_decode.restype = ctypes.c_int
@@ -72,7 +73,7 @@ def _load():
                 _dp, _dp, _dp, _dp, _dp, _dp, _dp,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
             lib.kda_oracle_ckpt_count.restype = ctypes.c_int64
-            lib.kda_oracle_ckpt_count.argtypes = [_ip, ctypes.c_int, ctypes.c_int]
+            lib.kda_oracle_ckpt_count.argtypes = [_ip, _lp, ctypes.c_int, ctypes.c_int]
             lib.kda_oracle_max_threads.restype = ctypes.c_int
             lib.kda_oracle_max_threads.argtypes = []
             _lib = lib
@@ -103,18 +104,22 @@ def max_threads() -> int:
     return int(_load().kda_oracle_max_threads())
 
 
-def ckpt_count(cu_seqlens, ckpt_stride: int) -> int:
+def ckpt_count(cu_seqlens, ckpt_stride: int, start_pos=None) -> int:
     cu = _i32(cu_seqlens)
-    return int(_load().kda_oracle_ckpt_count(cu.ctypes.data_as(_ip), len(cu) - 1, int(ckpt_stride)))
+    sp = None if start_pos is None else np.ascontiguousarray(np.asarray(start_pos, dtype=np.int64))
+    return int(_load().kda_oracle_ckpt_count(cu.ctypes.data_as(_ip), None if sp is None else sp.ctypes.data_as(_lp),
+                                             len(cu) - 1, int(ckpt_stride)))
 
 
 def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None,
-            ckpt_stride: int = 0, threads: int = 0, want_out: bool = True):
+            ckpt_stride: int = 0, threads: int = 0, want_out: bool = True, start_pos=None):
     """Run the fp64 recurrence over packed sequences.
 
     q, k, log_alpha: [T, H, Dk]; v: [T, H, Dv]; beta: [T, H];
     cu_seqlens: [N+1] (default: one sequence of length T);
     init_state: [N, H, Dk, Dv] or None (zeros).
+    start_pos: [N] absolute prompt position of each sequence's first token, which
+    places the checkpoints on the prompt's own stride grid (None = all 0).
     Returns (out [T,H,Dv] or None, final_state [N,H,Dk,Dv], ckpts [n_ckpt,H,Dk,Dv] or None).
     """
     q, k, v, la, b = _f64(q), _f64(k), _f64(v), _f64(log_alpha), _f64(beta)
@@ -130,10 +135,14 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None,
         assert s0.shape == (N, H, Dk, Dv)
     out = np.zeros((T, H, Dv), np.float64) if want_out else None
     fin = np.zeros((N, H, Dk, Dv), np.float64)
-    nck = ckpt_count(cu, ckpt_stride) if ckpt_stride > 0 else 0
+    sp = None if start_pos is None else np.ascontiguousarray(np.asarray(start_pos, dtype=np.int64))
+    if sp is not None:
+        assert sp.shape == (N,) and np.all(sp >= 0)
+    nck = ckpt_count(cu, ckpt_stride, sp) if ckpt_stride > 0 else 0
     ck = np.zeros((nck, H, Dk, Dv), np.float64) if ckpt_stride > 0 else None
     rc = _load().kda_oracle_prefill(
         _ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(b), _ptr(s0), cu.ctypes.data_as(_ip),
+        None if sp is None else sp.ctypes.data_as(_lp),
         N, H, Dk, Dv, int(ckpt_stride), _ptr(out), _ptr(fin), _ptr(ck), int(threads))
     if rc != 0:
         raise RuntimeError("kda_oracle_prefill failed")

@@ -21,13 +21,16 @@
  *     S_t = S' + beta_t k_t u^T                      (rank-one write)
  *     o_t = S_t^T q_t                                (read the updated state)
  *
- * Prefix-cache checkpoints follow the primer's section 5 ("vLLM saves KDA
- * recurrent state every 32K tokens, plus at prompt boundaries"): after p
- * tokens of a sequence of length len, the state is emitted when
- * p % ckpt_stride == 0 and p < len, and always at p == len; a sequence
- * therefore owns ceil(len / ckpt_stride) checkpoint slots, stored in
- * sequence order.  An empty sequence owns none and its final state equals
- * its initial state.
+ * Prefix-cache checkpoints follow the primer's section 5 (the serving engine
+ * saves the KDA recurrent state every 32K tokens of a prompt, plus at prompt
+ * boundaries).  A sequence may continue a cached prefix: its first token sits
+ * at absolute prompt position s (0 for a fresh prompt), and the 32K grid counts
+ * from the prompt's start.  After p tokens of a sequence of length len, the
+ * state is emitted when (s + p) % ckpt_stride == 0 and p < len, and always at
+ * p == len; with s = 0 a sequence owns ceil(len / ckpt_stride) slots, in
+ * general floor((s + len - 1) / stride) - floor(s / stride) + 1, stored in
+ * sequence order.  An empty sequence owns none and its final state equals its
+ * initial state.
  *
  * Inputs are double arrays so that every bf16 / fp32 value the GPU sees is
  * represented exactly.  All arithmetic is fp64.  Layouts are row-major:
@@ -79,18 +82,22 @@ static void kda_oracle_token(double* S, int Dk, int Dv,
     }
 }
 
-/* Number of checkpoint slots a sequence of length len owns. */
-static int64_t kda_oracle_seq_ckpts(int64_t len, int64_t stride)
+/* Number of checkpoint slots a sequence of length len owns when its first token
+ * sits at absolute position s: the stride multiples strictly inside (s, s + len),
+ * plus its end. */
+static int64_t kda_oracle_seq_ckpts(int64_t len, int64_t s, int64_t stride)
 {
     if (stride <= 0 || len <= 0) return 0;
-    return (len + stride - 1) / stride;
+    return (s + len - 1) / stride - s / stride + 1;
 }
 
-int64_t kda_oracle_ckpt_count(const int32_t* cu_seqlens, int num_seqs, int ckpt_stride)
+/* start_pos: [num_seqs] absolute position of each sequence's first token, or NULL (all 0). */
+int64_t kda_oracle_ckpt_count(const int32_t* cu_seqlens, const int64_t* start_pos, int num_seqs, int ckpt_stride)
 {
     int64_t total = 0;
     for (int n = 0; n < num_seqs; ++n)
-        total += kda_oracle_seq_ckpts((int64_t)cu_seqlens[n + 1] - cu_seqlens[n], ckpt_stride);
+        total += kda_oracle_seq_ckpts((int64_t)cu_seqlens[n + 1] - cu_seqlens[n], start_pos ? start_pos[n] : 0,
+                                      ckpt_stride);
     return total;
 }
 
@@ -101,12 +108,14 @@ int64_t kda_oracle_ckpt_count(const int32_t* cu_seqlens, int num_seqs, int ckpt_
  *   out:        [T_total, H, Dv]
  *   final_state:[num_seqs, H, Dk, Dv] or NULL.
  *   ckpt_states:[kda_oracle_ckpt_count(...), H, Dk, Dv] or NULL; ckpt_stride 0 = none.
+ *   start_pos:  [num_seqs] absolute prompt position of each sequence's first token
+ *               (checkpoint alignment only), or NULL (all 0).
  *   num_threads: OpenMP threads over (sequence, head) pairs; <= 0 = runtime default.
  * Returns 0, or -1 on an allocation failure / bad argument.
  */
 int kda_oracle_prefill(const double* q, const double* k, const double* v,
                        const double* log_alpha, const double* beta,
-                       const double* init_state, const int32_t* cu_seqlens,
+                       const double* init_state, const int32_t* cu_seqlens, const int64_t* start_pos,
                        int num_seqs, int H, int Dk, int Dv, int ckpt_stride,
                        double* out, double* final_state, double* ckpt_states,
                        int num_threads)
@@ -117,7 +126,8 @@ int kda_oracle_prefill(const double* q, const double* k, const double* v,
     ckpt_base[0] = 0;
     for (int n = 0; n < num_seqs; ++n)
         ckpt_base[n + 1] = ckpt_base[n] +
-            kda_oracle_seq_ckpts((int64_t)cu_seqlens[n + 1] - cu_seqlens[n], ckpt_stride);
+            kda_oracle_seq_ckpts((int64_t)cu_seqlens[n + 1] - cu_seqlens[n], start_pos ? start_pos[n] : 0,
+                                 ckpt_stride);
 
     const size_t SS = (size_t)Dk * Dv;
     const int pairs = num_seqs * H;
@@ -136,6 +146,7 @@ int kda_oracle_prefill(const double* q, const double* k, const double* v,
 
         const int64_t t0 = cu_seqlens[n], len = (int64_t)cu_seqlens[n + 1] - cu_seqlens[n];
         int64_t slot = ckpt_base[n];
+        const int64_t s = start_pos ? start_pos[n] : 0;
         for (int64_t pos = 0; pos < len; ++pos) {
             const size_t tok = (size_t)(t0 + pos);
             const size_t kh = (tok * H + h) * (size_t)Dk;
@@ -143,7 +154,7 @@ int kda_oracle_prefill(const double* q, const double* k, const double* v,
             kda_oracle_token(S, Dk, Dv, q + kh, k + kh, v + vh, log_alpha + kh,
                              beta[tok * H + h], u, out ? out + vh : NULL);
             const int64_t done = pos + 1;
-            if (ckpt_states && ckpt_stride > 0 && (done % ckpt_stride == 0 || done == len)) {
+            if (ckpt_states && ckpt_stride > 0 && ((s + done) % ckpt_stride == 0 || done == len)) {
                 memcpy(ckpt_states + ((size_t)slot * H + h) * SS, S, sizeof(double) * SS);
                 ++slot;
             }

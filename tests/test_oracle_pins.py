@@ -273,6 +273,54 @@ def test_resume_from_checkpoint():
     np.testing.assert_allclose(f2, fin, atol=1e-12)
 
 
+def test_checkpoints_on_the_absolute_grid_enumerated():
+    """A sequence continuing a prefix: its first token is at absolute position s, so the
+    stride grid counts from the prompt's start (primer section 5: every 32K tokens of the
+    prompt, plus at its end).  s = 6, len = 9, stride = 4: checkpoints after p = 2 and 6
+    tokens (absolute 8 and 12) and at the end p = 9; each equals the state of a run cut
+    there."""
+    rng = np.random.default_rng(15)
+    T, H, Dk, Dv, stride, s0pos = 9, 2, 8, 4, 4, 6
+    q = rng.standard_normal((T, H, Dk)); k = rng.standard_normal((T, H, Dk))
+    k /= np.linalg.norm(k, axis=2, keepdims=True)
+    v = rng.standard_normal((T, H, Dv)); la = -np.abs(rng.standard_normal((T, H, Dk))) * 0.3
+    beta = rng.uniform(0, 1, (T, H)); S0 = rng.standard_normal((1, H, Dk, Dv))
+    cu = np.array([0, T], np.int32)
+    assert oracle.ckpt_count(cu, stride, [s0pos]) == 3
+    assert oracle.ckpt_count(cu, stride, [0]) == oracle.ckpt_count(cu, stride) == 3   # ceil(9/4)
+    assert oracle.ckpt_count(cu, stride, [8]) == 3        # absolute 12, 16, end 17
+    assert oracle.ckpt_count(cu, stride, [7]) == 3        # absolute 8, 12, end 16 (a multiple, once)
+    _, fin, ck = oracle.prefill(q, k, v, la, beta, cu, S0, ckpt_stride=stride, start_pos=[s0pos])
+    for slot, p in enumerate([2, 6, 9]):
+        _, fp, _ = oracle.prefill(q[:p], k[:p], v[:p], la[:p], beta[:p], None, S0)
+        np.testing.assert_array_equal(ck[slot], fp[0])
+    np.testing.assert_array_equal(ck[-1], fin[0])
+
+
+def test_continuation_checkpoints_match_one_call():
+    """One call over a whole prompt equals a prefix call plus a continuation that starts
+    at absolute position P from the prefix's end state: same outputs, same final state,
+    and the continuation's checkpoints are the one-call checkpoints after P (the token
+    recurrence performs the same operations, so these are bit-identical)."""
+    rng = np.random.default_rng(16)
+    T, P, H, Dk, Dv, stride = 45, 13, 2, 8, 8, 8
+    q = rng.standard_normal((T, H, Dk)); k = rng.standard_normal((T, H, Dk))
+    k /= np.linalg.norm(k, axis=2, keepdims=True)
+    v = rng.standard_normal((T, H, Dv)); la = -np.abs(rng.standard_normal((T, H, Dk))) * 0.2
+    beta = rng.uniform(0, 1, (T, H)); S0 = rng.standard_normal((1, H, Dk, Dv))
+    o_all, f_all, c_all = oracle.prefill(q, k, v, la, beta, None, S0, ckpt_stride=stride)
+    o_a, f_a, c_a = oracle.prefill(q[:P], k[:P], v[:P], la[:P], beta[:P], None, S0, ckpt_stride=stride)
+    o_b, f_b, c_b = oracle.prefill(q[P:], k[P:], v[P:], la[P:], beta[P:], None, f_a, ckpt_stride=stride,
+                                   start_pos=[P])
+    np.testing.assert_array_equal(np.concatenate([o_a, o_b]), o_all)
+    np.testing.assert_array_equal(f_b, f_all)
+    # one call: absolute 8, 16, 24, 32, 40 and the end 45; the prefix: 8 and its end 13;
+    # the continuation: 16, 24, 32, 40 and 45
+    assert c_all.shape[0] == 6 and c_a.shape[0] == 2 and c_b.shape[0] == 5
+    np.testing.assert_array_equal(c_a[0], c_all[0])
+    np.testing.assert_array_equal(c_b, c_all[1:])
+
+
 def test_decode_steps_equal_prefill():
     rng = np.random.default_rng(14)
     T, N, H, Dk, Dv = 6, 3, 2, 8, 8
