@@ -109,11 +109,19 @@ int kda_chunk_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
 /*
  * kda_chunk_prefill_ex -- kda_chunk_prefill with a choice of decay layout.
  *
- * Identical to kda_chunk_prefill when decay == KDA_DECAY_CHANNEL.  With
- * KDA_DECAY_HEAD, log_alpha is fp32 [total_tokens, H] (one log-decay per head and
- * token, applied to every channel) and H must be a multiple of 4 (its 16-byte rows are
- * staged by TMA), else KDA_ERR_UNSUPPORTED.  With KDA_DECAY_NONE, log_alpha must be
- * NULL and alpha = 1.
+ * Identical to kda_chunk_prefill when decay == KDA_DECAY_CHANNEL and start_pos is
+ * NULL.
+ *   decay       KDA_DECAY_HEAD: log_alpha is fp32 [total_tokens, H] (one log-decay per
+ *               head and token, applied to every channel) and H must be a multiple of 4
+ *               (its 16-byte rows are staged by TMA), else KDA_ERR_UNSUPPORTED.
+ *               KDA_DECAY_NONE: log_alpha must be NULL, alpha = 1.
+ *   start_pos   (device) int32 [num_seqs] or NULL: absolute prompt position of each
+ *               sequence's first token, for a prefill that continues a cached prefix
+ *               (init_state = the state after those start_pos tokens).  Checkpoints
+ *               then fall where start_pos + p is a multiple of ckpt_stride (p < len),
+ *               plus at the sequence end, so they line up with the prompt's own grid;
+ *               slots per sequence: kda_ckpt_count_ex.  NULL = all 0.
+ *   start_pos_host the same values on the host (non-negative), NULL iff start_pos is.
  */
 int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                          const float* log_alpha, const uint16_t* beta,
@@ -122,7 +130,8 @@ int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v
                          int num_seqs, int total_tokens, int H, int Dk, int Dv,
                          void* out, int out_dtype,
                          float* final_state, float* ckpt_states, int ckpt_stride,
-                         int decay, void* stream);
+                         int decay, const int32_t* start_pos, const int32_t* start_pos_host,
+                         void* stream);
 
 /*
  * kda_chunk_prefill_noalloc -- kda_chunk_prefill that allocates nothing.
@@ -206,6 +215,13 @@ int kda_decode_multi(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  * ceil(len / ckpt_stride) (0 when ckpt_stride == 0).  cu_seqlens_host is a host
  * array of num_seqs + 1 offsets.  Returns -1 on invalid arguments. */
 int64_t kda_ckpt_count(const int32_t* cu_seqlens_host, int num_seqs, int ckpt_stride);
+
+/* Checkpoint slots of kda_chunk_prefill_ex with start positions: per sequence of
+ * length len > 0 starting at absolute position s, the multiples of ckpt_stride strictly
+ * inside (s, s + len) plus one for its end.  start_pos_host NULL = all 0 (then equal to
+ * kda_ckpt_count).  Returns -1 on invalid arguments. */
+int64_t kda_ckpt_count_ex(const int32_t* cu_seqlens_host, const int32_t* start_pos_host, int num_seqs,
+                          int ckpt_stride);
 
 /* Synchronises `stream`, then returns and clears the device status word:
  * KDA_OK, KDA_ERR_TIMEOUT (a bounded wait inside a kernel expired and the

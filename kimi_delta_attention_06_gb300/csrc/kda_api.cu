@@ -17,8 +17,8 @@ int launch_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, const
 int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* la,
                    const uint16_t* beta, const float* init_state, const int32_t* cu_seqlens,
                    int num_seqs, int total_tokens, int H, int Dk, int Dv, void* out, int out_f32,
-                   float* final_state, float* ckpt, int ckpt_stride, int decay, void* ws, int* status,
-                   cudaStream_t stream);
+                   float* final_state, float* ckpt, int ckpt_stride, int decay, const int32_t* start_pos,
+                   void* ws, int* status, cudaStream_t stream);
 size_t prefill_workspace_bytes(int num_seqs, int H);
 int launch_decode_multi(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* log_alpha,
                         const uint16_t* beta, float* pool, int num_slots, const int32_t* slots,
@@ -149,16 +149,23 @@ __global__ void expire_wait_kernel(unsigned long long limit_ns, int* status) {
 
 extern "C" {
 
-int64_t kda_ckpt_count(const int32_t* cu_seqlens_host, int num_seqs, int ckpt_stride) {
+int64_t kda_ckpt_count_ex(const int32_t* cu_seqlens_host, const int32_t* start_pos_host, int num_seqs,
+                          int ckpt_stride) {
     if (num_seqs < 0 || ckpt_stride < 0 || (num_seqs > 0 && !cu_seqlens_host)) return -1;
     if (ckpt_stride == 0) return 0;
     int64_t total = 0;
     for (int n = 0; n < num_seqs; ++n) {
         const int64_t len = static_cast<int64_t>(cu_seqlens_host[n + 1]) - cu_seqlens_host[n];
-        if (len < 0) return -1;
-        total += (len + ckpt_stride - 1) / ckpt_stride;
+        const int64_t s = start_pos_host ? start_pos_host[n] : 0;
+        if (len < 0 || s < 0) return -1;
+        // stride multiples strictly inside (s, s + len), plus the end
+        if (len > 0) total += (s + len - 1) / ckpt_stride - s / ckpt_stride + 1;
     }
     return total;
+}
+
+int64_t kda_ckpt_count(const int32_t* cu_seqlens_host, int num_seqs, int ckpt_stride) {
+    return kda_ckpt_count_ex(cu_seqlens_host, nullptr, num_seqs, ckpt_stride);
 }
 
 int kda_chunk_size(void) { return 64; }
@@ -178,10 +185,16 @@ static int prefill_pooled(const uint16_t* q, const uint16_t* k, const uint16_t* 
                           const uint16_t* beta, const float* init_state, const int32_t* cu_seqlens,
                           const int32_t* cu_seqlens_host, int num_seqs, int total_tokens, int H, int Dk, int Dv,
                           void* out, int out_dtype, float* final_state, float* ckpt_states, int ckpt_stride,
-                          int decay, void* stream) {
+                          int decay, const int32_t* start_pos, const int32_t* start_pos_host, void* stream) {
     int rc = check_prefill_args(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host, num_seqs,
                                 total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, decay);
     if (rc != KDA_OK || num_seqs == 0) return rc;
+    if ((start_pos == nullptr) != (start_pos_host == nullptr)) return KDA_ERR_INVALID_ARG;
+    if (start_pos) {
+        if (reinterpret_cast<uintptr_t>(start_pos) & 3u) return KDA_ERR_INVALID_ARG;
+        for (int n = 0; n < num_seqs; ++n)
+            if (start_pos_host[n] < 0) return KDA_ERR_INVALID_ARG;
+    }
     int* status = nullptr;
     rc = device_setup(&status);
     if (rc != KDA_OK) return rc;
@@ -194,7 +207,7 @@ static int prefill_pooled(const uint16_t* q, const uint16_t* k, const uint16_t* 
         return KDA_ERR_CUDA;
     rc = kda::launch_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, num_seqs, total_tokens, H, Dk, Dv,
                              out, out_dtype == KDA_OUT_F32, final_state, ckpt_states, ckpt_stride, decay,
-                             ws, status, st);
+                             start_pos, ws, status, st);
     const bool freed = cudaFreeAsync(ws, st) == cudaSuccess;
     return (rc == 0 && freed) ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -208,7 +221,8 @@ int kda_chunk_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                       float* final_state, float* ckpt_states, int ckpt_stride,
                       void* stream) {
     return prefill_pooled(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host, num_seqs, total_tokens,
-                          H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, KDA_DECAY_CHANNEL, stream);
+                          H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, KDA_DECAY_CHANNEL,
+                          nullptr, nullptr, stream);
 }
 
 int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -218,9 +232,10 @@ int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v
                          int num_seqs, int total_tokens, int H, int Dk, int Dv,
                          void* out, int out_dtype,
                          float* final_state, float* ckpt_states, int ckpt_stride,
-                         int decay, void* stream) {
+                         int decay, const int32_t* start_pos, const int32_t* start_pos_host, void* stream) {
     return prefill_pooled(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host, num_seqs, total_tokens,
-                          H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, decay, stream);
+                          H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, decay, start_pos,
+                          start_pos_host, stream);
 }
 
 int kda_chunk_prefill_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -242,7 +257,7 @@ int kda_chunk_prefill_noalloc(const uint16_t* q, const uint16_t* k, const uint16
     if (rc != KDA_OK) return rc;
     rc = kda::launch_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, num_seqs, total_tokens, H, Dk, Dv,
                              out, out_dtype == KDA_OUT_F32, final_state, ckpt_states, ckpt_stride,
-                             KDA_DECAY_CHANNEL, scratch, status, static_cast<cudaStream_t>(stream));
+                             KDA_DECAY_CHANNEL, nullptr, scratch, status, static_cast<cudaStream_t>(stream));
     return rc == 0 ? KDA_OK : KDA_ERR_CUDA;
 }
 

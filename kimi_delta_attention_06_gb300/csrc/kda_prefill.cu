@@ -128,7 +128,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // Decay layouts (include/kda.h kda_decay): per channel (KDA), one scalar per head and
 // token (Gated DeltaNet), or none (alpha = 1, DeltaNet).
-constexpr int DECAY_CHANNEL = 0, DECAY_HEAD = 1, DECAY_NONE = 2;
+enum : int { DECAY_CHANNEL = 0, DECAY_HEAD = 1, DECAY_NONE = 2 };
 
 struct TensorMaps {
     CUtensorMap q, k, la, v;     // 2-D views [tokens, H * D]; box = one head x 64 tokens
@@ -144,15 +144,30 @@ struct Params {
     const uint16_t* beta;
     const float* init_state;
     const int32_t* cu_seqlens;
+    const int32_t* start_pos;    // absolute prompt position of each sequence's first token, or null
     void* out;
     float* final_state;
     float* ckpt;
     uint8_t* ws;                 // hand-off ring: WS_BYTES_PER_CLUSTER per cluster
     int* status;
     int out_f32;
-    int decay;                   // DECAY_CHANNEL / DECAY_HEAD / DECAY_NONE
     int ckpt_stride;
     int H, dk, dv;
+};
+
+// Chunk grid of one sequence.  Chunks sit on the prompt's absolute 64-token grid, so
+// that absolute checkpoint positions (multiples of the stride, itself a multiple of
+// 64) always fall on chunk ends: a sequence continuing a prefix of s tokens starts
+// with a partial chunk whose first off = s % 64 rows precede it.  Row t of chunk c is
+// packed token row0(c) + t; rows outside [lo(c), hi(c)) are not the sequence's and
+// enter as zeros (k = q = v = 0, beta = 0, log_alpha = 0), which makes them no-ops.
+struct SeqGrid {
+    int t0, len, off, nchunks;
+    long long start;
+    __device__ __forceinline__ int row0(int c) const { return t0 - off + c * C; }
+    __device__ __forceinline__ int lo(int c) const { return c == 0 ? off : 0; }
+    __device__ __forceinline__ int hi(int c) const { return min(C, len + off - c * C); }
+    __device__ __forceinline__ int done(int c) const { return min(len, (c + 1) * C - off); }
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -277,15 +292,17 @@ __device__ __forceinline__ bool cta_wait(void* bar, uint32_t parity, bool cluste
 }
 
 // Issue the TMA loads of chunk c's inputs (q, k, log_alpha, v of one head) into the
-// staging area; completion is counted on `bar`.  One thread.
+// staging area; completion is counted on `bar`.  One thread.  DECAY is the decay layout
+// (a template argument, so the per-channel path carries no trace of the others).
+template <int DECAY>
 __device__ __forceinline__ void issue_input_tma(const TensorMaps& tmaps, const Params& p, uint8_t* sm, int c,
-                                                int t0, int h, void* bar) {
-    const int y = t0 + c * C;
-    const uint32_t la_bytes = p.decay == DECAY_CHANNEL ? C * p.dk * 4 : p.decay == DECAY_HEAD ? C * 4 * 4 : 0;
+                                                const SeqGrid& g, int h, void* bar) {
+    const int y = g.row0(c);            // may be negative for a leading partial chunk: zero fill
+    const uint32_t la_bytes = DECAY == DECAY_CHANNEL ? C * p.dk * 4 : DECAY == DECAY_HEAD ? C * 4 * 4 : 0;
     const uint32_t bytes = static_cast<uint32_t>(C * p.dk * (2 + 2) + C * p.dv * 2) + la_bytes;
     tc::mbar_arrive_expect_tx(bar, bytes);
-    if (p.decay == DECAY_CHANNEL) tc::tma_load_2d(tc::smem_u32(sm + ST_LA), &tmaps.la, h * p.dk, y, bar);
-    else if (p.decay == DECAY_HEAD) tc::tma_load_2d(tc::smem_u32(sm + ST_LA), &tmaps.la, h & ~3, y, bar);
+    if (DECAY == DECAY_CHANNEL) tc::tma_load_2d(tc::smem_u32(sm + ST_LA), &tmaps.la, h * p.dk, y, bar);
+    else if (DECAY == DECAY_HEAD) tc::tma_load_2d(tc::smem_u32(sm + ST_LA), &tmaps.la, h & ~3, y, bar);
     tc::tma_load_2d(tc::smem_u32(sm + ST_Q), &tmaps.q, h * p.dk, y, bar);
     tc::tma_load_2d(tc::smem_u32(sm + ST_K), &tmaps.k, h * p.dk, y, bar);
     tc::tma_load_2d(tc::smem_u32(sm + ST_V), &tmaps.v, h * p.dv, y, bar);
@@ -294,10 +311,12 @@ __device__ __forceinline__ void issue_input_tma(const TensorMaps& tmaps, const P
 // ============================================================================
 // Pull chunk c's inputs into L2 ahead of the TMA load that stages them: a strided
 // tile streamed from DRAM takes several microseconds to land, from L2 a fraction of one.
-__device__ __forceinline__ void prefetch_inputs(const TensorMaps& tmaps, const Params& p, int c, int t0, int h) {
-    const int y = t0 + c * C;
-    if (p.decay == DECAY_CHANNEL) tc::tma_prefetch_2d(&tmaps.la, h * p.dk, y);
-    else if (p.decay == DECAY_HEAD) tc::tma_prefetch_2d(&tmaps.la, h & ~3, y);
+template <int DECAY>
+__device__ __forceinline__ void prefetch_inputs(const TensorMaps& tmaps, const Params& p, int c, const SeqGrid& g,
+                                                int h) {
+    const int y = max(0, g.row0(c));
+    if (DECAY == DECAY_CHANNEL) tc::tma_prefetch_2d(&tmaps.la, h * p.dk, y);
+    else if (DECAY == DECAY_HEAD) tc::tma_prefetch_2d(&tmaps.la, h & ~3, y);
     tc::tma_prefetch_2d(&tmaps.q, h * p.dk, y);
     tc::tma_prefetch_2d(&tmaps.k, h * p.dk, y);
     tc::tma_prefetch_2d(&tmaps.v, h * p.dv, y);
@@ -305,7 +324,8 @@ __device__ __forceinline__ void prefetch_inputs(const TensorMaps& tmaps, const P
 
 // Prep CTA: prepares chunks c = pr, pr + 3, pr + 6, ... of one (sequence, head).
 // ============================================================================
-__device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm, int pr, int h, int t0, int len,
+template <int DECAY>
+__device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm, int pr, int h, const SeqGrid& g,
                           size_t cl) {
     uint8_t* A1 = sm + P_A1;
     uint8_t* B1 = sm + P_B1;
@@ -325,7 +345,7 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int dk = p.dk, dv = p.dv;
-    const int nchunks = (len + C - 1) / C;
+    const int nchunks = g.nchunks;
 
     if (warp == 0) tc::tmem_alloc(s_tmem, TM_PREP_COLS);
     cta_sync_tc();
@@ -348,21 +368,22 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
     // only where the value is stored, so the load stays in flight across the chunk
     // boundary) and pull the lines of the chunk after that into L2
     const bool beta_thread = tid >= 128 && tid < 192;
+    auto beta_ok = [&](int c) { return tid - 128 >= g.lo(c) && tid - 128 < g.hi(c); };
     auto beta_ptr = [&](int c) -> const uint16_t* {
-        return p.beta + static_cast<size_t>(t0 + c * C + (tid - 128)) * p.H + h;
+        return p.beta + static_cast<size_t>(g.row0(c) + (tid - 128)) * p.H + h;
     };
     auto load_beta = [&](int c) -> uint16_t {
-        return (tid - 128 < min(C, len - c * C)) ? *beta_ptr(c) : static_cast<uint16_t>(0);
+        return beta_ok(c) ? *beta_ptr(c) : static_cast<uint16_t>(0);
     };
     auto prefetch_beta = [&](int c) {
-        if (c < nchunks && tid - 128 < min(C, len - c * C))
+        if (c < nchunks && beta_ok(c))
             asm volatile("prefetch.global.L2 [%0];" :: "l"(beta_ptr(c)));
     };
     uint16_t bt = 0;
     if (pr < nchunks) {
         if (tid == 0) {
-            issue_input_tma(tmaps, p, sm, pr, t0, h, &mb[3]);
-            if (pr + NPREP_CTAS < nchunks) prefetch_inputs(tmaps, p, pr + NPREP_CTAS, t0, h);
+            issue_input_tma<DECAY>(tmaps, p, sm, pr, g, h, &mb[3]);
+            if (pr + NPREP_CTAS < nchunks) prefetch_inputs<DECAY>(tmaps, p, pr + NPREP_CTAS, g, h);
         }
         if (beta_thread) {
             bt = load_beta(pr);
@@ -373,10 +394,10 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
     bool ok = true;
     int kk = 0;                                         // index of this CTA's chunk
     for (int c = pr; c < nchunks; c += NPREP_CTAS, ++kk) {
-        const int nv = min(C, len - c * C);
+        const int lo = g.lo(c), hi = g.hi(c);          // the sequence's rows of this chunk
 
         // -- 0. inputs of this chunk: staging (TMA) -> registers --
-        if (tid == 0 && c + 2 * NPREP_CTAS < nchunks) prefetch_inputs(tmaps, p, c + 2 * NPREP_CTAS, t0, h);
+        if (tid == 0 && c + 2 * NPREP_CTAS < nchunks) prefetch_inputs<DECAY>(tmaps, p, c + 2 * NPREP_CTAS, g, h);
         if (!cta_wait(&mb[3], kk & 1, false)) { ok = false; break; }
         float4 g4[8];
         uint2 q2[8], k2[8];
@@ -384,26 +405,32 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int t = 8 * tg + i;
-            if (t < nv && ch_ok) {
-                if (p.decay == DECAY_CHANNEL) {
-                    g4[i] = *reinterpret_cast<const float4*>(sm + ST_LA + (t * dk + 4 * cg) * 4);
-                } else if (p.decay == DECAY_HEAD) {      // the head's scalar, on every channel
-                    const float x = *reinterpret_cast<const float*>(sm + ST_LA + (t * 4 + (h & 3)) * 4);
-                    g4[i] = make_float4(x, x, x, x);
-                } else {
-                    g4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-                q2[i] = *reinterpret_cast<const uint2*>(sm + ST_Q + (t * dk + 4 * cg) * 2);
-                k2[i] = *reinterpret_cast<const uint2*>(sm + ST_K + (t * dk + 4 * cg) * 2);
-            } else {
-                g4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                q2[i] = make_uint2(0u, 0u);
-                k2[i] = make_uint2(0u, 0u);
+            const bool ok_t = t >= lo && t < hi && ch_ok;
+            q2[i] = ok_t ? *reinterpret_cast<const uint2*>(sm + ST_Q + (t * dk + 4 * cg) * 2) : make_uint2(0u, 0u);
+            k2[i] = ok_t ? *reinterpret_cast<const uint2*>(sm + ST_K + (t * dk + 4 * cg) * 2) : make_uint2(0u, 0u);
+        }
+        if (DECAY == DECAY_CHANNEL) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int t = 8 * tg + i;
+                g4[i] = (t >= lo && t < hi && ch_ok)
+                    ? *reinterpret_cast<const float4*>(sm + ST_LA + (t * dk + 4 * cg) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
+        } else if (DECAY == DECAY_HEAD) {     // the head's scalar, on every channel
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int t = 8 * tg + i;
+                const float x = (t >= lo && t < hi && ch_ok)
+                    ? *reinterpret_cast<const float*>(sm + ST_LA + (t * 4 + (h & 3)) * 4) : 0.f;
+                g4[i] = make_float4(x, x, x, x);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) g4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         {
             const int tv = tid >> 2, cv = 32 * (tid & 3);
-            const bool vok = tv < nv && cv < dv;
+            const bool vok = tv >= lo && tv < hi && cv < dv;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 v4[j] = vok ? *reinterpret_cast<const uint4*>(sm + ST_V + (tv * dv + cv + 8 * j) * 2) : make_uint4(0u, 0u, 0u, 0u);
@@ -481,7 +508,7 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         if (!cta_wait(&mb[0], ph_mma & 1, false)) { ok = false; break; }
         ++ph_mma;
         // [Km; Qm] and Kb are dead until the next chunk: stage that chunk's inputs there
-        if (tid == 0 && c + NPREP_CTAS < nchunks) issue_input_tma(tmaps, p, sm, c + NPREP_CTAS, t0, h, &mb[3]);
+        if (tid == 0 && c + NPREP_CTAS < nchunks) issue_input_tma<DECAY>(tmaps, p, sm, c + NPREP_CTAS, g, h, &mb[3]);
         if (tid == ST_THREAD) {
             if (kk >= 2)
                 ring_ok = tc::mbar_wait_cluster_bounded(&mb[1 + (kk & 1)], ((kk - 2) >> 1) & 1, kWaitLimitNs) != 0;
@@ -686,7 +713,7 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
 // ============================================================================
 // Chain CTA: the sequential state recurrence of one (sequence, head).
 // ============================================================================
-__device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm, int n, int h, int t0, int len,
+__device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm, int n, int h, const SeqGrid& g,
                            size_t cl) {
     uint8_t* Sb = sm + K_S;
     uint64_t* mb = reinterpret_cast<uint64_t*>(sm + K_BAR);
@@ -698,7 +725,7 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
     const int H = p.H, dk = p.dk, dv = p.dv;
     const bool col_ok = 64 * wg < dv;
     const size_t vtok_stride = static_cast<size_t>(H) * dv;
-    const int nchunks = (len + C - 1) / C;
+    const int nchunks = g.nchunks, len = g.len;
 
     if (warp == 0) tc::tmem_alloc(s_tmem, TM_CHAIN_COLS);
     cta_sync_tc();
@@ -711,11 +738,14 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
     const uint32_t prep_free = tc::smem_u32(sm + P_BAR + 8);  // local offset of the prep CTAs' ring barriers
     const uint8_t* ring = p.ws + cl * WS_BYTES_PER_CLUSTER;
 
+    // this sequence's first checkpoint slot: the stride multiples strictly inside
+    // (s, s + len) of every earlier sequence, plus its end
     long long slot_ck = 0;
     if (p.ckpt && p.ckpt_stride > 0) {
         for (int m = 0; m < n; ++m) {
-            const int lm = p.cu_seqlens[m + 1] - p.cu_seqlens[m];
-            slot_ck += (lm + p.ckpt_stride - 1) / p.ckpt_stride;
+            const long long lm = p.cu_seqlens[m + 1] - p.cu_seqlens[m];
+            const long long sm0 = p.start_pos ? p.start_pos[m] : 0;
+            if (lm > 0) slot_ck += (sm0 + lm - 1) / p.ckpt_stride - sm0 / p.ckpt_stride + 1;
         }
     }
     float S[64];
@@ -780,8 +810,8 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
     };
     if (nchunks > 0) write_sb();
     for (int c = 0; c < nchunks; ++c) {
-        const int cs = t0 + c * C;
-        const int nv = min(C, len - c * C);
+        const int cs = g.row0(c);                       // packed row of chunk row 0
+        const int lo = g.lo(c), hi = g.hi(c);           // the sequence's rows of this chunk
         const int s = c & 1;
         uint8_t* slot = sm + K_SLOT + s * H_STRIDE;
         const uint32_t d1 = (s ? TM_D1B : TM_D1A);
@@ -826,7 +856,7 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
         if (d >= 64 && col_ok) {                         // O rows (TMEM lanes 64..127) while D3 runs
             const int t = d - 64;
             const uint32_t oaddr = lane_base + d1 + cb;
-            if (!p.out_f32 && nv == C) {
+            if (!p.out_f32 && lo == 0 && hi == C) {
                 // staged as a 128B-swizzled bf16 tile per warpgroup, written out by one TMA store
                 float a[64];
                 tmem_ld64(oaddr, a);
@@ -848,13 +878,15 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
                     tc::bulk_commit();
                 }
             } else {
-                const size_t ob = static_cast<size_t>(cs + t) * vtok_stride + static_cast<size_t>(h) * dv + 64 * wg;
+                const bool row_ok = t >= lo && t < hi;
+                const size_t ob = row_ok ? static_cast<size_t>(cs + t) * vtok_stride + static_cast<size_t>(h) * dv + 64 * wg
+                                         : 0;
 #pragma unroll
                 for (int c16 = 0; c16 < 64; c16 += 16) {
                     float a[16];
                     tc::tmem_ld16(oaddr + c16, a);
                     tc::tmem_wait_ld();
-                    if (t < nv) {
+                    if (row_ok) {
                         if (p.out_f32) {
                             float* op = reinterpret_cast<float*>(p.out) + ob + c16;
 #pragma unroll
@@ -891,8 +923,8 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
         if (c + 1 < nchunks) write_sb();
         // -- prefix-cache checkpoint at stride multiples and at the sequence end --
         if (p.ckpt && p.ckpt_stride > 0) {
-            const int done = c * C + nv;
-            if (done % p.ckpt_stride == 0 || done == len) {
+            const int done = g.done(c);                 // tokens of the sequence through this chunk
+            if ((g.start + done) % p.ckpt_stride == 0 || done == len) {
                 if (d < dk && col_ok) {
                     float* cp = p.ckpt + ((static_cast<size_t>(slot_ck) * H + h) * dk + d) * dv + 64 * wg;
 #pragma unroll
@@ -926,6 +958,7 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
     if (warp == 0) tc::tmem_dealloc(tm, TM_CHAIN_COLS);
 }
 
+template <int DECAY>
 __global__ void __launch_bounds__(NT, 1) kda_prefill_kernel(const Params p, const __grid_constant__ TensorMaps tmaps)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -934,8 +967,12 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_kernel(const Params p, cons
     const int cl = blockIdx.x / CLUSTER;                  // (sequence, head)
     const int h = cl % p.H;
     const int n = cl / p.H;
-    const int t0 = p.cu_seqlens[n];
-    const int len = p.cu_seqlens[n + 1] - t0;
+    SeqGrid g;
+    g.t0 = p.cu_seqlens[n];
+    g.len = p.cu_seqlens[n + 1] - g.t0;
+    g.start = p.start_pos ? p.start_pos[n] : 0;
+    g.off = static_cast<int>(g.start % C);
+    g.nchunks = g.len > 0 ? (g.len + g.off + C - 1) / C : 0;
 
     // every CTA initialises its barriers before any peer can touch them
     if (threadIdx.x == 0) {
@@ -949,8 +986,8 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_kernel(const Params p, cons
         tc::mbar_fence_init();
     }
     tc::cluster_sync();
-    if (rank == 0) chain_role(p, tmaps, sm, n, h, t0, len, static_cast<size_t>(cl));
-    else prep_role(p, tmaps, sm, rank - 1, h, t0, len, static_cast<size_t>(cl));
+    if (rank == 0) chain_role(p, tmaps, sm, n, h, g, static_cast<size_t>(cl));
+    else prep_role<DECAY>(p, tmaps, sm, rank - 1, h, g, static_cast<size_t>(cl));
     // no CTA leaves while a peer may still address its shared memory
     tc::cluster_sync();
 }
@@ -998,21 +1035,25 @@ size_t prefill_workspace_bytes(int num_seqs, int H) {
 int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* la,
                    const uint16_t* beta, const float* init_state, const int32_t* cu_seqlens,
                    int num_seqs, int total_tokens, int H, int Dk, int Dv, void* out, int out_f32,
-                   float* final_state, float* ckpt, int ckpt_stride, int decay, void* ws, int* status,
-                   cudaStream_t stream)
+                   float* final_state, float* ckpt, int ckpt_stride, int decay, const int32_t* start_pos,
+                   void* ws, int* status, cudaStream_t stream)
 {
     using namespace prefill;
-    static bool attr_done = false;
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(kda_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (decay != DECAY_CHANNEL && decay != DECAY_HEAD && decay != DECAY_NONE) return -3;
+    void (*kern)(const Params, const TensorMaps) = decay == DECAY_CHANNEL ? kda_prefill_kernel<DECAY_CHANNEL>
+                                                 : decay == DECAY_HEAD ? kda_prefill_kernel<DECAY_HEAD>
+                                                                       : kda_prefill_kernel<DECAY_NONE>;
+    static bool attr_done[3] = {false, false, false};
+    if (!attr_done[decay]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(SMEM_BYTES)) != cudaSuccess) return -3;
-        attr_done = true;
+        attr_done[decay] = true;
     }
     Params p;
     p.q = q; p.k = k; p.v = v; p.la = la; p.beta = beta; p.init_state = init_state;
-    p.cu_seqlens = cu_seqlens; p.out = out; p.final_state = final_state; p.ckpt = ckpt;
+    p.cu_seqlens = cu_seqlens; p.start_pos = start_pos; p.out = out; p.final_state = final_state; p.ckpt = ckpt;
     p.ws = static_cast<uint8_t*>(ws);
-    p.status = status; p.out_f32 = out_f32; p.ckpt_stride = ckpt_stride; p.decay = decay;
+    p.status = status; p.out_f32 = out_f32; p.ckpt_stride = ckpt_stride;
     p.H = H; p.dk = Dk; p.dv = Dv;
     const long long clusters = static_cast<long long>(num_seqs) * H;
     if (clusters == 0 || total_tokens == 0) {
@@ -1050,7 +1091,7 @@ int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kda_prefill_kernel, p, tmaps) != cudaSuccess) return -3;
+    if (cudaLaunchKernelEx(&cfg, kern, p, tmaps) != cudaSuccess) return -3;
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

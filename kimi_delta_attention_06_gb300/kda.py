@@ -66,7 +66,7 @@ def load():
                 fn.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp, _vp, _i, _vp]
             lib.kda_chunk_prefill_ex.restype = _i
             lib.kda_chunk_prefill_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i,
-                                                 _vp, _vp, _i, _i, _vp]
+                                                 _vp, _vp, _i, _i, _vp, _vp, _vp]
             lib.kda_decode_step.restype = _i
             lib.kda_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]
             lib.kda_decode_multi.restype = _i
@@ -74,6 +74,8 @@ def load():
                                              _i, _i, _i, _i, _i, _i, _vp]
             lib.kda_ckpt_count.restype = ctypes.c_int64
             lib.kda_ckpt_count.argtypes = [_vp, _i, _i]
+            lib.kda_ckpt_count_ex.restype = ctypes.c_int64
+            lib.kda_ckpt_count_ex.argtypes = [_vp, _vp, _i, _i]
             lib.kda_device_status.restype = _i
             lib.kda_device_status.argtypes = [_vp]
             lib.kda_status_string.restype = ctypes.c_char_p
@@ -129,16 +131,25 @@ def kda_ckpt_count(cu_seqlens_host: torch.Tensor, ckpt_stride: int) -> int:
     return int(n)
 
 
+def kda_ckpt_count_ex(cu_seqlens_host: torch.Tensor, start_pos_host, ckpt_stride: int) -> int:
+    cu = cu_seqlens_host.to(device="cpu", dtype=torch.int32).contiguous()
+    sp = None if start_pos_host is None else start_pos_host.to(device="cpu", dtype=torch.int32).contiguous()
+    n = load().kda_ckpt_count_ex(ctypes.c_void_p(cu.data_ptr()), None if sp is None else ctypes.c_void_p(sp.data_ptr()),
+                                 cu.numel() - 1, int(ckpt_stride))
+    if n < 0:
+        raise KdaError(KDA_ERR_INVALID_ARG, "kda_ckpt_count_ex")
+    return int(n)
+
+
 def _call_prefill(name, q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host, num_seqs,
-                  total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, stream,
-                  *extra):
+                  total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, stream):
     cu_host = cu_seqlens_host.to(device="cpu", dtype=torch.int32).contiguous()
     rc = getattr(load(), name)(
         _ptr(_bits16(q)), _ptr(_bits16(k)), _ptr(_bits16(v)), _ptr(log_alpha), _ptr(_bits16(beta)),
         _ptr(init_state), _ptr(cu_seqlens), ctypes.c_void_p(cu_host.data_ptr()),
         int(num_seqs), int(total_tokens), int(H), int(Dk), int(Dv),
         _ptr(out), int(out_dtype), _ptr(final_state), _ptr(ckpt_states), int(ckpt_stride),
-        *[int(x) for x in extra], _stream(stream))
+        _stream(stream))
     _check(rc, name)
 
 
@@ -151,10 +162,17 @@ def kda_chunk_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqle
 
 def kda_chunk_prefill_ex(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host,
                          num_seqs: int, total_tokens: int, H: int, Dk: int, Dv: int,
-                         out, out_dtype: int, final_state, ckpt_states, ckpt_stride: int, decay: int, stream=None):
-    _call_prefill("kda_chunk_prefill_ex", q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host,
-                  num_seqs, total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, stream,
-                  decay)
+                         out, out_dtype: int, final_state, ckpt_states, ckpt_stride: int, decay: int,
+                         start_pos=None, start_pos_host=None, stream=None):
+    sp_host = None if start_pos_host is None else start_pos_host.to(device="cpu", dtype=torch.int32).contiguous()
+    cu_host = cu_seqlens_host.to(device="cpu", dtype=torch.int32).contiguous()
+    rc = load().kda_chunk_prefill_ex(
+        _ptr(_bits16(q)), _ptr(_bits16(k)), _ptr(_bits16(v)), _ptr(log_alpha), _ptr(_bits16(beta)),
+        _ptr(init_state), _ptr(cu_seqlens), ctypes.c_void_p(cu_host.data_ptr()),
+        int(num_seqs), int(total_tokens), int(H), int(Dk), int(Dv),
+        _ptr(out), int(out_dtype), _ptr(final_state), _ptr(ckpt_states), int(ckpt_stride), int(decay),
+        _ptr(start_pos), None if sp_host is None else ctypes.c_void_p(sp_host.data_ptr()), _stream(stream))
+    _check(rc, "kda_chunk_prefill_ex")
 
 
 def kda_chunk_prefill_noalloc(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host,
@@ -195,9 +213,9 @@ def kda_device_status(stream=None) -> int:
 
 def prefill(q, k, v, log_alpha, beta, cu_seqlens_host, init_state=None, ckpt_stride: int = 0,
             out_dtype=torch.bfloat16, want_final: bool = True, cu_seqlens=None, stream=None,
-            decay: int = KDA_DECAY_CHANNEL):
+            decay: int = KDA_DECAY_CHANNEL, start_pos_host=None):
     """Allocate outputs and run kda_chunk_prefill (kda_chunk_prefill_ex for another decay
-    layout).  Returns (out, final_state, ckpt_states)."""
+    layout or for start positions).  Returns (out, final_state, ckpt_states)."""
     T, H, Dk = q.shape
     Dv = v.shape[2]
     cu_host = cu_seqlens_host.to(device="cpu", dtype=torch.int32).contiguous()
@@ -207,15 +225,17 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens_host, init_state=None, ckpt_str
         cu_seqlens = cu_host.to(dev, non_blocking=False)
     out = torch.empty(T, H, Dv, device=dev, dtype=out_dtype)
     fin = torch.empty(N, H, Dk, Dv, device=dev, dtype=torch.float32) if want_final else None
-    nck = kda_ckpt_count(cu_host, ckpt_stride) if ckpt_stride > 0 else 0
+    nck = kda_ckpt_count_ex(cu_host, start_pos_host, ckpt_stride) if ckpt_stride > 0 else 0
     ck = torch.empty(nck, H, Dk, Dv, device=dev, dtype=torch.float32) if ckpt_stride > 0 else None
     odt = KDA_OUT_F32 if out_dtype == torch.float32 else KDA_OUT_BF16
-    if decay == KDA_DECAY_CHANNEL:
+    if decay == KDA_DECAY_CHANNEL and start_pos_host is None:
         kda_chunk_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_host, N, T, H, Dk, Dv,
                           out, odt, fin, ck if nck > 0 else None, ckpt_stride, stream)
     else:
+        sp = None if start_pos_host is None else start_pos_host.to(device="cpu", dtype=torch.int32).contiguous()
         kda_chunk_prefill_ex(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_host, N, T, H, Dk, Dv,
-                             out, odt, fin, ck if nck > 0 else None, ckpt_stride, decay, stream)
+                             out, odt, fin, ck if nck > 0 else None, ckpt_stride, decay,
+                             None if sp is None else sp.to(dev), sp, stream)
     return out, fin, ck
 
 

@@ -54,7 +54,8 @@ def main(argv=None):
 
         def run():
             kda.kda_chunk_prefill_ex(c.q, c.k, c.v, la, c.beta, c.init_state, cu, c.cu_seqlens, N, T, a.H, a.D,
-                                     a.D, out, kda.KDA_OUT_BF16, fin, ck if nck else None, a.ckpt, decay, stream)
+                                     a.D, out, kda.KDA_OUT_BF16, fin, ck if nck else None, a.ckpt, decay,
+                                     stream=stream)
         units, count = f"{T} tokens, {N} sequences, decay {a.decay}", T
     elif a.what == "decode_multi":
         d = workloads.decode_case(N=a.N, H=a.H, D=a.D, steps=a.K, seed=4, device=dev)

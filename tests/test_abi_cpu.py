@@ -143,16 +143,32 @@ def test_prefill_ex_decay_rules_on_host(lib):
         cu = (ctypes.c_int32 * 3)(0, 64, 100)
         a = dict(q=0x1000, k=0x2000, v=0x3000, la=0x4000, beta=0x5000, s0=None, cu=0x6000,
                  cu_host=ctypes.cast(cu, ctypes.c_void_p), N=2, T=100, H=4, Dk=64, Dv=64,
-                 out=0x7000, out_dtype=0, fin=None, ck=None, stride=0, stream=None)
+                 out=0x7000, out_dtype=0, fin=None, ck=None, stride=0, sp=None, sp_host=None, stream=None)
         a.update(over)
         return getattr(lib, f)(a["q"], a["k"], a["v"], a["la"], a["beta"], a["s0"], a["cu"], a["cu_host"], a["N"],
                                a["T"], a["H"], a["Dk"], a["Dv"], a["out"], a["out_dtype"], a["fin"], a["ck"],
-                               a["stride"], decay, a["stream"])
+                               a["stride"], decay, a["sp"], a["sp_host"], a["stream"])
     assert raw(kda.KDA_DECAY_HEAD, H=6) == kda.KDA_ERR_UNSUPPORTED     # per-head rows need H % 4 == 0
     assert raw(kda.KDA_DECAY_NONE) == kda.KDA_ERR_INVALID_ARG          # log_alpha given but unused
     assert raw(kda.KDA_DECAY_CHANNEL, la=None) == kda.KDA_ERR_INVALID_ARG
     assert raw(7) == kda.KDA_ERR_INVALID_ARG
     assert raw(kda.KDA_DECAY_NONE, la=None, N=0, T=0) == kda.KDA_OK
+    sp = (ctypes.c_int32 * 2)(5, -1)
+    assert raw(kda.KDA_DECAY_CHANNEL, sp=0x9000) == kda.KDA_ERR_INVALID_ARG       # device copy without host copy
+    assert raw(kda.KDA_DECAY_CHANNEL, sp=0x9000,
+               sp_host=ctypes.cast(sp, ctypes.c_void_p)) == kda.KDA_ERR_INVALID_ARG   # negative position
+
+
+def test_ckpt_count_with_start_positions(lib):
+    cu = torch.tensor([0, 9, 9, 100], dtype=torch.int32)
+    # s = 6, len 9, stride 4: absolute 8, 12 and the end; empty: none; s = 0, len 91: ceil(91/4) = 23
+    assert kda.kda_ckpt_count_ex(cu, torch.tensor([6, 3, 0], dtype=torch.int32), 4) == 3 + 0 + 23
+    assert kda.kda_ckpt_count_ex(cu, None, 4) == kda.kda_ckpt_count(cu, 4) == 3 + 0 + 23
+    # 145408 tokens continuing a 40000-token prefix: absolute 65536, 98304, 131072, 163840 and the end
+    assert kda.kda_ckpt_count_ex(torch.tensor([0, 145408], dtype=torch.int32),
+                                 torch.tensor([40000], dtype=torch.int32), 32768) == 5
+    with pytest.raises(kda.KdaError):
+        kda.kda_ckpt_count_ex(cu, torch.tensor([0, -1, 0], dtype=torch.int32), 4)
 
 
 def test_binding_refuses_non_bf16(lib):
