@@ -36,7 +36,7 @@ T_PROMPT, H, D, CKPT = 145408, 32, 128, 32768
 DEC_N = 512
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 
-# Algorithmic bytes (see DESIGN.md "Roofline"): per token per head q, k, v bf16
+# Algorithmic bytes: per token per head q, k, v bf16
 # (3 x 256 B), log_alpha fp32 (512 B), beta bf16 (2 B), o bf16 (256 B).
 BYTES_PER_TOKEN_HEAD = 3 * 2 * D + 4 * D + 2 + 2 * D           # 1538
 STATE_BYTES = 4 * D * D                                          # one fp32 head state

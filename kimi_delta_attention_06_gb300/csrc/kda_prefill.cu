@@ -815,10 +815,9 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
         const int s = c & 1;
         uint8_t* slot = sm + K_SLOT + s * H_STRIDE;
         const uint32_t d1 = (s ? TM_D1B : TM_D1A);
-        if (tid == 0) {
-            if (issued == c && load_ok) load_ok = load(c, true);
-            probe(c + 2);
-        }
+        // (the next chunk's load is probed once this chunk's MMA is under way, not here,
+        // where every thread waits for thread 0)
+        if (tid == 0 && issued == c && load_ok) load_ok = load(c, true);
         if (!cta_wait(&mb[KB_FULL + s], (c >> 1) & 1, false)) { ok = false; break; }
         waited = c + 1;
         if (tid == 0) {

@@ -1,4 +1,4 @@
-"""GPU parity of prefix continuations (SURVEY NEXT f4): kda_chunk_prefill_ex with start
+"""GPU parity of prefix continuations: kda_chunk_prefill_ex with start
 positions, whose chunk grid and checkpoints sit on each prompt's absolute grid."""
 import numpy as np
 import pytest

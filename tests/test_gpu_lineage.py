@@ -1,4 +1,4 @@
-"""GPU parity of the lineage specialisations: Gated DeltaNet (one
+"""GPU parity of the lineage specialisations of the kernels: Gated DeltaNet (one
 log-decay per head and token) and DeltaNet (no decay), for the prefill
 (kda_chunk_prefill_ex) and the serving decode (kda_decode_multi).
 
