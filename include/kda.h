@@ -211,6 +211,49 @@ int kda_decode_multi(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                      void* out, int out_dtype,
                      int N, int K, int H, int Dk, int Dv, int decay, void* stream);
 
+/*
+ * kda_prepare_inputs -- the KDA module's input preparation in one pass (the module of
+ * the Kimi K3 primer, wiki summary, section 3: a short causal convolution of the
+ * projections, an L2 norm on q and k, the alpha and beta gates).  Writes exactly the
+ * inputs kda_chunk_prefill reads.
+ *
+ *   xq, xk, xv  (device) bf16 [total_tokens, H, D]: the raw projections
+ *   conv_w      (device) fp32 [3, H, D, KDA_CONV_WIDTH]: depthwise taps of q, k, v,
+ *               oldest tap first:  y[t] = sum_j conv_w[..., j] x[t - (W - 1) + j]
+ *   conv_state  (device) bf16 [num_seqs, 3, KDA_CONV_WIDTH - 1, H, D] or NULL: each
+ *               sequence's carried-in raw inputs (oldest first) for positions before its
+ *               first token (a prefix continuation); NULL = zeros
+ *   a_raw       (device) fp32 [total_tokens, H, D]: alpha-gate pre-activation
+ *   b_raw       (device) bf16 [total_tokens, H]: beta pre-activation
+ *   cu_seqlens  (device) / cu_seqlens_host: as for kda_chunk_prefill; the convolution
+ *               never reaches across a sequence start
+ *   conv_act    0 = the convolution alone, 1 = followed by SiLU
+ *   q, k        (device) bf16 [total_tokens, H, D]: act(conv) / sqrt(sum_c act(conv)^2 + 1e-6)
+ *   v           (device) bf16 [total_tokens, H, D]: act(conv)
+ *   log_alpha   (device) fp32 [total_tokens, H, D]: -softplus(a_raw)
+ *   beta        (device) bf16 [total_tokens, H]: sigmoid(b_raw)
+ * D in {64, 128}.
+ */
+#define KDA_CONV_WIDTH 4
+int kda_prepare_inputs(const uint16_t* xq, const uint16_t* xk, const uint16_t* xv,
+                       const float* conv_w, const uint16_t* conv_state,
+                       const float* a_raw, const uint16_t* b_raw,
+                       const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                       int num_seqs, int total_tokens, int H, int D, int conv_act,
+                       uint16_t* q, uint16_t* k, uint16_t* v, float* log_alpha, uint16_t* beta,
+                       void* stream);
+
+/*
+ * kda_output_norm -- the module's per-head output norm (same section):
+ *   y[t, h, :] = o[t, h, :] / sqrt(mean_c o[t, h, c]^2 + eps) * gamma[h, :]
+ *   o      (device) [total_tokens, H, Dv], bf16 or fp32 per o_dtype (kda_out_dtype)
+ *   gamma  (device) fp32 [H, Dv];  eps >= 0
+ *   y      (device) bf16 [total_tokens, H, Dv] (may alias o when o is bf16)
+ * Dv in {64, 128}.
+ */
+int kda_output_norm(const void* o, int o_dtype, const float* gamma, float eps,
+                    uint16_t* y, int total_tokens, int H, int Dv, void* stream);
+
 /* Number of checkpoint slots kda_chunk_prefill writes: sum over sequences of
  * ceil(len / ckpt_stride) (0 when ckpt_stride == 0).  cu_seqlens_host is a host
  * array of num_seqs + 1 offsets.  Returns -1 on invalid arguments. */

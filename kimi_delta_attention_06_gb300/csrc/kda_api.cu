@@ -20,6 +20,13 @@ int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
                    float* final_state, float* ckpt, int ckpt_stride, int decay, const int32_t* start_pos,
                    void* ws, int* status, cudaStream_t stream);
 size_t prefill_workspace_bytes(int num_seqs, int H);
+int launch_prepare_inputs(const uint16_t* xq, const uint16_t* xk, const uint16_t* xv, const float* conv_w,
+                          const uint16_t* conv_state, const float* a_raw, const uint16_t* b_raw,
+                          const int32_t* cu_seqlens, int num_seqs, int T, int H, int D, int act,
+                          uint16_t* q, uint16_t* k, uint16_t* v, float* log_alpha, uint16_t* beta,
+                          int* status, cudaStream_t stream);
+int launch_output_norm(const void* o, int o_f32, const float* gamma, float eps, uint16_t* y, int T, int H, int D,
+                       cudaStream_t stream);
 int launch_decode_multi(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* log_alpha,
                         const uint16_t* beta, float* pool, int num_slots, const int32_t* slots,
                         const int32_t* ntok, int commit, void* out, int out_f32,
@@ -314,6 +321,60 @@ int kda_decode_multi(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     rc = kda::launch_decode_multi(q, k, v, log_alpha, beta, state_pool, num_slots, state_slots, num_tokens, commit,
                                   out, out_dtype == KDA_OUT_F32, N, K, H, Dk, decay, status,
                                   static_cast<cudaStream_t>(stream));
+    return rc == 0 ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_prepare_inputs(const uint16_t* xq, const uint16_t* xk, const uint16_t* xv,
+                       const float* conv_w, const uint16_t* conv_state,
+                       const float* a_raw, const uint16_t* b_raw,
+                       const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                       int num_seqs, int total_tokens, int H, int D, int conv_act,
+                       uint16_t* q, uint16_t* k, uint16_t* v, float* log_alpha, uint16_t* beta,
+                       void* stream) {
+    if (num_seqs < 0 || total_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return KDA_ERR_UNSUPPORTED;
+    if (conv_act != 0 && conv_act != 1) return KDA_ERR_INVALID_ARG;
+    if (num_seqs > 0 && (!cu_seqlens || !cu_seqlens_host)) return KDA_ERR_INVALID_ARG;
+    if (num_seqs > 0) {
+        if (cu_seqlens_host[0] != 0 || cu_seqlens_host[num_seqs] != total_tokens) return KDA_ERR_INVALID_ARG;
+        for (int n = 0; n < num_seqs; ++n)
+            if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
+    } else if (total_tokens != 0) {
+        return KDA_ERR_INVALID_ARG;
+    }
+    if (total_tokens == 0) return KDA_OK;
+    const void* need[] = {xq, xk, xv, conv_w, a_raw, b_raw, q, k, v, log_alpha, beta};
+    for (const void* p : need)
+        if (!p) return KDA_ERR_INVALID_ARG;
+    const void* a16[] = {xq, xk, xv, conv_w, conv_state, a_raw, q, k, v, log_alpha};
+    for (const void* p : a16)
+        if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(b_raw) & 1u) || (reinterpret_cast<uintptr_t>(beta) & 1u) ||
+        (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
+        return KDA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(total_tokens) * H * D >= (int64_t(1) << 40)) return KDA_ERR_INVALID_ARG;
+    int* status = nullptr;
+    int rc = device_setup(&status);
+    if (rc != KDA_OK) return rc;
+    rc = kda::launch_prepare_inputs(xq, xk, xv, conv_w, conv_state, a_raw, b_raw, cu_seqlens, num_seqs, total_tokens,
+                                    H, D, conv_act, q, k, v, log_alpha, beta, status,
+                                    static_cast<cudaStream_t>(stream));
+    return rc == 0 ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_output_norm(const void* o, int o_dtype, const float* gamma, float eps,
+                    uint16_t* y, int total_tokens, int H, int Dv, void* stream) {
+    if (total_tokens < 0 || H <= 0 || !(eps >= 0.f)) return KDA_ERR_INVALID_ARG;
+    if (o_dtype != KDA_OUT_BF16 && o_dtype != KDA_OUT_F32) return KDA_ERR_INVALID_ARG;
+    if (Dv != 64 && Dv != 128) return KDA_ERR_UNSUPPORTED;
+    if (total_tokens == 0) return KDA_OK;
+    if (!o || !gamma || !y) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(o) || !aligned16(gamma) || !aligned16(y)) return KDA_ERR_INVALID_ARG;
+    int* status = nullptr;
+    int rc = device_setup(&status);
+    if (rc != KDA_OK) return rc;
+    rc = kda::launch_output_norm(o, o_dtype == KDA_OUT_F32, gamma, eps, y, total_tokens, H, Dv,
+                                 static_cast<cudaStream_t>(stream));
     return rc == 0 ? KDA_OK : KDA_ERR_CUDA;
 }
 

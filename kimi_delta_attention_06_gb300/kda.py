@@ -1,7 +1,8 @@
 """Thin ctypes binding of the KDA C ABI (include/kda.h).
 
 The functions named like the C entry points (``kda_chunk_prefill``,
-``kda_chunk_prefill_ex``, ``kda_chunk_prefill_noalloc``, ``kda_decode_step``, ``kda_decode_multi``, ``kda_ckpt_count``,
+``kda_chunk_prefill_ex``, ``kda_chunk_prefill_noalloc``, ``kda_decode_step``,
+``kda_prepare_inputs``, ``kda_output_norm``, ``kda_decode_multi``, ``kda_ckpt_count``,
 ``kda_device_status``, ``kda_status_string``, ``kda_chunk_size``) only marshal
 arguments: torch
 tensors become raw device pointers, the current torch stream becomes the
@@ -72,6 +73,11 @@ def load():
             lib.kda_decode_multi.restype = _i
             lib.kda_decode_multi.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _i,
                                              _i, _i, _i, _i, _i, _i, _vp]
+            lib.kda_prepare_inputs.restype = _i
+            lib.kda_prepare_inputs.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                               _vp, _vp, _vp, _vp, _vp, _vp]
+            lib.kda_output_norm.restype = _i
+            lib.kda_output_norm.argtypes = [_vp, _i, _vp, ctypes.c_float, _vp, _i, _i, _i, _vp]
             lib.kda_ckpt_count.restype = ctypes.c_int64
             lib.kda_ckpt_count.argtypes = [_vp, _i, _i]
             lib.kda_ckpt_count_ex.restype = ctypes.c_int64
@@ -199,6 +205,25 @@ def kda_decode_multi(q, k, v, log_alpha, beta, state_pool, num_slots: int, state
                                  _ptr(num_tokens), int(commit), _ptr(out), int(out_dtype),
                                  int(N), int(K), int(H), int(Dk), int(Dv), int(decay), _stream(stream))
     _check(rc, "kda_decode_multi")
+
+
+def kda_prepare_inputs(xq, xk, xv, conv_w, conv_state, a_raw, b_raw, cu_seqlens, cu_seqlens_host,
+                       num_seqs: int, total_tokens: int, H: int, D: int, conv_act: int,
+                       q, k, v, log_alpha, beta, stream=None):
+    cu_host = cu_seqlens_host.to(device="cpu", dtype=torch.int32).contiguous()
+    rc = load().kda_prepare_inputs(_ptr(_bits16(xq)), _ptr(_bits16(xk)), _ptr(_bits16(xv)), _ptr(conv_w),
+                                   _ptr(None if conv_state is None else _bits16(conv_state)), _ptr(a_raw),
+                                   _ptr(_bits16(b_raw)), _ptr(cu_seqlens), ctypes.c_void_p(cu_host.data_ptr()),
+                                   int(num_seqs), int(total_tokens), int(H), int(D), int(conv_act),
+                                   _ptr(_bits16(q)), _ptr(_bits16(k)), _ptr(_bits16(v)), _ptr(log_alpha),
+                                   _ptr(_bits16(beta)), _stream(stream))
+    _check(rc, "kda_prepare_inputs")
+
+
+def kda_output_norm(o, o_dtype: int, gamma, eps: float, y, total_tokens: int, H: int, Dv: int, stream=None):
+    rc = load().kda_output_norm(_ptr(o), int(o_dtype), _ptr(gamma), float(eps), _ptr(_bits16(y)),
+                                int(total_tokens), int(H), int(Dv), _stream(stream))
+    _check(rc, "kda_output_norm")
 
 
 def kda_debug_expire_wait(limit_ns: int, stream=None):

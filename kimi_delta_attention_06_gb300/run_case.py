@@ -5,6 +5,8 @@
       (prefill / varlen also take --decay channel|head|none: KDA, Gated DeltaNet, DeltaNet)
   python -m kimi_delta_attention_06_gb300.run_case --what decode --N 512 [--H 32] [--D 128] [--reps 2]
   python -m kimi_delta_attention_06_gb300.run_case --what decode_multi --N 512 --K 4 [--commit 1] [--reps 2]
+  python -m kimi_delta_attention_06_gb300.run_case --what prep --T 145408 [--reps 2]     (input preparation)
+  python -m kimi_delta_attention_06_gb300.run_case --what outnorm --T 145408 [--reps 2]  (output norm)
 
 Inputs are the seeded synthetic tensors of workloads.py, generated on the GPU
 (varlen: 16 packed sequences of log-uniform length, about 280k tokens).
@@ -22,7 +24,8 @@ from . import build, kda, workloads
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--what", choices=["prefill", "varlen", "decode", "decode_multi"], default="prefill")
+    ap.add_argument("--what", choices=["prefill", "varlen", "decode", "decode_multi", "prep", "outnorm"],
+                    default="prefill")
     ap.add_argument("--K", type=int, default=4, help="tokens per sequence (decode_multi)")
     ap.add_argument("--commit", type=int, default=0, help="decode_multi: 1 writes the states back")
     ap.add_argument("--decay", choices=["channel", "head", "none"], default="channel",
@@ -57,6 +60,33 @@ def main(argv=None):
                                      a.D, out, kda.KDA_OUT_BF16, fin, ck if nck else None, a.ckpt, decay,
                                      stream=stream)
         units, count = f"{T} tokens, {N} sequences, decay {a.decay}", T
+    elif a.what in ("prep", "outnorm"):
+        g = torch.Generator(device=dev).manual_seed(6)
+        T, H, D = a.T, a.H, a.D
+        cu_host = torch.tensor([0, T], dtype=torch.int32)
+        cu = cu_host.to(dev)
+        if a.what == "prep":
+            xs = [torch.randn(T, H, D, generator=g, device=dev).to(torch.bfloat16) for _ in range(3)]
+            w = torch.randn(3, H, D, 4, generator=g, device=dev) * 0.5
+            ar = torch.randn(T, H, D, generator=g, device=dev) - 2.0
+            br = torch.randn(T, H, generator=g, device=dev).to(torch.bfloat16)
+            outs = [torch.empty(T, H, D, device=dev, dtype=torch.bfloat16) for _ in range(3)]
+            la = torch.empty(T, H, D, device=dev)
+            be = torch.empty(T, H, device=dev, dtype=torch.bfloat16)
+
+            def run():
+                kda.kda_prepare_inputs(xs[0], xs[1], xs[2], w, None, ar, br, cu, cu_host, 1, T, H, D, 1,
+                                       outs[0], outs[1], outs[2], la, be, stream)
+            nbytes = T * H * (3 * 2 * D + 4 * D + 2) * 2          # read and write the same bytes
+        else:
+            o = torch.randn(T, H, D, generator=g, device=dev).to(torch.bfloat16)
+            gam = torch.rand(H, D, generator=g, device=dev) + 0.5
+            y = torch.empty_like(o)
+
+            def run():
+                kda.kda_output_norm(o, kda.KDA_OUT_BF16, gam, 1e-6, y, T, H, D, stream)
+            nbytes = T * H * D * 2 * 2
+        units, count = f"{T} tokens x {H} heads ({nbytes / 1e9:.3f} GB moved)", T
     elif a.what == "decode_multi":
         d = workloads.decode_case(N=a.N, H=a.H, D=a.D, steps=a.K, seed=4, device=dev)
         tok = {key: torch.stack([s[key] for s in d.steps], dim=1).contiguous()

@@ -33,6 +33,7 @@ def _declared_functions():
 def test_header_declares_expected_entry_points():
     names = _declared_functions()
     for n in ["kda_chunk_prefill", "kda_chunk_prefill_noalloc", "kda_decode_step", "kda_decode_multi", "kda_ckpt_count",
+              "kda_chunk_prefill_ex", "kda_ckpt_count_ex", "kda_prepare_inputs", "kda_output_norm",
               "kda_device_status", "kda_status_string", "kda_chunk_size", "kda_debug_expire_wait"]:
         assert n in names
 
@@ -169,6 +170,29 @@ def test_ckpt_count_with_start_positions(lib):
                                  torch.tensor([40000], dtype=torch.int32), 32768) == 5
     with pytest.raises(kda.KdaError):
         kda.kda_ckpt_count_ex(cu, torch.tensor([0, -1, 0], dtype=torch.int32), 4)
+
+
+def test_prepare_and_norm_reject_on_host(lib):
+    cu = (ctypes.c_int32 * 2)(0, 10)
+    cuh = ctypes.cast(cu, ctypes.c_void_p)
+    f = lib.kda_prepare_inputs
+    base = [0x1000, 0x2000, 0x3000, 0x4000, None, 0x5000, 0x6000, 0x7000, cuh, 1, 10, 2, 128, 1,
+            0x8000, 0x9000, 0xA000, 0xB000, 0xC000, None]
+    def call(**kw):
+        a = list(base)
+        for i, val in kw.items():
+            a[int(i[1:])] = val
+        return f(*a)
+    assert call(a12=96) == kda.KDA_ERR_UNSUPPORTED
+    assert call(a13=2) == kda.KDA_ERR_INVALID_ARG          # conv_act is 0 or 1
+    assert call(a0=None) == kda.KDA_ERR_INVALID_ARG
+    assert call(a3=0x4004) == kda.KDA_ERR_INVALID_ARG      # misaligned taps
+    assert call(a6=0x6001) == kda.KDA_ERR_INVALID_ARG      # misaligned beta pre-activation
+    assert call(a10=9) == kda.KDA_ERR_INVALID_ARG          # cu_seqlens end != total_tokens
+    g = lib.kda_output_norm
+    assert g(0x1000, 0, 0x2000, ctypes.c_float(-1.0), 0x3000, 5, 2, 128, None) == kda.KDA_ERR_INVALID_ARG
+    assert g(0x1000, 0, 0x2000, ctypes.c_float(1e-6), 0x3000, 5, 2, 96, None) == kda.KDA_ERR_UNSUPPORTED
+    assert g(0x1000, 0, 0x2000, ctypes.c_float(1e-6), 0x3000, 0, 2, 128, None) == kda.KDA_OK
 
 
 def test_binding_refuses_non_bf16(lib):
