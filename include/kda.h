@@ -90,10 +90,12 @@ typedef enum { KDA_DECAY_CHANNEL = 0, KDA_DECAY_HEAD = 1, KDA_DECAY_NONE = 2 } k
  *               j = 1 .. ceil(len / ckpt_stride) - 1, then the state at its end.
  *   ckpt_stride tokens between checkpoints, a positive multiple of 64, or 0 = none.
  *   stream      cudaStream_t (as void*).
- * Scratch: num_seqs * H * 497664 bytes of device memory for the prep -> chain
- * hand-off ring, taken stream-ordered on `stream` from a memory pool the library
- * owns (it keeps what it reserved, so repeated calls reuse it) and given back on
- * `stream` after the kernel.  Calls on different streams never share scratch.
+ * Scratch: 497664 bytes of device memory per prep -> chain hand-off ring, one ring per
+ * (sequence, head) that can run at the same time (at most SMs / 4, e.g. 38 rings =
+ * 18.9 MB on a 152-SM part, whatever num_seqs * H is), taken stream-ordered on `stream`
+ * from a memory pool the library owns (it keeps what it reserved, so repeated calls
+ * reuse it) and given back on `stream` after the kernel.  Calls on different streams
+ * never share scratch.
  * Returns KDA_OK or a negative kda_status.  Deterministic: identical inputs
  * give bit-identical outputs.
  */

@@ -34,6 +34,21 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2_bits(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Raise a kernel's dynamic shared-memory limit on the current device, once per device
+// (the attribute belongs to the device's copy of the kernel).  `done` holds one flag per
+// device ordinal; setting the attribute twice is harmless, so no lock is needed.
+constexpr int kMaxDevicesAttr = 64;
+inline bool raise_smem_limit(const void* kernel, int bytes, bool (&done)[kMaxDevicesAttr]) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesAttr) return false;
+    if (!done[dev]) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+            return false;
+        done[dev] = true;
+    }
+    return true;
+}
+
 // Record a device-side failure (first writer wins).
 __device__ __forceinline__ void set_status(int* status, int code) {
     if (status) atomicCAS(status, 0, code);

@@ -18,8 +18,9 @@ int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
                    const uint16_t* beta, const float* init_state, const int32_t* cu_seqlens,
                    int num_seqs, int total_tokens, int H, int Dk, int Dv, void* out, int out_f32,
                    float* final_state, float* ckpt, int ckpt_stride, int decay, const int32_t* start_pos,
-                   void* ws, int* status, cudaStream_t stream);
+                   void* ws, int* ring_flags, int ring_count, int* status, cudaStream_t stream);
 size_t prefill_workspace_bytes(int num_seqs, int H);
+int prefill_ring_count(int num_seqs, int H);
 int launch_prepare_inputs(const uint16_t* xq, const uint16_t* xk, const uint16_t* xv, const float* conv_w,
                           const uint16_t* conv_state, const float* a_raw, const uint16_t* b_raw,
                           const int32_t* cu_seqlens, int num_seqs, int T, int H, int D, int act,
@@ -209,12 +210,17 @@ static int prefill_pooled(const uint16_t* q, const uint16_t* k, const uint16_t* 
     rc = workspace_pool(&pool);
     if (rc != KDA_OK) return rc;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // rings for the clusters that can run at once (claimed per cluster), then their flags
+    const int rings = kda::prefill_ring_count(num_seqs, H);
+    if (rings <= 0) return KDA_ERR_CUDA;
+    const size_t ring_bytes = kda::prefill_workspace_bytes(1, rings);
     void* ws = nullptr;
-    if (cudaMallocFromPoolAsync(&ws, kda::prefill_workspace_bytes(num_seqs, H), pool, st) != cudaSuccess)
+    if (cudaMallocFromPoolAsync(&ws, ring_bytes + sizeof(int) * rings, pool, st) != cudaSuccess)
         return KDA_ERR_CUDA;
+    int* flags = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + ring_bytes);
     rc = kda::launch_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, num_seqs, total_tokens, H, Dk, Dv,
                              out, out_dtype == KDA_OUT_F32, final_state, ckpt_states, ckpt_stride, decay,
-                             start_pos, ws, status, st);
+                             start_pos, ws, flags, rings, status, st);
     const bool freed = cudaFreeAsync(ws, st) == cudaSuccess;
     return (rc == 0 && freed) ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -264,7 +270,7 @@ int kda_chunk_prefill_noalloc(const uint16_t* q, const uint16_t* k, const uint16
     if (rc != KDA_OK) return rc;
     rc = kda::launch_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, num_seqs, total_tokens, H, Dk, Dv,
                              out, out_dtype == KDA_OUT_F32, final_state, ckpt_states, ckpt_stride,
-                             KDA_DECAY_CHANNEL, nullptr, scratch, status, static_cast<cudaStream_t>(stream));
+                             KDA_DECAY_CHANNEL, nullptr, scratch, nullptr, 0, status, static_cast<cudaStream_t>(stream));
     return rc == 0 ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -284,10 +284,10 @@ int launch_prepare_inputs(const uint16_t* xq, const uint16_t* xk, const uint16_t
     const dim3 grid(static_cast<unsigned>(ctas));
     const size_t smem = 3 * static_cast<size_t>(kPrepRows + kHalo) * D * 2 + static_cast<size_t>(kPrepRows) * D * 4 + 16;
     if (D == 128) {
-        static bool attr = false;
-        if (!attr && cudaFuncSetAttribute(kda_prepare_inputs_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(smem)) != cudaSuccess) return -3;
-        attr = true;
+        static bool attr_done[kMaxDevicesAttr] = {};
+        if (!raise_smem_limit(reinterpret_cast<const void*>(kda_prepare_inputs_kernel<128>), static_cast<int>(smem),
+                              attr_done))
+            return -3;
         kda_prepare_inputs_kernel<128><<<grid, 256, smem, stream>>>(maps, conv_w, conv_state, b_raw, cu_seqlens,
                                                                     num_seqs, T, H, act, q, k, v, log_alpha, beta,
                                                                     status);

@@ -114,7 +114,8 @@ constexpr int KB_CONS = 4;     // [2] slot consumed
 constexpr int KB_READY = 6;    // [6] ring entry stored by its prep CTA
 constexpr int KB_COUNT = 12;
 constexpr uint32_t K_TMEM = K_BAR + 8 * KB_COUNT;
-constexpr uint32_t K_END = K_TMEM + 16;
+constexpr uint32_t K_RING = K_TMEM + 8;              // index of the hand-off ring this cluster uses
+constexpr uint32_t K_END = K_TMEM + 16;               // (TMEM address, ring index)
 
 constexpr uint32_t SMEM_BYTES = (P_END > K_END ? P_END : K_END) + 1024;   // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -148,7 +149,9 @@ struct Params {
     void* out;
     float* final_state;
     float* ckpt;
-    uint8_t* ws;                 // hand-off ring: WS_BYTES_PER_CLUSTER per cluster
+    uint8_t* ws;                 // hand-off rings, WS_BYTES_PER_CLUSTER each
+    int* ring_flags;             // null: cluster i owns ring i; else [ring_count] claim flags (0 = free)
+    int ring_count;
     int* status;
     int out_f32;
     int ckpt_stride;
@@ -326,7 +329,7 @@ __device__ __forceinline__ void prefetch_inputs(const TensorMaps& tmaps, const P
 // ============================================================================
 template <int DECAY>
 __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm, int pr, int h, const SeqGrid& g,
-                          size_t cl) {
+                          size_t ring_idx) {
     uint8_t* A1 = sm + P_A1;
     uint8_t* B1 = sm + P_B1;
     uint8_t* OUT = sm + P_OUT;
@@ -353,7 +356,7 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
     const uint32_t lane_base = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     // the chain CTA's (rank 0) ring-entry barriers, and this cluster's ring
     const uint32_t chain_ready0 = tc::mapa(tc::smem_u32(sm + K_BAR + 8 * KB_READY), 0);
-    uint8_t* ring = p.ws + cl * WS_BYTES_PER_CLUSTER;
+    uint8_t* ring = p.ws + ring_idx * WS_BYTES_PER_CLUSTER;
     // chunk whose bulk stores may still be in flight (same value in every thread)
     int pending = -1;
     auto publish = [&]() {      // ST_THREAD: once the stores of `pending` are complete, tell the chain
@@ -714,7 +717,7 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
 // Chain CTA: the sequential state recurrence of one (sequence, head).
 // ============================================================================
 __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm, int n, int h, const SeqGrid& g,
-                           size_t cl) {
+                           size_t ring_idx) {
     uint8_t* Sb = sm + K_S;
     uint64_t* mb = reinterpret_cast<uint64_t*>(sm + K_BAR);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + K_TMEM);
@@ -736,7 +739,7 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
     const uint32_t bar_o = 2u + static_cast<uint32_t>(wg);   // named barrier of its 64 O writers
     constexpr int O_ISSUER = 64;                               // O writer (per warpgroup) that issues the TMA store
     const uint32_t prep_free = tc::smem_u32(sm + P_BAR + 8);  // local offset of the prep CTAs' ring barriers
-    const uint8_t* ring = p.ws + cl * WS_BYTES_PER_CLUSTER;
+    const uint8_t* ring = p.ws + ring_idx * WS_BYTES_PER_CLUSTER;
 
     // this sequence's first checkpoint slot: the stride multiples strictly inside
     // (s, s + len) of every earlier sequence, plus its end
@@ -973,11 +976,28 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_kernel(const Params p, cons
     g.off = static_cast<int>(g.start % C);
     g.nchunks = g.len > 0 ? (g.len + g.off + C - 1) / C : 0;
 
+    // The cluster's hand-off ring.  With claim flags, rings are shared among the clusters
+    // that run at any one time: there are at least as many rings as co-resident clusters,
+    // so a starting cluster always finds a free one; the chain CTA claims it and its
+    // prep CTAs read the index from the chain CTA's shared memory.
+    int* s_ring = reinterpret_cast<int*>(sm + K_RING);      // meaningful in the chain CTA
     // every CTA initialises its barriers before any peer can touch them
     if (threadIdx.x == 0) {
         if (rank == 0) {
             uint64_t* mb = reinterpret_cast<uint64_t*>(sm + K_BAR);
             for (int i = 0; i < KB_COUNT; ++i) tc::mbar_init(&mb[i], 1);
+            int got = cl;
+            if (p.ring_flags) {
+                got = -1;
+                const uint64_t t_start = tc::globaltimer_ns();
+                for (int i = cl % p.ring_count;; i = (i + 1 == p.ring_count) ? 0 : i + 1) {
+                    if (atomicCAS(&p.ring_flags[i], 0, 1) == 0) { got = i; break; }
+                    if (tc::globaltimer_ns() - t_start > kWaitLimitNs) break;
+                }
+                if (got < 0) set_status(p.status, kStatusTimeout);
+                tc::fence_proxy_async_global();       // earlier users' copies precede ours
+            }
+            *s_ring = got;
         } else {
             uint64_t* mb = reinterpret_cast<uint64_t*>(sm + P_BAR);
             for (int i = 0; i < 4; ++i) tc::mbar_init(&mb[i], 1);
@@ -985,10 +1005,26 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_kernel(const Params p, cons
         tc::mbar_fence_init();
     }
     tc::cluster_sync();
-    if (rank == 0) chain_role(p, tmaps, sm, n, h, g, static_cast<size_t>(cl));
-    else prep_role<DECAY>(p, tmaps, sm, rank - 1, h, g, static_cast<size_t>(cl));
-    // no CTA leaves while a peer may still address its shared memory
+    int ring_idx;
+    if (rank == 0) {
+        ring_idx = *s_ring;
+    } else {
+        asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(ring_idx) : "r"(tc::mapa(tc::smem_u32(s_ring), 0)));
+    }
+    const bool have_ring = ring_idx >= 0;
+    if (!have_ring) {          // no ring could be claimed (status already records it): touch none
+        g.nchunks = 0;
+        ring_idx = 0;
+    }
+    if (rank == 0) chain_role(p, tmaps, sm, n, h, g, static_cast<size_t>(ring_idx));
+    else prep_role<DECAY>(p, tmaps, sm, rank - 1, h, g, static_cast<size_t>(ring_idx));
+    // no CTA leaves while a peer may still address its shared memory (or its ring)
     tc::cluster_sync();
+    if (rank == 0 && threadIdx.x == 0 && p.ring_flags && have_ring) {
+        tc::fence_proxy_async_global();
+        __threadfence();
+        atomicExch(&p.ring_flags[ring_idx], 0);
+    }
 }
 
 }  // namespace prefill
@@ -1031,27 +1067,39 @@ size_t prefill_workspace_bytes(int num_seqs, int H) {
     return static_cast<size_t>(num_seqs) * static_cast<size_t>(H) * prefill::WS_BYTES_PER_CLUSTER;
 }
 
+// Rings the shared-ring mode needs: never more than the clusters that can be resident at
+// once (each CTA takes most of an SM's shared memory, so at most one per SM).
+int prefill_ring_count(int num_seqs, int H) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    const long long clusters = static_cast<long long>(num_seqs) * H;
+    const long long resident = sms / prefill::CLUSTER;
+    return static_cast<int>(clusters < resident ? clusters : (resident > 0 ? resident : 1));
+}
+
 int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* la,
                    const uint16_t* beta, const float* init_state, const int32_t* cu_seqlens,
                    int num_seqs, int total_tokens, int H, int Dk, int Dv, void* out, int out_f32,
                    float* final_state, float* ckpt, int ckpt_stride, int decay, const int32_t* start_pos,
-                   void* ws, int* status, cudaStream_t stream)
+                   void* ws, int* ring_flags, int ring_count, int* status, cudaStream_t stream)
 {
     using namespace prefill;
     if (decay != DECAY_CHANNEL && decay != DECAY_HEAD && decay != DECAY_NONE) return -3;
     void (*kern)(const Params, const TensorMaps) = decay == DECAY_CHANNEL ? kda_prefill_kernel<DECAY_CHANNEL>
                                                  : decay == DECAY_HEAD ? kda_prefill_kernel<DECAY_HEAD>
                                                                        : kda_prefill_kernel<DECAY_NONE>;
-    static bool attr_done[3] = {false, false, false};
-    if (!attr_done[decay]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(SMEM_BYTES)) != cudaSuccess) return -3;
-        attr_done[decay] = true;
-    }
+    static bool attr_done[3][kMaxDevicesAttr] = {};
+    if (!raise_smem_limit(reinterpret_cast<const void*>(kern), static_cast<int>(SMEM_BYTES), attr_done[decay]))
+        return -3;
     Params p;
     p.q = q; p.k = k; p.v = v; p.la = la; p.beta = beta; p.init_state = init_state;
     p.cu_seqlens = cu_seqlens; p.start_pos = start_pos; p.out = out; p.final_state = final_state; p.ckpt = ckpt;
     p.ws = static_cast<uint8_t*>(ws);
+    p.ring_flags = ring_flags;
+    p.ring_count = ring_count;
+    if (ring_flags && (ring_count <= 0 || cudaMemsetAsync(ring_flags, 0, sizeof(int) * ring_count, stream) != cudaSuccess))
+        return -3;
     p.status = status; p.out_f32 = out_f32; p.ckpt_stride = ckpt_stride;
     p.H = H; p.dk = Dk; p.dv = Dv;
     const long long clusters = static_cast<long long>(num_seqs) * H;
