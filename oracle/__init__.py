@@ -58,25 +58,29 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _declare(lib):
+    """Set the ctypes signatures of a loaded oracle library."""
+    lib.kda_oracle_prefill.restype = ctypes.c_int
+    lib.kda_oracle_prefill.argtypes = [
+        _dp, _dp, _dp, _dp, _dp, _dp, _ip, _lp,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        _dp, _dp, _dp, ctypes.c_int]
+    lib.kda_oracle_decode.restype = ctypes.c_int
+    lib.kda_oracle_decode.argtypes = [
+        _dp, _dp, _dp, _dp, _dp, _dp, _dp,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.kda_oracle_ckpt_count.restype = ctypes.c_int64
+    lib.kda_oracle_ckpt_count.argtypes = [_ip, _lp, ctypes.c_int, ctypes.c_int]
+    lib.kda_oracle_max_threads.restype = ctypes.c_int
+    lib.kda_oracle_max_threads.argtypes = []
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            lib.kda_oracle_prefill.restype = ctypes.c_int
-            lib.kda_oracle_prefill.argtypes = [
-                _dp, _dp, _dp, _dp, _dp, _dp, _ip, _lp,
-                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                _dp, _dp, _dp, ctypes.c_int]
-            lib.kda_oracle_decode.restype = ctypes.c_int
-            lib.kda_oracle_decode.argtypes = [
-                _dp, _dp, _dp, _dp, _dp, _dp, _dp,
-                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
-            lib.kda_oracle_ckpt_count.restype = ctypes.c_int64
-            lib.kda_oracle_ckpt_count.argtypes = [_ip, _lp, ctypes.c_int, ctypes.c_int]
-            lib.kda_oracle_max_threads.restype = ctypes.c_int
-            lib.kda_oracle_max_threads.argtypes = []
-            _lib = lib
+            _lib = _declare(ctypes.CDLL(build()))
     return _lib
 
 
