@@ -351,38 +351,70 @@ def main(argv=None):
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         h_ck = torch.empty(ck.shape, dtype=ck.dtype).pin_memory()
         h_fin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
-        d_in = {k2: torch.empty_like(getattr(c, k2)) for k2 in host}
-        d_s0 = torch.empty_like(c.init_state)
         h2d = sum(v.numel() * v.element_size() for v in host.values()) + h_s0.numel() * 4
         d2h = out.numel() * 2 + ck.numel() * 4 + fin.numel() * 4
-        n_e2e = max(1, min(args.steps, 3))
+        n_e2e = max(2, min(args.steps, 6))
+        # Steps are pipelined over two device buffer sets: step i + 1's inputs are copied in
+        # (split over N_COPY copy streams) while step i computes and step i - 1's results are
+        # copied out.  Every step still moves all of its inputs in and all of its results out.
+        N_COPY = 2
+        bufs = [dict(d_in={k2: torch.empty_like(getattr(c, k2)) for k2 in host}, s0=torch.empty_like(c.init_state),
+                     out=torch.empty_like(out), fin=torch.empty_like(fin), ck=torch.empty_like(ck))
+                for _ in range(2)]
+        s_in = [torch.cuda.Stream(device=dev) for _ in range(N_COPY)]
+        s_out = torch.cuda.Stream(device=dev)
+        evs = [{k2: torch.cuda.Event() for k2 in [f"in{j}" for j in range(N_COPY)] + ["comp", "out"]}
+               for _ in range(2)]
 
-        def e2e_step():
-            for k2 in host:
-                d_in[k2].copy_(host[k2], non_blocking=True)
-            d_s0.copy_(h_s0, non_blocking=True)
-            kda.kda_chunk_prefill(d_in["q"], d_in["k"], d_in["v"], d_in["log_alpha"], d_in["beta"], d_s0, cu_dev,
-                                  c.cu_seqlens, 1, T_PROMPT, H, D, D, out, kda.KDA_OUT_BF16, fin, ck, CKPT, stream)
-            h_out.copy_(out, non_blocking=True)
-            h_ck.copy_(ck, non_blocking=True)
-            h_fin.copy_(fin, non_blocking=True)
+        def e2e_step(i):
+            bf, ev = bufs[i % 2], evs[i % 2]
+            for j, sj in enumerate(s_in):               # this buffer's inputs are free again
+                sj.wait_event(ev["comp"])
+                with torch.cuda.stream(sj):
+                    for k2, hv in host.items():          # a 1 / N_COPY row slice of every tensor per stream
+                        r0 = hv.shape[0] * j // N_COPY
+                        r1 = hv.shape[0] * (j + 1) // N_COPY
+                        bf["d_in"][k2][r0:r1].copy_(hv[r0:r1], non_blocking=True)
+                    if j == 0:
+                        bf["s0"].copy_(h_s0, non_blocking=True)
+                    ev["in%d" % j].record(sj)
+            for j in range(N_COPY):
+                stream.wait_event(ev["in%d" % j])
+            stream.wait_event(ev["out"])
+            d = bf["d_in"]
+            kda.kda_chunk_prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], bf["s0"], cu_dev,
+                                  c.cu_seqlens, 1, T_PROMPT, H, D, D, bf["out"], kda.KDA_OUT_BF16, bf["fin"], bf["ck"],
+                                  CKPT, stream)
+            ev["comp"].record(stream)
+            s_out.wait_event(ev["comp"])
+            with torch.cuda.stream(s_out):
+                h_out.copy_(bf["out"], non_blocking=True)
+                h_ck.copy_(bf["ck"], non_blocking=True)
+                h_fin.copy_(bf["fin"], non_blocking=True)
+                ev["out"].record(s_out)
 
-        e2e_step()
+        for i in range(2):
+            e2e_step(i)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
+        for sj in (*s_in, s_out):
+            sj.wait_event(a)
+        for i in range(n_e2e):
+            e2e_step(i)
+        stream.wait_event(evs[(n_e2e - 1) % 2]["out"])
         b.record(stream)
         torch.cuda.synchronize()
         (e_ms,) = reduce_max([a.elapsed_time(b) / n_e2e], device=dev)
         e2e = {"value": whole_job_rate(T_PROMPT, world, e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e_ms, "steps": n_e2e,
-               "note": "prefill only; pinned host inputs copied in, output + checkpoints + final state copied out"}
-        del host, d_in, h_out, h_ck
+               "note": "prefill only; pinned host inputs copied in, output + checkpoints + final state copied out; "
+                       "steps pipelined over two device buffer sets (copy-in of step i+1, split over 2 copy "
+                       "streams, and copy-out of step i-1 overlap the prefill of step i)"}
+        del host, bufs, h_out, h_ck
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
