@@ -79,3 +79,33 @@ def test_continuation_matches_one_call():
     P.check_state(f_b, f_all.cpu().double().numpy())
     P.check_state(c_b, c_all[2:].cpu().double().numpy())
     P.check_state(c_a[:2], c_all[:2].cpu().double().numpy())
+
+
+def test_continuation_70000_tokens_sampled_head():
+    """A 70000-token prompt served as a 40000-token prefix and a 30000-token continuation
+    (start position 40000, checkpoints every 32768 absolute tokens): H=32, D=128, one head
+    replayed by the oracle over the whole prompt; the continuation's checkpoints sit at
+    absolute 65536 and its end, equal to the one-call states there."""
+    T, P_len, H, D, stride = 70000, 40000, 32, 128, 32768
+    case = workloads.prefill_case([T], H=H, D=D, seed=140, device=DEV, ckpt_stride=stride)
+    cu_p = torch.tensor([0, P_len], dtype=torch.int32)
+    cu_c = torch.tensor([0, T - P_len], dtype=torch.int32)
+    _, f_a, c_a = kda.prefill(case.q[:P_len], case.k[:P_len], case.v[:P_len], case.log_alpha[:P_len],
+                              case.beta[:P_len], cu_p, init_state=case.init_state, ckpt_stride=stride)
+    o_b, f_b, c_b = kda.prefill(case.q[P_len:], case.k[P_len:], case.v[P_len:], case.log_alpha[P_len:],
+                                case.beta[P_len:], cu_c, init_state=f_a, ckpt_stride=stride,
+                                start_pos_host=torch.tensor([P_len], dtype=torch.int32))
+    torch.cuda.synchronize()
+    assert kda.kda_device_status() == kda.KDA_OK
+    assert c_a.shape[0] == 2 and c_b.shape[0] == 2          # prefix: 32768, end 40000; continuation: 65536, end
+    heads = [11]
+    sel = lambda x: x[:, heads].cpu()
+    ro, rf, rc = oracle.prefill(sel(case.q), sel(case.k), sel(case.v), sel(case.log_alpha), sel(case.beta),
+                                torch.tensor([0, T], dtype=torch.int32), case.init_state[:, heads].cpu(),
+                                ckpt_stride=stride)
+    # one-call checkpoints: 32768, 65536, end 70000
+    assert rc.shape[0] == 3
+    rows = np.arange(0, T - P_len, 300)
+    P.check_out(o_b[rows][:, heads], ro[P_len + rows], torch.bfloat16)
+    P.check_state(c_b[:, heads], rc[1:])
+    P.check_state(f_b[:, heads], rf)

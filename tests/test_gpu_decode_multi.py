@@ -140,3 +140,30 @@ def test_bad_slot_is_reported_and_skipped():
     assert kda.kda_device_status() == kda.KDA_ERR_INVALID_ARG
     assert torch.isnan(out[1]).all() and not torch.isnan(out[0]).any() and not torch.isnan(out[2]).any()
     assert kda.kda_device_status() == kda.KDA_OK                     # the word was cleared
+
+
+def test_full_pool_512x32_four_token_commit_sampled():
+    """512 sequences x 32 heads x 128 x 128 states (1.07 GB) in a shuffled pool, 4 tokens
+    each with mixed accepted counts; the oracle follows 6 sampled sequences (all heads)."""
+    N, K, H, D = 512, 4, 32, 128
+    c = workloads.decode_case(N=N, H=H, D=D, steps=K, seed=77, device=DEV)
+    tok = {key: torch.stack([s[key] for s in c.steps], dim=1).contiguous()
+           for key in ("q", "k", "v", "log_alpha", "beta")}
+    g = torch.Generator().manual_seed(5)
+    slots = torch.randperm(N, generator=g).to(torch.int32)
+    ntok = torch.randint(0, K + 1, (N,), generator=g).to(torch.int32)
+    pool = c.state                              # [N, H, D, D] on the device; slot s is row s
+    sample = [0, 100, 255, 300, 411, 511]
+    pool0 = pool[slots[sample].long()].double().cpu().numpy()
+    out = torch.full((N, K, H, D), float("nan"), device=DEV)
+    _call(tok, pool, slots.to(DEV), ntok.to(DEV), 1, out, N, K, H, D)
+    torch.cuda.synchronize()
+    assert kda.kda_device_status() == kda.KDA_OK
+    steps = [{key: tok[key][sample, j].cpu() for key in tok} for j in range(K)]
+    ro, rs = _oracle_run(steps, torch.from_numpy(pool0), ntok[sample].tolist())
+    got = out[sample].cpu()
+    for i, n in enumerate(sample):
+        nt = int(ntok[n])
+        if nt:
+            P.check_out(got[i, :nt], ro[i, :nt], torch.float32)
+        P.check_state(pool[int(slots[n])][None], rs[i][None])

@@ -5,6 +5,7 @@ log-decay per head and token) and DeltaNet (no decay), for the prefill
 Each layout is checked against the oracle, which takes the decay broadcast to every
 channel (or zero), and bit for bit against the per-channel kernels fed that same
 broadcast: the specialisations change where the decay comes from, not the arithmetic."""
+import numpy as np
 import pytest
 import torch
 
@@ -80,3 +81,25 @@ def test_decode_multi_layouts(decay):
         ro, ref = oracle.decode(q[:, j], k[:, j], v[:, j], la_full[:, j], beta[:, j], ref)
         P.check_out(outs[0][:, j], ro, torch.float32)
     P.check_state(pools[0], ref)
+
+
+@pytest.mark.parametrize("decay", [kda.KDA_DECAY_HEAD, kda.KDA_DECAY_NONE])
+def test_prefill_layouts_32768_sampled_heads(decay):
+    """One 32768-token prompt, H=32, D=128, checkpoints every 8192 tokens; the oracle
+    replays two heads (outputs on every 256th token, all checkpoints, the end state)."""
+    T, H, D, stride = 32768, 32, 128, 8192
+    case = workloads.prefill_case([T], H=H, D=D, seed=131 + decay, device=DEV, ckpt_stride=stride)
+    la_small = _head_decay(T, H, seed=7).to(DEV) if decay == kda.KDA_DECAY_HEAD else None
+    o, f, c = kda.prefill(case.q, case.k, case.v, la_small, case.beta, case.cu_seqlens, init_state=case.init_state,
+                          ckpt_stride=stride, out_dtype=torch.bfloat16, decay=decay)
+    torch.cuda.synchronize()
+    assert kda.kda_device_status() == kda.KDA_OK
+    heads = [2, 29]
+    la_full = (la_small.cpu()[:, heads, None].expand(T, 2, D) if la_small is not None else torch.zeros(T, 2, D))
+    sel = lambda x: x[:, heads].cpu()
+    ro, rf, rc = oracle.prefill(sel(case.q), sel(case.k), sel(case.v), la_full.contiguous(), sel(case.beta),
+                                case.cu_seqlens, case.init_state[:, heads].cpu(), ckpt_stride=stride)
+    rows = np.arange(0, T, 256)
+    P.check_out(o[rows][:, heads], ro[rows], torch.bfloat16)
+    P.check_state(f[:, heads], rf)
+    P.check_state(c[:, heads], rc)
