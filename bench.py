@@ -408,9 +408,24 @@ def main(argv=None):
         b.record(stream)
         torch.cuda.synchronize()
         (e_ms,) = reduce_max([a.elapsed_time(b) / n_e2e], device=dev)
+        # the host link itself: one pinned host -> device copy of the largest input, best of 3;
+        # the step cannot beat its input bytes at this rate
+        hq, dq = host["log_alpha"], bufs[0]["d_in"]["log_alpha"]
+        link_ms = []
+        for _ in range(3):
+            a.record(stream)
+            with torch.cuda.stream(stream):
+                dq.copy_(hq, non_blocking=True)
+            b.record(stream)
+            torch.cuda.synchronize()
+            link_ms.append(a.elapsed_time(b))
+        h2d_gbs = hq.numel() * hq.element_size() / (min(link_ms) / 1e3) / 1e9
+        floor_ms = h2d / (h2d_gbs * 1e9) * 1e3
         e2e = {"value": whole_job_rate(T_PROMPT, world, e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e_ms, "steps": n_e2e,
+               "link": {"h2d_gbs": round(h2d_gbs, 1), "h2d_floor_ms": round(floor_ms, 2),
+                        "frac_of_floor": round(floor_ms / e_ms, 3)},
                "note": "prefill only; pinned host inputs copied in, output + checkpoints + final state copied out; "
                        "steps pipelined over two device buffer sets (copy-in of step i+1, split over 2 copy "
                        "streams, and copy-out of step i-1 overlap the prefill of step i)"}

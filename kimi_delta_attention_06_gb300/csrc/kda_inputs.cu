@@ -11,7 +11,7 @@
 //   log_alpha = -softplus(a)  (fp32),   beta = sigmoid(b)  (bf16)
 // Positions before a sequence's first token read its carried-in history (conv_state:
 // the last 3 raw inputs of each stream, oldest first) or zeros.  One warp owns one head
-// and 8 tokens (inputs staged in shared memory by TMA); lane l owns channels
+// and 8 tokens (raw q, k, v rows staged in shared memory by TMA); lane l owns channels
 // [D/32 l, D/32 (l + 1)), so the L2 norm is a warp reduction; the conv taps of its
 // channels stay in registers and each token reads its window from the staged rows.
 //
@@ -25,9 +25,18 @@ namespace kda {
 
 constexpr int kConvW = 4;          // short-conv width
 
-__device__ __forceinline__ float silu(float x) { return x / (1.f + __expf(-x)); }
-__device__ __forceinline__ float sigmoidf(float x) { return 1.f / (1.f + __expf(-x)); }
-__device__ __forceinline__ float neg_softplus(float x) { return -(fmaxf(x, 0.f) + log1pf(__expf(-fabsf(x)))); }
+// The gates and the activation use the fast exponential, logarithm and division intrinsics
+// (a few ulp in fp32, far below the bf16 rounding of q, k, v and beta).  log(1 + e) keeps
+// its relative accuracy for tiny e through Kahan's identity log1p(e) = log(u) e / (u - 1),
+// u = 1 + e rounded (Goldberg, "What every computer scientist should know about
+// floating-point arithmetic", 1991, theorem 4), with log1p(e) = e where u rounds to 1.
+__device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.f + __expf(-x)); }
+__device__ __forceinline__ float sigmoidf(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
+__device__ __forceinline__ float log1p_small(float e) {     // e in [0, 1]
+    const float u = 1.f + e;
+    return u == 1.f ? e : __fdividef(__logf(u) * e, u - 1.f);
+}
+__device__ __forceinline__ float neg_softplus(float x) { return -(fmaxf(x, 0.f) + log1p_small(__expf(-fabsf(x)))); }
 
 template <int CPL>
 __device__ __forceinline__ void ld_bf16(const uint16_t* p, float (&x)[CPL]) {
@@ -50,27 +59,31 @@ __device__ __forceinline__ void st_bf16(uint16_t* p, const float (&x)[CPL]) {
 }
 
 // One CTA = one head x 64 tokens.  Thread 0 stages, by TMA, rows [t - 3, t + 64) of the
-// three raw streams (the conv halo included; rows before the tensor read as zeros) and
-// the 64 rows of the alpha pre-activation; warp w then takes tokens 8 w .. 8 w + 7.
+// three raw streams (the conv halo included; rows before the tensor read as zeros); warp w
+// then takes tokens 8 w .. 8 w + 7.  The alpha gate is elementwise: while the TMA is in
+// flight, every thread streams 8 float4 of the CTA's 64 x D pre-activation tile straight
+// from global memory into log_alpha (one 512-byte row per warp access), which keeps the
+// staged tiles at 51 KB and the token loop free of it.  Two CTAs per SM: the conv taps
+// stay in registers (a tighter register cap spills them).
 constexpr int kPrepRows = 64;
 constexpr int kHalo = kConvW - 1;
 
-struct PrepMaps { CUtensorMap xq, xk, xv, a; };
+struct PrepMaps { CUtensorMap xq, xk, xv; };
 
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
 kda_prepare_inputs_kernel(const __grid_constant__ PrepMaps maps, const float* __restrict__ conv_w,
-                          const uint16_t* __restrict__ conv_state, const uint16_t* __restrict__ b_raw,
+                          const uint16_t* __restrict__ conv_state, const float* __restrict__ a_raw,
+                          const uint16_t* __restrict__ b_raw,
                           const int32_t* __restrict__ cu, int num_seqs, int T, int H, int act,
                           uint16_t* __restrict__ q, uint16_t* __restrict__ k, uint16_t* __restrict__ v,
                           float* __restrict__ log_alpha, uint16_t* __restrict__ beta, int* status)
 {
     constexpr int CPL = D / 32;                        // channels per lane
-    constexpr uint32_t XROW = D * 2, XBYTES = (kPrepRows + kHalo) * XROW, ABYTES = kPrepRows * D * 4;
+    constexpr uint32_t XROW = D * 2, XBYTES = (kPrepRows + kHalo) * XROW;
     extern __shared__ __align__(1024) uint8_t smem[];        // no static shared memory: TMA targets stay aligned
     uint8_t* sx[3] = {smem, smem + XBYTES, smem + 2 * XBYTES};
-    const float* sa = reinterpret_cast<const float*>(smem + 3 * XBYTES);
-    uint64_t& bar = *reinterpret_cast<uint64_t*>(smem + 3 * XBYTES + ABYTES);
+    uint64_t& bar = *reinterpret_cast<uint64_t*>(smem + 3 * XBYTES);
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     // heads run fastest across CTAs, so CTAs in flight together read whole token rows
@@ -79,11 +92,28 @@ kda_prepare_inputs_kernel(const __grid_constant__ PrepMaps maps, const float* __
     if (threadIdx.x == 0) {
         kda::tc::mbar_init(&bar, 1);
         kda::tc::mbar_fence_init();
-        kda::tc::mbar_arrive_expect_tx(&bar, 3 * XBYTES + ABYTES);
+        kda::tc::mbar_arrive_expect_tx(&bar, 3 * XBYTES);
         kda::tc::tma_load_2d(kda::tc::smem_u32(sx[0]), &maps.xq, h * D, tb - kHalo, &bar);
         kda::tc::tma_load_2d(kda::tc::smem_u32(sx[1]), &maps.xk, h * D, tb - kHalo, &bar);
         kda::tc::tma_load_2d(kda::tc::smem_u32(sx[2]), &maps.xv, h * D, tb - kHalo, &bar);
-        kda::tc::tma_load_2d(kda::tc::smem_u32(sa), &maps.a, h * D, tb, &bar);
+    }
+    {   // log_alpha = -softplus(a) for rows tb .. tb + 63 of head h
+        constexpr int F4_ROW = D / 4, ROWS_PER_PASS = 256 / F4_ROW, PASSES = kPrepRows / ROWS_PER_PASS;
+        const int cf = threadIdx.x % F4_ROW, r0 = threadIdx.x / F4_ROW;
+        float4 av[PASSES];
+#pragma unroll
+        for (int i = 0; i < PASSES; ++i) {
+            const int t = tb + r0 + i * ROWS_PER_PASS;
+            av[i] = t < T ? *reinterpret_cast<const float4*>(a_raw + (static_cast<size_t>(t) * H + h) * D + 4 * cf)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < PASSES; ++i) {
+            const int t = tb + r0 + i * ROWS_PER_PASS;
+            if (t < T)
+                *reinterpret_cast<float4*>(log_alpha + (static_cast<size_t>(t) * H + h) * D + 4 * cf) =
+                    make_float4(neg_softplus(av[i].x), neg_softplus(av[i].y), neg_softplus(av[i].z), neg_softplus(av[i].w));
+        }
     }
     const int c0 = lane * CPL;
     float w[3][CPL][kConvW];                           // taps of this lane's channels
@@ -129,6 +159,15 @@ kda_prepare_inputs_kernel(const __grid_constant__ PrepMaps maps, const float* __
             float acc[CPL];
 #pragma unroll
             for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+            if (t - kHalo >= t0) {                                  // window inside the sequence
+#pragma unroll
+                for (int j = 0; j < kConvW; ++j) {
+                    float x[CPL];
+                    ld_bf16<CPL>(reinterpret_cast<const uint16_t*>(sx[s] + (t - tb + j) * XROW) + c0, x);
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) acc[c] += w[s][c][j] * x[c];
+                }
+            } else
 #pragma unroll
             for (int j = 0; j < kConvW; ++j) {
                 const int p = t - kHalo + j;
@@ -161,12 +200,6 @@ kda_prepare_inputs_kernel(const __grid_constant__ PrepMaps maps, const float* __
         }
 #pragma unroll
         for (int s = 0; s < 3; ++s) st_bf16<CPL>(ys[s] + row * D + c0, y[s]);
-        const float* ar = sa + (t - tb) * D + c0;
-        float la[CPL];
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) la[c] = neg_softplus(ar[c]);
-        if constexpr (CPL == 4) *reinterpret_cast<float4*>(log_alpha + row * D + c0) = make_float4(la[0], la[1], la[2], la[3]);
-        else *reinterpret_cast<float2*>(log_alpha + row * D + c0) = make_float2(la[0], la[1]);
         const float bt = __shfl_sync(0xffffffffu, braw, t - t_begin);
         if (lane == 0) beta[row] = f32_to_bf16_bits(sigmoidf(bt));
     }
@@ -276,23 +309,22 @@ int launch_prepare_inputs(const uint16_t* xq, const uint16_t* xk, const uint16_t
     const long long cols = static_cast<long long>(H) * D;
     if (!map_rows(&maps.xq, xq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, cols, D, kPrepRows + kHalo) ||
         !map_rows(&maps.xk, xk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, cols, D, kPrepRows + kHalo) ||
-        !map_rows(&maps.xv, xv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, cols, D, kPrepRows + kHalo) ||
-        !map_rows(&maps.a, a_raw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, T, cols, D, kPrepRows))
+        !map_rows(&maps.xv, xv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, cols, D, kPrepRows + kHalo))
         return -3;
     const long long ctas = static_cast<long long>((T + kPrepRows - 1) / kPrepRows) * H;
     if (ctas >= (1LL << 31)) return -3;
     const dim3 grid(static_cast<unsigned>(ctas));
-    const size_t smem = 3 * static_cast<size_t>(kPrepRows + kHalo) * D * 2 + static_cast<size_t>(kPrepRows) * D * 4 + 16;
+    const size_t smem = 3 * static_cast<size_t>(kPrepRows + kHalo) * D * 2 + 16;
     if (D == 128) {
         static bool attr_done[kMaxDevicesAttr] = {};
         if (!raise_smem_limit(reinterpret_cast<const void*>(kda_prepare_inputs_kernel<128>), static_cast<int>(smem),
                               attr_done))
             return -3;
-        kda_prepare_inputs_kernel<128><<<grid, 256, smem, stream>>>(maps, conv_w, conv_state, b_raw, cu_seqlens,
+        kda_prepare_inputs_kernel<128><<<grid, 256, smem, stream>>>(maps, conv_w, conv_state, a_raw, b_raw, cu_seqlens,
                                                                     num_seqs, T, H, act, q, k, v, log_alpha, beta,
                                                                     status);
     } else {
-        kda_prepare_inputs_kernel<64><<<grid, 256, smem, stream>>>(maps, conv_w, conv_state, b_raw, cu_seqlens,
+        kda_prepare_inputs_kernel<64><<<grid, 256, smem, stream>>>(maps, conv_w, conv_state, a_raw, b_raw, cu_seqlens,
                                                                    num_seqs, T, H, act, q, k, v, log_alpha, beta,
                                                                    status);
     }
