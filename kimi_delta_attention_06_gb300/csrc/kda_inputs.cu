@@ -10,10 +10,11 @@
 //   q, k      /= sqrt(sum over the head's channels of x^2 + 1e-6)
 //   log_alpha = -softplus(a)  (fp32),   beta = sigmoid(b)  (bf16)
 // Positions before a sequence's first token read its carried-in history (conv_state:
-// the last 3 raw inputs of each stream, oldest first) or zeros.  One warp owns one head
-// and 8 tokens (raw q, k, v rows staged in shared memory by TMA); lane l owns channels
-// [D/32 l, D/32 (l + 1)), so the L2 norm is a warp reduction; the conv taps of its
-// channels stay in registers and each token reads its window from the staged rows.
+// the last 3 raw inputs of each stream, oldest first) or zeros.  One warp owns one stream
+// (q, k or v) of one head for 16 tokens (raw q, k, v rows staged in shared memory by TMA);
+// lane l owns channels [D/32 l, D/32 (l + 1)), so the L2 norm is a warp reduction; the 4
+// conv taps of each of its channels stay in registers and each token reads its window from
+// the staged rows.
 //
 // kda_output_norm_kernel: y = o / sqrt(mean over the head's value channels of o^2 + eps)
 // * gamma[h] (bf16), one warp per (token, head).
@@ -60,18 +61,21 @@ __device__ __forceinline__ void st_bf16(uint16_t* p, const float (&x)[CPL]) {
 
 // One CTA = one head x 64 tokens.  Thread 0 stages, by TMA, rows [t - 3, t + 64) of the
 // three raw streams (the conv halo included; rows before the tensor read as zeros); warp w
-// then takes tokens 8 w .. 8 w + 7.  The alpha gate is elementwise: while the TMA is in
-// flight, every thread streams 8 float4 of the CTA's 64 x D pre-activation tile straight
-// from global memory into log_alpha (one 512-byte row per warp access), which keeps the
-// staged tiles at 51 KB and the token loop free of it.  Two CTAs per SM: the conv taps
-// stay in registers (a tighter register cap spills them).
+// then takes stream w / 4 of tokens 16 (w % 4) .. + 15.  The alpha gate is elementwise:
+// while the TMA is in flight, every thread streams a few float4 of the CTA's 64 x D
+// pre-activation tile straight from global memory into log_alpha (one 512-byte row per
+// warp access), which keeps the
+// staged tiles at 51 KB and the token loop free of it.  With one stream per warp the taps
+// take 16 registers a lane, and three 12-warp CTAs share an SM.
 constexpr int kPrepRows = 64;
 constexpr int kHalo = kConvW - 1;
 
 struct PrepMaps { CUtensorMap xq, xk, xv; };
 
+constexpr int kPrepThreads = 384;  // 12 warps: stream (q, k, v) x 4 groups of 16 tokens
+
 template <int D>
-__global__ void __launch_bounds__(256, 2)
+__global__ void __launch_bounds__(kPrepThreads, 3)
 kda_prepare_inputs_kernel(const __grid_constant__ PrepMaps maps, const float* __restrict__ conv_w,
                           const uint16_t* __restrict__ conv_state, const float* __restrict__ a_raw,
                           const uint16_t* __restrict__ b_raw,
@@ -97,33 +101,33 @@ kda_prepare_inputs_kernel(const __grid_constant__ PrepMaps maps, const float* __
         kda::tc::tma_load_2d(kda::tc::smem_u32(sx[1]), &maps.xk, h * D, tb - kHalo, &bar);
         kda::tc::tma_load_2d(kda::tc::smem_u32(sx[2]), &maps.xv, h * D, tb - kHalo, &bar);
     }
-    {   // log_alpha = -softplus(a) for rows tb .. tb + 63 of head h
-        constexpr int F4_ROW = D / 4, ROWS_PER_PASS = 256 / F4_ROW, PASSES = kPrepRows / ROWS_PER_PASS;
-        const int cf = threadIdx.x % F4_ROW, r0 = threadIdx.x / F4_ROW;
-        float4 av[PASSES];
+    {   // log_alpha = -softplus(a) for rows tb .. tb + 63 of head h (one 512-byte row per warp access)
+        constexpr int F4_ROW = D / 4, NF4 = kPrepRows * F4_ROW, PER = (NF4 + kPrepThreads - 1) / kPrepThreads;
+        float4 av[PER];
 #pragma unroll
-        for (int i = 0; i < PASSES; ++i) {
-            const int t = tb + r0 + i * ROWS_PER_PASS;
-            av[i] = t < T ? *reinterpret_cast<const float4*>(a_raw + (static_cast<size_t>(t) * H + h) * D + 4 * cf)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < PER; ++i) {
+            const int idx = threadIdx.x + i * kPrepThreads, t = tb + idx / F4_ROW;
+            av[i] = (idx < NF4 && t < T)
+                ? *reinterpret_cast<const float4*>(a_raw + (static_cast<size_t>(t) * H + h) * D + 4 * (idx % F4_ROW))
+                : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int i = 0; i < PASSES; ++i) {
-            const int t = tb + r0 + i * ROWS_PER_PASS;
-            if (t < T)
-                *reinterpret_cast<float4*>(log_alpha + (static_cast<size_t>(t) * H + h) * D + 4 * cf) =
+        for (int i = 0; i < PER; ++i) {
+            const int idx = threadIdx.x + i * kPrepThreads, t = tb + idx / F4_ROW;
+            if (idx < NF4 && t < T)
+                *reinterpret_cast<float4*>(log_alpha + (static_cast<size_t>(t) * H + h) * D + 4 * (idx % F4_ROW)) =
                     make_float4(neg_softplus(av[i].x), neg_softplus(av[i].y), neg_softplus(av[i].z), neg_softplus(av[i].w));
         }
     }
+    // this warp: stream st (0 q, 1 k, 2 v) for tokens tb + 16 g .. tb + 16 g + 15
+    const int st = warp >> 2, grp = warp & 3;
     const int c0 = lane * CPL;
-    float w[3][CPL][kConvW];                           // taps of this lane's channels
+    float w[CPL][kConvW];                              // taps of this lane's channels
 #pragma unroll
-    for (int s = 0; s < 3; ++s)
+    for (int c = 0; c < CPL; ++c)
 #pragma unroll
-        for (int c = 0; c < CPL; ++c)
-#pragma unroll
-            for (int j = 0; j < kConvW; ++j)
-                w[s][c][j] = conv_w[((static_cast<size_t>(s) * H + h) * D + c0 + c) * kConvW + j];
+        for (int j = 0; j < kConvW; ++j)
+            w[c][j] = conv_w[((static_cast<size_t>(st) * H + h) * D + c0 + c) * kConvW + j];
     __syncthreads();                                   // barrier initialised before anyone waits on it
     const uint32_t landed = kda::tc::mbar_wait_bounded(&bar, 0, kWaitLimitNs);
     if (!__syncthreads_and(landed)) {
@@ -131,10 +135,14 @@ kda_prepare_inputs_kernel(const __grid_constant__ PrepMaps maps, const float* __
         return;
     }
 
-    constexpr int TPW = kPrepRows / 8;                  // tokens per warp
-    const int t_begin = tb + warp * TPW;
+    constexpr int TPW = kPrepRows / 4;                  // tokens per warp
+    const int t_begin = tb + grp * TPW;
     const int t_end = min(T, t_begin + TPW);
     if (t_begin >= t_end) return;
+    if (st == 2 && lane < t_end - t_begin) {           // the v warps also write beta = sigmoid(b)
+        const size_t row = static_cast<size_t>(t_begin + lane) * H + h;
+        beta[row] = f32_to_bf16_bits(sigmoidf(bf16_bits_to_f32(b_raw[row])));
+    }
     // the sequence holding t_begin: cu[n] <= t_begin < cu[n + 1] (empty sequences skipped)
     int lo = 0, hi = num_seqs;
     while (hi - lo > 1) {
@@ -142,66 +150,59 @@ kda_prepare_inputs_kernel(const __grid_constant__ PrepMaps maps, const float* __
         if (cu[mid] <= t_begin) lo = mid; else hi = mid;
     }
     int n = lo;
-    // beta pre-activations of this warp's tokens, one per lane, fetched before the loop so
-    // that no store inside it waits on a global load
-    const float braw = lane < t_end - t_begin ? bf16_bits_to_f32(b_raw[static_cast<size_t>(t_begin + lane) * H + h]) : 0.f;
-    uint16_t* ys[3] = {q, k, v};
+    const uint8_t* xs = smem + st * XBYTES;
+    uint16_t* ys = st == 0 ? q : (st == 1 ? k : v);
     // tokens are independent: each reads its W taps from the staged rows (or, before its
     // sequence's first token, from the carried-in history / zeros)
-#pragma unroll 2
+#pragma unroll 4
     for (int t = t_begin; t < t_end; ++t) {
         while (cu[n + 1] <= t) ++n;
         const int t0 = cu[n];
         const size_t row = static_cast<size_t>(t) * H + h;
-        float y[3][CPL];
+        float y[CPL];
 #pragma unroll
-        for (int s = 0; s < 3; ++s) {
-            float acc[CPL];
+        for (int c = 0; c < CPL; ++c) y[c] = 0.f;
+        if (t - kHalo >= t0) {                                  // window inside the sequence
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
-            if (t - kHalo >= t0) {                                  // window inside the sequence
+            for (int j = 0; j < kConvW; ++j) {
+                float x[CPL];
+                ld_bf16<CPL>(reinterpret_cast<const uint16_t*>(xs + (t - tb + j) * XROW) + c0, x);
 #pragma unroll
-                for (int j = 0; j < kConvW; ++j) {
-                    float x[CPL];
-                    ld_bf16<CPL>(reinterpret_cast<const uint16_t*>(sx[s] + (t - tb + j) * XROW) + c0, x);
-#pragma unroll
-                    for (int c = 0; c < CPL; ++c) acc[c] += w[s][c][j] * x[c];
-                }
-            } else
+                for (int c = 0; c < CPL; ++c) y[c] += w[c][j] * x[c];
+            }
+        } else {
 #pragma unroll
             for (int j = 0; j < kConvW; ++j) {
                 const int p = t - kHalo + j;
                 float x[CPL];
                 if (p >= t0) {
-                    ld_bf16<CPL>(reinterpret_cast<const uint16_t*>(sx[s] + (p - tb + kHalo) * XROW) + c0, x);
+                    ld_bf16<CPL>(reinterpret_cast<const uint16_t*>(xs + (p - tb + kHalo) * XROW) + c0, x);
                 } else if (conv_state) {                        // carried in, t0 - p steps back
-                    ld_bf16<CPL>(conv_state + ((((static_cast<size_t>(n) * 3 + s) * kHalo + (kHalo - (t0 - p))) * H + h)
+                    ld_bf16<CPL>(conv_state + ((((static_cast<size_t>(n) * 3 + st) * kHalo + (kHalo - (t0 - p))) * H + h)
                                                * D + c0), x);
                 } else {
 #pragma unroll
                     for (int c = 0; c < CPL; ++c) x[c] = 0.f;
                 }
 #pragma unroll
-                for (int c = 0; c < CPL; ++c) acc[c] += w[s][c][j] * x[c];
+                for (int c = 0; c < CPL; ++c) y[c] += w[c][j] * x[c];
             }
-#pragma unroll
-            for (int c = 0; c < CPL; ++c) y[s][c] = act ? silu(acc[c]) : acc[c];
         }
+        if (act) {
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {                           // L2 norm of q and k over the head
+            for (int c = 0; c < CPL; ++c) y[c] = silu(y[c]);
+        }
+        if (st < 2) {                                           // L2 norm of q and k over the head
             float ss = 0.f;
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) ss += y[s][c] * y[s][c];
+            for (int c = 0; c < CPL; ++c) ss += y[c] * y[c];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
             const float inv = rsqrtf(ss + 1e-6f);
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) y[s][c] *= inv;
+            for (int c = 0; c < CPL; ++c) y[c] *= inv;
         }
-#pragma unroll
-        for (int s = 0; s < 3; ++s) st_bf16<CPL>(ys[s] + row * D + c0, y[s]);
-        const float bt = __shfl_sync(0xffffffffu, braw, t - t_begin);
-        if (lane == 0) beta[row] = f32_to_bf16_bits(sigmoidf(bt));
+        st_bf16<CPL>(ys + row * D + c0, y);
     }
 }
 
@@ -320,11 +321,11 @@ int launch_prepare_inputs(const uint16_t* xq, const uint16_t* xk, const uint16_t
         if (!raise_smem_limit(reinterpret_cast<const void*>(kda_prepare_inputs_kernel<128>), static_cast<int>(smem),
                               attr_done))
             return -3;
-        kda_prepare_inputs_kernel<128><<<grid, 256, smem, stream>>>(maps, conv_w, conv_state, a_raw, b_raw, cu_seqlens,
+        kda_prepare_inputs_kernel<128><<<grid, kPrepThreads, smem, stream>>>(maps, conv_w, conv_state, a_raw, b_raw, cu_seqlens,
                                                                     num_seqs, T, H, act, q, k, v, log_alpha, beta,
                                                                     status);
     } else {
-        kda_prepare_inputs_kernel<64><<<grid, 256, smem, stream>>>(maps, conv_w, conv_state, a_raw, b_raw, cu_seqlens,
+        kda_prepare_inputs_kernel<64><<<grid, kPrepThreads, smem, stream>>>(maps, conv_w, conv_state, a_raw, b_raw, cu_seqlens,
                                                                    num_seqs, T, H, act, q, k, v, log_alpha, beta,
                                                                    status);
     }
