@@ -167,16 +167,34 @@ kda_decode_multi_kernel(const uint16_t* __restrict__ q, const uint16_t* __restri
         s[it] = commit ? __ldcs(S + r * Sh::kLanesPerRow + c4) : __ldg(S + r * Sh::kLanesPerRow + c4);
     }
 
+    // Token inputs (row tid of q, k, v, log_alpha, and beta) are fetched one token ahead, so
+    // no token waits on a global load between its barriers.
+    uint16_t q_in = 0, k_in = 0, v_in = 0, b_in = 0;
+    float la_in = 0.f;
+    auto fetch = [&](int j) {
+        const size_t tok = static_cast<size_t>(n) * K + j;          // token row [n][j]
+        const size_t vec = (tok * H + h) * D;                       // its [H, D] vectors
+        if (tid < D) {
+            q_in = q[vec + tid];
+            k_in = k[vec + tid];
+            v_in = v[vec + tid];
+            // decay layouts: per channel (KDA), per head (Gated DeltaNet), none (DeltaNet)
+            la_in = decay == 0 ? log_alpha[vec + tid] : decay == 1 ? log_alpha[tok * H + h] : 0.f;
+        }
+        b_in = beta[tok * H + h];
+    };
+    if (nt > 0) fetch(0);
     for (int j = 0; j < nt; ++j) {
         const size_t tok = static_cast<size_t>(n) * K + j;          // token row [n][j]
         const size_t vec = (tok * H + h) * D;                       // its [H, D] vectors
+        const uint16_t q_j = q_in, k_j = k_in, v_j = v_in, b_j = b_in;
+        const float la_j = la_in;
+        if (j + 1 < nt) fetch(j + 1);
         float qk_part = 0.f;
         if (tid < D) {
-            const float qi = bf16_bits_to_f32(q[vec + tid]);
-            const float ki = bf16_bits_to_f32(k[vec + tid]);
-            // decay layouts: per channel (KDA), per head (Gated DeltaNet), none (DeltaNet)
-            const float a = decay == 0 ? expf(log_alpha[vec + tid])
-                          : decay == 1 ? expf(log_alpha[tok * H + h]) : 1.f;
+            const float qi = bf16_bits_to_f32(q_j);
+            const float ki = bf16_bits_to_f32(k_j);
+            const float a = decay == 2 ? 1.f : expf(la_j);
             s_a[tid] = a;
             s_k[tid] = ki;
             s_ak[tid] = a * ki;
@@ -209,12 +227,12 @@ kda_decode_multi_kernel(const uint16_t* __restrict__ q, const uint16_t* __restri
         }
         __syncthreads();
 
-        const float b = bf16_bits_to_f32(beta[tok * H + h]);
+        const float b = bf16_bits_to_f32(b_j);
         if (tid < D) {
             float t1 = 0.f, t2 = 0.f, qk = 0.f;
 #pragma unroll
             for (int w = 0; w < WARPS; ++w) { t1 += s_red[w][0][tid]; t2 += s_red[w][1][tid]; qk += s_qk[w]; }
-            const float u = bf16_bits_to_f32(v[vec + tid]) - t1;
+            const float u = bf16_bits_to_f32(v_j) - t1;
             s_u[tid] = u;
             const float ov = t2 + b * qk * u;
             if (out_f32) reinterpret_cast<float*>(out)[vec + tid] = ov;

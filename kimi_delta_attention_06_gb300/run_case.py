@@ -95,7 +95,7 @@ def main(argv=None):
 
         def run():
             kda.kda_decode_multi(tok["q"], tok["k"], tok["v"], tok["log_alpha"], tok["beta"], d.state, a.N, None,
-                                 None, a.commit, out, kda.KDA_OUT_BF16, a.N, a.K, a.H, a.D, a.D, stream)
+                                 None, a.commit, out, kda.KDA_OUT_BF16, a.N, a.K, a.H, a.D, a.D, stream=stream)
         units, count = f"{a.N} sequences x {a.K} tokens, commit={a.commit}", a.N * a.K
     else:
         d = workloads.decode_case(N=a.N, H=a.H, D=a.D, steps=1, seed=4, device=dev)
