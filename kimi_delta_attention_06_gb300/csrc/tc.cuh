@@ -139,13 +139,6 @@ __device__ __forceinline__ uint32_t mbar_wait_bounded(void* bar, uint32_t parity
     }
 }
 
-// Round an fp32 value to tf32 (nearest, ties away from zero); result stays in an fp32 register.
-__device__ __forceinline__ float to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
-}
-
 // ---- swizzled tile addressing ----------------------------------------------------------------
 // Byte offset of 32-bit element (row, col) in a 128B-swizzled tile of `rows` rows whose
 // 128-byte slabs (32 elements of `col`) are stored one after another.
@@ -211,17 +204,6 @@ __device__ __forceinline__ void cluster_sync() {
 // Arrive (release at cluster scope) on an mbarrier of another CTA of the cluster.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(cluster_addr) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cluster_addr, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;"
-                 :: "r"(cluster_addr), "r"(bytes) : "memory");
-}
-// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into another CTA's
-// shared memory; completion is signalled as transaction bytes on the destination mbarrier.
-__device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
-                                                    uint32_t mbar_cluster) {
-    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 :: "r"(dst_cluster), "r"(src_cta), "r"(bytes), "r"(mbar_cluster) : "memory");
 }
 // try_wait with cluster-scope acquire (for phases completed by remote arrivals).
 __device__ __forceinline__ uint32_t mbar_try_wait_cluster(void* bar, uint32_t parity) {
