@@ -122,12 +122,13 @@ kda_prepare_inputs_kernel(const __grid_constant__ PrepMaps maps, const float* __
     // this warp: stream st (0 q, 1 k, 2 v) for tokens tb + 16 g .. tb + 16 g + 15
     const int st = warp >> 2, grp = warp & 3;
     const int c0 = lane * CPL;
-    float w[CPL][kConvW];                              // taps of this lane's channels
+    float w[CPL][kConvW];                              // taps of this lane's channels (one float4 each)
+    static_assert(kConvW == 4, "one float4 of taps per channel");
 #pragma unroll
-    for (int c = 0; c < CPL; ++c)
-#pragma unroll
-        for (int j = 0; j < kConvW; ++j)
-            w[c][j] = conv_w[((static_cast<size_t>(st) * H + h) * D + c0 + c) * kConvW + j];
+    for (int c = 0; c < CPL; ++c) {
+        const float4 t4 = *reinterpret_cast<const float4*>(conv_w + ((static_cast<size_t>(st) * H + h) * D + c0 + c) * kConvW);
+        w[c][0] = t4.x; w[c][1] = t4.y; w[c][2] = t4.z; w[c][3] = t4.w;
+    }
     __syncthreads();                                   // barrier initialised before anyone waits on it
     const uint32_t landed = kda::tc::mbar_wait_bounded(&bar, 0, kWaitLimitNs);
     if (!__syncthreads_and(landed)) {
@@ -150,14 +151,14 @@ kda_prepare_inputs_kernel(const __grid_constant__ PrepMaps maps, const float* __
         if (cu[mid] <= t_begin) lo = mid; else hi = mid;
     }
     int n = lo;
+    int t0 = cu[n], t1 = cu[n + 1];                   // bounds of sequence n, reloaded only at a boundary
     const uint8_t* xs = smem + st * XBYTES;
     uint16_t* ys = st == 0 ? q : (st == 1 ? k : v);
     // tokens are independent: each reads its W taps from the staged rows (or, before its
     // sequence's first token, from the carried-in history / zeros)
 #pragma unroll 4
     for (int t = t_begin; t < t_end; ++t) {
-        while (cu[n + 1] <= t) ++n;
-        const int t0 = cu[n];
+        while (t >= t1) { ++n; t0 = t1; t1 = cu[n + 1]; }     // (skips empty sequences)
         const size_t row = static_cast<size_t>(t) * H + h;
         float y[CPL];
 #pragma unroll
