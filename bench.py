@@ -214,6 +214,14 @@ def time_oracle(budget_s=12.0):
             "decode_gbs": dec_gbs, "prefill_seconds": dt}
 
 
+def bench_config(world):
+    """The workload description both arms print (the reference arm times a bounded sample of it)."""
+    return {"workload": f"kda prefill T={T_PROMPT} H={H} Dk=Dv={D} ckpt every {CKPT} + decode N={DEC_N} H={H} D={D}",
+            "global_batch": world, "seq_len": T_PROMPT, "heads": H, "head_dim": D,
+            "ckpt_stride": CKPT, "decode_batch": DEC_N,
+            "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, rank):
     if rank != 0:
         return 0
@@ -229,8 +237,7 @@ def run_reference(args, rank):
             "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(x["prefill_seconds"] for x in samples),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": f"kda prefill T={T_PROMPT} H={H} D={D} (bounded CPU sample)",
-                       "global_batch": 1, "seq_len": T_PROMPT, "parallelism": "none (host cores)"},
+            "config": bench_config(args.gpus),
             "cpu_baseline": cb,
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -443,11 +450,7 @@ def main(argv=None):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "tf32/f32 (bf16 in/out)", "data": "synthetic",
-            "config": {"workload": f"kda prefill T={T_PROMPT} H={H} Dk=Dv={D} ckpt every {CKPT} "
-                                   f"+ decode N={DEC_N} H={H} D={D}",
-                       "global_batch": world, "seq_len": T_PROMPT, "heads": H, "head_dim": D,
-                       "ckpt_stride": CKPT, "decode_batch": DEC_N,
-                       "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"replicas x{world}"},
+            "config": bench_config(world),
             "prefill_ms": pre_avg, "decode_ms": dec_avg,
             "decode": {"value": dec_gbs * world, "unit": "GB/s", "tokens_per_s": whole_job_rate(DEC_N, world, dec_avg),
                        "frac_of_hbm_peak": dec_gbs / hbm},
