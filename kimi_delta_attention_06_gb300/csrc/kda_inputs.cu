@@ -154,12 +154,53 @@ kda_prepare_inputs_kernel(const __grid_constant__ PrepMaps maps, const float* __
     int t0 = cu[n], t1 = cu[n + 1];                   // bounds of sequence n, reloaded only at a boundary
     const uint8_t* xs = smem + st * XBYTES;
     uint16_t* ys = st == 0 ? q : (st == 1 ? k : v);
+    // activation, L2 norm (q, k) and store of token t's conv output
+    auto finish = [&](int t, float (&y)[CPL]) {
+        if (act) {
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) y[c] = silu(y[c]);
+        }
+        if (st < 2) {                                           // L2 norm of q and k over the head
+            float ss = 0.f;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) ss += y[c] * y[c];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float inv = rsqrtf(ss + 1e-6f);
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) y[c] *= inv;
+        }
+        st_bf16<CPL>(ys + (static_cast<size_t>(t) * H + h) * D + c0, y);
+    };
+    if (t_begin - kHalo >= t0 && t_end <= t1) {
+        // every window lies inside one sequence (the common case): the staged rows t - 3 .. t
+        // stay in a register window, one new row per token
+        float xw[kConvW][CPL];
+#pragma unroll
+        for (int j = 0; j < kHalo; ++j)
+            ld_bf16<CPL>(reinterpret_cast<const uint16_t*>(xs + (t_begin - tb + j) * XROW) + c0, xw[j]);
+#pragma unroll
+        for (int i = 0; i < TPW; ++i) {
+            const int t = t_begin + i;
+            if (t < t_end) {
+                ld_bf16<CPL>(reinterpret_cast<const uint16_t*>(xs + (t - tb + kHalo) * XROW) + c0, xw[(i + kHalo) % kConvW]);
+                float y[CPL];
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) y[c] = 0.f;
+#pragma unroll
+                for (int j = 0; j < kConvW; ++j)
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) y[c] += w[c][j] * xw[(i + j) % kConvW][c];
+                finish(t, y);
+            }
+        }
+        return;
+    }
     // tokens are independent: each reads its W taps from the staged rows (or, before its
     // sequence's first token, from the carried-in history / zeros)
 #pragma unroll 4
     for (int t = t_begin; t < t_end; ++t) {
         while (t >= t1) { ++n; t0 = t1; t1 = cu[n + 1]; }     // (skips empty sequences)
-        const size_t row = static_cast<size_t>(t) * H + h;
         float y[CPL];
 #pragma unroll
         for (int c = 0; c < CPL; ++c) y[c] = 0.f;
@@ -189,21 +230,7 @@ kda_prepare_inputs_kernel(const __grid_constant__ PrepMaps maps, const float* __
                 for (int c = 0; c < CPL; ++c) y[c] += w[c][j] * x[c];
             }
         }
-        if (act) {
-#pragma unroll
-            for (int c = 0; c < CPL; ++c) y[c] = silu(y[c]);
-        }
-        if (st < 2) {                                           // L2 norm of q and k over the head
-            float ss = 0.f;
-#pragma unroll
-            for (int c = 0; c < CPL; ++c) ss += y[c] * y[c];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            const float inv = rsqrtf(ss + 1e-6f);
-#pragma unroll
-            for (int c = 0; c < CPL; ++c) y[c] *= inv;
-        }
-        st_bf16<CPL>(ys + row * D + c0, y);
+        finish(t, y);
     }
 }
 
