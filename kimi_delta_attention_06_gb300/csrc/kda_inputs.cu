@@ -237,7 +237,7 @@ kda_prepare_inputs_kernel(const __grid_constant__ PrepMaps maps, const float* __
 // Output norm: a lane owns 8 consecutive channels (one 16-byte load), a row spans D / 8
 // lanes, so a warp covers 256 / D rows per step; each warp takes kNormSteps steps and
 // issues all its loads before reducing any row.
-constexpr int kNormSteps = 2;
+constexpr int kNormSteps = 1;
 
 template <int D>
 __global__ void __launch_bounds__(256)
