@@ -72,6 +72,25 @@ def test_prepare_inputs_against_reference(D, act, with_state):
     _close_bf16(beta, rb, "beta", scale=1.0)
 
 
+def test_prepare_inputs_boundaries_at_every_group_offset():
+    """16 sequences whose starts fall at every offset inside the 16-token groups a warp
+    takes (so groups mix whole-window and boundary tokens), several 64-token tiles each,
+    D = 128 with SiLU and carried-in conv state."""
+    lens = [16 * (i % 5 + 2) + 1 for i in range(16)]  # 33 .. 97 tokens, each 1 mod 16: starts at offsets 0..15
+    xq, xk, xv, w, a, b, cs, cu = _raw(lens, 2, 128, seed=77, with_state=True)
+    q, k, v, la, beta = _gpu_prepare(xq, xk, xv, w, a, b, cs, cu, 1)
+    torch.cuda.synchronize()
+    rq, rk, rv, rla, rb = prep.prepare_inputs(xq, xk, xv, w, a, b, cu, conv_state=cs, act=1)
+    starts = cu[:-1].numpy() % 16
+    assert sorted(set(starts.tolist())) == list(range(16))
+    for got, ref, nm in ((q, rq, "q"), (k, rk, "k")):
+        err = np.abs(got.float().cpu().double().numpy() - ref)
+        assert (err <= BF16_REL * np.abs(ref) + 2e-5).all(), nm
+    _close_bf16(v, rv, "v")
+    np.testing.assert_allclose(la.cpu().double().numpy(), rla, rtol=2e-6, atol=1e-7)
+    _close_bf16(beta, rb, "beta", scale=1.0)
+
+
 @pytest.mark.parametrize("o_f32", [False, True])
 def test_output_norm_against_reference(o_f32):
     g = torch.Generator().manual_seed(5)
