@@ -449,7 +449,7 @@ def main(argv=None):
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "tf32/f32 (bf16 in/out)", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp16/tf32 MMA, fp32 accumulate + state (bf16 in/out)", "data": "synthetic",
             "config": bench_config(world),
             "prefill_ms": pre_avg, "decode_ms": dec_avg,
             "decode": {"value": dec_gbs * world, "unit": "GB/s", "tokens_per_s": whole_job_rate(DEC_N, world, dec_avg),

@@ -8,6 +8,7 @@ namespace kda {
 
 // Status codes mirrored from include/kda.h (device side).
 constexpr int kStatusTimeout = -4;
+constexpr int kStatusRange = -5;
 
 // Device scratch of the prefill per (sequence, head): its hand-off ring of six
 // 82944-byte blocks.

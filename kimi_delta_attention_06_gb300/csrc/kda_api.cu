@@ -185,6 +185,7 @@ const char* kda_status_string(int status) {
         case KDA_ERR_UNSUPPORTED: return "unsupported shape or device";
         case KDA_ERR_CUDA: return "CUDA runtime error";
         case KDA_ERR_TIMEOUT: return "device-side wait timed out";
+        case KDA_ERR_RANGE: return "input outside the prefill's numeric domain";
         default: return "unknown status";
     }
 }

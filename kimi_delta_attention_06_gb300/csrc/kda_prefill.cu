@@ -7,8 +7,9 @@
 // 32K-token prefix-cache checkpoints).
 //
 // For one head and one chunk of C = 64 tokens, with g_t the chunk-local
-// cumulative log-decay (a vector over the Dk channels), r = token 31 the
-// reference point, and S the state entering the chunk:
+// cumulative log-decay (a vector over the Dk channels), g_r = g_C / 2 the
+// reference (the midpoint of the chunk's log-decay range), and S the state
+// entering the chunk:
 //
 //   Km = k * exp(g_t - g_r)    Qm = q * exp(g_t - g_r)    Kb = k * exp(g_r - g_t)
 //   L    = strict_lower(diag(beta) Km Kb^T)        A = lower_incl(Qm Kb^T)
@@ -24,8 +25,10 @@
 // the state and is prepared off the sequential path.
 // Products run as tcgen05 MMAs with fp32 accumulation in TMEM.  The two
 // intra-chunk products (Km Kb^T, Qm Kb^T) take tf32 operands: their factors
-// exp(+-(g_t - g_r)) span up to half a chunk of decay either way, which needs
-// an 8-bit exponent.  Everything else (start-referenced decayed operands with
+// exp(+-(g_t - g_r)) span up to half a chunk's total decay either way, which
+// needs an 8-bit exponent.  A chunk whose factors would leave the fp32 range
+// (summed |log_alpha| of a channel above about 174 over the chunk) records
+// KDA_ERR_RANGE.  Everything else (start-referenced decayed operands with
 // factors <= 1, A, T, X, U, the state) is range-safe and runs as fp16 MMAs
 // (10-bit mantissa like tf32, twice the rate, half the bytes).  The 64 x 64
 // triangular inverse runs on CUDA cores in fp32: 16 x 16 diagonal blocks by
@@ -126,6 +129,7 @@ constexpr uint32_t TM_G1 = 0, TM_M = 64, TM_W = 128, TM_PREP_COLS = 256;    // p
 constexpr uint32_t TM_D1A = 0, TM_D3 = 128, TM_D1B = 256, TM_CHAIN_COLS = 512;
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kMaxExp2 = 126.f;      // |x| bound for ex2(x) to stay a normal fp32 number
 
 // Decay layouts (include/kda.h kda_decay): per channel (KDA), one scalar per head and
 // token (Gated DeltaNet), or none (alpha = 1, DeltaNet).
@@ -450,18 +454,24 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         tc::named_sync(BAR_ALL, NT);     // totals visible; staging fully read; block free
         // -- 1b. decay factors and operand tiles --
         {
-            float4 off = make_float4(0.f, 0.f, 0.f, 0.f), gr = off, gc = off;
+            float4 off = make_float4(0.f, 0.f, 0.f, 0.f), gc = off;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const float4 tj = *reinterpret_cast<const float4*>(s_tot + j * 128 + 4 * cg);
                 if (j < tg) off = f4add(off, tj);
-                if (j < 4) gr = f4add(gr, tj);
                 gc = f4add(gc, tj);
             }
+            // reference: the midpoint g_C / 2 of the chunk's log-decay range [g_C, 0], so
+            // every factor exp(+-(g_t - g_r)) spans at most half the chunk's total decay
+            const float4 gr = make_float4(0.5f * gc.x, 0.5f * gc.y, 0.5f * gc.z, 0.5f * gc.w);
             const float4 L2 = make_float4(kLog2e, kLog2e, kLog2e, kLog2e);
             const float4 egr = f4ex2(f4mul(gr, L2));
             const float4 egc = f4ex2(f4mul(gc, L2));
-            const float4 ecr = f4ex2(f4mul(make_float4(gc.x - gr.x, gc.y - gr.y, gc.z - gr.z, gc.w - gr.w), L2));
+            const float4 ecr = egr;                        // exp(g_C - g_r) = exp(g_r)
+            // range: every exponent of 2 formed below must lie strictly inside (-126, 126)
+            // (beyond it ex2 overflows or flushes to zero); NaN fails the test too
+            bool out_of_range = !(fabsf(gr.x * kLog2e) < kMaxExp2) || !(fabsf(gr.y * kLog2e) < kMaxExp2) ||
+                                !(fabsf(gr.z * kLog2e) < kMaxExp2) || !(fabsf(gr.w * kLog2e) < kMaxExp2);
             if (tg == 0) *reinterpret_cast<float4*>(s_egc_out + 4 * cg) = egc;
             {   // V as an fp16 MN-major tile: thread -> (token tid / 4, columns 32 (tid % 4) .. +31)
                 const int tv = tid >> 2, cv = 32 * (tid & 3);
@@ -479,6 +489,8 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
                 const float4 g = f4add(g4[i], off);
                 const float4 x = make_float4((g.x - gr.x) * kLog2e, (g.y - gr.y) * kLog2e,
                                              (g.z - gr.z) * kLog2e, (g.w - gr.w) * kLog2e);
+                out_of_range |= !(fabsf(x.x) < kMaxExp2) || !(fabsf(x.y) < kMaxExp2) ||
+                                !(fabsf(x.z) < kMaxExp2) || !(fabsf(x.w) < kMaxExp2);
                 const float4 e1 = f4ex2(x);
                 const float4 e2 = f4ex2(make_float4(-x.x, -x.y, -x.z, -x.w));
                 const float4 kv = bf16x4_to_f4(k2[i]), qv = bf16x4_to_f4(q2[i]);
@@ -490,6 +502,7 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
                 st_h4(AH, 64 + t, 4 * cg, 128, f4mul(qm, egr));   // Q~ = q e^{g_t}
                 st_h4(KH, t, 4 * cg, 64, f4mul(kb, ecr));         // K^ = k e^{g_C - g_t}
             }
+            if (__any_sync(0xffffffffu, out_of_range) && lane == 0) set_status(p.status, kStatusRange);
         }
         if (beta_thread) s_beta[tid - 128] = bf16_bits_to_f32(bt);
         tc::fence_smem_to_async();
@@ -948,6 +961,14 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
         // loads still in flight must land before this CTA's shared memory goes away
         for (int j = waited; j < issued; ++j)
             tc::mbar_wait_bounded(&mb[KB_FULL + (j & 1)], static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs);
+    }
+    {   // a state driven outside the fp32 / fp16 operand range ends non-finite
+        bool fin = true;
+        if (d < dk && col_ok) {        // (rows / columns beyond Dk / Dv hold no state)
+#pragma unroll
+            for (int j = 0; j < 64; ++j) fin = fin && isfinite(S[j]);
+        }
+        if (ok && !__all_sync(0xffffffffu, fin) && (tid & 31) == 0) set_status(p.status, kStatusRange);
     }
     if (ok && p.final_state && d < dk && col_ok) {
         float* fp = p.final_state + ((static_cast<size_t>(n) * H + h) * dk + d) * dv + 64 * wg;

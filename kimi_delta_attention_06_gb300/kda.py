@@ -31,6 +31,7 @@ KDA_ERR_INVALID_ARG = -1
 KDA_ERR_UNSUPPORTED = -2
 KDA_ERR_CUDA = -3
 KDA_ERR_TIMEOUT = -4
+KDA_ERR_RANGE = -5
 KDA_OUT_BF16 = 0
 KDA_OUT_F32 = 1
 KDA_NOALLOC_MAX_SEQ_HEADS = 32

@@ -48,6 +48,8 @@ def test_status_strings_and_chunk_size(lib):
     assert kda.kda_status_string(0) == "ok"
     assert "invalid" in kda.kda_status_string(-1)
     assert "timed out" in kda.kda_status_string(-4)
+    assert "numeric domain" in kda.kda_status_string(-5)
+    assert kda.KDA_ERR_RANGE == -5
     assert kda.kda_chunk_size() == 64
 
 

@@ -1,5 +1,4 @@
 """GPU parity of kda_chunk_prefill against the fp64 oracle (through the C ABI)."""
-import numpy as np
 import pytest
 import torch
 
@@ -125,28 +124,37 @@ def test_single_sequence_8192_sampled_heads():
 
 def test_long_prompt_145408_checkpoints_sampled_head():
     """T=145408 (about 142k), H=32, D=128, checkpoints every 32768 tokens + the end (5 per head).
-    The oracle replays one head over the whole prompt; outputs are compared on every
-    1024th token of that head and all five checkpoints."""
+    The oracle replays one head over the whole prompt; that head's outputs are compared on
+    every token (all 64 rows of every chunk), together with all five checkpoints, in the
+    bf16 output mode the bench times and, under the strict bound, in the fp32 output mode."""
     c = workloads.single_case(145408, seed=2, device=DEV, ckpt_stride=32768)
     out, fin, ck = _run(c, torch.bfloat16, device_inputs=True)
     assert ck.shape[0] == 5
     heads = [5]
     ro, rf, rc = _oracle(c, heads)
-    rows = np.arange(0, 145408, 1024)
-    P.check_out(out[rows][:, heads], ro[rows], torch.bfloat16)
+    P.check_out(out[:, heads], ro, torch.bfloat16)
     P.check_state(fin[:, heads], rf)
     P.check_state(ck[:, heads], rc)
     torch.testing.assert_close(ck[4], fin[0], rtol=0, atol=0)
+    del out
+    out32, fin32, _ = _run(c, torch.float32, device_inputs=True)
+    P.check_out(out32[:, heads], ro, torch.float32)
+    assert torch.equal(fin32, fin)          # the output dtype changes only the final store
+    assert kda.kda_device_status() == 0
 
 
 def test_varlen_16_sequences_sampled():
     """16 packed sequences, log-uniform lengths in [1k, 64k] (~280k tokens), half with an
-    initial state, checkpoints every 32768 tokens; oracle on two heads of all sequences."""
+    initial state, checkpoints every 32768 tokens; oracle on two heads of all sequences,
+    compared on every token, in the bf16 and (strict bound) fp32 output modes."""
     c = workloads.varlen_case(device=DEV)
     out, fin, ck = _run(c, torch.bfloat16, device_inputs=True)
     heads = [3, 30]
     ro, rf, rc = _oracle(c, heads)
-    rows = np.arange(0, c.T, 512)
-    P.check_out(out[rows][:, heads], ro[rows], torch.bfloat16)
+    P.check_out(out[:, heads], ro, torch.bfloat16)
     P.check_state(fin[:, heads], rf)
     P.check_state(ck[:, heads], rc)
+    del out
+    out32, _, _ = _run(c, torch.float32, device_inputs=True)
+    P.check_out(out32[:, heads], ro, torch.float32)
+    assert kda.kda_device_status() == 0

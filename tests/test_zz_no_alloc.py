@@ -36,10 +36,14 @@ def _call(fn, case, dev_in, outs, stride):
        out, kda.KDA_OUT_BF16, fin, ck, stride)
 
 
-def test_noalloc_matches_pool_entry_point_twice():
+@pytest.mark.parametrize("lens", [[700, 64, 1130], [700, 64, 1130, 391]],
+                         ids=["24_pairs", "32_pairs_full_array"])
+def test_noalloc_matches_pool_entry_point_twice(lens):
+    """3 or 4 sequences x 8 heads, ragged lengths, nonzero initial states.  The 4-sequence case
+    fills every one of the KDA_NOALLOC_MAX_SEQ_HEADS rings, up to the array's end."""
     stride = 256
-    # 3 sequences x 8 heads = 24 (sequence, head) pairs, ragged lengths, nonzero initial states
-    case = workloads.prefill_case([700, 64, 1130], H=8, D=128, seed=21, ckpt_stride=stride)
+    case = workloads.prefill_case(lens, H=8, D=128, seed=21, ckpt_stride=stride)
+    assert len(lens) * 8 <= kda.KDA_NOALLOC_MAX_SEQ_HEADS
     dev_in = tuple(None if x is None else x.to(DEV) for x in
                    (case.q, case.k, case.v, case.log_alpha, case.beta, case.init_state, case.cu_seqlens))
     n_ck = kda.kda_ckpt_count(case.cu_seqlens, stride)
