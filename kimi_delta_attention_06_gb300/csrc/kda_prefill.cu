@@ -65,11 +65,10 @@ namespace prefill {
 
 constexpr int C = 64;           // chunk length (tokens)
 constexpr int DK = 128;         // internal key dim (Dk = 64 is zero-padded)
-constexpr int NT = 512;         // threads per CTA (16 warps: 4 per TMEM lane quadrant)
+constexpr int NT = 256;         // threads per CTA
 constexpr int NPREP_CTAS = 3;   // prep CTAs per cluster
 constexpr int CLUSTER = 1 + NPREP_CTAS;
-constexpr uint32_t BAR_ALL = 1;  // named barrier over the CTA's 512 threads
-constexpr uint32_t BAR_O = 2;    // chain CTA: named barrier of the 256 O-row threads
+constexpr uint32_t BAR_ALL = 1;  // named barrier over the CTA's 256 threads
 constexpr int ST_THREAD = 32;    // prep CTA: issues the ring stores and publishes them (not the MMA issuer)
 
 // Hand-off block: produced in a prep CTA, copied verbatim through the global ring into a chain slot.
@@ -96,10 +95,8 @@ constexpr uint32_t ST_V = P_B1;              // v bf16 [64][dv]
 constexpr uint32_t P_OUT = 98304;            // hand-off block                             (65 KB)
 constexpr uint32_t P_P = P_OUT + H_STRIDE;   // A f16, 64 rows x 64 K, K-major             (8 KB)
 constexpr uint32_t P_BETA = P_P + 8192;      // beta [64] f32
-constexpr uint32_t P_TOT = P_BETA + 256;     // 4-token-group log-decay totals [16][128] f32 (then
-                                             // their exclusive prefix over the groups)
-constexpr uint32_t P_GC = P_TOT + 8192;      // the chunk's total log-decay g_C [128] f32
-constexpr uint32_t P_BAR = P_GC + 512;       // mbarriers: 0 mma, 1-2 ring entry free, 3 tma
+constexpr uint32_t P_TOT = P_BETA + 256;     // token-group log-decay totals [8][128] f32
+constexpr uint32_t P_BAR = P_TOT + 4096;     // mbarriers: 0 mma, 1-2 ring entry free, 3 tma
 constexpr uint32_t P_TMEM = P_BAR + 32;
 // fp16 scratch of the inverse (row pitch LH halves)
 constexpr int LH = 72;
@@ -371,7 +368,6 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
     __half* Yh = reinterpret_cast<__half*>(sm + P_Y);
     float* s_beta = reinterpret_cast<float*>(sm + P_BETA);
     float* s_tot = reinterpret_cast<float*>(sm + P_TOT);
-    float* s_gc = reinterpret_cast<float*>(sm + P_GC);
     uint64_t* mb = reinterpret_cast<uint64_t*>(sm + P_BAR);    // 0: mma, 1-2: ring entry free, 3: tma
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + P_TMEM);
 
@@ -394,7 +390,7 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         tc::mbar_arrive_remote(chain_ready0 + 8u * static_cast<uint32_t>(pending % WS_SLOTS));
     };
 
-    const int cg = lane, tg = warp;                     // channels 4cg..4cg+3, tokens 4tg..4tg+3
+    const int cg = tid & 31, tg = tid >> 5;             // channels 4cg..4cg+3, tokens 8tg..8tg+7
     const bool ch_ok = 4 * cg < dk;
     // beta of token (tid - 128): warps 4-5 load the raw bits one chunk ahead (converted
     // only where the value is stored, so the load stays in flight across the chunk
@@ -431,81 +427,77 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         // -- 0. inputs of this chunk: staging (TMA) -> registers --
         if (tid == 0 && c + 2 * NPREP_CTAS < nchunks) prefetch_inputs<DECAY>(tmaps, p, c + 2 * NPREP_CTAS, g, h);
         if (!cta_wait(&mb[3], kk & 1, false)) { ok = false; break; }
-        float4 g4[4];
-        uint2 q2[4], k2[4];
-        uint4 v4[2];
+        float4 g4[8];
+        uint2 q2[8], k2[8];
+        uint4 v4[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int t = 4 * tg + i;
+        for (int i = 0; i < 8; ++i) {
+            const int t = 8 * tg + i;
             const bool ok_t = t >= lo && t < hi && ch_ok;
             q2[i] = ok_t ? *reinterpret_cast<const uint2*>(sm + ST_Q + (t * dk + 4 * cg) * 2) : make_uint2(0u, 0u);
             k2[i] = ok_t ? *reinterpret_cast<const uint2*>(sm + ST_K + (t * dk + 4 * cg) * 2) : make_uint2(0u, 0u);
         }
         if (DECAY == DECAY_CHANNEL) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int t = 4 * tg + i;
+            for (int i = 0; i < 8; ++i) {
+                const int t = 8 * tg + i;
                 g4[i] = (t >= lo && t < hi && ch_ok)
                     ? *reinterpret_cast<const float4*>(sm + ST_LA + (t * dk + 4 * cg) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         } else if (DECAY == DECAY_HEAD) {     // the head's scalar, on every channel
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int t = 4 * tg + i;
+            for (int i = 0; i < 8; ++i) {
+                const int t = 8 * tg + i;
                 const float x = (t >= lo && t < hi && ch_ok)
                     ? *reinterpret_cast<const float*>(sm + ST_LA + (t * 4 + (h & 3)) * 4) : 0.f;
                 g4[i] = make_float4(x, x, x, x);
             }
         } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) g4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i = 0; i < 8; ++i) g4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        const int tv = tid >> 3, cv = 16 * (tid & 7);   // V: token tid / 8, columns 16 (tid % 8) .. +15
         {
+            const int tv = tid >> 2, cv = 32 * (tid & 3);
             const bool vok = tv >= lo && tv < hi && cv < dv;
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
+            for (int j = 0; j < 4; ++j)
                 v4[j] = vok ? *reinterpret_cast<const uint4*>(sm + ST_V + (tv * dv + cv + 8 * j) * 2) : make_uint4(0u, 0u, 0u, 0u);
         }
-        // -- 1a. cumulative log-decay inside each 4-token group --
+        // -- 1a. cumulative log-decay inside each 8-token group --
         {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) { acc = f4add(acc, g4[i]); g4[i] = acc; }
+            for (int i = 0; i < 8; ++i) { acc = f4add(acc, g4[i]); g4[i] = acc; }
             *reinterpret_cast<float4*>(s_tot + tg * 128 + 4 * cg) = acc;
         }
         // the stores of the previous block must have read it before it is rewritten
         if (pending >= 0 && tid == ST_THREAD) tc::bulk_wait_read_all();
         tc::named_sync(BAR_ALL, NT);     // totals visible; staging fully read; block free
-        // -- 1b. exclusive prefix of the group totals, and g_C, per channel (one thread each) --
-        if (tid < 128) {
-            float x[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) x[j] = s_tot[j * 128 + tid];
-            float run = 0.f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) { s_tot[j * 128 + tid] = run; run += x[j]; }
-            s_gc[tid] = run;
-        }
-        tc::named_sync(BAR_ALL, NT);
-        // -- 1c. decay factors and operand tiles --
+        // -- 1b. decay factors and operand tiles --
         {
-            const float4 off = *reinterpret_cast<const float4*>(s_tot + tg * 128 + 4 * cg);
-            const float4 gc = *reinterpret_cast<const float4*>(s_gc + 4 * cg);
+            float4 off = make_float4(0.f, 0.f, 0.f, 0.f), gc = off;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 tj = *reinterpret_cast<const float4*>(s_tot + j * 128 + 4 * cg);
+                if (j < tg) off = f4add(off, tj);
+                gc = f4add(gc, tj);
+            }
             // reference: the midpoint g_C / 2 of the chunk's log-decay range [g_C, 0], so
             // every factor exp(+-(g_t - g_r)) spans at most half the chunk's total decay
             const float4 gr = make_float4(0.5f * gc.x, 0.5f * gc.y, 0.5f * gc.z, 0.5f * gc.w);
             const float4 L2 = make_float4(kLog2e, kLog2e, kLog2e, kLog2e);
             const float4 egr = f4ex2(f4mul(gr, L2));
+            const float4 egc = f4ex2(f4mul(gc, L2));
             const float4 ecr = egr;                        // exp(g_C - g_r) = exp(g_r)
             // range: every exponent of 2 formed below must lie strictly inside (-126, 126)
             // (beyond it ex2 overflows or flushes to zero); NaN fails the test too
             bool out_of_range = !(fabsf(gr.x * kLog2e) < kMaxExp2) || !(fabsf(gr.y * kLog2e) < kMaxExp2) ||
                                 !(fabsf(gr.z * kLog2e) < kMaxExp2) || !(fabsf(gr.w * kLog2e) < kMaxExp2);
-            if (tg == 0) *reinterpret_cast<float4*>(s_egc_out + 4 * cg) = f4ex2(f4mul(gc, L2));
-            {   // V as an fp16 MN-major tile
+            if (tg == 0) *reinterpret_cast<float4*>(s_egc_out + 4 * cg) = egc;
+            {   // V as an fp16 MN-major tile: thread -> (token tid / 4, columns 32 (tid % 4) .. +31)
+                const int tv = tid >> 2, cv = 32 * (tid & 3);
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
+                for (int j = 0; j < 4; ++j) {
                     const float2 a0 = bf16x2_bits_to_f32(v4[j].x), a1 = bf16x2_bits_to_f32(v4[j].y);
                     const float2 a2 = bf16x2_bits_to_f32(v4[j].z), a3 = bf16x2_bits_to_f32(v4[j].w);
                     const float x8[8] = {a0.x, a0.y, a1.x, a1.y, a2.x, a2.y, a3.x, a3.y};
@@ -513,8 +505,8 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
                 }
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int t = 4 * tg + i;
+            for (int i = 0; i < 8; ++i) {
+                const int t = 8 * tg + i;
                 const float4 g = f4add(g4[i], off);
                 const float4 x = make_float4((g.x - gr.x) * kLog2e, (g.y - gr.y) * kLog2e,
                                              (g.z - gr.z) * kLog2e, (g.w - gr.w) * kLog2e);
@@ -564,19 +556,17 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             }
         }
 
-        // -- 3. L (rows 0..63 -> fp16 scratch), A (rows 64..127 -> f16 tile) --
-        //    warp -> TMEM lane quadrant warp % 4, columns 16 (warp / 4) .. +15
+        // -- 3. L (rows 0..63 -> fp32 scratch), A (rows 64..127 -> f16 tile) --
         {
             const int r = (warp & 3) * 32 + lane;
-            const int c0 = (warp >> 2) * 16;
-            float v[16];
-            tc::tmem_ld16(lane_base + TM_G1 + c0, v);
-            tc::tmem_wait_ld();
+            const int c0 = (warp >> 2) * 32;                 // warps 0-3: cols 0..31, 4-7: 32..63
+            float v[32];
+            tmem_ld32(lane_base + TM_G1 + c0, v);
             if (r < 64) {
                 const float b = s_beta[r];
                 __half* Lr = Lh + r * LH + c0;
 #pragma unroll
-                for (int i = 0; i < 16; i += 8) {
+                for (int i = 0; i < 32; i += 8) {
                     uint4 w;
                     w.x = f16x2_bits((c0 + i + 0 < r) ? b * v[i + 0] : 0.f, (c0 + i + 1 < r) ? b * v[i + 1] : 0.f);
                     w.y = f16x2_bits((c0 + i + 2 < r) ? b * v[i + 2] : 0.f, (c0 + i + 3 < r) ? b * v[i + 3] : 0.f);
@@ -587,9 +577,9 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             } else {
                 const int t = r - 64;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = (c0 + i <= t) ? v[i] : 0.f;
+                for (int i = 0; i < 32; ++i) v[i] = (c0 + i <= t) ? v[i] : 0.f;
 #pragma unroll
-                for (int i = 0; i < 16; i += 8) st_h8(P, t, c0 + i, 64, v + i);
+                for (int i = 0; i < 32; i += 8) st_h8(P, t, c0 + i, 64, v + i);
             }
         }
         tc::fence_before_sync();
@@ -640,57 +630,54 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             }
         }
         tc::named_sync(BAR_ALL, NT);
-        {                         // 32 -> 64: warps 0-7, warp -> 16 x 8 tile (m = warp / 4, n = warp % 4)
-            const int m = (warp >> 2) & 1, nn = warp & 3;
+        {                         // 32 -> 64: warp -> 16 x 8 tile (m = warp / 4, n = warp % 4)
+            const int m = warp >> 2, nn = warp & 3;
             uint32_t a[4], b[2];
-            if (warp < 8) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {          // Y = L[32:64, 0:32] T[0:32, 0:32]
-                    ldsm_a(Lh, LH, 32 + 16 * m, 16 * ks, a);
-                    ldsm_b(Th, LH, 16 * ks, 8 * nn, b);
-                    mma16816(acc, a, b);
-                }
-                st_frag(Yh, LH, 16 * m, 8 * nn, acc, 1.f);
+            for (int ks = 0; ks < 2; ++ks) {              // Y = L[32:64, 0:32] T[0:32, 0:32]
+                ldsm_a(Lh, LH, 32 + 16 * m, 16 * ks, a);
+                ldsm_b(Th, LH, 16 * ks, 8 * nn, b);
+                mma16816(acc, a, b);
             }
+            st_frag(Yh, LH, 16 * m, 8 * nn, acc, 1.f);
             tc::named_sync(BAR_ALL, NT);
-            if (warp < 8) {
-                float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+            float acc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {          // T[32:64, 0:32] = -T[32:64, 32:64] Y
-                    ldsm_a(Th, LH, 32 + 16 * m, 32 + 16 * ks, a);
-                    ldsm_b(Yh, LH, 16 * ks, 8 * nn, b);
-                    mma16816(acc2, a, b);
-                }
-                st_frag(Th, LH, 32 + 16 * m, 8 * nn, acc2, -1.f);
+            for (int ks = 0; ks < 2; ++ks) {              // T[32:64, 0:32] = -T[32:64, 32:64] Y
+                ldsm_a(Th, LH, 32 + 16 * m, 32 + 16 * ks, a);
+                ldsm_b(Yh, LH, 16 * ks, 8 * nn, b);
+                mma16816(acc2, a, b);
             }
+            st_frag(Th, LH, 32 + 16 * m, 8 * nn, acc2, -1.f);
         }
         tc::named_sync(BAR_ALL, NT);
-        {   // T diag(beta) -> rows 0..63 of [T; Mqk]: thread -> (row tid / 8, 8 columns)
-            const int t = tid >> 3, c0 = (tid & 7) * 8;
-            float tb[8];
+        {   // T diag(beta) -> rows 0..63 of [T; Mqk]: thread -> (row, 16 columns)
+            const int t = tid >> 2, c0 = (tid & 3) * 16;
+            float tb[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) tb[i] = __half2float(Th[t * LH + c0 + i]) * s_beta[c0 + i];
+            for (int i = 0; i < 16; ++i) tb[i] = __half2float(Th[t * LH + c0 + i]) * s_beta[c0 + i];
             st_h8(Qt, t, c0, 128, tb);
+            st_h8(Qt, t, c0 + 8, 128, tb + 8);
         }
         tc::named_sync(BAR_ALL, NT);
         // -- 5. Mqk = A T diag(beta) on warp MMAs, into rows 64..127 of [T; Mqk] --
-        //    warp -> rows 16 (warp / 4) .. +15, columns 16 (warp % 4) .. +15; A and T are
+        //    warp -> rows 16 (warp / 2) .. +15, columns 32 (warp % 2) .. +31; A and T are
         //    lower triangular, so the K range stops at the row block's end
         {
-            const int m = warp >> 2, n0 = 16 * (warp & 3);
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            const int m = warp >> 1, n0 = 32 * (warp & 1);
+            float acc[4][4] = {};
             for (int ks = 0; ks <= m; ++ks) {
                 uint32_t a[4], b[2];
                 ldsm_a_sw(P, 64, 16 * m, 16 * ks, a);
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
+                for (int nt = 0; nt < 4; ++nt) {
                     ldsm_b_sw(Qt, 128, 16 * ks, n0 + 8 * nt, b);
                     mma16816(acc[nt], a, b);
                 }
             }
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) st_frag_sw(Qt, 128, 64 + 16 * m, n0 + 8 * nt, acc[nt]);
+            for (int nt = 0; nt < 4; ++nt) st_frag_sw(Qt, 128, 64 + 16 * m, n0 + 8 * nt, acc[nt]);
         }
         tc::fence_smem_to_async();
         cta_sync_tc();
@@ -706,30 +693,32 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         }
         if (!cta_wait(&mb[0], ph_mma & 1, false)) { ok = false; break; }
         ++ph_mma;
-        {   // rows 0..63: -W over K~; rows 64..127: Q' = Q~ - Mqk K~ in place
-            //  warp -> TMEM lane quadrant warp % 4, columns 32 (warp / 4) .. +31
+        {   // rows 0..63: -W over K~; rows 64..127: Q' = Q~ - Mqk K~ in place (warps 4-7: columns 64..127)
             const int r = (warp & 3) * 32 + lane;
-            const int c0 = (warp >> 2) * 32;
+            const int c0 = (warp >> 2) * 64;
             float v[32];
-            tmem_ld32(lane_base + TM_W + c0, v);
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-                const int col = c0 + i;
-                float x8[8];
-                if (r < 64) {
+            for (int q4 = 0; q4 < 2; ++q4) {
+                tmem_ld32(lane_base + TM_W + c0 + 32 * q4, v);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) x8[j] = -v[i + j];
-                } else {
-                    const uint4 w = *reinterpret_cast<const uint4*>(AH + tc::sw128_off16(r, col, 128));
-                    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+                for (int i = 0; i < 32; i += 8) {
+                    const int col = c0 + 32 * q4 + i;
+                    float x8[8];
+                    if (r < 64) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[j]));
-                        x8[2 * j] = f.x - v[i + 2 * j];
-                        x8[2 * j + 1] = f.y - v[i + 2 * j + 1];
+                        for (int j = 0; j < 8; ++j) x8[j] = -v[i + j];
+                    } else {
+                        const uint4 w = *reinterpret_cast<const uint4*>(AH + tc::sw128_off16(r, col, 128));
+                        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[j]));
+                            x8[2 * j] = f.x - v[i + 2 * j];
+                            x8[2 * j + 1] = f.y - v[i + 2 * j + 1];
+                        }
                     }
+                    st_h8(AH, r, col, 128, x8);
                 }
-                st_h8(AH, r, col, 128, x8);
             }
         }
         tc::fence_smem_to_async();
@@ -765,10 +754,10 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + K_TMEM);
 
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int d = (warp & 3) * 32 + (tid & 31);   // state row = TMEM lane (warp % 4 selects the quadrant)
-    const int cq = warp >> 2;                      // value columns 32 cq .. 32 cq + 31
+    const int d = tid & 127;                 // state row = TMEM lane
+    const int wg = tid >> 7;                 // value columns 64 wg .. 64 wg + 63
     const int H = p.H, dk = p.dk, dv = p.dv;
-    const bool col_ok = 32 * cq < dv;
+    const bool col_ok = 64 * wg < dv;
     const size_t vtok_stride = static_cast<size_t>(H) * dv;
     const int nchunks = g.nchunks, len = g.len;
 
@@ -776,12 +765,10 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
     cta_sync_tc();
     const uint32_t tm = *s_tmem;
     const uint32_t lane_base = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const uint32_t cb = static_cast<uint32_t>(32 * cq);      // this thread's TMEM column offset
-    // O staging: two 64-column boxes (128B-swizzled bf16, 64 rows each); columns 32 cq.. sit
-    // in box cq / 2 at inner column 32 (cq % 2)
-    uint8_t* Ot = sm + K_O + 8192 * (cq >> 1);
-    const int ocol = 32 * (cq & 1);
-    constexpr int O_ISSUER = 64;                               // tid of the O writer that issues the TMA stores
+    const uint32_t cb = static_cast<uint32_t>(64 * wg);      // this warpgroup's TMEM column offset
+    uint8_t* Ot = sm + K_O + 8192 * wg;                        // this warpgroup's O staging tile
+    const uint32_t bar_o = 2u + static_cast<uint32_t>(wg);   // named barrier of its 64 O writers
+    constexpr int O_ISSUER = 64;                               // O writer (per warpgroup) that issues the TMA store
     const uint32_t prep_free = tc::smem_u32(sm + P_BAR + 8);  // local offset of the prep CTAs' ring barriers
     const uint8_t* ring = p.ws + ring_idx * WS_BYTES_PER_CLUSTER;
 
@@ -795,12 +782,12 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
             if (lm > 0) slot_ck += (sm0 + lm - 1) / p.ckpt_stride - sm0 / p.ckpt_stride + 1;
         }
     }
-    float S[32];
+    float S[64];
     {
         const float* s0 = (p.init_state && col_ok && d < dk)
-            ? p.init_state + ((static_cast<size_t>(n) * H + h) * dk + d) * dv + 32 * cq : nullptr;
+            ? p.init_state + ((static_cast<size_t>(n) * H + h) * dk + d) * dv + 64 * wg : nullptr;
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
+        for (int j = 0; j < 64; j += 4) {
             float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
             if (s0) v4 = *reinterpret_cast<const float4*>(s0 + j);
             S[j] = v4.x; S[j + 1] = v4.y; S[j + 2] = v4.z; S[j + 3] = v4.w;
@@ -852,7 +839,7 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
     // the barrier of the next slot wait publishes it
     auto write_sb = [&]() {
 #pragma unroll
-        for (int j = 0; j < 32; j += 8) st_h8(Sb, d, 32 * cq + j, 128, S + j);
+        for (int j = 0; j < 64; j += 8) st_h8(Sb, d, 64 * wg + j, 128, S + j);
         tc::fence_smem_to_async();
     };
     if (nchunks > 0) write_sb();
@@ -882,10 +869,10 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
         if (!cta_wait(&mb[KB_MMA], ph_mma & 1, false)) { ok = false; break; }
         ++ph_mma;
         if (d < 64 && col_ok) {   // U -> MN-major f16 tile, over the (now dead) V tile of the slot
-            float r[32];
-            tmem_ld32(lane_base + d1 + cb, r);
+            float r[64];
+            tmem_ld64(lane_base + d1 + cb, r);
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) st_h8(slot + H_V, d, 32 * cq + j, 64, r + j);
+            for (int j = 0; j < 64; j += 8) st_h8(slot + H_V, d, 64 * wg + j, 64, r + j);
             tc::fence_smem_to_async();                   // only the U writers touched shared memory
         }
         cta_sync_tc();
@@ -899,39 +886,36 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
             if (c + 1 < nchunks && tc::mbar_test_wait(&mb[KB_FULL + (s ^ 1)], ((c + 1) >> 1) & 1)) issue_vpart(c + 1);
             probe(c + 2);
         }
-        if (d >= 64) {                                   // O rows (TMEM lanes 64..127) while D3 runs
+        if (d >= 64 && col_ok) {                         // O rows (TMEM lanes 64..127) while D3 runs
             const int t = d - 64;
             const uint32_t oaddr = lane_base + d1 + cb;
             if (!p.out_f32 && lo == 0 && hi == C) {
-                // staged as 128B-swizzled bf16 boxes of 64 columns, written out by TMA stores
-                float a[32];
-                if (col_ok) tmem_ld32(oaddr, a);
-                if (tid == O_ISSUER) tc::bulk_wait_read_all();     // the previous stores have read the tiles
-                tc::named_sync(BAR_O, 256);
-                if (col_ok) {
+                // staged as a 128B-swizzled bf16 tile per warpgroup, written out by one TMA store
+                float a[64];
+                tmem_ld64(oaddr, a);
+                if (d == O_ISSUER) tc::bulk_wait_read_all();       // the previous store has read the tile
+                tc::named_sync(bar_o, 64);
 #pragma unroll
-                    for (int j = 0; j < 32; j += 8) {
-                        uint4 w;
-                        w.x = f32x2_to_bf16x2_bits(a[j], a[j + 1]);
-                        w.y = f32x2_to_bf16x2_bits(a[j + 2], a[j + 3]);
-                        w.z = f32x2_to_bf16x2_bits(a[j + 4], a[j + 5]);
-                        w.w = f32x2_to_bf16x2_bits(a[j + 6], a[j + 7]);
-                        *reinterpret_cast<uint4*>(Ot + tc::sw128_off16(t, ocol + j, 64)) = w;
-                    }
-                    tc::fence_smem_to_async();
+                for (int j = 0; j < 64; j += 8) {
+                    uint4 w;
+                    w.x = f32x2_to_bf16x2_bits(a[j], a[j + 1]);
+                    w.y = f32x2_to_bf16x2_bits(a[j + 2], a[j + 3]);
+                    w.z = f32x2_to_bf16x2_bits(a[j + 4], a[j + 5]);
+                    w.w = f32x2_to_bf16x2_bits(a[j + 6], a[j + 7]);
+                    *reinterpret_cast<uint4*>(Ot + tc::sw128_off16(t, j, 64)) = w;
                 }
-                tc::named_sync(BAR_O, 256);
-                if (tid == O_ISSUER) {
-                    for (int b = 0; b < dv / 64; ++b)
-                        tc::tma_store_2d(&tmaps.o, tc::smem_u32(sm + K_O + 8192 * b), h * dv + 64 * b, cs);
+                tc::fence_smem_to_async();
+                tc::named_sync(bar_o, 64);
+                if (d == O_ISSUER) {
+                    tc::tma_store_2d(&tmaps.o, tc::smem_u32(Ot), h * dv + 64 * wg, cs);
                     tc::bulk_commit();
                 }
-            } else if (col_ok) {
+            } else {
                 const bool row_ok = t >= lo && t < hi;
-                const size_t ob = row_ok ? static_cast<size_t>(cs + t) * vtok_stride + static_cast<size_t>(h) * dv + 32 * cq
+                const size_t ob = row_ok ? static_cast<size_t>(cs + t) * vtok_stride + static_cast<size_t>(h) * dv + 64 * wg
                                          : 0;
 #pragma unroll
-                for (int c16 = 0; c16 < 32; c16 += 16) {
+                for (int c16 = 0; c16 < 64; c16 += 16) {
                     float a[16];
                     tc::tmem_ld16(oaddr + c16, a);
                     tc::tmem_wait_ld();
@@ -964,10 +948,10 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
             probe(c + 3);
         }
         {
-            float r[32];
-            tmem_ld32(lane_base + TM_D3 + cb, r);
+            float r[64];
+            tmem_ld64(lane_base + TM_D3 + cb, r);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) S[j] = gc * S[j] + r[j];
+            for (int j = 0; j < 64; ++j) S[j] = gc * S[j] + r[j];
         }
         if (c + 1 < nchunks) write_sb();
         // -- prefix-cache checkpoint at stride multiples and at the sequence end --
@@ -975,9 +959,9 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
             const int done = g.done(c);                 // tokens of the sequence through this chunk
             if ((g.start + done) % p.ckpt_stride == 0 || done == len) {
                 if (d < dk && col_ok) {
-                    float* cp = p.ckpt + ((static_cast<size_t>(slot_ck) * H + h) * dk + d) * dv + 32 * cq;
+                    float* cp = p.ckpt + ((static_cast<size_t>(slot_ck) * H + h) * dk + d) * dv + 64 * wg;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4)
+                    for (int j = 0; j < 64; j += 4)
                         *reinterpret_cast<float4*>(cp + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
                 }
                 ++slot_ck;
@@ -986,7 +970,7 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
     }
     // O tiles must stay until their stores have read them; the MMAs thread 0 issued
     // (possibly a V part of a chunk the loop never reached) must finish before TMEM is freed
-    if (tid == O_ISSUER) tc::bulk_wait_all();
+    if (d == O_ISSUER) tc::bulk_wait_all();
     if (tid == 0) {
         tc::mma_commit(&mb[KB_MMA]);
         tc::mbar_wait_bounded(&mb[KB_MMA], ph_mma & 1, kWaitLimitNs);
@@ -1000,17 +984,17 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
         bool fin = true;
         if (d < dk && col_ok) {        // (rows / columns beyond Dk / Dv hold no state)
 #pragma unroll
-            for (int j = 0; j < 32; ++j) fin = fin && isfinite(S[j]);
+            for (int j = 0; j < 64; ++j) fin = fin && isfinite(S[j]);
         }
         if (ok && !__all_sync(0xffffffffu, fin) && (tid & 31) == 0) set_status(p.status, kStatusRange);
     }
     if (ok && p.final_state && d < dk && col_ok) {
-        float* fp = p.final_state + ((static_cast<size_t>(n) * H + h) * dk + d) * dv + 32 * cq;
+        float* fp = p.final_state + ((static_cast<size_t>(n) * H + h) * dk + d) * dv + 64 * wg;
 #pragma unroll
-        for (int j = 0; j < 32; j += 4)
+        for (int j = 0; j < 64; j += 4)
             *reinterpret_cast<float4*>(fp + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
-    if ((!ok || !load_ok) && d == 0 && cq == 0) set_status(p.status, kStatusTimeout);
+    if ((!ok || !load_ok) && d == 0) set_status(p.status, kStatusTimeout);
     cta_sync_tc();
     if (warp == 0) tc::tmem_dealloc(tm, TM_CHAIN_COLS);
 }
