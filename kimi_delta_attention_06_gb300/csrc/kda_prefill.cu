@@ -794,10 +794,11 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
         }
     }
 
-    // Loader (thread 0): chunk j goes from ring entry j % 6 into slot j % 2 once its prep
-    // CTA has stored it and the chain is done with chunk j - 2.  Loads are issued
-    // in order; `issued` counts them.  Non-blocking probes run between thread 0's other
-    // duties so that the next chunk is normally in flight long before it is needed.
+    // Loader (thread LD, which issues no MMA): chunk j goes from ring entry j % 6 into slot
+    // j % 2 once its prep CTA has stored it and the chain is done with chunk j - 2.  Loads
+    // are issued in order; `issued` counts them.  Non-blocking probes run while thread 0
+    // issues MMAs, so that the next chunk is normally in flight long before it is needed.
+    constexpr int LD = 32;
     int issued = 0;
     bool load_ok = true;
     auto load = [&](int j, bool block) -> bool {
@@ -842,16 +843,72 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
         for (int j = 0; j < 64; j += 8) st_h8(Sb, d, 64 * wg + j, 128, S + j);
         tc::fence_smem_to_async();
     };
+    // O of chunk j (TMEM lanes 64..127 of TM_D1[j % 2]), by the 128 O-row threads.  It runs
+    // one chunk late, inside the next chunk's first-MMA window, where those threads would
+    // otherwise wait: the accumulator stays intact until chunk j + 2's V part, which is
+    // issued only after the barrier that follows this epilogue.
+    auto o_epilogue = [&](int j) {
+        const int t = d - 64;
+        const int cs = g.row0(j), lo = g.lo(j), hi = g.hi(j);
+        const uint32_t oaddr = lane_base + ((j & 1) ? TM_D1B : TM_D1A) + cb;
+        if (!p.out_f32 && lo == 0 && hi == C) {
+            // staged as a 128B-swizzled bf16 tile per warpgroup, written out by one TMA store
+            float a[64];
+            tmem_ld64(oaddr, a);
+            if (d == O_ISSUER) tc::bulk_wait_read_all();       // the previous store has read the tile
+            tc::named_sync(bar_o, 64);
+#pragma unroll
+            for (int q = 0; q < 64; q += 8) {
+                uint4 w;
+                w.x = f32x2_to_bf16x2_bits(a[q], a[q + 1]);
+                w.y = f32x2_to_bf16x2_bits(a[q + 2], a[q + 3]);
+                w.z = f32x2_to_bf16x2_bits(a[q + 4], a[q + 5]);
+                w.w = f32x2_to_bf16x2_bits(a[q + 6], a[q + 7]);
+                *reinterpret_cast<uint4*>(Ot + tc::sw128_off16(t, q, 64)) = w;
+            }
+            tc::fence_smem_to_async();
+            tc::named_sync(bar_o, 64);
+            if (d == O_ISSUER) {
+                tc::tma_store_2d(&tmaps.o, tc::smem_u32(Ot), h * dv + 64 * wg, cs);
+                tc::bulk_commit();
+            }
+        } else {
+            const bool row_ok = t >= lo && t < hi;
+            const size_t ob = row_ok ? static_cast<size_t>(cs + t) * vtok_stride + static_cast<size_t>(h) * dv + 64 * wg
+                                     : 0;
+#pragma unroll
+            for (int c16 = 0; c16 < 64; c16 += 16) {
+                float a[16];
+                tc::tmem_ld16(oaddr + c16, a);
+                tc::tmem_wait_ld();
+                if (row_ok) {
+                    if (p.out_f32) {
+                        float* op = reinterpret_cast<float*>(p.out) + ob + c16;
+#pragma unroll
+                        for (int q = 0; q < 16; q += 4)
+                            *reinterpret_cast<float4*>(op + q) = make_float4(a[q], a[q + 1], a[q + 2], a[q + 3]);
+                    } else {
+                        uint16_t* op = reinterpret_cast<uint16_t*>(p.out) + ob + c16;
+#pragma unroll
+                        for (int q = 0; q < 16; q += 8) {
+                            uint4 w;
+                            w.x = f32x2_to_bf16x2_bits(a[q], a[q + 1]);
+                            w.y = f32x2_to_bf16x2_bits(a[q + 2], a[q + 3]);
+                            w.z = f32x2_to_bf16x2_bits(a[q + 4], a[q + 5]);
+                            w.w = f32x2_to_bf16x2_bits(a[q + 6], a[q + 7]);
+                            *reinterpret_cast<uint4*>(op + q) = w;
+                        }
+                    }
+                }
+            }
+        }
+    };
     if (nchunks > 0) write_sb();
     for (int c = 0; c < nchunks; ++c) {
-        const int cs = g.row0(c);                       // packed row of chunk row 0
-        const int lo = g.lo(c), hi = g.hi(c);           // the sequence's rows of this chunk
         const int s = c & 1;
         uint8_t* slot = sm + K_SLOT + s * H_STRIDE;
         const uint32_t d1 = (s ? TM_D1B : TM_D1A);
-        // (the next chunk's load is probed once this chunk's MMA is under way, not here,
-        // where every thread waits for thread 0)
-        if (tid == 0 && issued == c && load_ok) load_ok = load(c, true);
+        if (tid == LD && issued == c && load_ok) load_ok = load(c, true);
         if (!cta_wait(&mb[KB_FULL + s], (c >> 1) & 1, false)) { ok = false; break; }
         waited = c + 1;
         if (tid == 0) {
@@ -863,8 +920,9 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
             issue_mma<true>(tm + d1, 128, Nmma, DK, tc::smem_u32(slot + H_AH), false, 128,
                             tc::smem_u32(Sb), true, 128u * 128u, true);
             tc::mma_commit(&mb[KB_MMA]);
-            probe(c + 2);
         }
+        if (tid == LD) probe(c + 2);
+        if (d >= 64 && col_ok && c > 0) o_epilogue(c - 1);   // the previous chunk's O, while this MMA runs
         const float gc = reinterpret_cast<const float*>(slot + H_EGC)[d];
         if (!cta_wait(&mb[KB_MMA], ph_mma & 1, false)) { ok = false; break; }
         ++ph_mma;
@@ -884,69 +942,11 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
             tc::mma_commit(&mb[KB_MMA]);
             // the next chunk's V part can run now if its slot has landed
             if (c + 1 < nchunks && tc::mbar_test_wait(&mb[KB_FULL + (s ^ 1)], ((c + 1) >> 1) & 1)) issue_vpart(c + 1);
-            probe(c + 2);
         }
-        if (d >= 64 && col_ok) {                         // O rows (TMEM lanes 64..127) while D3 runs
-            const int t = d - 64;
-            const uint32_t oaddr = lane_base + d1 + cb;
-            if (!p.out_f32 && lo == 0 && hi == C) {
-                // staged as a 128B-swizzled bf16 tile per warpgroup, written out by one TMA store
-                float a[64];
-                tmem_ld64(oaddr, a);
-                if (d == O_ISSUER) tc::bulk_wait_read_all();       // the previous store has read the tile
-                tc::named_sync(bar_o, 64);
-#pragma unroll
-                for (int j = 0; j < 64; j += 8) {
-                    uint4 w;
-                    w.x = f32x2_to_bf16x2_bits(a[j], a[j + 1]);
-                    w.y = f32x2_to_bf16x2_bits(a[j + 2], a[j + 3]);
-                    w.z = f32x2_to_bf16x2_bits(a[j + 4], a[j + 5]);
-                    w.w = f32x2_to_bf16x2_bits(a[j + 6], a[j + 7]);
-                    *reinterpret_cast<uint4*>(Ot + tc::sw128_off16(t, j, 64)) = w;
-                }
-                tc::fence_smem_to_async();
-                tc::named_sync(bar_o, 64);
-                if (d == O_ISSUER) {
-                    tc::tma_store_2d(&tmaps.o, tc::smem_u32(Ot), h * dv + 64 * wg, cs);
-                    tc::bulk_commit();
-                }
-            } else {
-                const bool row_ok = t >= lo && t < hi;
-                const size_t ob = row_ok ? static_cast<size_t>(cs + t) * vtok_stride + static_cast<size_t>(h) * dv + 64 * wg
-                                         : 0;
-#pragma unroll
-                for (int c16 = 0; c16 < 64; c16 += 16) {
-                    float a[16];
-                    tc::tmem_ld16(oaddr + c16, a);
-                    tc::tmem_wait_ld();
-                    if (row_ok) {
-                        if (p.out_f32) {
-                            float* op = reinterpret_cast<float*>(p.out) + ob + c16;
-#pragma unroll
-                            for (int j = 0; j < 16; j += 4)
-                                *reinterpret_cast<float4*>(op + j) = make_float4(a[j], a[j + 1], a[j + 2], a[j + 3]);
-                        } else {
-                            uint16_t* op = reinterpret_cast<uint16_t*>(p.out) + ob + c16;
-#pragma unroll
-                            for (int j = 0; j < 16; j += 8) {
-                                uint4 w;
-                                w.x = f32x2_to_bf16x2_bits(a[j], a[j + 1]);
-                                w.y = f32x2_to_bf16x2_bits(a[j + 2], a[j + 3]);
-                                w.z = f32x2_to_bf16x2_bits(a[j + 4], a[j + 5]);
-                                w.w = f32x2_to_bf16x2_bits(a[j + 6], a[j + 7]);
-                                *reinterpret_cast<uint4*>(op + j) = w;
-                            }
-                        }
-                    }
-                }
-            }
-        }
+        if (tid == LD) probe(c + 2);
         if (!cta_wait(&mb[KB_MMA], ph_mma & 1, false)) { ok = false; break; }
         ++ph_mma;
-        if (tid == 0) {
-            tc::mbar_arrive(&mb[KB_CONS + s]);           // slot s is consumed
-            probe(c + 3);
-        }
+        if (tid == LD) tc::mbar_arrive(&mb[KB_CONS + s]);   // slot s is consumed
         {
             float r[64];
             tmem_ld64(lane_base + TM_D3 + cb, r);
@@ -968,6 +968,8 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
             }
         }
     }
+    // the last chunk's O
+    if (ok && nchunks > 0 && d >= 64 && col_ok) o_epilogue(nchunks - 1);
     // O tiles must stay until their stores have read them; the MMAs thread 0 issued
     // (possibly a V part of a chunk the loop never reached) must finish before TMEM is freed
     if (d == O_ISSUER) tc::bulk_wait_all();
@@ -975,7 +977,7 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
         tc::mma_commit(&mb[KB_MMA]);
         tc::mbar_wait_bounded(&mb[KB_MMA], ph_mma & 1, kWaitLimitNs);
     }
-    if (tid == 0) {
+    if (tid == LD) {
         // loads still in flight must land before this CTA's shared memory goes away
         for (int j = waited; j < issued; ++j)
             tc::mbar_wait_bounded(&mb[KB_FULL + (j & 1)], static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs);
@@ -994,7 +996,8 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
         for (int j = 0; j < 64; j += 4)
             *reinterpret_cast<float4*>(fp + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
-    if ((!ok || !load_ok) && d == 0) set_status(p.status, kStatusTimeout);
+    if (!ok && d == 0) set_status(p.status, kStatusTimeout);
+    if (tid == LD && !load_ok) set_status(p.status, kStatusTimeout);
     cta_sync_tc();
     if (warp == 0) tc::tmem_dealloc(tm, TM_CHAIN_COLS);
 }
