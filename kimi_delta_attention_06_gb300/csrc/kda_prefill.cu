@@ -111,22 +111,26 @@ constexpr uint32_t K_S = 2 * H_STRIDE;               // S f16, 128 rows (channel
 // (U, 64 tokens x 128 N f16 MN-major, reuses the V tile of its slot once [T; Mqk] V is done)
 constexpr uint32_t K_O = K_S + 32768;                // O bf16 staging, 64 tokens x 64 columns per warpgroup (2 x 8 KB)
 constexpr uint32_t K_BAR = K_O + 16384;              // mbarriers (indices below)
-constexpr int KB_MMA = 0;      // [1] MMA completion (index 1 unused)
+constexpr int KB_MMA = 0;      // [1] MMA completion (thread 0's MMAs)
+constexpr int KB_VP = 1;       // [1] completion of a V part issued by the loader thread
 constexpr int KB_FULL = 2;     // [2] slot loaded
 constexpr int KB_CONS = 4;     // [2] slot consumed
 constexpr int KB_READY = 6;    // [6] ring entry stored by its prep CTA
 constexpr int KB_COUNT = 12;
 constexpr uint32_t K_TMEM = K_BAR + 8 * KB_COUNT;
 constexpr uint32_t K_RING = K_TMEM + 8;              // index of the hand-off ring this cluster uses
-constexpr uint32_t K_END = K_TMEM + 16;               // (TMEM address, ring index)
+constexpr uint32_t K_VFLAG = K_TMEM + 12;            // 1 + the chunk whose V part the loader issued
+constexpr uint32_t K_END = K_TMEM + 16;               // (TMEM address, ring index, V-part flag)
 
 constexpr uint32_t SMEM_BYTES = (P_END > K_END ? P_END : K_END) + 1024;   // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // TMEM columns.
 constexpr uint32_t TM_G1 = 0, TM_W = 128, TM_PREP_COLS = 256;    // prep CTA
-// chain CTA: [U; O] of chunk c in TM_D1[c % 2], so the next chunk's V part can start early
-constexpr uint32_t TM_D1A = 0, TM_D3 = 128, TM_D1B = 256, TM_CHAIN_COLS = 512;
+// chain CTA: [U; O] of chunk c in accumulator c % 3, so the next chunk's V part can start
+// while the previous chunk's O is still being read out
+constexpr uint32_t TM_D3 = 128, TM_CHAIN_COLS = 512;
+__device__ __forceinline__ uint32_t tm_d1(int j) { const int r = j % 3; return r == 0 ? 0u : (r == 1 ? 256u : 384u); }
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMaxExp2 = 126.f;      // |x| bound for ex2(x) to stay a normal fp32 number
@@ -456,12 +460,16 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
 #pragma unroll
             for (int i = 0; i < 8; ++i) g4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        // V: load j of a warp covers tokens 8 warp + 2 j + {0, 1}, each row read by 16 lanes
+        // (8 columns apiece), so every load is conflict-free
+        const int cv = 8 * (lane & 15);
         {
-            const int tv = tid >> 2, cv = 32 * (tid & 3);
-            const bool vok = tv >= lo && tv < hi && cv < dv;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                v4[j] = vok ? *reinterpret_cast<const uint4*>(sm + ST_V + (tv * dv + cv + 8 * j) * 2) : make_uint4(0u, 0u, 0u, 0u);
+            for (int j = 0; j < 4; ++j) {
+                const int tv = 8 * warp + 2 * j + (lane >> 4);
+                const bool vok = tv >= lo && tv < hi && cv < dv;
+                v4[j] = vok ? *reinterpret_cast<const uint4*>(sm + ST_V + (tv * dv + cv) * 2) : make_uint4(0u, 0u, 0u, 0u);
+            }
         }
         // -- 1a. cumulative log-decay inside each 8-token group --
         {
@@ -494,14 +502,14 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             bool out_of_range = !(fabsf(gr.x * kLog2e) < kMaxExp2) || !(fabsf(gr.y * kLog2e) < kMaxExp2) ||
                                 !(fabsf(gr.z * kLog2e) < kMaxExp2) || !(fabsf(gr.w * kLog2e) < kMaxExp2);
             if (tg == 0) *reinterpret_cast<float4*>(s_egc_out + 4 * cg) = egc;
-            {   // V as an fp16 MN-major tile: thread -> (token tid / 4, columns 32 (tid % 4) .. +31)
-                const int tv = tid >> 2, cv = 32 * (tid & 3);
+            {   // V as an fp16 MN-major tile (same token / column mapping as its staging load)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
+                    const int tv = 8 * warp + 2 * j + (lane >> 4);
                     const float2 a0 = bf16x2_bits_to_f32(v4[j].x), a1 = bf16x2_bits_to_f32(v4[j].y);
                     const float2 a2 = bf16x2_bits_to_f32(v4[j].z), a3 = bf16x2_bits_to_f32(v4[j].w);
                     const float x8[8] = {a0.x, a0.y, a1.x, a1.y, a2.x, a2.y, a3.x, a3.y};
-                    st_h8(OUT + H_V, tv, cv + 8 * j, 64, x8);
+                    if (cv < dv) st_h8(OUT + H_V, tv, cv, 64, x8);
                 }
             }
 #pragma unroll
@@ -656,7 +664,19 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             const int t = tid >> 2, c0 = (tid & 3) * 16;
             float tb[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) tb[i] = __half2float(Th[t * LH + c0 + i]) * s_beta[c0 + i];
+            for (int q = 0; q < 2; ++q) {
+                const uint4 w = *reinterpret_cast<const uint4*>(Th + t * LH + c0 + 8 * q);
+                const float4 b0 = *reinterpret_cast<const float4*>(s_beta + c0 + 8 * q);
+                const float4 b1 = *reinterpret_cast<const float4*>(s_beta + c0 + 8 * q + 4);
+                const float2 h0 = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+                const float2 h1 = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+                const float2 h2 = __half22float2(*reinterpret_cast<const __half2*>(&w.z));
+                const float2 h3 = __half22float2(*reinterpret_cast<const __half2*>(&w.w));
+                tb[8 * q + 0] = h0.x * b0.x; tb[8 * q + 1] = h0.y * b0.y;
+                tb[8 * q + 2] = h1.x * b0.z; tb[8 * q + 3] = h1.y * b0.w;
+                tb[8 * q + 4] = h2.x * b1.x; tb[8 * q + 5] = h2.y * b1.y;
+                tb[8 * q + 6] = h3.x * b1.z; tb[8 * q + 7] = h3.y * b1.w;
+            }
             st_h8(Qt, t, c0, 128, tb);
             st_h8(Qt, t, c0 + 8, 128, tb + 8);
         }
@@ -827,14 +847,17 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
     uint32_t ph_mma = 0;
     bool ok = true;
     int waited = 0;                           // chunks whose slot the CTA has waited for
-    int v_issued = 0;                         // chunks whose V part ([T; Mqk] V) is issued (thread 0)
+    volatile int* s_vflag = reinterpret_cast<volatile int*>(sm + K_VFLAG);
+    if (tid == 0) *s_vflag = 0;               // (published by the first slot wait's barrier)
+    uint32_t vp_seen = 0;                     // thread 0: loader V parts waited for
+    bool vp_ok = true;                        // thread 0: those waits all completed
+    uint32_t vp_done = 0;                     // loader: V parts issued and committed
     const int Nmma = dv;                      // 64 or 128 value columns per MMA
     // [U; O] = [T; Mqk] V for chunk j, into TM_D1[j % 2]
     auto issue_vpart = [&](int j) {
         const uint8_t* sl = sm + K_SLOT + (j & 1) * H_STRIDE;
-        issue_mma<true>(tm + ((j & 1) ? TM_D1B : TM_D1A), 128, Nmma, C, tc::smem_u32(sl + H_QT), false, 128,
+        issue_mma<true>(tm + tm_d1(j), 128, Nmma, C, tc::smem_u32(sl + H_QT), false, 128,
                         tc::smem_u32(sl + H_V), true, 64u * 128u);
-        v_issued = j + 1;
     };
     // S as the fp16 B operand of the next chunk's MMA (each thread: its row, its columns);
     // the barrier of the next slot wait publishes it
@@ -843,14 +866,14 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
         for (int j = 0; j < 64; j += 8) st_h8(Sb, d, 64 * wg + j, 128, S + j);
         tc::fence_smem_to_async();
     };
-    // O of chunk j (TMEM lanes 64..127 of TM_D1[j % 2]), by the 128 O-row threads.  It runs
-    // one chunk late, inside the next chunk's first-MMA window, where those threads would
-    // otherwise wait: the accumulator stays intact until chunk j + 2's V part, which is
-    // issued only after the barrier that follows this epilogue.
+    // O of chunk j (TMEM lanes 64..127 of accumulator j % 3), by the 128 O-row threads.  It
+    // runs one chunk late, inside the next chunk's first-MMA window, where those threads
+    // would otherwise wait: that accumulator is next written by chunk j + 3's V part, issued
+    // at the earliest in chunk j + 2's first-MMA window, after this epilogue's barriers.
     auto o_epilogue = [&](int j) {
         const int t = d - 64;
         const int cs = g.row0(j), lo = g.lo(j), hi = g.hi(j);
-        const uint32_t oaddr = lane_base + ((j & 1) ? TM_D1B : TM_D1A) + cb;
+        const uint32_t oaddr = lane_base + tm_d1(j) + cb;
         if (!p.out_f32 && lo == 0 && hi == C) {
             // staged as a 128B-swizzled bf16 tile per warpgroup, written out by one TMA store
             float a[64];
@@ -907,7 +930,7 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
     for (int c = 0; c < nchunks; ++c) {
         const int s = c & 1;
         uint8_t* slot = sm + K_SLOT + s * H_STRIDE;
-        const uint32_t d1 = (s ? TM_D1B : TM_D1A);
+        const uint32_t d1 = tm_d1(c);
         if (tid == LD && issued == c && load_ok) load_ok = load(c, true);
         if (!cta_wait(&mb[KB_FULL + s], (c >> 1) & 1, false)) { ok = false; break; }
         waited = c + 1;
@@ -915,16 +938,32 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
             // the ring entry is free again: its prep CTA may store chunk c + 6 there
             if (c + WS_SLOTS < nchunks)
                 tc::mbar_arrive_remote_relaxed(tc::mapa(prep_free + 8u * ((c / NPREP_CTAS) & 1), 1 + c % NPREP_CTAS));
-            if (v_issued == c) issue_vpart(c);
+            if (*s_vflag == c + 1) {           // the loader issued this V part: it has to be complete
+                vp_ok = tc::mbar_wait_bounded(&mb[KB_VP], vp_seen & 1u, kWaitLimitNs) != 0;
+                ++vp_seen;
+            } else {
+                issue_vpart(c);
+            }
             // -- [U; O] = [T; Mqk] V + [-W; Q'] S  (one accumulator) --
             issue_mma<true>(tm + d1, 128, Nmma, DK, tc::smem_u32(slot + H_AH), false, 128,
                             tc::smem_u32(Sb), true, 128u * 128u, true);
             tc::mma_commit(&mb[KB_MMA]);
         }
-        if (tid == LD) probe(c + 2);
+        if (tid == LD) {
+            probe(c + 2);
+            // the next chunk's V part, if its slot has landed, runs behind this MMA; issuing it
+            // here, while the MMA executes, keeps its issue time out of every barrier window
+            if (c + 1 < nchunks && tc::mbar_test_wait(&mb[KB_FULL + (s ^ 1)], ((c + 1) >> 1) & 1)) {
+                issue_vpart(c + 1);
+                tc::mma_commit(&mb[KB_VP]);
+                ++vp_done;
+                *s_vflag = c + 2;
+            }
+        }
         if (d >= 64 && col_ok && c > 0) o_epilogue(c - 1);   // the previous chunk's O, while this MMA runs
         const float gc = reinterpret_cast<const float*>(slot + H_EGC)[d];
-        if (!cta_wait(&mb[KB_MMA], ph_mma & 1, false)) { ok = false; break; }
+        // (thread 0's V-part wait joins the agreement here, so every thread leaves together)
+        if (!cta_wait(&mb[KB_MMA], ph_mma & 1, false, vp_ok)) { ok = false; break; }
         ++ph_mma;
         if (d < 64 && col_ok) {   // U -> MN-major f16 tile, over the (now dead) V tile of the slot
             float r[64];
@@ -940,8 +979,6 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
             issue_mma<true>(tm + TM_D3, 128, Nmma, C, tc::smem_u32(slot + H_KH), true, 64u * 128u,
                             tc::smem_u32(slot + H_V), true, 64u * 128u);
             tc::mma_commit(&mb[KB_MMA]);
-            // the next chunk's V part can run now if its slot has landed
-            if (c + 1 < nchunks && tc::mbar_test_wait(&mb[KB_FULL + (s ^ 1)], ((c + 1) >> 1) & 1)) issue_vpart(c + 1);
         }
         if (tid == LD) probe(c + 2);
         if (!cta_wait(&mb[KB_MMA], ph_mma & 1, false)) { ok = false; break; }
@@ -977,6 +1014,8 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
         tc::mma_commit(&mb[KB_MMA]);
         tc::mbar_wait_bounded(&mb[KB_MMA], ph_mma & 1, kWaitLimitNs);
     }
+    if (tid == LD && vp_done > 0)             // its last V part must finish before TMEM is freed
+        tc::mbar_wait_bounded(&mb[KB_VP], (vp_done - 1) & 1u, kWaitLimitNs);
     if (tid == LD) {
         // loads still in flight must land before this CTA's shared memory goes away
         for (int j = waited; j < issued; ++j)
