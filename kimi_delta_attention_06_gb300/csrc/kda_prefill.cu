@@ -92,6 +92,11 @@ constexpr uint32_t ST_LA = P_A1;             // log_alpha f32 [64][dk] (per-head
 constexpr uint32_t ST_Q = P_A1 + 32768;      // q bf16 [64][dk]
 constexpr uint32_t ST_K = P_A1 + 49152;      // k bf16 [64][dk]
 constexpr uint32_t ST_V = P_B1;              // v bf16 [64][dv]
+// Scalar-decay layouts (one log-decay per head and token, or none): q and k are staged by TMA
+// straight into the tcgen05 operand layout [K; Q] (bf16, K-major, 128B swizzle, slabs of 64
+// channels, 128 rows per slab: k rows 0..63, q rows 64..127), the G1 operand itself.
+constexpr uint32_t ST_KQ = P_A1;             // [K; Q] bf16, 128 rows x dk                (32 KB)
+constexpr uint32_t ST_LAH = P_A1 + 32768;    // log_alpha rows [64][4 heads] f32 around head h (1 KB)
 constexpr uint32_t P_OUT = 98304;            // hand-off block                             (65 KB)
 constexpr uint32_t P_P = P_OUT + H_STRIDE;   // A f16, 64 rows x 64 K, K-major             (8 KB)
 constexpr uint32_t P_BETA = P_P + 8192;      // beta [64] f32
@@ -141,7 +146,8 @@ enum : int { DECAY_CHANNEL = 0, DECAY_HEAD = 1, DECAY_NONE = 2 };
 
 struct TensorMaps {
     CUtensorMap q, k, la, v;     // 2-D views [tokens, H * D]; box = one head x 64 tokens
-                                 // (per-head decay: la is [tokens, H], box = 4 heads x 64 tokens)
+                                 // (per-head decay: la is [tokens, H], box = 4 heads x 64 tokens;
+                                 // scalar-decay layouts: q, k boxes of 64 channels, 128B swizzle)
     CUtensorMap o;               // bf16 output [tokens, H * Dv]; box = 64 columns x 64 tokens, 128B swizzle
 };
 
@@ -205,9 +211,10 @@ __device__ __forceinline__ void cta_sync_tc() {
 template <bool F16>
 __device__ __forceinline__ void issue_mma(uint32_t d_tmem, int M, int N, int K,
                                           uint32_t a_base, bool a_mn, uint32_t a_p,
-                                          uint32_t b_base, bool b_mn, uint32_t b_p, bool acc = false) {
+                                          uint32_t b_base, bool b_mn, uint32_t b_p, bool acc = false,
+                                          bool bf16 = false) {
     constexpr uint32_t esz = F16 ? 2u : 4u, kstep = 32u / esz, eps = 128u / esz;
-    const uint32_t id = tc::idesc(M, N, F16 ? tc::kFmtF16 : tc::kFmtTF32, a_mn, b_mn);
+    const uint32_t id = tc::idesc(M, N, F16 ? (bf16 ? tc::kFmtBF16 : tc::kFmtF16) : tc::kFmtTF32, a_mn, b_mn);
     for (uint32_t s = 0; s < static_cast<uint32_t>(K) / kstep; ++s) {
         const uint32_t k0 = kstep * s;
         const uint64_t da = a_mn ? tc::sdesc(a_base + k0 * 128u, a_p, 1024, tc::kSwizzle128B)
@@ -333,10 +340,17 @@ __device__ __forceinline__ void issue_input_tma(const TensorMaps& tmaps, const P
     const uint32_t la_bytes = DECAY == DECAY_CHANNEL ? C * p.dk * 4 : DECAY == DECAY_HEAD ? C * 4 * 4 : 0;
     const uint32_t bytes = static_cast<uint32_t>(C * p.dk * (2 + 2) + C * p.dv * 2) + la_bytes;
     tc::mbar_arrive_expect_tx(bar, bytes);
-    if (DECAY == DECAY_CHANNEL) tc::tma_load_2d(tc::smem_u32(sm + ST_LA), &tmaps.la, h * p.dk, y, bar);
-    else if (DECAY == DECAY_HEAD) tc::tma_load_2d(tc::smem_u32(sm + ST_LA), &tmaps.la, h & ~3, y, bar);
-    tc::tma_load_2d(tc::smem_u32(sm + ST_Q), &tmaps.q, h * p.dk, y, bar);
-    tc::tma_load_2d(tc::smem_u32(sm + ST_K), &tmaps.k, h * p.dk, y, bar);
+    if (DECAY == DECAY_CHANNEL) {
+        tc::tma_load_2d(tc::smem_u32(sm + ST_LA), &tmaps.la, h * p.dk, y, bar);
+        tc::tma_load_2d(tc::smem_u32(sm + ST_Q), &tmaps.q, h * p.dk, y, bar);
+        tc::tma_load_2d(tc::smem_u32(sm + ST_K), &tmaps.k, h * p.dk, y, bar);
+    } else {
+        if (DECAY == DECAY_HEAD) tc::tma_load_2d(tc::smem_u32(sm + ST_LAH), &tmaps.la, h & ~3, y, bar);
+        for (int sl = 0; sl < p.dk / 64; ++sl) {       // 64-channel boxes, 128B-swizzled
+            tc::tma_load_2d(tc::smem_u32(sm + ST_KQ + sl * 16384), &tmaps.k, h * p.dk + 64 * sl, y, bar);
+            tc::tma_load_2d(tc::smem_u32(sm + ST_KQ + sl * 16384 + 8192), &tmaps.q, h * p.dk + 64 * sl, y, bar);
+        }
+    }
     tc::tma_load_2d(tc::smem_u32(sm + ST_V), &tmaps.v, h * p.dv, y, bar);
 }
 
@@ -349,8 +363,11 @@ __device__ __forceinline__ void prefetch_inputs(const TensorMaps& tmaps, const P
     const int y = max(0, g.row0(c));
     if (DECAY == DECAY_CHANNEL) tc::tma_prefetch_2d(&tmaps.la, h * p.dk, y);
     else if (DECAY == DECAY_HEAD) tc::tma_prefetch_2d(&tmaps.la, h & ~3, y);
-    tc::tma_prefetch_2d(&tmaps.q, h * p.dk, y);
-    tc::tma_prefetch_2d(&tmaps.k, h * p.dk, y);
+    const int qk_box = DECAY == DECAY_CHANNEL ? p.dk : 64;
+    for (int x = 0; x < p.dk; x += qk_box) {
+        tc::tma_prefetch_2d(&tmaps.q, h * p.dk + x, y);
+        tc::tma_prefetch_2d(&tmaps.k, h * p.dk + x, y);
+    }
     tc::tma_prefetch_2d(&tmaps.v, h * p.dv, y);
 }
 
@@ -428,6 +445,7 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
     for (int c = pr; c < nchunks; c += NPREP_CTAS, ++kk) {
         const int lo = g.lo(c), hi = g.hi(c);          // the sequence's rows of this chunk
 
+        if constexpr (DECAY == DECAY_CHANNEL) {
         // -- 0. inputs of this chunk: staging (TMA) -> registers --
         if (tid == 0 && c + 2 * NPREP_CTAS < nchunks) prefetch_inputs<DECAY>(tmaps, p, c + 2 * NPREP_CTAS, g, h);
         if (!cta_wait(&mb[3], kk & 1, false)) { ok = false; break; }
@@ -533,6 +551,71 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             }
             if (__any_sync(0xffffffffu, out_of_range) && lane == 0) set_status(p.status, kStatusRange);
         }
+        } else {
+        // -- 0/1 (scalar decay). the token log-decay prefix, one exponential per token, and
+        //    the fp16 tiles; q and k stay in the staging tile, which is G1's operand --
+        if (tid == 0 && c + 2 * NPREP_CTAS < nchunks) prefetch_inputs<DECAY>(tmaps, p, c + 2 * NPREP_CTAS, g, h);
+        if (!cta_wait(&mb[3], kk & 1, false)) { ok = false; break; }
+        const int cv = 8 * (lane & 15);
+        uint4 v4[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int tv = 8 * warp + 2 * j + (lane >> 4);
+            const bool vok = tv >= lo && tv < hi && cv < dv;
+            v4[j] = vok ? *reinterpret_cast<const uint4*>(sm + ST_V + (tv * dv + cv) * 2) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (warp == 0) {            // g_t, t = 2 lane, 2 lane + 1: inclusive prefix over the chunk
+            float a0 = 0.f, a1 = 0.f;
+            if (DECAY == DECAY_HEAD) {
+                const int t0 = 2 * lane;
+                if (t0 >= lo && t0 < hi) a0 = *reinterpret_cast<const float*>(sm + ST_LAH + (t0 * 4 + (h & 3)) * 4);
+                if (t0 + 1 >= lo && t0 + 1 < hi)
+                    a1 = *reinterpret_cast<const float*>(sm + ST_LAH + ((t0 + 1) * 4 + (h & 3)) * 4);
+            }
+            float x = a0 + a1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            s_tot[2 * lane] = x - a1;
+            s_tot[2 * lane + 1] = x;
+        }
+        // the stores of the previous block must have read it before it is rewritten
+        if (pending >= 0 && tid == ST_THREAD) tc::bulk_wait_read_all();
+        tc::named_sync(BAR_ALL, NT);     // prefix visible; staging of v read; block free
+        {
+            const float gC = s_tot[63];
+            if (tid < 32) {
+                const float e = ex2(gC * kLog2e);
+                *reinterpret_cast<float4*>(s_egc_out + 4 * tid) = make_float4(e, e, e, e);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int tv = 8 * warp + 2 * j + (lane >> 4);
+                const float2 a0 = bf16x2_bits_to_f32(v4[j].x), a1 = bf16x2_bits_to_f32(v4[j].y);
+                const float2 a2 = bf16x2_bits_to_f32(v4[j].z), a3 = bf16x2_bits_to_f32(v4[j].w);
+                const float x8[8] = {a0.x, a0.y, a1.x, a1.y, a2.x, a2.y, a3.x, a3.y};
+                if (cv < dv) st_h8(OUT + H_V, tv, cv, 64, x8);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int t = 8 * tg + i;
+                const bool ok_t = t >= lo && t < hi && ch_ok;
+                const float gt = s_tot[t];
+                const float et = ex2(gt * kLog2e), ect = ex2((gC - gt) * kLog2e);   // both <= 1
+                const uint2 kr = ok_t ? *reinterpret_cast<const uint2*>(sm + ST_KQ + tc::sw128_off16(t, 4 * cg, 128))
+                                      : make_uint2(0u, 0u);
+                const uint2 qr = ok_t ? *reinterpret_cast<const uint2*>(sm + ST_KQ + tc::sw128_off16(64 + t, 4 * cg, 128))
+                                      : make_uint2(0u, 0u);
+                const float4 kv = bf16x4_to_f4(kr), qv = bf16x4_to_f4(qr);
+                const float4 e4 = make_float4(et, et, et, et), c4 = make_float4(ect, ect, ect, ect);
+                st_h4(AH, t, 4 * cg, 128, f4mul(kv, e4));        // K~ = k e^{g_t}
+                st_h4(AH, 64 + t, 4 * cg, 128, f4mul(qv, e4));   // Q~ = q e^{g_t}
+                st_h4(KH, t, 4 * cg, 64, f4mul(kv, c4));         // K^ = k e^{g_C - g_t}
+            }
+        }
+        }
         if (beta_thread) s_beta[tid - 128] = bf16_bits_to_f32(bt);
         tc::fence_smem_to_async();
         cta_sync_tc();
@@ -543,7 +626,11 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         uint8_t* entry = ring + static_cast<size_t>(c % WS_SLOTS) * H_STRIDE;
         bool ring_ok = true;
         if (tid == 0) {
-            issue_mma<false>(tm + TM_G1, 128, 64, DK, tc::smem_u32(A1), false, 128, tc::smem_u32(B1), false, 64);
+            if constexpr (DECAY == DECAY_CHANNEL)
+                issue_mma<false>(tm + TM_G1, 128, 64, DK, tc::smem_u32(A1), false, 128, tc::smem_u32(B1), false, 64);
+            else   // [K; Q] K^T in bf16, straight from the staged inputs (k rows 0..63 are the B operand)
+                issue_mma<true>(tm + TM_G1, 128, 64, dk, tc::smem_u32(sm + ST_KQ), false, 128, tc::smem_u32(sm + ST_KQ),
+                                false, 128, false, true);
             tc::mma_commit(&mb[0]);
         }
         // the previous block's stores have long completed: hand it to the chain (the
@@ -564,7 +651,42 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             }
         }
 
-        // -- 3. L (rows 0..63 -> fp32 scratch), A (rows 64..127 -> f16 tile) --
+        // -- 3. L (rows 0..63 -> fp16 scratch), A (rows 64..127 -> f16 tile) --
+        if constexpr (DECAY != DECAY_CHANNEL) {
+            // scalar decay: G1 holds the plain products, so each pair takes its decay factor
+            // exp(g_t - g_s) <= 1 here, and pairs outside the sequence's rows are masked
+            const int r = (warp & 3) * 32 + lane;
+            const int c0 = (warp >> 2) * 32;
+            const int t = r & 63;
+            float v[32];
+            tmem_ld32(lane_base + TM_G1 + c0, v);
+            const float gt = s_tot[t];
+            const bool row_in = t >= lo && t < hi;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int sc = c0 + i;
+                const bool keep = row_in && sc >= lo && sc < hi && (r < 64 ? sc < t : sc <= t);
+                float f = keep ? 1.f : 0.f;
+                if (DECAY == DECAY_HEAD && keep) f = ex2((gt - s_tot[sc]) * kLog2e);
+                v[i] *= f;
+            }
+            if (r < 64) {
+                const float b = s_beta[r];
+                __half* Lr = Lh + r * LH + c0;
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) {
+                    uint4 w;
+                    w.x = f16x2_bits(b * v[i + 0], b * v[i + 1]);
+                    w.y = f16x2_bits(b * v[i + 2], b * v[i + 3]);
+                    w.z = f16x2_bits(b * v[i + 4], b * v[i + 5]);
+                    w.w = f16x2_bits(b * v[i + 6], b * v[i + 7]);
+                    *reinterpret_cast<uint4*>(Lr + i) = w;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) st_h8(P, t, c0 + i, 64, v + i);
+            }
+        } else
         {
             const int r = (warp & 3) * 32 + lane;
             const int c0 = (warp >> 2) * 32;                 // warps 0-3: cols 0..31, 4-7: 32..63
@@ -1190,8 +1312,13 @@ int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
     }
     TensorMaps tmaps;
     if (total_tokens > 0) {
-        if (!make_map(&tmaps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, total_tokens, static_cast<long long>(H) * Dk, Dk) ||
-            !make_map(&tmaps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, total_tokens, static_cast<long long>(H) * Dk, Dk) ||
+        // q, k: one head per box (per-channel decay), or 64-channel boxes in the 128B-swizzled operand
+        // layout (scalar decay layouts, whose G1 reads the staged inputs directly)
+        const bool swz = decay != DECAY_CHANNEL;
+        const int qk_box = swz ? 64 : Dk;
+        const CUtensorMapSwizzle qk_swz = swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+        if (!make_map(&tmaps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, total_tokens, static_cast<long long>(H) * Dk, qk_box, qk_swz) ||
+            !make_map(&tmaps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, total_tokens, static_cast<long long>(H) * Dk, qk_box, qk_swz) ||
             !make_map(&tmaps.v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, total_tokens, static_cast<long long>(H) * Dv, Dv))
             return -3;
         memset(&tmaps.la, 0, sizeof(tmaps.la));

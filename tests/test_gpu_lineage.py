@@ -3,8 +3,11 @@ log-decay per head and token) and DeltaNet (no decay), for the prefill
 (kda_chunk_prefill_ex) and the serving decode (kda_decode_multi).
 
 Each layout is checked against the oracle, which takes the decay broadcast to every
-channel (or zero), and bit for bit against the per-channel kernels fed that same
-broadcast: the specialisations change where the decay comes from, not the arithmetic."""
+channel (or zero).  The prefill's scalar layouts have arithmetic of their own (the
+intra-chunk products in bf16 straight from the staged inputs, the decay applied per
+token pair), so they are compared with the oracle, and with the per-channel kernel fed
+the broadcast decay only within the parity bounds.  The decode's layouts change where the
+decay comes from, not the arithmetic, so they match the per-channel decode bit for bit."""
 import pytest
 import torch
 
@@ -48,12 +51,41 @@ def test_prefill_layouts(D, decay):
                              ckpt_stride=128, out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert kda.kda_device_status() == kda.KDA_OK
-    assert torch.equal(o1, o0) and torch.equal(f1, f0) and torch.equal(c1, c0)
     ro, rf, rc = oracle.prefill(case.q, case.k, case.v, la_full, case.beta, case.cu_seqlens, case.init_state,
                                 ckpt_stride=128)
-    P.check_out(o1, ro, torch.float32)
-    P.check_state(f1, rf)
-    P.check_state(c1, rc)
+    for o, f, c in ((o1, f1, c1), (o0, f0, c0)):
+        P.check_out(o, ro, torch.float32)
+        P.check_state(f, rf)
+        P.check_state(c, rc)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("decay", [kda.KDA_DECAY_HEAD, kda.KDA_DECAY_NONE])
+def test_prefill_layouts_prefix_continuations(D, decay):
+    """Sequences that start mid-chunk (prefix continuations) and end mid-chunk: the staged
+    q, k tiles then hold neighbouring sequences' tokens, which the scalar layouts' G1 must
+    mask out.  Checked against the oracle with start positions."""
+    lens = [200, 1, 130, 23, 256, 300]
+    start = [0, 40, 63, 1000, 64, 7]
+    stride = 128
+    case = workloads.prefill_case(lens, H=4, D=D, seed=140 + D + decay, ckpt_stride=stride)
+    T, H = case.T, case.H
+    if decay == kda.KDA_DECAY_HEAD:
+        la_small = _head_decay(T, H, seed=9 + D)
+        la_full = la_small[:, :, None].expand(T, H, D).contiguous()
+    else:
+        la_small, la_full = None, torch.zeros(T, H, D)
+    dev = lambda x: None if x is None else x.to(DEV)
+    o, f, c = kda.prefill(dev(case.q), dev(case.k), dev(case.v), dev(la_small), dev(case.beta), case.cu_seqlens,
+                          init_state=dev(case.init_state), ckpt_stride=stride, out_dtype=torch.float32, decay=decay,
+                          start_pos_host=torch.tensor(start, dtype=torch.int32))
+    torch.cuda.synchronize()
+    assert kda.kda_device_status() == kda.KDA_OK
+    ro, rf, rc = oracle.prefill(case.q, case.k, case.v, la_full, case.beta, case.cu_seqlens, case.init_state,
+                                ckpt_stride=stride, start_pos=start)
+    P.check_out(o, ro, torch.float32)
+    P.check_state(f, rf)
+    P.check_state(c, rc)
 
 
 @pytest.mark.parametrize("decay", [kda.KDA_DECAY_HEAD, kda.KDA_DECAY_NONE])
