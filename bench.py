@@ -214,6 +214,62 @@ def time_oracle(budget_s=12.0):
             "decode_gbs": dec_gbs, "prefill_seconds": dt}
 
 
+def time_module_path(dev, stream, rank, steps=10):
+    """The KDA module around the recurrence at T=145408, H=32, D=128, timed on the device:
+    kda_prepare_inputs (short conv + SiLU, L2 norm of q and k, alpha and beta gates) then
+    kda_chunk_prefill_ex with the per-head output norm fused into its output epilogue: two
+    launches per step.  The three-pass form (prepare, prefill, kda_output_norm) is timed
+    beside it; both write the same normed bf16 output."""
+    import torch
+    from kimi_delta_attention_06_gb300 import kda, workloads
+    m = workloads.module_case(T_PROMPT, H=H, D=D, seed=rank_seed(5, rank), device=dev)
+    cu = m.cu_seqlens.to(dev)
+    q, k, v = (torch.empty(T_PROMPT, H, D, device=dev, dtype=torch.bfloat16) for _ in range(3))
+    la = torch.empty(T_PROMPT, H, D, device=dev)
+    beta = torch.empty(T_PROMPT, H, device=dev, dtype=torch.bfloat16)
+    s0 = torch.zeros(1, H, D, D, device=dev)
+    o = torch.empty(T_PROMPT, H, D, device=dev, dtype=torch.bfloat16)
+    y = torch.empty_like(o)
+    fin = torch.empty(1, H, D, D, device=dev)
+
+    def prepare():
+        kda.kda_prepare_inputs(m.xq, m.xk, m.xv, m.conv_w, None, m.a_raw, m.b_raw, cu, m.cu_seqlens, 1, T_PROMPT,
+                               H, D, 1, q, k, v, la, beta, stream)
+
+    def prefill(norm):
+        kda.kda_chunk_prefill_ex(q, k, v, la, beta, s0, cu, m.cu_seqlens, 1, T_PROMPT, H, D, D, y if norm else o,
+                                 kda.KDA_OUT_BF16, fin, None, 0, kda.KDA_DECAY_CHANNEL,
+                                 out_norm_gamma=m.gamma if norm else None, out_norm_eps=1e-6, stream=stream)
+
+    def norm():
+        kda.kda_output_norm(o, kda.KDA_OUT_BF16, m.gamma, 1e-6, y, T_PROMPT, H, D, stream)
+
+    res = {}
+    for name, parts in (("fused", [prepare, lambda: prefill(True)]),
+                        ("separate", [prepare, lambda: prefill(False), norm])):
+        for _ in range(3):
+            for f in parts:
+                f()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(steps)]
+        torch.cuda.synchronize()
+        for i in range(steps):
+            ev[i][0].record(stream)
+            for j, f in enumerate(parts):
+                f()
+                ev[i][j + 1].record(stream)
+        torch.cuda.synchronize()
+        per = [statistics.median(e[j].elapsed_time(e[j + 1]) for e in ev) for j in range(len(parts))]
+        tot = statistics.median(e[0].elapsed_time(e[-1]) for e in ev)
+        res[name] = {"ms_per_step": tot, "launch_ms": per, "tokens_per_s": T_PROMPT / (tot / 1e3)}
+    if kda.kda_device_status() != 0:
+        raise RuntimeError("device status after the module path")
+    res["workload"] = (f"prepare (conv width 4 + SiLU, L2 norm, gates) -> prefill T={T_PROMPT} H={H} Dk=Dv={D} "
+                       f"-> per-head output norm; zero initial state, no checkpoints")
+    res["launches"] = {"fused": ["kda_prepare_inputs", "kda_chunk_prefill_ex (+norm)"],
+                       "separate": ["kda_prepare_inputs", "kda_chunk_prefill_ex", "kda_output_norm"]}
+    return res
+
+
 def bench_config(world):
     """The workload description both arms print (the reference arm times a bounded sample of it)."""
     return {"workload": f"kda prefill T={T_PROMPT} H={H} Dk=Dv={D} ckpt every {CKPT} + decode N={DEC_N} H={H} D={D}",
@@ -252,6 +308,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-module", action="store_true")
     args = ap.parse_args(argv)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -438,6 +495,8 @@ def main(argv=None):
                        "streams, and copy-out of step i-1 overlap the prefill of step i)"}
         del host, bufs, h_out, h_ck
 
+    module = None if args.no_module else time_module_path(dev, stream, rank)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = time_oracle()
@@ -463,6 +522,7 @@ def main(argv=None):
                               "state_bytes_per_prefill": kv_state_bytes(n_ck),
                               "note": "final state + checkpoints written per prefill / prefill time"},
             "clocks": clocks, "e2e": e2e, "gpu_launches": 2 * args.steps, "cpu_baseline": cpu,
+            "module": module,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

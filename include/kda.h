@@ -136,6 +136,13 @@ int kda_chunk_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  *               plus at the sequence end, so they line up with the prompt's own grid;
  *               slots per sequence: kda_ckpt_count_ex.  NULL = all 0.
  *   start_pos_host the same values on the host (non-negative), NULL iff start_pos is.
+ *   out_norm_gamma (device) fp32 [H, Dv], 16-byte aligned, or NULL.  When given, `out`
+ *               receives the module's per-head output norm of o instead of o itself (the
+ *               Kimi K3 primer, wiki summary, section 3; the same operation as
+ *               kda_output_norm, fused into the prefill's output epilogue and applied to the
+ *               fp32 accumulator before the single rounding to out_dtype):
+ *                   y[t, h, :] = o / sqrt(mean_c o[t, h, c]^2 + out_norm_eps) * gamma[h, :]
+ *   out_norm_eps   >= 0 and finite; ignored when out_norm_gamma is NULL.
  */
 int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                          const float* log_alpha, const uint16_t* beta,
@@ -145,6 +152,7 @@ int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v
                          void* out, int out_dtype,
                          float* final_state, float* ckpt_states, int ckpt_stride,
                          int decay, const int32_t* start_pos, const int32_t* start_pos_host,
+                         const float* out_norm_gamma, float out_norm_eps,
                          void* stream);
 
 /*

@@ -18,6 +18,7 @@ int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
                    const uint16_t* beta, const float* init_state, const int32_t* cu_seqlens,
                    int num_seqs, int total_tokens, int H, int Dk, int Dv, void* out, int out_f32,
                    float* final_state, float* ckpt, int ckpt_stride, int decay, const int32_t* start_pos,
+                   const float* norm_gamma, float norm_eps,
                    void* ws, int* ring_flags, int ring_count, int* status, cudaStream_t stream);
 size_t prefill_workspace_bytes(int num_seqs, int H);
 int prefill_ring_count(int num_seqs, int H);
@@ -194,10 +195,12 @@ static int prefill_pooled(const uint16_t* q, const uint16_t* k, const uint16_t* 
                           const uint16_t* beta, const float* init_state, const int32_t* cu_seqlens,
                           const int32_t* cu_seqlens_host, int num_seqs, int total_tokens, int H, int Dk, int Dv,
                           void* out, int out_dtype, float* final_state, float* ckpt_states, int ckpt_stride,
-                          int decay, const int32_t* start_pos, const int32_t* start_pos_host, void* stream) {
+                          int decay, const int32_t* start_pos, const int32_t* start_pos_host,
+                          const float* norm_gamma, float norm_eps, void* stream) {
     int rc = check_prefill_args(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host, num_seqs,
                                 total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, decay);
     if (rc != KDA_OK || num_seqs == 0) return rc;
+    if (norm_gamma && (!aligned16(norm_gamma) || !(norm_eps >= 0.f) || !(norm_eps < 3.0e38f))) return KDA_ERR_INVALID_ARG;
     if ((start_pos == nullptr) != (start_pos_host == nullptr)) return KDA_ERR_INVALID_ARG;
     if (start_pos) {
         if (reinterpret_cast<uintptr_t>(start_pos) & 3u) return KDA_ERR_INVALID_ARG;
@@ -221,7 +224,7 @@ static int prefill_pooled(const uint16_t* q, const uint16_t* k, const uint16_t* 
     int* flags = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + ring_bytes);
     rc = kda::launch_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, num_seqs, total_tokens, H, Dk, Dv,
                              out, out_dtype == KDA_OUT_F32, final_state, ckpt_states, ckpt_stride, decay,
-                             start_pos, ws, flags, rings, status, st);
+                             start_pos, norm_gamma, norm_eps, ws, flags, rings, status, st);
     const bool freed = cudaFreeAsync(ws, st) == cudaSuccess;
     return (rc == 0 && freed) ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -236,7 +239,7 @@ int kda_chunk_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                       void* stream) {
     return prefill_pooled(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host, num_seqs, total_tokens,
                           H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, KDA_DECAY_CHANNEL,
-                          nullptr, nullptr, stream);
+                          nullptr, nullptr, nullptr, 0.f, stream);
 }
 
 int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -246,10 +249,11 @@ int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v
                          int num_seqs, int total_tokens, int H, int Dk, int Dv,
                          void* out, int out_dtype,
                          float* final_state, float* ckpt_states, int ckpt_stride,
-                         int decay, const int32_t* start_pos, const int32_t* start_pos_host, void* stream) {
+                         int decay, const int32_t* start_pos, const int32_t* start_pos_host,
+                         const float* out_norm_gamma, float out_norm_eps, void* stream) {
     return prefill_pooled(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host, num_seqs, total_tokens,
                           H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, decay, start_pos,
-                          start_pos_host, stream);
+                          start_pos_host, out_norm_gamma, out_norm_eps, stream);
 }
 
 int kda_chunk_prefill_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -271,7 +275,8 @@ int kda_chunk_prefill_noalloc(const uint16_t* q, const uint16_t* k, const uint16
     if (rc != KDA_OK) return rc;
     rc = kda::launch_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, num_seqs, total_tokens, H, Dk, Dv,
                              out, out_dtype == KDA_OUT_F32, final_state, ckpt_states, ckpt_stride,
-                             KDA_DECAY_CHANNEL, nullptr, scratch, nullptr, 0, status, static_cast<cudaStream_t>(stream));
+                             KDA_DECAY_CHANNEL, nullptr, nullptr, 0.f, scratch, nullptr, 0, status,
+                             static_cast<cudaStream_t>(stream));
     return rc == 0 ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -69,6 +69,7 @@ constexpr int NT = 256;         // threads per CTA
 constexpr int NPREP_CTAS = 3;   // prep CTAs per cluster
 constexpr int CLUSTER = 1 + NPREP_CTAS;
 constexpr uint32_t BAR_ALL = 1;  // named barrier over the CTA's 256 threads
+constexpr uint32_t BAR_NORM = 4; // chain CTA: named barrier of the O-row threads of both warpgroups
 constexpr int ST_THREAD = 32;    // prep CTA: issues the ring stores and publishes them (not the MMA issuer)
 
 // Hand-off block: produced in a prep CTA, copied verbatim through the global ring into a chain slot.
@@ -125,7 +126,9 @@ constexpr int KB_COUNT = 12;
 constexpr uint32_t K_TMEM = K_BAR + 8 * KB_COUNT;
 constexpr uint32_t K_RING = K_TMEM + 8;              // index of the hand-off ring this cluster uses
 constexpr uint32_t K_VFLAG = K_TMEM + 12;            // 1 + the chunk whose V part the loader issued
-constexpr uint32_t K_END = K_TMEM + 16;               // (TMEM address, ring index, V-part flag)
+constexpr uint32_t K_GAM = K_TMEM + 16;              // output-norm gamma of the head [128] f32
+constexpr uint32_t K_SS = K_GAM + 512;               // output norm: row sums of squares [2][64] f32
+constexpr uint32_t K_END = K_SS + 512;
 
 constexpr uint32_t SMEM_BYTES = (P_END > K_END ? P_END : K_END) + 1024;   // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -168,6 +171,8 @@ struct Params {
     int ring_count;
     int* status;
     int out_f32;
+    const float* norm_gamma;     // per-head output norm fused into the O epilogue: gamma [H, Dv], or null
+    float norm_eps;
     int ckpt_stride;
     int H, dk, dv;
 };
@@ -970,6 +975,10 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
     bool ok = true;
     int waited = 0;                           // chunks whose slot the CTA has waited for
     volatile int* s_vflag = reinterpret_cast<volatile int*>(sm + K_VFLAG);
+    float* s_gam = reinterpret_cast<float*>(sm + K_GAM);
+    float* s_ss = reinterpret_cast<float*>(sm + K_SS);
+    if (p.norm_gamma && tid < dv) s_gam[tid] = p.norm_gamma[static_cast<size_t>(h) * dv + tid];   // (published
+                                              // by the first slot wait's barrier)
     if (tid == 0) *s_vflag = 0;               // (published by the first slot wait's barrier)
     uint32_t vp_seen = 0;                     // thread 0: loader V parts waited for
     bool vp_ok = true;                        // thread 0: those waits all completed
@@ -996,10 +1005,26 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
         const int t = d - 64;
         const int cs = g.row0(j), lo = g.lo(j), hi = g.hi(j);
         const uint32_t oaddr = lane_base + tm_d1(j) + cb;
+        float a[64];
+        tmem_ld64(oaddr, a);
+        if (p.norm_gamma) {
+            // the module's per-head output norm on the fp32 accumulator: y = o / rms(o) * gamma[h];
+            // the two warpgroups' column halves of a row meet through shared memory
+            float ss = 0.f;
+#pragma unroll
+            for (int q = 0; q < 64; ++q) ss = fmaf(a[q], a[q], ss);
+            s_ss[64 * wg + t] = ss;
+            tc::named_sync(BAR_NORM, dv == 128 ? 128 : 64);
+            const float tot = dv == 128 ? s_ss[t] + s_ss[64 + t] : s_ss[t];
+            const float rinv = 1.f / sqrtf(tot / static_cast<float>(dv) + p.norm_eps);
+#pragma unroll
+            for (int q = 0; q < 64; q += 4) {
+                const float4 gm = *reinterpret_cast<const float4*>(s_gam + 64 * wg + q);
+                a[q] *= rinv * gm.x; a[q + 1] *= rinv * gm.y; a[q + 2] *= rinv * gm.z; a[q + 3] *= rinv * gm.w;
+            }
+        }
         if (!p.out_f32 && lo == 0 && hi == C) {
             // staged as a 128B-swizzled bf16 tile per warpgroup, written out by one TMA store
-            float a[64];
-            tmem_ld64(oaddr, a);
             if (d == O_ISSUER) tc::bulk_wait_read_all();       // the previous store has read the tile
             tc::named_sync(bar_o, 64);
 #pragma unroll
@@ -1017,33 +1042,23 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
                 tc::tma_store_2d(&tmaps.o, tc::smem_u32(Ot), h * dv + 64 * wg, cs);
                 tc::bulk_commit();
             }
-        } else {
-            const bool row_ok = t >= lo && t < hi;
-            const size_t ob = row_ok ? static_cast<size_t>(cs + t) * vtok_stride + static_cast<size_t>(h) * dv + 64 * wg
-                                     : 0;
+        } else if (t >= lo && t < hi) {
+            const size_t ob = static_cast<size_t>(cs + t) * vtok_stride + static_cast<size_t>(h) * dv + 64 * wg;
+            if (p.out_f32) {
+                float* op = reinterpret_cast<float*>(p.out) + ob;
 #pragma unroll
-            for (int c16 = 0; c16 < 64; c16 += 16) {
-                float a[16];
-                tc::tmem_ld16(oaddr + c16, a);
-                tc::tmem_wait_ld();
-                if (row_ok) {
-                    if (p.out_f32) {
-                        float* op = reinterpret_cast<float*>(p.out) + ob + c16;
+                for (int q = 0; q < 64; q += 4)
+                    *reinterpret_cast<float4*>(op + q) = make_float4(a[q], a[q + 1], a[q + 2], a[q + 3]);
+            } else {
+                uint16_t* op = reinterpret_cast<uint16_t*>(p.out) + ob;
 #pragma unroll
-                        for (int q = 0; q < 16; q += 4)
-                            *reinterpret_cast<float4*>(op + q) = make_float4(a[q], a[q + 1], a[q + 2], a[q + 3]);
-                    } else {
-                        uint16_t* op = reinterpret_cast<uint16_t*>(p.out) + ob + c16;
-#pragma unroll
-                        for (int q = 0; q < 16; q += 8) {
-                            uint4 w;
-                            w.x = f32x2_to_bf16x2_bits(a[q], a[q + 1]);
-                            w.y = f32x2_to_bf16x2_bits(a[q + 2], a[q + 3]);
-                            w.z = f32x2_to_bf16x2_bits(a[q + 4], a[q + 5]);
-                            w.w = f32x2_to_bf16x2_bits(a[q + 6], a[q + 7]);
-                            *reinterpret_cast<uint4*>(op + q) = w;
-                        }
-                    }
+                for (int q = 0; q < 64; q += 8) {
+                    uint4 w;
+                    w.x = f32x2_to_bf16x2_bits(a[q], a[q + 1]);
+                    w.y = f32x2_to_bf16x2_bits(a[q + 2], a[q + 3]);
+                    w.z = f32x2_to_bf16x2_bits(a[q + 4], a[q + 5]);
+                    w.w = f32x2_to_bf16x2_bits(a[q + 6], a[q + 7]);
+                    *reinterpret_cast<uint4*>(op + q) = w;
                 }
             }
         }
@@ -1285,6 +1300,7 @@ int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
                    const uint16_t* beta, const float* init_state, const int32_t* cu_seqlens,
                    int num_seqs, int total_tokens, int H, int Dk, int Dv, void* out, int out_f32,
                    float* final_state, float* ckpt, int ckpt_stride, int decay, const int32_t* start_pos,
+                   const float* norm_gamma, float norm_eps,
                    void* ws, int* ring_flags, int ring_count, int* status, cudaStream_t stream)
 {
     using namespace prefill;
@@ -1304,6 +1320,7 @@ int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
     if (ring_flags && (ring_count <= 0 || cudaMemsetAsync(ring_flags, 0, sizeof(int) * ring_count, stream) != cudaSuccess))
         return -3;
     p.status = status; p.out_f32 = out_f32; p.ckpt_stride = ckpt_stride;
+    p.norm_gamma = norm_gamma; p.norm_eps = norm_eps;
     p.H = H; p.dk = Dk; p.dv = Dv;
     const long long clusters = static_cast<long long>(num_seqs) * H;
     if (clusters == 0 || total_tokens == 0) {

@@ -68,7 +68,7 @@ def load():
                 fn.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp, _vp, _i, _vp]
             lib.kda_chunk_prefill_ex.restype = _i
             lib.kda_chunk_prefill_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i,
-                                                 _vp, _vp, _i, _i, _vp, _vp, _vp]
+                                                 _vp, _vp, _i, _i, _vp, _vp, _vp, ctypes.c_float, _vp]
             lib.kda_decode_step.restype = _i
             lib.kda_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]
             lib.kda_decode_multi.restype = _i
@@ -170,7 +170,8 @@ def kda_chunk_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqle
 def kda_chunk_prefill_ex(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host,
                          num_seqs: int, total_tokens: int, H: int, Dk: int, Dv: int,
                          out, out_dtype: int, final_state, ckpt_states, ckpt_stride: int, decay: int,
-                         start_pos=None, start_pos_host=None, stream=None):
+                         start_pos=None, start_pos_host=None, out_norm_gamma=None, out_norm_eps: float = 1e-6,
+                         stream=None):
     sp_host = None if start_pos_host is None else start_pos_host.to(device="cpu", dtype=torch.int32).contiguous()
     cu_host = cu_seqlens_host.to(device="cpu", dtype=torch.int32).contiguous()
     rc = load().kda_chunk_prefill_ex(
@@ -178,7 +179,8 @@ def kda_chunk_prefill_ex(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_se
         _ptr(init_state), _ptr(cu_seqlens), ctypes.c_void_p(cu_host.data_ptr()),
         int(num_seqs), int(total_tokens), int(H), int(Dk), int(Dv),
         _ptr(out), int(out_dtype), _ptr(final_state), _ptr(ckpt_states), int(ckpt_stride), int(decay),
-        _ptr(start_pos), None if sp_host is None else ctypes.c_void_p(sp_host.data_ptr()), _stream(stream))
+        _ptr(start_pos), None if sp_host is None else ctypes.c_void_p(sp_host.data_ptr()),
+        _ptr(out_norm_gamma), float(out_norm_eps), _stream(stream))
     _check(rc, "kda_chunk_prefill_ex")
 
 
@@ -239,9 +241,10 @@ def kda_device_status(stream=None) -> int:
 
 def prefill(q, k, v, log_alpha, beta, cu_seqlens_host, init_state=None, ckpt_stride: int = 0,
             out_dtype=torch.bfloat16, want_final: bool = True, cu_seqlens=None, stream=None,
-            decay: int = KDA_DECAY_CHANNEL, start_pos_host=None):
+            decay: int = KDA_DECAY_CHANNEL, start_pos_host=None, norm_gamma=None, norm_eps: float = 1e-6):
     """Allocate outputs and run kda_chunk_prefill (kda_chunk_prefill_ex for another decay
-    layout or for start positions).  Returns (out, final_state, ckpt_states)."""
+    layout, for start positions or with the output norm fused in: norm_gamma [H, Dv]).
+    Returns (out, final_state, ckpt_states)."""
     T, H, Dk = q.shape
     Dv = v.shape[2]
     cu_host = cu_seqlens_host.to(device="cpu", dtype=torch.int32).contiguous()
@@ -254,14 +257,14 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens_host, init_state=None, ckpt_str
     nck = kda_ckpt_count_ex(cu_host, start_pos_host, ckpt_stride) if ckpt_stride > 0 else 0
     ck = torch.empty(nck, H, Dk, Dv, device=dev, dtype=torch.float32) if ckpt_stride > 0 else None
     odt = KDA_OUT_F32 if out_dtype == torch.float32 else KDA_OUT_BF16
-    if decay == KDA_DECAY_CHANNEL and start_pos_host is None:
+    if decay == KDA_DECAY_CHANNEL and start_pos_host is None and norm_gamma is None:
         kda_chunk_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_host, N, T, H, Dk, Dv,
                           out, odt, fin, ck if nck > 0 else None, ckpt_stride, stream)
     else:
         sp = None if start_pos_host is None else start_pos_host.to(device="cpu", dtype=torch.int32).contiguous()
         kda_chunk_prefill_ex(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_host, N, T, H, Dk, Dv,
                              out, odt, fin, ck if nck > 0 else None, ckpt_stride, decay,
-                             None if sp is None else sp.to(dev), sp, stream)
+                             None if sp is None else sp.to(dev), sp, norm_gamma, norm_eps, stream)
     return out, fin, ck
 
 

@@ -160,3 +160,32 @@ def decode_case(N: int = 512, H: int = 32, D: int = 128, steps: int = 64, seed: 
         q, k, v, la, beta = _token_inputs(N, H, D, D, g, device, la_shift)
         st.append(dict(q=q, k=k, v=v, log_alpha=la, beta=beta))
     return DecodeCase(f"decode_N{N}_H{H}_D{D}", state, st)
+
+
+@dataclass
+class ModuleCase:
+    """Raw inputs of the KDA module around the recurrence: the q, k, v projections before
+    the short convolution, its depthwise taps, the gate pre-activations, and the output
+    norm weight."""
+    xq: torch.Tensor           # [T, H, D] bf16
+    xk: torch.Tensor
+    xv: torch.Tensor
+    conv_w: torch.Tensor       # [3, H, D, 4] fp32
+    a_raw: torch.Tensor        # [T, H, D] fp32 (alpha gate pre-activation)
+    b_raw: torch.Tensor        # [T, H] bf16 (beta pre-activation)
+    gamma: torch.Tensor        # [H, D] fp32 (output norm weight)
+    cu_seqlens: torch.Tensor   # [2] int32, host
+
+
+def module_case(T: int, H: int = 32, D: int = 128, seed: int = 5, device="cpu") -> ModuleCase:
+    """One T-token prompt: projections ~ N(0, 1), taps ~ N(0, 0.5^2), alpha pre-activations
+    ~ N(-2, 1) (so -softplus gives the decays of the prefill cases), beta pre-activations
+    ~ N(0, 1), norm weight ~ U(0.5, 1.5)."""
+    g = _gen(seed, device)
+    xq, xk, xv = (torch.randn(T, H, D, generator=g, device=device).to(torch.bfloat16) for _ in range(3))
+    w = torch.randn(3, H, D, 4, generator=g, device=device) * 0.5
+    a = torch.randn(T, H, D, generator=g, device=device) - 2.0
+    b = torch.randn(T, H, generator=g, device=device).to(torch.bfloat16)
+    gamma = torch.rand(H, D, generator=g, device=device) + 0.5
+    cu = torch.tensor([0, T], dtype=torch.int32)
+    return ModuleCase(xq, xk, xv, w.contiguous(), a.contiguous(), b, gamma.contiguous(), cu)

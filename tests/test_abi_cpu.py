@@ -146,11 +146,12 @@ def test_prefill_ex_decay_rules_on_host(lib):
         cu = (ctypes.c_int32 * 3)(0, 64, 100)
         a = dict(q=0x1000, k=0x2000, v=0x3000, la=0x4000, beta=0x5000, s0=None, cu=0x6000,
                  cu_host=ctypes.cast(cu, ctypes.c_void_p), N=2, T=100, H=4, Dk=64, Dv=64,
-                 out=0x7000, out_dtype=0, fin=None, ck=None, stride=0, sp=None, sp_host=None, stream=None)
+                 out=0x7000, out_dtype=0, fin=None, ck=None, stride=0, sp=None, sp_host=None, gamma=None, eps=1e-6,
+                 stream=None)
         a.update(over)
         return getattr(lib, f)(a["q"], a["k"], a["v"], a["la"], a["beta"], a["s0"], a["cu"], a["cu_host"], a["N"],
                                a["T"], a["H"], a["Dk"], a["Dv"], a["out"], a["out_dtype"], a["fin"], a["ck"],
-                               a["stride"], decay, a["sp"], a["sp_host"], a["stream"])
+                               a["stride"], decay, a["sp"], a["sp_host"], a["gamma"], a["eps"], a["stream"])
     assert raw(kda.KDA_DECAY_HEAD, H=6) == kda.KDA_ERR_UNSUPPORTED     # per-head rows need H % 4 == 0
     assert raw(kda.KDA_DECAY_NONE) == kda.KDA_ERR_INVALID_ARG          # log_alpha given but unused
     assert raw(kda.KDA_DECAY_CHANNEL, la=None) == kda.KDA_ERR_INVALID_ARG
@@ -160,6 +161,11 @@ def test_prefill_ex_decay_rules_on_host(lib):
     assert raw(kda.KDA_DECAY_CHANNEL, sp=0x9000) == kda.KDA_ERR_INVALID_ARG       # device copy without host copy
     assert raw(kda.KDA_DECAY_CHANNEL, sp=0x9000,
                sp_host=ctypes.cast(sp, ctypes.c_void_p)) == kda.KDA_ERR_INVALID_ARG   # negative position
+    # the fused output norm: gamma 16-byte aligned, eps finite and >= 0
+    assert raw(kda.KDA_DECAY_CHANNEL, gamma=0xA004) == kda.KDA_ERR_INVALID_ARG
+    assert raw(kda.KDA_DECAY_CHANNEL, gamma=0xA000, eps=-1.0) == kda.KDA_ERR_INVALID_ARG
+    assert raw(kda.KDA_DECAY_CHANNEL, gamma=0xA000, eps=float("nan")) == kda.KDA_ERR_INVALID_ARG
+    assert raw(kda.KDA_DECAY_CHANNEL, gamma=0xA000, eps=float("inf")) == kda.KDA_ERR_INVALID_ARG
 
 
 def test_ckpt_count_with_start_positions(lib):

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 from oracle import prep
-from kimi_delta_attention_06_gb300 import kda
+from kimi_delta_attention_06_gb300 import kda, workloads
 from tests import _parity as P
 
 pytestmark = pytest.mark.gpu
@@ -123,3 +123,41 @@ def test_module_path_prepare_prefill_norm():
     yr = prep.output_norm(ro, gamma, eps=1e-6)
     rel = np.abs(y.float().cpu().double().numpy() - yr).max() / np.sqrt((yr ** 2).mean())
     assert rel < 3e-2
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("D", [64, 128])
+def test_prefill_with_fused_output_norm(out_dtype, D):
+    """The per-head output norm fused into the prefill's output epilogue, against the fp64
+    recurrence followed by the fp64 norm, on ragged sequences (full chunks leave through
+    the TMA store, partial ones through plain stores) and a prefix continuation."""
+    lens = [300, 1, 129, 64]
+    H = 4
+    case = workloads.prefill_case(lens, H=H, D=D, seed=30 + D, ckpt_stride=0)
+    gamma = torch.rand(H, D, generator=torch.Generator().manual_seed(3)) + 0.5
+    start = torch.tensor([0, 5, 100, 64], dtype=torch.int32)
+    dev = lambda x: None if x is None else x.to(DEV)
+    y, fin, _ = kda.prefill(dev(case.q), dev(case.k), dev(case.v), dev(case.log_alpha), dev(case.beta),
+                            case.cu_seqlens, init_state=dev(case.init_state), out_dtype=out_dtype,
+                            start_pos_host=start, norm_gamma=gamma.to(DEV), norm_eps=1e-6)
+    o, fin2, _ = kda.prefill(dev(case.q), dev(case.k), dev(case.v), dev(case.log_alpha), dev(case.beta),
+                             case.cu_seqlens, init_state=dev(case.init_state), out_dtype=torch.float32,
+                             start_pos_host=start)
+    torch.cuda.synchronize()
+    assert kda.kda_device_status() == kda.KDA_OK
+    assert torch.equal(fin, fin2)                        # the norm touches only the output
+    ro, rf, _ = oracle.prefill(case.q, case.k, case.v, case.log_alpha, case.beta, case.cu_seqlens,
+                               case.init_state, start_pos=start.tolist())
+    P.check_state(fin, rf)
+    yr = prep.output_norm(ro, gamma, eps=1e-6)
+    yg = y.float().cpu().double().numpy()
+    rel = np.abs(yg - yr).max() / np.sqrt((yr ** 2).mean())
+    assert rel < 3e-2, rel
+    # the separate norm pass applied to the fp32 output gives the same up to its bf16 rounding
+    # (half an ulp, 2^-8 |y|, on each side) and the rsqrt's few ulps
+    ys = torch.empty(o.shape, device=DEV, dtype=torch.bfloat16)
+    kda.kda_output_norm(o, kda.KDA_OUT_F32, gamma.to(DEV), 1e-6, ys, o.shape[0], H, D)
+    torch.cuda.synchronize()
+    yf, ysf = y.float(), ys.float()
+    rms = ysf.pow(2).mean().sqrt()
+    assert ((yf - ysf).abs() <= 2.0 ** -7 * ysf.abs() + 1e-3 * rms).all()
