@@ -118,7 +118,7 @@ constexpr uint32_t K_S = 2 * H_STRIDE;               // S f16, 128 rows (channel
 constexpr uint32_t K_O = K_S + 32768;                // O bf16 staging, 64 tokens x 64 columns per warpgroup (2 x 8 KB)
 constexpr uint32_t K_BAR = K_O + 16384;              // mbarriers (indices below)
 constexpr int KB_MMA = 0;      // [1] MMA completion (thread 0's MMAs)
-constexpr int KB_VP = 1;       // [1] completion of a V part issued by the loader thread
+constexpr int KB_VP = 1;       // [1] completion of a V part issued by thread VP (not thread 0)
 constexpr int KB_FULL = 2;     // [2] slot loaded
 constexpr int KB_CONS = 4;     // [2] slot consumed
 constexpr int KB_READY = 6;    // [6] ring entry stored by its prep CTA
@@ -402,6 +402,8 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
     const int nchunks = g.nchunks;
 
     if (warp == 0) tc::tmem_alloc(s_tmem, TM_PREP_COLS);
+    for (int i = tid; i < 64 * LH / 8; i += NT)            // T scratch: its upper blocks stay zero
+        reinterpret_cast<uint4*>(Th)[i] = make_uint4(0u, 0u, 0u, 0u);
     cta_sync_tc();
     const uint32_t tm = *s_tmem;
     const uint32_t lane_base = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);
@@ -724,9 +726,7 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         // -- 4. T = (I + L)^{-1} by recursive doubling over 16 x 16 blocks --
         //    blocks [[A, 0], [B, D]]^{-1} = [[A^-1, 0], [-D^-1 B A^-1, D^-1]]; the block
         //    products run on warp-level tensor-core MMAs (fp16 in, fp32 accumulate)
-        for (int i = tid; i < 64 * LH / 8; i += NT)
-            reinterpret_cast<uint4*>(Th)[i] = make_uint4(0u, 0u, 0u, 0u);
-        tc::named_sync(BAR_ALL, NT);
+        //    (T's blocks above the diagonal are never written: zero since the kernel started)
         if (tid < 64) {            // diagonal blocks, column-oriented forward substitution (fp32)
             const int bb = tid >> 4, cc = tid & 15;
             const __half* Lb = Lh + (16 * bb) * LH + 16 * bb;
@@ -946,6 +946,7 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
     // are issued in order; `issued` counts them.  Non-blocking probes run while thread 0
     // issues MMAs, so that the next chunk is normally in flight long before it is needed.
     constexpr int LD = 32;
+    constexpr int VP = 96;                    // issues the next chunk's V part (an O-row thread)
     int issued = 0;
     bool load_ok = true;
     auto load = [&](int j, bool block) -> bool {
@@ -982,7 +983,7 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
     if (tid == 0) *s_vflag = 0;               // (published by the first slot wait's barrier)
     uint32_t vp_seen = 0;                     // thread 0: loader V parts waited for
     bool vp_ok = true;                        // thread 0: those waits all completed
-    uint32_t vp_done = 0;                     // loader: V parts issued and committed
+    uint32_t vp_done = 0;                     // thread VP: V parts issued and committed
     const int Nmma = dv;                      // 64 or 128 value columns per MMA
     // [U; O] = [T; Mqk] V for chunk j, into TM_D1[j % 2]
     auto issue_vpart = [&](int j) {
@@ -1075,7 +1076,7 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
             // the ring entry is free again: its prep CTA may store chunk c + 6 there
             if (c + WS_SLOTS < nchunks)
                 tc::mbar_arrive_remote_relaxed(tc::mapa(prep_free + 8u * ((c / NPREP_CTAS) & 1), 1 + c % NPREP_CTAS));
-            if (*s_vflag == c + 1) {           // the loader issued this V part: it has to be complete
+            if (*s_vflag == c + 1) {           // thread VP issued this V part: it has to be complete
                 vp_ok = tc::mbar_wait_bounded(&mb[KB_VP], vp_seen & 1u, kWaitLimitNs) != 0;
                 ++vp_seen;
             } else {
@@ -1086,22 +1087,20 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
                             tc::smem_u32(Sb), true, 128u * 128u, true);
             tc::mma_commit(&mb[KB_MMA]);
         }
-        if (tid == LD) {
-            probe(c + 2);
-            // the next chunk's V part, if its slot has landed, runs behind this MMA; issuing it
-            // here, while the MMA executes, keeps its issue time out of every barrier window
-            if (c + 1 < nchunks && tc::mbar_test_wait(&mb[KB_FULL + (s ^ 1)], ((c + 1) >> 1) & 1)) {
-                issue_vpart(c + 1);
-                tc::mma_commit(&mb[KB_VP]);
-                ++vp_done;
-                *s_vflag = c + 2;
-            }
-        }
+        if (tid == LD) probe(c + 2);
         if (d >= 64 && col_ok && c > 0) o_epilogue(c - 1);   // the previous chunk's O, while this MMA runs
         const float gc = reinterpret_cast<const float*>(slot + H_EGC)[d];
         // (thread 0's V-part wait joins the agreement here, so every thread leaves together)
         if (!cta_wait(&mb[KB_MMA], ph_mma & 1, false, vp_ok)) { ok = false; break; }
         ++ph_mma;
+        // the next chunk's V part, if its slot has landed: the pipe is idle while the U rows
+        // are read out, and the issuing thread (an O-row thread) has nothing else to do here
+        if (tid == VP && c + 1 < nchunks && tc::mbar_test_wait(&mb[KB_FULL + (s ^ 1)], ((c + 1) >> 1) & 1)) {
+            issue_vpart(c + 1);
+            tc::mma_commit(&mb[KB_VP]);
+            ++vp_done;
+            *s_vflag = c + 2;
+        }
         if (d < 64 && col_ok) {   // U -> MN-major f16 tile, over the (now dead) V tile of the slot
             float r[64];
             tmem_ld64(lane_base + d1 + cb, r);
@@ -1151,7 +1150,7 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
         tc::mma_commit(&mb[KB_MMA]);
         tc::mbar_wait_bounded(&mb[KB_MMA], ph_mma & 1, kWaitLimitNs);
     }
-    if (tid == LD && vp_done > 0)             // its last V part must finish before TMEM is freed
+    if (tid == VP && vp_done > 0)             // its last V part must finish before TMEM is freed
         tc::mbar_wait_bounded(&mb[KB_VP], (vp_done - 1) & 1u, kWaitLimitNs);
     if (tid == LD) {
         // loads still in flight must land before this CTA's shared memory goes away
