@@ -11,7 +11,14 @@ in HBM and larger than the 129 MB L2, so no L2 flush is needed between steps.
 `value` = prefill tokens/s (whole job: tokens of all ranks / max-over-ranks
 time).  The decode step's state-update bandwidth is reported alongside.
 
+With N > 1 ranks (one per GPU), --split chooses what a rank serves:
+  replicas (default)  its own prompt and decode batch: weak scaling;
+  heads               H / N heads of the one prompt and of the one decode batch:
+                      strong scaling.  KDA heads are independent recurrences, so
+                      neither split has a collective on the data path.
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--split replicas|heads]
 
 --impl reference times the fp64 CPU oracle on the host cores instead (a
 bounded sample of the same workload), the reference arm for this method.
@@ -44,20 +51,20 @@ STATE_BYTES = 4 * D * D                                          # one fp32 head
 FLOPS_PER_CHUNK = 12 * 64 ** 3 + 8 * 64 ** 2 * D + 6 * 64 * D ** 2
 
 
-def prefill_algorithmic_bytes(T, n_ckpt_per_head):
+def prefill_algorithmic_bytes(T, n_ckpt_per_head, heads=H):
     # inputs + output, plus init-state read, final-state write and checkpoint writes
-    return BYTES_PER_TOKEN_HEAD * T * H + STATE_BYTES * H * (2 + n_ckpt_per_head)
+    return BYTES_PER_TOKEN_HEAD * T * heads + STATE_BYTES * heads * (2 + n_ckpt_per_head)
 
 
-def kv_state_bytes(n_ckpt_per_head):
+def kv_state_bytes(n_ckpt_per_head, heads=H):
     """Bytes of recurrent state one prefill hands to a prefix cache: the final state and
     every checkpoint, all heads (the 'KV size' of KV throughput = KV size / prefill time)."""
-    return STATE_BYTES * H * (1 + n_ckpt_per_head)
+    return STATE_BYTES * heads * (1 + n_ckpt_per_head)
 
 
-def decode_algorithmic_bytes(N):
+def decode_algorithmic_bytes(N, heads=H):
     # state read + write, plus q, k, v, log_alpha, beta in and o out
-    return N * H * (2 * STATE_BYTES + BYTES_PER_TOKEN_HEAD)
+    return N * heads * (2 * STATE_BYTES + BYTES_PER_TOKEN_HEAD)
 
 
 def reduce_max(values, device="cpu"):
@@ -79,6 +86,34 @@ def whole_job_rate(units_per_rank, world, slowest_ms):
 def rank_seed(base, rank):
     """Each rank serves its own prompt and decode batch (independent problems)."""
     return base + 1000 * rank
+
+
+def head_range(h_total, world, rank):
+    """Heads [h0, h1) of rank `rank` when one problem's h_total heads are split evenly
+    over `world` ranks."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError(f"rank {rank} outside a world of {world}")
+    if h_total % world:
+        raise ValueError(f"{h_total} heads do not split evenly over {world} ranks")
+    n = h_total // world
+    return rank * n, (rank + 1) * n
+
+
+def job_rate(units, world, slowest_ms, split):
+    """Whole-job throughput.  replicas: every rank processes `units` of its own (weak
+    scaling); heads: the ranks process one set of `units` between them (strong scaling).
+    Either way the job takes as long as the slowest rank."""
+    if split not in ("replicas", "heads"):
+        raise ValueError(split)
+    return whole_job_rate(units, world if split == "replicas" else 1, slowest_ms)
+
+
+def rank_problem(split, world, rank):
+    """(heads served, seed offset) of a rank: replicas draw their own problems from
+    per-rank seeds; a head split cuts the one problem (seed offset 0) into head ranges."""
+    if split == "heads":
+        return head_range(H, world, rank), 0
+    return (0, H), 1000 * rank
 
 
 def read_peaks():
@@ -214,7 +249,7 @@ def time_oracle(budget_s=12.0):
             "decode_gbs": dec_gbs, "prefill_seconds": dt}
 
 
-def time_module_path(dev, stream, rank, steps=10):
+def time_module_path(dev, stream, heads=(0, H), seed_offset=0, steps=10):
     """The KDA module around the recurrence at T=145408, H=32, D=128, timed on the device:
     kda_prepare_inputs (short conv + SiLU, L2 norm of q and k, alpha and beta gates) then
     kda_chunk_prefill_ex with the per-head output norm fused into its output epilogue: two
@@ -222,27 +257,30 @@ def time_module_path(dev, stream, rank, steps=10):
     beside it; both write the same normed bf16 output."""
     import torch
     from kimi_delta_attention_06_gb300 import kda, workloads
-    m = workloads.module_case(T_PROMPT, H=H, D=D, seed=rank_seed(5, rank), device=dev)
+    m = workloads.module_case(T_PROMPT, H=H, D=D, seed=5 + seed_offset, device=dev)
+    Hl = heads[1] - heads[0]
+    if Hl != H:
+        m = workloads.head_slice(m, *heads)
     cu = m.cu_seqlens.to(dev)
-    q, k, v = (torch.empty(T_PROMPT, H, D, device=dev, dtype=torch.bfloat16) for _ in range(3))
-    la = torch.empty(T_PROMPT, H, D, device=dev)
-    beta = torch.empty(T_PROMPT, H, device=dev, dtype=torch.bfloat16)
-    s0 = torch.zeros(1, H, D, D, device=dev)
-    o = torch.empty(T_PROMPT, H, D, device=dev, dtype=torch.bfloat16)
+    q, k, v = (torch.empty(T_PROMPT, Hl, D, device=dev, dtype=torch.bfloat16) for _ in range(3))
+    la = torch.empty(T_PROMPT, Hl, D, device=dev)
+    beta = torch.empty(T_PROMPT, Hl, device=dev, dtype=torch.bfloat16)
+    s0 = torch.zeros(1, Hl, D, D, device=dev)
+    o = torch.empty(T_PROMPT, Hl, D, device=dev, dtype=torch.bfloat16)
     y = torch.empty_like(o)
-    fin = torch.empty(1, H, D, D, device=dev)
+    fin = torch.empty(1, Hl, D, D, device=dev)
 
     def prepare():
         kda.kda_prepare_inputs(m.xq, m.xk, m.xv, m.conv_w, None, m.a_raw, m.b_raw, cu, m.cu_seqlens, 1, T_PROMPT,
-                               H, D, 1, q, k, v, la, beta, stream)
+                               Hl, D, 1, q, k, v, la, beta, stream)
 
     def prefill(norm):
-        kda.kda_chunk_prefill_ex(q, k, v, la, beta, s0, cu, m.cu_seqlens, 1, T_PROMPT, H, D, D, y if norm else o,
+        kda.kda_chunk_prefill_ex(q, k, v, la, beta, s0, cu, m.cu_seqlens, 1, T_PROMPT, Hl, D, D, y if norm else o,
                                  kda.KDA_OUT_BF16, fin, None, 0, kda.KDA_DECAY_CHANNEL,
                                  out_norm_gamma=m.gamma if norm else None, out_norm_eps=1e-6, stream=stream)
 
     def norm():
-        kda.kda_output_norm(o, kda.KDA_OUT_BF16, m.gamma, 1e-6, y, T_PROMPT, H, D, stream)
+        kda.kda_output_norm(o, kda.KDA_OUT_BF16, m.gamma, 1e-6, y, T_PROMPT, Hl, D, stream)
 
     res = {}
     for name, parts in (("fused", [prepare, lambda: prefill(True)]),
@@ -260,22 +298,104 @@ def time_module_path(dev, stream, rank, steps=10):
         torch.cuda.synchronize()
         per = [statistics.median(e[j].elapsed_time(e[j + 1]) for e in ev) for j in range(len(parts))]
         tot = statistics.median(e[0].elapsed_time(e[-1]) for e in ev)
-        res[name] = {"ms_per_step": tot, "launch_ms": per, "tokens_per_s": T_PROMPT / (tot / 1e3)}
+        res[name] = {"ms_per_step": tot, "launch_ms": per, "tokens_per_s": T_PROMPT / (tot / 1e3),
+                     "heads": Hl}
     if kda.kda_device_status() != 0:
         raise RuntimeError("device status after the module path")
-    res["workload"] = (f"prepare (conv width 4 + SiLU, L2 norm, gates) -> prefill T={T_PROMPT} H={H} Dk=Dv={D} "
+    res["workload"] = (f"prepare (conv width 4 + SiLU, L2 norm, gates) -> prefill T={T_PROMPT} H={Hl} Dk=Dv={D} "
                        f"-> per-head output norm; zero initial state, no checkpoints")
     res["launches"] = {"fused": ["kda_prepare_inputs", "kda_chunk_prefill_ex (+norm)"],
                        "separate": ["kda_prepare_inputs", "kda_chunk_prefill_ex", "kda_output_norm"]}
     return res
 
 
-def bench_config(world):
+def _median_ms(fns, stream, steps):
+    """Median CUDA-event time of `fns` run back to back, after 3 untimed rounds."""
+    import torch
+    for _ in range(3):
+        for f in fns:
+            f()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record(stream)
+        for f in fns:
+            f()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+
+def time_other_rows(dev, stream, heads=(0, H), seed_offset=0, steps=10):
+    """The workloads beside the headline, timed on the device after the main timed region:
+    - varlen: 16 packed sequences of log-uniform length in [1k, 64k] (279,375 tokens), even
+      ones from an initial state, checkpoints every 32768 tokens;
+    - layouts: the T=145408 prompt with one decay per head (Gated DeltaNet) and with none
+      (DeltaNet), through kda_chunk_prefill_ex;
+    - serving decode: kda_decode_multi over a 512-slot x H state pool, K = 8 tokens per
+      sequence, verify (states untouched) and commit (states written back)."""
+    import torch
+    from kimi_delta_attention_06_gb300 import kda, workloads
+    h0, h1 = heads
+    Hl = h1 - h0
+    res = {}
+
+    def cut(case):
+        return case if Hl == H else workloads.head_slice(case, h0, h1)
+
+    vc = cut(workloads.varlen_case(seed=3 + seed_offset, device=dev, H=H, D=D, ckpt_stride=CKPT))
+    cu = vc.cu_seqlens.to(dev)
+    out = torch.empty(vc.T, Hl, D, device=dev, dtype=torch.bfloat16)
+    fin = torch.empty(vc.N, Hl, D, D, device=dev)
+    nck = kda.kda_ckpt_count(vc.cu_seqlens, CKPT)
+    ck = torch.empty(max(nck, 1), Hl, D, D, device=dev)
+    ms = _median_ms([lambda: kda.kda_chunk_prefill(vc.q, vc.k, vc.v, vc.log_alpha, vc.beta, vc.init_state, cu,
+                                                   vc.cu_seqlens, vc.N, vc.T, Hl, D, D, out, kda.KDA_OUT_BF16, fin,
+                                                   ck if nck else None, CKPT, stream)], stream, steps)
+    res["varlen"] = {"ms": ms, "tokens": vc.T, "sequences": vc.N, "tokens_per_s": vc.T / (ms / 1e3),
+                     "workload": vc.name}
+    del vc, out, fin, ck
+
+    c = cut(workloads.single_case(T_PROMPT, seed=2 + seed_offset, device=dev, ckpt_stride=CKPT))
+    cu = c.cu_seqlens.to(dev)
+    out = torch.empty(T_PROMPT, Hl, D, device=dev, dtype=torch.bfloat16)
+    fin = torch.empty(1, Hl, D, D, device=dev)
+    lay = {}
+    for name, decay, la in (("gated_deltanet", kda.KDA_DECAY_HEAD, c.log_alpha[:, :, 0].contiguous()),
+                            ("deltanet", kda.KDA_DECAY_NONE, None)):
+        ms = _median_ms([lambda: kda.kda_chunk_prefill_ex(c.q, c.k, c.v, la, c.beta, c.init_state, cu, c.cu_seqlens,
+                                                          1, T_PROMPT, Hl, D, D, out, kda.KDA_OUT_BF16, fin, None,
+                                                          0, decay, stream=stream)], stream, steps)
+        lay[name] = {"ms": ms, "tokens_per_s": T_PROMPT / (ms / 1e3)}
+    res["layouts"] = lay
+    del c, out, fin
+
+    K = 8
+    d = cut(workloads.decode_case(N=DEC_N, H=H, D=D, steps=K, seed=4 + seed_offset, device=dev))
+    tok = {key: torch.stack([st[key] for st in d.steps], dim=1).contiguous()
+           for key in ("q", "k", "v", "log_alpha", "beta")}
+    dout = torch.empty(DEC_N, K, Hl, D, device=dev, dtype=torch.bfloat16)
+    sd = {}
+    for name, commit in (("verify", 0), ("commit", 1)):
+        ms = _median_ms([lambda: kda.kda_decode_multi(tok["q"], tok["k"], tok["v"], tok["log_alpha"], tok["beta"],
+                                                      d.state, DEC_N, None, None, commit, dout, kda.KDA_OUT_BF16,
+                                                      DEC_N, K, Hl, D, D, stream=stream)], stream, steps)
+        sd[name + "_ms"] = ms
+    sd.update({"sequences": DEC_N, "tokens_per_sequence": K,
+               "verify_tokens_per_s": DEC_N * K / (sd["verify_ms"] / 1e3)})
+    res["serving_decode"] = sd
+    if kda.kda_device_status() != 0:
+        raise RuntimeError("device status after the other rows")
+    return res
+
+
+def bench_config(world, split="replicas"):
     """The workload description both arms print (the reference arm times a bounded sample of it)."""
+    par = f"replicas x{world}" if split == "replicas" else f"heads split over {world} ranks ({H // world} per rank)"
     return {"workload": f"kda prefill T={T_PROMPT} H={H} Dk=Dv={D} ckpt every {CKPT} + decode N={DEC_N} H={H} D={D}",
-            "global_batch": world, "seq_len": T_PROMPT, "heads": H, "head_dim": D,
+            "global_batch": world if split == "replicas" else 1, "seq_len": T_PROMPT, "heads": H, "head_dim": D,
             "ckpt_stride": CKPT, "decode_batch": DEC_N,
-            "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"replicas x{world}"}
+            "l2": "inputs larger than L2 (no flush needed)", "parallelism": par}
 
 
 def run_reference(args, rank):
@@ -291,9 +411,10 @@ def run_reference(args, rank):
     cb["value"] = v
     line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(x["prefill_seconds"] for x in samples),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "higher_is_better": True, "scaling": "weak" if args.split == "replicas" else "strong",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": bench_config(args.gpus),
+            "config": bench_config(args.gpus, args.split),
             "cpu_baseline": cb,
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -309,6 +430,9 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-module", action="store_true")
+    ap.add_argument("--no-other", action="store_true", help="skip the varlen, layout and serving-decode rows")
+    ap.add_argument("--split", choices=["replicas", "heads"], default="replicas",
+                    help="N > 1: each rank serves its own problem (replicas) or H/N heads of one (heads)")
     args = ap.parse_args(argv)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -331,25 +455,30 @@ def main(argv=None):
     kda.load()
     stream = torch.cuda.current_stream()
 
-    # ---- inputs (seeded per rank: each rank serves its own prompt and decode batch) ----
-    c = workloads.single_case(T_PROMPT, seed=rank_seed(2, rank), device=dev, ckpt_stride=CKPT)
+    # ---- inputs: replicas draw per-rank problems; a head split cuts the one problem ----
+    split = args.split
+    (h0, h1), seed_off = rank_problem(split, world, rank)
+    Hl = h1 - h0
+    c = workloads.single_case(T_PROMPT, seed=2 + seed_off, device=dev, ckpt_stride=CKPT)
+    dc = workloads.decode_case(N=DEC_N, H=H, D=D, steps=1, seed=4 + seed_off, device=dev)
+    if Hl != H:
+        c, dc = workloads.head_slice(c, h0, h1), workloads.head_slice(dc, h0, h1)
     cu_dev = c.cu_seqlens.to(dev)
-    out = torch.empty(T_PROMPT, H, D, device=dev, dtype=torch.bfloat16)
-    fin = torch.empty(1, H, D, D, device=dev, dtype=torch.float32)
+    out = torch.empty(T_PROMPT, Hl, D, device=dev, dtype=torch.bfloat16)
+    fin = torch.empty(1, Hl, D, D, device=dev, dtype=torch.float32)
     n_ck = kda.kda_ckpt_count(c.cu_seqlens, CKPT)
-    ck = torch.empty(n_ck, H, D, D, device=dev, dtype=torch.float32)
-    dc = workloads.decode_case(N=DEC_N, H=H, D=D, steps=1, seed=rank_seed(4, rank), device=dev)
+    ck = torch.empty(n_ck, Hl, D, D, device=dev, dtype=torch.float32)
     dstate = dc.state
     ds = dc.steps[0]
-    dout = torch.empty(DEC_N, H, D, device=dev, dtype=torch.bfloat16)
+    dout = torch.empty(DEC_N, Hl, D, device=dev, dtype=torch.bfloat16)
 
     def prefill():
         kda.kda_chunk_prefill(c.q, c.k, c.v, c.log_alpha, c.beta, c.init_state, cu_dev, c.cu_seqlens, 1, T_PROMPT,
-                              H, D, D, out, kda.KDA_OUT_BF16, fin, ck, CKPT, stream)
+                              Hl, D, D, out, kda.KDA_OUT_BF16, fin, ck, CKPT, stream)
 
     def decode():
         kda.kda_decode_step(ds["q"], ds["k"], ds["v"], ds["log_alpha"], ds["beta"], dstate, dout,
-                            kda.KDA_OUT_BF16, DEC_N, H, D, D, stream)
+                            kda.KDA_OUT_BF16, DEC_N, Hl, D, D, stream)
 
     for _ in range(max(3, args.warmup)):
         prefill(); decode()
@@ -395,14 +524,14 @@ def main(argv=None):
     pre_avg = pre_sum / args.steps
     dec_avg = dec_sum / args.steps
 
-    tokens_all = T_PROMPT * world
-    value = whole_job_rate(T_PROMPT, world, pre_avg)
+    value = job_rate(T_PROMPT, world, pre_avg, split)
     hbm, bf16, bf16s, peak_src = read_peaks()
-    pre_bytes = prefill_algorithmic_bytes(T_PROMPT, n_ck)
-    dec_bytes = decode_algorithmic_bytes(DEC_N)
+    # per-rank (per-GPU) bytes and FLOPs: the roofline is a single GPU's
+    pre_bytes = prefill_algorithmic_bytes(T_PROMPT, n_ck, Hl)
+    dec_bytes = decode_algorithmic_bytes(DEC_N, Hl)
     pre_gbs = pre_bytes / (pre_avg / 1e3) / 1e9
     dec_gbs = dec_bytes / (dec_avg / 1e3) / 1e9
-    useful_tflops = FLOPS_PER_CHUNK * (T_PROMPT / 64) * H / (pre_avg / 1e3) / 1e12
+    useful_tflops = FLOPS_PER_CHUNK * (T_PROMPT / 64) * Hl / (pre_avg / 1e3) / 1e12
 
     # ---- end to end through host buffers (pinned), copies inside the timed region ----
     e2e = None
@@ -447,7 +576,7 @@ def main(argv=None):
             stream.wait_event(ev["out"])
             d = bf["d_in"]
             kda.kda_chunk_prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], bf["s0"], cu_dev,
-                                  c.cu_seqlens, 1, T_PROMPT, H, D, D, bf["out"], kda.KDA_OUT_BF16, bf["fin"], bf["ck"],
+                                  c.cu_seqlens, 1, T_PROMPT, Hl, D, D, bf["out"], kda.KDA_OUT_BF16, bf["fin"], bf["ck"],
                                   CKPT, stream)
             ev["comp"].record(stream)
             s_out.wait_event(ev["comp"])
@@ -485,7 +614,7 @@ def main(argv=None):
             link_ms.append(a.elapsed_time(b))
         h2d_gbs = hq.numel() * hq.element_size() / (min(link_ms) / 1e3) / 1e9
         floor_ms = h2d / (h2d_gbs * 1e9) * 1e3
-        e2e = {"value": whole_job_rate(T_PROMPT, world, e_ms), "unit": "tokens/s",
+        e2e = {"value": job_rate(T_PROMPT, world, e_ms, split), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e_ms, "steps": n_e2e,
                "link": {"h2d_gbs": round(h2d_gbs, 1), "h2d_floor_ms": round(floor_ms, 2),
@@ -495,7 +624,8 @@ def main(argv=None):
                        "streams, and copy-out of step i-1 overlap the prefill of step i)"}
         del host, bufs, h_out, h_ck
 
-    module = None if args.no_module else time_module_path(dev, stream, rank)
+    module = None if args.no_module else time_module_path(dev, stream, (h0, h1), seed_off)
+    other = None if args.no_other else time_other_rows(dev, stream, (h0, h1), seed_off)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -508,21 +638,22 @@ def main(argv=None):
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "fp16/tf32 MMA, fp32 accumulate + state (bf16 in/out)", "data": "synthetic",
-            "config": bench_config(world),
+            "scaling": "weak" if split == "replicas" else "strong", "vs_baseline": None,
+            "dtype": "fp16/tf32 MMA, fp32 accumulate + state (bf16 in/out)", "data": "synthetic",
+            "config": bench_config(world, split), "heads_per_rank": Hl,
             "prefill_ms": pre_avg, "decode_ms": dec_avg,
-            "decode": {"value": dec_gbs * world, "unit": "GB/s", "tokens_per_s": whole_job_rate(DEC_N, world, dec_avg),
+            "decode": {"value": dec_gbs * world, "unit": "GB/s", "tokens_per_s": job_rate(DEC_N, world, dec_avg, split),
                        "frac_of_hbm_peak": dec_gbs / hbm},
             "roofline": {"bound": "hbm", "achieved": pre_gbs, "peak": hbm, "unit": "GB/s",
                          "frac": pre_gbs / hbm, "traffic": traffic, "kernel": "kda_prefill_kernel",
                          "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": pre_bytes},
             "useful_flops": {"tflops": useful_tflops, "frac_of_bf16_peak": useful_tflops / bf16,
                              "frac_of_bf16_sustained": useful_tflops / bf16s, "peak_source": peak_src},
-            "kv_throughput": {"value": kv_state_bytes(n_ck) * world / (pre_avg * 1e-3) / 1e9, "unit": "GB/s",
-                              "state_bytes_per_prefill": kv_state_bytes(n_ck),
+            "kv_throughput": {"value": kv_state_bytes(n_ck, Hl) * world / (pre_avg * 1e-3) / 1e9, "unit": "GB/s",
+                              "state_bytes_per_prefill": kv_state_bytes(n_ck, Hl),
                               "note": "final state + checkpoints written per prefill / prefill time"},
             "clocks": clocks, "e2e": e2e, "gpu_launches": 2 * args.steps, "cpu_baseline": cpu,
-            "module": module,
+            "module": module, "other": other,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -21,7 +21,7 @@ fp32.  The oracle receives exactly the same (rounded) values.
 from __future__ import annotations
 
 import math
-from dataclasses import dataclass
+from dataclasses import dataclass, replace
 from typing import List, Optional
 
 import torch
@@ -189,3 +189,24 @@ def module_case(T: int, H: int = 32, D: int = 128, seed: int = 5, device="cpu") 
     gamma = torch.rand(H, D, generator=g, device=device) + 0.5
     cu = torch.tensor([0, T], dtype=torch.int32)
     return ModuleCase(xq, xk, xv, w.contiguous(), a.contiguous(), b, gamma.contiguous(), cu)
+
+
+def head_slice(case, h0: int, h1: int):
+    """The same inputs restricted to heads [h0, h1): one rank's share when a prompt's
+    heads are split over ranks.  Works on PrefillCase, DecodeCase and ModuleCase; every
+    sliced tensor is made contiguous (the kernels take packed [.., H, ..] layouts)."""
+    def cut(x, dim):
+        return None if x is None else x.narrow(dim, h0, h1 - h0).contiguous()
+
+    if isinstance(case, PrefillCase):
+        return replace(case, name=f"{case.name}_heads{h0}-{h1}", q=cut(case.q, 1), k=cut(case.k, 1),
+                       v=cut(case.v, 1), log_alpha=cut(case.log_alpha, 1), beta=cut(case.beta, 1),
+                       init_state=cut(case.init_state, 1))
+    if isinstance(case, DecodeCase):
+        return DecodeCase(f"{case.name}_heads{h0}-{h1}", cut(case.state, 1),
+                          [{k: cut(v, 1) for k, v in st.items()} for st in case.steps])
+    if isinstance(case, ModuleCase):
+        return replace(case, xq=cut(case.xq, 1), xk=cut(case.xk, 1), xv=cut(case.xv, 1),
+                       conv_w=cut(case.conv_w, 1), a_raw=cut(case.a_raw, 1), b_raw=cut(case.b_raw, 1),
+                       gamma=cut(case.gamma, 0))
+    raise TypeError(f"no head layout known for {type(case).__name__}")
