@@ -15,7 +15,9 @@ With N > 1 ranks (one per GPU), --split chooses what a rank serves:
   replicas (default)  its own prompt and decode batch: weak scaling;
   heads               H / N heads of the one prompt and of the one decode batch:
                       strong scaling.  KDA heads are independent recurrences, so
-                      neither split has a collective on the data path.
+                      neither split has a collective on the data path.  With few
+                      heads per rank the prompt's chunks are split too
+                      (kda_chunk_prefill_segmented; --segments auto|P).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--split replicas|heads]
@@ -368,6 +370,28 @@ def time_other_rows(dev, stream, heads=(0, H), seed_offset=0, steps=10):
                                                           0, decay, stream=stream)], stream, steps)
         lay[name] = {"ms": ms, "tokens_per_s": T_PROMPT / (ms / 1e3)}
     res["layouts"] = lay
+    # one GPU's share of the prompt when 32 heads are split over 8 GPUs: 4 heads, plain
+    # against segmented (the chain of each head is serial, so 4 heads alone leave most
+    # SMs idle)
+    if Hl >= 4:
+        c4 = workloads.head_slice(c, 0, 4)
+        nck = kda.kda_ckpt_count(c4.cu_seqlens, CKPT)
+        o4 = torch.empty(T_PROMPT, 4, D, device=dev, dtype=torch.bfloat16)
+        f4 = torch.empty(1, 4, D, D, device=dev)
+        k4 = torch.empty(nck, 4, D, D, device=dev)
+        p4 = kda.segments_for(4)
+        plain = _median_ms([lambda: kda.kda_chunk_prefill(c4.q, c4.k, c4.v, c4.log_alpha, c4.beta, c4.init_state, cu,
+                                                          c4.cu_seqlens, 1, T_PROMPT, 4, D, D, o4, kda.KDA_OUT_BF16,
+                                                          f4, k4, CKPT, stream)], stream, steps)
+        segd = _median_ms([lambda: kda.kda_chunk_prefill_segmented(c4.q, c4.k, c4.v, c4.log_alpha, c4.beta,
+                                                                   c4.init_state, T_PROMPT, 4, D, D, o4,
+                                                                   kda.KDA_OUT_BF16, f4, k4, CKPT,
+                                                                   kda.KDA_DECAY_CHANNEL, 0, p4, stream=stream)],
+                          stream, steps)
+        res["segmented_4_heads"] = {"plain_ms": plain, "segmented_ms": segd, "segments": p4,
+                                    "tokens_per_s": T_PROMPT / (segd / 1e3),
+                                    "workload": f"prefill T={T_PROMPT} H=4 D={D} ckpt every {CKPT}"}
+        del c4, o4, f4, k4
     del c, out, fin
 
     K = 8
@@ -433,6 +457,8 @@ def main(argv=None):
     ap.add_argument("--no-other", action="store_true", help="skip the varlen, layout and serving-decode rows")
     ap.add_argument("--split", choices=["replicas", "heads"], default="replicas",
                     help="N > 1: each rank serves its own problem (replicas) or H/N heads of one (heads)")
+    ap.add_argument("--segments", default="auto",
+                    help="prefill segments per prompt: auto (fill the GPU when a rank holds few heads) or P")
     args = ap.parse_args(argv)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -471,10 +497,18 @@ def main(argv=None):
     dstate = dc.state
     ds = dc.steps[0]
     dout = torch.empty(DEC_N, Hl, D, device=dev, dtype=torch.bfloat16)
+    seg = kda.segments_for(Hl) if args.segments == "auto" else int(args.segments)
+
+    def prefill_call(q, k, v, la, beta, s0, o, f, cp):
+        if seg > 0:
+            kda.kda_chunk_prefill_segmented(q, k, v, la, beta, s0, T_PROMPT, Hl, D, D, o, kda.KDA_OUT_BF16, f, cp,
+                                            CKPT, kda.KDA_DECAY_CHANNEL, 0, seg, stream=stream)
+        else:
+            kda.kda_chunk_prefill(q, k, v, la, beta, s0, cu_dev, c.cu_seqlens, 1, T_PROMPT, Hl, D, D, o,
+                                  kda.KDA_OUT_BF16, f, cp, CKPT, stream)
 
     def prefill():
-        kda.kda_chunk_prefill(c.q, c.k, c.v, c.log_alpha, c.beta, c.init_state, cu_dev, c.cu_seqlens, 1, T_PROMPT,
-                              Hl, D, D, out, kda.KDA_OUT_BF16, fin, ck, CKPT, stream)
+        prefill_call(c.q, c.k, c.v, c.log_alpha, c.beta, c.init_state, out, fin, ck)
 
     def decode():
         kda.kda_decode_step(ds["q"], ds["k"], ds["v"], ds["log_alpha"], ds["beta"], dstate, dout,
@@ -575,9 +609,7 @@ def main(argv=None):
                 stream.wait_event(ev["in%d" % j])
             stream.wait_event(ev["out"])
             d = bf["d_in"]
-            kda.kda_chunk_prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], bf["s0"], cu_dev,
-                                  c.cu_seqlens, 1, T_PROMPT, Hl, D, D, bf["out"], kda.KDA_OUT_BF16, bf["fin"], bf["ck"],
-                                  CKPT, stream)
+            prefill_call(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], bf["s0"], bf["out"], bf["fin"], bf["ck"])
             ev["comp"].record(stream)
             s_out.wait_event(ev["comp"])
             with torch.cuda.stream(s_out):
@@ -640,7 +672,7 @@ def main(argv=None):
             "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak" if split == "replicas" else "strong", "vs_baseline": None,
             "dtype": "fp16/tf32 MMA, fp32 accumulate + state (bf16 in/out)", "data": "synthetic",
-            "config": bench_config(world, split), "heads_per_rank": Hl,
+            "config": bench_config(world, split), "heads_per_rank": Hl, "segments": seg,
             "prefill_ms": pre_avg, "decode_ms": dec_avg,
             "decode": {"value": dec_gbs * world, "unit": "GB/s", "tokens_per_s": job_rate(DEC_N, world, dec_avg, split),
                        "frac_of_hbm_peak": dec_gbs / hbm},
@@ -652,7 +684,7 @@ def main(argv=None):
             "kv_throughput": {"value": kv_state_bytes(n_ck, Hl) * world / (pre_avg * 1e-3) / 1e9, "unit": "GB/s",
                               "state_bytes_per_prefill": kv_state_bytes(n_ck, Hl),
                               "note": "final state + checkpoints written per prefill / prefill time"},
-            "clocks": clocks, "e2e": e2e, "gpu_launches": 2 * args.steps, "cpu_baseline": cpu,
+            "clocks": clocks, "e2e": e2e, "gpu_launches": (2 if seg == 0 else 6) * args.steps, "cpu_baseline": cpu,
             "module": module, "other": other,
         }
         print(json.dumps(line), flush=True)

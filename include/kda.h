@@ -156,6 +156,66 @@ int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v
                          void* stream);
 
 /*
+ * kda_chunk_prefill_segmented -- one prompt's prefill with its chunks split into
+ * segments that run side by side, for a GPU that holds few heads.
+ *
+ * The result is the prefill of ONE sequence of total_tokens tokens (the arguments and
+ * outputs of kda_chunk_prefill_ex with num_seqs = 1, cu_seqlens = {0, total_tokens}
+ * and start_pos given on the host), computed another way.  Each head's chunks form one
+ * serial chain in kda_chunk_prefill, so a call over few heads leaves most SMs idle and
+ * takes as long as a call over many.  This entry point cuts the prompt, on the
+ * absolute 64-token chunk grid, into up to `segments` runs of equal chunk counts and
+ * uses that the recurrence S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} +
+ * beta_t k_t v_t^T is linear in (S_0, v) (Kimi Linear, "Kimi Delta Attention"): over a
+ * segment, S_end = Phi S_start + B.  Three prefill launches and one small kernel:
+ *   A  segments 0 .. P-2 from zeros (segment 0 from init_state): B_p, and segment 0's
+ *      final state, which is segment 1's initial state;
+ *   B  segments 1 .. P-2 from S_start = I with v = 0: the transitions Phi_p (Dk x Dk);
+ *   chain  S_start[p + 1] = Phi_p S_start[p] + B_p for p = 1 .. P-2, in fp32, serially;
+ *   F  all P segments from their S_start, writing out, the checkpoints and the final
+ *      state.
+ * About 3 - 3/P prefills of work in about 2/P of the serial time: worth it only while
+ * P * H * 4 CTAs fit on the GPU at once (e.g. P = 8 for H = 4 on 152 SMs).  When fewer
+ * than 3 segments result (segments < 3, or a prompt of fewer than 3 chunks), the call
+ * runs as one plain prefill.
+ *   Dk == Dv is required (Phi is carried as a Dk x Dv state), else KDA_ERR_UNSUPPORTED.
+ *   start_pos   absolute position of the prompt's first token (>= 0), as start_pos of
+ *               kda_chunk_prefill_ex: it places the chunk grid and the checkpoints.
+ *   segments    1 .. KDA_MAX_SEGMENTS, else KDA_ERR_INVALID_ARG.
+ *   ckpt_states holds kda_ckpt_count_ex({0, total_tokens}, {start_pos}, 1, ckpt_stride)
+ *               slots, the same checkpoints as the one-sequence kda_chunk_prefill_ex.
+ *   out_norm_gamma / out_norm_eps as in kda_chunk_prefill_ex (applied in run F).
+ * The results equal those of kda_chunk_prefill_ex within rounding, not bit for bit
+ * (S_start is formed through Phi and B instead of by the chain).  Deterministic.
+ * Scratch, stream-ordered from the library's pool on `stream` and given back after the
+ * call: the hand-off rings of each launch, plus (4P + ckpt slots) * H * Dk * Dv * 4
+ * bytes of states and (T_B) * H * Dv * 2 bytes of zero v for run B (T_B = the tokens of
+ * segments 1 .. P-2).  `out` is written by runs A and B before run F overwrites it.
+ * Errors: those of kda_chunk_prefill_ex; a failing launch returns its status and
+ * leaves the outputs unspecified.
+ */
+/*
+ * kda_prefill_clusters_at_once -- how many (sequence, head) pairs of the prefill the
+ * current device runs at the same time (each takes one 4-CTA cluster; the figure comes
+ * from the CUDA occupancy calculator for the kernel's launch shape).  A call over more
+ * pairs runs in waves.  For kda_chunk_prefill_segmented, segments = this / H (when that
+ * is at least 3) keeps the final run to one wave.  Returns the count (> 0) or a negative
+ * kda_status (no sm_103a device: KDA_ERR_UNSUPPORTED).
+ */
+int kda_prefill_clusters_at_once(void);
+
+#define KDA_MAX_SEGMENTS 64
+int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                const float* log_alpha, const uint16_t* beta,
+                                const float* init_state,
+                                int total_tokens, int H, int Dk, int Dv,
+                                void* out, int out_dtype,
+                                float* final_state, float* ckpt_states, int ckpt_stride,
+                                int decay, int start_pos, int segments,
+                                const float* out_norm_gamma, float out_norm_eps,
+                                void* stream);
+
+/*
  * kda_chunk_prefill_noalloc -- kda_chunk_prefill that allocates nothing.
  *
  * The paper has no counterpart for this call: it is an interface variant of this

@@ -14,6 +14,14 @@ constexpr int kStatusRange = -5;
 // 82944-byte blocks.
 constexpr size_t kPrefillRingBytesPerPair = 6 * 82944;
 
+// Segmented prefill: the int32 index arrays of its runs (cu_seqlens and start positions),
+// built on the host and handed to the setup kernel by value.
+constexpr int kSegIdxMax = 512;
+struct SegIdxBuf {
+    int n;
+    int32_t v[kSegIdxMax];
+};
+
 // Bounded waits give up after this many nanoseconds (about one second).
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 

@@ -3,6 +3,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 #include <cuda_runtime.h>
 
 #include "../../include/kda.h"
@@ -22,6 +23,7 @@ int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
                    void* ws, int* ring_flags, int ring_count, int* status, cudaStream_t stream);
 size_t prefill_workspace_bytes(int num_seqs, int H);
 int prefill_ring_count(int num_seqs, int H);
+int prefill_max_active_clusters();
 int launch_prepare_inputs(const uint16_t* xq, const uint16_t* xk, const uint16_t* xv, const float* conv_w,
                           const uint16_t* conv_state, const float* a_raw, const uint16_t* b_raw,
                           const int32_t* cu_seqlens, int num_seqs, int T, int H, int D, int act,
@@ -29,6 +31,9 @@ int launch_prepare_inputs(const uint16_t* xq, const uint16_t* xk, const uint16_t
                           int* status, cudaStream_t stream);
 int launch_output_norm(const void* o, int o_f32, const float* gamma, float eps, uint16_t* y, int T, int H, int D,
                        cudaStream_t stream);
+int launch_segment_setup(const SegIdxBuf& ib, int32_t* idx, float* ident, int n_ident, float* zinit, int n_zinit,
+                         const float* init_state, int H, int D, cudaStream_t stream);
+int launch_segment_chain(const float* phi, float* sst, int P, int H, int D, cudaStream_t stream);
 int launch_decode_multi(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* log_alpha,
                         const uint16_t* beta, float* pool, int num_slots, const int32_t* slots,
                         const int32_t* ntok, int commit, void* out, int out_f32,
@@ -179,6 +184,14 @@ int64_t kda_ckpt_count(const int32_t* cu_seqlens_host, int num_seqs, int ckpt_st
 
 int kda_chunk_size(void) { return 64; }
 
+int kda_prefill_clusters_at_once(void) {
+    int* status = nullptr;
+    const int rc = device_setup(&status);
+    if (rc != KDA_OK) return rc;
+    const int n = kda::prefill_max_active_clusters();
+    return n > 0 ? n : KDA_ERR_CUDA;
+}
+
 const char* kda_status_string(int status) {
     switch (status) {
         case KDA_OK: return "ok";
@@ -254,6 +267,181 @@ int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v
     return prefill_pooled(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host, num_seqs, total_tokens,
                           H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, decay, start_pos,
                           start_pos_host, out_norm_gamma, out_norm_eps, stream);
+}
+
+int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                const float* log_alpha, const uint16_t* beta,
+                                const float* init_state,
+                                int total_tokens, int H, int Dk, int Dv,
+                                void* out, int out_dtype,
+                                float* final_state, float* ckpt_states, int ckpt_stride,
+                                int decay, int start_pos, int segments,
+                                const float* out_norm_gamma, float out_norm_eps, void* stream) {
+    if (segments < 1 || segments > KDA_MAX_SEGMENTS || start_pos < 0 || total_tokens < 0) return KDA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(start_pos) + total_tokens > INT32_MAX) return KDA_ERR_INVALID_ARG;
+    const int32_t cu1[2] = {0, total_tokens};
+    // (the one-sequence checks of the plain call; cu1 stands in for the device cu_seqlens,
+    // which this entry point builds itself)
+    int rc = check_prefill_args(q, k, v, log_alpha, beta, init_state, cu1, cu1, 1, total_tokens, H, Dk, Dv, out,
+                                out_dtype, final_state, ckpt_states, ckpt_stride, decay);
+    if (rc != KDA_OK) return rc;
+    if (Dk != Dv) return KDA_ERR_UNSUPPORTED;
+    if (out_norm_gamma && (!aligned16(out_norm_gamma) || !(out_norm_eps >= 0.f) || !(out_norm_eps < 3.0e38f)))
+        return KDA_ERR_INVALID_ARG;
+
+    // segment bounds on the absolute chunk grid: equal chunk counts, the last one shorter
+    const int C = 64;
+    const int64_t s0 = start_pos, T = total_tokens;
+    const int64_t c_first = s0 / C, c_end = (s0 + T + C - 1) / C;
+    const int64_t n_chunks = T > 0 ? c_end - c_first : 0;
+    int P = 1;
+    int64_t per = n_chunks;
+    if (segments >= 3 && n_chunks >= 3) {
+        per = (n_chunks + segments - 1) / segments;
+        P = static_cast<int>((n_chunks + per - 1) / per);
+        if (P < 3) P = 1;
+    }
+    std::vector<int32_t> b(P + 1);
+    for (int p = 0; p <= P; ++p) {
+        const int64_t x = C * (c_first + p * per) - s0;
+        b[p] = static_cast<int32_t>(x < 0 ? 0 : (x > T ? T : x));
+    }
+    b[0] = 0;
+    b[P] = total_tokens;
+
+    // run B starts on a token index that keeps every per-token row 16-byte aligned (beta
+    // and per-head log-decay rows are H * 2 and H * 4 bytes): a short leading sequence
+    // fills the gap up to segment 1 and its result is ignored
+    const int32_t b1a = P >= 3 ? (b[1] & ~7) : 0;
+    const int lead = (P >= 3 && b1a < b[1]) ? 1 : 0;
+    const int nA = P >= 3 ? P - 1 : 0, nB = P >= 3 ? P - 2 + lead : 0;
+
+    // host index arrays: run A, run B, run F (cu_seqlens, start positions)
+    std::vector<int32_t> a_cu, a_sp, b_cu, b_sp, f_cu, f_sp;
+    for (int p = 0; p <= nA; ++p) a_cu.push_back(b[p]);
+    for (int p = 0; p < nA; ++p) a_sp.push_back(start_pos + b[p]);
+    if (nB > 0) {
+        b_cu.push_back(0);
+        if (lead) { b_cu.push_back(b[1] - b1a); b_sp.push_back(start_pos + b1a); }
+        for (int p = 1; p <= P - 2; ++p) { b_cu.push_back(b[p + 1] - b1a); b_sp.push_back(start_pos + b[p]); }
+    }
+    for (int p = 0; p <= P; ++p) f_cu.push_back(b[p]);
+    for (int p = 0; p < P; ++p) f_sp.push_back(start_pos + b[p]);
+    kda::SegIdxBuf ib;
+    ib.n = 0;
+    int o_acu = 0, o_asp = 0, o_bcu = 0, o_bsp = 0, o_fcu = 0, o_fsp = 0;
+    auto put = [&](const std::vector<int32_t>& x, int* off) {
+        *off = ib.n;
+        for (int32_t e : x) ib.v[ib.n++] = e;
+    };
+    put(a_cu, &o_acu); put(a_sp, &o_asp); put(b_cu, &o_bcu); put(b_sp, &o_bsp); put(f_cu, &o_fcu); put(f_sp, &o_fsp);
+    if (ib.n > kda::kSegIdxMax) return KDA_ERR_INVALID_ARG;
+
+    // checkpoints of run F, and which of them are the prompt's own (the segment ends that
+    // are neither a stride multiple nor the prompt's end are extra)
+    std::vector<int> keep;
+    int64_t n_ck_f = 0;
+    if (ckpt_states && P >= 3) {
+        for (int p = 0; p < P; ++p) {
+            const int64_t a = s0 + b[p], e = s0 + b[p + 1];
+            for (int64_t m = (a / ckpt_stride + 1) * ckpt_stride; m < e; m += ckpt_stride) keep.push_back(n_ck_f++);
+            if (e % ckpt_stride == 0 || p == P - 1) keep.push_back(static_cast<int>(n_ck_f));
+            ++n_ck_f;
+        }
+        const int32_t sp1[1] = {start_pos};
+        if (static_cast<int64_t>(keep.size()) != kda_ckpt_count_ex(cu1, sp1, 1, ckpt_stride)) return KDA_ERR_INVALID_ARG;
+    }
+
+    int* status = nullptr;
+    rc = device_setup(&status);
+    if (rc != KDA_OK) return rc;
+    cudaMemPool_t pool = nullptr;
+    rc = workspace_pool(&pool);
+    if (rc != KDA_OK) return rc;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    // scratch: index arrays | run A initial states | run B identities | Phi | S_start |
+    // run F final states | run F checkpoints | zero v of run B
+    const size_t slot = static_cast<size_t>(H) * Dk * Dv * sizeof(float);
+    const bool zinit_needed = P >= 3 && init_state != nullptr;
+    const int64_t tB = P >= 3 ? static_cast<int64_t>(b[P - 1]) - b1a : 0;
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const size_t o_idx = 0;
+    const size_t o_zin = o_idx + up(sizeof(int32_t) * ib.n);
+    const size_t o_idn = o_zin + (zinit_needed ? slot * nA : 0);
+    const size_t o_phi = o_idn + slot * nB;
+    const size_t o_sst = o_phi + slot * nB;
+    const size_t o_fin = o_sst + (P >= 3 ? slot * P : 0);
+    const size_t o_ck = o_fin + (P >= 3 ? slot * P : 0);
+    const size_t o_zv = o_ck + slot * static_cast<size_t>(n_ck_f);
+    const size_t total = o_zv + up(static_cast<size_t>(tB) * H * Dv * 2);
+    uint8_t* ws = nullptr;
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), total, pool, st) != cudaSuccess) return KDA_ERR_CUDA;
+    int32_t* idx = reinterpret_cast<int32_t*>(ws + o_idx);
+    float* zin = reinterpret_cast<float*>(ws + o_zin);
+    float* idn = reinterpret_cast<float*>(ws + o_idn);
+    float* phi = reinterpret_cast<float*>(ws + o_phi);
+    float* sst = reinterpret_cast<float*>(ws + o_sst);
+    float* fin = reinterpret_cast<float*>(ws + o_fin);
+    float* ck = reinterpret_cast<float*>(ws + o_ck);
+    uint16_t* zv = reinterpret_cast<uint16_t*>(ws + o_zv);
+
+    auto finish = [&](int r) {
+        const bool freed = cudaFreeAsync(ws, st) == cudaSuccess;
+        return r != KDA_OK ? r : (freed ? KDA_OK : KDA_ERR_CUDA);
+    };
+    if (kda::launch_segment_setup(ib, idx, idn, nB, zin, zinit_needed ? nA : 0, init_state, H, Dk, st) != 0)
+        return finish(KDA_ERR_CUDA);
+    if (P < 3)   // one plain prefill
+        return finish(prefill_pooled(q, k, v, log_alpha, beta, init_state, idx + o_fcu, f_cu.data(), 1, total_tokens,
+                                     H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, decay,
+                                     idx + o_fsp, f_sp.data(), out_norm_gamma, out_norm_eps, stream));
+
+    if (tB > 0 && cudaMemsetAsync(zv, 0, static_cast<size_t>(tB) * H * Dv * 2, st) != cudaSuccess)
+        return finish(KDA_ERR_CUDA);
+    // A: segments 0 .. P-2; segment 0's final state lands in S_start[1], B_p in S_start[p + 1]
+    rc = prefill_pooled(q, k, v, log_alpha, beta, zinit_needed ? zin : nullptr, idx + o_acu, a_cu.data(), nA,
+                        b[P - 1], H, Dk, Dv, out, out_dtype, sst + slot / sizeof(float), nullptr, 0, decay,
+                        idx + o_asp, a_sp.data(), nullptr, 0.f, stream);
+    if (rc != KDA_OK) return finish(rc);
+    // B: from S_start = I with v = 0, tokens from b1a on (the leading sequence, if any, first)
+    {
+        const size_t tok = static_cast<size_t>(b1a) * H;
+        const size_t la_row = decay == KDA_DECAY_CHANNEL ? static_cast<size_t>(Dk) : 1;
+        const size_t osz = out_dtype == KDA_OUT_F32 ? 4 : 2;
+        rc = prefill_pooled(q + tok * Dk, k + tok * Dk, zv, log_alpha ? log_alpha + tok * la_row : nullptr,
+                            beta + tok, idn, idx + o_bcu, b_cu.data(), nB, static_cast<int>(tB), H, Dk, Dv,
+                            static_cast<uint8_t*>(out) + tok * Dv * osz, out_dtype, phi, nullptr, 0, decay,
+                            idx + o_bsp, b_sp.data(), nullptr, 0.f, stream);
+        if (rc != KDA_OK) return finish(rc);
+    }
+    // chain: S_start[p + 1] = Phi_p S_start[p] + B_p, p = 1 .. P-2 (Phi_p in slot p - 1 + lead)
+    if (kda::launch_segment_chain(phi + static_cast<size_t>(lead) * (slot / sizeof(float)), sst, P, H, Dk, st) != 0)
+        return finish(KDA_ERR_CUDA);
+    // S_start[0] = the prompt's initial state
+    const cudaError_t e0 = init_state ? cudaMemcpyAsync(sst, init_state, slot, cudaMemcpyDeviceToDevice, st)
+                                      : cudaMemsetAsync(sst, 0, slot, st);
+    if (e0 != cudaSuccess) return finish(KDA_ERR_CUDA);
+    // F: every segment from its S_start
+    rc = prefill_pooled(q, k, v, log_alpha, beta, sst, idx + o_fcu, f_cu.data(), P, total_tokens, H, Dk, Dv, out,
+                        out_dtype, fin, ckpt_states ? ck : nullptr, ckpt_states ? ckpt_stride : 0, decay,
+                        idx + o_fsp, f_sp.data(), out_norm_gamma, out_norm_eps, stream);
+    if (rc != KDA_OK) return finish(rc);
+    if (final_state &&
+        cudaMemcpyAsync(final_state, fin + static_cast<size_t>(P - 1) * (slot / sizeof(float)), slot,
+                        cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        return finish(KDA_ERR_CUDA);
+    // the prompt's checkpoints, in order: runs of consecutive kept slots, one copy each
+    for (size_t i = 0, u = 0; i < keep.size();) {
+        size_t j = i + 1;
+        while (j < keep.size() && keep[j] == keep[j - 1] + 1) ++j;
+        if (cudaMemcpyAsync(ckpt_states + u * (slot / sizeof(float)), ck + static_cast<size_t>(keep[i]) * (slot / sizeof(float)),
+                            (j - i) * slot, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+            return finish(KDA_ERR_CUDA);
+        u += j - i;
+        i = j;
+    }
+    return finish(KDA_OK);
 }
 
 int kda_chunk_prefill_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t* v,

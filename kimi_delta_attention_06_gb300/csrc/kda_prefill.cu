@@ -1295,6 +1295,29 @@ int prefill_ring_count(int num_seqs, int H) {
     return static_cast<int>(clusters < resident ? clusters : (resident > 0 ? resident : 1));
 }
 
+// How many of the prefill's clusters (one per sequence and head) the current device holds
+// at once, from the occupancy calculator for the kernel's own launch shape.
+int prefill_max_active_clusters() {
+    using namespace prefill;
+    void (*kern)(const Params, const TensorMaps) = kda_prefill_kernel<DECAY_CHANNEL>;
+    static bool attr_done[kMaxDevicesAttr] = {};
+    if (!raise_smem_limit(reinterpret_cast<const void*>(kern), static_cast<int>(SMEM_BYTES), attr_done)) return -1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CLUSTER, 1, 1);
+    cfg.blockDim = dim3(NT, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kern), &cfg) != cudaSuccess) return -1;
+    return n;
+}
+
 int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* la,
                    const uint16_t* beta, const float* init_state, const int32_t* cu_seqlens,
                    int num_seqs, int total_tokens, int H, int Dk, int Dv, void* out, int out_f32,

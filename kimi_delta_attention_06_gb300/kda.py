@@ -35,6 +35,7 @@ KDA_ERR_RANGE = -5
 KDA_OUT_BF16 = 0
 KDA_OUT_F32 = 1
 KDA_NOALLOC_MAX_SEQ_HEADS = 32
+KDA_MAX_SEGMENTS = 64
 KDA_DECAY_CHANNEL = 0
 KDA_DECAY_HEAD = 1
 KDA_DECAY_NONE = 2
@@ -69,6 +70,11 @@ def load():
             lib.kda_chunk_prefill_ex.restype = _i
             lib.kda_chunk_prefill_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i,
                                                  _vp, _vp, _i, _i, _vp, _vp, _vp, ctypes.c_float, _vp]
+            lib.kda_chunk_prefill_segmented.restype = _i
+            lib.kda_chunk_prefill_segmented.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _i,
+                                                        _vp, _vp, _i, _i, _i, _i, _vp, ctypes.c_float, _vp]
+            lib.kda_prefill_clusters_at_once.restype = _i
+            lib.kda_prefill_clusters_at_once.argtypes = []
             lib.kda_decode_step.restype = _i
             lib.kda_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]
             lib.kda_decode_multi.restype = _i
@@ -184,6 +190,32 @@ def kda_chunk_prefill_ex(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_se
     _check(rc, "kda_chunk_prefill_ex")
 
 
+def kda_chunk_prefill_segmented(q, k, v, log_alpha, beta, init_state, total_tokens: int, H: int, Dk: int, Dv: int,
+                                out, out_dtype: int, final_state, ckpt_states, ckpt_stride: int, decay: int,
+                                start_pos: int, segments: int, out_norm_gamma=None, out_norm_eps: float = 1e-6,
+                                stream=None):
+    rc = load().kda_chunk_prefill_segmented(
+        _ptr(_bits16(q)), _ptr(_bits16(k)), _ptr(_bits16(v)), _ptr(log_alpha), _ptr(_bits16(beta)),
+        _ptr(init_state), int(total_tokens), int(H), int(Dk), int(Dv),
+        _ptr(out), int(out_dtype), _ptr(final_state), _ptr(ckpt_states), int(ckpt_stride), int(decay),
+        int(start_pos), int(segments), _ptr(out_norm_gamma), float(out_norm_eps), _stream(stream))
+    _check(rc, "kda_chunk_prefill_segmented")
+
+
+def kda_prefill_clusters_at_once() -> int:
+    n = load().kda_prefill_clusters_at_once()
+    _check(min(n, 0), "kda_prefill_clusters_at_once")
+    return int(n)
+
+
+def segments_for(H: int, clusters_at_once: Optional[int] = None) -> int:
+    """Segments for kda_chunk_prefill_segmented that fill the device in one wave of the final
+    run (clusters_at_once // H), or 0 (a plain prefill) when that is below 3."""
+    n = kda_prefill_clusters_at_once() if clusters_at_once is None else int(clusters_at_once)
+    p = min(n // max(1, int(H)), KDA_MAX_SEGMENTS)
+    return p if p >= 3 else 0
+
+
 def kda_chunk_prefill_noalloc(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host,
                               num_seqs: int, total_tokens: int, H: int, Dk: int, Dv: int,
                               out, out_dtype: int, final_state, ckpt_states, ckpt_stride: int, stream=None):
@@ -241,9 +273,11 @@ def kda_device_status(stream=None) -> int:
 
 def prefill(q, k, v, log_alpha, beta, cu_seqlens_host, init_state=None, ckpt_stride: int = 0,
             out_dtype=torch.bfloat16, want_final: bool = True, cu_seqlens=None, stream=None,
-            decay: int = KDA_DECAY_CHANNEL, start_pos_host=None, norm_gamma=None, norm_eps: float = 1e-6):
+            decay: int = KDA_DECAY_CHANNEL, start_pos_host=None, norm_gamma=None, norm_eps: float = 1e-6,
+            segments: int = 0):
     """Allocate outputs and run kda_chunk_prefill (kda_chunk_prefill_ex for another decay
-    layout, for start positions or with the output norm fused in: norm_gamma [H, Dv]).
+    layout, for start positions or with the output norm fused in: norm_gamma [H, Dv];
+    kda_chunk_prefill_segmented when segments > 0, for one sequence).
     Returns (out, final_state, ckpt_states)."""
     T, H, Dk = q.shape
     Dv = v.shape[2]
@@ -257,7 +291,14 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens_host, init_state=None, ckpt_str
     nck = kda_ckpt_count_ex(cu_host, start_pos_host, ckpt_stride) if ckpt_stride > 0 else 0
     ck = torch.empty(nck, H, Dk, Dv, device=dev, dtype=torch.float32) if ckpt_stride > 0 else None
     odt = KDA_OUT_F32 if out_dtype == torch.float32 else KDA_OUT_BF16
-    if decay == KDA_DECAY_CHANNEL and start_pos_host is None and norm_gamma is None:
+    if segments > 0:
+        if N != 1:
+            raise ValueError("the segmented prefill takes one sequence")
+        sp0 = 0 if start_pos_host is None else int(torch.as_tensor(start_pos_host).reshape(-1)[0])
+        kda_chunk_prefill_segmented(q, k, v, log_alpha, beta, init_state, T, H, Dk, Dv, out, odt, fin,
+                                    ck if nck > 0 else None, ckpt_stride, decay, sp0, segments, norm_gamma,
+                                    norm_eps, stream)
+    elif decay == KDA_DECAY_CHANNEL and start_pos_host is None and norm_gamma is None:
         kda_chunk_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_host, N, T, H, Dk, Dv,
                           out, odt, fin, ck if nck > 0 else None, ckpt_stride, stream)
     else:

@@ -2,7 +2,8 @@
 
   python -m kimi_delta_attention_06_gb300.run_case --what prefill --T 8192 [--H 32] [--D 128] [--reps 2]
   python -m kimi_delta_attention_06_gb300.run_case --what varlen [--H 32] [--D 128] [--reps 2]
-      (prefill / varlen also take --decay channel|head|none: KDA, Gated DeltaNet, DeltaNet)
+      (prefill / varlen also take --decay channel|head|none: KDA, Gated DeltaNet, DeltaNet;
+       prefill --segments P runs kda_chunk_prefill_segmented with P segments)
   python -m kimi_delta_attention_06_gb300.run_case --what decode --N 512 [--H 32] [--D 128] [--reps 2]
   python -m kimi_delta_attention_06_gb300.run_case --what decode_multi --N 512 --K 4 [--commit 1] [--reps 2]
   python -m kimi_delta_attention_06_gb300.run_case --what prep --T 145408 [--reps 2]     (input preparation)
@@ -36,6 +37,7 @@ def main(argv=None):
     ap.add_argument("--D", type=int, default=128)
     ap.add_argument("--ckpt", type=int, default=32768)
     ap.add_argument("--reps", type=int, default=2)
+    ap.add_argument("--segments", type=int, default=0, help="prefill: segments of kda_chunk_prefill_segmented")
     a = ap.parse_args(argv)
     build.build()
     dev = torch.device("cuda", 0)
@@ -56,10 +58,15 @@ def main(argv=None):
         ck = torch.empty(max(nck, 1), a.H, a.D, a.D, device=dev)
 
         def run():
-            kda.kda_chunk_prefill_ex(c.q, c.k, c.v, la, c.beta, c.init_state, cu, c.cu_seqlens, N, T, a.H, a.D,
-                                     a.D, out, kda.KDA_OUT_BF16, fin, ck if nck else None, a.ckpt, decay,
-                                     stream=stream)
-        units, count = f"{T} tokens, {N} sequences, decay {a.decay}", T
+            if a.segments > 0 and a.what == "prefill":
+                kda.kda_chunk_prefill_segmented(c.q, c.k, c.v, la, c.beta, c.init_state, T, a.H, a.D, a.D, out,
+                                                kda.KDA_OUT_BF16, fin, ck if nck else None, a.ckpt, decay, 0,
+                                                a.segments, stream=stream)
+            else:
+                kda.kda_chunk_prefill_ex(c.q, c.k, c.v, la, c.beta, c.init_state, cu, c.cu_seqlens, N, T, a.H,
+                                         a.D, a.D, out, kda.KDA_OUT_BF16, fin, ck if nck else None, a.ckpt, decay,
+                                         stream=stream)
+        units, count = f"{T} tokens, {N} sequences, decay {a.decay}, segments {a.segments}", T
     elif a.what in ("prep", "outnorm"):
         g = torch.Generator(device=dev).manual_seed(6)
         T, H, D = a.T, a.H, a.D

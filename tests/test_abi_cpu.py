@@ -34,7 +34,8 @@ def test_header_declares_expected_entry_points():
     names = _declared_functions()
     for n in ["kda_chunk_prefill", "kda_chunk_prefill_noalloc", "kda_decode_step", "kda_decode_multi", "kda_ckpt_count",
               "kda_chunk_prefill_ex", "kda_ckpt_count_ex", "kda_prepare_inputs", "kda_output_norm",
-              "kda_device_status", "kda_status_string", "kda_chunk_size", "kda_debug_expire_wait"]:
+              "kda_device_status", "kda_status_string", "kda_chunk_size", "kda_debug_expire_wait",
+              "kda_chunk_prefill_segmented"]:
         assert n in names
 
 
@@ -166,6 +167,34 @@ def test_prefill_ex_decay_rules_on_host(lib):
     assert raw(kda.KDA_DECAY_CHANNEL, gamma=0xA000, eps=-1.0) == kda.KDA_ERR_INVALID_ARG
     assert raw(kda.KDA_DECAY_CHANNEL, gamma=0xA000, eps=float("nan")) == kda.KDA_ERR_INVALID_ARG
     assert raw(kda.KDA_DECAY_CHANNEL, gamma=0xA000, eps=float("inf")) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_segmented_prefill_rejects_on_host(lib):
+    f = lib.kda_chunk_prefill_segmented
+
+    def raw(**over):
+        a = dict(q=0x1000, k=0x2000, v=0x3000, la=0x4000, beta=0x5000, s0=None, T=1000, H=4, Dk=128, Dv=128,
+                 out=0x7000, out_dtype=0, fin=None, ck=None, stride=0, decay=kda.KDA_DECAY_CHANNEL, sp=0, P=8,
+                 gamma=None, eps=1e-6, stream=None)
+        a.update(over)
+        return f(a["q"], a["k"], a["v"], a["la"], a["beta"], a["s0"], a["T"], a["H"], a["Dk"], a["Dv"], a["out"],
+                 a["out_dtype"], a["fin"], a["ck"], a["stride"], a["decay"], a["sp"], a["P"], a["gamma"], a["eps"],
+                 a["stream"])
+    assert raw(P=0) == kda.KDA_ERR_INVALID_ARG
+    assert raw(P=65) == kda.KDA_ERR_INVALID_ARG                        # at most KDA_MAX_SEGMENTS
+    assert raw(sp=-1) == kda.KDA_ERR_INVALID_ARG
+    assert raw(sp=2 ** 31 - 10) == kda.KDA_ERR_INVALID_ARG             # positions past int32
+    assert raw(T=-1) == kda.KDA_ERR_INVALID_ARG
+    assert raw(Dv=64) == kda.KDA_ERR_UNSUPPORTED                       # Phi is carried as a Dk x Dv state
+    assert raw(Dk=96, Dv=96) == kda.KDA_ERR_UNSUPPORTED
+    assert raw(q=None) == kda.KDA_ERR_INVALID_ARG
+    assert raw(q=0x1008) == kda.KDA_ERR_INVALID_ARG                    # 16-byte alignment
+    assert raw(decay=kda.KDA_DECAY_NONE) == kda.KDA_ERR_INVALID_ARG    # log_alpha given but unused
+    assert raw(decay=kda.KDA_DECAY_HEAD, H=6) == kda.KDA_ERR_UNSUPPORTED
+    assert raw(ck=0x8000, stride=0) == kda.KDA_ERR_INVALID_ARG
+    assert raw(stride=100) == kda.KDA_ERR_INVALID_ARG                   # multiple of 64
+    assert raw(gamma=0xA004) == kda.KDA_ERR_INVALID_ARG
+    assert raw(gamma=0xA000, eps=float("nan")) == kda.KDA_ERR_INVALID_ARG
 
 
 def test_ckpt_count_with_start_positions(lib):
