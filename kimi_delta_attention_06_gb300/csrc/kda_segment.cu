@@ -34,51 +34,85 @@ __global__ void seg_setup_kernel(SegIdxBuf ib, int32_t* idx, float* ident, int n
         zinit[e] = (e < per && init_state) ? init_state[e] : 0.f;
 }
 
-// Chain the segment results, one CTA per (16-column block, head): the state's columns are
-// independent, so each CTA carries a Dk x 16 slab of S_start through the segments in order.
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+constexpr int kSlab = 4;          // state columns per CTA
+
+// Chain the segment results, one CTA per (4-column block, head): the state's columns are
+// independent, so each CTA carries a D x 4 slab of S_start through the segments in order.
+// Each step's Phi (D x D, contiguous) is copied into shared memory (row pitch D + 4) while
+// the previous step computes; thread (row i, columns 2 (tid & 1) .. +1) forms its two
+// outputs as fp32 dot products over the whole row.
 // phi   [P-2, H, D, D]  transitions of segments 1 .. P-2
 // sst   [P, H, D, D]    slot 1 holds segment 0's final state; slot p + 1 (p = 1 .. P-2) holds
 //                       B_p on entry and S_start[p + 1] = Phi_p S_start[p] + B_p on exit
 // (slot 0, the prompt's own initial state, is not touched)
 __global__ void __launch_bounds__(256) seg_chain_kernel(const float* __restrict__ phi, float* sst, int P, int H,
                                                          int D) {
-    __shared__ __align__(16) float slab[128][16];
-    const int h = blockIdx.y, c0 = 16 * blockIdx.x;
-    const int i = threadIdx.x >> 1, j0 = 8 * (threadIdx.x & 1);     // row, first of 8 columns
+    extern __shared__ __align__(16) float sm[];
+    const int pitch = D + 4;
+    float* slab = sm;                                 // [D][kSlab]
+    float* phis = sm + 128 * kSlab;                   // 2 x [D][pitch]
+    const int h = blockIdx.y, c0 = kSlab * blockIdx.x;
+    const int i = threadIdx.x >> 1, j0 = 2 * (threadIdx.x & 1);
     const size_t per = static_cast<size_t>(H) * D * D;
     const size_t head = static_cast<size_t>(h) * D * D;
+    auto stage = [&](int p) {                         // Phi_p into buffer (p - 1) & 1
+        const float* src = phi + static_cast<size_t>(p - 1) * per + head;
+        float* dst = phis + ((p - 1) & 1) * D * pitch;
+        const int q4 = D / 4;
+        for (int e = threadIdx.x; e < D * q4; e += blockDim.x) {
+            const int r = e / q4, c = 4 * (e % q4);
+            cp_async16(dst + r * pitch + c, src + static_cast<size_t>(r) * D + c);
+        }
+        cp_async_commit();
+    };
     if (i < D) {
         const float* s1 = sst + per + head + static_cast<size_t>(i) * D + c0 + j0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) slab[i][j0 + j] = s1[j];
+        slab[i * kSlab + j0] = s1[0];
+        slab[i * kSlab + j0 + 1] = s1[1];
     }
-    __syncthreads();
+    stage(1);
     for (int p = 1; p <= P - 2; ++p) {
-        float acc[8];
-        float* dst = sst + static_cast<size_t>(p + 1) * per + head + static_cast<size_t>(i) * D + c0 + j0;
+        if (p + 1 <= P - 2) {
+            stage(p + 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();                              // Phi_p and the slab are in place
+        float a0 = 0.f, a1 = 0.f;
+        float* dst = sst + static_cast<size_t>(p + 1) * per + head + static_cast<size_t>(i < D ? i : 0) * D + c0 + j0;
         if (i < D) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] = dst[j];                // B_p
-            const float* row = phi + static_cast<size_t>(p - 1) * per + head + static_cast<size_t>(i) * D;
+            a0 = dst[0];                              // B_p
+            a1 = dst[1];
+            const float* row = phis + ((p - 1) & 1) * D * pitch + i * pitch;
+#pragma unroll 8
             for (int kk = 0; kk < D; kk += 4) {
                 const float4 f = *reinterpret_cast<const float4*>(row + kk);
-                const float fv[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[j] = fmaf(fv[u], slab[kk + u][j0 + j], acc[j]);
-                }
+                const float2 s0 = *reinterpret_cast<const float2*>(slab + (kk + 0) * kSlab + j0);
+                const float2 s1 = *reinterpret_cast<const float2*>(slab + (kk + 1) * kSlab + j0);
+                const float2 s2 = *reinterpret_cast<const float2*>(slab + (kk + 2) * kSlab + j0);
+                const float2 s3 = *reinterpret_cast<const float2*>(slab + (kk + 3) * kSlab + j0);
+                a0 = fmaf(f.x, s0.x, a0); a1 = fmaf(f.x, s0.y, a1);
+                a0 = fmaf(f.y, s1.x, a0); a1 = fmaf(f.y, s1.y, a1);
+                a0 = fmaf(f.z, s2.x, a0); a1 = fmaf(f.z, s2.y, a1);
+                a0 = fmaf(f.w, s3.x, a0); a1 = fmaf(f.w, s3.y, a1);
             }
         }
-        __syncthreads();                                                // every row has read the slab
+        __syncthreads();                              // every row has read the slab and Phi_p
         if (i < D) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                slab[i][j0 + j] = acc[j];
-                dst[j] = acc[j];
-            }
+            slab[i * kSlab + j0] = a0;
+            slab[i * kSlab + j0 + 1] = a1;
+            dst[0] = a0;
+            dst[1] = a1;
         }
-        __syncthreads();
     }
 }
 
@@ -93,8 +127,13 @@ int launch_segment_setup(const SegIdxBuf& ib, int32_t* idx, float* ident, int n_
 
 int launch_segment_chain(const float* phi, float* sst, int P, int H, int D, cudaStream_t stream) {
     if (P < 3 || (D != 64 && D != 128)) return -1;
-    const dim3 grid(D / 16, H);
-    seg_chain_kernel<<<grid, 256, 0, stream>>>(phi, sst, P, H, D);
+    const int smem = static_cast<int>(sizeof(float) * (128 * kSlab + 2 * D * (D + 4)));
+    static bool attr_done[kMaxDevicesAttr] = {};
+    if (!raise_smem_limit(reinterpret_cast<const void*>(seg_chain_kernel), 128 * kSlab * 4 + 2 * 128 * 132 * 4,
+                          attr_done))
+        return -3;
+    const dim3 grid(D / kSlab, H);
+    seg_chain_kernel<<<grid, 256, smem, stream>>>(phi, sst, P, H, D);
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
