@@ -43,6 +43,23 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2_bits(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Two-lane fp32 arithmetic (one instruction, each lane rounded as its scalar form).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)),
+          "l"(*reinterpret_cast<const uint64_t*>(&c)));
+    return *reinterpret_cast<const float2*>(&d);
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)));
+    return *reinterpret_cast<const float2*>(&d);
+}
+
 // Raise a kernel's dynamic shared-memory limit on the current device, once per device
 // (the attribute belongs to the device's copy of the kernel).  `done` holds one flag per
 // device ordinal; setting the attribute twice is harmless, so no lock is needed.

@@ -1011,17 +1011,23 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
         if (p.norm_gamma) {
             // the module's per-head output norm on the fp32 accumulator: y = o / rms(o) * gamma[h];
             // the two warpgroups' column halves of a row meet through shared memory
-            float ss = 0.f;
+            float2 ss2 = make_float2(0.f, 0.f);      // even and odd columns, two lanes at a time
 #pragma unroll
-            for (int q = 0; q < 64; ++q) ss = fmaf(a[q], a[q], ss);
-            s_ss[64 * wg + t] = ss;
+            for (int q = 0; q < 64; q += 2) {
+                const float2 x = make_float2(a[q], a[q + 1]);
+                ss2 = ffma2(x, x, ss2);
+            }
+            s_ss[64 * wg + t] = ss2.x + ss2.y;
             tc::named_sync(BAR_NORM, dv == 128 ? 128 : 64);
             const float tot = dv == 128 ? s_ss[t] + s_ss[64 + t] : s_ss[t];
             const float rinv = 1.f / sqrtf(tot / static_cast<float>(dv) + p.norm_eps);
+            const float2 r2 = make_float2(rinv, rinv);
 #pragma unroll
             for (int q = 0; q < 64; q += 4) {
                 const float4 gm = *reinterpret_cast<const float4*>(s_gam + 64 * wg + q);
-                a[q] *= rinv * gm.x; a[q + 1] *= rinv * gm.y; a[q + 2] *= rinv * gm.z; a[q + 3] *= rinv * gm.w;
+                const float2 lo = fmul2(make_float2(a[q], a[q + 1]), fmul2(r2, make_float2(gm.x, gm.y)));
+                const float2 hi = fmul2(make_float2(a[q + 2], a[q + 3]), fmul2(r2, make_float2(gm.z, gm.w)));
+                a[q] = lo.x; a[q + 1] = lo.y; a[q + 2] = hi.x; a[q + 3] = hi.y;
             }
         }
         if (!p.out_f32 && lo == 0 && hi == C) {
@@ -1123,8 +1129,13 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
         {
             float r[64];
             tmem_ld64(lane_base + TM_D3 + cb, r);
+            const float2 g2 = make_float2(gc, gc);
 #pragma unroll
-            for (int j = 0; j < 64; ++j) S[j] = gc * S[j] + r[j];
+            for (int j = 0; j < 64; j += 2) {
+                const float2 u = ffma2(g2, make_float2(S[j], S[j + 1]), make_float2(r[j], r[j + 1]));
+                S[j] = u.x;
+                S[j + 1] = u.y;
+            }
         }
         if (c + 1 < nchunks) write_sb();
         // -- prefix-cache checkpoint at stride multiples and at the sequence end --
