@@ -270,6 +270,13 @@ __device__ __forceinline__ void st_h4(uint8_t* tile, uint32_t row, uint32_t col,
 
 __device__ __forceinline__ float4 f4mul(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
 __device__ __forceinline__ float4 f4add(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
+// f4mul on two-lane fp32 instructions (each lane rounds exactly as the scalar product): faster in
+// the scalar-decay tile build, slower in the per-channel one, where it is not used
+__device__ __forceinline__ float4 f4mul_x2(float4 a, float4 b) {
+    const float2 lo = fmul2(make_float2(a.x, a.y), make_float2(b.x, b.y));
+    const float2 hi = fmul2(make_float2(a.z, a.w), make_float2(b.z, b.w));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
 __device__ __forceinline__ float4 f4ex2(float4 a) { return make_float4(ex2(a.x), ex2(a.y), ex2(a.z), ex2(a.w)); }
 __device__ __forceinline__ float4 bf16x4_to_f4(uint2 w) {
     const float2 a = bf16x2_bits_to_f32(w.x), b = bf16x2_bits_to_f32(w.y);
@@ -617,9 +624,9 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
                                       : make_uint2(0u, 0u);
                 const float4 kv = bf16x4_to_f4(kr), qv = bf16x4_to_f4(qr);
                 const float4 e4 = make_float4(et, et, et, et), c4 = make_float4(ect, ect, ect, ect);
-                st_h4(AH, t, 4 * cg, 128, f4mul(kv, e4));        // K~ = k e^{g_t}
-                st_h4(AH, 64 + t, 4 * cg, 128, f4mul(qv, e4));   // Q~ = q e^{g_t}
-                st_h4(KH, t, 4 * cg, 64, f4mul(kv, c4));         // K^ = k e^{g_C - g_t}
+                st_h4(AH, t, 4 * cg, 128, f4mul_x2(kv, e4));        // K~ = k e^{g_t}
+                st_h4(AH, 64 + t, 4 * cg, 128, f4mul_x2(qv, e4));   // Q~ = q e^{g_t}
+                st_h4(KH, t, 4 * cg, 64, f4mul_x2(kv, c4));         // K^ = k e^{g_C - g_t}
             }
         }
         }
