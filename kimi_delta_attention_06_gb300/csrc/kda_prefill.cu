@@ -325,6 +325,13 @@ __device__ __forceinline__ void ldsm_b_sw(const uint8_t* tile, uint32_t rows, in
     asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
                  : "=r"(b[0]), "=r"(b[1]) : "r"(tc::smem_u32(ptr)));
 }
+// ... with a scale per column (s0 for the even column of each pair, s1 for the odd one)
+__device__ __forceinline__ void st_frag_sw_sc(uint8_t* tile, uint32_t rows, int r0, int n0, const float (&d)[4],
+                                              float s0, float s1) {
+    const int l = threadIdx.x & 31, g = l >> 2, t = l & 3;
+    *reinterpret_cast<__half2*>(tile + tc::sw128_off16(r0 + g, n0 + 2 * t, rows)) = __floats2half2_rn(s0 * d[0], s1 * d[1]);
+    *reinterpret_cast<__half2*>(tile + tc::sw128_off16(r0 + g + 8, n0 + 2 * t, rows)) = __floats2half2_rn(s0 * d[2], s1 * d[3]);
+}
 __device__ __forceinline__ void st_frag_sw(uint8_t* tile, uint32_t rows, int r0, int n0, const float (&d)[4]) {
     const int l = threadIdx.x & 31, g = l >> 2, t = l & 3;
     *reinterpret_cast<__half2*>(tile + tc::sw128_off16(r0 + g, n0 + 2 * t, rows)) = __floats2half2_rn(d[0], d[1]);
@@ -411,6 +418,8 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
     if (warp == 0) tc::tmem_alloc(s_tmem, TM_PREP_COLS);
     for (int i = tid; i < 64 * LH / 8; i += NT)            // T scratch: its upper blocks stay zero
         reinterpret_cast<uint4*>(Th)[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = tid; i < 64 * 128 / 16; i += NT)          // rows 0..63 of [T; Mqk] (T diag(beta)): the
+        reinterpret_cast<uint4*>(Qt)[i] = make_uint4(0u, 0u, 0u, 0u);   // blocks above the diagonal stay zero
     cta_sync_tc();
     const uint32_t tm = *s_tmem;
     const uint32_t lane_base = tm + (static_cast<uint32_t>((warp & 3) * 32) << 16);
@@ -749,6 +758,22 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             for (int r = 0; r < 16; ++r) Th[(16 * bb + r) * LH + 16 * bb + cc] = __float2half_rn(sv[r]);
         }
         tc::named_sync(BAR_ALL, NT);
+        if (warp >= 2 && tid < 64 + 128) {
+            // meanwhile, T diag(beta) of the diagonal blocks into rows 0..63 of [T; Mqk]:
+            // thread -> (block, row, 8 columns); the blocks below the diagonal get theirs from
+            // the fp32 products that form them
+            const int u = tid - 64, bb = u >> 5, row = 16 * bb + ((u >> 1) & 15), c0 = 16 * bb + 8 * (u & 1);
+            const uint4 w = *reinterpret_cast<const uint4*>(Th + row * LH + c0);
+            const float4 b0 = *reinterpret_cast<const float4*>(s_beta + c0);
+            const float4 b1 = *reinterpret_cast<const float4*>(s_beta + c0 + 4);
+            const float2 h0 = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+            const float2 h1 = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+            const float2 h2 = __half22float2(*reinterpret_cast<const __half2*>(&w.z));
+            const float2 h3 = __half22float2(*reinterpret_cast<const __half2*>(&w.w));
+            const float tb[8] = {h0.x * b0.x, h0.y * b0.y, h1.x * b0.z, h1.y * b0.w,
+                                 h2.x * b1.x, h2.y * b1.y, h3.x * b1.z, h3.y * b1.w};
+            st_h8(Qt, row, c0, 128, tb);
+        }
         if (warp < 2) {           // 16 -> 32: warp 0 merges blocks (1,0), warp 1 blocks (3,2)
             const int R = 16 * (2 * warp + 1), Cc = 16 * (2 * warp);
             __half* Yw = Yh + warp * 16 * LH;
@@ -769,6 +794,8 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
                 ldsm_b(Yw, LH, 0, 8 * nt, b);
                 mma16816(acc, a, b);
                 st_frag(Th, LH, R, Cc + 8 * nt, acc, -1.f);
+                const int cb = Cc + 8 * nt + 2 * (lane & 3);
+                st_frag_sw_sc(Qt, 128, R, Cc + 8 * nt, acc, -s_beta[cb], -s_beta[cb + 1]);
             }
         }
         tc::named_sync(BAR_ALL, NT);
@@ -792,27 +819,8 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
                 mma16816(acc2, a, b);
             }
             st_frag(Th, LH, 32 + 16 * m, 8 * nn, acc2, -1.f);
-        }
-        tc::named_sync(BAR_ALL, NT);
-        {   // T diag(beta) -> rows 0..63 of [T; Mqk]: thread -> (row, 16 columns)
-            const int t = tid >> 2, c0 = (tid & 3) * 16;
-            float tb[16];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const uint4 w = *reinterpret_cast<const uint4*>(Th + t * LH + c0 + 8 * q);
-                const float4 b0 = *reinterpret_cast<const float4*>(s_beta + c0 + 8 * q);
-                const float4 b1 = *reinterpret_cast<const float4*>(s_beta + c0 + 8 * q + 4);
-                const float2 h0 = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
-                const float2 h1 = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
-                const float2 h2 = __half22float2(*reinterpret_cast<const __half2*>(&w.z));
-                const float2 h3 = __half22float2(*reinterpret_cast<const __half2*>(&w.w));
-                tb[8 * q + 0] = h0.x * b0.x; tb[8 * q + 1] = h0.y * b0.y;
-                tb[8 * q + 2] = h1.x * b0.z; tb[8 * q + 3] = h1.y * b0.w;
-                tb[8 * q + 4] = h2.x * b1.x; tb[8 * q + 5] = h2.y * b1.y;
-                tb[8 * q + 6] = h3.x * b1.z; tb[8 * q + 7] = h3.y * b1.w;
-            }
-            st_h8(Qt, t, c0, 128, tb);
-            st_h8(Qt, t, c0 + 8, 128, tb + 8);
+            const int cb = 8 * nn + 2 * (lane & 3);
+            st_frag_sw_sc(Qt, 128, 32 + 16 * m, 8 * nn, acc2, -s_beta[cb], -s_beta[cb + 1]);
         }
         tc::named_sync(BAR_ALL, NT);
         // -- 5. Mqk = A T diag(beta) on warp MMAs, into rows 64..127 of [T; Mqk] --
