@@ -188,9 +188,11 @@ int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v
  * The results equal those of kda_chunk_prefill_ex within rounding, not bit for bit
  * (S_start is formed through Phi and B instead of by the chain).  Deterministic.
  * Scratch, stream-ordered from the library's pool on `stream` and given back after the
- * call: the hand-off rings of each launch, plus (4P + ckpt slots) * H * Dk * Dv * 4
- * bytes of states and (T_B) * H * Dv * 2 bytes of zero v for run B (T_B = the tokens of
- * segments 1 .. P-2).  `out` is written by runs A and B before run F overwrites it.
+ * call: the hand-off rings of each launch, at most (5P + C_F) * H * Dk * Dv * 4 bytes
+ * of states (C_F = run F's checkpoint slots: the prompt's own plus one per segment end)
+ * and T_B * H * Dv * 2 bytes of zero v for run B (T_B = the tokens of segments 1 .. P-2
+ * and at most 7 before them).  `out` is written by runs A and B before run F
+ * overwrites it.
  * Errors: those of kda_chunk_prefill_ex; a failing launch returns its status and
  * leaves the outputs unspecified.
  */
