@@ -206,6 +206,25 @@ int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v
  */
 int kda_prefill_clusters_at_once(void);
 
+/*
+ * kda_segment_plan -- the plan kda_chunk_prefill_segmented follows, on the host only.
+ *
+ *   bounds      (host) int32 [KDA_MAX_SEGMENTS + 1]: receives the segment bounds, in tokens
+ *               from the prompt's first token: bounds[0] = 0 < bounds[1] < ... <
+ *               bounds[P] = total_tokens.  Interior bounds sit on the absolute 64-token
+ *               chunk grid (start_pos + bounds[p] is a multiple of 64); every segment but
+ *               the last has the same number of chunks.
+ *   ckpt_slots  (host) int32 [ckpt_slots_cap] or NULL: when ckpt_stride > 0 and P >= 3,
+ *               receives, for each of the prompt's own checkpoints in order, the index of
+ *               the final run's checkpoint slot it is copied from (that run writes one
+ *               more slot at every segment end that is neither a stride multiple nor the
+ *               prompt's end).  Fewer slots than the prompt's checkpoints ->
+ *               KDA_ERR_INVALID_ARG.
+ * Returns P (1 = one plain prefill, else 3 .. segments) or a negative kda_status.
+ */
+int kda_segment_plan(int total_tokens, int start_pos, int segments, int ckpt_stride,
+                     int32_t* bounds, int32_t* ckpt_slots, int ckpt_slots_cap);
+
 #define KDA_MAX_SEGMENTS 64
 int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                 const float* log_alpha, const uint16_t* beta,

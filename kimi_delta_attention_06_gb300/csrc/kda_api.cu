@@ -159,6 +159,61 @@ __global__ void expire_wait_kernel(unsigned long long limit_ns, int* status) {
     }
 }
 
+// The plan of a segmented prefill: the segment bounds on the prompt's absolute 64-token
+// chunk grid (tokens from the prompt's start; equal chunk counts, the last segment
+// shorter; P = 1 when fewer than 3 segments result) and, when ckpt_stride > 0, for each of
+// the prompt's own checkpoints in order, the slot of the final run's checkpoints it comes
+// from (that run also writes one at every segment end).
+struct SegPlan {
+    int P = 1;
+    std::vector<int32_t> b;
+    std::vector<int> keep;
+    int64_t n_ck_f = 0;
+};
+
+int plan_segments(int total_tokens, int start_pos, int segments, int ckpt_stride, SegPlan* out) {
+    if (segments < 1 || segments > KDA_MAX_SEGMENTS || start_pos < 0 || total_tokens < 0) return KDA_ERR_INVALID_ARG;
+    if (ckpt_stride < 0 || ckpt_stride % 64 != 0) return KDA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(start_pos) + total_tokens > INT32_MAX) return KDA_ERR_INVALID_ARG;
+    const int C = 64;
+    const int64_t s0 = start_pos, T = total_tokens;
+    const int64_t c_first = s0 / C, c_end = (s0 + T + C - 1) / C;
+    const int64_t n_chunks = T > 0 ? c_end - c_first : 0;
+    int P = 1;
+    int64_t per = n_chunks;
+    if (segments >= 3 && n_chunks >= 3) {
+        per = (n_chunks + segments - 1) / segments;
+        P = static_cast<int>((n_chunks + per - 1) / per);
+        if (P < 3) P = 1;
+    }
+    std::vector<int32_t> b(P + 1);
+    for (int p = 0; p <= P; ++p) {
+        const int64_t x = C * (c_first + p * per) - s0;
+        b[p] = static_cast<int32_t>(x < 0 ? 0 : (x > T ? T : x));
+    }
+    b[0] = 0;
+    b[P] = total_tokens;
+    std::vector<int> keep;
+    int64_t n_ck_f = 0;
+    if (ckpt_stride > 0 && P >= 3) {
+        for (int p = 0; p < P; ++p) {
+            const int64_t a = s0 + b[p], e = s0 + b[p + 1];
+            for (int64_t m = (a / ckpt_stride + 1) * ckpt_stride; m < e; m += ckpt_stride)
+                keep.push_back(static_cast<int>(n_ck_f++));
+            if (e % ckpt_stride == 0 || p == P - 1) keep.push_back(static_cast<int>(n_ck_f));
+            ++n_ck_f;
+        }
+        const int32_t cu1[2] = {0, total_tokens};
+        const int32_t sp1[1] = {start_pos};
+        if (static_cast<int64_t>(keep.size()) != kda_ckpt_count_ex(cu1, sp1, 1, ckpt_stride)) return KDA_ERR_INVALID_ARG;
+    }
+    out->P = P;
+    out->b = std::move(b);
+    out->keep = std::move(keep);
+    out->n_ck_f = n_ck_f;
+    return KDA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -183,6 +238,19 @@ int64_t kda_ckpt_count(const int32_t* cu_seqlens_host, int num_seqs, int ckpt_st
 }
 
 int kda_chunk_size(void) { return 64; }
+
+int kda_segment_plan(int total_tokens, int start_pos, int segments, int ckpt_stride, int32_t* bounds,
+                     int32_t* ckpt_slots, int ckpt_slots_cap) {
+    if (!bounds) return KDA_ERR_INVALID_ARG;
+    SegPlan plan;
+    const int rc = plan_segments(total_tokens, start_pos, segments, ckpt_stride, &plan);
+    if (rc != KDA_OK) return rc;
+    if (ckpt_slots && static_cast<int64_t>(plan.keep.size()) > ckpt_slots_cap) return KDA_ERR_INVALID_ARG;
+    for (int p = 0; p <= plan.P; ++p) bounds[p] = plan.b[p];
+    if (ckpt_slots)
+        for (size_t i = 0; i < plan.keep.size(); ++i) ckpt_slots[i] = plan.keep[i];
+    return plan.P;
+}
 
 int kda_prefill_clusters_at_once(void) {
     int* status = nullptr;
@@ -289,25 +357,11 @@ int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint
     if (out_norm_gamma && (!aligned16(out_norm_gamma) || !(out_norm_eps >= 0.f) || !(out_norm_eps < 3.0e38f)))
         return KDA_ERR_INVALID_ARG;
 
-    // segment bounds on the absolute chunk grid: equal chunk counts, the last one shorter
-    const int C = 64;
-    const int64_t s0 = start_pos, T = total_tokens;
-    const int64_t c_first = s0 / C, c_end = (s0 + T + C - 1) / C;
-    const int64_t n_chunks = T > 0 ? c_end - c_first : 0;
-    int P = 1;
-    int64_t per = n_chunks;
-    if (segments >= 3 && n_chunks >= 3) {
-        per = (n_chunks + segments - 1) / segments;
-        P = static_cast<int>((n_chunks + per - 1) / per);
-        if (P < 3) P = 1;
-    }
-    std::vector<int32_t> b(P + 1);
-    for (int p = 0; p <= P; ++p) {
-        const int64_t x = C * (c_first + p * per) - s0;
-        b[p] = static_cast<int32_t>(x < 0 ? 0 : (x > T ? T : x));
-    }
-    b[0] = 0;
-    b[P] = total_tokens;
+    SegPlan plan;
+    rc = plan_segments(total_tokens, start_pos, segments, ckpt_states ? ckpt_stride : 0, &plan);
+    if (rc != KDA_OK) return rc;
+    const int P = plan.P;
+    const std::vector<int32_t>& b = plan.b;
 
     // run B starts on a token index that keeps every per-token row 16-byte aligned (beta
     // and per-head log-decay rows are H * 2 and H * 4 bytes): a short leading sequence
@@ -327,6 +381,9 @@ int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint
     }
     for (int p = 0; p <= P; ++p) f_cu.push_back(b[p]);
     for (int p = 0; p < P; ++p) f_sp.push_back(start_pos + b[p]);
+    if (a_cu.size() + a_sp.size() + b_cu.size() + b_sp.size() + f_cu.size() + f_sp.size() >
+        static_cast<size_t>(kda::kSegIdxMax))
+        return KDA_ERR_INVALID_ARG;
     kda::SegIdxBuf ib;
     ib.n = 0;
     int o_acu = 0, o_asp = 0, o_bcu = 0, o_bsp = 0, o_fcu = 0, o_fsp = 0;
@@ -335,22 +392,9 @@ int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint
         for (int32_t e : x) ib.v[ib.n++] = e;
     };
     put(a_cu, &o_acu); put(a_sp, &o_asp); put(b_cu, &o_bcu); put(b_sp, &o_bsp); put(f_cu, &o_fcu); put(f_sp, &o_fsp);
-    if (ib.n > kda::kSegIdxMax) return KDA_ERR_INVALID_ARG;
 
-    // checkpoints of run F, and which of them are the prompt's own (the segment ends that
-    // are neither a stride multiple nor the prompt's end are extra)
-    std::vector<int> keep;
-    int64_t n_ck_f = 0;
-    if (ckpt_states && P >= 3) {
-        for (int p = 0; p < P; ++p) {
-            const int64_t a = s0 + b[p], e = s0 + b[p + 1];
-            for (int64_t m = (a / ckpt_stride + 1) * ckpt_stride; m < e; m += ckpt_stride) keep.push_back(n_ck_f++);
-            if (e % ckpt_stride == 0 || p == P - 1) keep.push_back(static_cast<int>(n_ck_f));
-            ++n_ck_f;
-        }
-        const int32_t sp1[1] = {start_pos};
-        if (static_cast<int64_t>(keep.size()) != kda_ckpt_count_ex(cu1, sp1, 1, ckpt_stride)) return KDA_ERR_INVALID_ARG;
-    }
+    const std::vector<int>& keep = plan.keep;
+    const int64_t n_ck_f = plan.n_ck_f;
 
     int* status = nullptr;
     rc = device_setup(&status);

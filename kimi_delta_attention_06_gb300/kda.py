@@ -73,6 +73,8 @@ def load():
             lib.kda_chunk_prefill_segmented.restype = _i
             lib.kda_chunk_prefill_segmented.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _i,
                                                         _vp, _vp, _i, _i, _i, _i, _vp, ctypes.c_float, _vp]
+            lib.kda_segment_plan.restype = _i
+            lib.kda_segment_plan.argtypes = [_i, _i, _i, _i, _vp, _vp, _i]
             lib.kda_prefill_clusters_at_once.restype = _i
             lib.kda_prefill_clusters_at_once.argtypes = []
             lib.kda_decode_step.restype = _i
@@ -200,6 +202,22 @@ def kda_chunk_prefill_segmented(q, k, v, log_alpha, beta, init_state, total_toke
         _ptr(out), int(out_dtype), _ptr(final_state), _ptr(ckpt_states), int(ckpt_stride), int(decay),
         int(start_pos), int(segments), _ptr(out_norm_gamma), float(out_norm_eps), _stream(stream))
     _check(rc, "kda_chunk_prefill_segmented")
+
+
+def kda_segment_plan(total_tokens: int, start_pos: int, segments: int, ckpt_stride: int = 0):
+    """(bounds, ckpt_slots) of kda_chunk_prefill_segmented's plan: the segment bounds in tokens
+    from the prompt's start, and for each of the prompt's checkpoints the final run's slot it
+    comes from (empty when there are no checkpoints or one plain prefill runs)."""
+    bounds = (ctypes.c_int32 * (KDA_MAX_SEGMENTS + 1))()
+    cap = 1 << 16
+    slots = (ctypes.c_int32 * cap)()
+    P = load().kda_segment_plan(int(total_tokens), int(start_pos), int(segments), int(ckpt_stride),
+                                ctypes.cast(bounds, ctypes.c_void_p), ctypes.cast(slots, ctypes.c_void_p), cap)
+    _check(min(P, 0), "kda_segment_plan")
+    n = kda_ckpt_count_ex(torch.tensor([0, int(total_tokens)], dtype=torch.int32),
+                          torch.tensor([int(start_pos)], dtype=torch.int32), ckpt_stride) \
+        if ckpt_stride > 0 and P >= 3 else 0
+    return [int(x) for x in bounds[:P + 1]], [int(x) for x in slots[:n]]
 
 
 def kda_prefill_clusters_at_once() -> int:

@@ -237,3 +237,71 @@ def test_binding_refuses_non_bf16(lib):
         kda.kda_decode_step(torch.zeros(1, 1, 64), torch.zeros(1, 1, 64), torch.zeros(1, 1, 64),
                             torch.zeros(1, 1, 64), torch.zeros(1, 1), torch.zeros(1, 1, 64, 64),
                             torch.zeros(1, 1, 64), 1, 1, 1, 64, 64)
+
+
+def _run_f_slot_positions(bounds, start_pos, stride):
+    """Absolute positions of the final run's checkpoint slots: per segment, the stride
+    multiples strictly inside it, then its end."""
+    pos = []
+    for a, e in zip(bounds[:-1], bounds[1:]):
+        a, e = start_pos + a, start_pos + e
+        m = (a // stride + 1) * stride
+        while m < e:
+            pos.append(m)
+            m += stride
+        pos.append(e)
+    return pos
+
+
+def test_segment_plan_properties(lib):
+    """kda_segment_plan on a seeded sweep of prompt lengths, start positions, segment counts
+    and strides: bounds on the absolute chunk grid with equal chunk counts, and the kept
+    checkpoint slots sit exactly at the prompt's own checkpoint positions (the oracle's
+    count and the stride grid)."""
+    import random
+    import oracle
+    oracle.build()
+    rng = random.Random(7)
+    cases = [(145408, 0, 9, 32768), (5000, 4133, 8, 1024), (5000, 37, 5, 1024), (192, 0, 3, 64),
+             (193, 0, 64, 64), (64 * 200, 63, 64, 128)]
+    for _ in range(300):
+        cases.append((rng.randint(0, 40000), rng.choice([0, rng.randint(0, 100000)]), rng.randint(1, 64),
+                      rng.choice([0, 64, 128, 4096, 32768])))
+    for T, s0, seg, stride in cases:
+        bounds, slots = kda.kda_segment_plan(T, s0, seg, stride)
+        P = len(bounds) - 1
+        n_chunks = 0 if T == 0 else (s0 + T + 63) // 64 - s0 // 64
+        if seg < 3 or n_chunks < 3:
+            assert P == 1, (T, s0, seg)
+        else:
+            per = -(-n_chunks // seg)
+            assert P == (1 if -(-n_chunks // per) < 3 else -(-n_chunks // per))
+        assert bounds[0] == 0 and bounds[-1] == T
+        assert all(x < y for x, y in zip(bounds, bounds[1:])) or T == 0
+        if P >= 3:
+            assert all((s0 + x) % 64 == 0 for x in bounds[1:-1])
+            chunks = [(s0 + y + 63) // 64 - (s0 + x) // 64 for x, y in zip(bounds, bounds[1:])]
+            assert len(set(chunks[:-1])) == 1 and 1 <= chunks[-1] <= chunks[0]
+        if stride and P >= 3:
+            got = [_run_f_slot_positions(bounds, s0, stride)[i] for i in slots]
+            want = [m for m in range((s0 // stride + 1) * stride, s0 + T, stride)] + [s0 + T]
+            assert got == want, (T, s0, seg, stride)
+            assert len(slots) == oracle.ckpt_count([0, T], stride, [s0])
+            assert slots == sorted(slots)
+        else:
+            assert slots == []
+
+
+def test_segment_plan_rejects(lib):
+    b = (ctypes.c_int32 * 65)()
+    f = lib.kda_segment_plan
+    vp = ctypes.cast(b, ctypes.c_void_p)
+    assert f(1000, 0, 0, 0, vp, None, 0) == kda.KDA_ERR_INVALID_ARG
+    assert f(1000, 0, 65, 0, vp, None, 0) == kda.KDA_ERR_INVALID_ARG
+    assert f(1000, -1, 8, 0, vp, None, 0) == kda.KDA_ERR_INVALID_ARG
+    assert f(-1, 0, 8, 0, vp, None, 0) == kda.KDA_ERR_INVALID_ARG
+    assert f(1000, 0, 8, 100, vp, None, 0) == kda.KDA_ERR_INVALID_ARG       # stride: multiple of 64
+    assert f(1000, 0, 8, 0, None, None, 0) == kda.KDA_ERR_INVALID_ARG        # bounds required
+    slots = (ctypes.c_int32 * 1)()
+    assert f(145408, 0, 9, 32768, vp, ctypes.cast(slots, ctypes.c_void_p), 1) == kda.KDA_ERR_INVALID_ARG  # 5 > 1
+    assert f(145408, 0, 9, 32768, vp, None, 0) == 9
