@@ -17,6 +17,8 @@ constexpr size_t kPrefillRingBytesPerPair = 6 * 82944;
 // Segmented prefill: the int32 index arrays of its runs (cu_seqlens and start positions),
 // built on the host and handed to the setup kernel by value.
 constexpr int kSegIdxMax = 512;
+// Blocks per (segment, head) of the segmented prefill's transition bound (partial sums each).
+constexpr int kSegBoundBlocks = 64;
 struct SegIdxBuf {
     int n;
     int32_t v[kSegIdxMax];

@@ -20,7 +20,8 @@ int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
                    int num_seqs, int total_tokens, int H, int Dk, int Dv, void* out, int out_f32,
                    float* final_state, float* ckpt, int ckpt_stride, int decay, const int32_t* start_pos,
                    const float* norm_gamma, float norm_eps,
-                   void* ws, int* ring_flags, int ring_count, int* status, cudaStream_t stream);
+                   void* ws, int* ring_flags, int ring_count, int* status, cudaStream_t stream,
+                   const int* skip = nullptr);
 size_t prefill_workspace_bytes(int num_seqs, int H);
 int prefill_ring_count(int num_seqs, int H);
 int prefill_max_active_clusters();
@@ -33,7 +34,10 @@ int launch_output_norm(const void* o, int o_f32, const float* gamma, float eps, 
                        cudaStream_t stream);
 int launch_segment_setup(const SegIdxBuf& ib, int32_t* idx, float* ident, int n_ident, float* zinit, int n_zinit,
                          const float* init_state, int H, int D, cudaStream_t stream);
-int launch_segment_chain(const float* phi, float* sst, int P, int H, int D, cudaStream_t stream);
+int launch_segment_chain(const float* phi, const int* skip, float* sst, int P, int H, int D, cudaStream_t stream);
+int launch_segment_bound(const uint16_t* k, const float* la, const uint16_t* beta, int decay, int H, int D,
+                         const int32_t* seg_start, int nseg, int lead, float* partial, int* skip,
+                         cudaStream_t stream);
 int launch_decode_multi(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* log_alpha,
                         const uint16_t* beta, float* pool, int num_slots, const int32_t* slots,
                         const int32_t* ntok, int commit, void* out, int out_f32,
@@ -277,7 +281,7 @@ static int prefill_pooled(const uint16_t* q, const uint16_t* k, const uint16_t* 
                           const int32_t* cu_seqlens_host, int num_seqs, int total_tokens, int H, int Dk, int Dv,
                           void* out, int out_dtype, float* final_state, float* ckpt_states, int ckpt_stride,
                           int decay, const int32_t* start_pos, const int32_t* start_pos_host,
-                          const float* norm_gamma, float norm_eps, void* stream) {
+                          const float* norm_gamma, float norm_eps, void* stream, const int* skip = nullptr) {
     int rc = check_prefill_args(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_seqlens_host, num_seqs,
                                 total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, decay);
     if (rc != KDA_OK || num_seqs == 0) return rc;
@@ -305,7 +309,7 @@ static int prefill_pooled(const uint16_t* q, const uint16_t* k, const uint16_t* 
     int* flags = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + ring_bytes);
     rc = kda::launch_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, num_seqs, total_tokens, H, Dk, Dv,
                              out, out_dtype == KDA_OUT_F32, final_state, ckpt_states, ckpt_stride, decay,
-                             start_pos, norm_gamma, norm_eps, ws, flags, rings, status, st);
+                             start_pos, norm_gamma, norm_eps, ws, flags, rings, status, st, skip);
     const bool freed = cudaFreeAsync(ws, st) == cudaSuccess;
     return (rc == 0 && freed) ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -405,7 +409,7 @@ int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     // scratch: index arrays | run A initial states | run B identities | Phi | S_start |
-    // run F final states | run F checkpoints | zero v of run B
+    // run F final states | run F checkpoints | zero v of run B | bound partial sums | skip list
     const size_t slot = static_cast<size_t>(H) * Dk * Dv * sizeof(float);
     const bool zinit_needed = P >= 3 && init_state != nullptr;
     const int64_t tB = P >= 3 ? static_cast<int64_t>(b[P - 1]) - b1a : 0;
@@ -418,7 +422,10 @@ int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint
     const size_t o_fin = o_sst + (P >= 3 ? slot * P : 0);
     const size_t o_ck = o_fin + (P >= 3 ? slot * P : 0);
     const size_t o_zv = o_ck + slot * static_cast<size_t>(n_ck_f);
-    const size_t total = o_zv + up(static_cast<size_t>(tB) * H * Dv * 2);
+    const int nseg = P >= 3 ? P - 2 : 0;
+    const size_t o_part = o_zv + up(static_cast<size_t>(tB) * H * Dv * 2);
+    const size_t o_skip = o_part + up(sizeof(float) * static_cast<size_t>(nseg) * H * kda::kSegBoundBlocks);
+    const size_t total = o_skip + up(sizeof(int) * static_cast<size_t>(nB) * H);
     uint8_t* ws = nullptr;
     if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), total, pool, st) != cudaSuccess) return KDA_ERR_CUDA;
     int32_t* idx = reinterpret_cast<int32_t*>(ws + o_idx);
@@ -429,6 +436,8 @@ int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint
     float* fin = reinterpret_cast<float*>(ws + o_fin);
     float* ck = reinterpret_cast<float*>(ws + o_ck);
     uint16_t* zv = reinterpret_cast<uint16_t*>(ws + o_zv);
+    float* part = reinterpret_cast<float*>(ws + o_part);
+    int* skip = reinterpret_cast<int*>(ws + o_skip);
 
     auto finish = [&](int r) {
         const bool freed = cudaFreeAsync(ws, st) == cudaSuccess;
@@ -443,6 +452,10 @@ int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint
 
     if (tB > 0 && cudaMemsetAsync(zv, 0, static_cast<size_t>(tB) * H * Dv * 2, st) != cudaSuccess)
         return finish(KDA_ERR_CUDA);
+    // which transitions cannot matter (their norm bound is below fp32 rounding): those runs are
+    // skipped and their segment starts from B alone
+    if (kda::launch_segment_bound(k, log_alpha, beta, decay, H, Dk, idx + o_fcu + 1, nseg, lead, part, skip, st) != 0)
+        return finish(KDA_ERR_CUDA);
     // A: segments 0 .. P-2; segment 0's final state lands in S_start[1], B_p in S_start[p + 1]
     rc = prefill_pooled(q, k, v, log_alpha, beta, zinit_needed ? zin : nullptr, idx + o_acu, a_cu.data(), nA,
                         b[P - 1], H, Dk, Dv, out, out_dtype, sst + slot / sizeof(float), nullptr, 0, decay,
@@ -456,11 +469,12 @@ int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint
         rc = prefill_pooled(q + tok * Dk, k + tok * Dk, zv, log_alpha ? log_alpha + tok * la_row : nullptr,
                             beta + tok, idn, idx + o_bcu, b_cu.data(), nB, static_cast<int>(tB), H, Dk, Dv,
                             static_cast<uint8_t*>(out) + tok * Dv * osz, out_dtype, phi, nullptr, 0, decay,
-                            idx + o_bsp, b_sp.data(), nullptr, 0.f, stream);
+                            idx + o_bsp, b_sp.data(), nullptr, 0.f, stream, skip);
         if (rc != KDA_OK) return finish(rc);
     }
     // chain: S_start[p + 1] = Phi_p S_start[p] + B_p, p = 1 .. P-2 (Phi_p in slot p - 1 + lead)
-    if (kda::launch_segment_chain(phi + static_cast<size_t>(lead) * (slot / sizeof(float)), sst, P, H, Dk, st) != 0)
+    if (kda::launch_segment_chain(phi + static_cast<size_t>(lead) * (slot / sizeof(float)), skip + lead * H, sst, P, H,
+                                  Dk, st) != 0)
         return finish(KDA_ERR_CUDA);
     // S_start[0] = the prompt's initial state
     const cudaError_t e0 = init_state ? cudaMemcpyAsync(sst, init_state, slot, cudaMemcpyDeviceToDevice, st)

@@ -175,6 +175,7 @@ struct Params {
     float norm_eps;
     int ckpt_stride;
     int H, dk, dv;
+    const int* skip;             // [num_seqs * H] or null: a nonzero entry makes that (sequence, head) a no-op
 };
 
 // Chunk grid of one sequence.  Chunks sit on the prompt's absolute 64-token grid, so
@@ -1210,6 +1211,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_kernel(const Params p, cons
     uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     const int rank = static_cast<int>(tc::cluster_ctarank());
     const int cl = blockIdx.x / CLUSTER;                  // (sequence, head)
+    if (p.skip && p.skip[cl]) return;                     // (the same for every CTA of the cluster)
     const int h = cl % p.H;
     const int n = cl / p.H;
     SeqGrid g;
@@ -1349,7 +1351,7 @@ int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
                    int num_seqs, int total_tokens, int H, int Dk, int Dv, void* out, int out_f32,
                    float* final_state, float* ckpt, int ckpt_stride, int decay, const int32_t* start_pos,
                    const float* norm_gamma, float norm_eps,
-                   void* ws, int* ring_flags, int ring_count, int* status, cudaStream_t stream)
+                   void* ws, int* ring_flags, int ring_count, int* status, cudaStream_t stream, const int* skip)
 {
     using namespace prefill;
     if (decay != DECAY_CHANNEL && decay != DECAY_HEAD && decay != DECAY_NONE) return -3;
@@ -1370,6 +1372,7 @@ int launch_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v, cons
     p.status = status; p.out_f32 = out_f32; p.ckpt_stride = ckpt_stride;
     p.norm_gamma = norm_gamma; p.norm_eps = norm_eps;
     p.H = H; p.dk = Dk; p.dv = Dv;
+    p.skip = skip;
     const long long clusters = static_cast<long long>(num_seqs) * H;
     if (clusters == 0 || total_tokens == 0) {
         // nothing to stream; empty sequences still hand back their initial states

@@ -8,6 +8,14 @@
 // zeros, and Phi the final state of a run from S_0 = I with v = 0.  The helpers here set
 // up those runs (segment bounds, identity and zero initial states) and chain the segment
 // results: S_start[p + 1] = Phi_p S_start[p] + B_p, serially over the segments.
+//
+// A transition that cannot matter is not formed.  Each token's factor has spectral norm at
+// most max_c alpha_{t,c} * max(1, |1 - beta_t |k_t|^2|) (the projection I - beta k k^T has
+// eigenvalues 1 and 1 - beta |k|^2), so log ||Phi_p|| <= sum over the segment of
+// max_c log alpha_{t,c} + log max(1, |1 - beta_t |k_t|^2|).  Where that bound is below
+// kSkipLogNorm (2^-64, far under fp32 rounding of the state), Phi_p S_start[p] is dropped:
+// its run is skipped and S_start[p + 1] = B_p.
+#include <cmath>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -34,6 +42,72 @@ __global__ void seg_setup_kernel(SegIdxBuf ib, int32_t* idx, float* ident, int n
         zinit[e] = (e < per && init_state) ? init_state[e] : 0.f;
 }
 
+constexpr float kSkipLogNorm = -44.3614195558365f;   // -64 ln 2
+constexpr int kBoundBlocks = kSegBoundBlocks;
+
+// Partial sums of the bound above: grid (kBoundBlocks, segments, H), one warp per token
+// (lanes over channels), warps and blocks strided over the segment's tokens.
+// seg_start [nseg + 1]: token bounds of the segments; partial [(seg * H + h) * kBoundBlocks + blk].
+__global__ void __launch_bounds__(256) seg_bound_kernel(const uint16_t* __restrict__ k, const float* __restrict__ la,
+                                                        const uint16_t* __restrict__ beta, int decay, int H, int D,
+                                                        const int32_t* __restrict__ seg_start, float* partial) {
+    __shared__ float s_w[8];
+    const int blk = blockIdx.x, seg = blockIdx.y, h = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = seg_start[seg], t1 = seg_start[seg + 1];
+    const bool lane_ok = 4 * lane < D;
+    float acc = 0.f;
+    for (int t = t0 + blk * 8 + warp; t < t1; t += 8 * kBoundBlocks) {
+        const size_t row = static_cast<size_t>(t) * H + h;
+        float m = 0.f, kk = 0.f;
+        if (lane_ok) {
+            const uint2 kw = *reinterpret_cast<const uint2*>(k + row * D + 4 * lane);
+            const float2 k01 = bf16x2_bits_to_f32(kw.x), k23 = bf16x2_bits_to_f32(kw.y);
+            kk = k01.x * k01.x + k01.y * k01.y + k23.x * k23.x + k23.y * k23.y;
+        }
+        if (decay == 0) {          // per channel: the largest log-decay of the token
+            m = -INFINITY;
+            if (lane_ok) {
+                const float4 a = *reinterpret_cast<const float4*>(la + row * D + 4 * lane);
+                m = fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            kk += __shfl_xor_sync(0xffffffffu, kk, o);
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        }
+        if (decay == 1) m = la[row];
+        const float b = bf16_bits_to_f32(beta[row]);
+        acc += m + logf(fmaxf(1.f, fabsf(1.f - b * kk)));
+    }
+    if (lane == 0) s_w[warp] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float sum = 0.f;
+        for (int w = 0; w < 8; ++w) sum += s_w[w];
+        partial[(static_cast<size_t>(seg) * H + h) * kBoundBlocks + blk] = sum;
+    }
+}
+
+// The skip list of the transitions' run: row 0 is the leading sequence when there is one
+// (its result is never used), then one row per segment; decay 2 (none) skips nothing.
+__global__ void seg_flag_kernel(const float* partial, int nseg, int H, int lead, int decay, int* skip) {
+    for (int i = threadIdx.x; i < (nseg + lead) * H; i += blockDim.x) {
+        const int r = i / H, h = i % H;
+        int sk = 0;
+        if (r < lead) {
+            sk = 1;
+        } else if (decay != 2) {
+            const float* pp = partial + (static_cast<size_t>(r - lead) * H + h) * kBoundBlocks;
+            float sum = 0.f;
+            for (int b = 0; b < kBoundBlocks; ++b) sum += pp[b];
+            sk = sum < kSkipLogNorm ? 1 : 0;
+        }
+        skip[i] = sk;
+    }
+}
+
 __device__ __forceinline__ void cp_async16(float* dst, const float* src) {
     const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
@@ -50,11 +124,12 @@ constexpr int kSlab = 4;          // state columns per CTA
 // the previous step computes; thread (row i, columns 2 (tid & 1) .. +1) forms its two
 // outputs as fp32 dot products over the whole row.
 // phi   [P-2, H, D, D]  transitions of segments 1 .. P-2
+// skip  [P-2, H]        nonzero: Phi_p was not formed (its bound says it cannot matter)
 // sst   [P, H, D, D]    slot 1 holds segment 0's final state; slot p + 1 (p = 1 .. P-2) holds
 //                       B_p on entry and S_start[p + 1] = Phi_p S_start[p] + B_p on exit
 // (slot 0, the prompt's own initial state, is not touched)
-__global__ void __launch_bounds__(256) seg_chain_kernel(const float* __restrict__ phi, float* sst, int P, int H,
-                                                         int D) {
+__global__ void __launch_bounds__(256) seg_chain_kernel(const float* __restrict__ phi, const int* __restrict__ skip,
+                                                         float* sst, int P, int H, int D) {
     extern __shared__ __align__(16) float sm[];
     const int pitch = D + 4;
     float* slab = sm;                                 // [D][kSlab]
@@ -89,9 +164,12 @@ __global__ void __launch_bounds__(256) seg_chain_kernel(const float* __restrict_
         __syncthreads();                              // Phi_p and the slab are in place
         float a0 = 0.f, a1 = 0.f;
         float* dst = sst + static_cast<size_t>(p + 1) * per + head + static_cast<size_t>(i < D ? i : 0) * D + c0 + j0;
+        const bool use_phi = !skip[static_cast<size_t>(p - 1) * H + h];
         if (i < D) {
             a0 = dst[0];                              // B_p
             a1 = dst[1];
+        }
+        if (i < D && use_phi) {
             const float* row = phis + ((p - 1) & 1) * D * pitch + i * pitch;
 #pragma unroll 8
             for (int kk = 0; kk < D; kk += 4) {
@@ -125,7 +203,19 @@ int launch_segment_setup(const SegIdxBuf& ib, int32_t* idx, float* ident, int n_
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
-int launch_segment_chain(const float* phi, float* sst, int P, int H, int D, cudaStream_t stream) {
+int launch_segment_bound(const uint16_t* k, const float* la, const uint16_t* beta, int decay, int H, int D,
+                         const int32_t* seg_start, int nseg, int lead, float* partial, int* skip,
+                         cudaStream_t stream) {
+    if (nseg < 0 || lead < 0 || H <= 0 || (D != 64 && D != 128) || decay < 0 || decay > 2) return -1;
+    if (decay != 2 && nseg > 0) {
+        const dim3 grid(kBoundBlocks, nseg, H);
+        seg_bound_kernel<<<grid, 256, 0, stream>>>(k, la, beta, decay, H, D, seg_start, partial);
+    }
+    if (nseg + lead > 0) seg_flag_kernel<<<1, 256, 0, stream>>>(partial, nseg, H, lead, decay, skip);
+    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+int launch_segment_chain(const float* phi, const int* skip, float* sst, int P, int H, int D, cudaStream_t stream) {
     if (P < 3 || (D != 64 && D != 128)) return -1;
     const int smem = static_cast<int>(sizeof(float) * (128 * kSlab + 2 * D * (D + 4)));
     static bool attr_done[kMaxDevicesAttr] = {};
@@ -133,7 +223,7 @@ int launch_segment_chain(const float* phi, float* sst, int P, int H, int D, cuda
                           attr_done))
         return -3;
     const dim3 grid(D / kSlab, H);
-    seg_chain_kernel<<<grid, 256, smem, stream>>>(phi, sst, P, H, D);
+    seg_chain_kernel<<<grid, 256, smem, stream>>>(phi, skip, sst, P, H, D);
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

@@ -146,3 +146,31 @@ def test_segmented_long_prompt_4_heads_every_row():
     P.check_out(out32, ro, torch.float32)
     assert torch.equal(fin32, fin)
     assert kda.kda_device_status() == 0
+
+
+def test_segmented_skips_only_transitions_that_cannot_matter():
+    """Heads 0 and 1 decay strongly (their transition over a segment is far below fp32
+    rounding, so it is not formed), heads 2 and 3 weakly (it is formed and applied): every
+    head must match the oracle, and a prompt whose decays are all weak must match too."""
+    c = workloads.prefill_case([6000], H=4, D=128, seed=38, device=DEV, la_shift=-1.0, s0_std=0.05,
+                               ckpt_stride=1024)
+    # log-decays in [-0.15, -0.05] per token and channel on heads 0-1 (a 1000-token segment
+    # decays by at least e^-50), in [-0.002, 0] on heads 2-3; both well inside the prefill's
+    # per-chunk domain
+    g = torch.Generator(device=DEV).manual_seed(40)
+    u = torch.rand(c.log_alpha.shape, generator=g, device=DEV)
+    strong, weak = -0.05 - 0.1 * u, -0.002 * u
+    c.log_alpha = torch.where(torch.arange(4, device=DEV).view(1, 4, 1) < 2, strong, weak).contiguous()
+    for start_pos in (0, 77):
+        ro, rf, rc = _ref(c, kda.KDA_DECAY_CHANNEL, start_pos)
+        out, fin, ck = _seg(c, kda.KDA_DECAY_CHANNEL, 6, start_pos, torch.float32)
+        P.check_out(out, ro, torch.float32)
+        P.check_state(fin, rf)
+        P.check_state(ck, rc, "checkpoints")
+    weak = workloads.prefill_case([6000], H=4, D=128, seed=39, device=DEV, la_shift=-8.0, s0_std=0.05,
+                                  ckpt_stride=0)
+    ro, rf, _ = _ref(weak, kda.KDA_DECAY_CHANNEL, 0)
+    out, fin, _ = _seg(weak, kda.KDA_DECAY_CHANNEL, 6, 0, torch.float32)
+    P.check_out(out, ro, torch.float32)
+    P.check_state(fin, rf)
+    assert kda.kda_device_status() == 0
