@@ -167,17 +167,22 @@ int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v
  * absolute 64-token chunk grid, into up to `segments` runs of equal chunk counts and
  * uses that the recurrence S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} +
  * beta_t k_t v_t^T is linear in (S_0, v) (Kimi Linear, "Kimi Delta Attention"): over a
- * segment, S_end = Phi S_start + B.  Three prefill launches and one small kernel:
- *   A  segments 0 .. P-2 from zeros (segment 0 from init_state): B_p, and segment 0's
- *      final state, which is segment 1's initial state;
- *   B  segments 1 .. P-2 from S_start = I with v = 0: the transitions Phi_p (Dk x Dk);
+ * segment, S_end = Phi S_start + B.  Small helper kernels and three prefill launches:
+ *   A  segments 0 .. P-2: segment 0 from init_state (its outputs and checkpoints are
+ *      final; its final state is segment 1's initial state), the others from zeros (B_p);
+ *   bound  per (segment, head), an upper bound on log ||Phi_p|| from log_alpha, beta and
+ *      |k|^2 (each token's factor has norm at most max_c alpha * max(1, |1 - beta |k|^2|));
+ *   B  segments 1 .. P-2 from S_start = I with v = 0: the transitions Phi_p (Dk x Dk), except
+ *      where the bound is below 2^-64, far under fp32 rounding: those clusters return at once
+ *      and Phi_p S_start is dropped;
  *   chain  S_start[p + 1] = Phi_p S_start[p] + B_p for p = 1 .. P-2, in fp32, serially;
- *   F  all P segments from their S_start, writing out, the checkpoints and the final
- *      state.
- * About 3 - 3/P prefills of work in about 2/P of the serial time: worth it only while
- * P * H * 4 CTAs fit on the GPU at once (e.g. P = 8 for H = 4 on 152 SMs).  When fewer
- * than 3 segments result (segments < 3, or a prompt of fewer than 3 chunks), the call
- * runs as one plain prefill.
+ *   F  segments 1 .. P-1 from their S_start, writing the rest of out, the checkpoints and
+ *      the final state.
+ * About 3 - 4/P prefills of work (2 - 2/P when every transition is dropped) in about 3/P
+ * (2/P) of the serial time: worth it while (P - 1) * H * 4 CTAs fit on the GPU at once
+ * (P - 1 = kda_prefill_clusters_at_once() / H, e.g. P = 10 for H = 4 on a 152-SM GB300).
+ * When fewer than 3 segments result (segments < 3, or a prompt of fewer than 3 chunks),
+ * the call runs as one plain prefill.
  *   Dk == Dv is required (Phi is carried as a Dk x Dv state), else KDA_ERR_UNSUPPORTED.
  *   start_pos   absolute position of the prompt's first token (>= 0), as start_pos of
  *               kda_chunk_prefill_ex: it places the chunk grid and the checkpoints.
@@ -200,8 +205,8 @@ int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v
  * kda_prefill_clusters_at_once -- how many (sequence, head) pairs of the prefill the
  * current device runs at the same time (each takes one 4-CTA cluster; the figure comes
  * from the CUDA occupancy calculator for the kernel's launch shape).  A call over more
- * pairs runs in waves.  For kda_chunk_prefill_segmented, segments = this / H (when that
- * is at least 3) keeps the final run to one wave.  Returns the count (> 0) or a negative
+ * pairs runs in waves.  For kda_chunk_prefill_segmented, segments = this / H + 1 (when
+ * that is at least 3) keeps each of its runs to one wave.  Returns the count (> 0) or a negative
  * kda_status (no sm_103a device: KDA_ERR_UNSUPPORTED).
  */
 int kda_prefill_clusters_at_once(void);
@@ -215,11 +220,13 @@ int kda_prefill_clusters_at_once(void);
  *               chunk grid (start_pos + bounds[p] is a multiple of 64); every segment but
  *               the last has the same number of chunks.
  *   ckpt_slots  (host) int32 [ckpt_slots_cap] or NULL: when ckpt_stride > 0 and P >= 3,
- *               receives, for each of the prompt's own checkpoints in order, the index of
- *               the final run's checkpoint slot it is copied from (that run writes one
- *               more slot at every segment end that is neither a stride multiple nor the
- *               prompt's end).  Fewer slots than the prompt's checkpoints ->
- *               KDA_ERR_INVALID_ARG.
+ *               receives, for each of the prompt's own checkpoints in order, the checkpoint
+ *               slot it is copied from, counted over run A's slots followed by run F's (see
+ *               kda_chunk_prefill_segmented; each run writes a slot at every stride multiple
+ *               inside and at the end of each of its sequences, in sequence order, and run F
+ *               starts with a leading sequence from b1a = bounds[1] rounded down to a
+ *               multiple of 8 when that is below bounds[1]).  Fewer slots than the prompt's
+ *               checkpoints -> KDA_ERR_INVALID_ARG.
  * Returns P (1 = one plain prefill, else 3 .. segments) or a negative kda_status.
  */
 int kda_segment_plan(int total_tokens, int start_pos, int segments, int ckpt_stride,

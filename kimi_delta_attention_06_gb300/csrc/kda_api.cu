@@ -33,7 +33,8 @@ int launch_prepare_inputs(const uint16_t* xq, const uint16_t* xk, const uint16_t
 int launch_output_norm(const void* o, int o_f32, const float* gamma, float eps, uint16_t* y, int T, int H, int D,
                        cudaStream_t stream);
 int launch_segment_setup(const SegIdxBuf& ib, int32_t* idx, float* ident, int n_ident, float* zinit, int n_zinit,
-                         const float* init_state, int H, int D, cudaStream_t stream);
+                         const float* init_state, int* flags, int n_flags, int n_flags_set, int H, int D,
+                         cudaStream_t stream);
 int launch_segment_chain(const float* phi, const int* skip, float* sst, int P, int H, int D, cudaStream_t stream);
 int launch_segment_bound(const uint16_t* k, const float* la, const uint16_t* beta, int decay, int H, int D,
                          const int32_t* seg_start, int nseg, int lead, float* partial, int* skip,
@@ -163,16 +164,25 @@ __global__ void expire_wait_kernel(unsigned long long limit_ns, int* status) {
     }
 }
 
-// The plan of a segmented prefill: the segment bounds on the prompt's absolute 64-token
-// chunk grid (tokens from the prompt's start; equal chunk counts, the last segment
-// shorter; P = 1 when fewer than 3 segments result) and, when ckpt_stride > 0, for each of
-// the prompt's own checkpoints in order, the slot of the final run's checkpoints it comes
-// from (that run also writes one at every segment end).
+// The plan of a segmented prefill.
+//   b[0..P]   segment bounds, tokens from the prompt's start, on the absolute 64-token chunk
+//             grid (equal chunk counts, the last segment shorter; P = 1 when fewer than 3
+//             segments result, which runs one plain prefill)
+//   b1a       segment 1's start rounded down to a multiple of 8 tokens; the runs that start
+//             there (B and F) put a short leading sequence [b1a, b1) first (lead = 1) so that
+//             every per-token row they address stays 16-byte aligned; it is skipped
+//   checkpoints: run A (segments 0 .. P-2) writes n_ck_a slots and run F (the leading
+//             sequence, then segments 1 .. P-1) n_ck_f; keep[i] is the slot, in run A's slots
+//             followed by run F's, of the prompt's i-th own checkpoint (segment 0's come from
+//             run A, the rest from run F; every run also writes one slot at each of its
+//             sequences' ends, which is kept only at a stride multiple or the prompt's end)
 struct SegPlan {
     int P = 1;
     std::vector<int32_t> b;
+    int32_t b1a = 0;
+    int lead = 0;
     std::vector<int> keep;
-    int64_t n_ck_f = 0;
+    int64_t n_ck_a = 0, n_ck_f = 0;
 };
 
 int plan_segments(int total_tokens, int start_pos, int segments, int ckpt_stride, SegPlan* out) {
@@ -197,24 +207,35 @@ int plan_segments(int total_tokens, int start_pos, int segments, int ckpt_stride
     }
     b[0] = 0;
     b[P] = total_tokens;
+    const int32_t b1a = P >= 3 ? (b[1] & ~7) : 0;
+    const int lead = (P >= 3 && b1a < b[1]) ? 1 : 0;
     std::vector<int> keep;
-    int64_t n_ck_f = 0;
+    int64_t n_a = 0, n_f = 0;
     if (ckpt_stride > 0 && P >= 3) {
-        for (int p = 0; p < P; ++p) {
-            const int64_t a = s0 + b[p], e = s0 + b[p + 1];
-            for (int64_t m = (a / ckpt_stride + 1) * ckpt_stride; m < e; m += ckpt_stride)
-                keep.push_back(static_cast<int>(n_ck_f++));
-            if (e % ckpt_stride == 0 || p == P - 1) keep.push_back(static_cast<int>(n_ck_f));
-            ++n_ck_f;
-        }
+        // slots of one sequence [a, e) (absolute positions): the stride multiples strictly inside,
+        // then its end; `own` marks those that are the prompt's checkpoints
+        auto slots = [&](int64_t a, int64_t e, bool last, int64_t base, int64_t* n, bool own_any) {
+            for (int64_t m = (a / ckpt_stride + 1) * ckpt_stride; m < e; m += ckpt_stride) {
+                if (own_any) keep.push_back(static_cast<int>(base + *n));
+                ++*n;
+            }
+            if (own_any && (e % ckpt_stride == 0 || last)) keep.push_back(static_cast<int>(base + *n));
+            ++*n;
+        };
+        for (int p = 0; p <= P - 2; ++p) slots(s0 + b[p], s0 + b[p + 1], false, 0, &n_a, p == 0);
+        if (lead) slots(s0 + b1a, s0 + b[1], false, 0, &n_f, false);
+        for (int p = 1; p <= P - 1; ++p) slots(s0 + b[p], s0 + b[p + 1], p == P - 1, n_a, &n_f, true);
         const int32_t cu1[2] = {0, total_tokens};
         const int32_t sp1[1] = {start_pos};
         if (static_cast<int64_t>(keep.size()) != kda_ckpt_count_ex(cu1, sp1, 1, ckpt_stride)) return KDA_ERR_INVALID_ARG;
     }
     out->P = P;
     out->b = std::move(b);
+    out->b1a = b1a;
+    out->lead = lead;
     out->keep = std::move(keep);
-    out->n_ck_f = n_ck_f;
+    out->n_ck_a = n_a;
+    out->n_ck_f = n_f;
     return KDA_OK;
 }
 
@@ -367,38 +388,41 @@ int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint
     const int P = plan.P;
     const std::vector<int32_t>& b = plan.b;
 
-    // run B starts on a token index that keeps every per-token row 16-byte aligned (beta
-    // and per-head log-decay rows are H * 2 and H * 4 bytes): a short leading sequence
-    // fills the gap up to segment 1 and its result is ignored
-    const int32_t b1a = P >= 3 ? (b[1] & ~7) : 0;
-    const int lead = (P >= 3 && b1a < b[1]) ? 1 : 0;
-    const int nA = P >= 3 ? P - 1 : 0, nB = P >= 3 ? P - 2 + lead : 0;
+    const int32_t b1a = plan.b1a;
+    const int lead = plan.lead;
+    const int nA = P >= 3 ? P - 1 : 0;              // run A: segments 0 .. P-2
+    const int nB = P >= 3 ? P - 2 + lead : 0;       // run B: [leading,] segments 1 .. P-2
+    const int nF = P >= 3 ? P - 1 + lead : 0;       // run F: [leading,] segments 1 .. P-1
 
-    // host index arrays: run A, run B, run F (cu_seqlens, start positions)
-    std::vector<int32_t> a_cu, a_sp, b_cu, b_sp, f_cu, f_sp;
-    for (int p = 0; p <= nA; ++p) a_cu.push_back(b[p]);
-    for (int p = 0; p < nA; ++p) a_sp.push_back(start_pos + b[p]);
-    if (nB > 0) {
+    // host index arrays (cu_seqlens, start positions) of the runs; B and F count tokens from b1a
+    std::vector<int32_t> a_cu, a_sp, b_cu, b_sp, f_cu, f_sp, bnd(b.begin(), b.end()), sp0{start_pos};
+    if (P >= 3) {
+        for (int p = 0; p <= nA; ++p) a_cu.push_back(b[p]);
+        for (int p = 0; p < nA; ++p) a_sp.push_back(start_pos + b[p]);
         b_cu.push_back(0);
-        if (lead) { b_cu.push_back(b[1] - b1a); b_sp.push_back(start_pos + b1a); }
+        f_cu.push_back(0);
+        if (lead) {
+            b_cu.push_back(b[1] - b1a); b_sp.push_back(start_pos + b1a);
+            f_cu.push_back(b[1] - b1a); f_sp.push_back(start_pos + b1a);
+        }
         for (int p = 1; p <= P - 2; ++p) { b_cu.push_back(b[p + 1] - b1a); b_sp.push_back(start_pos + b[p]); }
+        for (int p = 1; p <= P - 1; ++p) { f_cu.push_back(b[p + 1] - b1a); f_sp.push_back(start_pos + b[p]); }
     }
-    for (int p = 0; p <= P; ++p) f_cu.push_back(b[p]);
-    for (int p = 0; p < P; ++p) f_sp.push_back(start_pos + b[p]);
-    if (a_cu.size() + a_sp.size() + b_cu.size() + b_sp.size() + f_cu.size() + f_sp.size() >
+    if (a_cu.size() + a_sp.size() + b_cu.size() + b_sp.size() + f_cu.size() + f_sp.size() + bnd.size() + sp0.size() >
         static_cast<size_t>(kda::kSegIdxMax))
         return KDA_ERR_INVALID_ARG;
     kda::SegIdxBuf ib;
     ib.n = 0;
-    int o_acu = 0, o_asp = 0, o_bcu = 0, o_bsp = 0, o_fcu = 0, o_fsp = 0;
+    int o_acu = 0, o_asp = 0, o_bcu = 0, o_bsp = 0, o_fcu = 0, o_fsp = 0, o_bnd = 0, o_sp0 = 0;
     auto put = [&](const std::vector<int32_t>& x, int* off) {
         *off = ib.n;
         for (int32_t e : x) ib.v[ib.n++] = e;
     };
     put(a_cu, &o_acu); put(a_sp, &o_asp); put(b_cu, &o_bcu); put(b_sp, &o_bsp); put(f_cu, &o_fcu); put(f_sp, &o_fsp);
+    put(bnd, &o_bnd); put(sp0, &o_sp0);
 
     const std::vector<int>& keep = plan.keep;
-    const int64_t n_ck_f = plan.n_ck_f;
+    const int64_t n_ck = plan.n_ck_a + plan.n_ck_f;
 
     int* status = nullptr;
     rc = device_setup(&status);
@@ -409,10 +433,14 @@ int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     // scratch: index arrays | run A initial states | run B identities | Phi | S_start |
-    // run F final states | run F checkpoints | zero v of run B | bound partial sums | skip list
+    // run F final states | checkpoints of runs A and F | zero v of run B | bound partial sums |
+    // run B skip list | run F skip list
     const size_t slot = static_cast<size_t>(H) * Dk * Dv * sizeof(float);
+    const size_t slot_f = slot / sizeof(float);
     const bool zinit_needed = P >= 3 && init_state != nullptr;
     const int64_t tB = P >= 3 ? static_cast<int64_t>(b[P - 1]) - b1a : 0;
+    const int64_t tF = P >= 3 ? static_cast<int64_t>(total_tokens) - b1a : 0;
+    const int nseg = P >= 3 ? P - 2 : 0;
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     const size_t o_idx = 0;
     const size_t o_zin = o_idx + up(sizeof(int32_t) * ib.n);
@@ -420,12 +448,12 @@ int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint
     const size_t o_phi = o_idn + slot * nB;
     const size_t o_sst = o_phi + slot * nB;
     const size_t o_fin = o_sst + (P >= 3 ? slot * P : 0);
-    const size_t o_ck = o_fin + (P >= 3 ? slot * P : 0);
-    const size_t o_zv = o_ck + slot * static_cast<size_t>(n_ck_f);
-    const int nseg = P >= 3 ? P - 2 : 0;
+    const size_t o_ck = o_fin + slot * nF;
+    const size_t o_zv = o_ck + slot * static_cast<size_t>(n_ck);
     const size_t o_part = o_zv + up(static_cast<size_t>(tB) * H * Dv * 2);
     const size_t o_skip = o_part + up(sizeof(float) * static_cast<size_t>(nseg) * H * kda::kSegBoundBlocks);
-    const size_t total = o_skip + up(sizeof(int) * static_cast<size_t>(nB) * H);
+    const size_t o_fskip = o_skip + up(sizeof(int) * static_cast<size_t>(nB) * H);
+    const size_t total = o_fskip + up(sizeof(int) * static_cast<size_t>(nF) * H);
     uint8_t* ws = nullptr;
     if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), total, pool, st) != cudaSuccess) return KDA_ERR_CUDA;
     int32_t* idx = reinterpret_cast<int32_t*>(ws + o_idx);
@@ -438,56 +466,57 @@ int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint
     uint16_t* zv = reinterpret_cast<uint16_t*>(ws + o_zv);
     float* part = reinterpret_cast<float*>(ws + o_part);
     int* skip = reinterpret_cast<int*>(ws + o_skip);
+    int* fskip = reinterpret_cast<int*>(ws + o_fskip);
 
     auto finish = [&](int r) {
         const bool freed = cudaFreeAsync(ws, st) == cudaSuccess;
         return r != KDA_OK ? r : (freed ? KDA_OK : KDA_ERR_CUDA);
     };
-    if (kda::launch_segment_setup(ib, idx, idn, nB, zin, zinit_needed ? nA : 0, init_state, H, Dk, st) != 0)
+    if (kda::launch_segment_setup(ib, idx, idn, nB, zin, zinit_needed ? nA : 0, init_state, fskip, nF * H, lead * H,
+                                  H, Dk, st) != 0)
         return finish(KDA_ERR_CUDA);
     if (P < 3)   // one plain prefill
-        return finish(prefill_pooled(q, k, v, log_alpha, beta, init_state, idx + o_fcu, f_cu.data(), 1, total_tokens,
+        return finish(prefill_pooled(q, k, v, log_alpha, beta, init_state, idx + o_bnd, bnd.data(), 1, total_tokens,
                                      H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, decay,
-                                     idx + o_fsp, f_sp.data(), out_norm_gamma, out_norm_eps, stream));
+                                     idx + o_sp0, sp0.data(), out_norm_gamma, out_norm_eps, stream));
 
     if (tB > 0 && cudaMemsetAsync(zv, 0, static_cast<size_t>(tB) * H * Dv * 2, st) != cudaSuccess)
         return finish(KDA_ERR_CUDA);
     // which transitions cannot matter (their norm bound is below fp32 rounding): those runs are
     // skipped and their segment starts from B alone
-    if (kda::launch_segment_bound(k, log_alpha, beta, decay, H, Dk, idx + o_fcu + 1, nseg, lead, part, skip, st) != 0)
+    if (kda::launch_segment_bound(k, log_alpha, beta, decay, H, Dk, idx + o_bnd + 1, nseg, lead, part, skip, st) != 0)
         return finish(KDA_ERR_CUDA);
-    // A: segments 0 .. P-2; segment 0's final state lands in S_start[1], B_p in S_start[p + 1]
+    const size_t la_row = decay == KDA_DECAY_CHANNEL ? static_cast<size_t>(Dk) : 1;
+    const size_t osz = out_dtype == KDA_OUT_F32 ? 4 : 2;
+    const size_t tok = static_cast<size_t>(b1a) * H;        // token rows before b1a
+    // A: segments 0 .. P-2.  Segment 0 starts from the prompt's initial state, so its outputs
+    // (normed, if asked) and checkpoints are final; its final state lands in S_start[1], and
+    // B_p (p >= 1, from zeros) in S_start[p + 1]
     rc = prefill_pooled(q, k, v, log_alpha, beta, zinit_needed ? zin : nullptr, idx + o_acu, a_cu.data(), nA,
-                        b[P - 1], H, Dk, Dv, out, out_dtype, sst + slot / sizeof(float), nullptr, 0, decay,
-                        idx + o_asp, a_sp.data(), nullptr, 0.f, stream);
+                        b[P - 1], H, Dk, Dv, out, out_dtype, sst + slot_f, ckpt_states ? ck : nullptr,
+                        ckpt_states ? ckpt_stride : 0, decay, idx + o_asp, a_sp.data(), out_norm_gamma, out_norm_eps,
+                        stream);
     if (rc != KDA_OK) return finish(rc);
     // B: from S_start = I with v = 0, tokens from b1a on (the leading sequence, if any, first)
-    {
-        const size_t tok = static_cast<size_t>(b1a) * H;
-        const size_t la_row = decay == KDA_DECAY_CHANNEL ? static_cast<size_t>(Dk) : 1;
-        const size_t osz = out_dtype == KDA_OUT_F32 ? 4 : 2;
-        rc = prefill_pooled(q + tok * Dk, k + tok * Dk, zv, log_alpha ? log_alpha + tok * la_row : nullptr,
-                            beta + tok, idn, idx + o_bcu, b_cu.data(), nB, static_cast<int>(tB), H, Dk, Dv,
-                            static_cast<uint8_t*>(out) + tok * Dv * osz, out_dtype, phi, nullptr, 0, decay,
-                            idx + o_bsp, b_sp.data(), nullptr, 0.f, stream, skip);
-        if (rc != KDA_OK) return finish(rc);
-    }
+    rc = prefill_pooled(q + tok * Dk, k + tok * Dk, zv, log_alpha ? log_alpha + tok * la_row : nullptr, beta + tok,
+                        idn, idx + o_bcu, b_cu.data(), nB, static_cast<int>(tB), H, Dk, Dv,
+                        static_cast<uint8_t*>(out) + tok * Dv * osz, out_dtype, phi, nullptr, 0, decay,
+                        idx + o_bsp, b_sp.data(), nullptr, 0.f, stream, skip);
+    if (rc != KDA_OK) return finish(rc);
     // chain: S_start[p + 1] = Phi_p S_start[p] + B_p, p = 1 .. P-2 (Phi_p in slot p - 1 + lead)
-    if (kda::launch_segment_chain(phi + static_cast<size_t>(lead) * (slot / sizeof(float)), skip + lead * H, sst, P, H,
-                                  Dk, st) != 0)
+    if (kda::launch_segment_chain(phi + static_cast<size_t>(lead) * slot_f, skip + lead * H, sst, P, H, Dk, st) != 0)
         return finish(KDA_ERR_CUDA);
-    // S_start[0] = the prompt's initial state
-    const cudaError_t e0 = init_state ? cudaMemcpyAsync(sst, init_state, slot, cudaMemcpyDeviceToDevice, st)
-                                      : cudaMemsetAsync(sst, 0, slot, st);
-    if (e0 != cudaSuccess) return finish(KDA_ERR_CUDA);
-    // F: every segment from its S_start
-    rc = prefill_pooled(q, k, v, log_alpha, beta, sst, idx + o_fcu, f_cu.data(), P, total_tokens, H, Dk, Dv, out,
-                        out_dtype, fin, ckpt_states ? ck : nullptr, ckpt_states ? ckpt_stride : 0, decay,
-                        idx + o_fsp, f_sp.data(), out_norm_gamma, out_norm_eps, stream);
+    // F: segments 1 .. P-1 from S_start[1 ..] (the leading sequence, skipped, takes slot 0)
+    rc = prefill_pooled(q + tok * Dk, k + tok * Dk, v + tok * Dv, log_alpha ? log_alpha + tok * la_row : nullptr,
+                        beta + tok, sst + (lead ? 0 : slot_f), idx + o_fcu, f_cu.data(), nF, static_cast<int>(tF), H,
+                        Dk, Dv, static_cast<uint8_t*>(out) + tok * Dv * osz, out_dtype, fin,
+                        ckpt_states ? ck + static_cast<size_t>(plan.n_ck_a) * slot_f : nullptr,
+                        ckpt_states ? ckpt_stride : 0, decay, idx + o_fsp, f_sp.data(), out_norm_gamma, out_norm_eps,
+                        stream, lead ? fskip : nullptr);
     if (rc != KDA_OK) return finish(rc);
     if (final_state &&
-        cudaMemcpyAsync(final_state, fin + static_cast<size_t>(P - 1) * (slot / sizeof(float)), slot,
-                        cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        cudaMemcpyAsync(final_state, fin + static_cast<size_t>(nF - 1) * slot_f, slot, cudaMemcpyDeviceToDevice,
+                        st) != cudaSuccess)
         return finish(KDA_ERR_CUDA);
     // the prompt's checkpoints, in order: runs of consecutive kept slots, one copy each
     for (size_t i = 0, u = 0; i < keep.size();) {

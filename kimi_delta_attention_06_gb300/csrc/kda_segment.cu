@@ -27,12 +27,14 @@ namespace {
 
 // The runs' index arrays (built on the host), then their initial states: ident
 // [n_ident, H, D, D] = I per head; zinit [n_zinit, H, D, D] = the prompt's initial state in
-// slot 0 (zeros if none) and zeros elsewhere.
+// slot 0 (zeros if none) and zeros elsewhere; and a skip list flags [n_flags] whose first
+// n_flags_set entries are 1 (the leading sequence of a run), the rest 0.
 __global__ void seg_setup_kernel(SegIdxBuf ib, int32_t* idx, float* ident, int n_ident, float* zinit, int n_zinit,
-                                 const float* init_state, int H, int D) {
+                                 const float* init_state, int* flags, int n_flags, int n_flags_set, int H, int D) {
     const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const long long nth = static_cast<long long>(gridDim.x) * blockDim.x;
     for (long long e = tid; e < ib.n; e += nth) idx[e] = ib.v[e];
+    for (long long e = tid; e < n_flags; e += nth) flags[e] = e < n_flags_set ? 1 : 0;
     const long long per = static_cast<long long>(H) * D * D;                           // one state slot
     for (long long e = tid; e < static_cast<long long>(n_ident) * per; e += nth) {
         const int rc = static_cast<int>(e % (static_cast<long long>(D) * D));
@@ -197,9 +199,11 @@ __global__ void __launch_bounds__(256) seg_chain_kernel(const float* __restrict_
 }  // namespace
 
 int launch_segment_setup(const SegIdxBuf& ib, int32_t* idx, float* ident, int n_ident, float* zinit, int n_zinit,
-                         const float* init_state, int H, int D, cudaStream_t stream) {
-    if (ib.n < 0 || ib.n > kSegIdxMax || n_ident < 0 || n_zinit < 0) return -1;
-    seg_setup_kernel<<<4 * 152, 256, 0, stream>>>(ib, idx, ident, n_ident, zinit, n_zinit, init_state, H, D);
+                         const float* init_state, int* flags, int n_flags, int n_flags_set, int H, int D,
+                         cudaStream_t stream) {
+    if (ib.n < 0 || ib.n > kSegIdxMax || n_ident < 0 || n_zinit < 0 || n_flags < 0 || n_flags_set < 0) return -1;
+    seg_setup_kernel<<<4 * 152, 256, 0, stream>>>(ib, idx, ident, n_ident, zinit, n_zinit, init_state, flags, n_flags,
+                                                  n_flags_set, H, D);
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

@@ -206,8 +206,9 @@ def kda_chunk_prefill_segmented(q, k, v, log_alpha, beta, init_state, total_toke
 
 def kda_segment_plan(total_tokens: int, start_pos: int, segments: int, ckpt_stride: int = 0):
     """(bounds, ckpt_slots) of kda_chunk_prefill_segmented's plan: the segment bounds in tokens
-    from the prompt's start, and for each of the prompt's checkpoints the final run's slot it
-    comes from (empty when there are no checkpoints or one plain prefill runs)."""
+    from the prompt's start, and for each of the prompt's checkpoints the slot it comes from,
+    counted over run A's slots then run F's (empty when there are no checkpoints or one plain
+    prefill runs)."""
     bounds = (ctypes.c_int32 * (KDA_MAX_SEGMENTS + 1))()
     cap = 1 << 16
     slots = (ctypes.c_int32 * cap)()
@@ -227,10 +228,13 @@ def kda_prefill_clusters_at_once() -> int:
 
 
 def segments_for(H: int, clusters_at_once: Optional[int] = None) -> int:
-    """Segments for kda_chunk_prefill_segmented that fill the device in one wave of the final
-    run (clusters_at_once // H), or 0 (a plain prefill) when that is below 3."""
+    """Segments for kda_chunk_prefill_segmented whose runs (P - 1 segments each) fill the
+    device in one wave (clusters_at_once // H + 1, at most 32: beyond that the serial chain
+    of segment states and the per-segment fixed costs grow while the runs shrink, and short
+    segments are less likely to let their transitions be dropped), or 0 (a plain prefill)
+    when that is below 3."""
     n = kda_prefill_clusters_at_once() if clusters_at_once is None else int(clusters_at_once)
-    p = min(n // max(1, int(H)), KDA_MAX_SEGMENTS)
+    p = min(n // max(1, int(H)) + 1, 32)
     return p if p >= 3 else 0
 
 

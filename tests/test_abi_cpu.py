@@ -239,17 +239,27 @@ def test_binding_refuses_non_bf16(lib):
                             torch.zeros(1, 1, 64), 1, 1, 1, 64, 64)
 
 
-def _run_f_slot_positions(bounds, start_pos, stride):
-    """Absolute positions of the final run's checkpoint slots: per segment, the stride
+def _slot_positions(bounds, start_pos, stride):
+    """Absolute positions of the checkpoint slots the segmented prefill's runs write, run A's
+    (segments 0 .. P-2) followed by run F's (a leading sequence from segment 1's start rounded
+    down to 8 tokens, when that differs, then segments 1 .. P-1): per sequence, the stride
     multiples strictly inside it, then its end."""
-    pos = []
-    for a, e in zip(bounds[:-1], bounds[1:]):
-        a, e = start_pos + a, start_pos + e
+    def seq(a, e):
+        out = []
         m = (a // stride + 1) * stride
         while m < e:
-            pos.append(m)
+            out.append(m)
             m += stride
-        pos.append(e)
+        return out + [e]
+    P = len(bounds) - 1
+    pos = []
+    for p in range(P - 1):
+        pos += seq(start_pos + bounds[p], start_pos + bounds[p + 1])
+    b1a = bounds[1] & ~7
+    if b1a < bounds[1]:
+        pos += seq(start_pos + b1a, start_pos + bounds[1])
+    for p in range(1, P):
+        pos += seq(start_pos + bounds[p], start_pos + bounds[p + 1])
     return pos
 
 
@@ -283,7 +293,7 @@ def test_segment_plan_properties(lib):
             chunks = [(s0 + y + 63) // 64 - (s0 + x) // 64 for x, y in zip(bounds, bounds[1:])]
             assert len(set(chunks[:-1])) == 1 and 1 <= chunks[-1] <= chunks[0]
         if stride and P >= 3:
-            got = [_run_f_slot_positions(bounds, s0, stride)[i] for i in slots]
+            got = [_slot_positions(bounds, s0, stride)[i] for i in slots]
             want = [m for m in range((s0 // stride + 1) * stride, s0 + T, stride)] + [s0 + T]
             assert got == want, (T, s0, seg, stride)
             assert len(slots) == oracle.ckpt_count([0, T], stride, [s0])
