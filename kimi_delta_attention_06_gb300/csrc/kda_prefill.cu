@@ -759,11 +759,13 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             for (int r = 0; r < 16; ++r) Th[(16 * bb + r) * LH + 16 * bb + cc] = __float2half_rn(sv[r]);
         }
         tc::named_sync(BAR_ALL, NT);
-        if (warp >= 2 && tid < 64 + 128) {
-            // meanwhile, T diag(beta) of the diagonal blocks into rows 0..63 of [T; Mqk]:
-            // thread -> (block, row, 8 columns); the blocks below the diagonal get theirs from
-            // the fp32 products that form them
-            const int u = tid - 64, bb = u >> 5, row = 16 * bb + ((u >> 1) & 15), c0 = 16 * bb + 8 * (u & 1);
+        if ((warp & 3) >= 2) {
+            // meanwhile, T diag(beta) of the diagonal blocks into rows 0..63 of [T; Mqk], on the
+            // warps of the two schedulers that the merging warps 0 and 1 do not use: thread ->
+            // (block, row, 8 columns); the blocks below the diagonal get theirs from the fp32
+            // products that form them
+            const int u = (2 * (warp >> 2) + (warp & 1)) * 32 + lane;
+            const int bb = u >> 5, row = 16 * bb + ((u >> 1) & 15), c0 = 16 * bb + 8 * (u & 1);
             const uint4 w = *reinterpret_cast<const uint4*>(Th + row * LH + c0);
             const float4 b0 = *reinterpret_cast<const float4*>(s_beta + c0);
             const float4 b1 = *reinterpret_cast<const float4*>(s_beta + c0 + 4);
