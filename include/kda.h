@@ -156,82 +156,74 @@ int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v
                          void* stream);
 
 /*
- * kda_chunk_prefill_segmented -- one prompt's prefill with its chunks split into
- * segments that run side by side, for a GPU that holds few heads.
+ * kda_chunk_prefill_segmented_ex -- the prefill of a few long sequences with their chunks
+ * split into segments that run side by side, for a GPU that holds few heads.
  *
- * The result is the prefill of ONE sequence of total_tokens tokens (the arguments and
- * outputs of kda_chunk_prefill_ex with num_seqs = 1, cu_seqlens = {0, total_tokens}
- * and start_pos given on the host), computed another way.  Each head's chunks form one
- * serial chain in kda_chunk_prefill, so a call over few heads leaves most SMs idle and
- * takes as long as a call over many.  This entry point cuts the prompt, on the
- * absolute 64-token chunk grid, into up to `segments` runs of equal chunk counts and
- * uses that the recurrence S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} +
- * beta_t k_t v_t^T is linear in (S_0, v) (Kimi Linear, "Kimi Delta Attention"): over a
- * segment, S_end = Phi S_start + B.  Small helper kernels and three prefill launches:
- *   A  segments 0 .. P-2: segment 0 from init_state (its outputs and checkpoints are
- *      final; its final state is segment 1's initial state), the others from zeros (B_p);
- *   bound  per (segment, head), an upper bound on log ||Phi_p|| from log_alpha, beta and
+ * The result is that of kda_chunk_prefill_ex over the same sequences (start positions
+ * given on the host), computed another way.  Each (sequence, head) forms one serial chain
+ * of chunks in kda_chunk_prefill_ex, so a call over few heads and few sequences leaves most
+ * SMs idle and takes as long as one sequence's chain.  This entry point cuts every sequence
+ * of enough chunks, on its absolute 64-token chunk grid, into P_n >= 3 segments of about
+ * L = (the call's chunks) / `segments` chunks each (shorter sequences stay whole), and uses
+ * that the recurrence S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ * is linear in (S_0, v) (Kimi Linear, "Kimi Delta Attention"): over a segment,
+ * S_end = Phi S_start + B.  Three prefill launches run over the list of all segments, each
+ * with a skip list, plus small helper kernels:
+ *   A  every segment of a split sequence but its last: the first from the sequence's
+ *      initial state (its outputs, norm and checkpoints are final; its end state is the
+ *      second segment's start), the others from zeros (B);
+ *   bound  per (segment, head), an upper bound on log ||Phi|| from log_alpha, beta and
  *      |k|^2 (each token's factor has norm at most max_c alpha * max(1, |1 - beta |k|^2|));
- *   B  segments 1 .. P-2 from S_start = I with v = 0: the transitions Phi_p (Dk x Dk), except
- *      where the bound is below 2^-64, far under fp32 rounding: those clusters return at once
- *      and Phi_p S_start is dropped;
- *   chain  S_start[p + 1] = Phi_p S_start[p] + B_p for p = 1 .. P-2, in fp32, serially;
- *   F  segments 1 .. P-1 from their S_start, writing the rest of out, the checkpoints and
- *      the final state.
- * About 3 - 4/P prefills of work (2 - 2/P when every transition is dropped) in about 3/P
- * (2/P) of the serial time: worth it while (P - 1) * H * 4 CTAs fit on the GPU at once
- * (P - 1 = kda_prefill_clusters_at_once() / H, e.g. P = 10 for H = 4 on a 152-SM GB300).
- * When fewer than 3 segments result (segments < 3, or a prompt of fewer than 3 chunks),
- * the call runs as one plain prefill.
+ *   B  the middle segments from S_start = I with v = 0: the transitions Phi (Dk x Dk),
+ *      except where the bound is below 2^-64, far under fp32 rounding: those clusters
+ *      return at once and Phi S_start is dropped;
+ *   chain  S_start[p + 1] = Phi_p S_start[p] + B_p along each split sequence, fp32;
+ *   F  every other segment (all but a split sequence's first; whole sequences as they
+ *      are) from its S_start, writing the rest of out, the checkpoints and the final states.
+ * About 3 - 4/P prefills of work for a sequence of P segments (2 - 2/P when every
+ * transition is dropped) in about 3/P (2/P) of the serial time: worth it while each run's
+ * (segment, head) pairs fit on the GPU at once (kda_prefill_clusters_at_once).
+ *   cu_seqlens_host (host) int32 [num_seqs + 1], as in kda_chunk_prefill (the library makes
+ *               its own device copies).
+ *   num_seqs    at most KDA_MAX_SEGMENTED_SEQS (else KDA_ERR_UNSUPPORTED); with more than
+ *               32 sequences, or `segments` < 3, nothing is split and the call is one plain
+ *               prefill.
+ *   start_pos_host (host) int32 [num_seqs] (>= 0) or NULL (all 0), as start_pos of
+ *               kda_chunk_prefill_ex: it places each sequence's chunk and checkpoint grid.
+ *   segments    1 .. KDA_MAX_SEGMENTS, else KDA_ERR_INVALID_ARG: about how many segments
+ *               (of all sequences together) each run holds per head.
+ *   ckpt_states kda_ckpt_count_ex(cu_seqlens_host, start_pos_host, num_seqs, ckpt_stride)
+ *               slots, the same checkpoints as kda_chunk_prefill_ex.
  *   Dk == Dv is required (Phi is carried as a Dk x Dv state), else KDA_ERR_UNSUPPORTED.
- *   start_pos   absolute position of the prompt's first token (>= 0), as start_pos of
- *               kda_chunk_prefill_ex: it places the chunk grid and the checkpoints.
- *   segments    1 .. KDA_MAX_SEGMENTS, else KDA_ERR_INVALID_ARG.
- *   ckpt_states holds kda_ckpt_count_ex({0, total_tokens}, {start_pos}, 1, ckpt_stride)
- *               slots, the same checkpoints as the one-sequence kda_chunk_prefill_ex.
- *   out_norm_gamma / out_norm_eps as in kda_chunk_prefill_ex (applied in run F).
+ *   Everything else as in kda_chunk_prefill_ex (out_norm_gamma applied in runs A and F).
  * The results equal those of kda_chunk_prefill_ex within rounding, not bit for bit
  * (S_start is formed through Phi and B instead of by the chain).  Deterministic.
  * Scratch, stream-ordered from the library's pool on `stream` and given back after the
- * call: the hand-off rings of each launch, at most (5P + C_F) * H * Dk * Dv * 4 bytes
- * of states (C_F = run F's checkpoint slots: the prompt's own plus one per segment end)
- * and T_B * H * Dv * 2 bytes of zero v for run B (T_B = the tokens of segments 1 .. P-2
- * and at most 7 before them).  `out` is written by runs A and B before run F
- * overwrites it.
- * Errors: those of kda_chunk_prefill_ex; a failing launch returns its status and
- * leaves the outputs unspecified.
+ * call: the hand-off rings of each launch, (5 S + 2 C) * H * Dk * Dv * 4 bytes of states
+ * (S = the segments of all sequences, C = checkpoint slots of one run: per segment, the
+ * stride multiples inside it and its end), total_tokens * H * Dv * 2 bytes of zero v for
+ * run B, and small index and skip arrays.  `out` is written by runs A and B before run F
+ * overwrites the segments it owns.
+ * Errors: those of kda_chunk_prefill_ex; a failing launch returns its status and leaves
+ * the outputs unspecified.
  */
-/*
- * kda_prefill_clusters_at_once -- how many (sequence, head) pairs of the prefill the
- * current device runs at the same time (each takes one 4-CTA cluster; the figure comes
- * from the CUDA occupancy calculator for the kernel's launch shape).  A call over more
- * pairs runs in waves.  For kda_chunk_prefill_segmented, segments = this / H + 1 (when
- * that is at least 3) keeps each of its runs to one wave.  Returns the count (> 0) or a negative
- * kda_status (no sm_103a device: KDA_ERR_UNSUPPORTED).
- */
-int kda_prefill_clusters_at_once(void);
+#define KDA_MAX_SEGMENTED_SEQS 128
+int kda_chunk_prefill_segmented_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                   const float* log_alpha, const uint16_t* beta,
+                                   const float* init_state,
+                                   const int32_t* cu_seqlens_host, int num_seqs, int total_tokens,
+                                   int H, int Dk, int Dv,
+                                   void* out, int out_dtype,
+                                   float* final_state, float* ckpt_states, int ckpt_stride,
+                                   int decay, const int32_t* start_pos_host, int segments,
+                                   const float* out_norm_gamma, float out_norm_eps,
+                                   void* stream);
 
 /*
- * kda_segment_plan -- the plan kda_chunk_prefill_segmented follows, on the host only.
- *
- *   bounds      (host) int32 [KDA_MAX_SEGMENTS + 1]: receives the segment bounds, in tokens
- *               from the prompt's first token: bounds[0] = 0 < bounds[1] < ... <
- *               bounds[P] = total_tokens.  Interior bounds sit on the absolute 64-token
- *               chunk grid (start_pos + bounds[p] is a multiple of 64); every segment but
- *               the last has the same number of chunks.
- *   ckpt_slots  (host) int32 [ckpt_slots_cap] or NULL: when ckpt_stride > 0 and P >= 3,
- *               receives, for each of the prompt's own checkpoints in order, the checkpoint
- *               slot it is copied from, counted over run A's slots followed by run F's (see
- *               kda_chunk_prefill_segmented; each run writes a slot at every stride multiple
- *               inside and at the end of each of its sequences, in sequence order, and run F
- *               starts with a leading sequence from b1a = bounds[1] rounded down to a
- *               multiple of 8 when that is below bounds[1]).  Fewer slots than the prompt's
- *               checkpoints -> KDA_ERR_INVALID_ARG.
- * Returns P (1 = one plain prefill, else 3 .. segments) or a negative kda_status.
+ * kda_chunk_prefill_segmented -- kda_chunk_prefill_segmented_ex for ONE sequence of
+ * total_tokens tokens whose first token sits at absolute position start_pos (>= 0):
+ * cu_seqlens = {0, total_tokens}, start positions = {start_pos}.
  */
-int kda_segment_plan(int total_tokens, int start_pos, int segments, int ckpt_stride,
-                     int32_t* bounds, int32_t* ckpt_slots, int ckpt_slots_cap);
-
 #define KDA_MAX_SEGMENTS 64
 int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                 const float* log_alpha, const uint16_t* beta,
@@ -242,6 +234,36 @@ int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint
                                 int decay, int start_pos, int segments,
                                 const float* out_norm_gamma, float out_norm_eps,
                                 void* stream);
+
+/*
+ * kda_prefill_clusters_at_once -- how many (sequence, head) pairs of the prefill the
+ * current device runs at the same time (each takes one 4-CTA cluster; the figure comes
+ * from the CUDA occupancy calculator for the kernel's launch shape).  A call over more
+ * pairs runs in waves.  For one sequence, kda_chunk_prefill_segmented with segments =
+ * this / H + 1 (when that is at least 3) keeps each of its runs to one wave.  Returns the
+ * count (> 0) or a negative kda_status (no sm_103a device: KDA_ERR_UNSUPPORTED).
+ */
+int kda_prefill_clusters_at_once(void);
+
+/*
+ * kda_segment_plan -- the plan kda_chunk_prefill_segmented follows for one sequence, on
+ * the host only.
+ *
+ *   bounds      (host) int32 [KDA_MAX_SEGMENTS + 1]: receives the segment bounds, in tokens
+ *               from the prompt's first token: bounds[0] = 0 < bounds[1] < ... <
+ *               bounds[P] = total_tokens.  Interior bounds sit on the absolute 64-token
+ *               chunk grid (start_pos + bounds[p] is a multiple of 64); every segment but
+ *               the last has the same number of chunks.
+ *   ckpt_slots  (host) int32 [ckpt_slots_cap] or NULL: when ckpt_stride > 0 and P >= 3,
+ *               receives, for each of the prompt's own checkpoints in order, the slot it is
+ *               copied from, counted over run A's slots followed by run F's.  Both runs
+ *               write the same layout: per segment, in order, a slot at every stride
+ *               multiple strictly inside it and one at its end.  Fewer slots than the
+ *               prompt's checkpoints -> KDA_ERR_INVALID_ARG.
+ * Returns P (1 = one plain prefill, else 3 .. segments) or a negative kda_status.
+ */
+int kda_segment_plan(int total_tokens, int start_pos, int segments, int ckpt_stride,
+                     int32_t* bounds, int32_t* ckpt_slots, int ckpt_slots_cap);
 
 /*
  * kda_chunk_prefill_noalloc -- kda_chunk_prefill that allocates nothing.

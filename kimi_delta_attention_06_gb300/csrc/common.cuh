@@ -14,9 +14,18 @@ constexpr int kStatusRange = -5;
 // 82944-byte blocks.
 constexpr size_t kPrefillRingBytesPerPair = 6 * 82944;
 
-// Segmented prefill: the int32 index arrays of its runs (cu_seqlens and start positions),
-// built on the host and handed to the setup kernel by value.
+// Segmented prefill: the int32 index arrays of its runs (segment bounds, start positions,
+// roles, owning sequences; the call's own cu_seqlens and start positions), built on the host
+// and handed to the setup kernel by value; the split sequences' segment ranges, handed to the
+// chain kernel by value; and the role bits of a segment.
 constexpr int kSegIdxMax = 512;
+constexpr int kSegMaxChains = 32;
+constexpr int kSegFirst = 1, kSegLast = 2, kSegMulti = 4;
+struct SegChainBuf {
+    int n;
+    int32_t g0[kSegMaxChains];
+    int32_t np[kSegMaxChains];
+};
 // Blocks per (segment, head) of the segmented prefill's transition bound (partial sums each).
 constexpr int kSegBoundBlocks = 64;
 struct SegIdxBuf {

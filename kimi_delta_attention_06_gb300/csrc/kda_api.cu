@@ -32,12 +32,13 @@ int launch_prepare_inputs(const uint16_t* xq, const uint16_t* xk, const uint16_t
                           int* status, cudaStream_t stream);
 int launch_output_norm(const void* o, int o_f32, const float* gamma, float eps, uint16_t* y, int T, int H, int D,
                        cudaStream_t stream);
-int launch_segment_setup(const SegIdxBuf& ib, int32_t* idx, float* ident, int n_ident, float* zinit, int n_zinit,
-                         const float* init_state, int* flags, int n_flags, int n_flags_set, int H, int D,
+int launch_segment_setup(const SegIdxBuf& ib, int32_t* idx, int n_seg, int o_role, int o_seq, int H, int D,
+                         const float* init_state, float* ident, float* zin, float* sst, int* skip_a, int* skip_f,
                          cudaStream_t stream);
-int launch_segment_chain(const float* phi, const int* skip, float* sst, int P, int H, int D, cudaStream_t stream);
 int launch_segment_bound(const uint16_t* k, const float* la, const uint16_t* beta, int decay, int H, int D,
-                         const int32_t* seg_start, int nseg, int lead, float* partial, int* skip,
+                         const int32_t* seg_cu, const int32_t* role, int n_seg, float* partial, int* skip_b,
+                         cudaStream_t stream);
+int launch_segment_chain(const SegChainBuf& cb, const float* phi, const int* skip_b, float* sst, int H, int D,
                          cudaStream_t stream);
 int launch_decode_multi(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* log_alpha,
                         const uint16_t* beta, float* pool, int num_slots, const int32_t* slots,
@@ -164,78 +165,98 @@ __global__ void expire_wait_kernel(unsigned long long limit_ns, int* status) {
     }
 }
 
-// The plan of a segmented prefill.
-//   b[0..P]   segment bounds, tokens from the prompt's start, on the absolute 64-token chunk
-//             grid (equal chunk counts, the last segment shorter; P = 1 when fewer than 3
-//             segments result, which runs one plain prefill)
-//   b1a       segment 1's start rounded down to a multiple of 8 tokens; the runs that start
-//             there (B and F) put a short leading sequence [b1a, b1) first (lead = 1) so that
-//             every per-token row they address stays 16-byte aligned; it is skipped
-//   checkpoints: run A (segments 0 .. P-2) writes n_ck_a slots and run F (the leading
-//             sequence, then segments 1 .. P-1) n_ck_f; keep[i] is the slot, in run A's slots
-//             followed by run F's, of the prompt's i-th own checkpoint (segment 0's come from
-//             run A, the rest from run F; every run also writes one slot at each of its
-//             sequences' ends, which is kept only at a stride multiple or the prompt's end)
+// The plan of a segmented prefill over N sequences.  Every sequence of more than a few
+// chunks is cut, on its absolute 64-token chunk grid, into P_n >= 3 segments of about L
+// chunks (L = the call's chunks / `segments`, so that every run holds about `segments`
+// segments per head); the others stay whole (P_n = 1).  All segments, in sequence order,
+// tile the call's tokens, and each of the runs A, B and F covers all of them with a skip
+// list.  Checkpoints: runs A and F write the same slot layout (per segment, the stride
+// multiples strictly inside it, then its end; a skipped segment's slots stay unwritten);
+// keep[i] is the slot, counted over run A's slots then run F's, of the call's i-th own
+// checkpoint (a split sequence's first segment from run A, the rest from run F).
 struct SegPlan {
-    int P = 1;
-    std::vector<int32_t> b;
-    int32_t b1a = 0;
-    int lead = 0;
+    int n_seg = 0;
+    std::vector<int32_t> cu, sp, role, seq;     // per segment (cu: n_seg + 1 bounds)
+    std::vector<int32_t> g0, np;                // per split sequence: first segment, segments
+    std::vector<int32_t> last;                  // per sequence: its last segment
     std::vector<int> keep;
-    int64_t n_ck_a = 0, n_ck_f = 0;
+    int64_t n_ck = 0;
 };
 
-int plan_segments(int total_tokens, int start_pos, int segments, int ckpt_stride, SegPlan* out) {
-    if (segments < 1 || segments > KDA_MAX_SEGMENTS || start_pos < 0 || total_tokens < 0) return KDA_ERR_INVALID_ARG;
+constexpr int kSegMaxSeqs = 32;
+
+int plan_segments(const int32_t* cu_host, const int32_t* sp_host, int N, int segments, int ckpt_stride,
+                  SegPlan* out) {
+    if (segments < 1 || segments > KDA_MAX_SEGMENTS || N < 0) return KDA_ERR_INVALID_ARG;
     if (ckpt_stride < 0 || ckpt_stride % 64 != 0) return KDA_ERR_INVALID_ARG;
-    if (static_cast<int64_t>(start_pos) + total_tokens > INT32_MAX) return KDA_ERR_INVALID_ARG;
+    if (N > 0 && !cu_host) return KDA_ERR_INVALID_ARG;
     const int C = 64;
-    const int64_t s0 = start_pos, T = total_tokens;
-    const int64_t c_first = s0 / C, c_end = (s0 + T + C - 1) / C;
-    const int64_t n_chunks = T > 0 ? c_end - c_first : 0;
-    int P = 1;
-    int64_t per = n_chunks;
-    if (segments >= 3 && n_chunks >= 3) {
-        per = (n_chunks + segments - 1) / segments;
-        P = static_cast<int>((n_chunks + per - 1) / per);
-        if (P < 3) P = 1;
+    std::vector<int64_t> chunks(N);
+    int64_t total = 0;
+    for (int n = 0; n < N; ++n) {
+        const int64_t len = static_cast<int64_t>(cu_host[n + 1]) - cu_host[n];
+        const int64_t s0 = sp_host ? sp_host[n] : 0;
+        if (len < 0 || s0 < 0 || s0 + len > INT32_MAX) return KDA_ERR_INVALID_ARG;
+        chunks[n] = len > 0 ? (s0 + len + C - 1) / C - s0 / C : 0;
+        total += chunks[n];
     }
-    std::vector<int32_t> b(P + 1);
-    for (int p = 0; p <= P; ++p) {
-        const int64_t x = C * (c_first + p * per) - s0;
-        b[p] = static_cast<int32_t>(x < 0 ? 0 : (x > T ? T : x));
-    }
-    b[0] = 0;
-    b[P] = total_tokens;
-    const int32_t b1a = P >= 3 ? (b[1] & ~7) : 0;
-    const int lead = (P >= 3 && b1a < b[1]) ? 1 : 0;
-    std::vector<int> keep;
-    int64_t n_a = 0, n_f = 0;
-    if (ckpt_stride > 0 && P >= 3) {
-        // slots of one sequence [a, e) (absolute positions): the stride multiples strictly inside,
-        // then its end; `own` marks those that are the prompt's checkpoints
-        auto slots = [&](int64_t a, int64_t e, bool last, int64_t base, int64_t* n, bool own_any) {
-            for (int64_t m = (a / ckpt_stride + 1) * ckpt_stride; m < e; m += ckpt_stride) {
-                if (own_any) keep.push_back(static_cast<int>(base + *n));
-                ++*n;
+    // segment length in chunks; sequences of fewer than 3 such segments stay whole
+    const bool split_any = segments >= 3 && N <= kSegMaxSeqs && total >= 3;
+    const int64_t L = split_any ? (total + segments - 1) / segments : 0;
+    SegPlan pl;
+    pl.cu.push_back(0);
+    for (int n = 0; n < N; ++n) {
+        const int64_t t0 = cu_host[n], len = static_cast<int64_t>(cu_host[n + 1]) - t0;
+        const int64_t s0 = sp_host ? sp_host[n] : 0;
+        int P = 1;
+        if (split_any && chunks[n] >= 3) {
+            P = static_cast<int>((chunks[n] + L - 1) / L);
+            if (P < 3) P = 1;
+        }
+        if (P > 1 && static_cast<int>(pl.g0.size()) >= kda::kSegMaxChains) P = 1;
+        const int g_first = pl.n_seg;
+        for (int p = 0; p < P; ++p) {
+            int64_t e = len;
+            if (p + 1 < P) {
+                const int64_t x = C * (s0 / C + (p + 1) * L) - s0;
+                e = x < 0 ? 0 : (x > len ? len : x);
             }
-            if (own_any && (e % ckpt_stride == 0 || last)) keep.push_back(static_cast<int>(base + *n));
-            ++*n;
-        };
-        for (int p = 0; p <= P - 2; ++p) slots(s0 + b[p], s0 + b[p + 1], false, 0, &n_a, p == 0);
-        if (lead) slots(s0 + b1a, s0 + b[1], false, 0, &n_f, false);
-        for (int p = 1; p <= P - 1; ++p) slots(s0 + b[p], s0 + b[p + 1], p == P - 1, n_a, &n_f, true);
-        const int32_t cu1[2] = {0, total_tokens};
-        const int32_t sp1[1] = {start_pos};
-        if (static_cast<int64_t>(keep.size()) != kda_ckpt_count_ex(cu1, sp1, 1, ckpt_stride)) return KDA_ERR_INVALID_ARG;
+            const int64_t a = pl.cu.back() - t0;
+            pl.cu.push_back(static_cast<int32_t>(t0 + e));
+            pl.sp.push_back(static_cast<int32_t>(s0 + a));
+            int r = 0;
+            if (p == 0) r |= kda::kSegFirst;
+            if (p == P - 1) r |= kda::kSegLast;
+            if (P > 1) r |= kda::kSegMulti;
+            pl.role.push_back(r);
+            pl.seq.push_back(n);
+            ++pl.n_seg;
+        }
+        if (P > 1) { pl.g0.push_back(g_first); pl.np.push_back(P); }
+        pl.last.push_back(pl.n_seg - 1);
     }
-    out->P = P;
-    out->b = std::move(b);
-    out->b1a = b1a;
-    out->lead = lead;
-    out->keep = std::move(keep);
-    out->n_ck_a = n_a;
-    out->n_ck_f = n_f;
+    if (ckpt_stride > 0) {
+        // slot layout per segment, then which slots are the call's own checkpoints
+        std::vector<int64_t> base(pl.n_seg + 1, 0);
+        for (int g = 0; g < pl.n_seg; ++g) {
+            const int64_t a = pl.sp[g], e = a + (pl.cu[g + 1] - pl.cu[g]);
+            base[g + 1] = base[g] + (e > a ? (e - 1) / ckpt_stride - a / ckpt_stride + 1 : 0);
+        }
+        pl.n_ck = base[pl.n_seg];
+        for (int g = 0; g < pl.n_seg; ++g) {
+            const int64_t a = pl.sp[g], e = a + (pl.cu[g + 1] - pl.cu[g]);
+            if (e <= a) continue;
+            const bool from_a = (pl.role[g] & kda::kSegMulti) && (pl.role[g] & kda::kSegFirst);
+            const int64_t off = from_a ? 0 : pl.n_ck;
+            int64_t s = base[g];
+            for (int64_t m = (a / ckpt_stride + 1) * ckpt_stride; m < e; m += ckpt_stride)
+                pl.keep.push_back(static_cast<int>(off + s++));
+            if (e % ckpt_stride == 0 || (pl.role[g] & kda::kSegLast)) pl.keep.push_back(static_cast<int>(off + s));
+        }
+        if (static_cast<int64_t>(pl.keep.size()) != kda_ckpt_count_ex(cu_host, sp_host, N, ckpt_stride))
+            return KDA_ERR_INVALID_ARG;
+    }
+    *out = std::move(pl);
     return KDA_OK;
 }
 
@@ -266,15 +287,18 @@ int kda_chunk_size(void) { return 64; }
 
 int kda_segment_plan(int total_tokens, int start_pos, int segments, int ckpt_stride, int32_t* bounds,
                      int32_t* ckpt_slots, int ckpt_slots_cap) {
-    if (!bounds) return KDA_ERR_INVALID_ARG;
+    if (!bounds || total_tokens < 0 || start_pos < 0) return KDA_ERR_INVALID_ARG;
+    const int32_t cu1[2] = {0, total_tokens};
+    const int32_t sp1[1] = {start_pos};
     SegPlan plan;
-    const int rc = plan_segments(total_tokens, start_pos, segments, ckpt_stride, &plan);
+    const int rc = plan_segments(cu1, sp1, 1, segments, ckpt_stride, &plan);
     if (rc != KDA_OK) return rc;
-    if (ckpt_slots && static_cast<int64_t>(plan.keep.size()) > ckpt_slots_cap) return KDA_ERR_INVALID_ARG;
-    for (int p = 0; p <= plan.P; ++p) bounds[p] = plan.b[p];
-    if (ckpt_slots)
+    const bool split = plan.n_seg > 1;
+    if (ckpt_slots && split && static_cast<int64_t>(plan.keep.size()) > ckpt_slots_cap) return KDA_ERR_INVALID_ARG;
+    for (int g = 0; g <= plan.n_seg; ++g) bounds[g] = plan.cu[g];
+    if (ckpt_slots && split)
         for (size_t i = 0; i < plan.keep.size(); ++i) ckpt_slots[i] = plan.keep[i];
-    return plan.P;
+    return plan.n_seg;
 }
 
 int kda_prefill_clusters_at_once(void) {
@@ -362,67 +386,52 @@ int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v
                           start_pos_host, out_norm_gamma, out_norm_eps, stream);
 }
 
-int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                                const float* log_alpha, const uint16_t* beta,
-                                const float* init_state,
-                                int total_tokens, int H, int Dk, int Dv,
-                                void* out, int out_dtype,
-                                float* final_state, float* ckpt_states, int ckpt_stride,
-                                int decay, int start_pos, int segments,
-                                const float* out_norm_gamma, float out_norm_eps, void* stream) {
-    if (segments < 1 || segments > KDA_MAX_SEGMENTS || start_pos < 0 || total_tokens < 0) return KDA_ERR_INVALID_ARG;
-    if (static_cast<int64_t>(start_pos) + total_tokens > INT32_MAX) return KDA_ERR_INVALID_ARG;
-    const int32_t cu1[2] = {0, total_tokens};
-    // (the one-sequence checks of the plain call; cu1 stands in for the device cu_seqlens,
-    // which this entry point builds itself)
-    int rc = check_prefill_args(q, k, v, log_alpha, beta, init_state, cu1, cu1, 1, total_tokens, H, Dk, Dv, out,
-                                out_dtype, final_state, ckpt_states, ckpt_stride, decay);
+int kda_chunk_prefill_segmented_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                   const float* log_alpha, const uint16_t* beta,
+                                   const float* init_state,
+                                   const int32_t* cu_seqlens_host, int num_seqs, int total_tokens,
+                                   int H, int Dk, int Dv,
+                                   void* out, int out_dtype,
+                                   float* final_state, float* ckpt_states, int ckpt_stride,
+                                   int decay, const int32_t* start_pos_host, int segments,
+                                   const float* out_norm_gamma, float out_norm_eps, void* stream) {
+    if (segments < 1 || segments > KDA_MAX_SEGMENTS || num_seqs < 0 || total_tokens < 0) return KDA_ERR_INVALID_ARG;
+    if (num_seqs > KDA_MAX_SEGMENTED_SEQS) return KDA_ERR_UNSUPPORTED;
+    // (the checks of the plain call; the host cu_seqlens stands in for the device copy, which
+    // this entry point builds itself)
+    int rc = check_prefill_args(q, k, v, log_alpha, beta, init_state, cu_seqlens_host, cu_seqlens_host, num_seqs,
+                                total_tokens, H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, decay);
     if (rc != KDA_OK) return rc;
     if (Dk != Dv) return KDA_ERR_UNSUPPORTED;
     if (out_norm_gamma && (!aligned16(out_norm_gamma) || !(out_norm_eps >= 0.f) || !(out_norm_eps < 3.0e38f)))
         return KDA_ERR_INVALID_ARG;
+    if (start_pos_host)
+        for (int n = 0; n < num_seqs; ++n)
+            if (start_pos_host[n] < 0) return KDA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return KDA_OK;
 
     SegPlan plan;
-    rc = plan_segments(total_tokens, start_pos, segments, ckpt_states ? ckpt_stride : 0, &plan);
+    rc = plan_segments(cu_seqlens_host, start_pos_host, num_seqs, segments, ckpt_states ? ckpt_stride : 0, &plan);
     if (rc != KDA_OK) return rc;
-    const int P = plan.P;
-    const std::vector<int32_t>& b = plan.b;
+    const int n_seg = plan.n_seg;
+    const bool split = !plan.g0.empty();
 
-    const int32_t b1a = plan.b1a;
-    const int lead = plan.lead;
-    const int nA = P >= 3 ? P - 1 : 0;              // run A: segments 0 .. P-2
-    const int nB = P >= 3 ? P - 2 + lead : 0;       // run B: [leading,] segments 1 .. P-2
-    const int nF = P >= 3 ? P - 1 + lead : 0;       // run F: [leading,] segments 1 .. P-1
-
-    // host index arrays (cu_seqlens, start positions) of the runs; B and F count tokens from b1a
-    std::vector<int32_t> a_cu, a_sp, b_cu, b_sp, f_cu, f_sp, bnd(b.begin(), b.end()), sp0{start_pos};
-    if (P >= 3) {
-        for (int p = 0; p <= nA; ++p) a_cu.push_back(b[p]);
-        for (int p = 0; p < nA; ++p) a_sp.push_back(start_pos + b[p]);
-        b_cu.push_back(0);
-        f_cu.push_back(0);
-        if (lead) {
-            b_cu.push_back(b[1] - b1a); b_sp.push_back(start_pos + b1a);
-            f_cu.push_back(b[1] - b1a); f_sp.push_back(start_pos + b1a);
-        }
-        for (int p = 1; p <= P - 2; ++p) { b_cu.push_back(b[p + 1] - b1a); b_sp.push_back(start_pos + b[p]); }
-        for (int p = 1; p <= P - 1; ++p) { f_cu.push_back(b[p + 1] - b1a); f_sp.push_back(start_pos + b[p]); }
-    }
-    if (a_cu.size() + a_sp.size() + b_cu.size() + b_sp.size() + f_cu.size() + f_sp.size() + bnd.size() + sp0.size() >
-        static_cast<size_t>(kda::kSegIdxMax))
-        return KDA_ERR_INVALID_ARG;
+    // device index arrays: segment bounds, start positions, roles, owning sequences; the
+    // call's own cu_seqlens and start positions
+    std::vector<int32_t> ucu(cu_seqlens_host, cu_seqlens_host + num_seqs + 1), usp(num_seqs, 0);
+    if (start_pos_host) usp.assign(start_pos_host, start_pos_host + num_seqs);
+    const size_t n_idx = (split ? plan.cu.size() + plan.sp.size() + plan.role.size() + plan.seq.size() : 0) +
+                         ucu.size() + usp.size();
+    if (n_idx > static_cast<size_t>(kda::kSegIdxMax)) return KDA_ERR_UNSUPPORTED;
     kda::SegIdxBuf ib;
     ib.n = 0;
-    int o_acu = 0, o_asp = 0, o_bcu = 0, o_bsp = 0, o_fcu = 0, o_fsp = 0, o_bnd = 0, o_sp0 = 0;
+    int o_cu = 0, o_sp = 0, o_role = 0, o_seq = 0, o_ucu = 0, o_usp = 0;
     auto put = [&](const std::vector<int32_t>& x, int* off) {
         *off = ib.n;
         for (int32_t e : x) ib.v[ib.n++] = e;
     };
-    put(a_cu, &o_acu); put(a_sp, &o_asp); put(b_cu, &o_bcu); put(b_sp, &o_bsp); put(f_cu, &o_fcu); put(f_sp, &o_fsp);
-    put(bnd, &o_bnd); put(sp0, &o_sp0);
-
-    const std::vector<int>& keep = plan.keep;
-    const int64_t n_ck = plan.n_ck_a + plan.n_ck_f;
+    if (split) { put(plan.cu, &o_cu); put(plan.sp, &o_sp); put(plan.role, &o_role); put(plan.seq, &o_seq); }
+    put(ucu, &o_ucu); put(usp, &o_usp);
 
     int* status = nullptr;
     rc = device_setup(&status);
@@ -431,29 +440,40 @@ int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint
     rc = workspace_pool(&pool);
     if (rc != KDA_OK) return rc;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-
-    // scratch: index arrays | run A initial states | run B identities | Phi | S_start |
-    // run F final states | checkpoints of runs A and F | zero v of run B | bound partial sums |
-    // run B skip list | run F skip list
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     const size_t slot = static_cast<size_t>(H) * Dk * Dv * sizeof(float);
     const size_t slot_f = slot / sizeof(float);
-    const bool zinit_needed = P >= 3 && init_state != nullptr;
-    const int64_t tB = P >= 3 ? static_cast<int64_t>(b[P - 1]) - b1a : 0;
-    const int64_t tF = P >= 3 ? static_cast<int64_t>(total_tokens) - b1a : 0;
-    const int nseg = P >= 3 ? P - 2 : 0;
-    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+
+    if (!split) {   // no sequence is long enough to split: one plain prefill
+        int32_t* idx = nullptr;
+        if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&idx), up(sizeof(int32_t) * ib.n), pool, st) !=
+            cudaSuccess)
+            return KDA_ERR_CUDA;
+        rc = kda::launch_segment_setup(ib, idx, 0, 0, 0, H, Dk, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                       st) == 0 ? KDA_OK : KDA_ERR_CUDA;
+        if (rc == KDA_OK)
+            rc = prefill_pooled(q, k, v, log_alpha, beta, init_state, idx + o_ucu, ucu.data(), num_seqs, total_tokens,
+                                H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, decay,
+                                idx + o_usp, usp.data(), out_norm_gamma, out_norm_eps, stream);
+        const bool freed = cudaFreeAsync(idx, st) == cudaSuccess;
+        return rc != KDA_OK ? rc : (freed ? KDA_OK : KDA_ERR_CUDA);
+    }
+
+    // scratch: index arrays | run A initial states | identities | Phi | S_start | run F final
+    // states | checkpoints of runs A and F | zero v | bound partial sums | skip lists A, B, F
     const size_t o_idx = 0;
     const size_t o_zin = o_idx + up(sizeof(int32_t) * ib.n);
-    const size_t o_idn = o_zin + (zinit_needed ? slot * nA : 0);
-    const size_t o_phi = o_idn + slot * nB;
-    const size_t o_sst = o_phi + slot * nB;
-    const size_t o_fin = o_sst + (P >= 3 ? slot * P : 0);
-    const size_t o_ck = o_fin + slot * nF;
-    const size_t o_zv = o_ck + slot * static_cast<size_t>(n_ck);
-    const size_t o_part = o_zv + up(static_cast<size_t>(tB) * H * Dv * 2);
-    const size_t o_skip = o_part + up(sizeof(float) * static_cast<size_t>(nseg) * H * kda::kSegBoundBlocks);
-    const size_t o_fskip = o_skip + up(sizeof(int) * static_cast<size_t>(nB) * H);
-    const size_t total = o_fskip + up(sizeof(int) * static_cast<size_t>(nF) * H);
+    const size_t o_idn = o_zin + slot * n_seg;
+    const size_t o_phi = o_idn + slot * n_seg;
+    const size_t o_sst = o_phi + slot * n_seg;
+    const size_t o_fin = o_sst + slot * n_seg;
+    const size_t o_ck = o_fin + slot * n_seg;
+    const size_t o_zv = o_ck + slot * static_cast<size_t>(2 * plan.n_ck);
+    const size_t o_part = o_zv + up(static_cast<size_t>(total_tokens) * H * Dv * 2);
+    const size_t o_ska = o_part + up(sizeof(float) * static_cast<size_t>(n_seg) * H * kda::kSegBoundBlocks);
+    const size_t o_skb = o_ska + up(sizeof(int) * static_cast<size_t>(n_seg) * H);
+    const size_t o_skf = o_skb + up(sizeof(int) * static_cast<size_t>(n_seg) * H);
+    const size_t total = o_skf + up(sizeof(int) * static_cast<size_t>(n_seg) * H);
     uint8_t* ws = nullptr;
     if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), total, pool, st) != cudaSuccess) return KDA_ERR_CUDA;
     int32_t* idx = reinterpret_cast<int32_t*>(ws + o_idx);
@@ -465,70 +485,86 @@ int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint
     float* ck = reinterpret_cast<float*>(ws + o_ck);
     uint16_t* zv = reinterpret_cast<uint16_t*>(ws + o_zv);
     float* part = reinterpret_cast<float*>(ws + o_part);
-    int* skip = reinterpret_cast<int*>(ws + o_skip);
-    int* fskip = reinterpret_cast<int*>(ws + o_fskip);
-
+    int* skip_a = reinterpret_cast<int*>(ws + o_ska);
+    int* skip_b = reinterpret_cast<int*>(ws + o_skb);
+    int* skip_f = reinterpret_cast<int*>(ws + o_skf);
     auto finish = [&](int r) {
         const bool freed = cudaFreeAsync(ws, st) == cudaSuccess;
         return r != KDA_OK ? r : (freed ? KDA_OK : KDA_ERR_CUDA);
     };
-    if (kda::launch_segment_setup(ib, idx, idn, nB, zin, zinit_needed ? nA : 0, init_state, fskip, nF * H, lead * H,
-                                  H, Dk, st) != 0)
-        return finish(KDA_ERR_CUDA);
-    if (P < 3)   // one plain prefill
-        return finish(prefill_pooled(q, k, v, log_alpha, beta, init_state, idx + o_bnd, bnd.data(), 1, total_tokens,
-                                     H, Dk, Dv, out, out_dtype, final_state, ckpt_states, ckpt_stride, decay,
-                                     idx + o_sp0, sp0.data(), out_norm_gamma, out_norm_eps, stream));
+    const int32_t* seg_cu = idx + o_cu;
+    const int32_t* seg_sp = idx + o_sp;
+    const bool want_ck = ckpt_states != nullptr && ckpt_stride > 0;
 
-    if (tB > 0 && cudaMemsetAsync(zv, 0, static_cast<size_t>(tB) * H * Dv * 2, st) != cudaSuccess)
+    if (kda::launch_segment_setup(ib, idx, n_seg, o_role, o_seq, H, Dk, init_state, idn, zin, sst, skip_a, skip_f,
+                                  st) != 0)
         return finish(KDA_ERR_CUDA);
-    // which transitions cannot matter (their norm bound is below fp32 rounding): those runs are
-    // skipped and their segment starts from B alone
-    if (kda::launch_segment_bound(k, log_alpha, beta, decay, H, Dk, idx + o_bnd + 1, nseg, lead, part, skip, st) != 0)
+    if (total_tokens > 0 && cudaMemsetAsync(zv, 0, static_cast<size_t>(total_tokens) * H * Dv * 2, st) != cudaSuccess)
         return finish(KDA_ERR_CUDA);
-    const size_t la_row = decay == KDA_DECAY_CHANNEL ? static_cast<size_t>(Dk) : 1;
-    const size_t osz = out_dtype == KDA_OUT_F32 ? 4 : 2;
-    const size_t tok = static_cast<size_t>(b1a) * H;        // token rows before b1a
-    // A: segments 0 .. P-2.  Segment 0 starts from the prompt's initial state, so its outputs
-    // (normed, if asked) and checkpoints are final; its final state lands in S_start[1], and
-    // B_p (p >= 1, from zeros) in S_start[p + 1]
-    rc = prefill_pooled(q, k, v, log_alpha, beta, zinit_needed ? zin : nullptr, idx + o_acu, a_cu.data(), nA,
-                        b[P - 1], H, Dk, Dv, out, out_dtype, sst + slot_f, ckpt_states ? ck : nullptr,
-                        ckpt_states ? ckpt_stride : 0, decay, idx + o_asp, a_sp.data(), out_norm_gamma, out_norm_eps,
-                        stream);
+    // which transitions cannot matter (their norm bound is below fp32 rounding): run B leaves
+    // them out and the chain takes the segment's B alone
+    if (kda::launch_segment_bound(k, log_alpha, beta, decay, H, Dk, seg_cu, idx + o_role, n_seg, part, skip_b, st) != 0)
+        return finish(KDA_ERR_CUDA);
+    // A: a split sequence's segments but its last; its first segment from the sequence's initial
+    // state (outputs, norm and checkpoints final), the others from zeros (B); the end state of
+    // segment g lands in S_start slot g + 1
+    rc = prefill_pooled(q, k, v, log_alpha, beta, zin, seg_cu, plan.cu.data(), n_seg, total_tokens, H, Dk, Dv, out,
+                        out_dtype, sst + slot_f, want_ck ? ck : nullptr, want_ck ? ckpt_stride : 0, decay, seg_sp,
+                        plan.sp.data(), out_norm_gamma, out_norm_eps, stream, skip_a);
     if (rc != KDA_OK) return finish(rc);
-    // B: from S_start = I with v = 0, tokens from b1a on (the leading sequence, if any, first)
-    rc = prefill_pooled(q + tok * Dk, k + tok * Dk, zv, log_alpha ? log_alpha + tok * la_row : nullptr, beta + tok,
-                        idn, idx + o_bcu, b_cu.data(), nB, static_cast<int>(tB), H, Dk, Dv,
-                        static_cast<uint8_t*>(out) + tok * Dv * osz, out_dtype, phi, nullptr, 0, decay,
-                        idx + o_bsp, b_sp.data(), nullptr, 0.f, stream, skip);
+    // B: the middle segments, from S_start = I with v = 0 (Phi), where the bound does not rule them out
+    rc = prefill_pooled(q, k, zv, log_alpha, beta, idn, seg_cu, plan.cu.data(), n_seg, total_tokens, H, Dk, Dv, out,
+                        out_dtype, phi, nullptr, 0, decay, seg_sp, plan.sp.data(), nullptr, 0.f, stream, skip_b);
     if (rc != KDA_OK) return finish(rc);
-    // chain: S_start[p + 1] = Phi_p S_start[p] + B_p, p = 1 .. P-2 (Phi_p in slot p - 1 + lead)
-    if (kda::launch_segment_chain(phi + static_cast<size_t>(lead) * slot_f, skip + lead * H, sst, P, H, Dk, st) != 0)
-        return finish(KDA_ERR_CUDA);
-    // F: segments 1 .. P-1 from S_start[1 ..] (the leading sequence, skipped, takes slot 0)
-    rc = prefill_pooled(q + tok * Dk, k + tok * Dk, v + tok * Dv, log_alpha ? log_alpha + tok * la_row : nullptr,
-                        beta + tok, sst + (lead ? 0 : slot_f), idx + o_fcu, f_cu.data(), nF, static_cast<int>(tF), H,
-                        Dk, Dv, static_cast<uint8_t*>(out) + tok * Dv * osz, out_dtype, fin,
-                        ckpt_states ? ck + static_cast<size_t>(plan.n_ck_a) * slot_f : nullptr,
-                        ckpt_states ? ckpt_stride : 0, decay, idx + o_fsp, f_sp.data(), out_norm_gamma, out_norm_eps,
-                        stream, lead ? fskip : nullptr);
+    // chain: S_start[p + 1] = Phi_p S_start[p] + B_p along every split sequence
+    kda::SegChainBuf cb;
+    cb.n = static_cast<int>(plan.g0.size());
+    for (int z = 0; z < cb.n; ++z) { cb.g0[z] = plan.g0[z]; cb.np[z] = plan.np[z]; }
+    if (kda::launch_segment_chain(cb, phi, skip_b, sst, H, Dk, st) != 0) return finish(KDA_ERR_CUDA);
+    // F: every segment but the first of a split sequence, from its S_start
+    rc = prefill_pooled(q, k, v, log_alpha, beta, sst, seg_cu, plan.cu.data(), n_seg, total_tokens, H, Dk, Dv, out,
+                        out_dtype, fin, want_ck ? ck + static_cast<size_t>(plan.n_ck) * slot_f : nullptr,
+                        want_ck ? ckpt_stride : 0, decay, seg_sp, plan.sp.data(), out_norm_gamma, out_norm_eps, stream,
+                        skip_f);
     if (rc != KDA_OK) return finish(rc);
-    if (final_state &&
-        cudaMemcpyAsync(final_state, fin + static_cast<size_t>(nF - 1) * slot_f, slot, cudaMemcpyDeviceToDevice,
-                        st) != cudaSuccess)
-        return finish(KDA_ERR_CUDA);
-    // the prompt's checkpoints, in order: runs of consecutive kept slots, one copy each
-    for (size_t i = 0, u = 0; i < keep.size();) {
-        size_t j = i + 1;
-        while (j < keep.size() && keep[j] == keep[j - 1] + 1) ++j;
-        if (cudaMemcpyAsync(ckpt_states + u * (slot / sizeof(float)), ck + static_cast<size_t>(keep[i]) * (slot / sizeof(float)),
-                            (j - i) * slot, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-            return finish(KDA_ERR_CUDA);
-        u += j - i;
-        i = j;
+    // each sequence's final state: its last segment's, from run F
+    if (final_state)
+        for (int n = 0; n < num_seqs; ++n)
+            if (cudaMemcpyAsync(final_state + static_cast<size_t>(n) * slot_f,
+                                fin + static_cast<size_t>(plan.last[n]) * slot_f, slot, cudaMemcpyDeviceToDevice,
+                                st) != cudaSuccess)
+                return finish(KDA_ERR_CUDA);
+    // the call's checkpoints, in order: runs of consecutive kept slots, one copy each
+    if (want_ck) {
+        const std::vector<int>& keep = plan.keep;
+        for (size_t i = 0, u = 0; i < keep.size();) {
+            size_t j = i + 1;
+            while (j < keep.size() && keep[j] == keep[j - 1] + 1) ++j;
+            if (cudaMemcpyAsync(ckpt_states + u * slot_f, ck + static_cast<size_t>(keep[i]) * slot_f, (j - i) * slot,
+                                cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+                return finish(KDA_ERR_CUDA);
+            u += j - i;
+            i = j;
+        }
     }
     return finish(KDA_OK);
+}
+
+int kda_chunk_prefill_segmented(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                const float* log_alpha, const uint16_t* beta,
+                                const float* init_state,
+                                int total_tokens, int H, int Dk, int Dv,
+                                void* out, int out_dtype,
+                                float* final_state, float* ckpt_states, int ckpt_stride,
+                                int decay, int start_pos, int segments,
+                                const float* out_norm_gamma, float out_norm_eps, void* stream) {
+    if (total_tokens < 0 || start_pos < 0) return KDA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(start_pos) + total_tokens > INT32_MAX) return KDA_ERR_INVALID_ARG;
+    const int32_t cu1[2] = {0, total_tokens};
+    const int32_t sp1[1] = {start_pos};
+    return kda_chunk_prefill_segmented_ex(q, k, v, log_alpha, beta, init_state, cu1, 1, total_tokens, H, Dk, Dv, out,
+                                          out_dtype, final_state, ckpt_states, ckpt_stride, decay, sp1, segments,
+                                          out_norm_gamma, out_norm_eps, stream);
 }
 
 int kda_chunk_prefill_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t* v,

@@ -1,13 +1,16 @@
-// kda_segment.cu -- device helpers of the segmented prefill (kda_chunk_prefill_segmented).
+// kda_segment.cu -- device helpers of the segmented prefill (kda_chunk_prefill_segmented_ex).
 //
 // The KDA recurrence S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
 // (Kimi Linear, "Kimi Delta Attention", the per-channel gated delta rule) is linear in the
 // pair (S_0, v): over a segment of tokens, S_end = Phi S_0 + B, where Phi (Dk x Dk) is the
 // product of the segment's per-token transitions and B is the state the segment reaches
 // from S_0 = 0.  The prefill kernel itself yields both: B is the final state of a run from
-// zeros, and Phi the final state of a run from S_0 = I with v = 0.  The helpers here set
-// up those runs (segment bounds, identity and zero initial states) and chain the segment
-// results: S_start[p + 1] = Phi_p S_start[p] + B_p, serially over the segments.
+// zeros, and Phi the final state of a run from S_0 = I with v = 0.  Each sequence of a call
+// is cut into segments; three prefill launches run over the list of all segments, each with
+// a skip list that picks the segments it forms (A: B_p and the first segment's true end
+// state; B: Phi_p; F: the outputs from the chained start states).  The helpers here set up
+// those runs and chain the segment results of each sequence serially:
+// S_start[p + 1] = Phi_p S_start[p] + B_p.
 //
 // A transition that cannot matter is not formed.  Each token's factor has spectral norm at
 // most max_c alpha_{t,c} * max(1, |1 - beta_t |k_t|^2|) (the projection I - beta k k^T has
@@ -25,38 +28,57 @@ namespace kda {
 
 namespace {
 
-// The runs' index arrays (built on the host), then their initial states: ident
-// [n_ident, H, D, D] = I per head; zinit [n_zinit, H, D, D] = the prompt's initial state in
-// slot 0 (zeros if none) and zeros elsewhere; and a skip list flags [n_flags] whose first
-// n_flags_set entries are 1 (the leading sequence of a run), the rest 0.
-__global__ void seg_setup_kernel(SegIdxBuf ib, int32_t* idx, float* ident, int n_ident, float* zinit, int n_zinit,
-                                 const float* init_state, int* flags, int n_flags, int n_flags_set, int H, int D) {
-    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const long long nth = static_cast<long long>(gridDim.x) * blockDim.x;
-    for (long long e = tid; e < ib.n; e += nth) idx[e] = ib.v[e];
-    for (long long e = tid; e < n_flags; e += nth) flags[e] = e < n_flags_set ? 1 : 0;
-    const long long per = static_cast<long long>(H) * D * D;                           // one state slot
-    for (long long e = tid; e < static_cast<long long>(n_ident) * per; e += nth) {
-        const int rc = static_cast<int>(e % (static_cast<long long>(D) * D));
-        ident[e] = (rc / D == rc % D) ? 1.f : 0.f;
-    }
-    for (long long e = tid; e < static_cast<long long>(n_zinit) * per; e += nth)
-        zinit[e] = (e < per && init_state) ? init_state[e] : 0.f;
-}
-
 constexpr float kSkipLogNorm = -44.3614195558365f;   // -64 ln 2
 constexpr int kBoundBlocks = kSegBoundBlocks;
 
+// Segment roles (bits of the role array): first / last segment of its sequence, and whether
+// the sequence is split at all (a sequence of one segment runs as a plain prefill in run F).
+__device__ __forceinline__ bool runs_in_a(int r) { return (r & kSegMulti) && !(r & kSegLast); }
+__device__ __forceinline__ bool runs_in_b(int r) { return (r & kSegMulti) && !(r & (kSegFirst | kSegLast)); }
+__device__ __forceinline__ bool runs_in_f(int r) { return !(r & kSegMulti) || !(r & kSegFirst); }
+
+// Copies the index arrays (built on the host) to the device, then per segment g:
+//   ident[g] = I;  zin[g] = the sequence's initial state if g is its first segment, else 0
+//   (run A's initial states);  sst[g] = the sequence's initial state if g is its first
+//   segment (run F's initial state of an unsplit sequence; run A and the chain fill the
+//   others);  skip_a / skip_f = whether runs A / F leave the segment out (per head).
+__global__ void seg_setup_kernel(SegIdxBuf ib, int32_t* idx, int n_seg, int o_role, int o_seq, int H, int D,
+                                 const float* init_state, float* ident, float* zin, float* sst, int* skip_a,
+                                 int* skip_f) {
+    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long nth = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long e = tid; e < ib.n; e += nth) idx[e] = ib.v[e];
+    for (long long e = tid; e < static_cast<long long>(n_seg) * H; e += nth) {
+        const int r = ib.v[o_role + e / H];
+        skip_a[e] = runs_in_a(r) ? 0 : 1;
+        skip_f[e] = runs_in_f(r) ? 0 : 1;
+    }
+    const long long per = static_cast<long long>(H) * D * D;                           // one state slot
+    for (long long e = tid; e < static_cast<long long>(n_seg) * per; e += nth) {
+        const int g = static_cast<int>(e / per);
+        const long long w = e % per;
+        const int rc = static_cast<int>(w % (static_cast<long long>(D) * D));
+        ident[e] = (rc / D == rc % D) ? 1.f : 0.f;
+        const bool first = (ib.v[o_role + g] & kSegFirst) != 0;
+        const float s0 = (first && init_state) ? init_state[static_cast<long long>(ib.v[o_seq + g]) * per + w] : 0.f;
+        zin[e] = s0;
+        if (first) sst[e] = s0;
+    }
+}
+
 // Partial sums of the bound above: grid (kBoundBlocks, segments, H), one warp per token
-// (lanes over channels), warps and blocks strided over the segment's tokens.
-// seg_start [nseg + 1]: token bounds of the segments; partial [(seg * H + h) * kBoundBlocks + blk].
+// (lanes over channels), warps and blocks strided over the segment's tokens; segments that
+// run B leaves out are not read.  seg_cu [n_seg + 1]: token bounds of the segments;
+// partial [(seg * H + h) * kBoundBlocks + blk].
 __global__ void __launch_bounds__(256) seg_bound_kernel(const uint16_t* __restrict__ k, const float* __restrict__ la,
                                                         const uint16_t* __restrict__ beta, int decay, int H, int D,
-                                                        const int32_t* __restrict__ seg_start, float* partial) {
+                                                        const int32_t* __restrict__ seg_cu,
+                                                        const int32_t* __restrict__ role, float* partial) {
     __shared__ float s_w[8];
     const int blk = blockIdx.x, seg = blockIdx.y, h = blockIdx.z;
+    if (!runs_in_b(role[seg])) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t0 = seg_start[seg], t1 = seg_start[seg + 1];
+    const int t0 = seg_cu[seg], t1 = seg_cu[seg + 1];
     const bool lane_ok = 4 * lane < D;
     float acc = 0.f;
     for (int t = t0 + blk * 8 + warp; t < t1; t += 8 * kBoundBlocks) {
@@ -92,21 +114,22 @@ __global__ void __launch_bounds__(256) seg_bound_kernel(const uint16_t* __restri
     }
 }
 
-// The skip list of the transitions' run: row 0 is the leading sequence when there is one
-// (its result is never used), then one row per segment; decay 2 (none) skips nothing.
-__global__ void seg_flag_kernel(const float* partial, int nseg, int H, int lead, int decay, int* skip) {
-    for (int i = threadIdx.x; i < (nseg + lead) * H; i += blockDim.x) {
-        const int r = i / H, h = i % H;
-        int sk = 0;
-        if (r < lead) {
-            sk = 1;
-        } else if (decay != 2) {
-            const float* pp = partial + (static_cast<size_t>(r - lead) * H + h) * kBoundBlocks;
-            float sum = 0.f;
-            for (int b = 0; b < kBoundBlocks; ++b) sum += pp[b];
-            sk = sum < kSkipLogNorm ? 1 : 0;
+// Run B's skip list: segments it does not form, and those whose transition the bound rules
+// out (decay 2, none, rules out nothing).
+__global__ void seg_flag_kernel(const float* partial, const int32_t* role, int n_seg, int H, int decay, int* skip_b) {
+    for (int i = threadIdx.x; i < n_seg * H; i += blockDim.x) {
+        const int g = i / H;
+        int sk = 1;
+        if (runs_in_b(role[g])) {
+            sk = 0;
+            if (decay != 2) {
+                const float* pp = partial + static_cast<size_t>(i) * kBoundBlocks;
+                float sum = 0.f;
+                for (int b = 0; b < kBoundBlocks; ++b) sum += pp[b];
+                sk = sum < kSkipLogNorm ? 1 : 0;
+            }
         }
-        skip[i] = sk;
+        skip_b[i] = sk;
     }
 }
 
@@ -120,28 +143,28 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 
 constexpr int kSlab = 4;          // state columns per CTA
 
-// Chain the segment results, one CTA per (4-column block, head): the state's columns are
-// independent, so each CTA carries a D x 4 slab of S_start through the segments in order.
-// Each step's Phi (D x D, contiguous) is copied into shared memory (row pitch D + 4) while
-// the previous step computes; thread (row i, columns 2 (tid & 1) .. +1) forms its two
-// outputs as fp32 dot products over the whole row.
-// phi   [P-2, H, D, D]  transitions of segments 1 .. P-2
-// skip  [P-2, H]        nonzero: Phi_p was not formed (its bound says it cannot matter)
-// sst   [P, H, D, D]    slot 1 holds segment 0's final state; slot p + 1 (p = 1 .. P-2) holds
-//                       B_p on entry and S_start[p + 1] = Phi_p S_start[p] + B_p on exit
-// (slot 0, the prompt's own initial state, is not touched)
-__global__ void __launch_bounds__(256) seg_chain_kernel(const float* __restrict__ phi, const int* __restrict__ skip,
-                                                         float* sst, int P, int H, int D) {
+// Chain the segment results of each split sequence, one CTA per (4-column block, head,
+// sequence): the state's columns are independent, so each CTA carries a D x 4 slab of its
+// sequence's S_start through the sequence's segments in order.  Each step's Phi (D x D,
+// contiguous) is copied into shared memory (row pitch D + 4) while the previous step
+// computes; thread (row i, columns 2 (tid & 1) .. +1) forms its two outputs as fp32 dot
+// products over the whole row.  For chain z, segments g0 .. g0 + P - 1 (global indices):
+// phi   [n_seg, H, D, D]  slot g holds Phi of segment g (formed where skip_b is 0)
+// sst   [n_seg, H, D, D]  slot g0 + 1 holds the end state of segment g0; slot g0 + p + 1
+//                         (p = 1 .. P-2) holds B on entry and S_start = Phi S_start + B on exit
+__global__ void __launch_bounds__(256) seg_chain_kernel(SegChainBuf cb, const float* __restrict__ phi,
+                                                         const int* __restrict__ skip_b, float* sst, int H, int D) {
     extern __shared__ __align__(16) float sm[];
     const int pitch = D + 4;
     float* slab = sm;                                 // [D][kSlab]
     float* phis = sm + 128 * kSlab;                   // 2 x [D][pitch]
     const int h = blockIdx.y, c0 = kSlab * blockIdx.x;
+    const int g0 = cb.g0[blockIdx.z], P = cb.np[blockIdx.z];
     const int i = threadIdx.x >> 1, j0 = 2 * (threadIdx.x & 1);
     const size_t per = static_cast<size_t>(H) * D * D;
     const size_t head = static_cast<size_t>(h) * D * D;
-    auto stage = [&](int p) {                         // Phi_p into buffer (p - 1) & 1
-        const float* src = phi + static_cast<size_t>(p - 1) * per + head;
+    auto stage = [&](int p) {                         // Phi of segment g0 + p into buffer (p - 1) & 1
+        const float* src = phi + static_cast<size_t>(g0 + p) * per + head;
         float* dst = phis + ((p - 1) & 1) * D * pitch;
         const int q4 = D / 4;
         for (int e = threadIdx.x; e < D * q4; e += blockDim.x) {
@@ -151,7 +174,7 @@ __global__ void __launch_bounds__(256) seg_chain_kernel(const float* __restrict_
         cp_async_commit();
     };
     if (i < D) {
-        const float* s1 = sst + per + head + static_cast<size_t>(i) * D + c0 + j0;
+        const float* s1 = sst + static_cast<size_t>(g0 + 1) * per + head + static_cast<size_t>(i) * D + c0 + j0;
         slab[i * kSlab + j0] = s1[0];
         slab[i * kSlab + j0 + 1] = s1[1];
     }
@@ -163,12 +186,13 @@ __global__ void __launch_bounds__(256) seg_chain_kernel(const float* __restrict_
         } else {
             cp_async_wait<0>();
         }
-        __syncthreads();                              // Phi_p and the slab are in place
+        __syncthreads();                              // Phi and the slab are in place
         float a0 = 0.f, a1 = 0.f;
-        float* dst = sst + static_cast<size_t>(p + 1) * per + head + static_cast<size_t>(i < D ? i : 0) * D + c0 + j0;
-        const bool use_phi = !skip[static_cast<size_t>(p - 1) * H + h];
+        float* dst = sst + static_cast<size_t>(g0 + p + 1) * per + head +
+                     static_cast<size_t>(i < D ? i : 0) * D + c0 + j0;
+        const bool use_phi = !skip_b[static_cast<size_t>(g0 + p) * H + h];
         if (i < D) {
-            a0 = dst[0];                              // B_p
+            a0 = dst[0];                              // B
             a1 = dst[1];
         }
         if (i < D && use_phi) {
@@ -186,7 +210,7 @@ __global__ void __launch_bounds__(256) seg_chain_kernel(const float* __restrict_
                 a0 = fmaf(f.w, s3.x, a0); a1 = fmaf(f.w, s3.y, a1);
             }
         }
-        __syncthreads();                              // every row has read the slab and Phi_p
+        __syncthreads();                              // every row has read the slab and Phi
         if (i < D) {
             slab[i * kSlab + j0] = a0;
             slab[i * kSlab + j0 + 1] = a1;
@@ -198,36 +222,39 @@ __global__ void __launch_bounds__(256) seg_chain_kernel(const float* __restrict_
 
 }  // namespace
 
-int launch_segment_setup(const SegIdxBuf& ib, int32_t* idx, float* ident, int n_ident, float* zinit, int n_zinit,
-                         const float* init_state, int* flags, int n_flags, int n_flags_set, int H, int D,
+int launch_segment_setup(const SegIdxBuf& ib, int32_t* idx, int n_seg, int o_role, int o_seq, int H, int D,
+                         const float* init_state, float* ident, float* zin, float* sst, int* skip_a, int* skip_f,
                          cudaStream_t stream) {
-    if (ib.n < 0 || ib.n > kSegIdxMax || n_ident < 0 || n_zinit < 0 || n_flags < 0 || n_flags_set < 0) return -1;
-    seg_setup_kernel<<<4 * 152, 256, 0, stream>>>(ib, idx, ident, n_ident, zinit, n_zinit, init_state, flags, n_flags,
-                                                  n_flags_set, H, D);
+    if (ib.n < 0 || ib.n > kSegIdxMax || n_seg < 0 || o_role < 0 || o_seq < 0 || o_role + n_seg > ib.n ||
+        o_seq + n_seg > ib.n)
+        return -1;
+    seg_setup_kernel<<<4 * 152, 256, 0, stream>>>(ib, idx, n_seg, o_role, o_seq, H, D, init_state, ident, zin, sst,
+                                                  skip_a, skip_f);
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
 int launch_segment_bound(const uint16_t* k, const float* la, const uint16_t* beta, int decay, int H, int D,
-                         const int32_t* seg_start, int nseg, int lead, float* partial, int* skip,
+                         const int32_t* seg_cu, const int32_t* role, int n_seg, float* partial, int* skip_b,
                          cudaStream_t stream) {
-    if (nseg < 0 || lead < 0 || H <= 0 || (D != 64 && D != 128) || decay < 0 || decay > 2) return -1;
-    if (decay != 2 && nseg > 0) {
-        const dim3 grid(kBoundBlocks, nseg, H);
-        seg_bound_kernel<<<grid, 256, 0, stream>>>(k, la, beta, decay, H, D, seg_start, partial);
+    if (n_seg <= 0 || H <= 0 || (D != 64 && D != 128) || decay < 0 || decay > 2) return -1;
+    if (decay != 2) {
+        const dim3 grid(kBoundBlocks, n_seg, H);
+        seg_bound_kernel<<<grid, 256, 0, stream>>>(k, la, beta, decay, H, D, seg_cu, role, partial);
     }
-    if (nseg + lead > 0) seg_flag_kernel<<<1, 256, 0, stream>>>(partial, nseg, H, lead, decay, skip);
+    seg_flag_kernel<<<1, 256, 0, stream>>>(partial, role, n_seg, H, decay, skip_b);
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
-int launch_segment_chain(const float* phi, const int* skip, float* sst, int P, int H, int D, cudaStream_t stream) {
-    if (P < 3 || (D != 64 && D != 128)) return -1;
+int launch_segment_chain(const SegChainBuf& cb, const float* phi, const int* skip_b, float* sst, int H, int D,
+                         cudaStream_t stream) {
+    if (cb.n <= 0 || cb.n > kSegMaxChains || (D != 64 && D != 128)) return -1;
     const int smem = static_cast<int>(sizeof(float) * (128 * kSlab + 2 * D * (D + 4)));
     static bool attr_done[kMaxDevicesAttr] = {};
     if (!raise_smem_limit(reinterpret_cast<const void*>(seg_chain_kernel), 128 * kSlab * 4 + 2 * 128 * 132 * 4,
                           attr_done))
         return -3;
-    const dim3 grid(D / kSlab, H);
-    seg_chain_kernel<<<grid, 256, smem, stream>>>(phi, skip, sst, P, H, D);
+    const dim3 grid(D / kSlab, H, cb.n);
+    seg_chain_kernel<<<grid, 256, smem, stream>>>(cb, phi, skip_b, sst, H, D);
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

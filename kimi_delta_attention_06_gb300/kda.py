@@ -73,6 +73,9 @@ def load():
             lib.kda_chunk_prefill_segmented.restype = _i
             lib.kda_chunk_prefill_segmented.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _i,
                                                         _vp, _vp, _i, _i, _i, _i, _vp, ctypes.c_float, _vp]
+            lib.kda_chunk_prefill_segmented_ex.restype = _i
+            lib.kda_chunk_prefill_segmented_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp,
+                                                           _i, _vp, _vp, _i, _i, _vp, _i, _vp, ctypes.c_float, _vp]
             lib.kda_segment_plan.restype = _i
             lib.kda_segment_plan.argtypes = [_i, _i, _i, _i, _vp, _vp, _i]
             lib.kda_prefill_clusters_at_once.restype = _i
@@ -204,6 +207,22 @@ def kda_chunk_prefill_segmented(q, k, v, log_alpha, beta, init_state, total_toke
     _check(rc, "kda_chunk_prefill_segmented")
 
 
+def kda_chunk_prefill_segmented_ex(q, k, v, log_alpha, beta, init_state, cu_seqlens_host, num_seqs: int,
+                                   total_tokens: int, H: int, Dk: int, Dv: int, out, out_dtype: int, final_state,
+                                   ckpt_states, ckpt_stride: int, decay: int, start_pos_host, segments: int,
+                                   out_norm_gamma=None, out_norm_eps: float = 1e-6, stream=None):
+    cu_host = cu_seqlens_host.to(device="cpu", dtype=torch.int32).contiguous()
+    sp_host = None if start_pos_host is None else \
+        torch.as_tensor(start_pos_host).to(device="cpu", dtype=torch.int32).contiguous()
+    rc = load().kda_chunk_prefill_segmented_ex(
+        _ptr(_bits16(q)), _ptr(_bits16(k)), _ptr(_bits16(v)), _ptr(log_alpha), _ptr(_bits16(beta)),
+        _ptr(init_state), ctypes.c_void_p(cu_host.data_ptr()), int(num_seqs), int(total_tokens), int(H), int(Dk),
+        int(Dv), _ptr(out), int(out_dtype), _ptr(final_state), _ptr(ckpt_states), int(ckpt_stride), int(decay),
+        None if sp_host is None else ctypes.c_void_p(sp_host.data_ptr()), int(segments), _ptr(out_norm_gamma),
+        float(out_norm_eps), _stream(stream))
+    _check(rc, "kda_chunk_prefill_segmented_ex")
+
+
 def kda_segment_plan(total_tokens: int, start_pos: int, segments: int, ckpt_stride: int = 0):
     """(bounds, ckpt_slots) of kda_chunk_prefill_segmented's plan: the segment bounds in tokens
     from the prompt's start, and for each of the prompt's checkpoints the slot it comes from,
@@ -299,7 +318,7 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens_host, init_state=None, ckpt_str
             segments: int = 0):
     """Allocate outputs and run kda_chunk_prefill (kda_chunk_prefill_ex for another decay
     layout, for start positions or with the output norm fused in: norm_gamma [H, Dv];
-    kda_chunk_prefill_segmented when segments > 0, for one sequence).
+    kda_chunk_prefill_segmented(_ex) when segments > 0).
     Returns (out, final_state, ckpt_states)."""
     T, H, Dk = q.shape
     Dv = v.shape[2]
@@ -313,13 +332,15 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens_host, init_state=None, ckpt_str
     nck = kda_ckpt_count_ex(cu_host, start_pos_host, ckpt_stride) if ckpt_stride > 0 else 0
     ck = torch.empty(nck, H, Dk, Dv, device=dev, dtype=torch.float32) if ckpt_stride > 0 else None
     odt = KDA_OUT_F32 if out_dtype == torch.float32 else KDA_OUT_BF16
-    if segments > 0:
-        if N != 1:
-            raise ValueError("the segmented prefill takes one sequence")
+    if segments > 0 and N == 1:
         sp0 = 0 if start_pos_host is None else int(torch.as_tensor(start_pos_host).reshape(-1)[0])
         kda_chunk_prefill_segmented(q, k, v, log_alpha, beta, init_state, T, H, Dk, Dv, out, odt, fin,
                                     ck if nck > 0 else None, ckpt_stride, decay, sp0, segments, norm_gamma,
                                     norm_eps, stream)
+    elif segments > 0:
+        kda_chunk_prefill_segmented_ex(q, k, v, log_alpha, beta, init_state, cu_host, N, T, H, Dk, Dv, out, odt,
+                                       fin, ck if nck > 0 else None, ckpt_stride, decay, start_pos_host, segments,
+                                       norm_gamma, norm_eps, stream)
     elif decay == KDA_DECAY_CHANNEL and start_pos_host is None and norm_gamma is None:
         kda_chunk_prefill(q, k, v, log_alpha, beta, init_state, cu_seqlens, cu_host, N, T, H, Dk, Dv,
                           out, odt, fin, ck if nck > 0 else None, ckpt_stride, stream)

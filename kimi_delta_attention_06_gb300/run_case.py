@@ -3,7 +3,7 @@
   python -m kimi_delta_attention_06_gb300.run_case --what prefill --T 8192 [--H 32] [--D 128] [--reps 2]
   python -m kimi_delta_attention_06_gb300.run_case --what varlen [--H 32] [--D 128] [--reps 2]
       (prefill / varlen also take --decay channel|head|none: KDA, Gated DeltaNet, DeltaNet;
-       prefill --segments P runs kda_chunk_prefill_segmented with P segments)
+       prefill / varlen --segments P run kda_chunk_prefill_segmented(_ex) with P segments)
   python -m kimi_delta_attention_06_gb300.run_case --what decode --N 512 [--H 32] [--D 128] [--reps 2]
   python -m kimi_delta_attention_06_gb300.run_case --what decode_multi --N 512 --K 4 [--commit 1] [--reps 2]
   python -m kimi_delta_attention_06_gb300.run_case --what prep --T 145408 [--reps 2]     (input preparation)
@@ -58,7 +58,11 @@ def main(argv=None):
         ck = torch.empty(max(nck, 1), a.H, a.D, a.D, device=dev)
 
         def run():
-            if a.segments > 0 and a.what == "prefill":
+            if a.segments > 0 and a.what == "varlen":
+                kda.kda_chunk_prefill_segmented_ex(c.q, c.k, c.v, la, c.beta, c.init_state, c.cu_seqlens, N, T, a.H,
+                                                   a.D, a.D, out, kda.KDA_OUT_BF16, fin, ck if nck else None, a.ckpt,
+                                                   decay, None, a.segments, stream=stream)
+            elif a.segments > 0 and a.what == "prefill":
                 kda.kda_chunk_prefill_segmented(c.q, c.k, c.v, la, c.beta, c.init_state, T, a.H, a.D, a.D, out,
                                                 kda.KDA_OUT_BF16, fin, ck if nck else None, a.ckpt, decay, 0,
                                                 a.segments, stream=stream)

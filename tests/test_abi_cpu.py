@@ -197,6 +197,32 @@ def test_segmented_prefill_rejects_on_host(lib):
     assert raw(gamma=0xA000, eps=float("nan")) == kda.KDA_ERR_INVALID_ARG
 
 
+def test_segmented_ex_rejects_on_host(lib):
+    f = lib.kda_chunk_prefill_segmented_ex
+    cu = (ctypes.c_int32 * 4)(0, 3000, 3000, 7000)
+    sp = (ctypes.c_int32 * 3)(0, 64, 5)
+
+    def raw(**over):
+        a = dict(q=0x1000, k=0x2000, v=0x3000, la=0x4000, beta=0x5000, s0=None, cu=ctypes.cast(cu, ctypes.c_void_p),
+                 N=3, T=7000, H=4, Dk=128, Dv=128, out=0x7000, out_dtype=0, fin=None, ck=None, stride=0,
+                 decay=kda.KDA_DECAY_CHANNEL, sp=ctypes.cast(sp, ctypes.c_void_p), P=8, gamma=None, eps=1e-6,
+                 stream=None)
+        a.update(over)
+        return f(a["q"], a["k"], a["v"], a["la"], a["beta"], a["s0"], a["cu"], a["N"], a["T"], a["H"], a["Dk"],
+                 a["Dv"], a["out"], a["out_dtype"], a["fin"], a["ck"], a["stride"], a["decay"], a["sp"], a["P"],
+                 a["gamma"], a["eps"], a["stream"])
+    assert raw(P=0) == kda.KDA_ERR_INVALID_ARG
+    assert raw(P=65) == kda.KDA_ERR_INVALID_ARG
+    assert raw(N=129) == kda.KDA_ERR_UNSUPPORTED                  # at most KDA_MAX_SEGMENTED_SEQS
+    assert raw(T=6999) == kda.KDA_ERR_INVALID_ARG                 # cu_seqlens must end at total_tokens
+    assert raw(cu=None) == kda.KDA_ERR_INVALID_ARG
+    bad = (ctypes.c_int32 * 3)(0, -1, 5)
+    assert raw(sp=ctypes.cast(bad, ctypes.c_void_p)) == kda.KDA_ERR_INVALID_ARG
+    assert raw(Dv=64) == kda.KDA_ERR_UNSUPPORTED
+    assert raw(stride=100) == kda.KDA_ERR_INVALID_ARG
+    assert raw(N=0, T=0) == kda.KDA_OK                            # nothing to do, nothing launched
+
+
 def test_ckpt_count_with_start_positions(lib):
     cu = torch.tensor([0, 9, 9, 100], dtype=torch.int32)
     # s = 6, len 9, stride 4: absolute 8, 12 and the end; empty: none; s = 0, len 91: ceil(91/4) = 23
@@ -240,27 +266,18 @@ def test_binding_refuses_non_bf16(lib):
 
 
 def _slot_positions(bounds, start_pos, stride):
-    """Absolute positions of the checkpoint slots the segmented prefill's runs write, run A's
-    (segments 0 .. P-2) followed by run F's (a leading sequence from segment 1's start rounded
-    down to 8 tokens, when that differs, then segments 1 .. P-1): per sequence, the stride
-    multiples strictly inside it, then its end."""
-    def seq(a, e):
-        out = []
+    """Absolute positions of the checkpoint slots the segmented prefill's runs A and F write:
+    both cover every segment, so each writes, per segment in order, the stride multiples
+    strictly inside it, then its end; run A's slots come first, then run F's."""
+    pos = []
+    for a, e in zip(bounds[:-1], bounds[1:]):
+        a, e = start_pos + a, start_pos + e
         m = (a // stride + 1) * stride
         while m < e:
-            out.append(m)
+            pos.append(m)
             m += stride
-        return out + [e]
-    P = len(bounds) - 1
-    pos = []
-    for p in range(P - 1):
-        pos += seq(start_pos + bounds[p], start_pos + bounds[p + 1])
-    b1a = bounds[1] & ~7
-    if b1a < bounds[1]:
-        pos += seq(start_pos + b1a, start_pos + bounds[1])
-    for p in range(1, P):
-        pos += seq(start_pos + bounds[p], start_pos + bounds[p + 1])
-    return pos
+        pos.append(e)
+    return pos + pos
 
 
 def test_segment_plan_properties(lib):
@@ -297,7 +314,10 @@ def test_segment_plan_properties(lib):
             want = [m for m in range((s0 // stride + 1) * stride, s0 + T, stride)] + [s0 + T]
             assert got == want, (T, s0, seg, stride)
             assert len(slots) == oracle.ckpt_count([0, T], stride, [s0])
-            assert slots == sorted(slots)
+            n_run = len(_slot_positions(bounds, s0, stride)) // 2
+            # the first segment's checkpoints come from run A, every later one from run F
+            assert all((i < n_run) == (pos < s0 + bounds[1]) for i, pos in
+                       zip(slots, [_slot_positions(bounds, s0, stride)[i] for i in slots]) if pos != s0 + bounds[1])
         else:
             assert slots == []
 

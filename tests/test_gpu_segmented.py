@@ -174,3 +174,39 @@ def test_segmented_skips_only_transitions_that_cannot_matter():
     P.check_out(out, ro, torch.float32)
     P.check_state(fin, rf)
     assert kda.kda_device_status() == 0
+
+
+@pytest.mark.parametrize("decay", [kda.KDA_DECAY_CHANNEL, kda.KDA_DECAY_HEAD])
+def test_segmented_varlen_matches_oracle(decay):
+    """kda_chunk_prefill_segmented_ex over seven sequences: split ones (3, 4 and 5 segments)
+    beside whole ones, an empty one, initial states on every other sequence, start positions
+    on and off the chunk grid, checkpoints every 512 tokens.  Per-channel decay forms every
+    transition here; per-head decay has them dropped by the bound."""
+    lens = [3000, 200, 5000, 64, 0, 1500, 7000]
+    sp = [0, 10, 4133, 0, 7, 64, 99]
+    c = workloads.prefill_case(lens, H=4, D=128, seed=41, device=DEV, la_shift=-1.0, s0_std=0.05,
+                               s0_every_other=True, ckpt_stride=512)
+    ro, rf, rc = oracle.prefill(c.q.cpu(), c.k.cpu(), c.v.cpu(), _oracle_la(c, decay), c.beta.cpu(), c.cu_seqlens,
+                                c.init_state.cpu(), ckpt_stride=512, start_pos=sp)
+    spt = torch.tensor(sp, dtype=torch.int32)
+    for od in (torch.float32, torch.bfloat16):
+        out, fin, ck = kda.prefill(c.q, c.k, c.v, _la(c, decay), c.beta, c.cu_seqlens, init_state=c.init_state,
+                                   ckpt_stride=512, out_dtype=od, decay=decay, start_pos_host=spt, segments=12)
+        assert ck.shape[0] == rc.shape[0]
+        P.check_out(out, ro, od)
+        P.check_state(fin, rf)
+        P.check_state(ck, rc, "checkpoints")
+    assert kda.kda_device_status() == 0
+
+
+def test_segmented_varlen_plain_when_nothing_splits():
+    """More than 32 sequences, or sequences too short to split: one plain prefill, bit for bit
+    the kda_chunk_prefill_ex result."""
+    c = workloads.prefill_case([100] * 40, H=4, D=128, seed=42, device=DEV, ckpt_stride=64)
+    o0, f0, k0 = kda.prefill(c.q, c.k, c.v, c.log_alpha, c.beta, c.cu_seqlens, init_state=c.init_state,
+                             ckpt_stride=64, out_dtype=torch.float32,
+                             start_pos_host=torch.zeros(40, dtype=torch.int32))
+    o, f, k = kda.prefill(c.q, c.k, c.v, c.log_alpha, c.beta, c.cu_seqlens, init_state=c.init_state,
+                          ckpt_stride=64, out_dtype=torch.float32, start_pos_host=torch.zeros(40, dtype=torch.int32),
+                          segments=16)
+    assert torch.equal(o, o0) and torch.equal(f, f0) and torch.equal(k, k0)
