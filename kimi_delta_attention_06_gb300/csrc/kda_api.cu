@@ -499,8 +499,13 @@ int kda_chunk_prefill_segmented_ex(const uint16_t* q, const uint16_t* k, const u
     if (kda::launch_segment_setup(ib, idx, n_seg, o_role, o_seq, H, Dk, init_state, idn, zin, sst, skip_a, skip_f,
                                   st) != 0)
         return finish(KDA_ERR_CUDA);
-    if (total_tokens > 0 && cudaMemsetAsync(zv, 0, static_cast<size_t>(total_tokens) * H * Dv * 2, st) != cudaSuccess)
-        return finish(KDA_ERR_CUDA);
+    // v = 0 only where run B may read it: the middle segments of each split sequence
+    for (size_t z = 0; z < plan.g0.size(); ++z) {
+        const int g0 = plan.g0[z], P = plan.np[z];
+        const size_t t0 = static_cast<size_t>(plan.cu[g0 + 1]), t1 = static_cast<size_t>(plan.cu[g0 + P - 1]);
+        if (t1 > t0 && cudaMemsetAsync(zv + t0 * H * Dv, 0, (t1 - t0) * H * Dv * 2, st) != cudaSuccess)
+            return finish(KDA_ERR_CUDA);
+    }
     // which transitions cannot matter (their norm bound is below fp32 rounding): run B leaves
     // them out and the chain takes the segment's B alone
     if (kda::launch_segment_bound(k, log_alpha, beta, decay, H, Dk, seg_cu, idx + o_role, n_seg, part, skip_b, st) != 0)
