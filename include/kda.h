@@ -163,8 +163,9 @@ int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v
  * given on the host), computed another way.  Each (sequence, head) forms one serial chain
  * of chunks in kda_chunk_prefill_ex, so a call over few heads and few sequences leaves most
  * SMs idle and takes as long as one sequence's chain.  This entry point cuts every sequence
- * of enough chunks, on its absolute 64-token chunk grid, into P_n >= 3 segments of about
- * L = (the call's chunks) / `segments` chunks each (shorter sequences stay whole), and uses
+ * of enough chunks, on its absolute 64-token chunk grid, into segments of about
+ * L = (the call's chunks) / `segments` chunks each (P_n >= 2 when the call has several
+ * sequences, P_n >= 3 for one; shorter sequences stay whole), and uses
  * that the recurrence S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
  * is linear in (S_0, v) (Kimi Linear, "Kimi Delta Attention"): over a segment,
  * S_end = Phi S_start + B.  Three prefill launches run over the list of all segments, each

@@ -200,8 +200,11 @@ int plan_segments(const int32_t* cu_host, const int32_t* sp_host, int N, int seg
         chunks[n] = len > 0 ? (s0 + len + C - 1) / C - s0 / C : 0;
         total += chunks[n];
     }
-    // segment length in chunks; sequences of fewer than 3 such segments stay whole
-    const bool split_any = segments >= 3 && N <= kSegMaxSeqs && total >= 3;
+    // segment length in chunks.  A sequence of one such segment stays whole; one of two is cut
+    // too when the call has several sequences (its halves then sit in runs A and F, which
+    // shortens the longest chain of each run), but not alone (two halves in series take as
+    // long as the whole)
+    const bool split_any = segments >= 3 && N <= kSegMaxSeqs && total >= 2;
     const int64_t L = split_any ? (total + segments - 1) / segments : 0;
     SegPlan pl;
     pl.cu.push_back(0);
@@ -209,9 +212,9 @@ int plan_segments(const int32_t* cu_host, const int32_t* sp_host, int N, int seg
         const int64_t t0 = cu_host[n], len = static_cast<int64_t>(cu_host[n + 1]) - t0;
         const int64_t s0 = sp_host ? sp_host[n] : 0;
         int P = 1;
-        if (split_any && chunks[n] >= 3) {
+        if (split_any && chunks[n] >= 2) {
             P = static_cast<int>((chunks[n] + L - 1) / L);
-            if (P < 3) P = 1;
+            if (P < 2 || (N == 1 && P < 3)) P = 1;
         }
         if (P > 1 && static_cast<int>(pl.g0.size()) >= kda::kSegMaxChains) P = 1;
         const int g_first = pl.n_seg;
@@ -502,6 +505,7 @@ int kda_chunk_prefill_segmented_ex(const uint16_t* q, const uint16_t* k, const u
     // v = 0 only where run B may read it: the middle segments of each split sequence
     for (size_t z = 0; z < plan.g0.size(); ++z) {
         const int g0 = plan.g0[z], P = plan.np[z];
+        if (P < 3) continue;
         const size_t t0 = static_cast<size_t>(plan.cu[g0 + 1]), t1 = static_cast<size_t>(plan.cu[g0 + P - 1]);
         if (t1 > t0 && cudaMemsetAsync(zv + t0 * H * Dv, 0, (t1 - t0) * H * Dv * 2, st) != cudaSuccess)
             return finish(KDA_ERR_CUDA);
@@ -523,9 +527,10 @@ int kda_chunk_prefill_segmented_ex(const uint16_t* q, const uint16_t* k, const u
     if (rc != KDA_OK) return finish(rc);
     // chain: S_start[p + 1] = Phi_p S_start[p] + B_p along every split sequence
     kda::SegChainBuf cb;
-    cb.n = static_cast<int>(plan.g0.size());
-    for (int z = 0; z < cb.n; ++z) { cb.g0[z] = plan.g0[z]; cb.np[z] = plan.np[z]; }
-    if (kda::launch_segment_chain(cb, phi, skip_b, sst, H, Dk, st) != 0) return finish(KDA_ERR_CUDA);
+    cb.n = 0;
+    for (size_t z = 0; z < plan.g0.size(); ++z)
+        if (plan.np[z] >= 3) { cb.g0[cb.n] = plan.g0[z]; cb.np[cb.n] = plan.np[z]; ++cb.n; }
+    if (cb.n > 0 && kda::launch_segment_chain(cb, phi, skip_b, sst, H, Dk, st) != 0) return finish(KDA_ERR_CUDA);
     // F: every segment but the first of a split sequence, from its S_start
     rc = prefill_pooled(q, k, v, log_alpha, beta, sst, seg_cu, plan.cu.data(), n_seg, total_tokens, H, Dk, Dv, out,
                         out_dtype, fin, want_ck ? ck + static_cast<size_t>(plan.n_ck) * slot_f : nullptr,

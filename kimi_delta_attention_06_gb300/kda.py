@@ -246,14 +246,19 @@ def kda_prefill_clusters_at_once() -> int:
     return int(n)
 
 
-def segments_for(H: int, clusters_at_once: Optional[int] = None) -> int:
-    """Segments for kda_chunk_prefill_segmented whose runs (P - 1 segments each) fill the
-    device in one wave (clusters_at_once // H + 1, at most 32: beyond that the serial chain
-    of segment states and the per-segment fixed costs grow while the runs shrink, and short
-    segments are less likely to let their transitions be dropped), or 0 (a plain prefill)
-    when that is below 3."""
+def segments_for(H: int, clusters_at_once: Optional[int] = None, num_seqs: int = 1) -> int:
+    """Segments for kda_chunk_prefill_segmented(_ex): clusters_at_once // H + 1, at most 32, so
+    that each run (P - 1 segments of a single sequence per head) fills the device in one wave.
+    0 (a plain prefill) when that is below 3, or when the call's (sequence, head) pairs
+    already fill the device (num_seqs * H >= clusters_at_once): splitting then only adds work.
+    Beyond 32 segments the serial chain of segment states and the per-segment fixed costs
+    grow while the runs shrink, and short segments are less likely to let their transitions
+    be dropped."""
     n = kda_prefill_clusters_at_once() if clusters_at_once is None else int(clusters_at_once)
-    p = min(n // max(1, int(H)) + 1, 32)
+    H, num_seqs = max(1, int(H)), max(1, int(num_seqs))
+    if num_seqs * H >= n:
+        return 0
+    p = min(n // H + 1, 32)
     return p if p >= 3 else 0
 
 
