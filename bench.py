@@ -331,7 +331,8 @@ def _median_ms(fns, stream, steps):
 def time_other_rows(dev, stream, heads=(0, H), seed_offset=0, steps=10):
     """The workloads beside the headline, timed on the device after the main timed region:
     - varlen: 16 packed sequences of log-uniform length in [1k, 64k] (279,375 tokens), even
-      ones from an initial state, checkpoints every 32768 tokens;
+      ones from an initial state, checkpoints every 32768 tokens; and the same pack on 2
+      heads, plain and segmented;
     - layouts: the T=145408 prompt with one decay per head (Gated DeltaNet) and with none
       (DeltaNet), through kda_chunk_prefill_ex;
     - serving decode: kda_decode_multi over a 512-slot x H state pool, K = 8 tokens per
@@ -356,6 +357,27 @@ def time_other_rows(dev, stream, heads=(0, H), seed_offset=0, steps=10):
                                                    ck if nck else None, CKPT, stream)], stream, steps)
     res["varlen"] = {"ms": ms, "tokens": vc.T, "sequences": vc.N, "tokens_per_s": vc.T / (ms / 1e3),
                      "workload": vc.name}
+    # the same pack on 2 heads (one GPU's share of a 32-head model over 16 GPUs): plain
+    # against segmented (kda_chunk_prefill_segmented_ex)
+    if Hl >= 2:
+        v2 = workloads.head_slice(vc, 0, 2)
+        o2 = torch.empty(v2.T, 2, D, device=dev, dtype=torch.bfloat16)
+        f2 = torch.empty(v2.N, 2, D, D, device=dev)
+        k2 = torch.empty(max(nck, 1), 2, D, D, device=dev)
+        p2 = kda.segments_for(2, num_seqs=v2.N)
+        plain = _median_ms([lambda: kda.kda_chunk_prefill(v2.q, v2.k, v2.v, v2.log_alpha, v2.beta, v2.init_state, cu,
+                                                          v2.cu_seqlens, v2.N, v2.T, 2, D, D, o2, kda.KDA_OUT_BF16,
+                                                          f2, k2 if nck else None, CKPT, stream)], stream, steps)
+        segd = _median_ms([lambda: kda.kda_chunk_prefill_segmented_ex(v2.q, v2.k, v2.v, v2.log_alpha, v2.beta,
+                                                                      v2.init_state, v2.cu_seqlens, v2.N, v2.T, 2, D,
+                                                                      D, o2, kda.KDA_OUT_BF16, f2,
+                                                                      k2 if nck else None, CKPT,
+                                                                      kda.KDA_DECAY_CHANNEL, None, p2,
+                                                                      stream=stream)], stream, steps)
+        res["segmented_varlen_2_heads"] = {"plain_ms": plain, "segmented_ms": segd, "segments": p2,
+                                           "tokens_per_s": v2.T / (segd / 1e3),
+                                           "workload": f"{vc.name} heads 0-1, ckpt every {CKPT}"}
+        del v2, o2, f2, k2
     del vc, out, fin, ck
 
     c = cut(workloads.single_case(T_PROMPT, seed=2 + seed_offset, device=dev, ckpt_stride=CKPT))
