@@ -52,3 +52,23 @@ def test_decode_head_split_matches_the_full_launch():
             assert torch.equal(o_r, out[:, h0:h1])
             assert torch.equal(p.state, state[:, h0:h1])
     assert kda.kda_device_status() == 0
+
+
+def test_segmented_head_split_matches_the_full_launch():
+    """A head-split rank that runs the segmented prefill (as `bench.py --split heads` does when
+    a rank holds few heads) gives its heads of the full plain launch within the parity
+    tolerances (not bit for bit: the segment start states are formed through the segment
+    transitions and offsets)."""
+    from tests import _parity as P
+    full = workloads.prefill_case([20000], H=8, D=128, seed=23, device=DEV, ckpt_stride=4096)
+    out, fin, ck = kda.prefill(full.q, full.k, full.v, full.log_alpha, full.beta, full.cu_seqlens,
+                               init_state=full.init_state, ckpt_stride=4096, out_dtype=torch.float32)
+    for rank in range(2):
+        h0, h1 = bench.head_range(8, 2, rank)
+        c = workloads.head_slice(full, h0, h1)
+        o_r, f_r, c_r = kda.prefill(c.q, c.k, c.v, c.log_alpha, c.beta, c.cu_seqlens, init_state=c.init_state,
+                                    ckpt_stride=4096, out_dtype=torch.float32, segments=8)
+        P.check_out(o_r, out[:, h0:h1], torch.float32)
+        P.check_state(f_r, fin[:, h0:h1])
+        P.check_state(c_r, ck[:, h0:h1])
+    assert kda.kda_device_status() == 0
