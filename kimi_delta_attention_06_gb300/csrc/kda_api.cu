@@ -120,6 +120,21 @@ int workspace_pool(cudaMemPool_t* pool) {
     return KDA_OK;
 }
 
+// A second stream per device for work that can run beside a prefill on the SMs it leaves idle
+// (created once, non-blocking; ordered against the caller's stream with events).
+cudaStream_t g_side[kMaxDevices] = {};
+int side_stream(cudaStream_t* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_side[dev] && cudaStreamCreateWithFlags(&g_side[dev], cudaStreamNonBlocking) != cudaSuccess) {
+        g_side[dev] = nullptr;
+        return KDA_ERR_CUDA;
+    }
+    *out = g_side[dev];
+    return KDA_OK;
+}
+
 bool head_dims_ok(int Dk, int Dv) { return (Dk == 64 || Dk == 128) && (Dv == 64 || Dv == 128); }
 
 // Host-side checks shared by the two prefill entry points.
@@ -502,24 +517,40 @@ int kda_chunk_prefill_segmented_ex(const uint16_t* q, const uint16_t* k, const u
     if (kda::launch_segment_setup(ib, idx, n_seg, o_role, o_seq, H, Dk, init_state, idn, zin, sst, skip_a, skip_f,
                                   st) != 0)
         return finish(KDA_ERR_CUDA);
-    // v = 0 only where run B may read it: the middle segments of each split sequence
-    for (size_t z = 0; z < plan.g0.size(); ++z) {
-        const int g0 = plan.g0[z], P = plan.np[z];
-        if (P < 3) continue;
-        const size_t t0 = static_cast<size_t>(plan.cu[g0 + 1]), t1 = static_cast<size_t>(plan.cu[g0 + P - 1]);
-        if (t1 > t0 && cudaMemsetAsync(zv + t0 * H * Dv, 0, (t1 - t0) * H * Dv * 2, st) != cudaSuccess)
-            return finish(KDA_ERR_CUDA);
-    }
-    // which transitions cannot matter (their norm bound is below fp32 rounding): run B leaves
-    // them out and the chain takes the segment's B alone
-    if (kda::launch_segment_bound(k, log_alpha, beta, decay, H, Dk, seg_cu, idx + o_role, n_seg, part, skip_b, st) != 0)
-        return finish(KDA_ERR_CUDA);
     // A: a split sequence's segments but its last; its first segment from the sequence's initial
     // state (outputs, norm and checkpoints final), the others from zeros (B); the end state of
     // segment g lands in S_start slot g + 1
+    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaStream_t side = nullptr;
+    if (side_stream(&side) != KDA_OK || cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess || cudaEventRecord(fork, st) != cudaSuccess) {
+        if (fork) cudaEventDestroy(fork);
+        if (join) cudaEventDestroy(join);
+        return finish(KDA_ERR_CUDA);
+    }
     rc = prefill_pooled(q, k, v, log_alpha, beta, zin, seg_cu, plan.cu.data(), n_seg, total_tokens, H, Dk, Dv, out,
                         out_dtype, sst + slot_f, want_ck ? ck : nullptr, want_ck ? ckpt_stride : 0, decay, seg_sp,
                         plan.sp.data(), out_norm_gamma, out_norm_eps, stream, skip_a);
+    // beside run A, on the SMs it leaves idle: v = 0 where run B may read it (the middle
+    // segments), and which transitions cannot matter (their norm bound is below fp32
+    // rounding: run B leaves them out and the chain takes the segment's B alone)
+    bool side_ok = cudaStreamWaitEvent(side, fork, 0) == cudaSuccess;
+    for (size_t z = 0; side_ok && z < plan.g0.size(); ++z) {
+        const int g0 = plan.g0[z], P = plan.np[z];
+        if (P < 3) continue;
+        const size_t t0 = static_cast<size_t>(plan.cu[g0 + 1]), t1 = static_cast<size_t>(plan.cu[g0 + P - 1]);
+        if (t1 > t0) side_ok = cudaMemsetAsync(zv + t0 * H * Dv, 0, (t1 - t0) * H * Dv * 2, side) == cudaSuccess;
+    }
+    side_ok = side_ok &&
+              kda::launch_segment_bound(k, log_alpha, beta, decay, H, Dk, seg_cu, idx + o_role, n_seg, part, skip_b,
+                                        side) == 0;
+    side_ok = side_ok && cudaEventRecord(join, side) == cudaSuccess && cudaStreamWaitEvent(st, join, 0) == cudaSuccess;
+    cudaEventDestroy(fork);
+    cudaEventDestroy(join);
+    if (!side_ok) {            // the scratch must outlive whatever reached the side stream
+        cudaStreamSynchronize(side);
+        return finish(rc != KDA_OK ? rc : KDA_ERR_CUDA);
+    }
     if (rc != KDA_OK) return finish(rc);
     // B: the middle segments, from S_start = I with v = 0 (Phi), where the bound does not rule them out
     rc = prefill_pooled(q, k, zv, log_alpha, beta, idn, seg_cu, plan.cu.data(), n_seg, total_tokens, H, Dk, Dv, out,
