@@ -205,6 +205,10 @@ int kda_chunk_prefill_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v
  * stride multiples inside it and its end), total_tokens * H * Dv * 2 bytes of zero v for
  * run B, and small index and skip arrays.  `out` is written by runs A and B before run F
  * overwrites the segments it owns.
+ * Streams: besides `stream`, the call puts the bound and the zero-v fill on a second stream
+ * the library owns (one per device, created on first use), forked from `stream` after the
+ * call's first kernel and joined back into it before run B, both with events, so the call
+ * stays ordered on `stream` like any other.
  * Errors: those of kda_chunk_prefill_ex; a failing launch returns its status and leaves
  * the outputs unspecified.
  */
