@@ -27,6 +27,26 @@ struct DecodeShape {
     static_assert(kRowsPerWarp % kRowsPerIter == 0, "shape");
 };
 
+// The two per-row updates of the step, on two-lane fp32 instructions (each lane rounds as
+// the scalar fma / mul; the single-token and K-token kernels share them, so a one-token
+// commit reproduces the single-token step bit for bit):
+//   r1 += (alpha k)_row * S[row, 4 columns],  r2 += (alpha q)_row * S[row, 4 columns]
+__device__ __forceinline__ void col_sums(float4& r1, float4& r2, float ak, float aq, float4 x) {
+    const float2 ak2 = make_float2(ak, ak), aq2 = make_float2(aq, aq);
+    const float2 xl = make_float2(x.x, x.y), xh = make_float2(x.z, x.w);
+    const float2 r1l = ffma2(ak2, xl, make_float2(r1.x, r1.y)), r1h = ffma2(ak2, xh, make_float2(r1.z, r1.w));
+    const float2 r2l = ffma2(aq2, xl, make_float2(r2.x, r2.y)), r2h = ffma2(aq2, xh, make_float2(r2.z, r2.w));
+    r1 = make_float4(r1l.x, r1l.y, r1h.x, r1h.y);
+    r2 = make_float4(r2l.x, r2l.y, r2h.x, r2h.y);
+}
+//   S[row, 4 columns] = alpha_row S[row, 4 columns] + (beta k_row) u[4 columns]
+__device__ __forceinline__ float4 state_update(float4 x, float a, float kr, float4 u) {
+    const float2 a2 = make_float2(a, a), k2 = make_float2(kr, kr);
+    const float2 lo = ffma2(a2, make_float2(x.x, x.y), fmul2(k2, make_float2(u.x, u.y)));
+    const float2 hi = ffma2(a2, make_float2(x.z, x.w), fmul2(k2, make_float2(u.z, u.w)));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
 template <int D, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32, 2)
 kda_decode_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
@@ -77,8 +97,7 @@ kda_decode_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k
     for (int it = 0; it < Sh::kIters; ++it) {
         const int r = warp * Sh::kRowsPerWarp + it * Sh::kRowsPerIter + rsub;
         const float ak = s_ak[r], aq = s_aq[r];
-        r1.x += ak * s[it].x; r1.y += ak * s[it].y; r1.z += ak * s[it].z; r1.w += ak * s[it].w;
-        r2.x += aq * s[it].x; r2.y += aq * s[it].y; r2.z += aq * s[it].z; r2.w += aq * s[it].w;
+        col_sums(r1, r2, ak, aq, s[it]);
     }
 #pragma unroll
     for (int off = Sh::kLanesPerRow; off < 32; off <<= 1) {
@@ -115,12 +134,7 @@ kda_decode_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k
         const int r = warp * Sh::kRowsPerWarp + it * Sh::kRowsPerIter + rsub;
         const float a = s_a[r];
         const float kr = b * s_k[r];
-        float4 n;
-        n.x = a * s[it].x + kr * u4.x;
-        n.y = a * s[it].y + kr * u4.y;
-        n.z = a * s[it].z + kr * u4.z;
-        n.w = a * s[it].w + kr * u4.w;
-        __stcs(S + r * Sh::kLanesPerRow + c4, n);
+        __stcs(S + r * Sh::kLanesPerRow + c4, state_update(s[it], a, kr, u4));
     }
 }
 
@@ -211,8 +225,7 @@ kda_decode_multi_kernel(const uint16_t* __restrict__ q, const uint16_t* __restri
         for (int it = 0; it < Sh::kIters; ++it) {
             const int r = warp * Sh::kRowsPerWarp + it * Sh::kRowsPerIter + rsub;
             const float ak = s_ak[r], aq = s_aq[r];
-            r1.x += ak * s[it].x; r1.y += ak * s[it].y; r1.z += ak * s[it].z; r1.w += ak * s[it].w;
-            r2.x += aq * s[it].x; r2.y += aq * s[it].y; r2.z += aq * s[it].z; r2.w += aq * s[it].w;
+            col_sums(r1, r2, ak, aq, s[it]);
         }
 #pragma unroll
         for (int off = Sh::kLanesPerRow; off < 32; off <<= 1) {
@@ -246,10 +259,7 @@ kda_decode_multi_kernel(const uint16_t* __restrict__ q, const uint16_t* __restri
             const int r = warp * Sh::kRowsPerWarp + it * Sh::kRowsPerIter + rsub;
             const float a = s_a[r];
             const float kr = b * s_k[r];
-            s[it].x = a * s[it].x + kr * u4.x;
-            s[it].y = a * s[it].y + kr * u4.y;
-            s[it].z = a * s[it].z + kr * u4.z;
-            s[it].w = a * s[it].w + kr * u4.w;
+            s[it] = state_update(s[it], a, kr, u4);
         }
         __syncthreads();       // the shared scalars of this token are dead only now
     }
