@@ -55,7 +55,8 @@ kda_decode_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k
                   void* __restrict__ out, int out_f32)
 {
     using Sh = DecodeShape<D, WARPS>;
-    __shared__ float s_a[D], s_k[D], s_ak[D], s_aq[D], s_u[D];
+    __shared__ __align__(16) float2 s_akq[D], s_ak2[D];   // (alpha k, alpha q) and (alpha, k) per row
+    __shared__ float s_u[D];
     __shared__ float s_red[WARPS][2][D];
     __shared__ float s_qk[WARPS];
 
@@ -80,10 +81,8 @@ kda_decode_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k
         const float qi = bf16_bits_to_f32(q[o]);
         const float ki = bf16_bits_to_f32(k[o]);
         const float a = expf(log_alpha[o]);
-        s_a[tid] = a;
-        s_k[tid] = ki;
-        s_ak[tid] = a * ki;
-        s_aq[tid] = a * qi;
+        s_ak2[tid] = make_float2(a, ki);
+        s_akq[tid] = make_float2(a * ki, a * qi);
         qk_part = qi * ki;
     }
 #pragma unroll
@@ -96,7 +95,8 @@ kda_decode_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k
 #pragma unroll
     for (int it = 0; it < Sh::kIters; ++it) {
         const int r = warp * Sh::kRowsPerWarp + it * Sh::kRowsPerIter + rsub;
-        const float ak = s_ak[r], aq = s_aq[r];
+        const float2 akq = s_akq[r];
+        const float ak = akq.x, aq = akq.y;
         col_sums(r1, r2, ak, aq, s[it]);
     }
 #pragma unroll
@@ -132,8 +132,9 @@ kda_decode_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k
 #pragma unroll
     for (int it = 0; it < Sh::kIters; ++it) {
         const int r = warp * Sh::kRowsPerWarp + it * Sh::kRowsPerIter + rsub;
-        const float a = s_a[r];
-        const float kr = b * s_k[r];
+        const float2 ak2 = s_ak2[r];
+        const float a = ak2.x;
+        const float kr = b * ak2.y;
         __stcs(S + r * Sh::kLanesPerRow + c4, state_update(s[it], a, kr, u4));
     }
 }
@@ -157,7 +158,8 @@ kda_decode_multi_kernel(const uint16_t* __restrict__ q, const uint16_t* __restri
                         void* __restrict__ out, int out_f32, int K, int H, int decay, int* status)
 {
     using Sh = DecodeShape<D, WARPS>;
-    __shared__ float s_a[D], s_k[D], s_ak[D], s_aq[D], s_u[D];
+    __shared__ __align__(16) float2 s_akq[D], s_ak2[D];   // (alpha k, alpha q) and (alpha, k) per row
+    __shared__ float s_u[D];
     __shared__ float s_red[WARPS][2][D];
     __shared__ float s_qk[WARPS];
 
@@ -209,10 +211,8 @@ kda_decode_multi_kernel(const uint16_t* __restrict__ q, const uint16_t* __restri
             const float qi = bf16_bits_to_f32(q_j);
             const float ki = bf16_bits_to_f32(k_j);
             const float a = decay == 2 ? 1.f : expf(la_j);
-            s_a[tid] = a;
-            s_k[tid] = ki;
-            s_ak[tid] = a * ki;
-            s_aq[tid] = a * qi;
+            s_ak2[tid] = make_float2(a, ki);
+            s_akq[tid] = make_float2(a * ki, a * qi);
             qk_part = qi * ki;
         }
 #pragma unroll
@@ -224,7 +224,8 @@ kda_decode_multi_kernel(const uint16_t* __restrict__ q, const uint16_t* __restri
 #pragma unroll
         for (int it = 0; it < Sh::kIters; ++it) {
             const int r = warp * Sh::kRowsPerWarp + it * Sh::kRowsPerIter + rsub;
-            const float ak = s_ak[r], aq = s_aq[r];
+            const float2 akq = s_akq[r];
+        const float ak = akq.x, aq = akq.y;
             col_sums(r1, r2, ak, aq, s[it]);
         }
 #pragma unroll
@@ -257,8 +258,9 @@ kda_decode_multi_kernel(const uint16_t* __restrict__ q, const uint16_t* __restri
 #pragma unroll
         for (int it = 0; it < Sh::kIters; ++it) {
             const int r = warp * Sh::kRowsPerWarp + it * Sh::kRowsPerIter + rsub;
-            const float a = s_a[r];
-            const float kr = b * s_k[r];
+            const float2 ak2 = s_ak2[r];
+            const float a = ak2.x;
+            const float kr = b * ak2.y;
             s[it] = state_update(s[it], a, kr, u4);
         }
         __syncthreads();       // the shared scalars of this token are dead only now
