@@ -158,10 +158,12 @@ kda_decode_multi_kernel(const uint16_t* __restrict__ q, const uint16_t* __restri
                         void* __restrict__ out, int out_f32, int K, int H, int decay, int* status)
 {
     using Sh = DecodeShape<D, WARPS>;
-    __shared__ __align__(16) float2 s_akq[D], s_ak2[D];   // (alpha k, alpha q) and (alpha, k) per row
+    // per-row scalars of a token, double-buffered by token parity so that the next token's
+    // may be written while slower warps still read this one's: (alpha k, alpha q), (alpha, k)
+    __shared__ __align__(16) float2 s_akq[2][D], s_ak2[2][D];
     __shared__ float s_u[D];
     __shared__ float s_red[WARPS][2][D];
-    __shared__ float s_qk[WARPS];
+    __shared__ float s_qk[2][WARPS];
 
     const int pair = blockIdx.x;                       // n * H + h
     const int n = pair / H, h = pair - n * H;
@@ -211,20 +213,20 @@ kda_decode_multi_kernel(const uint16_t* __restrict__ q, const uint16_t* __restri
             const float qi = bf16_bits_to_f32(q_j);
             const float ki = bf16_bits_to_f32(k_j);
             const float a = decay == 2 ? 1.f : expf(la_j);
-            s_ak2[tid] = make_float2(a, ki);
-            s_akq[tid] = make_float2(a * ki, a * qi);
+            s_ak2[j & 1][tid] = make_float2(a, ki);
+            s_akq[j & 1][tid] = make_float2(a * ki, a * qi);
             qk_part = qi * ki;
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) qk_part += __shfl_xor_sync(0xffffffffu, qk_part, off);
-        if (lane == 0) s_qk[warp] = qk_part;
+        if (lane == 0) s_qk[j & 1][warp] = qk_part;
         __syncthreads();
 
         float4 r1 = make_float4(0.f, 0.f, 0.f, 0.f), r2 = r1;
 #pragma unroll
         for (int it = 0; it < Sh::kIters; ++it) {
             const int r = warp * Sh::kRowsPerWarp + it * Sh::kRowsPerIter + rsub;
-            const float2 akq = s_akq[r];
+            const float2 akq = s_akq[j & 1][r];
         const float ak = akq.x, aq = akq.y;
             col_sums(r1, r2, ak, aq, s[it]);
         }
@@ -245,7 +247,7 @@ kda_decode_multi_kernel(const uint16_t* __restrict__ q, const uint16_t* __restri
         if (tid < D) {
             float t1 = 0.f, t2 = 0.f, qk = 0.f;
 #pragma unroll
-            for (int w = 0; w < WARPS; ++w) { t1 += s_red[w][0][tid]; t2 += s_red[w][1][tid]; qk += s_qk[w]; }
+            for (int w = 0; w < WARPS; ++w) { t1 += s_red[w][0][tid]; t2 += s_red[w][1][tid]; qk += s_qk[j & 1][w]; }
             const float u = bf16_bits_to_f32(v_j) - t1;
             s_u[tid] = u;
             const float ov = t2 + b * qk * u;
@@ -258,12 +260,14 @@ kda_decode_multi_kernel(const uint16_t* __restrict__ q, const uint16_t* __restri
 #pragma unroll
         for (int it = 0; it < Sh::kIters; ++it) {
             const int r = warp * Sh::kRowsPerWarp + it * Sh::kRowsPerIter + rsub;
-            const float2 ak2 = s_ak2[r];
+            const float2 ak2 = s_ak2[j & 1][r];
             const float a = ak2.x;
             const float kr = b * ak2.y;
             s[it] = state_update(s[it], a, kr, u4);
         }
-        __syncthreads();       // the shared scalars of this token are dead only now
+        // (no barrier here: the next token stages its scalars in the other buffer, and s_u and
+        // s_red are next written only after the next token's first barrier, which every
+        // thread reaches only when done with this token)
     }
     if (commit && nt > 0) {
 #pragma unroll
