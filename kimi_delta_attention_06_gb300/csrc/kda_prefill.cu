@@ -109,7 +109,11 @@ constexpr int LH = 72;
 constexpr uint32_t P_L = P_TMEM + 32;                // L  [64][LH]
 constexpr uint32_t P_T = P_L + 64 * LH * 2;          // T  [64][LH]
 constexpr uint32_t P_Y = P_T + 64 * LH * 2;          // Y  [32][LH] (also 2 x [16][LH])
-constexpr uint32_t P_END = P_Y + 32 * LH * 2;
+// fp32 diagonal 16 x 16 blocks of L, column-major ([block][column][row], blocks 1040 B apart
+// so that the two blocks one warp reads fall in different banks)
+constexpr int LT_BLK = 260;
+constexpr uint32_t P_LT = P_Y + 32 * LH * 2;
+constexpr uint32_t P_END = P_LT + 4 * LT_BLK * 4;
 
 // Chain CTA shared memory.
 constexpr uint32_t K_SLOT = 0;                       // 2 hand-off slots
@@ -339,6 +343,44 @@ __device__ __forceinline__ void st_frag_sw(uint8_t* tile, uint32_t rows, int r0,
     *reinterpret_cast<__half2*>(tile + tc::sw128_off16(r0 + g + 8, n0 + 2 * t, rows)) = __floats2half2_rn(d[2], d[3]);
 }
 
+// 32 columns (c0 .. c0 + 31) of row r < 64 of L = strict_lower(diag(beta) G1), from the G1
+// values v: the row's diagonal 16 x 16 block goes to the fp32 column-major scratch LT (for the
+// substitution), the part below the diagonal blocks to the fp16 tile Lh (for the merges).
+// Nothing reads Lh on or above the diagonal blocks, so those parts are not written.
+__device__ __forceinline__ void st_lrow(float* LT, __half* Lh, const float (&v)[32], float b, int r, int c0) {
+    __half* Lr = Lh + r * LH + c0;
+    if ((r >> 5) == (c0 >> 5)) {                 // the 32 x 32 block on the diagonal
+        const bool lower = (r & 16) != 0;        // rows 16..31 of it: v[0..15] lie below the diagonal
+        float* col = LT + (r >> 4) * LT_BLK + (r & 15);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float x = lower ? v[16 + i] : v[i];
+            col[i * 16] = i < (r & 15) ? b * x : 0.f;
+        }
+        if (lower) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 8) {
+                uint4 w;
+                w.x = f16x2_bits(b * v[i + 0], b * v[i + 1]);
+                w.y = f16x2_bits(b * v[i + 2], b * v[i + 3]);
+                w.z = f16x2_bits(b * v[i + 4], b * v[i + 5]);
+                w.w = f16x2_bits(b * v[i + 6], b * v[i + 7]);
+                *reinterpret_cast<uint4*>(Lr + i) = w;
+            }
+        }
+    } else if (r >= 32 && c0 == 0) {             // rows 32..63, columns 0..31: all below
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) {
+            uint4 w;
+            w.x = f16x2_bits(b * v[i + 0], b * v[i + 1]);
+            w.y = f16x2_bits(b * v[i + 2], b * v[i + 3]);
+            w.z = f16x2_bits(b * v[i + 4], b * v[i + 5]);
+            w.w = f16x2_bits(b * v[i + 6], b * v[i + 7]);
+            *reinterpret_cast<uint4*>(Lr + i) = w;
+        }
+    }                                            // (rows 0..31, columns 32..63: above)
+}
+
 // Bounded wait on an mbarrier phase, agreed by all threads of the CTA (together
 // with each thread's own `mine` flag).
 __device__ __forceinline__ bool cta_wait(void* bar, uint32_t parity, bool cluster_scope, bool mine = true) {
@@ -407,6 +449,7 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
     __half* Lh = reinterpret_cast<__half*>(sm + P_L);
     __half* Th = reinterpret_cast<__half*>(sm + P_T);
     __half* Yh = reinterpret_cast<__half*>(sm + P_Y);
+    float* LT = reinterpret_cast<float*>(sm + P_LT);
     float* s_beta = reinterpret_cast<float*>(sm + P_BETA);
     float* s_tot = reinterpret_cast<float*>(sm + P_TOT);
     uint64_t* mb = reinterpret_cast<uint64_t*>(sm + P_BAR);    // 0: mma, 1-2: ring entry free, 3: tma
@@ -540,9 +583,15 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             const float4 egc = f4ex2(f4mul(gc, L2));
             const float4 ecr = egr;                        // exp(g_C - g_r) = exp(g_r)
             // range: every exponent of 2 formed below must lie strictly inside (-126, 126)
-            // (beyond it ex2 overflows or flushes to zero); NaN fails the test too
-            bool out_of_range = !(fabsf(gr.x * kLog2e) < kMaxExp2) || !(fabsf(gr.y * kLog2e) < kMaxExp2) ||
-                                !(fabsf(gr.z * kLog2e) < kMaxExp2) || !(fabsf(gr.w * kLog2e) < kMaxExp2);
+            // (beyond it ex2 overflows or flushes to zero).  With every log-decay <= 0 the
+            // prefix g_t falls from 0 to g_C, so each exponent (g_t - g_C / 2) log2 e lies
+            // within +-(g_C / 2) log2 e: testing the midpoint bounds them all, and a NaN or
+            // infinite log-decay reaches g_C and fails the test too
+            const bool out_of_range = !(fabsf(gr.x * kLog2e) < kMaxExp2) || !(fabsf(gr.y * kLog2e) < kMaxExp2) ||
+                                      !(fabsf(gr.z * kLog2e) < kMaxExp2) || !(fabsf(gr.w * kLog2e) < kMaxExp2);
+            // exponent of token t: (g4[t] + off - g_r) log2 e = g4[t] log2 e + ofl
+            const float4 ofl = make_float4((off.x - gr.x) * kLog2e, (off.y - gr.y) * kLog2e,
+                                           (off.z - gr.z) * kLog2e, (off.w - gr.w) * kLog2e);
             if (tg == 0) *reinterpret_cast<float4*>(s_egc_out + 4 * cg) = egc;
             {   // V as an fp16 MN-major tile (same token / column mapping as its staging load)
 #pragma unroll
@@ -557,11 +606,8 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int t = 8 * tg + i;
-                const float4 g = f4add(g4[i], off);
-                const float4 x = make_float4((g.x - gr.x) * kLog2e, (g.y - gr.y) * kLog2e,
-                                             (g.z - gr.z) * kLog2e, (g.w - gr.w) * kLog2e);
-                out_of_range |= !(fabsf(x.x) < kMaxExp2) || !(fabsf(x.y) < kMaxExp2) ||
-                                !(fabsf(x.z) < kMaxExp2) || !(fabsf(x.w) < kMaxExp2);
+                const float4 x = make_float4(fmaf(g4[i].x, kLog2e, ofl.x), fmaf(g4[i].y, kLog2e, ofl.y),
+                                             fmaf(g4[i].z, kLog2e, ofl.z), fmaf(g4[i].w, kLog2e, ofl.w));
                 const float4 e1 = f4ex2(x);
                 const float4 e2 = f4ex2(make_float4(-x.x, -x.y, -x.z, -x.w));
                 const float4 kv = bf16x4_to_f4(k2[i]), qv = bf16x4_to_f4(q2[i]);
@@ -695,17 +741,7 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
                 v[i] *= f;
             }
             if (r < 64) {
-                const float b = s_beta[r];
-                __half* Lr = Lh + r * LH + c0;
-#pragma unroll
-                for (int i = 0; i < 32; i += 8) {
-                    uint4 w;
-                    w.x = f16x2_bits(b * v[i + 0], b * v[i + 1]);
-                    w.y = f16x2_bits(b * v[i + 2], b * v[i + 3]);
-                    w.z = f16x2_bits(b * v[i + 4], b * v[i + 5]);
-                    w.w = f16x2_bits(b * v[i + 6], b * v[i + 7]);
-                    *reinterpret_cast<uint4*>(Lr + i) = w;
-                }
+                st_lrow(LT, Lh, v, s_beta[r], r, c0);
             } else {
 #pragma unroll
                 for (int i = 0; i < 32; i += 8) st_h8(P, t, c0 + i, 64, v + i);
@@ -717,17 +753,7 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             float v[32];
             tmem_ld32(lane_base + TM_G1 + c0, v);
             if (r < 64) {
-                const float b = s_beta[r];
-                __half* Lr = Lh + r * LH + c0;
-#pragma unroll
-                for (int i = 0; i < 32; i += 8) {
-                    uint4 w;
-                    w.x = f16x2_bits((c0 + i + 0 < r) ? b * v[i + 0] : 0.f, (c0 + i + 1 < r) ? b * v[i + 1] : 0.f);
-                    w.y = f16x2_bits((c0 + i + 2 < r) ? b * v[i + 2] : 0.f, (c0 + i + 3 < r) ? b * v[i + 3] : 0.f);
-                    w.z = f16x2_bits((c0 + i + 4 < r) ? b * v[i + 4] : 0.f, (c0 + i + 5 < r) ? b * v[i + 5] : 0.f);
-                    w.w = f16x2_bits((c0 + i + 6 < r) ? b * v[i + 6] : 0.f, (c0 + i + 7 < r) ? b * v[i + 7] : 0.f);
-                    *reinterpret_cast<uint4*>(Lr + i) = w;
-                }
+                st_lrow(LT, Lh, v, s_beta[r], r, c0);
             } else {
                 const int t = r - 64;
 #pragma unroll
@@ -746,14 +772,20 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         //    (T's blocks above the diagonal are never written: zero since the kernel started)
         if (tid < 64) {            // diagonal blocks, column-oriented forward substitution (fp32)
             const int bb = tid >> 4, cc = tid & 15;
-            const __half* Lb = Lh + (16 * bb) * LH + 16 * bb;
+            const float* Lc = LT + bb * LT_BLK;          // Lc[16 j + r] = L[16 bb + r][16 bb + j]
             float sv[16];
 #pragma unroll
             for (int r = 0; r < 16; ++r) sv[r] = (r == cc) ? 1.f : 0.f;
 #pragma unroll
             for (int j = 0; j < 15; ++j) {
 #pragma unroll
-                for (int r = j + 1; r < 16; ++r) sv[r] -= __half2float(Lb[r * LH + j]) * sv[j];
+                for (int q = (j + 1) >> 2; q < 4; ++q) {   // rows 4q .. 4q + 3 of column j, one load
+                    const float4 l = *reinterpret_cast<const float4*>(Lc + 16 * j + 4 * q);
+                    const float lq[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (4 * q + e > j) sv[4 * q + e] -= lq[e] * sv[j];
+                }
             }
 #pragma unroll
             for (int r = 0; r < 16; ++r) Th[(16 * bb + r) * LH + 16 * bb + cc] = __float2half_rn(sv[r]);
