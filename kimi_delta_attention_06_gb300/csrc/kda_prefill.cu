@@ -203,6 +203,11 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+__device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {   // a - b, fp16 pairs
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
 __device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
@@ -341,6 +346,25 @@ __device__ __forceinline__ void st_frag_sw(uint8_t* tile, uint32_t rows, int r0,
     const int l = threadIdx.x & 31, g = l >> 2, t = l & 3;
     *reinterpret_cast<__half2*>(tile + tc::sw128_off16(r0 + g, n0 + 2 * t, rows)) = __floats2half2_rn(d[0], d[1]);
     *reinterpret_cast<__half2*>(tile + tc::sw128_off16(r0 + g + 8, n0 + 2 * t, rows)) = __floats2half2_rn(d[2], d[3]);
+}
+
+// Rows 16 M .. 16 M + 15 of Mqk = A (T diag(beta)), columns n0 .. n0 + 15, on warp MMAs: A is
+// the fp16 tile P (64 x 64), T diag(beta) rows 0..63 of the [T; Mqk] tile, which takes the
+// result in rows 64 + 16 M ..; both factors are lower triangular, so K stops at block M.
+template <int M>
+__device__ __forceinline__ void mqk_rows(const uint8_t* P, uint8_t* Qt, int n0) {
+    float acc[2][4] = {};
+#pragma unroll
+    for (int ks = 0; ks <= M; ++ks) {
+        uint32_t a[4], b0[2], b1[2];
+        ldsm_a_sw(P, 64, 16 * M, 16 * ks, a);
+        ldsm_b_sw(Qt, 128, 16 * ks, n0, b0);
+        ldsm_b_sw(Qt, 128, 16 * ks, n0 + 8, b1);
+        mma16816(acc[0], a, b0);
+        mma16816(acc[1], a, b1);
+    }
+    st_frag_sw(Qt, 128, 64 + 16 * M, n0, acc[0]);
+    st_frag_sw(Qt, 128, 64 + 16 * M, n0 + 8, acc[1]);
 }
 
 // 32 columns (c0 .. c0 + 31) of row r < 64 of L = strict_lower(diag(beta) G1), from the G1
@@ -742,7 +766,7 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             }
             if (r < 64) {
                 st_lrow(LT, Lh, v, s_beta[r], r, c0);
-            } else {
+            } else if (t >= 32 || c0 == 0) {          // (columns 32..63 of rows 0..31: never read)
 #pragma unroll
                 for (int i = 0; i < 32; i += 8) st_h8(P, t, c0 + i, 64, v + i);
             }
@@ -755,11 +779,18 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             if (r < 64) {
                 st_lrow(LT, Lh, v, s_beta[r], r, c0);
             } else {
+                // A = lower_incl(G1 rows 64..127): the Mqk products read A only up to each
+                // 16-row block's end, so columns 32..63 of rows 0..31 are never read, and only
+                // the two 32 x 32 blocks on the diagonal need their upper triangle zeroed
                 const int t = r - 64;
+                if ((t >> 5) == (c0 >> 5)) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = (c0 + i <= t) ? v[i] : 0.f;
+                    for (int i = 0; i < 32; ++i) v[i] = (i <= (t & 31)) ? v[i] : 0.f;
+                }
+                if (t >= 32 || c0 == 0) {
 #pragma unroll
-                for (int i = 0; i < 32; i += 8) st_h8(P, t, c0 + i, 64, v + i);
+                    for (int i = 0; i < 32; i += 8) st_h8(P, t, c0 + i, 64, v + i);
+                }
             }
         }
         tc::fence_before_sync();
@@ -859,22 +890,15 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         }
         tc::named_sync(BAR_ALL, NT);
         // -- 5. Mqk = A T diag(beta) on warp MMAs, into rows 64..127 of [T; Mqk] --
-        //    warp -> rows 16 (warp / 2) .. +15, columns 32 (warp % 2) .. +31; A and T are
-        //    lower triangular, so the K range stops at the row block's end
-        {
-            const int m = warp >> 1, n0 = 32 * (warp & 1);
-            float acc[4][4] = {};
-            for (int ks = 0; ks <= m; ++ks) {
-                uint32_t a[4], b[2];
-                ldsm_a_sw(P, 64, 16 * m, 16 * ks, a);
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
-                    ldsm_b_sw(Qt, 128, 16 * ks, n0 + 8 * nt, b);
-                    mma16816(acc[nt], a, b);
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) st_frag_sw(Qt, 128, 64 + 16 * m, n0 + 8 * nt, acc[nt]);
+        //    A and T are lower triangular, so row block m needs K blocks 0..m only: warps 0-3
+        //    take row blocks 3 and 0, warps 4-7 row blocks 2 and 1, each on columns
+        //    16 (warp % 4) .. +15 (ten MMAs per warp)
+        if (warp < 4) {
+            mqk_rows<3>(P, Qt, 16 * (warp & 3));
+            mqk_rows<0>(P, Qt, 16 * (warp & 3));
+        } else {
+            mqk_rows<2>(P, Qt, 16 * (warp & 3));
+            mqk_rows<1>(P, Qt, 16 * (warp & 3));
         }
         tc::fence_smem_to_async();
         cta_sync_tc();
@@ -900,21 +924,20 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
 #pragma unroll
                 for (int i = 0; i < 32; i += 8) {
                     const int col = c0 + 32 * q4 + i;
-                    float x8[8];
-                    if (r < 64) {
+                    uint4* dst = reinterpret_cast<uint4*>(AH + tc::sw128_off16(r, col, 128));
+                    uint32_t w[4];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) x8[j] = -v[i + j];
-                    } else {
-                        const uint4 w = *reinterpret_cast<const uint4*>(AH + tc::sw128_off16(r, col, 128));
-                        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+                    for (int j = 0; j < 4; ++j) w[j] = f16x2_bits(v[i + 2 * j], v[i + 2 * j + 1]);
+                    if (r < 64) {            // -W: flip the fp16 sign bits (exact)
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[j]));
-                            x8[2 * j] = f.x - v[i + 2 * j];
-                            x8[2 * j + 1] = f.y - v[i + 2 * j + 1];
-                        }
+                        for (int j = 0; j < 4; ++j) w[j] ^= 0x80008000u;
+                    } else {                 // Q' = Q~ - Mqk K~, in fp16 (the product rounded first)
+                        const uint4 q = *dst;
+                        const uint32_t qv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) w[j] = hsub2_bits(qv[j], w[j]);
                     }
-                    st_h8(AH, r, col, 128, x8);
+                    *dst = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
         }
