@@ -108,11 +108,10 @@ constexpr uint32_t P_TMEM = P_BAR + 32;
 constexpr int LH = 72;
 constexpr uint32_t P_L = P_TMEM + 32;                // L  [64][LH]
 constexpr uint32_t P_T = P_L + 64 * LH * 2;          // T  [64][LH]
-constexpr uint32_t P_Y = P_T + 64 * LH * 2;          // Y  [32][LH] (also 2 x [16][LH])
 // fp32 diagonal 16 x 16 blocks of L, column-major ([block][column][row], blocks 1040 B apart
 // so that the two blocks one warp reads fall in different banks)
 constexpr int LT_BLK = 260;
-constexpr uint32_t P_LT = P_Y + 32 * LH * 2;
+constexpr uint32_t P_LT = P_T + 64 * LH * 2;
 constexpr uint32_t P_END = P_LT + 4 * LT_BLK * 4;
 
 // Chain CTA shared memory.
@@ -313,6 +312,15 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
+// A 16 x 8 fp32 accumulator fragment (rows g, g + 8; columns 2t, 2t + 1 of lane 4g + t) as the
+// fp16 B fragment of a following m16n8k16 product whose K runs over those 16 rows: each 8 x 8
+// half is rounded to fp16 pairs and transposed within the warp (movmatrix), which puts rows
+// 2t, 2t + 1 of column g in lane 4g + t, the B layout.
+__device__ __forceinline__ void frag_to_b(const float (&d)[4], uint32_t (&b)[2]) {
+    const uint32_t lo = f16x2_bits(d[0], d[1]), hi = f16x2_bits(d[2], d[3]);
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(b[0]) : "r"(lo));
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(b[1]) : "r"(hi));
+}
 // Store a 16 x 8 fp32 accumulator fragment, scaled by `sc`, as fp16 at (r0, n0) of a row-major tile.
 __device__ __forceinline__ void st_frag(__half* base, int pitch, int r0, int n0, const float (&d)[4], float sc) {
     const int l = threadIdx.x & 31, g = l >> 2, t = l & 3;
@@ -472,7 +480,6 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
     uint8_t* P = sm + P_P;
     __half* Lh = reinterpret_cast<__half*>(sm + P_L);
     __half* Th = reinterpret_cast<__half*>(sm + P_T);
-    __half* Yh = reinterpret_cast<__half*>(sm + P_Y);
     float* LT = reinterpret_cast<float*>(sm + P_LT);
     float* s_beta = reinterpret_cast<float*>(sm + P_BETA);
     float* s_tot = reinterpret_cast<float*>(sm + P_TOT);
@@ -842,23 +849,20 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         }
         if (warp < 2) {           // 16 -> 32: warp 0 merges blocks (1,0), warp 1 blocks (3,2)
             const int R = 16 * (2 * warp + 1), Cc = 16 * (2 * warp);
-            __half* Yw = Yh + warp * 16 * LH;
-            uint32_t a[4], b[2];
+            uint32_t a[4], b[2], yb[2][2];
             ldsm_a(Lh, LH, R, Cc, a);
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {              // Y = L_DA T_AA
+            for (int nt = 0; nt < 2; ++nt) {              // Y = L_DA T_AA, kept as fp16 B fragments
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
                 ldsm_b(Th, LH, Cc, Cc + 8 * nt, b);
                 mma16816(acc, a, b);
-                st_frag(Yw, LH, 0, 8 * nt, acc, 1.f);
+                frag_to_b(acc, yb[nt]);
             }
-            __syncwarp();
             ldsm_a(Th, LH, R, R, a);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {              // T_DA = -T_DD Y
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                ldsm_b(Yw, LH, 0, 8 * nt, b);
-                mma16816(acc, a, b);
+                mma16816(acc, a, yb[nt]);
                 st_frag(Th, LH, R, Cc + 8 * nt, acc, -1.f);
                 const int cb = Cc + 8 * nt + 2 * (lane & 3);
                 st_frag_sw_sc(Qt, 128, R, Cc + 8 * nt, acc, -s_beta[cb], -s_beta[cb + 1]);
@@ -866,23 +870,27 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         }
         tc::named_sync(BAR_ALL, NT);
         {                         // 32 -> 64: warp -> 16 x 8 tile (m = warp / 4, n = warp % 4)
+            //    each warp forms the two 16 x 8 blocks of Y = L[32:64, 0:32] T[0:32, 0:32] in
+            //    its column tile itself (both row blocks), as fp16 B fragments in registers
             const int m = warp >> 2, nn = warp & 3;
-            uint32_t a[4], b[2];
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t a[4], bt[2][2], yb[2][2];
 #pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {              // Y = L[32:64, 0:32] T[0:32, 0:32]
-                ldsm_a(Lh, LH, 32 + 16 * m, 16 * ks, a);
-                ldsm_b(Th, LH, 16 * ks, 8 * nn, b);
-                mma16816(acc, a, b);
+            for (int ks = 0; ks < 2; ++ks) ldsm_b(Th, LH, 16 * ks, 8 * nn, bt[ks]);
+#pragma unroll
+            for (int yk = 0; yk < 2; ++yk) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    ldsm_a(Lh, LH, 32 + 16 * yk, 16 * ks, a);
+                    mma16816(acc, a, bt[ks]);
+                }
+                frag_to_b(acc, yb[yk]);
             }
-            st_frag(Yh, LH, 16 * m, 8 * nn, acc, 1.f);
-            tc::named_sync(BAR_ALL, NT);
             float acc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {              // T[32:64, 0:32] = -T[32:64, 32:64] Y
                 ldsm_a(Th, LH, 32 + 16 * m, 32 + 16 * ks, a);
-                ldsm_b(Yh, LH, 16 * ks, 8 * nn, b);
-                mma16816(acc2, a, b);
+                mma16816(acc2, a, yb[ks]);
             }
             st_frag(Th, LH, 32 + 16 * m, 8 * nn, acc2, -1.f);
             const int cb = 8 * nn + 2 * (lane & 3);
