@@ -546,7 +546,9 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         if constexpr (DECAY == DECAY_CHANNEL) {
         // -- 0. inputs of this chunk: staging (TMA) -> registers --
         if (tid == 0 && c + 2 * NPREP_CTAS < nchunks) prefetch_inputs<DECAY>(tmaps, p, c + 2 * NPREP_CTAS, g, h);
-        if (!cta_wait(&mb[3], kk & 1, false)) { ok = false; break; }
+        // (each thread waits for the staged inputs itself; the outcome joins the agreement of
+        // the barrier below)
+        const bool st_ok = tc::mbar_wait_bounded(&mb[3], kk & 1, kWaitLimitNs) != 0;
         float4 g4[8];
         uint2 q2[8], k2[8];
         uint4 v4[4];
@@ -596,7 +598,7 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         }
         // the stores of the previous block must have read it before it is rewritten
         if (pending >= 0 && tid == ST_THREAD) tc::bulk_wait_read_all();
-        tc::named_sync(BAR_ALL, NT);     // totals visible; staging fully read; block free
+        if (!tc::named_sync_and(BAR_ALL, NT, st_ok)) { ok = false; break; }   // totals visible; staging read; block free
         // -- 1b. decay factors and operand tiles --
         {
             float4 off = make_float4(0.f, 0.f, 0.f, 0.f), gc = off;
@@ -656,7 +658,9 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         // -- 0/1 (scalar decay). the token log-decay prefix, one exponential per token, and
         //    the fp16 tiles; q and k stay in the staging tile, which is G1's operand --
         if (tid == 0 && c + 2 * NPREP_CTAS < nchunks) prefetch_inputs<DECAY>(tmaps, p, c + 2 * NPREP_CTAS, g, h);
-        if (!cta_wait(&mb[3], kk & 1, false)) { ok = false; break; }
+        // (each thread waits for the staged inputs itself; the outcome joins the agreement of
+        // the barrier below)
+        const bool st_ok = tc::mbar_wait_bounded(&mb[3], kk & 1, kWaitLimitNs) != 0;
         const int cv = 8 * (lane & 15);
         uint4 v4[4];
 #pragma unroll
@@ -684,7 +688,7 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         }
         // the stores of the previous block must have read it before it is rewritten
         if (pending >= 0 && tid == ST_THREAD) tc::bulk_wait_read_all();
-        tc::named_sync(BAR_ALL, NT);     // prefix visible; staging of v read; block free
+        if (!tc::named_sync_and(BAR_ALL, NT, st_ok)) { ok = false; break; }   // prefix visible; staging of v read; block free
         {
             const float gC = s_tot[63];
             if (tid < 32) {
@@ -738,7 +742,10 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
         // release this takes overlaps the MMA)
         if (tid == ST_THREAD && pending >= 0) publish();
         pending = -1;
-        if (!cta_wait(&mb[0], ph_mma & 1, false)) { ok = false; break; }
+        // each thread waits for G1 itself and goes on to its part of L and A (no CTA barrier:
+        // the outcome joins the agreement after them)
+        const bool g1_ok = tc::mbar_wait_bounded(&mb[0], ph_mma & 1, kWaitLimitNs) != 0;
+        tc::fence_after_sync();
         ++ph_mma;
         // [Km; Qm] and Kb are dead until the next chunk: stage that chunk's inputs there
         if (tid == 0 && c + NPREP_CTAS < nchunks) issue_input_tma<DECAY>(tmaps, p, sm, c + NPREP_CTAS, g, h, &mb[3]);
@@ -801,7 +808,7 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             }
         }
         tc::fence_before_sync();
-        if (!tc::named_sync_and(BAR_ALL, NT, ring_ok)) { ok = false; break; }
+        if (!tc::named_sync_and(BAR_ALL, NT, ring_ok && g1_ok)) { ok = false; break; }
         tc::fence_after_sync();
 
         // -- 4. T = (I + L)^{-1} by recursive doubling over 16 x 16 blocks --
@@ -920,7 +927,8 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             issue_mma<true>(tm + TM_W, 128, DK, C, tc::smem_u32(Qt), false, 128, tc::smem_u32(AH), true, 128u * 128u);
             tc::mma_commit(&mb[0]);
         }
-        if (!cta_wait(&mb[0], ph_mma & 1, false)) { ok = false; break; }
+        const bool wy_ok = tc::mbar_wait_bounded(&mb[0], ph_mma & 1, kWaitLimitNs) != 0;   // (agreed below)
+        tc::fence_after_sync();
         ++ph_mma;
         {   // rows 0..63: -W over K~; rows 64..127: Q' = Q~ - Mqk K~ in place (warps 4-7: columns 64..127)
             const int r = (warp & 3) * 32 + lane;
@@ -950,7 +958,9 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             }
         }
         tc::fence_smem_to_async();
-        cta_sync_tc();
+        tc::fence_before_sync();
+        if (!tc::named_sync_and(BAR_ALL, NT, wy_ok)) { ok = false; break; }
+        tc::fence_after_sync();
         if (tid == ST_THREAD) {                           // [-W; Q'] is final: the block is complete
             tc::bulk_store_s2g(entry + H_AH, tc::smem_u32(AH), H_KH - H_AH);
             tc::bulk_commit();
