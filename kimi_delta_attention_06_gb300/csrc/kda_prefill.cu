@@ -769,14 +769,15 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
             float v[32];
             tmem_ld32(lane_base + TM_G1 + c0, v);
             const float gt = s_tot[t];
-            const bool row_in = t >= lo && t < hi;
+            // pair (t, s) is kept when both tokens are the sequence's and s < t (L) or s <= t (A):
+            // lo <= s <= shi, with shi = -1 for a row outside the sequence
+            const int shi = (t >= lo && t < hi) ? min(hi - 1, r < 64 ? t - 1 : t) : -1;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int sc = c0 + i;
-                const bool keep = row_in && sc >= lo && sc < hi && (r < 64 ? sc < t : sc <= t);
-                float f = keep ? 1.f : 0.f;
-                if (DECAY == DECAY_HEAD && keep) f = ex2((gt - s_tot[sc]) * kLog2e);
-                v[i] *= f;
+                const bool keep = sc >= lo && sc <= shi;
+                if (DECAY == DECAY_HEAD) v[i] *= keep ? ex2((gt - s_tot[sc]) * kLog2e) : 0.f;
+                else v[i] = keep ? v[i] : 0.f;
             }
             if (r < 64) {
                 st_lrow(LT, Lh, v, s_beta[r], r, c0);
