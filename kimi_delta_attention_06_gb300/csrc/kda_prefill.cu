@@ -986,6 +986,7 @@ __device__ void prep_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm,
 // ============================================================================
 // Chain CTA: the sequential state recurrence of one (sequence, head).
 // ============================================================================
+template <int DECAY>
 __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm, int n, int h, const SeqGrid& g,
                            size_t ring_idx) {
     uint8_t* Sb = sm + K_S;
@@ -1014,11 +1015,20 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
     // this sequence's first checkpoint slot: the stride multiples strictly inside
     // (s, s + len) of every earlier sequence, plus its end
     long long slot_ck = 0;
+    // the next chunk that ends on a stride multiple of the prompt: chunk c ends at absolute
+    // position (start - off) + 64 (c + 1), and the stride is a multiple of 64 (used by the
+    // scalar-decay layouts, whose chain sets the pace)
+    int ck_next = -1;
     if (p.ckpt && p.ckpt_stride > 0) {
         for (int m = 0; m < n; ++m) {
             const long long lm = p.cu_seqlens[m + 1] - p.cu_seqlens[m];
             const long long sm0 = p.start_pos ? p.start_pos[m] : 0;
             if (lm > 0) slot_ck += (sm0 + lm - 1) / p.ckpt_stride - sm0 / p.ckpt_stride + 1;
+        }
+        if constexpr (DECAY != DECAY_CHANNEL) {
+            const int period = p.ckpt_stride / C;
+            const int phase = static_cast<int>(((g.start - g.off) / C + 1) % period);   // of chunk 0
+            ck_next = phase == 0 ? 0 : period - phase;
         }
     }
     float S[64];
@@ -1233,7 +1243,14 @@ __device__ void chain_role(const Params& p, const TensorMaps& tmaps, uint8_t* sm
         // -- prefix-cache checkpoint at stride multiples and at the sequence end --
         if (p.ckpt && p.ckpt_stride > 0) {
             const int done = g.done(c);                 // tokens of the sequence through this chunk
-            if ((g.start + done) % p.ckpt_stride == 0 || done == len) {
+            bool at_stride;                             // (g.start + done) is a stride multiple
+            if constexpr (DECAY != DECAY_CHANNEL) {
+                at_stride = c == ck_next;
+                if (at_stride) ck_next += p.ckpt_stride / C;
+            } else {
+                at_stride = (g.start + done) % p.ckpt_stride == 0;
+            }
+            if (at_stride || done == len) {
                 if (d < dk && col_ok) {
                     float* cp = p.ckpt + ((static_cast<size_t>(slot_ck) * H + h) * dk + d) * dv + 64 * wg;
 #pragma unroll
@@ -1337,7 +1354,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_kernel(const Params p, cons
         g.nchunks = 0;
         ring_idx = 0;
     }
-    if (rank == 0) chain_role(p, tmaps, sm, n, h, g, static_cast<size_t>(ring_idx));
+    if (rank == 0) chain_role<DECAY>(p, tmaps, sm, n, h, g, static_cast<size_t>(ring_idx));
     else prep_role<DECAY>(p, tmaps, sm, rank - 1, h, g, static_cast<size_t>(ring_idx));
     // no CTA leaves while a peer may still address its shared memory (or its ring)
     tc::cluster_sync();
